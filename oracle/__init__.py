@@ -1,0 +1,157 @@
+"""fp64 CPU oracle for shared-prefix (cascade) beam decode attention.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()``
+and by ``bench.py``'s CPU-baseline leg, never by the product package.
+
+The C source (``bsp_oracle.c``) holds the plain definitions; this module builds
+it with gcc (``build()``) and wraps it with numpy arrays. ``brute`` holds an
+independent pure-Python restatement used to pin the C code on tiny inputs.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bsp_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liborc.so")
+
+DTYPES = {"bf16": 0, "fp16": 1}
+ERRORS = {0: "ok", 1: "bad argument", 2: "index out of range", 3: "out of memory"}
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, OpenMP) into ``oracle/_build/liborc.so``."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-fno-fast-math",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    p = ctypes.c_void_p
+    i32 = ctypes.c_int32
+    lib.orc_half_to_double.restype = ctypes.c_double
+    lib.orc_half_to_double.argtypes = [ctypes.c_uint16, ctypes.c_int]
+    lib.orc_bucket_rows.restype = i32
+    lib.orc_bucket_rows.argtypes = [i32, i32]
+    lib.orc_attend.restype = None
+    lib.orc_attend.argtypes = [ctypes.c_int, ctypes.c_int, p, p, p, ctypes.c_double, p, p, p]
+    lib.orc_merge.restype = None
+    lib.orc_merge.argtypes = [ctypes.c_int, ctypes.c_int, p, p, p, p]
+    lib.orc_decode_attn.restype = ctypes.c_int
+    lib.orc_decode_attn.argtypes = [ctypes.c_int] * 8 + [p, p, p, ctypes.c_int, p, ctypes.c_int, p,
+                                                       ctypes.c_int, p, p, p, ctypes.c_double, p,
+                                                       ctypes.c_int, p, p]
+    lib.orc_append_kv.restype = ctypes.c_int
+    lib.orc_append_kv.argtypes = [ctypes.c_int] * 5 + [p, p, p, ctypes.c_int64, p, p]
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def half_to_double(bits: int, dtype: str) -> float:
+    return _load().orc_half_to_double(int(bits) & 0xFFFF, DTYPES[dtype])
+
+
+def bucket_rows(valid: int, capacity: int) -> int:
+    return int(_load().orc_bucket_rows(int(valid), int(capacity)))
+
+
+def attend(q, K, V, scale):
+    """One fp64 query against explicit keys: returns (O [D], LSE)."""
+    q = _c(q, np.float64)
+    K = _c(K, np.float64).reshape(-1, q.shape[0])
+    V = _c(V, np.float64).reshape(-1, q.shape[0])
+    n, D = K.shape
+    s = np.empty(max(n, 1), np.float64)
+    o = np.empty(D, np.float64)
+    lse = np.empty(1, np.float64)
+    _load().orc_attend(D, n, _ptr(q), _ptr(K), _ptr(V), float(scale), _ptr(s), _ptr(o), _ptr(lse))
+    return o, float(lse[0])
+
+
+def merge(Os, Ls):
+    """Log-sum-exp merge of k partial states: Os [k][D], Ls [k] -> (O [D], LSE)."""
+    Os = _c(Os, np.float64)
+    Ls = _c(Ls, np.float64).reshape(-1)
+    k, D = Os.shape
+    o = np.empty(D, np.float64)
+    lse = np.empty(1, np.float64)
+    _load().orc_merge(D, k, _ptr(Os), _ptr(Ls), _ptr(o), _ptr(lse))
+    return o, float(lse[0])
+
+
+def decode_attn(*, dtype, B, W, Hq, Hkv, D, ps, num_pages, prefix_len, tail_len, prefix_pages,
+                beam_pages, cache_indirection, q_bits, k_pool_bits, v_pool_bits, scale, rows=None):
+    """Unsplit fp64 decode attention over each beam's logical sequence.
+
+    q_bits [R,Hq,D], pools [num_pages,Hkv,ps,D] as uint16 bit patterns.
+    Returns (O [nrows,Hq,D] float64, LSE [nrows,Hq] float64) for ``rows``
+    (all B*W rows when None).
+    """
+    prefix_len = _c(prefix_len, np.int32)
+    tail_len = _c(tail_len, np.int32)
+    prefix_pages = _c(prefix_pages, np.int32).reshape(B, -1)
+    beam_pages = _c(beam_pages, np.int32).reshape(B * W, -1)
+    ci = _c(cache_indirection, np.int32).reshape(B, W, -1)
+    q_bits = _c(q_bits, np.uint16)
+    k_pool_bits = _c(k_pool_bits, np.uint16)
+    v_pool_bits = _c(v_pool_bits, np.uint16)
+    if rows is None:
+        nrows = B * W
+        rows_arr = None
+    else:
+        rows_arr = _c(rows, np.int32)
+        nrows = rows_arr.shape[0]
+    O = np.empty((nrows, Hq, D), np.float64)
+    L = np.empty((nrows, Hq), np.float64)
+    rc = _load().orc_decode_attn(
+        DTYPES[dtype], B, W, Hq, Hkv, D, ps, num_pages,
+        _ptr(prefix_len), _ptr(tail_len), _ptr(prefix_pages), prefix_pages.shape[1],
+        _ptr(beam_pages), beam_pages.shape[1], _ptr(ci), ci.shape[2],
+        _ptr(q_bits), _ptr(k_pool_bits), _ptr(v_pool_bits), float(scale),
+        None if rows_arr is None else _ptr(rows_arr), nrows, _ptr(O), _ptr(L))
+    if rc != 0:
+        raise ValueError(f"oracle decode_attn: {ERRORS.get(rc, rc)}")
+    return O, L
+
+
+def append_kv(*, Hkv, D, ps, num_pages, out_cache_loc, k_new_bits, v_new_bits, k_pool_bits,
+              v_pool_bits, row_stride=None):
+    """Paged KV append in place on uint16 pools; raises on a bad slot (pools unchanged)."""
+    loc = _c(out_cache_loc, np.int32)
+    kn = _c(k_new_bits, np.uint16)
+    vn = _c(v_new_bits, np.uint16)
+    assert k_pool_bits.flags.c_contiguous and v_pool_bits.flags.c_contiguous
+    assert k_pool_bits.dtype == np.uint16 and v_pool_bits.dtype == np.uint16
+    n = loc.shape[0]
+    if row_stride is None:
+        row_stride = Hkv * D
+    rc = _load().orc_append_kv(Hkv, D, ps, num_pages, n, _ptr(loc), _ptr(kn), _ptr(vn),
+                               int(row_stride), _ptr(k_pool_bits), _ptr(v_pool_bits))
+    if rc != 0:
+        raise ValueError(f"oracle append_kv: {ERRORS.get(rc, rc)}")

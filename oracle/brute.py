@@ -1,0 +1,76 @@
+"""Pure-Python brute force of cascade beam decode attention, for tiny inputs.
+
+TEST INFRASTRUCTURE ONLY. An independent restatement of the same definition as
+``bsp_oracle.c`` (different language, different code): it materialises each
+beam's logical K/V sequence densely, one position at a time, and applies the
+textbook softmax-weighted average with Python floats. It pins the C oracle's
+paged gather and attention arithmetic on small cases.
+
+Definition followed: TensorRT-LLM PR #21738 ("Add opt-in cascade attention for
+wide beam search on KVCM V2"), description: the prompt is read through beam 0's
+page table and each beam's tail through cache_indirection, and the split
+prefix/tail states merge exactly to unsplit attention.
+"""
+from __future__ import annotations
+
+import math
+import struct
+
+
+def half_bits_to_float(bits: int, dtype: str) -> float:
+    """Decode one 16-bit pattern with the struct module (IEEE half or bf16)."""
+    bits &= 0xFFFF
+    if dtype == "fp16":
+        return struct.unpack("<e", struct.pack("<H", bits))[0]
+    return struct.unpack("<f", struct.pack("<I", bits << 16))[0]
+
+
+def logical_sequence(b, w, *, W, ps, prefix_len, tail_len, prefix_pages, beam_pages, ci):
+    """List of (page, slot) for each logical position of beam w of request b."""
+    seq = []
+    P, T = int(prefix_len[b]), int(tail_len[b])
+    for pos in range(P + T):
+        if pos < P:
+            page = int(prefix_pages[b][pos // ps])
+        else:
+            src = int(ci[b][w][pos])
+            page = int(beam_pages[b * W + src][pos // ps])
+        seq.append((page, pos % ps))
+    return seq
+
+
+def attend(q, keys, values, scale):
+    """softmax(scale * q.k_j) weighted mean of values; (O, LSE) in Python floats."""
+    if not keys:
+        return [0.0] * len(q), -math.inf
+    scores = [scale * math.fsum(a * c for a, c in zip(q, k)) for k in keys]
+    top = max(scores)
+    weights = [math.exp(s - top) for s in scores]
+    total = math.fsum(weights)
+    out = [math.fsum(wt * v[d] for wt, v in zip(weights, values)) / total for d in range(len(q))]
+    return out, top + math.log(total)
+
+
+def decode_attn(*, dtype, B, W, Hq, Hkv, D, ps, prefix_len, tail_len, prefix_pages, beam_pages,
+                cache_indirection, q_bits, k_pool_bits, v_pool_bits, scale):
+    """Nested lists O[r][h][d], LSE[r][h] for every row r = b*W + w."""
+    G = Hq // Hkv
+    O, L = [], []
+    for b in range(B):
+        for w in range(W):
+            r = b * W + w
+            seq = logical_sequence(b, w, W=W, ps=ps, prefix_len=prefix_len, tail_len=tail_len,
+                                   prefix_pages=prefix_pages, beam_pages=beam_pages,
+                                   ci=cache_indirection)
+            row_o, row_l = [], []
+            for h in range(Hq):
+                g = h // G
+                q = [half_bits_to_float(x, dtype) for x in q_bits[r][h]]
+                keys = [[half_bits_to_float(x, dtype) for x in k_pool_bits[p][g][s]] for p, s in seq]
+                vals = [[half_bits_to_float(x, dtype) for x in v_pool_bits[p][g][s]] for p, s in seq]
+                o, lse = attend(q, keys, vals, scale)
+                row_o.append(o)
+                row_l.append(lse)
+            O.append(row_o)
+            L.append(row_l)
+    return O, L

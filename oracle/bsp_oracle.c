@@ -1,0 +1,273 @@
+/*
+ * Plain fp64 CPU oracle for shared-prefix (cascade) beam decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the tests, the package's smoke() check and the
+ * benchmark's CPU-baseline leg may load this library. The product path never
+ * calls it and shares no code with it.
+ *
+ * What it computes (the plain definition, no splitting, no tiling):
+ *
+ *   For request b, beam w (row r = b*W + w), query head h, kv head g = h / G:
+ *   the logical key list of the beam is positions 0 .. P_b + T_b - 1.
+ *     - positions j < P_b (the shared prompt) are read through beam 0's prompt
+ *       page table: page = prefix_pages[b][j / ps], slot = j % ps
+ *       (TensorRT-LLM PR #21738, "Add opt-in cascade attention for wide beam
+ *       search on KVCM V2": description, "Prefix: the shared prompt is attended
+ *       once per request"; commit "...for KV cache manager V2": "the prompt page
+ *       table of beam 0 comes from the manager").
+ *     - positions j = P_b + t, t < T_b (the beam's generated tail) are gathered
+ *       through cache_indirection: source beam s = ci[b][w][j], page =
+ *       beam_pages[b*W + s][j / ps], slot = j % ps (same page, description,
+ *       "Tail: each beam's own generated tokens, gathered through
+ *       cache_indirection").
+ *   s_j = scale * <q, k_j>;  O = sum_j softmax(s)_j v_j;  LSE = ln sum_j exp(s_j).
+ *   An empty key list gives O = 0 and LSE = -inf.
+ *   The page's cascade splits this into prefix and tail and merges the two by
+ *   log-sum-exp, which reaches this unsplit result exactly (description,
+ *   "Each decode step is split and merged exactly with the log-sum-exp").
+ *
+ *   Only valid rows are read, never the whole allocation (TensorRT-Model-Connect
+ *   PR #2202, "prefill and decode over the cached prefix, not the whole KV
+ *   allocation", Exit Criteria and Implementation: kv_cache.{h,cpp}).
+ *
+ *   The paged append writes each new token's K and V rows at its flat slot:
+ *   page = loc / ps, offset = loc % ps (TensorRT-LLM PR #18614, "Fuse MiniMax-M3
+ *   MSA per-layer KV-cache writes into one kernel": description, "derives
+ *   (page, within-page) from out_cache_loc").
+ *
+ * Pool layout: [num_pages][Hkv][ps][D] of 16-bit floats (bf16 or fp16 bits).
+ * q layout: [R][Hq][D]. cache_indirection: [B][W][max_seq] int32.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_BF16 0
+#define ORC_FP16 1
+
+#define ORC_OK 0
+#define ORC_ERR_ARG 1
+#define ORC_ERR_INDEX 2
+#define ORC_ERR_NOMEM 3
+
+/* Exact value of a bf16 or IEEE binary16 bit pattern. bf16 is the top half of
+ * an IEEE binary32; binary16 has 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+double orc_half_to_double(uint16_t bits, int dtype)
+{
+    if (dtype == ORC_BF16) {
+        uint32_t u = ((uint32_t)bits) << 16;
+        float f;
+        memcpy(&f, &u, sizeof f);
+        return (double)f;
+    }
+    int sign = (bits >> 15) & 1;
+    int e = (bits >> 10) & 0x1f;
+    int m = bits & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);               /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(m + 1024), e - 25);  /* (1 + m/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* Bound cache rows for a valid prefix of `valid` rows: rounded up to a
+ * 256-row bucket, one row for an empty cache, capped at the allocation
+ * (TensorRT-Model-Connect PR #2202, Implementation: kv_cache.{h,cpp},
+ * kCacheRowBucket; Notes For Future Readers). */
+int32_t orc_bucket_rows(int32_t valid, int32_t capacity)
+{
+    if (valid <= 0)
+        return 1;
+    int64_t r = (((int64_t)valid + 255) / 256) * 256;
+    return r < capacity ? (int32_t)r : capacity;
+}
+
+/* One query against n explicit keys, all in fp64.
+ * s_j = scale <q, k_j>, m = max s_j, Z = sum exp(s_j - m),
+ * O = sum exp(s_j - m) v_j / Z, LSE = m + ln Z. n == 0: O = 0, LSE = -inf.
+ * `s` is caller scratch of n doubles. */
+void orc_attend(int D, int n, const double *q, const double *K, const double *V,
+                double scale, double *s, double *o, double *lse)
+{
+    for (int d = 0; d < D; ++d)
+        o[d] = 0.0;
+    if (n == 0) {
+        *lse = -INFINITY;
+        return;
+    }
+    double m = -INFINITY;
+    for (int j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d)
+            acc += q[d] * K[(size_t)j * D + d];
+        s[j] = scale * acc;
+        if (s[j] > m)
+            m = s[j];
+    }
+    double Z = 0.0;
+    for (int j = 0; j < n; ++j) {
+        double p = exp(s[j] - m);
+        Z += p;
+        for (int d = 0; d < D; ++d)
+            o[d] += p * V[(size_t)j * D + d];
+    }
+    for (int d = 0; d < D; ++d)
+        o[d] /= Z;
+    *lse = m + log(Z);
+}
+
+/* Log-sum-exp merge of k partial attention states (O_i, L_i) over disjoint key
+ * sets: L = ln sum exp(L_i), O = sum exp(L_i - L) O_i. All L_i = -inf (every
+ * set empty) gives O = 0, L = -inf (TensorRT-LLM PR #21738, description: the
+ * prefix and tail states are "merged exactly with the log-sum-exp"). */
+void orc_merge(int D, int k, const double *O, const double *L, double *o, double *lse)
+{
+    double m = -INFINITY;
+    for (int i = 0; i < k; ++i)
+        if (L[i] > m)
+            m = L[i];
+    for (int d = 0; d < D; ++d)
+        o[d] = 0.0;
+    if (m == -INFINITY) {
+        *lse = -INFINITY;
+        return;
+    }
+    double Z = 0.0;
+    for (int i = 0; i < k; ++i)
+        Z += exp(L[i] - m);
+    double total = m + log(Z);
+    for (int i = 0; i < k; ++i) {
+        double wgt = exp(L[i] - total);
+        for (int d = 0; d < D; ++d)
+            o[d] += wgt * O[(size_t)i * D + d];
+    }
+    *lse = total;
+}
+
+/* Physical (page, slot) of logical position j of row r, or -1 on a bad index. */
+static int64_t orc_key_row(int j, int b, int w, int W, int P, int ps, int num_pages,
+                           const int32_t *prefix_pages, int maxp_prefix,
+                           const int32_t *beam_pages, int maxp, const int32_t *ci, int max_seq,
+                           int *bad)
+{
+    int page;
+    if (j < P) {
+        if (j / ps >= maxp_prefix) { *bad = 1; return -1; }
+        page = prefix_pages[(size_t)b * maxp_prefix + j / ps];
+    } else {
+        if (j >= max_seq) { *bad = 1; return -1; }
+        int src = ci[((size_t)b * W + w) * max_seq + j];
+        if (src < 0 || src >= W) { *bad = 1; return -1; }
+        if (j / ps >= maxp) { *bad = 1; return -1; }
+        page = beam_pages[((size_t)b * W + src) * maxp + j / ps];
+    }
+    if (page < 0 || page >= num_pages) { *bad = 1; return -1; }
+    return (int64_t)page * ps + (j % ps);
+}
+
+/* Unsplit decode attention for the rows listed in `rows` (all R rows when
+ * rows == NULL). Outputs: O [nrows][Hq][D], LSE [nrows][Hq], fp64.
+ * Returns ORC_ERR_INDEX if any page id or indirection value it would read is
+ * out of range (nothing is read from a bad index). */
+int orc_decode_attn(int dtype, int B, int W, int Hq, int Hkv, int D, int ps, int num_pages,
+                    const int32_t *prefix_len, const int32_t *tail_len,
+                    const int32_t *prefix_pages, int maxp_prefix,
+                    const int32_t *beam_pages, int maxp, const int32_t *ci, int max_seq,
+                    const uint16_t *q, const uint16_t *kpool, const uint16_t *vpool,
+                    double scale, const int32_t *rows, int nrows, double *O, double *LSE)
+{
+    if (B < 0 || W <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || ps <= 0)
+        return ORC_ERR_ARG;
+    const int G = Hq / Hkv;
+    const int R = B * W;
+    if (rows == NULL)
+        nrows = R;
+    int err = ORC_OK;
+
+#pragma omp parallel
+    {
+        int maxn = 0;
+        for (int b = 0; b < B; ++b)
+            if (prefix_len[b] + tail_len[b] > maxn)
+                maxn = prefix_len[b] + tail_len[b];
+        double *K = malloc(sizeof(double) * ((size_t)maxn * D + 1));
+        double *V = malloc(sizeof(double) * ((size_t)maxn * D + 1));
+        double *s = malloc(sizeof(double) * ((size_t)maxn + 1));
+        double *qd = malloc(sizeof(double) * (size_t)D);
+        if (!K || !V || !s || !qd) {
+#pragma omp atomic write
+            err = ORC_ERR_NOMEM;
+        }
+#pragma omp for collapse(2) schedule(dynamic, 1)
+        for (int i = 0; i < nrows; ++i) {
+            for (int g = 0; g < Hkv; ++g) {
+                if (err != ORC_OK)
+                    continue;
+                int r = rows ? rows[i] : i;
+                if (r < 0 || r >= R) {
+#pragma omp atomic write
+                    err = ORC_ERR_ARG;
+                    continue;
+                }
+                int b = r / W, w = r % W;
+                int P = prefix_len[b], T = tail_len[b], n = P + T;
+                int bad = 0;
+                for (int j = 0; j < n && !bad; ++j) {
+                    int64_t kr = orc_key_row(j, b, w, W, P, ps, num_pages, prefix_pages, maxp_prefix,
+                                             beam_pages, maxp, ci, max_seq, &bad);
+                    if (bad)
+                        break;
+                    int64_t page = kr / ps, slot = kr % ps;
+                    size_t base = (((size_t)page * Hkv + g) * ps + (size_t)slot) * D;
+                    for (int d = 0; d < D; ++d) {
+                        K[(size_t)j * D + d] = orc_half_to_double(kpool[base + d], dtype);
+                        V[(size_t)j * D + d] = orc_half_to_double(vpool[base + d], dtype);
+                    }
+                }
+                if (bad) {
+#pragma omp atomic write
+                    err = ORC_ERR_INDEX;
+                    continue;
+                }
+                for (int hh = 0; hh < G; ++hh) {
+                    int h = g * G + hh;
+                    for (int d = 0; d < D; ++d)
+                        qd[d] = orc_half_to_double(q[((size_t)r * Hq + h) * D + d], dtype);
+                    orc_attend(D, n, qd, K, V, scale, s, O + ((size_t)i * Hq + h) * D,
+                               LSE + (size_t)i * Hq + h);
+                }
+            }
+        }
+        free(K);
+        free(V);
+        free(s);
+        free(qd);
+    }
+    return err;
+}
+
+/* Paged KV append: for each new token i and kv head h, copy the D-element K and
+ * V rows to pool[loc_i / ps][h][loc_i % ps][:], as bits. All slots are checked
+ * before anything is written, so a bad slot leaves both pools unchanged. */
+int orc_append_kv(int Hkv, int D, int ps, int num_pages, int n, const int32_t *loc,
+                  const uint16_t *knew, const uint16_t *vnew, int64_t row_stride,
+                  uint16_t *kpool, uint16_t *vpool)
+{
+    for (int i = 0; i < n; ++i)
+        if (loc[i] < 0 || (int64_t)loc[i] >= (int64_t)num_pages * ps)
+            return ORC_ERR_INDEX;
+    for (int i = 0; i < n; ++i) {
+        int64_t page = loc[i] / ps, off = loc[i] % ps;
+        for (int h = 0; h < Hkv; ++h) {
+            size_t dst = (((size_t)page * Hkv + h) * ps + (size_t)off) * D;
+            size_t src = (size_t)i * (size_t)row_stride + (size_t)h * D;
+            memcpy(kpool + dst, knew + src, sizeof(uint16_t) * (size_t)D);
+            memcpy(vpool + dst, vnew + src, sizeof(uint16_t) * (size_t)D);
+        }
+    }
+    return ORC_OK;
+}
