@@ -1,0 +1,215 @@
+"""Thin ctypes binding of libbsp.so (include/bsp.h): argument marshalling only.
+
+Every step of the decode path runs in the library's CUDA kernels. The functions
+mirror the C entry points by name; torch tensors supply device memory, pinned
+host staging and the current CUDA stream. If the native library is missing or
+fails to load, every call raises ``NativeLibraryError``: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+BSP_OK = 0
+STATUS_NAMES = {0: "BSP_OK", 1: "BSP_ERR_INVALID_ARG", 2: "BSP_ERR_UNSUPPORTED", 3: "BSP_ERR_PAGE_INDEX",
+                4: "BSP_ERR_CAPACITY", 5: "BSP_ERR_STALE_PLAN", 6: "BSP_ERR_CUDA", 7: "BSP_ERR_DEVICE_TIMEOUT"}
+DTYPES = {"bf16": 0, "fp16": 1, torch.bfloat16: 0, torch.float16: 1}
+FLAG_LSE_BASE2 = 1
+FLAG_CHECK = 2
+MAX_TAIL = 8
+MAX_GROUP = 8
+DEVFLAG_PAGE_INDEX = 1
+DEVFLAG_TIMEOUT = 2
+
+
+class NativeLibraryError(RuntimeError):
+    pass
+
+
+class BspError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
+
+
+class Geometry(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("geo", Geometry)] + [(n, ctypes.c_int32) for n in (
+        "batch", "beam_width", "max_tail", "prefix_pages_stride", "num_units", "num_parts", "row_blocks",
+        "beams_per_block", "tile_keys", "max_prefix_len", "max_total_len", "num_sms", "max_tail_len",
+        "reserved_i")] + [
+        ("generation", ctypes.c_uint64), ("ws_device", ctypes.c_void_p), ("ws_device_bytes", ctypes.c_uint64),
+        ("ws_host", ctypes.c_void_p), ("image_bytes", ctypes.c_uint64), ("off_req", ctypes.c_uint64),
+        ("off_units", ctypes.c_uint64), ("off_pages", ctypes.c_uint64), ("off_part_lse", ctypes.c_uint64),
+        ("off_part_o", ctypes.c_uint64), ("device_bytes_used", ctypes.c_uint64),
+        ("reserved", ctypes.c_uint64 * 4)]
+
+
+_lib = None
+EXPORTS = ["bsp_status_string", "bsp_bucket_rows", "bsp_workspace_size", "bsp_plan_build", "bsp_plan",
+           "bsp_append_kv", "bsp_decode_attn", "bsp_read_device_status"]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libbsp.so (building it first only when asked)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise NativeLibraryError(
+            f"{_build.LIB} is missing: build it with beam_search_shared_gb300.build.build() "
+            "(there is no fallback path)")
+    try:
+        lib = ctypes.CDLL(_build.LIB)
+    except OSError as e:  # pragma: no cover - depends on the box
+        raise NativeLibraryError(f"cannot load {_build.LIB}: {e}") from e
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    P = ctypes.POINTER
+    lib.bsp_status_string.restype = ctypes.c_char_p
+    lib.bsp_status_string.argtypes = [i32]
+    lib.bsp_bucket_rows.restype = i32
+    lib.bsp_bucket_rows.argtypes = [i32, i32]
+    lib.bsp_workspace_size.restype = i32
+    lib.bsp_workspace_size.argtypes = [P(Geometry), i32, i32, i32, P(sz), P(sz)]
+    lib.bsp_plan_build.restype = i32
+    lib.bsp_plan_build.argtypes = [P(Geometry), i32, i32, vp, vp, vp, i32, i32, i32, vp, sz, P(Plan)]
+    lib.bsp_plan.restype = i32
+    lib.bsp_plan.argtypes = [P(Geometry), i32, i32, vp, vp, vp, i32, i32, vp, sz, vp, sz, vp, P(Plan)]
+    lib.bsp_append_kv.restype = i32
+    lib.bsp_append_kv.argtypes = [P(Plan), vp, vp, i64, vp, i32, vp, vp, vp]
+    lib.bsp_decode_attn.restype = i32
+    lib.bsp_decode_attn.argtypes = [P(Plan), vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, i32, vp, vp, vp]
+    lib.bsp_read_device_status.restype = i32
+    lib.bsp_read_device_status.argtypes = [P(Plan), vp, i32, P(i32)]
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, st: int):
+    if st != BSP_OK:
+        raise BspError(fn, st)
+
+
+def status_string(status: int) -> str:
+    return load().bsp_status_string(int(status)).decode()
+
+
+def geometry(num_q_heads, num_kv_heads, head_dim, page_size, num_pages, dtype) -> Geometry:
+    return Geometry(int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size), int(num_pages),
+                    DTYPES[dtype])
+
+
+def bucket_rows(valid_rows: int, capacity: int) -> int:
+    return int(load().bsp_bucket_rows(int(valid_rows), int(capacity)))
+
+
+def workspace_size(geo: Geometry, max_batch: int, max_beam: int, max_prefix_pages: int):
+    d, h = ctypes.c_size_t(), ctypes.c_size_t()
+    _check("bsp_workspace_size", load().bsp_workspace_size(ctypes.byref(geo), int(max_batch), int(max_beam),
+                                                           int(max_prefix_pages), ctypes.byref(d), ctypes.byref(h)))
+    return d.value, h.value
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def plan_build(geo: Geometry, batch, beam_width, prefix_len, tail_len, prefix_pages, max_tail, num_sms,
+               image_bytes: int = 1 << 24):
+    """Host-only planning. Returns (Plan, image bytes as a numpy uint8 array)."""
+    pl, tl = _i32(prefix_len), _i32(tail_len)
+    pp = _i32(prefix_pages).reshape(int(batch), -1) if int(batch) else np.zeros((0, 1), np.int32)
+    img = np.zeros(int(image_bytes), np.uint8)
+    plan = Plan()
+    _check("bsp_plan_build", load().bsp_plan_build(
+        ctypes.byref(geo), int(batch), int(beam_width), _ptr(pl), _ptr(tl), _ptr(pp), pp.shape[1], int(max_tail),
+        int(num_sms), _ptr(img), img.nbytes, ctypes.byref(plan)))
+    return plan, img[:plan.image_bytes]
+
+
+class Workspace:
+    """A device workspace and its pinned host staging buffer, sized by bsp_workspace_size."""
+
+    def __init__(self, geo: Geometry, max_batch: int, max_beam: int, max_prefix_pages: int, device=None):
+        dev_bytes, host_bytes = workspace_size(geo, max_batch, max_beam, max_prefix_pages)
+        device = torch.device("cuda") if device is None else torch.device(device)
+        self.device = torch.empty(dev_bytes, dtype=torch.uint8, device=device)
+        self.device.zero_()
+        self.host = torch.empty(host_bytes, dtype=torch.uint8, pin_memory=True)
+        self.host.zero_()
+
+    def plan(self, geo: Geometry, batch, beam_width, prefix_len, tail_len, prefix_pages, max_tail=MAX_TAIL,
+             stream=None) -> Plan:
+        return plan(geo, batch, beam_width, prefix_len, tail_len, prefix_pages, max_tail, self, stream)
+
+
+def plan(geo: Geometry, batch, beam_width, prefix_len, tail_len, prefix_pages, max_tail, ws: Workspace,
+         stream=None) -> Plan:
+    """bsp_plan: host arrays in, plan staged into ``ws`` on ``stream`` (no sync)."""
+    pl, tl = _i32(prefix_len), _i32(tail_len)
+    pp = _i32(prefix_pages).reshape(int(batch), -1) if int(batch) else np.zeros((0, 1), np.int32)
+    out = Plan()
+    _check("bsp_plan", load().bsp_plan(
+        ctypes.byref(geo), int(batch), int(beam_width), _ptr(pl), _ptr(tl), _ptr(pp), pp.shape[1], int(max_tail),
+        _dptr(ws.device), ws.device.numel(), _dptr(ws.host), ws.host.numel(), _stream(stream), ctypes.byref(out)))
+    return out
+
+
+def append_kv(plan_: Plan, k_new: torch.Tensor, v_new: torch.Tensor, out_cache_loc: torch.Tensor,
+              k_pool: torch.Tensor, v_pool: torch.Tensor, src_row_stride: Optional[int] = None, stream=None):
+    """bsp_append_kv: k_new/v_new rows [n, Hkv*D] (row stride in elements), out_cache_loc int32 [n]."""
+    n = int(out_cache_loc.numel())
+    if src_row_stride is None:
+        src_row_stride = int(k_new.stride(0)) if k_new.dim() >= 1 and n else plan_.geo.num_kv_heads * plan_.geo.head_dim
+    _check("bsp_append_kv", load().bsp_append_kv(
+        ctypes.byref(plan_), _dptr(k_new), _dptr(v_new), int(src_row_stride), _dptr(out_cache_loc), n,
+        _dptr(k_pool), _dptr(v_pool), _stream(stream)))
+
+
+def decode_attn(plan_: Plan, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                beam_pages: Optional[torch.Tensor], cache_indirection: Optional[torch.Tensor], softmax_scale: float,
+                o: torch.Tensor, lse: torch.Tensor, flags: int = 0, stream=None):
+    """bsp_decode_attn: writes o [R,Hq,D] and lse [R,Hq] (fp32)."""
+    bps = int(beam_pages.shape[-1]) if beam_pages is not None else 0
+    max_seq = int(cache_indirection.shape[-1]) if cache_indirection is not None else 0
+    _check("bsp_decode_attn", load().bsp_decode_attn(
+        ctypes.byref(plan_), _dptr(q), _dptr(k_pool), _dptr(v_pool), _dptr(beam_pages), bps,
+        _dptr(cache_indirection), max_seq, float(softmax_scale), int(flags), _dptr(o), _dptr(lse),
+        _stream(stream)))
+
+
+def read_device_status(plan_: Plan, clear: bool = True, stream=None):
+    """Synchronises the stream; returns (status, device flag bits)."""
+    flags = ctypes.c_int32(0)
+    st = load().bsp_read_device_status(ctypes.byref(plan_), _stream(stream), int(bool(clear)), ctypes.byref(flags))
+    return int(st), int(flags.value)

@@ -1,0 +1,502 @@
+// Host side of libbsp.so: argument validation, per-step planning, plan
+// staging without a stream sync, tensor-map encoding and kernel launches.
+// Everything here is declared in include/bsp.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstring>
+#include <limits>
+#include <thread>
+#include <vector>
+
+#include "../../include/bsp.h"
+#include "bsp_internal.h"
+
+namespace {
+
+using namespace bsp;
+
+constexpr uint64_t kStagingMagic = 0x3150534250534253ull;
+constexpr size_t kStagingHeaderBytes = 256;
+
+// First bytes of the caller's host staging buffer.
+struct StagingHeader {
+    uint64_t magic;
+    uint64_t generation;     // latest plan staged through this buffer
+    uint64_t echoed[2];      // generation whose image copy from slot i has executed (written by the stream)
+    uint64_t ws_device;      // device workspace this buffer is paired with
+};
+static_assert(sizeof(StagingHeader) <= kStagingHeaderBytes, "staging header");
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+int ilog2(int x) {
+    int l = 0;
+    while ((1 << l) < x) ++l;
+    return l;
+}
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bsp_status check_geometry(const bsp_geometry* geo) {
+    if (!geo) return BSP_ERR_INVALID_ARG;
+    if (geo->dtype != BSP_DTYPE_BF16 && geo->dtype != BSP_DTYPE_FP16) return BSP_ERR_UNSUPPORTED;
+    if (geo->head_dim != 64 && geo->head_dim != 128 && geo->head_dim != 256) return BSP_ERR_UNSUPPORTED;
+    if (geo->num_q_heads <= 0 || geo->num_kv_heads <= 0 || geo->num_pages <= 0) return BSP_ERR_INVALID_ARG;
+    if (geo->num_q_heads % geo->num_kv_heads != 0) return BSP_ERR_UNSUPPORTED;
+    if (geo->num_q_heads / geo->num_kv_heads > BSP_MAX_GROUP) return BSP_ERR_UNSUPPORTED;
+    if (!is_pow2(geo->page_size) || geo->page_size < 8 || geo->page_size > 128) return BSP_ERR_UNSUPPORTED;
+    // pool rows are addressed with 32-bit TMA coordinates
+    if (static_cast<int64_t>(geo->num_pages) * geo->num_kv_heads * geo->page_size >= (int64_t(1) << 31))
+        return BSP_ERR_UNSUPPORTED;
+    return BSP_OK;
+}
+
+// Query rows of one (request, kv head) are W*G; a CTA takes whole beams, at most 128 rows.
+void row_blocks(int W, int G, int* nrb, int* wblk) {
+    const int wmax = std::max(1, kRowsPerBlock / G);
+    const int n = static_cast<int>(ceil_div(W, wmax));
+    *nrb = n;
+    *wblk = static_cast<int>(ceil_div(W, n));
+}
+
+struct DeviceLayout {
+    size_t image, part_lse, part_o, total;
+};
+
+DeviceLayout device_layout(size_t image_bytes, int64_t parts, int W, const bsp_geometry& geo) {
+    DeviceLayout L;
+    L.image = align_up(image_bytes, kAlign);
+    L.part_lse = align_up(static_cast<size_t>(parts) * W * geo.num_q_heads * sizeof(float), kAlign);
+    L.part_o = align_up(static_cast<size_t>(parts) * W * geo.num_q_heads * geo.head_dim * sizeof(float), kAlign);
+    L.total = kStatusBytes + L.image + L.part_lse + L.part_o;
+    return L;
+}
+
+bool plan_is_current(const bsp_plan_t* plan) {
+    if (!plan->ws_host || !plan->ws_device || plan->generation == 0) return false;
+    const StagingHeader* hdr = static_cast<const StagingHeader*>(plan->ws_host);
+    return hdr->magic == kStagingMagic && hdr->generation == plan->generation &&
+           hdr->ws_device == reinterpret_cast<uint64_t>(plan->ws_device);
+}
+
+bsp_status check_plan(const bsp_plan_t* plan) {
+    if (!plan) return BSP_ERR_INVALID_ARG;
+    if (plan->generation == 0 || !plan->ws_device || !plan->ws_host) return BSP_ERR_INVALID_ARG;
+    if (!plan_is_current(plan)) return BSP_ERR_STALE_PLAN;
+    return check_geometry(&plan->geo);
+}
+
+// Device memory (or managed) pointer, 16-byte aligned.
+bool device_ptr_ok(const void* p) {
+    if (!p || (reinterpret_cast<uintptr_t>(p) & 15u)) return false;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+bool encode_map(CUtensorMap* m, int dtype, int rank, const void* base, const cuuint64_t* dims,
+                const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, dtype == BSP_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides_bytes, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* bsp_status_string(int32_t status) {
+    switch (status) {
+        case BSP_OK: return "ok";
+        case BSP_ERR_INVALID_ARG: return "invalid argument";
+        case BSP_ERR_UNSUPPORTED: return "unsupported configuration";
+        case BSP_ERR_PAGE_INDEX: return "page index, slot or indirection value out of range";
+        case BSP_ERR_CAPACITY: return "workspace, staging buffer or tail bound too small";
+        case BSP_ERR_STALE_PLAN: return "stale plan (superseded by a newer plan on this workspace)";
+        case BSP_ERR_CUDA: return "CUDA call failed";
+        case BSP_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait expired";
+        default: return "unknown status";
+    }
+}
+
+int32_t bsp_bucket_rows(int32_t valid_rows, int32_t capacity) {
+    if (capacity < 1) return -1;
+    if (valid_rows <= 0) return 1;
+    const int64_t r = ceil_div(valid_rows, 256) * 256;
+    return r < capacity ? static_cast<int32_t>(r) : capacity;
+}
+
+bsp_status bsp_workspace_size(const bsp_geometry* geo, int32_t max_batch, int32_t max_beam, int32_t max_prefix_pages,
+                              size_t* device_bytes, size_t* host_bytes) {
+    bsp_status st = check_geometry(geo);
+    if (st != BSP_OK) return st;
+    if (max_batch < 0 || max_beam < 1 || max_prefix_pages < 0 || !device_bytes || !host_bytes)
+        return BSP_ERR_INVALID_ARG;
+    const int G = geo->num_q_heads / geo->num_kv_heads;
+    int nrb, wblk;
+    row_blocks(max_beam, G, &nrb, &wblk);
+    const int64_t parts_cap = static_cast<int64_t>(max_batch) + kExtraParts;
+    const int64_t units_max = parts_cap * geo->num_kv_heads * nrb;
+    const size_t image = kImageHeaderBytes + static_cast<size_t>(max_batch) * kReqFields * 4 +
+                         static_cast<size_t>(units_max) * kUnitFields * 4 +
+                         static_cast<size_t>(max_batch) * max_prefix_pages * 4;
+    DeviceLayout L = device_layout(image, parts_cap, max_beam, *geo);
+    *device_bytes = L.total;
+    *host_bytes = kStagingHeaderBytes + 2 * L.image;
+    return BSP_OK;
+}
+
+bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len,
+                          const int32_t* tail_len, const int32_t* prefix_pages, int32_t prefix_pages_stride,
+                          int32_t max_tail, int32_t num_sms, void* image, size_t image_bytes, bsp_plan_t* out) {
+    bsp_status st = check_geometry(geo);
+    if (st != BSP_OK) return st;
+    if (!out || batch < 0 || beam_width < 1 || num_sms < 1 || prefix_pages_stride < 0) return BSP_ERR_INVALID_ARG;
+    if (max_tail < 0) return BSP_ERR_INVALID_ARG;
+    if (max_tail > BSP_MAX_TAIL) return BSP_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(batch) * beam_width > (int64_t(1) << 30)) return BSP_ERR_UNSUPPORTED;
+    if (batch > 0 && (!prefix_len || !tail_len)) return BSP_ERR_INVALID_ARG;
+    const int ps = geo->page_size;
+    const int G = geo->num_q_heads / geo->num_kv_heads;
+    const int Hkv = geo->num_kv_heads;
+
+    int max_p = 0, max_total = 0, max_t = 0;
+    int64_t total_pages = 0;
+    for (int b = 0; b < batch; ++b) {
+        if (prefix_len[b] < 0 || tail_len[b] < 0) return BSP_ERR_INVALID_ARG;
+        if (prefix_len[b] > (1 << 30)) return BSP_ERR_UNSUPPORTED;
+        if (tail_len[b] > max_tail) return BSP_ERR_CAPACITY;
+        max_p = std::max(max_p, prefix_len[b]);
+        max_total = std::max(max_total, prefix_len[b] + tail_len[b]);
+        max_t = std::max(max_t, tail_len[b]);
+        total_pages += ceil_div(prefix_len[b], ps);
+    }
+    if (max_p > 0) {
+        if (!prefix_pages) return BSP_ERR_INVALID_ARG;
+        if (ceil_div(max_p, ps) > prefix_pages_stride) return BSP_ERR_INVALID_ARG;
+    }
+    for (int b = 0; b < batch; ++b) {
+        const int64_t n = ceil_div(prefix_len[b], ps);
+        for (int64_t j = 0; j < n; ++j) {
+            const int32_t pg = prefix_pages[static_cast<int64_t>(b) * prefix_pages_stride + j];
+            if (pg < 0 || pg >= geo->num_pages) return BSP_ERR_PAGE_INDEX;
+        }
+    }
+
+    // ---- work units: (request, kv head, key split, query-row block)
+    int nrb, wblk;
+    row_blocks(beam_width, G, &nrb, &wblk);
+    std::vector<int64_t> tiles(batch);
+    int64_t total_tiles = 0, active = 0;
+    for (int b = 0; b < batch; ++b) {
+        tiles[b] = ceil_div(prefix_len[b], kTileKeys);
+        total_tiles += tiles[b];
+        active += tiles[b] > 0;
+    }
+    const int64_t base_units = active * Hkv * nrb;
+    const int64_t target = 2 * static_cast<int64_t>(num_sms);
+    int64_t chunk = std::numeric_limits<int32_t>::max();  // tiles per split
+    if (base_units > 0 && base_units < target)
+        chunk = std::max<int64_t>(2, ceil_div(total_tiles * Hkv * nrb, target));
+    std::vector<int32_t> nsplit(batch);
+    int64_t parts = 0;
+    for (;;) {
+        parts = 0;
+        for (int b = 0; b < batch; ++b) {
+            nsplit[b] = tiles[b] == 0 ? 0 : static_cast<int32_t>(ceil_div(tiles[b], chunk));
+            parts += nsplit[b];
+        }
+        if (parts <= static_cast<int64_t>(batch) + kExtraParts) break;
+        chunk *= 2;
+    }
+    struct Unit {
+        int32_t f[kUnitFields];
+    };
+    std::vector<Unit> units;
+    units.reserve(static_cast<size_t>(parts * Hkv * nrb));
+    std::vector<int32_t> part_off(batch), page_off(batch);
+    int64_t poff = 0, pgoff = 0;
+    for (int b = 0; b < batch; ++b) {
+        part_off[b] = static_cast<int32_t>(poff);
+        page_off[b] = static_cast<int32_t>(pgoff);
+        for (int s = 0; s < nsplit[b]; ++s) {
+            const int32_t t0 = static_cast<int32_t>(s * tiles[b] / nsplit[b]);
+            const int32_t t1 = static_cast<int32_t>((s + 1) * tiles[b] / nsplit[b]);
+            for (int g = 0; g < Hkv; ++g)
+                for (int rb = 0; rb < nrb; ++rb) {
+                    Unit u{};
+                    u.f[kUnitReq] = b;
+                    u.f[kUnitKvHead] = g;
+                    u.f[kUnitRowBlock] = rb;
+                    u.f[kUnitTile0] = t0;
+                    u.f[kUnitTile1] = t1;
+                    u.f[kUnitPart] = static_cast<int32_t>(poff + s);
+                    units.push_back(u);
+                }
+        }
+        poff += nsplit[b];
+        pgoff += ceil_div(prefix_len[b], ps);
+    }
+    // longest units first (row blocks of one split stay adjacent: equal keys keep their order)
+    std::stable_sort(units.begin(), units.end(), [](const Unit& a, const Unit& c) {
+        return (a.f[kUnitTile1] - a.f[kUnitTile0]) > (c.f[kUnitTile1] - c.f[kUnitTile0]);
+    });
+    if (units.size() > static_cast<size_t>(std::numeric_limits<int32_t>::max())) return BSP_ERR_UNSUPPORTED;
+
+    // ---- image
+    const size_t off_req = kImageHeaderBytes;
+    const size_t off_units = off_req + static_cast<size_t>(batch) * kReqFields * 4;
+    const size_t off_pages = off_units + units.size() * kUnitFields * 4;
+    const size_t need = off_pages + static_cast<size_t>(total_pages) * 4;
+    if (!image || image_bytes < need) return BSP_ERR_CAPACITY;
+    uint8_t* img = static_cast<uint8_t*>(image);
+    std::memset(img, 0, kImageHeaderBytes);
+    reinterpret_cast<int32_t*>(img)[2] = batch;
+    reinterpret_cast<int32_t*>(img)[3] = static_cast<int32_t>(units.size());
+    int32_t* req = reinterpret_cast<int32_t*>(img + off_req);
+    for (int b = 0; b < batch; ++b) {
+        int32_t* r = req + static_cast<size_t>(b) * kReqFields;
+        std::memset(r, 0, kReqFields * 4);
+        r[kReqPrefix] = prefix_len[b];
+        r[kReqTail] = tail_len[b];
+        r[kReqSplits] = nsplit[b];
+        r[kReqPartOff] = part_off[b];
+        r[kReqPageOff] = page_off[b];
+    }
+    if (!units.empty()) std::memcpy(img + off_units, units.data(), units.size() * sizeof(Unit));
+    int32_t* pages = reinterpret_cast<int32_t*>(img + off_pages);
+    for (int b = 0; b < batch; ++b) {
+        const int64_t n = ceil_div(prefix_len[b], ps);
+        if (n) std::memcpy(pages + page_off[b], prefix_pages + static_cast<int64_t>(b) * prefix_pages_stride, n * 4);
+    }
+
+    std::memset(out, 0, sizeof(*out));
+    out->geo = *geo;
+    out->batch = batch;
+    out->beam_width = beam_width;
+    out->max_tail = max_tail;
+    out->prefix_pages_stride = prefix_pages_stride;
+    out->num_units = static_cast<int32_t>(units.size());
+    out->num_parts = static_cast<int32_t>(parts);
+    out->row_blocks = nrb;
+    out->beams_per_block = wblk;
+    out->tile_keys = kTileKeys;
+    out->max_prefix_len = max_p;
+    out->max_total_len = max_total;
+    out->num_sms = num_sms;
+    out->max_tail_len = max_t;
+    out->image_bytes = need;
+    // offsets relative to the device workspace
+    DeviceLayout L = device_layout(need, parts, beam_width, *geo);
+    out->off_req = kStatusBytes + off_req;
+    out->off_units = kStatusBytes + off_units;
+    out->off_pages = kStatusBytes + off_pages;
+    out->off_part_lse = kStatusBytes + L.image;
+    out->off_part_o = kStatusBytes + L.image + L.part_lse;
+    out->device_bytes_used = L.total;
+    return BSP_OK;
+}
+
+bsp_status bsp_plan(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len,
+                    const int32_t* tail_len, const int32_t* prefix_pages, int32_t prefix_pages_stride, int32_t max_tail,
+                    void* ws_device, size_t ws_device_bytes, void* ws_host, size_t ws_host_bytes, void* stream,
+                    bsp_plan_t* out) {
+    if (!out || !ws_device || !ws_host) return BSP_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(ws_device) & (kAlign - 1)) || (reinterpret_cast<uintptr_t>(ws_host) & 63u))
+        return BSP_ERR_INVALID_ARG;
+    if (ws_host_bytes < kStagingHeaderBytes + 2 * kAlign) return BSP_ERR_CAPACITY;
+    if (ws_device_bytes < kStatusBytes + kAlign) return BSP_ERR_CAPACITY;
+    if (!device_ptr_ok(ws_device)) return BSP_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    StagingHeader* hdr = static_cast<StagingHeader*>(ws_host);
+    if (hdr->magic != kStagingMagic || hdr->ws_device != reinterpret_cast<uint64_t>(ws_device)) {
+        std::memset(hdr, 0, kStagingHeaderBytes);
+        hdr->magic = kStagingMagic;
+        hdr->ws_device = reinterpret_cast<uint64_t>(ws_device);
+    }
+    const uint64_t gen = hdr->generation + 1;
+    const int slot = static_cast<int>(gen & 1);
+    const size_t slot_bytes = (ws_host_bytes - kStagingHeaderBytes) / 2 / kAlign * kAlign;
+    uint8_t* slot_ptr = static_cast<uint8_t*>(ws_host) + kStagingHeaderBytes + slot * slot_bytes;
+    if (gen >= 3) {
+        // the copy that last read this slot (generation gen-2) must have executed
+        const auto t0 = std::chrono::steady_clock::now();
+        while (reinterpret_cast<volatile uint64_t*>(hdr->echoed)[slot] < gen - 2) {
+            cudaError_t q = cudaStreamQuery(s);
+            if (q != cudaSuccess && q != cudaErrorNotReady) return BSP_ERR_CUDA;
+            if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(10)) return BSP_ERR_CUDA;
+            std::this_thread::yield();
+        }
+    }
+    bsp_plan_t plan;
+    bsp_status st = bsp_plan_build(geo, batch, beam_width, prefix_len, tail_len, prefix_pages, prefix_pages_stride,
+                                   max_tail, sms, slot_ptr, slot_bytes, &plan);
+    if (st != BSP_OK) return st;
+    if (plan.device_bytes_used > ws_device_bytes) return BSP_ERR_CAPACITY;
+    std::memcpy(slot_ptr, &gen, sizeof gen);  // image header: generation
+    uint8_t* dimg = static_cast<uint8_t*>(ws_device) + kStatusBytes;
+    if (cudaMemcpyAsync(dimg, slot_ptr, plan.image_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return BSP_ERR_CUDA;
+    if (cudaMemcpyAsync(&hdr->echoed[slot], dimg, sizeof(uint64_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    hdr->generation = gen;
+    plan.generation = gen;
+    plan.ws_device = ws_device;
+    plan.ws_device_bytes = ws_device_bytes;
+    plan.ws_host = ws_host;
+    *out = plan;
+    return BSP_OK;
+}
+
+bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, const void* v_new, int64_t src_row_stride,
+                         const int32_t* out_cache_loc, int32_t n, void* k_pool, void* v_pool, void* stream) {
+    bsp_status st = check_plan(plan);
+    if (st != BSP_OK) return st;
+    if (n < 0) return BSP_ERR_INVALID_ARG;
+    if (n == 0) return BSP_OK;
+    const bsp_geometry& geo = plan->geo;
+    if (static_cast<int64_t>(n) > static_cast<int64_t>(plan->batch) * plan->beam_width) return BSP_ERR_INVALID_ARG;
+    if (src_row_stride < static_cast<int64_t>(geo.num_kv_heads) * geo.head_dim || (src_row_stride & 7))
+        return BSP_ERR_INVALID_ARG;
+    if (!device_ptr_ok(k_new) || !device_ptr_ok(v_new) || !device_ptr_ok(out_cache_loc) || !device_ptr_ok(k_pool) ||
+        !device_ptr_ok(v_pool))
+        return BSP_ERR_INVALID_ARG;
+    AppendParams p{};
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.src_row_stride = src_row_stride;
+    p.loc = out_cache_loc;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.status = static_cast<int32_t*>(plan->ws_device);
+    p.n = n;
+    p.Hkv = geo.num_kv_heads;
+    p.D = geo.head_dim;
+    p.ps_log2 = ilog2(geo.page_size);
+    p.num_pages = geo.num_pages;
+    return launch_append(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+}
+
+bsp_status bsp_read_device_status(const bsp_plan_t* plan, void* stream, int32_t clear, int32_t* flags_out) {
+    if (!plan || !plan->ws_device) return BSP_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return BSP_ERR_CUDA;
+    int32_t flags = 0;
+    if (cudaMemcpy(&flags, plan->ws_device, sizeof flags, cudaMemcpyDeviceToHost) != cudaSuccess) return BSP_ERR_CUDA;
+    if (clear && cudaMemset(plan->ws_device, 0, sizeof flags) != cudaSuccess) return BSP_ERR_CUDA;
+    if (flags_out) *flags_out = flags;
+    if (flags & BSP_DEVFLAG_PAGE_INDEX) return BSP_ERR_PAGE_INDEX;
+    if (flags & BSP_DEVFLAG_TIMEOUT) return BSP_ERR_DEVICE_TIMEOUT;
+    return BSP_OK;
+}
+
+bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
+                           int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse, void* stream) {
+    bsp_status st = check_plan(plan);
+    if (st != BSP_OK) return st;
+    if (flags & ~(BSP_FLAG_LSE_BASE2 | BSP_FLAG_CHECK)) return BSP_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BSP_ERR_INVALID_ARG;
+    const bsp_geometry& geo = plan->geo;
+    const int64_t R = static_cast<int64_t>(plan->batch) * plan->beam_width;
+    if (R == 0) return BSP_OK;
+    if (!device_ptr_ok(q) || !device_ptr_ok(k_pool) || !device_ptr_ok(v_pool) || !device_ptr_ok(o) ||
+        !device_ptr_ok(lse))
+        return BSP_ERR_INVALID_ARG;
+    if (plan->max_tail_len > 0) {
+        if (!device_ptr_ok(beam_pages) || !device_ptr_ok(cache_indirection)) return BSP_ERR_INVALID_ARG;
+        if (max_seq < plan->max_total_len || max_seq < 1) return BSP_ERR_INVALID_ARG;
+        if (beam_pages_stride < ceil_div(plan->max_total_len, geo.page_size)) return BSP_ERR_INVALID_ARG;
+    }
+    const int D = geo.head_dim, Hq = geo.num_q_heads, Hkv = geo.num_kv_heads, G = Hq / Hkv;
+    const bool bf16 = geo.dtype == BSP_DTYPE_BF16;
+    const float log2e = 1.4426950408889634f;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(plan->ws_device);
+
+    if (plan->num_units > 0) {
+        CUtensorMap tq, tk, tv;
+        cuuint64_t qdims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(R)};
+        cuuint64_t qstr[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2};
+        cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(plan->beams_per_block)};
+        const int ps = geo.page_size;
+        cuuint64_t kdims[2] = {static_cast<cuuint64_t>(D),
+                               static_cast<cuuint64_t>(geo.num_pages) * Hkv * ps};
+        cuuint64_t kstr[1] = {static_cast<cuuint64_t>(D) * 2};
+        cuuint32_t kbox[2] = {64, static_cast<cuuint32_t>(std::min(ps, kTileKeys))};
+        if (!encode_map(&tq, geo.dtype, 3, q, qdims, qstr, qbox) || !encode_map(&tk, geo.dtype, 2, k_pool, kdims, kstr, kbox) ||
+            !encode_map(&tv, geo.dtype, 2, v_pool, kdims, kstr, kbox))
+            return BSP_ERR_CUDA;
+        PrefixParams pp{};
+        pp.units = reinterpret_cast<const int32_t*>(ws + plan->off_units);
+        pp.req = reinterpret_cast<const int32_t*>(ws + plan->off_req);
+        pp.pages = reinterpret_cast<const int32_t*>(ws + plan->off_pages);
+        pp.part_o = reinterpret_cast<float*>(ws + plan->off_part_o);
+        pp.part_lse = reinterpret_cast<float*>(ws + plan->off_part_lse);
+        pp.status = reinterpret_cast<int32_t*>(ws);
+        pp.W = plan->beam_width;
+        pp.Hq = Hq;
+        pp.Hkv = Hkv;
+        pp.G = G;
+        pp.ps_log2 = ilog2(ps);
+        pp.Wblk = plan->beams_per_block;
+        pp.num_pages = geo.num_pages;
+        pp.scale_log2 = softmax_scale * log2e;
+        if (launch_prefix(D, bf16, plan->num_units, tq, tk, tv, pp, s) != cudaSuccess) return BSP_ERR_CUDA;
+    }
+    TailParams tp{};
+    tp.q = q;
+    tp.k_pool = k_pool;
+    tp.v_pool = v_pool;
+    tp.beam_pages = beam_pages;
+    tp.ci = cache_indirection;
+    tp.req = reinterpret_cast<const int32_t*>(ws + plan->off_req);
+    tp.part_o = reinterpret_cast<const float*>(ws + plan->off_part_o);
+    tp.part_lse = reinterpret_cast<const float*>(ws + plan->off_part_lse);
+    tp.o = o;
+    tp.lse = lse;
+    tp.status = reinterpret_cast<int32_t*>(ws);
+    tp.B = plan->batch;
+    tp.W = plan->beam_width;
+    tp.Hq = Hq;
+    tp.Hkv = Hkv;
+    tp.G = G;
+    tp.ps_log2 = ilog2(geo.page_size);
+    tp.num_pages = geo.num_pages;
+    tp.beam_pages_stride = beam_pages_stride;
+    tp.max_seq = max_seq;
+    tp.scale_log2 = softmax_scale * log2e;
+    tp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
+    if (launch_tail(D, bf16, tp, s) != cudaSuccess) return BSP_ERR_CUDA;
+    if (flags & BSP_FLAG_CHECK) return bsp_read_device_status(plan, stream, 1, nullptr);
+    return BSP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// Internal contract between the host library (bsp_host.cpp) and the kernels:
+// the staged plan image layout and the launch parameter blocks.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace bsp {
+
+// Prompt-attention tiling.
+constexpr int kTileKeys = 64;      // keys per prompt tile (MMA N of Q*K^T, MMA K of P*V)
+constexpr int kRowsPerBlock = 128; // query rows per CTA (MMA M)
+constexpr int kExtraParts = 64;    // key splits beyond one per request the workspace holds
+
+// Device workspace: [status words | plan image | partial LSE | partial O].
+constexpr size_t kStatusBytes = 256;
+constexpr size_t kAlign = 256;
+
+// Plan image (int32 fields, offsets relative to the image start).
+constexpr int kImageHeaderBytes = 64;  // u64 generation, i32 batch, i32 num_units, ...
+// Per-request record.
+enum ReqField { kReqPrefix = 0, kReqTail = 1, kReqSplits = 2, kReqPartOff = 3, kReqPageOff = 4, kReqFields = 8 };
+// Per-work-unit record: request, kv head, query-row block, key tiles [kt0, kt1), partial slot.
+enum UnitField { kUnitReq = 0, kUnitKvHead = 1, kUnitRowBlock = 2, kUnitTile0 = 3, kUnitTile1 = 4, kUnitPart = 5,
+                 kUnitFields = 8 };
+
+struct PrefixParams {
+    const int32_t* units;
+    const int32_t* req;
+    const int32_t* pages;
+    float* part_o;    // [part][W][Hq][D]   (normalised partial output)
+    float* part_lse;  // [part][W][Hq]      (log2-sum-exp2 of the scaled scores)
+    int32_t* status;
+    int W, Hq, Hkv, G, ps_log2, Wblk, num_pages;
+    float scale_log2;  // softmax_scale * log2(e)
+};
+
+struct TailParams {
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* beam_pages;
+    const int32_t* ci;
+    const int32_t* req;
+    const float* part_o;
+    const float* part_lse;
+    void* o;
+    float* lse;
+    int32_t* status;
+    int B, W, Hq, Hkv, G, ps_log2, num_pages, beam_pages_stride, max_seq;
+    float scale_log2;
+    int lse_base2;
+};
+
+struct AppendParams {
+    const void* k_new;
+    const void* v_new;
+    int64_t src_row_stride;  // elements
+    const int32_t* loc;
+    void* k_pool;
+    void* v_pool;
+    int32_t* status;
+    int n, Hkv, D, ps_log2, num_pages;
+};
+
+cudaError_t launch_prefix(int head_dim, bool bf16, int num_units, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const PrefixParams& p, cudaStream_t stream);
+cudaError_t launch_tail(int head_dim, bool bf16, const TailParams& p, cudaStream_t stream);
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+
+}  // namespace bsp

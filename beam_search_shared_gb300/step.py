@@ -1,0 +1,93 @@
+"""One decode step on the GPU through the C ABI: device buffers for a case, plan, append, attention.
+
+Holds the device-resident state of a synthetic step (pools, page tables,
+indirection, queries, new token rows) and calls the binding. Used by the tests,
+the benchmark and ``__graft_entry__.smoke()``.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import bsp
+from .synth import Case
+
+
+class DeviceStep:
+    def __init__(self, case: Case, device="cuda", max_tail: int = bsp.MAX_TAIL,
+                 workspace: Optional[bsp.Workspace] = None):
+        wl = case.workload
+        self.case = case
+        self.device = torch.device(device)
+        dev = self.device
+        self.geo = bsp.geometry(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.page_size, case.num_pages,
+                                wl.dtype)
+        self.max_tail = max_tail
+        self.q = case.q.to(dev)
+        self.k_pool = case.k_pool.to(dev)
+        self.v_pool = case.v_pool.to(dev)
+        R = wl.batch * wl.beam_width
+        self.k_new = case.k_new.to(dev).reshape(case.k_new.shape[0], -1)
+        self.v_new = case.v_new.to(dev).reshape(case.v_new.shape[0], -1)
+        self.out_cache_loc = torch.from_numpy(case.out_cache_loc).to(dev)
+        self.beam_pages = torch.from_numpy(case.beam_pages).to(dev)
+        self.cache_indirection = torch.from_numpy(case.cache_indirection).to(dev)
+        self.o = torch.empty((R, wl.num_q_heads, wl.head_dim), dtype=self.q.dtype, device=dev)
+        self.lse = torch.empty((R, wl.num_q_heads), dtype=torch.float32, device=dev)
+        self.scale = 1.0 / math.sqrt(wl.head_dim)
+        self.ws = workspace or bsp.Workspace(self.geo, max(1, wl.batch), wl.beam_width,
+                                             case.prefix_pages.shape[1], device=dev)
+        self.plan = None
+
+    def make_plan(self, stream=None):
+        c = self.case
+        wl = c.workload
+        self.plan = self.ws.plan(self.geo, wl.batch, wl.beam_width, c.prefix_len, c.tail_len, c.prefix_pages,
+                                 self.max_tail, stream=stream)
+        return self.plan
+
+    def append(self, stream=None):
+        bsp.append_kv(self.plan, self.k_new, self.v_new, self.out_cache_loc, self.k_pool, self.v_pool,
+                      stream=stream)
+
+    def attend(self, flags: int = 0, stream=None):
+        bsp.decode_attn(self.plan, self.q, self.k_pool, self.v_pool, self.beam_pages, self.cache_indirection,
+                        self.scale, self.o, self.lse, flags=flags, stream=stream)
+
+    def run(self, flags: int = 0, stream=None):
+        """plan + append (full steps) + attention, then the device status (syncs)."""
+        self.make_plan(stream)
+        if self.case.full_step:
+            self.append(stream)
+        self.attend(flags, stream)
+        return bsp.read_device_status(self.plan, clear=True, stream=stream)
+
+
+def algorithmic_bytes(case: Case) -> dict:
+    """Bytes each kernel must move at least once, from the drawn lengths.
+
+    prefix: valid K+V prompt rows once per (request, kv head) + Q + fp32 partial O/LSE write;
+    tail:   gathered K+V tail rows per (beam, kv head) + Q + partial read + O/LSE write;
+    append: read + write of the new K and V rows.
+    """
+    wl = case.workload
+    e = 2
+    D, Hq, Hkv, W = wl.head_dim, wl.num_q_heads, wl.num_kv_heads, wl.beam_width
+    P = case.prefix_len.astype(np.int64)
+    T = case.tail_len.astype(np.int64)
+    R = wl.batch * W
+    active = P > 0
+    prefix_kv = int(np.sum(P)) * Hkv * D * e * 2
+    q_bytes = R * Hq * D * e
+    part = int(np.sum(active)) * W * Hq * (D + 1) * 4
+    prefix = prefix_kv + int(np.sum(active)) * W * Hq * D * e + part
+    tail_kv = int(np.sum(T)) * W * Hkv * D * e * 2
+    tail = tail_kv + q_bytes + part + R * Hq * (D * e + 4)
+    n = int(case.out_cache_loc.shape[0])
+    append = n * Hkv * D * e * 2 * 2
+    flops = int(np.sum(P)) * W * Hq * D * 4
+    return {"prefix": prefix, "tail": tail, "append": append, "prefix_flops": flops,
+            "prefix_kv": prefix_kv}

@@ -1,0 +1,251 @@
+/*
+ * bsp.h - C ABI of the GB300 shared-prefix (cascade) beam decode attention
+ * library (libbsp.so).
+ *
+ * One decode step of wide beam search over a paged KV cache, per layer:
+ *   bsp_plan        host planning: validates lengths and beam 0's prompt page
+ *                   tables, splits the prompt attention into work units and
+ *                   stages the plan to the device without a stream sync;
+ *   bsp_append_kv   writes each beam's new token K/V at its flat cache slot;
+ *   bsp_decode_attn attends each request's shared prompt once for all of its
+ *                   beams (tensor cores), each beam's own tail through
+ *                   cache_indirection, and merges the two by log-sum-exp,
+ *                   returning O and LSE.
+ * The method: TensorRT-LLM PR #21738, "Add opt-in cascade attention for wide
+ * beam search on KVCM V2" (description, "Solution"); the valid-prefix bound:
+ * TensorRT-Model-Connect PR #2202, "prefill and decode over the cached prefix,
+ * not the whole KV allocation"; the append: TensorRT-LLM PR #18614, "Fuse
+ * MiniMax-M3 MSA per-layer KV-cache writes into one kernel".
+ *
+ * Conventions for every call
+ *  - Memory: all device and host memory is owned by the caller. The library
+ *    allocates nothing and keeps no state between calls beyond what it writes
+ *    into the caller's workspace.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Every device effect of a call is enqueued on that stream; no call
+ *    synchronises the stream unless documented (BSP_FLAG_CHECK,
+ *    bsp_read_device_status).
+ *  - Errors: arguments are validated on the host before anything is enqueued;
+ *    on any error nothing is launched and pools/outputs are left unchanged.
+ *    Indices that live in device memory (beam_pages, cache_indirection,
+ *    out_cache_loc) cannot be validated without a sync: kernels bounds-check
+ *    them, skip the access and set a flag in the workspace's device status
+ *    word, which bsp_read_device_status (or BSP_FLAG_CHECK) reports as
+ *    BSP_ERR_PAGE_INDEX. Kernels never trap.
+ *  - Layouts (row-major, innermost last, 16-bit elements unless stated):
+ *      q, o            [R = batch * beam_width][num_q_heads][head_dim], row r = b*W + w
+ *      lse             [R][num_q_heads] float32
+ *      k_pool, v_pool  [num_pages][num_kv_heads][page_size][head_dim]
+ *      beam_pages      [R][beam_pages_stride] int32 page ids of each beam's sequence
+ *      cache_indirection [batch][beam_width][max_seq] int32 source beam per position
+ *    Query head h uses kv head h / (num_q_heads / num_kv_heads).
+ *    Device pointers must be 16-byte aligned.
+ */
+#ifndef BSP_H_
+#define BSP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BSP_API __attribute__((visibility("default")))
+#else
+#define BSP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bsp_status {
+    BSP_OK = 0,
+    BSP_ERR_INVALID_ARG = 1,  /* null/misaligned/host pointer, bad length or stride */
+    BSP_ERR_UNSUPPORTED = 2,  /* dtype, head_dim, group size, page size or tail outside the supported set */
+    BSP_ERR_PAGE_INDEX = 3,   /* a page id, slot or indirection value out of range */
+    BSP_ERR_CAPACITY = 4,     /* workspace or staging buffer too small */
+    BSP_ERR_STALE_PLAN = 5,   /* plan superseded by a newer bsp_plan on the same workspace */
+    BSP_ERR_CUDA = 6,         /* a CUDA runtime/driver call failed */
+    BSP_ERR_DEVICE_TIMEOUT = 7 /* a kernel's bounded wait gave up (reported by status reads) */
+} bsp_status;
+
+enum { BSP_DTYPE_BF16 = 0, BSP_DTYPE_FP16 = 1 };
+
+/* bsp_decode_attn flags */
+enum {
+    BSP_FLAG_LSE_BASE2 = 1, /* write LSE as log2-sum-exp2 instead of the natural log */
+    BSP_FLAG_CHECK = 2      /* synchronise after the launches and report device status */
+};
+
+#define BSP_MAX_TAIL 8   /* tail positions per beam (TensorRT-LLM PR #21738, "Correctness and limits") */
+#define BSP_MAX_GROUP 8  /* query heads per kv head */
+
+/* Bits of the device status word. */
+#define BSP_DEVFLAG_PAGE_INDEX 1
+#define BSP_DEVFLAG_TIMEOUT 2
+
+typedef struct bsp_geometry {
+    int32_t num_q_heads;  /* Hq */
+    int32_t num_kv_heads; /* Hkv; Hq % Hkv == 0, Hq / Hkv <= BSP_MAX_GROUP */
+    int32_t head_dim;     /* 64, 128 or 256 */
+    int32_t page_size;    /* tokens per page: 8, 16, 32, 64 or 128 */
+    int32_t num_pages;    /* pages in each pool */
+    int32_t dtype;        /* BSP_DTYPE_*; q, pools, o and new K/V share it */
+} bsp_geometry;
+
+/*
+ * Plan of one decode step, filled by bsp_plan / bsp_plan_build. Caller-owned
+ * plain data; the fields below `generation` describe the staged device image
+ * and are read by the launches. A plan refers to the workspace it was staged
+ * into; it stays valid until the next bsp_plan on that workspace.
+ */
+typedef struct bsp_plan_t {
+    bsp_geometry geo;
+    int32_t batch;               /* B */
+    int32_t beam_width;          /* W */
+    int32_t max_tail;            /* bound on every tail_len, <= BSP_MAX_TAIL */
+    int32_t prefix_pages_stride; /* row stride of the prefix_pages table given to the plan */
+    int32_t num_units;           /* prompt-attention work units (CTAs) */
+    int32_t num_parts;           /* (request, key split) prompt partial states */
+    int32_t row_blocks;          /* query-row blocks per (request, kv head) */
+    int32_t beams_per_block;     /* beams in one query-row block */
+    int32_t tile_keys;           /* keys per prompt tile */
+    int32_t max_prefix_len;      /* max_b P_b */
+    int32_t max_total_len;       /* max_b P_b + T_b */
+    int32_t num_sms;             /* SM count the units were balanced for */
+    int32_t max_tail_len;        /* max_b T_b */
+    int32_t reserved_i;
+    uint64_t generation;         /* staging generation of this plan (0: built only, not staged) */
+    void* ws_device;             /* device workspace the plan was staged into */
+    uint64_t ws_device_bytes;
+    void* ws_host;               /* host staging buffer paired with ws_device */
+    uint64_t image_bytes;        /* bytes of the staged plan image */
+    uint64_t off_req;            /* byte offsets into ws_device */
+    uint64_t off_units;
+    uint64_t off_pages;
+    uint64_t off_part_lse;
+    uint64_t off_part_o;
+    uint64_t device_bytes_used;
+    uint64_t reserved[4];
+} bsp_plan_t;
+
+/* Human-readable name of a bsp_status value. Never NULL. */
+BSP_API const char* bsp_status_string(int32_t status);
+
+/*
+ * Rows to bind for a cached prefix of `valid_rows` rows in an allocation of
+ * `capacity` rows: rounded up to a 256-row bucket, one (masked) row for an
+ * empty cache, capped at the allocation (TensorRT-Model-Connect PR #2202,
+ * Implementation: kv_cache.{h,cpp}, kCacheRowBucket). The kernels themselves
+ * read only the valid rows; this is the bound a caller binds when it needs a
+ * shape that changes once per 256 tokens. Returns -1 if capacity < 1.
+ */
+BSP_API int32_t bsp_bucket_rows(int32_t valid_rows, int32_t capacity);
+
+/*
+ * Upper bounds of the device workspace and the host staging buffer for plans
+ * with batch <= max_batch, beam_width <= max_beam and prompt page tables of at
+ * most max_prefix_pages pages (TensorRT-LLM PR #21738, "size the float
+ * workspace from the engine's maximum rows"). The host staging buffer should
+ * be pinned (page-locked) for the copy to be asynchronous.
+ */
+BSP_API bsp_status bsp_workspace_size(const bsp_geometry* geo, int32_t max_batch, int32_t max_beam,
+                              int32_t max_prefix_pages, size_t* device_bytes, size_t* host_bytes);
+
+/*
+ * Host-only planning: validates the step and writes the device plan image into
+ * `image` (host memory, `image_bytes` capacity) without touching CUDA. Used by
+ * bsp_plan; exposed for tests and for callers that stage the image themselves.
+ *   prefix_len[b]   valid prompt rows P_b >= 0 of request b (host)
+ *   tail_len[b]     tail positions T_b in [0, max_tail] (host); the tail
+ *                   includes the current token once it is appended
+ *   prefix_pages    host [batch][prefix_pages_stride]: beam 0's page ids of the
+ *                   prompt; the first ceil(P_b / page_size) entries of row b
+ *                   are read and each must lie in [0, num_pages), else
+ *                   BSP_ERR_PAGE_INDEX (never clamped) (TensorRT-LLM PR #21738,
+ *                   "Raise on an invalid prompt page index")
+ *   max_tail        <= BSP_MAX_TAIL ("Under CUDA graphs a beam may generate at
+ *                   most ... MAX_TAIL tokens")
+ *   num_sms         SMs to balance the prompt work units for (> 0)
+ * `plan_out->generation` is 0 and the workspace fields are left NULL.
+ */
+BSP_API bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_width,
+                          const int32_t* prefix_len, const int32_t* tail_len, const int32_t* prefix_pages,
+                          int32_t prefix_pages_stride, int32_t max_tail, int32_t num_sms, void* image,
+                          size_t image_bytes, bsp_plan_t* plan_out);
+
+/*
+ * Plans one decode step (per-step host planning, TensorRT-LLM PR #21738:
+ * "the per-step host plan runs ... so it precedes both CUDA-graph capture and
+ * replay"; "Stage CUDA-graph plan inputs pinned ... so re-planning each step
+ * does not synchronize the stream").
+ * Builds the image (bsp_plan_build, balanced for the current device's SM
+ * count), writes it into one of two slots of `ws_host` and enqueues its copy
+ * into `ws_device` on `stream`. The workspace pair (ws_device, ws_host) must
+ * have at least the sizes bsp_workspace_size reports; ws_host should be pinned.
+ * A slot is rewritten only after the stream has finished copying the plan
+ * that used it two plans earlier (the stream echoes a generation number back
+ * into ws_host); if that has not happened the call waits for it, up to 10 s,
+ * then returns BSP_ERR_CUDA. Planning again makes every earlier plan of this
+ * workspace stale (BSP_ERR_STALE_PLAN from the launches) (TensorRT-LLM PR
+ * #21738, "Drop the previous step's plan").
+ */
+BSP_API bsp_status bsp_plan(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len,
+                    const int32_t* tail_len, const int32_t* prefix_pages, int32_t prefix_pages_stride,
+                    int32_t max_tail, void* ws_device, size_t ws_device_bytes, void* ws_host,
+                    size_t ws_host_bytes, void* stream, bsp_plan_t* plan_out);
+
+/*
+ * Paged KV append: for every new token i < n and kv head h, copies the
+ * head_dim elements of k_new / v_new row i, head h to
+ * pool[out_cache_loc[i] / page_size][h][out_cache_loc[i] % page_size][:],
+ * bit for bit, in one launch (TensorRT-LLM PR #18614, description: one launch
+ * per layer "derives (page, within-page) from out_cache_loc in-register and
+ * writes K, V ... together").
+ *   k_new, v_new    device [n] rows of num_kv_heads * head_dim contiguous
+ *                   elements, rows `src_row_stride` elements apart
+ *                   (>= num_kv_heads * head_dim, a multiple of 8) - e.g. a
+ *                   column slice of a fused QKV projection
+ *   out_cache_loc   device int32 [n] flat slots; a slot outside
+ *                   [0, num_pages * page_size) is skipped and flagged
+ *   n               0 is a no-op returning BSP_OK; must be <= batch * beam_width
+ * Duplicate slots are a caller error (the surviving row is unspecified).
+ */
+BSP_API bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, const void* v_new, int64_t src_row_stride,
+                         const int32_t* out_cache_loc, int32_t n, void* k_pool, void* v_pool, void* stream);
+
+/*
+ * Cascade decode attention (TensorRT-LLM PR #21738, description, "Solution"):
+ * for every row r = b*W + w and query head h,
+ *   O[r][h] = softmax(scale * q K^T) V over the beam's logical sequence:
+ *             prompt positions j < P_b read through beam 0's prompt pages
+ *             (the plan's prefix_pages), tail positions j in [P_b, P_b + T_b)
+ *             read through beam_pages[b*W + cache_indirection[b][w][j]];
+ *   LSE[r][h] = log-sum-exp of the scaled scores (natural log, or base 2 with
+ *             BSP_FLAG_LSE_BASE2); an empty sequence gives O = 0, LSE = -inf.
+ * The prompt is attended once per (request, kv head) for all beams and query
+ * heads (tensor cores), the tail per beam, and the two merge exactly by
+ * log-sum-exp. Only the valid P_b prompt rows are read, never the allocation.
+ *   beam_pages_stride  entries per beam_pages row, >= ceil(max(P_b+T_b)/page_size)
+ *   max_seq            innermost extent of cache_indirection, >= max(P_b + T_b)
+ *   softmax_scale      > 0, typically 1/sqrt(head_dim)
+ *   flags              BSP_FLAG_* bits
+ * The plan must be the latest one staged into its workspace.
+ */
+BSP_API bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
+                           int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse,
+                           void* stream);
+
+/*
+ * Synchronises `stream`, then reads the workspace's device status word into
+ * *flags_out (BSP_DEVFLAG_* bits set by kernels since the last clear) and
+ * clears it when `clear` is non-zero. Returns BSP_ERR_PAGE_INDEX or
+ * BSP_ERR_DEVICE_TIMEOUT when a bit is set, BSP_OK otherwise.
+ */
+BSP_API bsp_status bsp_read_device_status(const bsp_plan_t* plan, void* stream, int32_t clear, int32_t* flags_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSP_H_ */

@@ -1,0 +1,201 @@
+"""Host-side tests of libbsp.so: exports, status codes, bucket rule and planning.
+
+No CUDA device is needed: only entry points that stay on the host are called.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from beam_search_shared_gb300 import bsp, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+STATUS_OFFSET = 256  # device status words precede the plan image
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return bsp.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "bsp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsp_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(bsp.EXPORTS), names
+    for n in names:
+        assert hasattr(lib, n), n
+    # nothing else leaks out of the library (symbols are hidden by default)
+    out = os.popen(f"nm -D --defined-only {build.LIB}").read()
+    exported = sorted(set(re.findall(r" T (bsp_\w+)", out)))
+    assert exported == names
+
+
+def test_status_strings(lib):
+    for code, name in bsp.STATUS_NAMES.items():
+        assert bsp.status_string(code)
+    assert bsp.status_string(99) == "unknown status"
+
+
+def test_bucket_rows_matches_oracle_rule(lib):
+    for cap in (1, 64, 300, 10368):
+        for valid in list(range(0, 600)) + [2047, 2048, 10000, 10240, 10241, 10368, 20000]:
+            assert bsp.bucket_rows(valid, cap) == oracle.bucket_rows(valid, cap), (valid, cap)
+    assert bsp.bucket_rows(5, 0) == -1
+
+
+def geo(Hq=16, Hkv=8, D=128, ps=32, npages=1000, dtype="bf16"):
+    return bsp.geometry(Hq, Hkv, D, ps, npages, dtype)
+
+
+def test_workspace_size_grows_with_limits(lib):
+    d1, h1 = bsp.workspace_size(geo(), 64, 30, 32)
+    d2, h2 = bsp.workspace_size(geo(), 128, 96, 128)
+    assert 0 < d1 < d2 and 0 < h1 < h2
+    with pytest.raises(bsp.BspError, match="UNSUPPORTED"):
+        bsp.workspace_size(geo(D=96), 1, 1, 1)
+
+
+def _err(fn, *a, **k):
+    with pytest.raises(bsp.BspError) as e:
+        fn(*a, **k)
+    return bsp.STATUS_NAMES[e.value.status]
+
+
+def test_plan_build_validation(lib):
+    P, T = [100, 40], [2, 0]
+    pages = np.arange(8, dtype=np.int32).reshape(2, 4)
+    ok = lambda **kw: bsp.plan_build(kw.pop("g", geo()), kw.pop("B", 2), kw.pop("W", 4), kw.pop("P", P),
+                                     kw.pop("T", T), kw.pop("pages", pages), kw.pop("max_tail", 8),
+                                     kw.pop("sms", 152))
+    ok()
+    assert _err(ok, g=geo(dtype="bf16", D=80)) == "BSP_ERR_UNSUPPORTED"
+    assert _err(ok, g=geo(Hq=18, Hkv=2)) == "BSP_ERR_UNSUPPORTED"     # group 9 > 8
+    assert _err(ok, g=geo(Hq=12, Hkv=8)) == "BSP_ERR_UNSUPPORTED"     # not a multiple
+    assert _err(ok, g=geo(ps=24)) == "BSP_ERR_UNSUPPORTED"
+    assert _err(ok, g=geo(ps=256)) == "BSP_ERR_UNSUPPORTED"
+    assert _err(ok, g=geo(npages=0)) == "BSP_ERR_INVALID_ARG"
+    assert _err(ok, T=[9, 0]) == "BSP_ERR_CAPACITY"                  # tail above max_tail
+    assert _err(ok, T=[3, 0], max_tail=2) == "BSP_ERR_CAPACITY"
+    assert _err(ok, max_tail=9) == "BSP_ERR_UNSUPPORTED"
+    assert _err(ok, P=[-1, 4]) == "BSP_ERR_INVALID_ARG"
+    assert _err(ok, W=0) == "BSP_ERR_INVALID_ARG"
+    assert _err(ok, sms=0) == "BSP_ERR_INVALID_ARG"
+    bad = pages.copy()
+    bad[1, 1] = 1000                                                  # second prompt page of request 1
+    assert _err(ok, P=[100, 40], pages=bad) == "BSP_ERR_PAGE_INDEX"
+    bad[1, 1] = -1
+    assert _err(ok, pages=bad) == "BSP_ERR_PAGE_INDEX"
+    # entries past ceil(P/ps) are never read
+    bad = pages.copy()
+    bad[1, 2:] = -7
+    ok(pages=bad)
+    # a page table narrower than the longest prompt
+    assert _err(ok, P=[200, 40]) == "BSP_ERR_INVALID_ARG"
+
+
+def decode_image(plan, img):
+    i32 = img.view(np.int32)
+    base = STATUS_OFFSET
+    req = i32[(plan.off_req - base) // 4:(plan.off_units - base) // 4].reshape(plan.batch, 8)
+    units = i32[(plan.off_units - base) // 4:(plan.off_pages - base) // 4].reshape(plan.num_units, 8)
+    pages = i32[(plan.off_pages - base) // 4:]
+    return req, units, pages
+
+
+def check_units_cover(plan, req, units, P, tile=64):
+    """Every (request, kv head, row block) covers its prompt tiles exactly once."""
+    B, Hkv, nrb = plan.batch, plan.geo.num_kv_heads, plan.row_blocks
+    cover = {}
+    for b_, g_, rb_, t0, t1, part, _, _ in units:
+        assert 0 <= t0 < t1
+        key = (b_, g_, rb_)
+        cover.setdefault(key, []).append((t0, t1, part))
+    for b in range(B):
+        ntile = -(-P[b] // tile)
+        for g in range(Hkv):
+            for rb in range(nrb):
+                spans = sorted(cover.get((b, g, rb), []))
+                if ntile == 0:
+                    assert not spans
+                    continue
+                assert spans[0][0] == 0 and spans[-1][1] == ntile
+                for (a0, a1, _), (c0, c1, _) in zip(spans, spans[1:]):
+                    assert a1 == c0
+                parts = [s[2] for s in spans]
+                assert parts == list(range(req[b][3], req[b][3] + req[b][2]))
+    assert len(cover) == sum(1 for b in range(B) if P[b] > 0) * Hkv * nrb
+
+
+def test_plan_image_wide_batch_needs_no_split(lib):
+    rng = np.random.default_rng(3)
+    B, W, ps = 64, 30, 32
+    P = rng.integers(400, 601, B)
+    T = rng.integers(0, 5, B)
+    maxp = -(-P.max() // ps)
+    pages = rng.integers(0, 5000, (B, maxp)).astype(np.int32)
+    plan, img = bsp.plan_build(geo(npages=5000), B, W, P, T, pages, 8, 152)
+    req, units, pl = decode_image(plan, img)
+    assert plan.row_blocks == 1 and plan.beams_per_block == 30
+    assert plan.num_units == B * 8 and plan.num_parts == B
+    assert plan.max_tail_len == T.max() and plan.max_total_len == (P + T).max()
+    np.testing.assert_array_equal(req[:, 0], P)
+    np.testing.assert_array_equal(req[:, 1], T)
+    np.testing.assert_array_equal(req[:, 2], 1)
+    check_units_cover(plan, req, units, P)
+    lens = units[:, 4] - units[:, 3]
+    assert np.all(np.diff(lens) <= 0)                      # longest first
+    for b in range(B):
+        n = -(-P[b] // ps)
+        np.testing.assert_array_equal(pl[req[b][4]:req[b][4] + n], pages[b, :n])
+
+
+def test_plan_image_wide_beam_row_blocks(lib):
+    B, W = 3, 96
+    P = [3000, 2900, 0]
+    T = [1, 0, 3]
+    pages = np.tile(np.arange(94, dtype=np.int32), (B, 1))
+    plan, img = bsp.plan_build(geo(npages=200), B, W, P, T, pages, 8, 152)
+    req, units, _ = decode_image(plan, img)
+    assert plan.row_blocks == 2 and plan.beams_per_block == 48    # 192 rows -> 2 x 96
+    check_units_cover(plan, req, units, P)
+    assert req[2][2] == 0                                            # empty prompt: no split, no unit
+
+
+def test_plan_image_single_long_request_is_split(lib):
+    """One request with 8 kv heads is split along its keys to fill the GPU."""
+    P = [10000]
+    pages = np.arange(324, dtype=np.int32)[None]
+    plan, img = bsp.plan_build(geo(Hq=32, Hkv=8, npages=324, dtype="fp16"), 1, 1, P, [1], pages, 8, 152)
+    req, units, _ = decode_image(plan, img)
+    assert plan.num_parts == req[0][2] > 8
+    assert plan.num_parts <= 1 + 64
+    assert plan.num_units == plan.num_parts * 8
+    check_units_cover(plan, req, units, P)
+    lens = units[:, 4] - units[:, 3]
+    assert lens.max() - lens.min() <= 1
+
+
+def test_plan_image_empty_batch_and_empty_prompts(lib):
+    plan, img = bsp.plan_build(geo(), 0, 4, [], [], np.zeros((0, 1), np.int32), 8, 152)
+    assert plan.num_units == 0 and plan.batch == 0
+    plan, img = bsp.plan_build(geo(), 2, 4, [0, 0], [1, 3], np.zeros((2, 1), np.int32), 8, 152)
+    assert plan.num_units == 0 and plan.num_parts == 0 and plan.max_tail_len == 3
+
+
+def test_plan_struct_layout_matches_header(lib):
+    """The ctypes mirror has the field order and sizes of bsp_plan_t."""
+    text = open(os.path.join(ROOT, "include", "bsp.h")).read()
+    body = text[text.index("typedef struct bsp_plan_t"):text.index("} bsp_plan_t;")]
+    fields = re.findall(r"^\s+(?:int32_t|uint64_t|void\*|bsp_geometry)\s+(\w+)", body, flags=re.M)
+    names = [f[0] for f in bsp.Plan._fields_]
+    assert fields == names
+    assert ctypes.sizeof(bsp.Plan) % 8 == 0
