@@ -94,7 +94,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.bsp_append_kv.restype = i32
     lib.bsp_append_kv.argtypes = [P(Plan), vp, vp, i64, vp, i32, vp, vp, vp]
     lib.bsp_decode_attn.restype = i32
-    lib.bsp_decode_attn.argtypes = [P(Plan), vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, i32, vp, vp, vp]
+    lib.bsp_decode_attn.argtypes = [P(Plan), vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, i32, vp, vp, vp, vp]
     lib.bsp_read_device_status.restype = i32
     lib.bsp_read_device_status.argtypes = [P(Plan), vp, i32, P(i32)]
     _lib = lib
@@ -198,13 +198,22 @@ def append_kv(plan_: Plan, k_new: torch.Tensor, v_new: torch.Tensor, out_cache_l
 
 def decode_attn(plan_: Plan, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
                 beam_pages: Optional[torch.Tensor], cache_indirection: Optional[torch.Tensor], softmax_scale: float,
-                o: torch.Tensor, lse: torch.Tensor, flags: int = 0, stream=None):
-    """bsp_decode_attn: writes o [R,Hq,D] and lse [R,Hq] (fp32)."""
+                o: torch.Tensor, lse: torch.Tensor, flags: int = 0, events=None, stream=None):
+    """bsp_decode_attn: writes o [R,Hq,D] and lse [R,Hq] (fp32).
+
+    ``events``: optional 3 torch.cuda.Event(enable_timing=True) recorded around the prompt and tail kernels.
+    """
     bps = int(beam_pages.shape[-1]) if beam_pages is not None else 0
     max_seq = int(cache_indirection.shape[-1]) if cache_indirection is not None else 0
+    ev = None
+    if events is not None:
+        for e in events:
+            if e.cuda_event == 0:
+                e.record()  # materialise the underlying cudaEvent_t
+        ev = (ctypes.c_void_p * 3)(*[e.cuda_event for e in events])
     _check("bsp_decode_attn", load().bsp_decode_attn(
         ctypes.byref(plan_), _dptr(q), _dptr(k_pool), _dptr(v_pool), _dptr(beam_pages), bps,
-        _dptr(cache_indirection), max_seq, float(softmax_scale), int(flags), _dptr(o), _dptr(lse),
+        _dptr(cache_indirection), max_seq, float(softmax_scale), int(flags), _dptr(o), _dptr(lse), ev,
         _stream(stream)))
 
 

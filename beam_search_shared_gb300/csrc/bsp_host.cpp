@@ -419,7 +419,8 @@ bsp_status bsp_read_device_status(const bsp_plan_t* plan, void* stream, int32_t 
 
 bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
                            const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
-                           int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse, void* stream) {
+                           int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse,
+                           void* const* events, void* stream) {
     bsp_status st = check_plan(plan);
     if (st != BSP_OK) return st;
     if (flags & ~(BSP_FLAG_LSE_BASE2 | BSP_FLAG_CHECK)) return BSP_ERR_INVALID_ARG;
@@ -441,6 +442,10 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(plan->ws_device);
 
+    auto record = [&](int i) -> bool {
+        return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
+    };
+    if (!record(0)) return BSP_ERR_CUDA;
     if (plan->num_units > 0) {
         CUtensorMap tq, tk, tv;
         cuuint64_t qdims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(R)};
@@ -471,6 +476,7 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
         pp.scale_log2 = softmax_scale * log2e;
         if (launch_prefix(D, bf16, plan->num_units, tq, tk, tv, pp, s) != cudaSuccess) return BSP_ERR_CUDA;
     }
+    if (!record(1)) return BSP_ERR_CUDA;
     TailParams tp{};
     tp.q = q;
     tp.k_pool = k_pool;
@@ -495,6 +501,7 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
     tp.scale_log2 = softmax_scale * log2e;
     tp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
     if (launch_tail(D, bf16, tp, s) != cudaSuccess) return BSP_ERR_CUDA;
+    if (!record(2)) return BSP_ERR_CUDA;
     if (flags & BSP_FLAG_CHECK) return bsp_read_device_status(plan, stream, 1, nullptr);
     return BSP_OK;
 }

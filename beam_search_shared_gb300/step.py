@@ -53,16 +53,16 @@ class DeviceStep:
         bsp.append_kv(self.plan, self.k_new, self.v_new, self.out_cache_loc, self.k_pool, self.v_pool,
                       stream=stream)
 
-    def attend(self, flags: int = 0, stream=None):
+    def attend(self, flags: int = 0, events=None, stream=None):
         bsp.decode_attn(self.plan, self.q, self.k_pool, self.v_pool, self.beam_pages, self.cache_indirection,
-                        self.scale, self.o, self.lse, flags=flags, stream=stream)
+                        self.scale, self.o, self.lse, flags=flags, events=events, stream=stream)
 
     def run(self, flags: int = 0, stream=None):
         """plan + append (full steps) + attention, then the device status (syncs)."""
         self.make_plan(stream)
         if self.case.full_step:
             self.append(stream)
-        self.attend(flags, stream)
+        self.attend(flags, stream=stream)
         return bsp.read_device_status(self.plan, clear=True, stream=stream)
 
 

@@ -1,0 +1,398 @@
+#!/usr/bin/env python3
+"""Benchmark of one cascade beam decode step: paged KV append + shared-prefix decode attention.
+
+A step is one layer over the whole batch: bsp_append_kv then bsp_decode_attn (prompt kernel on tensor
+cores, tail + log-sum-exp merge kernel). Default workload: the Qwen3-0.6B-shaped layer (batch 64,
+beam 30, 16/8 heads, head_dim 128, bf16, page 32, prompt U{400..600}, tail U{0..4}).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Prints one JSON line (rank 0). Under torchrun each rank runs its own independent batch (requests
+shard across GPUs; nothing is exchanged on the data path) and the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "beam decode-attn steps/s"
+DEFAULT_WORKLOAD = "qwen3_0p6b_b64_w30"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "prefix_traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--sets", type=int, default=3, help="rotated input sets (each larger than L2)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed plumbing (host only)
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.result = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if self.proc is None:
+            return False
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if sm:
+            self.result = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                           "samples": len(sm)}
+        return False
+
+
+# ---------------------------------------------------------------- peaks / traffic
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def prefix_source_hash():
+    h = hashlib.sha256()
+    for name in ("bsp_prefix.cu", "bsp_ptx.cuh", "bsp_internal.h"):
+        with open(os.path.join(ROOT, "beam_search_shared_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per prompt-kernel launch from the committed ncu summary, if the kernel is unchanged."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as f:
+        d = json.load(f)
+    if d.get("kernel_source_sha") != prefix_source_hash() or d.get("workload") != workload:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- oracle timing (CPU)
+class OracleTimer:
+    """The fp64 oracle (append scatter + unsplit attention) timed on bounded row samples of one step."""
+
+    def __init__(self, case):
+        import oracle
+        from beam_search_shared_gb300 import synth
+        self.oracle = oracle
+        self.case = case
+        wl = case.workload
+        self.R = wl.batch * wl.beam_width
+        self.kp, self.vp = synth.bits(case.k_pool).copy(), synth.bits(case.v_pool).copy()
+        self.kn, self.vn = synth.bits(case.k_new), synth.bits(case.v_new)
+        self.kw = dict(dtype=wl.dtype, B=wl.batch, W=wl.beam_width, Hq=wl.num_q_heads, Hkv=wl.num_kv_heads,
+                       D=wl.head_dim, ps=wl.page_size, num_pages=case.num_pages, prefix_len=case.prefix_len,
+                       tail_len=case.tail_len, prefix_pages=case.prefix_pages, beam_pages=case.beam_pages,
+                       cache_indirection=case.cache_indirection, q_bits=synth.bits(case.q), k_pool_bits=self.kp,
+                       v_pool_bits=self.vp, scale=1 / math.sqrt(wl.head_dim))
+        self.rng = np.random.default_rng(0)
+        oracle.build()
+        cores = len(os.sched_getaffinity(0))
+        self.cores = min(cores, int(os.environ.get("OMP_NUM_THREADS", cores)))
+        t0 = time.perf_counter()
+        self.sample(min(self.R, 8))
+        self.per_row = (time.perf_counter() - t0) / min(self.R, 8)
+
+    def rows_for(self, seconds):
+        return int(max(1, min(self.R, seconds / max(self.per_row, 1e-9))))
+
+    def sample(self, n):
+        rows = np.sort(self.rng.choice(self.R, n, replace=False)).astype(np.int32)
+        self.oracle.decode_attn(rows=rows, **self.kw)
+
+    def step_seconds(self, n):
+        """One step's time: the append in full plus n of R rows of attention, scaled to all rows."""
+        wl = self.case.workload
+        t0 = time.perf_counter()
+        self.oracle.append_kv(Hkv=wl.num_kv_heads, D=wl.head_dim, ps=wl.page_size, num_pages=self.case.num_pages,
+                              out_cache_loc=self.case.out_cache_loc, k_new_bits=self.kn, v_new_bits=self.vn,
+                              k_pool_bits=self.kp, v_pool_bits=self.vp)
+        t_app = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        self.sample(n)
+        t_attn = time.perf_counter() - t0
+        return t_app + t_attn * self.R / n, t_app + t_attn
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    return "unknown"
+
+
+# ---------------------------------------------------------------- main
+def main():
+    args = parse()
+    rank, world, local = dist_init(args)
+    from beam_search_shared_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    R = wl.batch * wl.beam_width
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        timer = OracleTimer(synth.make_case(wl, 1000, full_step=True, device="cpu"))
+        for _ in range(max(3, args.warmup)):
+            timer.step_seconds(1)
+        n = timer.rows_for(args.cpu_seconds / max(1, args.steps))
+        per_step, spent = [], 0.0
+        for _ in range(args.steps):
+            s, w = timer.step_seconds(n)
+            per_step.append(s)
+            spent += w
+        v = 1.0 / statistics.mean(per_step)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": 1e3 / v,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": wl.name, "batch": wl.batch, "beam_width": wl.beam_width},
+                "cpu_baseline": {"value": v, "unit": "steps/s", "cores": timer.cores, "kind": "oracle",
+                                 "sample": f"{n} of {timer.R} beam rows per step ({spent:.1f} s in total), "
+                                           f"scaled linearly; append scatter in full; {cpu_model()}"},
+                "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    from beam_search_shared_gb300 import bsp
+    from beam_search_shared_gb300.step import DeviceStep, algorithmic_bytes
+    bsp.load(build_if_missing=True)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    # ---- inputs: rotated sets, each its own workspace and plan
+    sets = []
+    for i in range(args.sets):
+        case = synth.make_case(wl, 1000 + 97 * rank + i, full_step=True, device=dev)
+        st = DeviceStep(case, device=dev)
+        st.make_plan()
+        sets.append(st)
+    torch.cuda.synchronize()
+    ab = [algorithmic_bytes(s.case) for s in sets]
+    stream = torch.cuda.current_stream()
+
+    def step(i, events=None):
+        s = sets[i % len(sets)]
+        s.append()
+        s.attend(events=events)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    for s in sets:
+        assert bsp.read_device_status(s.plan) == (0, 0)
+
+    # ---- timed region: K steps, per-kernel events on the launching stream
+    K = args.steps
+    ev_step0 = torch.cuda.Event(enable_timing=True)
+    ev_step1 = torch.cuda.Event(enable_timing=True)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev_app = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        ev_step0.record(stream)
+        for i in range(K):
+            s = sets[i % len(sets)]
+            ev_app[i].record(stream)
+            s.append()
+            s.attend(events=evs[i])
+        ev_step1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    elapsed_ms = ev_step0.elapsed_time(ev_step1)
+    elapsed_ms = reduce_max(elapsed_ms, world)
+    t_app = [ev_app[i].elapsed_time(evs[i][0]) for i in range(K)]
+    t_pre = [evs[i][0].elapsed_time(evs[i][1]) for i in range(K)]
+    t_tail = [evs[i][1].elapsed_time(evs[i][2]) for i in range(K)]
+    ms_per_step = elapsed_ms / K
+    value = world * K / (elapsed_ms / 1e3)
+
+    hbm_gbs, bf16_tflops, peak_kind = measured_peaks()
+    prefix_bytes = statistics.mean(a["prefix"] for a in ab)
+    prefix_ms = statistics.mean(t_pre)
+    achieved = prefix_bytes / (prefix_ms / 1e3) / 1e9
+    tail_gbs = statistics.mean(a["tail"] for a in ab) / (statistics.mean(t_tail) / 1e3) / 1e9
+    app_gbs = statistics.mean(a["append"] for a in ab) / (statistics.mean(t_app) / 1e3) / 1e9
+    prefix_tflops = statistics.mean(a["prefix_flops"] for a in ab) / (prefix_ms / 1e3) / 1e12
+    traffic = profiled_traffic(wl.name)
+
+    # ---- e2e: host buffers through the C ABI (plan from host arrays, H2D inputs, D2H outputs)
+    e2e = run_e2e(sets[0], args.e2e_steps, world)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.batch, "beam_width": wl.beam_width,
+                   "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                   "page_size": wl.page_size, "prompt": f"U{{{wl.prompt[0]}..{wl.prompt[1]}}}",
+                   "tail": f"U{{{wl.tail[0]}..{wl.tail[1]}}}", "parallelism": f"dp{world} (independent batches)",
+                   "beam_steps_per_s": value * R,
+                   "l2": f"inputs larger than L2: {len(sets)} rotated input sets, each step moving "
+                         f"{(prefix_bytes + statistics.mean(a['tail'] for a in ab)) / 1e6:.0f} MB",
+                   "us_append": 1e3 * statistics.mean(t_app), "us_prefix": 1e3 * prefix_ms,
+                   "us_tail_merge": 1e3 * statistics.mean(t_tail),
+                   "gbs_append": app_gbs, "gbs_tail_merge": tail_gbs, "prefix_tflops": prefix_tflops,
+                   "prefix_units": sets[0].plan.num_units},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved / hbm_gbs, "traffic": traffic,
+                     "kernel": "prefix_attn_kernel", "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": prefix_bytes},
+        "e2e": e2e,
+        "gpu_launches": K * (2 + (1 if sets[0].plan.num_units > 0 else 0)),
+        "clocks": clk.result,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        timer = OracleTimer(synth.make_case(wl, 1000, full_step=True, device="cpu"))
+        n = timer.rows_for(args.cpu_seconds)
+        s, w = timer.step_seconds(n)
+        line["cpu_baseline"] = {"value": 1.0 / s, "unit": "steps/s", "cores": timer.cores, "kind": "oracle",
+                                "sample": f"{n} of {timer.R} beam rows of one step ({w:.1f} s), scaled "
+                                          f"linearly; append scatter in full; {cpu_model()}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(st, steps, world):
+    """Steps through the public API from pinned host buffers: plan + H2D inputs + append + attention + D2H."""
+    from beam_search_shared_gb300 import bsp
+    c = st.case
+    wl = c.workload
+    pin = lambda t: t.detach().cpu().contiguous().pin_memory()
+    h_q, h_kn, h_vn = pin(c.q), pin(c.k_new.reshape(c.k_new.shape[0], -1)), pin(c.v_new.reshape(c.v_new.shape[0], -1))
+    h_loc = pin(torch.from_numpy(c.out_cache_loc))
+    h_bp = pin(torch.from_numpy(c.beam_pages))
+    h_ci = pin(torch.from_numpy(c.cache_indirection))
+    h_o = torch.empty(st.o.shape, dtype=st.o.dtype).pin_memory()
+    h_lse = torch.empty(st.lse.shape, dtype=torch.float32).pin_memory()
+    d_q, d_kn, d_vn = torch.empty_like(st.q), torch.empty_like(st.k_new), torch.empty_like(st.v_new)
+    d_loc, d_bp, d_ci = torch.empty_like(st.out_cache_loc), torch.empty_like(st.beam_pages), torch.empty_like(
+        st.cache_indirection)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_loc, h_bp, h_ci))
+    h2d += int(st.plan.image_bytes)
+    d2h = h_o.numel() * h_o.element_size() + h_lse.numel() * 4
+
+    def one():
+        plan = st.ws.plan(st.geo, wl.batch, wl.beam_width, c.prefix_len, c.tail_len, c.prefix_pages, st.max_tail)
+        for d, h in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_loc, h_loc), (d_bp, h_bp), (d_ci, h_ci)):
+            d.copy_(h, non_blocking=True)
+        bsp.append_kv(plan, d_kn, d_vn, d_loc, st.k_pool, st.v_pool)
+        bsp.decode_attn(plan, d_q, st.k_pool, st.v_pool, d_bp, d_ci, st.scale, st.o, st.lse)
+        h_o.copy_(st.o, non_blocking=True)
+        h_lse.copy_(st.lse, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = reduce_max(time.perf_counter() - t0, world)
+    st.make_plan()  # leave the set's own plan current
+    torch.cuda.synchronize()
+    return {"value": world * steps / dt, "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+if __name__ == "__main__":
+    main()

@@ -229,12 +229,15 @@ BSP_API bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, cons
  *   max_seq            innermost extent of cache_indirection, >= max(P_b + T_b)
  *   softmax_scale      > 0, typically 1/sqrt(head_dim)
  *   flags              BSP_FLAG_* bits
+ *   events             NULL, or 3 cudaEvent_t (as void*) recorded on `stream`
+ *                      before the prompt kernel, between the prompt and the
+ *                      tail kernels, and after the tail kernel (timing only)
  * The plan must be the latest one staged into its workspace.
  */
 BSP_API bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
                            const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
                            int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse,
-                           void* stream);
+                           void* const* events, void* stream);
 
 /*
  * Synchronises `stream`, then reads the workspace's device status word into
