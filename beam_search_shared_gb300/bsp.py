@@ -92,7 +92,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.bsp_plan.restype = i32
     lib.bsp_plan.argtypes = [P(Geometry), i32, i32, vp, vp, vp, i32, i32, vp, sz, vp, sz, vp, P(Plan)]
     lib.bsp_append_kv.restype = i32
-    lib.bsp_append_kv.argtypes = [P(Plan), vp, vp, i64, vp, i32, vp, vp, vp]
+    lib.bsp_append_kv.argtypes = [P(Plan), vp, vp, i64, vp, i32, vp, vp, vp, vp]
     lib.bsp_decode_attn.restype = i32
     lib.bsp_decode_attn.argtypes = [P(Plan), vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, i32, vp, vp, vp, vp]
     lib.bsp_read_device_status.restype = i32
@@ -185,15 +185,29 @@ def plan(geo: Geometry, batch, beam_width, prefix_len, tail_len, prefix_pages, m
     return out
 
 
+def _events(events, n):
+    if events is None:
+        return None
+    assert len(events) == n
+    for e in events:
+        if e.cuda_event == 0:
+            e.record()  # materialise the underlying cudaEvent_t
+    return (ctypes.c_void_p * n)(*[e.cuda_event for e in events])
+
+
 def append_kv(plan_: Plan, k_new: torch.Tensor, v_new: torch.Tensor, out_cache_loc: torch.Tensor,
-              k_pool: torch.Tensor, v_pool: torch.Tensor, src_row_stride: Optional[int] = None, stream=None):
-    """bsp_append_kv: k_new/v_new rows [n, Hkv*D] (row stride in elements), out_cache_loc int32 [n]."""
+              k_pool: torch.Tensor, v_pool: torch.Tensor, src_row_stride: Optional[int] = None, events=None,
+              stream=None):
+    """bsp_append_kv: k_new/v_new rows [n, Hkv*D] (row stride in elements), out_cache_loc int32 [n].
+
+    ``events``: optional 2 timing events recorded before and after the append kernel.
+    """
     n = int(out_cache_loc.numel())
     if src_row_stride is None:
         src_row_stride = int(k_new.stride(0)) if k_new.dim() >= 1 and n else plan_.geo.num_kv_heads * plan_.geo.head_dim
     _check("bsp_append_kv", load().bsp_append_kv(
         ctypes.byref(plan_), _dptr(k_new), _dptr(v_new), int(src_row_stride), _dptr(out_cache_loc), n,
-        _dptr(k_pool), _dptr(v_pool), _stream(stream)))
+        _dptr(k_pool), _dptr(v_pool), _events(events, 2), _stream(stream)))
 
 
 def decode_attn(plan_: Plan, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
@@ -205,12 +219,7 @@ def decode_attn(plan_: Plan, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torc
     """
     bps = int(beam_pages.shape[-1]) if beam_pages is not None else 0
     max_seq = int(cache_indirection.shape[-1]) if cache_indirection is not None else 0
-    ev = None
-    if events is not None:
-        for e in events:
-            if e.cuda_event == 0:
-                e.record()  # materialise the underlying cudaEvent_t
-        ev = (ctypes.c_void_p * 3)(*[e.cuda_event for e in events])
+    ev = _events(events, 3)
     _check("bsp_decode_attn", load().bsp_decode_attn(
         ctypes.byref(plan_), _dptr(q), _dptr(k_pool), _dptr(v_pool), _dptr(beam_pages), bps,
         _dptr(cache_indirection), max_seq, float(softmax_scale), int(flags), _dptr(o), _dptr(lse), ev,

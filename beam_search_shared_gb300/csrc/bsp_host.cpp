@@ -125,6 +125,16 @@ bool encode_map(CUtensorMap* m, int dtype, int rank, const void* base, const cuu
     return r == CUDA_SUCCESS;
 }
 
+// Records a timing event; under stream capture it becomes an external event-record node.
+bool record_event(void* const* events, int i, cudaStream_t s) {
+    if (!events) return true;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return false;
+    cudaEvent_t ev = static_cast<cudaEvent_t>(events[i]);
+    if (cs == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal) == cudaSuccess;
+    return cudaEventRecord(ev, s) == cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -376,7 +386,8 @@ bsp_status bsp_plan(const bsp_geometry* geo, int32_t batch, int32_t beam_width, 
 }
 
 bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, const void* v_new, int64_t src_row_stride,
-                         const int32_t* out_cache_loc, int32_t n, void* k_pool, void* v_pool, void* stream) {
+                         const int32_t* out_cache_loc, int32_t n, void* k_pool, void* v_pool,
+                         void* const* events, void* stream) {
     bsp_status st = check_plan(plan);
     if (st != BSP_OK) return st;
     if (n < 0) return BSP_ERR_INVALID_ARG;
@@ -401,7 +412,10 @@ bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, const void* 
     p.D = geo.head_dim;
     p.ps_log2 = ilog2(geo.page_size);
     p.num_pages = geo.num_pages;
-    return launch_append(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!record_event(events, 0, s)) return BSP_ERR_CUDA;
+    if (launch_append(p, s) != cudaSuccess) return BSP_ERR_CUDA;
+    return record_event(events, 1, s) ? BSP_OK : BSP_ERR_CUDA;
 }
 
 bsp_status bsp_read_device_status(const bsp_plan_t* plan, void* stream, int32_t clear, int32_t* flags_out) {
@@ -442,9 +456,7 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(plan->ws_device);
 
-    auto record = [&](int i) -> bool {
-        return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
-    };
+    auto record = [&](int i) -> bool { return record_event(events, i, s); };
     if (!record(0)) return BSP_ERR_CUDA;
     if (plan->num_units > 0) {
         CUtensorMap tq, tk, tv;

@@ -30,8 +30,9 @@ class DeviceStep:
         self.k_pool = case.k_pool.to(dev)
         self.v_pool = case.v_pool.to(dev)
         R = wl.batch * wl.beam_width
-        self.k_new = case.k_new.to(dev).reshape(case.k_new.shape[0], -1)
-        self.v_new = case.v_new.to(dev).reshape(case.v_new.shape[0], -1)
+        n, row = case.k_new.shape[0], wl.num_kv_heads * wl.head_dim
+        self.k_new = case.k_new.to(dev).reshape(n, row)
+        self.v_new = case.v_new.to(dev).reshape(n, row)
         self.out_cache_loc = torch.from_numpy(case.out_cache_loc).to(dev)
         self.beam_pages = torch.from_numpy(case.beam_pages).to(dev)
         self.cache_indirection = torch.from_numpy(case.cache_indirection).to(dev)
@@ -49,9 +50,9 @@ class DeviceStep:
                                  self.max_tail, stream=stream)
         return self.plan
 
-    def append(self, stream=None):
+    def append(self, events=None, stream=None):
         bsp.append_kv(self.plan, self.k_new, self.v_new, self.out_cache_loc, self.k_pool, self.v_pool,
-                      stream=stream)
+                      events=events, stream=stream)
 
     def attend(self, flags: int = 0, events=None, stream=None):
         bsp.decode_attn(self.plan, self.q, self.k_pool, self.v_pool, self.beam_pages, self.cache_indirection,

@@ -208,10 +208,14 @@ BSP_API bsp_status bsp_plan(const bsp_geometry* geo, int32_t batch, int32_t beam
  *   out_cache_loc   device int32 [n] flat slots; a slot outside
  *                   [0, num_pages * page_size) is skipped and flagged
  *   n               0 is a no-op returning BSP_OK; must be <= batch * beam_width
+ *   events          NULL, or 2 cudaEvent_t (as void*) recorded on `stream`
+ *                   before and after the append kernel (timing only; under
+ *                   stream capture they become external event-record nodes)
  * Duplicate slots are a caller error (the surviving row is unspecified).
  */
 BSP_API bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, const void* v_new, int64_t src_row_stride,
-                         const int32_t* out_cache_loc, int32_t n, void* k_pool, void* v_pool, void* stream);
+                         const int32_t* out_cache_loc, int32_t n, void* k_pool, void* v_pool,
+                         void* const* events, void* stream);
 
 /*
  * Cascade decode attention (TensorRT-LLM PR #21738, description, "Solution"):
@@ -231,7 +235,9 @@ BSP_API bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, cons
  *   flags              BSP_FLAG_* bits
  *   events             NULL, or 3 cudaEvent_t (as void*) recorded on `stream`
  *                      before the prompt kernel, between the prompt and the
- *                      tail kernels, and after the tail kernel (timing only)
+ *                      tail kernels, and after the tail kernel (timing only;
+ *                      under stream capture they become external event-record
+ *                      nodes)
  * The plan must be the latest one staged into its workspace.
  */
 BSP_API bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
