@@ -57,7 +57,8 @@ class Plan(ctypes.Structure):
 
 _lib = None
 EXPORTS = ["bsp_status_string", "bsp_bucket_rows", "bsp_workspace_size", "bsp_plan_build", "bsp_plan",
-           "bsp_append_kv", "bsp_decode_attn", "bsp_read_device_status"]
+           "bsp_append_kv", "bsp_decode_attn", "bsp_read_device_status", "bsp_decode_attn_noalloc"]
+NOALLOC_SCRATCH_MIB = 32
 
 
 def library_path() -> str:
@@ -97,6 +98,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.bsp_decode_attn.argtypes = [P(Plan), vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, i32, vp, vp, vp, vp]
     lib.bsp_read_device_status.restype = i32
     lib.bsp_read_device_status.argtypes = [P(Plan), vp, i32, P(i32)]
+    lib.bsp_decode_attn_noalloc.restype = i32
+    lib.bsp_decode_attn_noalloc.argtypes = [P(Geometry), i32, i32, vp, vp, vp, i32, i32, vp, vp, vp, vp, i32, vp, i32,
+                                            ctypes.c_float, i32, vp, vp, vp]
     _lib = lib
     return lib
 
@@ -231,3 +235,22 @@ def read_device_status(plan_: Plan, clear: bool = True, stream=None):
     flags = ctypes.c_int32(0)
     st = load().bsp_read_device_status(ctypes.byref(plan_), _stream(stream), int(bool(clear)), ctypes.byref(flags))
     return int(st), int(flags.value)
+
+
+def decode_attn_noalloc(geo: Geometry, batch, beam_width, prefix_len, tail_len, prefix_pages, max_tail,
+                        q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                        beam_pages: Optional[torch.Tensor], cache_indirection: Optional[torch.Tensor],
+                        softmax_scale: float, o: torch.Tensor, lse: torch.Tensor, flags: int = 0, stream=None):
+    """bsp_decode_attn_noalloc: plan + cascade attention with the library's fixed device scratch.
+
+    For callers that cannot allocate device memory: no workspace is passed and nothing is allocated.
+    Calls share one scratch array per GPU; calls whose GPU work overlaps race on it.
+    """
+    pl, tl = _i32(prefix_len), _i32(tail_len)
+    pp = _i32(prefix_pages).reshape(int(batch), -1) if int(batch) else np.zeros((0, 1), np.int32)
+    bps = int(beam_pages.shape[-1]) if beam_pages is not None else 0
+    max_seq = int(cache_indirection.shape[-1]) if cache_indirection is not None else 0
+    _check("bsp_decode_attn_noalloc", load().bsp_decode_attn_noalloc(
+        ctypes.byref(geo), int(batch), int(beam_width), _ptr(pl), _ptr(tl), _ptr(pp), pp.shape[1], int(max_tail),
+        _dptr(q), _dptr(k_pool), _dptr(v_pool), _dptr(beam_pages), bps, _dptr(cache_indirection), max_seq,
+        float(softmax_scale), int(flags), _dptr(o), _dptr(lse), _stream(stream)))

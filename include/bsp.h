@@ -253,6 +253,43 @@ BSP_API bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const 
  */
 BSP_API bsp_status bsp_read_device_status(const bsp_plan_t* plan, void* stream, int32_t clear, int32_t* flags_out);
 
+/* Size, in MiB, of the fixed device scratch array of bsp_decode_attn_noalloc (one per GPU). */
+#define BSP_NOALLOC_SCRATCH_MIB 32
+
+/*
+ * bsp_decode_attn_noalloc - the same cascade decode attention as
+ * bsp_decode_attn, for callers that cannot allocate device memory.
+ * (This entry point has no counterpart on the pages the method comes from.)
+ *
+ * Some callers cannot call cudaMalloc on the decode path: serving engines that
+ * give the whole GPU to their KV-cache pools at start-up and forbid later
+ * allocations, plugins whose host runtime owns every device allocation, and
+ * code that must not take the allocator's locks while it decodes. This call
+ * takes no workspace: it plans the step itself (the arguments of bsp_plan) and
+ * keeps its scratch (plan image, status word, prompt partial states) in one
+ * fixed device array of BSP_NOALLOC_SCRATCH_MIB MiB compiled into the library.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - Every GPU that loads libbsp.so holds that array until the process exits.
+ *  - The first call on a device looks up the array's device address (with that
+ *    device current); make that first call before any stream capture.
+ *  - All calls share the array, which keeps the last call's contents; the call
+ *    clears the status word itself. Calls whose GPU work overlaps (different
+ *    streams or host threads) race on the array: serialise them.
+ *  - A step whose plan image and prompt partials need more than the array is
+ *    rejected with BSP_ERR_CAPACITY before anything is enqueued.
+ * Inputs, outputs, layouts, flags (BSP_FLAG_LSE_BASE2, BSP_FLAG_CHECK) and
+ * errors are those of bsp_plan and bsp_decode_attn; the plan arrays are host
+ * memory, every other pointer device memory. The plan image is copied from
+ * host memory that is not page-locked.
+ */
+BSP_API bsp_status bsp_decode_attn_noalloc(const bsp_geometry* geo, int32_t batch, int32_t beam_width,
+                                           const int32_t* prefix_len, const int32_t* tail_len,
+                                           const int32_t* prefix_pages, int32_t prefix_pages_stride,
+                                           int32_t max_tail, const void* q, const void* k_pool,
+                                           const void* v_pool, const int32_t* beam_pages, int32_t beam_pages_stride,
+                                           const int32_t* cache_indirection, int32_t max_seq, float softmax_scale,
+                                           int32_t flags, void* o, float* lse, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
