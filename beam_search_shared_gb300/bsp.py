@@ -47,7 +47,7 @@ class Plan(ctypes.Structure):
     _fields_ = [("geo", Geometry)] + [(n, ctypes.c_int32) for n in (
         "batch", "beam_width", "max_tail", "prefix_pages_stride", "num_units", "num_parts", "row_blocks",
         "beams_per_block", "tile_keys", "max_prefix_len", "max_total_len", "num_sms", "max_tail_len",
-        "reserved_i")] + [
+        "prefix_ctas")] + [
         ("generation", ctypes.c_uint64), ("ws_device", ctypes.c_void_p), ("ws_device_bytes", ctypes.c_uint64),
         ("ws_host", ctypes.c_void_p), ("image_bytes", ctypes.c_uint64), ("off_req", ctypes.c_uint64),
         ("off_units", ctypes.c_uint64), ("off_pages", ctypes.c_uint64), ("off_part_lse", ctypes.c_uint64),

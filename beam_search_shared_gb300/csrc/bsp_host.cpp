@@ -10,6 +10,8 @@
 #include <cmath>
 #include <cstring>
 #include <limits>
+#include <queue>
+#include <utility>
 #include <thread>
 #include <vector>
 
@@ -172,7 +174,7 @@ bsp_status bsp_workspace_size(const bsp_geometry* geo, int32_t max_batch, int32_
     const int64_t parts_cap = static_cast<int64_t>(max_batch) + kExtraParts;
     const int64_t units_max = parts_cap * geo->num_kv_heads * nrb;
     const size_t image = kImageHeaderBytes + static_cast<size_t>(max_batch) * kReqFields * 4 +
-                         static_cast<size_t>(units_max) * kUnitFields * 4 +
+                         static_cast<size_t>(units_max) * (kUnitFields + 1) * 4 + 4 +
                          static_cast<size_t>(max_batch) * max_prefix_pages * 4;
     DeviceLayout L = device_layout(image, parts_cap, max_beam, *geo);
     *device_bytes = L.total;
@@ -271,16 +273,42 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
         poff += nsplit[b];
         pgoff += ceil_div(prefix_len[b], ps);
     }
-    // longest units first (row blocks of one split stay adjacent: equal keys keep their order)
+    // Longest units first (row blocks of one split stay adjacent: equal keys keep their order),
+    // then each unit goes to the persistent CTA with the least work so far. The list is
+    // written grouped by CTA; cta_off[c] .. cta_off[c+1] are CTA c's units, in the order
+    // they were dealt.
     std::stable_sort(units.begin(), units.end(), [](const Unit& a, const Unit& c) {
         return (a.f[kUnitTile1] - a.f[kUnitTile0]) > (c.f[kUnitTile1] - c.f[kUnitTile0]);
     });
     if (units.size() > static_cast<size_t>(std::numeric_limits<int32_t>::max())) return BSP_ERR_UNSUPPORTED;
+    const int64_t nu = static_cast<int64_t>(units.size());
+    const int64_t ctas = std::min<int64_t>(nu, num_sms);
+    std::vector<int32_t> cta_off(static_cast<size_t>(ctas) + 1, 0);
+    if (ctas > 0) {
+        std::vector<std::vector<int32_t>> lists(static_cast<size_t>(ctas));
+        using Load = std::pair<int64_t, int64_t>;  // (tiles so far, cta)
+        std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+        for (int64_t c = 0; c < ctas; ++c) heap.push({0, c});
+        for (int64_t i = 0; i < nu; ++i) {
+            Load ld = heap.top();
+            heap.pop();
+            lists[static_cast<size_t>(ld.second)].push_back(static_cast<int32_t>(i));
+            heap.push({ld.first + units[i].f[kUnitTile1] - units[i].f[kUnitTile0], ld.second});
+        }
+        std::vector<Unit> dealt;
+        dealt.reserve(units.size());
+        for (int64_t c = 0; c < ctas; ++c) {
+            for (int32_t i : lists[static_cast<size_t>(c)]) dealt.push_back(units[i]);
+            cta_off[static_cast<size_t>(c) + 1] = static_cast<int32_t>(dealt.size());
+        }
+        units.swap(dealt);
+    }
 
     // ---- image
     const size_t off_req = kImageHeaderBytes;
     const size_t off_units = off_req + static_cast<size_t>(batch) * kReqFields * 4;
-    const size_t off_pages = off_units + units.size() * kUnitFields * 4;
+    const size_t off_cta = off_units + units.size() * kUnitFields * 4;
+    const size_t off_pages = off_cta + cta_off.size() * 4;
     const size_t need = off_pages + static_cast<size_t>(total_pages) * 4;
     if (!image || image_bytes < need) return BSP_ERR_CAPACITY;
     uint8_t* img = static_cast<uint8_t*>(image);
@@ -298,6 +326,7 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
         r[kReqPageOff] = page_off[b];
     }
     if (!units.empty()) std::memcpy(img + off_units, units.data(), units.size() * sizeof(Unit));
+    std::memcpy(img + off_cta, cta_off.data(), cta_off.size() * 4);
     int32_t* pages = reinterpret_cast<int32_t*>(img + off_pages);
     for (int b = 0; b < batch; ++b) {
         const int64_t n = ceil_div(prefix_len[b], ps);
@@ -319,6 +348,7 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
     out->max_total_len = max_total;
     out->num_sms = num_sms;
     out->max_tail_len = max_t;
+    out->prefix_ctas = static_cast<int32_t>(ctas);
     out->image_bytes = need;
     // offsets relative to the device workspace
     DeviceLayout L = device_layout(need, parts, beam_width, *geo);
@@ -464,8 +494,8 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
         cuuint64_t qstr[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2};
         cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(plan->beams_per_block)};
         const int ps = geo.page_size;
-        cuuint64_t kdims[2] = {static_cast<cuuint64_t>(D),
-                               static_cast<cuuint64_t>(geo.num_pages) * Hkv * ps};
+        // pools viewed as 2-D [pool row][head_dim]; one box = min(page, 64) rows x 64 columns
+        cuuint64_t kdims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(geo.num_pages) * Hkv * ps};
         cuuint64_t kstr[1] = {static_cast<cuuint64_t>(D) * 2};
         cuuint32_t kbox[2] = {64, static_cast<cuuint32_t>(std::min(ps, kTileKeys))};
         if (!encode_map(&tq, geo.dtype, 3, q, qdims, qstr, qbox) || !encode_map(&tk, geo.dtype, 2, k_pool, kdims, kstr, kbox) ||
@@ -473,6 +503,7 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
             return BSP_ERR_CUDA;
         PrefixParams pp{};
         pp.units = reinterpret_cast<const int32_t*>(ws + plan->off_units);
+        pp.cta_off = pp.units + static_cast<size_t>(plan->num_units) * kUnitFields;
         pp.req = reinterpret_cast<const int32_t*>(ws + plan->off_req);
         pp.pages = reinterpret_cast<const int32_t*>(ws + plan->off_pages);
         pp.part_o = reinterpret_cast<float*>(ws + plan->off_part_o);
@@ -485,8 +516,9 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
         pp.ps_log2 = ilog2(ps);
         pp.Wblk = plan->beams_per_block;
         pp.num_pages = geo.num_pages;
+        pp.num_units = plan->num_units;
         pp.scale_log2 = softmax_scale * log2e;
-        if (launch_prefix(D, bf16, plan->num_units, tq, tk, tv, pp, s) != cudaSuccess) return BSP_ERR_CUDA;
+        if (launch_prefix(D, bf16, plan->prefix_ctas, tq, tk, tv, pp, s) != cudaSuccess) return BSP_ERR_CUDA;
     }
     if (!record(1)) return BSP_ERR_CUDA;
     TailParams tp{};
@@ -512,7 +544,7 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
     tp.max_seq = max_seq;
     tp.scale_log2 = softmax_scale * log2e;
     tp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
-    if (launch_tail(D, bf16, tp, s) != cudaSuccess) return BSP_ERR_CUDA;
+    if (launch_tail(D, bf16, plan->max_tail_len, tp, s) != cudaSuccess) return BSP_ERR_CUDA;
     if (!record(2)) return BSP_ERR_CUDA;
     if (flags & BSP_FLAG_CHECK) return bsp_read_device_status(plan, stream, 1, nullptr);
     return BSP_OK;

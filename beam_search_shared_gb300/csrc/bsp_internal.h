@@ -26,13 +26,15 @@ enum UnitField { kUnitReq = 0, kUnitKvHead = 1, kUnitRowBlock = 2, kUnitTile0 = 
                  kUnitFields = 8 };
 
 struct PrefixParams {
-    const int32_t* units;
+    const int32_t* units;    // [num_units][kUnitFields], grouped by CTA
+    const int32_t* cta_off;  // [gridDim.x + 1]: CTA c runs units cta_off[c] .. cta_off[c+1]-1
     const int32_t* req;
     const int32_t* pages;
     float* part_o;    // [part][W][Hq][D]   (normalised partial output)
     float* part_lse;  // [part][W][Hq]      (log2-sum-exp2 of the scaled scores)
     int32_t* status;
     int W, Hq, Hkv, G, ps_log2, Wblk, num_pages;
+    int num_units;     // units in the list
     float scale_log2;  // softmax_scale * log2(e)
 };
 
@@ -64,9 +66,9 @@ struct AppendParams {
     int n, Hkv, D, ps_log2, num_pages;
 };
 
-cudaError_t launch_prefix(int head_dim, bool bf16, int num_units, const CUtensorMap& tq, const CUtensorMap& tk,
+cudaError_t launch_prefix(int head_dim, bool bf16, int ctas, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const PrefixParams& p, cudaStream_t stream);
-cudaError_t launch_tail(int head_dim, bool bf16, const TailParams& p, cudaStream_t stream);
+cudaError_t launch_tail(int head_dim, bool bf16, int max_tail_len, const TailParams& p, cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 
 }  // namespace bsp

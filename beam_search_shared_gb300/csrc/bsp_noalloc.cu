@@ -158,6 +158,7 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
             return BSP_ERR_CUDA;
         PrefixParams pp{};
         pp.units = reinterpret_cast<const int32_t*>(ws + plan.off_units);
+        pp.cta_off = pp.units + static_cast<size_t>(plan.num_units) * kUnitFields;
         pp.req = reinterpret_cast<const int32_t*>(ws + plan.off_req);
         pp.pages = reinterpret_cast<const int32_t*>(ws + plan.off_pages);
         pp.part_o = reinterpret_cast<float*>(ws + plan.off_part_o);
@@ -170,8 +171,9 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
         pp.ps_log2 = noalloc_log2(ps);
         pp.Wblk = plan.beams_per_block;
         pp.num_pages = geo->num_pages;
+        pp.num_units = plan.num_units;
         pp.scale_log2 = softmax_scale * log2e;
-        if (launch_prefix(D, bf16, plan.num_units, tq, tk, tv, pp, s) != cudaSuccess) return BSP_ERR_CUDA;
+        if (launch_prefix(D, bf16, plan.prefix_ctas, tq, tk, tv, pp, s) != cudaSuccess) return BSP_ERR_CUDA;
     }
     TailParams tp{};
     tp.q = q;
@@ -196,7 +198,7 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
     tp.max_seq = max_seq;
     tp.scale_log2 = softmax_scale * log2e;
     tp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
-    if (launch_tail(D, bf16, tp, s) != cudaSuccess) return BSP_ERR_CUDA;
+    if (launch_tail(D, bf16, plan.max_tail_len, tp, s) != cudaSuccess) return BSP_ERR_CUDA;
     if (flags & BSP_FLAG_CHECK) {
         int32_t dflags = 0;
         if (cudaStreamSynchronize(s) != cudaSuccess) return BSP_ERR_CUDA;

@@ -4,25 +4,39 @@
 // request"; all beam_width x GQA-group query rows of a request share one K/V
 // stream, which makes Q*K^T and P*V dense contractions).
 //
-// One CTA = one work unit: (request b, kv head g, query-row block, range of
-// 64-key tiles). Query rows of the block are (beam w, head j) pairs, row
-// = w_local * G + j, at most 128 (the MMA M). Only the valid prompt rows
-// [0, P_b) are read (TensorRT-Model-Connect PR #2202, "prefill and decode
-// over the cached prefix, not the whole KV allocation").
+// Work unit = (request b, kv head g, query-row block, range of 64-key tiles).
+// Query rows of a block are (beam w, head j) pairs, row = w_local * G + j, at
+// most 128 (the MMA M). Only the valid prompt rows [0, P_b) are read
+// (TensorRT-Model-Connect PR #2202, "prefill and decode over the cached prefix,
+// not the whole KV allocation").
+//
+// Persistent: one CTA per SM walks its own list of units (the host deals the
+// units longest first to the least-loaded CTA). Every ring is
+// indexed by a tile counter that runs across units, so the producer prefetches
+// the next unit's Q and K/V while the current one is still being reduced, and
+// the MMA warp issues the next unit's first Q*K^T while the softmax warps write
+// the previous unit's partial output.
 //
 // Warp roles (192 threads):
-//   warp 0     TMA producer: Q once, then K and V tiles of the unit's pages
-//              (beam 0's prompt pages) into a STAGES-deep ring;
-//   warp 1     TMEM allocation and the MMA issuer (one thread):
-//              S[i%2] = Q K_i^T, then O += P_{i-1} V_{i-1};
-//   warps 2-5  softmax: thread <-> query row <-> TMEM lane; reads S from
-//              TMEM, online softmax in base 2 with a lazy rescale of O (only
-//              when the row maximum grows by more than 2^8), writes P (16-bit,
-//              swizzled K-major) to shared memory, epilogue writes the
-//              normalised partial O and its log2-sum-exp2 (fp32) to the
-//              workspace for the tail kernel's merge.
+//   warp 0     TMA producer: Q of each unit into one of NQ buffers (3-D box
+//              [W_blk][G][64]), K and V of the unit's pages (beam 0's prompt
+//              pages) into a KST-deep K ring and a VST-deep V ring, one 2-D box
+//              of min(page, 64) rows x 64 columns per page, column half and
+//              tensor, each lane issuing its own boxes; a tile's column half c
+//              of K (or V) is a 128-byte-swizzled region of 64 rows; page ids
+//              come from a 32-entry window held one per lane. A K slot is
+//              released as soon as Q*K^T has read it, a V slot after P*V, so
+//              the short-lived K slots need fewer stages than the V slots;
+//   warp 1     TMEM allocation; one thread issues tcgen05.mma:
+//              S[t%2] = Q K_t^T, then O (+)= P_{t-1} V_{t-1};
+//   warps 2-5  softmax: thread <-> query row <-> TMEM lane; reads S from TMEM,
+//              masks keys >= P_b, online softmax in base 2 with a lazy rescale
+//              of O (only when a row maximum grows by more than 2^8), writes P
+//              (16-bit, swizzled K-major) to shared memory, zeroes V rows past
+//              the valid keys of the last tile, and at the end of each unit
+//              writes the normalised fp32 partial O and its log2-sum-exp2.
 // TMEM columns: S0 [0,64), S1 [64,128), O [128, 128+D).
-// Every wait is bounded (2 s per CTA); on expiry the CTA flags
+// Every wait is bounded (1 s without progress); on expiry the CTA flags
 // BSP_DEVFLAG_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -38,34 +52,68 @@ namespace bsp {
 template <int D>
 struct PrefixCfg {
     static constexpr int TK = kTileKeys;
-    static constexpr int NC = D / 64;                       // 128-byte column regions per row
-    static constexpr int STAGES = D == 64 ? 6 : (D == 128 ? 4 : 2);
-    static constexpr int Q_BYTES = kRowsPerBlock * D * 2;   // NC regions of 128 rows x 128 B
-    static constexpr int P_BYTES = kRowsPerBlock * TK * 2;  // one region
-    static constexpr int KV_BYTES = TK * D * 2;             // one of K or V per stage
-    static constexpr int STAGE_BYTES = 2 * KV_BYTES;
-    static constexpr int OFF_P = Q_BYTES;
-    static constexpr int OFF_STAGE = Q_BYTES + P_BYTES;
-    static constexpr int OFF_BAR = OFF_STAGE + STAGES * STAGE_BYTES;
-    static constexpr int SMEM = OFF_BAR + 256 + 1024;       // barriers + alignment slack
-    static constexpr int S_COL = 0;
-    static constexpr int O_COL = 2 * TK;
-    static constexpr uint32_t TMEM_COLS = (O_COL + D) <= 256 ? 256u : 512u;
+    static constexpr int NC = D / 64;                        // 128-byte column regions per row
+    static constexpr int NQ = D == 256 ? 1 : 2;              // Q buffers
+    static constexpr int KST = D == 64 ? 8 : (D == 128 ? 4 : 2);   // K ring depth
+    static constexpr int VST = D == 64 ? 8 : (D == 128 ? 6 : 3);   // V ring depth
+    static constexpr int Q_BYTES = kRowsPerBlock * D * 2;    // NC regions of 128 rows x 128 B
+    static constexpr int KV_BYTES = TK * D * 2;              // one K (or V) tile
+    static constexpr int OFF_K = NQ * Q_BYTES;
+    static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
+    static constexpr int OFF_BAR = OFF_V + VST * KV_BYTES;
+    static constexpr int SMEM = OFF_BAR + 512 + 1024;        // barriers + alignment slack
+    // Q is the A operand of Q*K^T from tensor memory when it fits next to S, O and P
+    // (head_dim <= 128); P always is the A operand of P*V from tensor memory.
+    static constexpr bool Q_IN_TMEM = D <= 128;
+    static constexpr int S_COL = 0;                          // S[0], S[1]: TK fp32 columns each
+    static constexpr int O_COL = 2 * TK;                     // O: D fp32 columns
+    static constexpr int QT_COL = O_COL + D;                 // Q[0], Q[1]: D/2 columns each (2 x 16-bit)
+    static constexpr int PT_COL = QT_COL + (Q_IN_TMEM ? D : 0);  // P[0], P[1]: TK/2 columns each
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(PT_COL + TK <= 512, "tensor memory");
     static constexpr int THREADS = 192;
 };
 
 struct PrefixBarriers {
-    uint64_t kv_full[8];
-    uint64_t kv_empty[8];
-    uint64_t q_full;
+    uint64_t k_full[8];
+    uint64_t k_empty[8];  // KST <= 8
+    uint64_t v_full[8];
+    uint64_t v_empty[8];  // VST <= 8
+    uint64_t q_full[2];   // Q of a unit landed in shared memory
+    uint64_t q_empty[2];  // that shared-memory Q buffer may be reloaded
+    uint64_t qt_full[2];  // Q of unit k copied into tensor-memory buffer k % 2
     uint64_t s_full[2];
     uint64_t s_free[2];
-    uint64_t p_full;
-    uint64_t o_done;
+    uint64_t p_full[2];  // tile t arrives on p_full[t % 2]
+    uint64_t o_done[2];  // P*V of tile t completes o_done[t % 2]
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
 };
+
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s without progress
+constexpr uint64_t kDrainNs = 200000000ull;
+
+struct UnitInfo {
+    int b, g, rb, kt0, kt1, part, P, page_off;
+};
+
+__device__ __forceinline__ UnitInfo load_unit(const PrefixParams& p, int u) {
+    const int4 a = __ldg(reinterpret_cast<const int4*>(p.units + static_cast<long long>(u) * kUnitFields));
+    const int4 c = __ldg(reinterpret_cast<const int4*>(p.units + static_cast<long long>(u) * kUnitFields + 4));
+    const int4 r = __ldg(reinterpret_cast<const int4*>(p.req + a.x * kReqFields));
+    const int4 r2 = __ldg(reinterpret_cast<const int4*>(p.req + a.x * kReqFields + 4));
+    UnitInfo ui;
+    ui.b = a.x;
+    ui.g = a.y;
+    ui.rb = a.z;
+    ui.kt0 = a.w;
+    ui.kt1 = c.x;
+    ui.part = c.y;
+    ui.P = r.x;
+    ui.page_off = r2.x;
+    return ui;
+}
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -83,47 +131,46 @@ __global__ void __launch_bounds__(192, 1)
 prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefixParams p) {
     using C = PrefixCfg<D>;
-    constexpr int TK = C::TK, NC = C::NC, STAGES = C::STAGES;
+    constexpr int TK = C::TK, NC = C::NC, NQ = C::NQ, KST = C::KST, VST = C::VST;
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem;
-    uint8_t* sP = smem + C::OFF_P;
+    // shared-memory P tile of global tile gt
+    auto k_tile = [&](int gt) -> uint8_t* { return smem + C::OFF_K + (gt % KST) * C::KV_BYTES; };
+    auto v_tile = [&](int gt) -> uint8_t* { return smem + C::OFF_V + (gt % VST) * C::KV_BYTES; };
     PrefixBarriers* bars = reinterpret_cast<PrefixBarriers*>(smem + C::OFF_BAR);
     volatile int* abort_flag = &bars->abort_flag;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const uint64_t deadline = globaltimer_ns() + 2000000000ull;
-
-    // ---- unit
-    const int* u = p.units + static_cast<long long>(blockIdx.x) * kUnitFields;
-    const int b = __ldg(u + kUnitReq), g = __ldg(u + kUnitKvHead), rb = __ldg(u + kUnitRowBlock);
-    const int kt0 = __ldg(u + kUnitTile0), kt1 = __ldg(u + kUnitTile1), part = __ldg(u + kUnitPart);
-    const int* rq = p.req + b * kReqFields;
-    const int P = __ldg(rq + kReqPrefix);
-    const int page_off = __ldg(rq + kReqPageOff);
-    const int key_begin = kt0 * TK;
-    const int key_end = min(kt1 * TK, P);
-    const int ntiles = kt1 - kt0;
-    const int w0 = rb * p.Wblk;
-    const int nbeams = min(p.Wblk, p.W - w0);
-    const int M = nbeams * p.G;
+    const int u_begin = __ldg(p.cta_off + blockIdx.x);
+    const int u_end = __ldg(p.cta_off + blockIdx.x + 1);
+    const int ps = 1 << p.ps_log2;
 
     // ---- setup
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&bars->kv_full[s], 1);
-            mbar_init(&bars->kv_empty[s], 1);
+        for (int s = 0; s < KST; ++s) {
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->k_empty[s], 1);
         }
-        mbar_init(&bars->q_full, 1);
+        for (int s = 0; s < VST; ++s) {
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->v_empty[s], 1);
+        }
+        for (int i = 0; i < NQ; ++i) {
+            mbar_init(&bars->q_full[i], 1);
+            // released by the softmax warps once they copied it to tensor memory, else by the
+            // MMA thread after the unit's last Q*K^T
+            mbar_init(&bars->q_empty[i], C::Q_IN_TMEM ? 4 : 1);
+        }
         for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->qt_full[i], 4);  // one arrival per softmax warp
             mbar_init(&bars->s_full[i], 1);
             mbar_init(&bars->s_free[i], 128);
         }
-        mbar_init(&bars->p_full, 128);
-        mbar_init(&bars->o_done, 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&bars->p_full[i], 4);  // one arrival per softmax warp
+        for (int i = 0; i < 2; ++i) mbar_init(&bars->o_done[i], 1);
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -132,13 +179,15 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         prefetch_tmap(&tm_v);
     }
     if (warp == 1) tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
-    // zero the query rows the TMA box does not cover, so padded rows stay finite
+    // zero the query rows no TMA box covers, so padded rows stay finite
     {
         const int filled = p.Wblk * p.G;
         const int nz = (kRowsPerBlock - filled) * 8;  // 16-byte chunks per region
-        for (int c = 0; c < NC; ++c)
-            for (int idx = tid; idx < nz; idx += C::THREADS)
-                reinterpret_cast<uint4*>(sQ + c * kRowsPerBlock * 128 + filled * 128)[idx] = make_uint4(0, 0, 0, 0);
+        for (int qb = 0; qb < NQ; ++qb)
+            for (int c = 0; c < NC; ++c)
+                for (int idx = tid; idx < nz; idx += C::THREADS)
+                    reinterpret_cast<uint4*>(smem + qb * C::Q_BYTES + c * kRowsPerBlock * 128 + filled * 128)[idx] =
+                        make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -148,53 +197,76 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
     if (warp == 0) {
         // ================= TMA producer =================
-        const int* pg = p.pages + page_off;
-        const int npages = (P + (1 << p.ps_log2) - 1) >> p.ps_log2;
-        const int ps = 1 << p.ps_log2;
-        const int BR = ps < TK ? ps : TK;  // rows per box
-        int win_base = -1, my_page = 0;
-        int issued = 0;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&bars->q_full, NC * p.Wblk * p.G * 128);
-            for (int c = 0; c < NC; ++c)
-                tma_load_3d(sQ + c * kRowsPerBlock * 128, &tm_q, &bars->q_full, c * 64, g * p.G, b * p.W + w0);
-        }
+        const int BR = ps < TK ? ps : TK;  // rows per box (a page, or 64 rows of a larger page)
+        int gt = 0, k = 0;
         bool ok = true;
-        for (int i = 0; i < ntiles && ok; ++i) {
-            const int s = i % STAGES;
-            if (i >= STAGES) {
-                ok = mbar_wait(&bars->kv_empty[s], ((i / STAGES) - 1) & 1, abort_flag, deadline);
+        for (int u = u_begin; u < u_end && ok; ++u, ++k) {
+            const UnitInfo ui = load_unit(p, u);
+            const int qb = k % NQ;
+            if (k >= NQ) {
+                ok = mbar_wait(&bars->q_empty[qb], ((k / NQ) - 1) & 1, abort_flag, kWaitTimeoutNs);
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
             }
-            const int key0 = key_begin + i * TK;
-            const int valid = min(TK, key_end - key0);
-            const int nchunks = (valid + BR - 1) / BR;
-            uint8_t* sK = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
-            uint8_t* sV = sK + C::KV_BYTES;
-            if (lane == 0) mbar_arrive_expect_tx(&bars->kv_full[s], nchunks * BR * 128 * NC * 2);
-            for (int ch = 0; ch < nchunks; ++ch) {
-                const int key = key0 + ch * BR;
-                const int pidx = key >> p.ps_log2;
-                if (win_base < 0 || pidx >= win_base + 32) {  // warp-uniform
-                    win_base = pidx;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars->q_full[qb], NC * p.Wblk * p.G * 128);
+                for (int c = 0; c < NC; ++c)
+                    tma_load_3d(smem + qb * C::Q_BYTES + c * kRowsPerBlock * 128, &tm_q, &bars->q_full[qb], c * 64,
+                                ui.g * p.G, ui.b * p.W + ui.rb * p.Wblk);
+            }
+            const int key_begin = ui.kt0 * TK;
+            const int key_end = min(ui.kt1 * TK, ui.P);
+            const int ntiles = ui.kt1 - ui.kt0;
+            const int* pg = p.pages + ui.page_off;
+            const int npages = (ui.P + ps - 1) >> p.ps_log2;
+            int win_base = -1, my_page = 0;
+            for (int t = 0; t < ntiles; ++t, ++gt) {
+                if (gt >= KST) {
+                    ok = mbar_wait(&bars->k_empty[gt % KST], ((gt / KST) - 1) & 1, abort_flag, kWaitTimeoutNs);
+                    ok = __all_sync(FULL, ok);
+                    if (!ok) break;
+                }
+                const int key0 = key_begin + t * TK;
+                const int valid = min(TK, key_end - key0);
+                const int nchunks = (valid + BR - 1) / BR;  // pages (or 64-row slices) with valid keys
+                const int tile_bytes = nchunks * BR * D * 2;
+                const int pidx0 = key0 >> p.ps_log2;
+                const int pidx_last = (key0 + (nchunks - 1) * BR) >> p.ps_log2;
+                if (win_base < 0 || pidx_last >= win_base + 32) {  // warp-uniform
+                    win_base = pidx0;
                     my_page = (win_base + lane < npages) ? __ldg(pg + win_base + lane) : 0;
                 }
-                int page = __shfl_sync(FULL, my_page, pidx - win_base);
-                if (static_cast<unsigned>(page) >= static_cast<unsigned>(p.num_pages)) {
-                    if (lane == 0) atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
-                    page = 0;
-                }
-                const int row = ((page * p.Hkv + g) << p.ps_log2) + (key & (ps - 1));
-                if (lane == 0) {
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) {
-                        tma_load_2d(sK + c * TK * 128 + ch * BR * 128, &tm_k, &bars->kv_full[s], c * 64, row);
-                        tma_load_2d(sV + c * TK * 128 + ch * BR * 128, &tm_v, &bars->kv_full[s], c * 64, row);
+                // box b of a tensor: column half b % NC of chunk b / NC
+                const int nbox = nchunks * NC;
+                for (int tensor = 0; tensor < 2; ++tensor) {
+                    if (tensor == 1 && gt >= VST) {
+                        ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kWaitTimeoutNs);
+                        ok = __all_sync(FULL, ok);
+                        if (!ok) break;
+                    }
+                    uint64_t* full = tensor ? &bars->v_full[gt % VST] : &bars->k_full[gt % KST];
+                    uint8_t* base = tensor ? v_tile(gt) : k_tile(gt);
+                    const void* map = tensor ? static_cast<const void*>(&tm_v) : static_cast<const void*>(&tm_k);
+                    if (lane == 0) mbar_arrive_expect_tx(full, tile_bytes);
+                    for (int b0 = 0; b0 < nbox; b0 += 32) {
+                        const int bx = b0 + lane;
+                        const int ch = min(bx / NC, nchunks - 1);
+                        const int key = key0 + ch * BR;
+                        int page = __shfl_sync(FULL, my_page, (key >> p.ps_log2) - win_base);
+                        if (bx < nbox) {
+                            if (static_cast<unsigned>(page) >= static_cast<unsigned>(p.num_pages)) {
+                                atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
+                                page = 0;
+                            }
+                            const int c = bx % NC;
+                            const int row = ((page * p.Hkv + ui.g) << p.ps_log2) + (key & (ps - 1));
+                            tma_load_2d(base + c * TK * 128 + ch * BR * 128, map, full, c * 64, row);
+                        }
                     }
                 }
+                if (!ok) break;
+                __syncwarp();
             }
-            issued = i + 1;
         }
         if (!ok) {
             if (lane == 0) {
@@ -202,66 +274,90 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
             }
             // drain: let this CTA's own copies land before the CTA exits
-            const uint64_t dl = globaltimer_ns() + 200000000ull;
-            for (int j = max(0, issued - STAGES); j < issued; ++j)
-                while (!mbar_try_wait(&bars->kv_full[j % STAGES], (j / STAGES) & 1) && globaltimer_ns() < dl) {
+            const uint64_t t0 = globaltimer_ns();
+            for (int j = max(0, gt - KST); j <= gt; ++j)
+                while (!mbar_try_wait(&bars->k_full[j % KST], (j / KST) & 1) && globaltimer_ns() - t0 < kDrainNs) {
                 }
-            if (lane == 0) {
-                while (!mbar_try_wait(&bars->q_full, 0) && globaltimer_ns() < dl) {
+            for (int j = max(0, gt - VST); j <= gt; ++j)
+                while (!mbar_try_wait(&bars->v_full[j % VST], (j / VST) & 1) && globaltimer_ns() - t0 < kDrainNs) {
                 }
-            }
+            for (int j = max(0, k - NQ); j <= k; ++j)
+                while (!mbar_try_wait(&bars->q_full[j % NQ], (j / NQ) & 1) && globaltimer_ns() - t0 < kDrainNs) {
+                }
         }
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
             constexpr uint32_t ID_QK = idesc_f16(128, TK, BF16, false);
             constexpr uint32_t ID_PV = idesc_f16(128, D, BF16, true);
-            const uint32_t q_addr = smem_u32(sQ);
-            const uint32_t p_addr = smem_u32(sP);
-            bool ok = mbar_wait(&bars->q_full, 0, abort_flag, deadline);
-            int pv_issued = 0;
-            auto issue_pv = [&](int j) -> bool {
-                if (!mbar_wait(&bars->p_full, j & 1, abort_flag, deadline)) return false;
+            int gt = 0, k = 0;
+            int pend = -1;           // tile whose P*V is not issued yet
+            bool pend_first = false;  // ... and it opens its unit (overwrite O)
+            bool ok = true;
+            auto issue_pv = [&](int j, bool first) -> bool {
+                if (!mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, abort_flag, kWaitTimeoutNs)) return false;
+                if (!mbar_wait(&bars->v_full[j % VST], (j / VST) & 1, abort_flag, kWaitTimeoutNs)) return false;
                 tc_fence_after();
-                const int sj = j % STAGES;
-                const uint32_t v_addr = smem_u32(smem + C::OFF_STAGE + sj * C::STAGE_BYTES + C::KV_BYTES);
+                const uint32_t p_tmem = tmem + C::PT_COL + (j & 1) * (TK / 2);
+                const uint32_t v_addr = smem_u32(v_tile(j));
 #pragma unroll
                 for (int kk = 0; kk < TK / 16; ++kk) {
-                    const uint64_t a = sdesc_sw128(p_addr + kk * 32, 16, 1024);
                     const uint64_t bd = sdesc_sw128(v_addr + kk * 16 * 128, TK * 128, 1024);
-                    mma_f16(tmem + C::O_COL, a, bd, ID_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_f16_tmem_a(tmem + C::O_COL, p_tmem + kk * 8, bd, ID_PV, (!first || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(&bars->o_done);
-                mma_commit(&bars->kv_empty[sj]);
-                pv_issued = j + 1;
+                mma_commit(&bars->o_done[j & 1]);
+                mma_commit(&bars->v_empty[j % VST]);
                 return true;
             };
-            for (int i = 0; i < ntiles && ok; ++i) {
-                const int s = i % STAGES;
-                ok = mbar_wait(&bars->kv_full[s], (i / STAGES) & 1, abort_flag, deadline);
-                if (ok && i >= 2) ok = mbar_wait(&bars->s_free[i & 1], ((i - 2) >> 1) & 1, abort_flag, deadline);
+            for (int u = u_begin; u < u_end && ok; ++u, ++k) {
+                const int4 a = __ldg(reinterpret_cast<const int4*>(p.units + static_cast<long long>(u) * kUnitFields));
+                const int kt1 = __ldg(p.units + static_cast<long long>(u) * kUnitFields + kUnitTile1);
+                const int ntiles = kt1 - a.w;
+                const int qb = k % NQ;
+                if constexpr (C::Q_IN_TMEM)
+                    ok = mbar_wait(&bars->qt_full[k & 1], (k >> 1) & 1, abort_flag, kWaitTimeoutNs);
+                else
+                    ok = mbar_wait(&bars->q_full[qb], (k / NQ) & 1, abort_flag, kWaitTimeoutNs);
                 if (!ok) break;
-                tc_fence_after();
-                const uint32_t k_addr = smem_u32(smem + C::OFF_STAGE + s * C::STAGE_BYTES);
+                const uint32_t q_addr = smem_u32(smem + qb * C::Q_BYTES);
+                const uint32_t q_tmem = tmem + C::QT_COL + (k & 1) * (D / 2);
+                for (int t = 0; t < ntiles; ++t, ++gt) {
+                    ok = mbar_wait(&bars->k_full[gt % KST], (gt / KST) & 1, abort_flag, kWaitTimeoutNs);
+                    if (ok && gt >= 2) ok = mbar_wait(&bars->s_free[gt & 1], ((gt - 2) >> 1) & 1, abort_flag, kWaitTimeoutNs);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t k_addr = smem_u32(k_tile(gt));
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = sdesc_sw128(q_addr + (kk >> 2) * (kRowsPerBlock * 128) + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(k_addr + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
-                    mma_f16(tmem + C::S_COL + (i & 1) * TK, a, bd, ID_QK, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t bd = sdesc_sw128(k_addr + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
+                        if constexpr (C::Q_IN_TMEM) {
+                            mma_f16_tmem_a(tmem + C::S_COL + (gt & 1) * TK, q_tmem + kk * 8, bd, ID_QK, kk > 0 ? 1u : 0u);
+                        } else {
+                            const uint64_t ad =
+                                sdesc_sw128(q_addr + (kk >> 2) * (kRowsPerBlock * 128) + (kk & 3) * 32, 16, 1024);
+                            mma_f16(tmem + C::S_COL + (gt & 1) * TK, ad, bd, ID_QK, kk > 0 ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(&bars->s_full[gt & 1]);
+                    mma_commit(&bars->k_empty[gt % KST]);  // K of this tile has been read
+                    if (!C::Q_IN_TMEM && t == ntiles - 1) mma_commit(&bars->q_empty[qb]);  // Q no longer read
+                    if (pend >= 0) {
+                        ok = issue_pv(pend, pend_first);
+                        if (!ok) break;
+                    }
+                    pend = gt;
+                    pend_first = t == 0;
                 }
-                mma_commit(&bars->s_full[i & 1]);
-                if (i >= 1) ok = issue_pv(i - 1);
             }
-            if (ok && ntiles > 0) ok = issue_pv(ntiles - 1);
+            if (ok && pend >= 0) ok = issue_pv(pend, pend_first);
             if (!ok) {
                 *abort_flag = 1;
                 atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
             }
-            (void)pv_issued;
             // drain: every MMA issued by this thread completes before TMEM is freed
             mma_commit(&bars->drain);
-            const uint64_t dl = globaltimer_ns() + 200000000ull;
-            while (!mbar_try_wait(&bars->drain, 0) && globaltimer_ns() < dl) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&bars->drain, 0) && globaltimer_ns() - t0 < kDrainNs) {
             }
         }
     } else {
@@ -270,42 +366,116 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const float sl2 = p.scale_log2;
-        float m = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int i = 0; i < ntiles; ++i) {
-            const int key0 = key_begin + i * TK;
-            const int valid = min(TK, key_end - key0);
-            ok = mbar_wait(&bars->s_full[i & 1], (i >> 1) & 1, abort_flag, deadline);
-            ok = __all_sync(FULL, ok);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t sr[2][32];
-            tmem_ld32(lane_base + C::S_COL + (i & 1) * TK, sr[0]);
-            tmem_ld32(lane_base + C::S_COL + (i & 1) * TK + 32, sr[1]);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&bars->s_free[i & 1]);
-            float sv[TK];
-            float mx = -INFINITY;
+        int gt = 0;
+        // Copies Q of the k-th unit of this CTA from its shared-memory buffer (128-byte swizzle)
+        // into tensor-memory buffer k % 2, then releases the shared-memory buffer.
+        auto copy_q = [&](int k) -> bool {
+            if constexpr (C::Q_IN_TMEM) {
+                const int qb = k % NQ;
+                if (!__all_sync(FULL, mbar_wait(&bars->q_full[qb], (k / NQ) & 1, abort_flag, kWaitTimeoutNs)))
+                    return false;
+                const uint8_t* qrow = smem + qb * C::Q_BYTES + row * 128;
 #pragma unroll
-            for (int c = 0; c < TK; ++c) {
-                const float v = (c < valid) ? __uint_as_float(sr[c >> 5][c & 31]) * sl2 : -INFINITY;
-                sv[c] = v;
-                mx = fmaxf(mx, v);
+                for (int c0 = 0; c0 < D / 2; c0 += 32) {  // 32 columns = 64 elements = one region
+                    uint32_t qr[32];
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(qrow + (c0 / 32) * (kRowsPerBlock * 128) +
+                                                                        ((cc ^ (row & 7)) << 4));
+                        qr[4 * cc] = v.x;
+                        qr[4 * cc + 1] = v.y;
+                        qr[4 * cc + 2] = v.z;
+                        qr[4 * cc + 3] = v.w;
+                    }
+                    tmem_st32(lane_base + C::QT_COL + (k & 1) * (D / 2) + c0, qr);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars->qt_full[k & 1]);
+                    mbar_arrive(&bars->q_empty[qb]);
+                }
             }
-            if (i > 0) {
-                // P_{i-1} V_{i-1} has finished: O may be rescaled and the P buffer reused
-                ok = mbar_wait(&bars->o_done, (i - 1) & 1, abort_flag, deadline);
+            return true;
+        };
+        UnitInfo cur;
+        if (u_begin < u_end) {
+            cur = load_unit(p, u_begin);
+            ok = copy_q(0);
+        }
+        for (int u = u_begin; u < u_end && ok; ++u) {
+            UnitInfo nxt = cur;
+            if (u + 1 < u_end) nxt = load_unit(p, u + 1);  // prefetch
+            const int key_begin = cur.kt0 * TK;
+            const int key_end = min(cur.kt1 * TK, cur.P);
+            const int ntiles = cur.kt1 - cur.kt0;
+            const int w0 = cur.rb * p.Wblk;
+            const int M = min(p.Wblk, p.W - w0) * p.G;
+            // a warp whose 32 rows are all padding skips the arithmetic but keeps the
+            // barrier protocol (the p_full ordering below keeps its arrivals in the right phase)
+            const bool warp_live = quad * 32 < M;
+            float m = -INFINITY, l = 0.f;
+            for (int t = 0; t < ntiles; ++t, ++gt) {
+                const int valid = min(TK, key_end - (key_begin + t * TK));
+                ok = mbar_wait(&bars->s_full[gt & 1], (gt >> 1) & 1, abort_flag, kWaitTimeoutNs);
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
                 tc_fence_after();
-                const bool need = mx > m + 8.0f;
-                if (__any_sync(FULL, need)) {
-                    const float alpha = need ? exp2f(m - mx) : 1.0f;
-                    if (need) {
+                uint32_t sr[2][32];
+                if (warp_live) {
+                    tmem_ld32(lane_base + C::S_COL + (gt & 1) * TK, sr[0]);
+                    tmem_ld32(lane_base + C::S_COL + (gt & 1) * TK + 32, sr[1]);
+                    tmem_wait_ld();
+                }
+                tc_fence_before();
+                mbar_arrive(&bars->s_free[gt & 1]);
+                float alpha = 1.0f;
+                bool rescale = false;
+                uint32_t pk[TK / 2];
+                if (warp_live) {
+                    float sv[TK];
+                    float mp[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) mp[j] = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < TK; ++c) {
+                        const float v = (c < valid) ? __uint_as_float(sr[c >> 5][c & 31]) * sl2 : -INFINITY;
+                        sv[c] = v;
+                        mp[c & 7] = fmaxf(mp[c & 7], v);
+                    }
+                    const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                           fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+                    // lazy maximum: keep the old one unless the row maximum grew by more than 2^8
+                    const bool need = t > 0 && mx > m + 8.0f;
+                    rescale = __any_sync(FULL, need);
+                    if (t == 0) {
+                        m = mx;
+                    } else if (need) {
+                        alpha = exp2f(m - mx);
                         m = mx;
                         l *= alpha;
                     }
+                    // probabilities and row sum, before waiting for the previous P*V
+                    float rsp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int c = 0; c < TK; c += 2) {
+                        const float p0 = exp2f(sv[c] - m);
+                        const float p1 = exp2f(sv[c + 1] - m);
+                        rsp[(c >> 1) & 3] += p0 + p1;
+                        pk[c >> 1] = pack2<BF16>(p0, p1);
+                    }
+                    l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
+                }
+                if (rescale) {
+                    // O is rescaled only after P*V of the previous tile has finished; P*V of
+                    // this tile waits for p_full. (Q*K^T of this tile completing implies P*V two
+                    // tiles back has, so the phase of o_done[(t-1) % 2] waited for is exact.)
+                    ok = mbar_wait(&bars->o_done[(gt - 1) & 1], ((gt - 1) >> 1) & 1, abort_flag, kWaitTimeoutNs);
+                    ok = __all_sync(FULL, ok);
+                    if (!ok) break;
+                    tc_fence_after();
 #pragma unroll 1
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t orr[32];
@@ -317,72 +487,74 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     }
                     tmem_wait_st();
                 }
-            } else {
-                m = mx;
+                if (warp_live) {
+                    // P (16-bit pairs) to tensor-memory buffer t % 2, the A operand of P*V; it was
+                    // last read by P*V two tiles back, which Q*K^T of this tile completing implies is done
+                    tmem_st32(lane_base + C::PT_COL + (gt & 1) * (TK / 2), pk);
+                    tmem_wait_st();
+                }
+                if (valid < TK) {
+                    // last tile: zero V rows past the valid keys (stale or garbage rows
+                    // times P = 0 must not produce NaN)
+                    ok = mbar_wait(&bars->v_full[gt % VST], (gt / VST) & 1, abort_flag, kWaitTimeoutNs);
+                    ok = __all_sync(FULL, ok);
+                    if (!ok) break;
+                    uint8_t* sV = v_tile(gt);
+                    const int nzc = (TK - valid) * 8;  // 16-byte chunks per column half
+                    for (int c = 0; c < NC; ++c)
+                        for (int idx = tid - 64; idx < nzc; idx += 128)
+                            reinterpret_cast<uint4*>(sV + c * TK * 128 + valid * 128)[idx] = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                // a warp arrives for this tile only once every warp has arrived for the previous
+                // one, so no warp's arrival can land in an earlier tile's phase
+                if (gt > 0) {
+                    ok = mbar_wait(&bars->p_full[(gt - 1) & 1], ((gt - 1) >> 1) & 1, abort_flag, kWaitTimeoutNs);
+                    ok = __all_sync(FULL, ok);
+                    if (!ok) break;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->p_full[gt & 1]);
             }
-            // probabilities, row sum, P to shared memory (128-byte swizzle, K-major)
-            float rs = 0.f;
-            uint32_t pk[TK / 2];
-#pragma unroll
-            for (int c = 0; c < TK; c += 2) {
-                const float p0 = exp2f(sv[c] - m);
-                const float p1 = exp2f(sv[c + 1] - m);
-                rs += p0 + p1;
-                pk[c >> 1] = pack2<BF16>(p0, p1);
-            }
-            l += rs;
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc)
-                *reinterpret_cast<uint4*>(sP + row * 128 + ((cc ^ (row & 7)) << 4)) =
-                    make_uint4(pk[cc * 4], pk[cc * 4 + 1], pk[cc * 4 + 2], pk[cc * 4 + 3]);
-            if (valid < TK) {
-                // last tile: zero V rows past the valid keys (stale or garbage rows times P = 0
-                // must not produce NaN)
-                const int s = i % STAGES;
-                ok = mbar_wait(&bars->kv_full[s], (i / STAGES) & 1, abort_flag, deadline);
-                ok = __all_sync(FULL, ok);
+            if (!ok || ntiles == 0) break;
+            // the next unit's Q goes to tensor memory before this epilogue, so its first Q*K^T
+            // can be issued while the epilogue runs
+            if (u + 1 < u_end) {
+                ok = copy_q(u + 1 - u_begin);
                 if (!ok) break;
-                uint8_t* sV = smem + C::OFF_STAGE + s * C::STAGE_BYTES + C::KV_BYTES;
-                const int nzc = (TK - valid) * 8;  // 16-byte chunks per region
-                const int t = tid - 64;
-                for (int c = 0; c < NC; ++c)
-                    for (int idx = t; idx < nzc; idx += 128)
-                        reinterpret_cast<uint4*>(sV + c * TK * 128 + valid * 128)[idx] = make_uint4(0, 0, 0, 0);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bars->p_full);
-        }
-        if (ok && ntiles > 0) {
-            ok = mbar_wait(&bars->o_done, (ntiles - 1) & 1, abort_flag, deadline);
+            // ---- epilogue of the unit: normalised partial O and its log2-sum-exp2
+            // (P*V of the last tile completes o_done[last % 2]; P*V of the tile before it
+            // completed earlier, in issue order)
+            ok = mbar_wait(&bars->o_done[(gt - 1) & 1], ((gt - 1) >> 1) & 1, abort_flag, kWaitTimeoutNs);
             ok = __all_sync(FULL, ok);
-        }
-        if (ok && ntiles > 0) {
+            if (!ok) break;
             tc_fence_after();
             const bool live = row < M;
             const int wl = row / p.G, jh = row % p.G;
-            const long long prow = (static_cast<long long>(part) * p.W + (w0 + wl)) * p.Hq + g * p.G + jh;
+            const long long prow = (static_cast<long long>(cur.part) * p.W + (w0 + wl)) * p.Hq + cur.g * p.G + jh;
             float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
             const float inv = 1.0f / l;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 0; c0 < D && warp_live; c0 += 32) {
                 uint32_t orr[32];
                 tmem_ld32(lane_base + C::O_COL + c0, orr);
                 tmem_wait_ld();
                 if (live) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        dst[(c0 >> 2) + e] = make_float4(__uint_as_float(orr[4 * e]) * inv, __uint_as_float(orr[4 * e + 1]) * inv,
-                                                         __uint_as_float(orr[4 * e + 2]) * inv, __uint_as_float(orr[4 * e + 3]) * inv);
+                        dst[(c0 >> 2) + e] =
+                            make_float4(__uint_as_float(orr[4 * e]) * inv, __uint_as_float(orr[4 * e + 1]) * inv,
+                                        __uint_as_float(orr[4 * e + 2]) * inv, __uint_as_float(orr[4 * e + 3]) * inv);
                 }
             }
             if (live) p.part_lse[prow] = m + log2f(l);
+            cur = nxt;
         }
-        if (!ok) {
-            if (lane == 0) {
-                *abort_flag = 1;
-                atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
-            }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
         }
     }
     tc_fence_before();
@@ -395,26 +567,27 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 }
 
 template <int D, bool BF16>
-static cudaError_t launch_prefix_t(int num_units, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+static cudaError_t launch_prefix_t(int ctas, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                    const PrefixParams& p, cudaStream_t stream) {
     using C = PrefixCfg<D>;
-    static_assert(sizeof(PrefixBarriers) <= 256, "barrier block");
+    static_assert(sizeof(PrefixBarriers) <= 512, "barrier block");
+    static_assert(C::SMEM <= 227 * 1024, "shared memory");
     cudaError_t e = cudaFuncSetAttribute(prefix_attn_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    prefix_attn_kernel<D, BF16><<<num_units, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+    prefix_attn_kernel<D, BF16><<<ctas, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefix(int head_dim, bool bf16, int num_units, const CUtensorMap& tq, const CUtensorMap& tk,
+cudaError_t launch_prefix(int head_dim, bool bf16, int ctas, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const PrefixParams& p, cudaStream_t stream) {
-    if (num_units == 0) return cudaSuccess;
+    if (ctas == 0 || p.num_units == 0) return cudaSuccess;
     switch (head_dim) {
-        case 64: return bf16 ? launch_prefix_t<64, true>(num_units, tq, tk, tv, p, stream)
-                             : launch_prefix_t<64, false>(num_units, tq, tk, tv, p, stream);
-        case 128: return bf16 ? launch_prefix_t<128, true>(num_units, tq, tk, tv, p, stream)
-                              : launch_prefix_t<128, false>(num_units, tq, tk, tv, p, stream);
-        case 256: return bf16 ? launch_prefix_t<256, true>(num_units, tq, tk, tv, p, stream)
-                              : launch_prefix_t<256, false>(num_units, tq, tk, tv, p, stream);
+        case 64: return bf16 ? launch_prefix_t<64, true>(ctas, tq, tk, tv, p, stream)
+                             : launch_prefix_t<64, false>(ctas, tq, tk, tv, p, stream);
+        case 128: return bf16 ? launch_prefix_t<128, true>(ctas, tq, tk, tv, p, stream)
+                              : launch_prefix_t<128, false>(ctas, tq, tk, tv, p, stream);
+        case 256: return bf16 ? launch_prefix_t<256, true>(ctas, tq, tk, tv, p, stream)
+                              : launch_prefix_t<256, false>(ctas, tq, tk, tv, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

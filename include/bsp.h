@@ -113,7 +113,7 @@ typedef struct bsp_plan_t {
     int32_t max_total_len;       /* max_b P_b + T_b */
     int32_t num_sms;             /* SM count the units were balanced for */
     int32_t max_tail_len;        /* max_b T_b */
-    int32_t reserved_i;
+    int32_t prefix_ctas;         /* persistent CTAs of the prompt kernel (<= num_sms) */
     uint64_t generation;         /* staging generation of this plan (0: built only, not staged) */
     void* ws_device;             /* device workspace the plan was staged into */
     uint64_t ws_device_bytes;

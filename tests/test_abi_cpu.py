@@ -102,12 +102,16 @@ def test_plan_build_validation(lib):
     assert _err(ok, P=[200, 40]) == "BSP_ERR_INVALID_ARG"
 
 
-def decode_image(plan, img):
+def decode_image(plan, img, with_cta=False):
     i32 = img.view(np.int32)
     base = STATUS_OFFSET
     req = i32[(plan.off_req - base) // 4:(plan.off_units - base) // 4].reshape(plan.batch, 8)
-    units = i32[(plan.off_units - base) // 4:(plan.off_pages - base) // 4].reshape(plan.num_units, 8)
+    u0 = (plan.off_units - base) // 4
+    units = i32[u0:u0 + plan.num_units * 8].reshape(plan.num_units, 8)
+    cta_off = i32[u0 + plan.num_units * 8:(plan.off_pages - base) // 4]
     pages = i32[(plan.off_pages - base) // 4:]
+    if with_cta:
+        return req, units, pages, cta_off
     return req, units, pages
 
 
@@ -143,7 +147,7 @@ def test_plan_image_wide_batch_needs_no_split(lib):
     maxp = -(-P.max() // ps)
     pages = rng.integers(0, 5000, (B, maxp)).astype(np.int32)
     plan, img = bsp.plan_build(geo(npages=5000), B, W, P, T, pages, 8, 152)
-    req, units, pl = decode_image(plan, img)
+    req, units, pl, cta_off = decode_image(plan, img, with_cta=True)
     assert plan.row_blocks == 1 and plan.beams_per_block == 30
     assert plan.num_units == B * 8 and plan.num_parts == B
     assert plan.max_tail_len == T.max() and plan.max_total_len == (P + T).max()
@@ -151,8 +155,11 @@ def test_plan_image_wide_batch_needs_no_split(lib):
     np.testing.assert_array_equal(req[:, 1], T)
     np.testing.assert_array_equal(req[:, 2], 1)
     check_units_cover(plan, req, units, P)
-    lens = units[:, 4] - units[:, 3]
-    assert np.all(np.diff(lens) <= 0)                      # longest first
+    assert plan.prefix_ctas == 152 and len(cta_off) == 153
+    assert cta_off[0] == 0 and cta_off[-1] == plan.num_units and np.all(np.diff(cta_off) >= 1)
+    tiles = units[:, 4] - units[:, 3]
+    per_cta = np.array([tiles[cta_off[c]:cta_off[c + 1]].sum() for c in range(152)])
+    assert per_cta.max() <= per_cta.mean() + tiles.max()    # greedy dealing balances the persistent CTAs
     for b in range(B):
         n = -(-P[b] // ps)
         np.testing.assert_array_equal(pl[req[b][4]:req[b][4] + n], pages[b, :n])
