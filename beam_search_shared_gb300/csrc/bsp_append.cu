@@ -56,6 +56,13 @@ __global__ void __launch_bounds__(256) append_kv_kernel(AppendParams p) {
     }
 }
 
+// the same L1/shared split as the prompt kernel, so SMs are not reconfigured between the
+// kernels of a step
+cudaError_t prepare_append() {
+    return cudaFuncSetAttribute(append_kv_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+}
+
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
     const long long warps = static_cast<long long>(p.n) * p.Hkv;
     if (warps == 0) return cudaSuccess;

@@ -273,28 +273,111 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
         poff += nsplit[b];
         pgoff += ceil_div(prefix_len[b], ps);
     }
-    // Longest units first (row blocks of one split stay adjacent: equal keys keep their order),
-    // then each unit goes to the persistent CTA with the least work so far. The list is
-    // written grouped by CTA; cta_off[c] .. cta_off[c+1] are CTA c's units, in the order
-    // they were dealt.
+    // Units go to the persistent CTAs so that the largest per-CTA tile count is small.
+    // Longest units first (row blocks of one split stay adjacent: equal keys keep their
+    // order); LPT (each unit to the least-loaded CTA) gives an upper bound L on the largest
+    // load, then MULTIFIT (Coffman, Garey & Johnson 1978) looks for the smallest capacity
+    // C < L at which first-fit-decreasing packs every unit into at most num_sms bins. With
+    // few units per CTA, LPT alone can stack four short units on one CTA while others hold
+    // three long ones. The list is written grouped by CTA; cta_off[c] .. cta_off[c+1] are
+    // CTA c's units, longest first.
     std::stable_sort(units.begin(), units.end(), [](const Unit& a, const Unit& c) {
         return (a.f[kUnitTile1] - a.f[kUnitTile0]) > (c.f[kUnitTile1] - c.f[kUnitTile0]);
     });
     if (units.size() > static_cast<size_t>(std::numeric_limits<int32_t>::max())) return BSP_ERR_UNSUPPORTED;
     const int64_t nu = static_cast<int64_t>(units.size());
-    const int64_t ctas = std::min<int64_t>(nu, num_sms);
-    std::vector<int32_t> cta_off(static_cast<size_t>(ctas) + 1, 0);
-    if (ctas > 0) {
-        std::vector<std::vector<int32_t>> lists(static_cast<size_t>(ctas));
+    auto utiles = [&](int64_t i) -> int64_t { return units[i].f[kUnitTile1] - units[i].f[kUnitTile0]; };
+    std::vector<std::vector<int32_t>> lists;
+    if (nu > 0) {
+        const int64_t bins = std::min<int64_t>(nu, num_sms);
+        lists.assign(static_cast<size_t>(bins), {});
         using Load = std::pair<int64_t, int64_t>;  // (tiles so far, cta)
         std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-        for (int64_t c = 0; c < ctas; ++c) heap.push({0, c});
+        for (int64_t c = 0; c < bins; ++c) heap.push({0, c});
+        int64_t total = 0, lpt_max = 0;
         for (int64_t i = 0; i < nu; ++i) {
             Load ld = heap.top();
             heap.pop();
             lists[static_cast<size_t>(ld.second)].push_back(static_cast<int32_t>(i));
-            heap.push({ld.first + units[i].f[kUnitTile1] - units[i].f[kUnitTile0], ld.second});
+            heap.push({ld.first + utiles(i), ld.second});
+            lpt_max = std::max(lpt_max, ld.first + utiles(i));
+            total += utiles(i);
         }
+        // first-fit-decreasing into bins of capacity cap; false if more than `bins` are needed
+        std::vector<std::vector<int32_t>> ffd;
+        auto pack = [&](int64_t cap) -> bool {
+            ffd.clear();
+            std::vector<int64_t> load;
+            for (int64_t i = 0; i < nu; ++i) {
+                size_t j = 0;
+                while (j < load.size() && load[j] + utiles(i) > cap) ++j;
+                if (j == load.size()) {
+                    if (static_cast<int64_t>(load.size()) == bins) return false;
+                    load.push_back(0);
+                    ffd.emplace_back();
+                }
+                load[j] += utiles(i);
+                ffd[j].push_back(static_cast<int32_t>(i));
+            }
+            return true;
+        };
+        int64_t lo = std::max<int64_t>(ceil_div(total, bins), utiles(0)), hi = lpt_max - 1;
+        std::vector<std::vector<int32_t>> best;
+        while (lo <= hi) {
+            const int64_t mid = lo + (hi - lo) / 2;
+            if (pack(mid)) {
+                best.swap(ffd);
+                hi = mid - 1;
+            } else {
+                lo = mid + 1;
+            }
+        }
+        if (!best.empty()) lists.swap(best);
+        lists.resize(static_cast<size_t>(bins));
+        // local search on the most-loaded CTA: move one of its units to a CTA that stays below
+        // its load, or swap one of its units for a shorter one of another CTA; stop when
+        // neither lowers it
+        std::vector<int64_t> load(static_cast<size_t>(bins), 0);
+        for (int64_t c = 0; c < bins; ++c)
+            for (int32_t i : lists[static_cast<size_t>(c)]) load[static_cast<size_t>(c)] += utiles(i);
+        for (int iter = 0; iter < 4 * nu; ++iter) {
+            const size_t a = static_cast<size_t>(std::max_element(load.begin(), load.end()) - load.begin());
+            const int64_t M = load[a];
+            bool moved = false;
+            for (size_t xi = 0; xi < lists[a].size() && !moved; ++xi) {
+                const int64_t x = utiles(lists[a][xi]);
+                for (size_t b = 0; b < load.size() && !moved; ++b) {
+                    if (b == a) continue;
+                    if (load[b] + x < M) {
+                        lists[b].push_back(lists[a][xi]);
+                        lists[a].erase(lists[a].begin() + static_cast<std::ptrdiff_t>(xi));
+                        load[b] += x;
+                        load[a] -= x;
+                        moved = true;
+                        break;
+                    }
+                    for (size_t yi = 0; yi < lists[b].size(); ++yi) {
+                        const int64_t y = utiles(lists[b][yi]);
+                        if (y < x && load[b] - y + x < M) {
+                            std::swap(lists[a][xi], lists[b][yi]);
+                            load[a] += y - x;
+                            load[b] += x - y;
+                            moved = true;
+                            break;
+                        }
+                    }
+                }
+            }
+            if (!moved) break;
+        }
+        lists.erase(std::remove_if(lists.begin(), lists.end(), [](const std::vector<int32_t>& l) { return l.empty(); }),
+                    lists.end());
+        for (auto& l : lists)  // longest first within a CTA
+            std::stable_sort(l.begin(), l.end(), [&](int32_t x, int32_t y) { return utiles(x) > utiles(y); });
+    }
+    const int64_t ctas = static_cast<int64_t>(lists.size());
+    std::vector<int32_t> cta_off(static_cast<size_t>(ctas) + 1, 0);
+    {
         std::vector<Unit> dealt;
         dealt.reserve(units.size());
         for (int64_t c = 0; c < ctas; ++c) {
@@ -443,6 +526,7 @@ bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, const void* 
     p.ps_log2 = ilog2(geo.page_size);
     p.num_pages = geo.num_pages;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (prepare_append() != cudaSuccess) return BSP_ERR_CUDA;
     if (!record_event(events, 0, s)) return BSP_ERR_CUDA;
     if (launch_append(p, s) != cudaSuccess) return BSP_ERR_CUDA;
     return record_event(events, 1, s) ? BSP_OK : BSP_ERR_CUDA;
@@ -486,10 +570,14 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(plan->ws_device);
 
-    auto record = [&](int i) -> bool { return record_event(events, i, s); };
-    if (!record(0)) return BSP_ERR_CUDA;
-    if (plan->num_units > 0) {
-        CUtensorMap tq, tk, tv;
+    // everything that is not a launch (attributes, tensor maps, parameters) comes before the
+    // first timing event
+    const bool prefix = plan->num_units > 0;
+    if (prefix && prepare_prefix(D, bf16) != cudaSuccess) return BSP_ERR_CUDA;
+    if (prepare_tail(D, bf16, plan->max_tail_len) != cudaSuccess) return BSP_ERR_CUDA;
+    CUtensorMap tq, tk, tv;
+    PrefixParams pp{};
+    if (prefix) {
         cuuint64_t qdims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(R)};
         cuuint64_t qstr[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2};
         cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(plan->beams_per_block)};
@@ -501,7 +589,6 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
         if (!encode_map(&tq, geo.dtype, 3, q, qdims, qstr, qbox) || !encode_map(&tk, geo.dtype, 2, k_pool, kdims, kstr, kbox) ||
             !encode_map(&tv, geo.dtype, 2, v_pool, kdims, kstr, kbox))
             return BSP_ERR_CUDA;
-        PrefixParams pp{};
         pp.units = reinterpret_cast<const int32_t*>(ws + plan->off_units);
         pp.cta_off = pp.units + static_cast<size_t>(plan->num_units) * kUnitFields;
         pp.req = reinterpret_cast<const int32_t*>(ws + plan->off_req);
@@ -518,9 +605,7 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
         pp.num_pages = geo.num_pages;
         pp.num_units = plan->num_units;
         pp.scale_log2 = softmax_scale * log2e;
-        if (launch_prefix(D, bf16, plan->prefix_ctas, tq, tk, tv, pp, s) != cudaSuccess) return BSP_ERR_CUDA;
     }
-    if (!record(1)) return BSP_ERR_CUDA;
     TailParams tp{};
     tp.q = q;
     tp.k_pool = k_pool;
@@ -544,7 +629,14 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
     tp.max_seq = max_seq;
     tp.scale_log2 = softmax_scale * log2e;
     tp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
-    if (launch_tail(D, bf16, plan->max_tail_len, tp, s) != cudaSuccess) return BSP_ERR_CUDA;
+
+    auto record = [&](int i) -> bool { return record_event(events, i, s); };
+    if (!record(0)) return BSP_ERR_CUDA;
+    if (prefix && launch_prefix(D, bf16, plan->prefix_ctas, tq, tk, tv, pp, s) != cudaSuccess) return BSP_ERR_CUDA;
+    if (!record(1)) return BSP_ERR_CUDA;
+    // without timing events between them, the tail kernel overlaps the end of the prompt kernel
+    if (launch_tail(D, bf16, plan->max_tail_len, tp, prefix && events == nullptr, s) != cudaSuccess)
+        return BSP_ERR_CUDA;
     if (!record(2)) return BSP_ERR_CUDA;
     if (flags & BSP_FLAG_CHECK) return bsp_read_device_status(plan, stream, 1, nullptr);
     return BSP_OK;

@@ -68,7 +68,16 @@ struct AppendParams {
 
 cudaError_t launch_prefix(int head_dim, bool bf16, int ctas, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const PrefixParams& p, cudaStream_t stream);
-cudaError_t launch_tail(int head_dim, bool bf16, int max_tail_len, const TailParams& p, cudaStream_t stream);
+// Kernel attributes (shared-memory size and split) are set by the prepare_* calls, once before
+// the launches, so that timing events recorded around a launch bracket the launch alone.
+cudaError_t prepare_prefix(int head_dim, bool bf16);
+cudaError_t prepare_tail(int head_dim, bool bf16, int max_tail_len);
+// after_prefix: the prompt kernel was the last launch on `stream`; the tail kernel is then a
+// programmatic dependent launch of it (it starts on SMs the prompt kernel has left, resolves and
+// prefetches its tail rows, and waits for the prompt kernel's partials before merging).
+cudaError_t launch_tail(int head_dim, bool bf16, int max_tail_len, const TailParams& p, bool after_prefix,
+                        cudaStream_t stream);
+cudaError_t prepare_append();
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 
 }  // namespace bsp

@@ -173,7 +173,9 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
         pp.num_pages = geo->num_pages;
         pp.num_units = plan.num_units;
         pp.scale_log2 = softmax_scale * log2e;
-        if (launch_prefix(D, bf16, plan.prefix_ctas, tq, tk, tv, pp, s) != cudaSuccess) return BSP_ERR_CUDA;
+        if (prepare_prefix(D, bf16) != cudaSuccess ||
+            launch_prefix(D, bf16, plan.prefix_ctas, tq, tk, tv, pp, s) != cudaSuccess)
+            return BSP_ERR_CUDA;
     }
     TailParams tp{};
     tp.q = q;
@@ -198,7 +200,9 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
     tp.max_seq = max_seq;
     tp.scale_log2 = softmax_scale * log2e;
     tp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
-    if (launch_tail(D, bf16, plan.max_tail_len, tp, s) != cudaSuccess) return BSP_ERR_CUDA;
+    if (prepare_tail(D, bf16, plan.max_tail_len) != cudaSuccess ||
+        launch_tail(D, bf16, plan.max_tail_len, tp, plan.num_units > 0, s) != cudaSuccess)
+        return BSP_ERR_CUDA;
     if (flags & BSP_FLAG_CHECK) {
         int32_t dflags = 0;
         if (cudaStreamSynchronize(s) != cudaSuccess) return BSP_ERR_CUDA;

@@ -11,31 +11,39 @@
 // not the whole KV allocation").
 //
 // Persistent: one CTA per SM walks its own list of units (the host deals the
-// units longest first to the least-loaded CTA). Every ring is
-// indexed by a tile counter that runs across units, so the producer prefetches
-// the next unit's Q and K/V while the current one is still being reduced, and
-// the MMA warp issues the next unit's first Q*K^T while the softmax warps write
-// the previous unit's partial output.
+// units longest first to the least-loaded CTA). Every ring is indexed by a
+// tile counter that runs across units, so the producer prefetches the next
+// unit's Q and K/V while the current one is still being reduced, and the
+// output of a finished unit is written by warps of its own while the next
+// unit's tiles go through the tensor core and the softmax.
 //
-// Warp roles (192 threads):
-//   warp 0     TMA producer: Q of each unit into one of NQ buffers (3-D box
-//              [W_blk][G][64]), K and V of the unit's pages (beam 0's prompt
-//              pages) into a KST-deep K ring and a VST-deep V ring, one 2-D box
-//              of min(page, 64) rows x 64 columns per page, column half and
+// Warp roles (320 threads):
+//   warp 0     TMA producer: Q of each unit (3-D box [W_blk][G][64]) and the K
+//              and V of the unit's pages (beam 0's prompt pages) into a
+//              KST-deep K ring and a VST-deep V ring, one 2-D box of
+//              min(page, 64) rows x 64 columns per page, column half and
 //              tensor, each lane issuing its own boxes; a tile's column half c
 //              of K (or V) is a 128-byte-swizzled region of 64 rows; page ids
 //              come from a 32-entry window held one per lane. A K slot is
-//              released as soon as Q*K^T has read it, a V slot after P*V, so
-//              the short-lived K slots need fewer stages than the V slots;
+//              released as soon as Q*K^T has read it, a V slot after P*V;
 //   warp 1     TMEM allocation; one thread issues tcgen05.mma:
-//              S[t%2] = Q K_t^T, then O (+)= P_{t-1} V_{t-1};
+//              S[t%2] = Q K_t^T, then O[k%NO] (+)= P_{t-1} V_{t-1} (unit k);
 //   warps 2-5  softmax: thread <-> query row <-> TMEM lane; reads S from TMEM,
 //              masks keys >= P_b, online softmax in base 2 with a lazy rescale
 //              of O (only when a row maximum grows by more than 2^8), writes P
-//              (16-bit, swizzled K-major) to shared memory, zeroes V rows past
-//              the valid keys of the last tile, and at the end of each unit
-//              writes the normalised fp32 partial O and its log2-sum-exp2.
-// TMEM columns: S0 [0,64), S1 [64,128), O [128, 128+D).
+//              (16-bit pairs) over the first TK/2 columns of its own S buffer,
+//              where P*V reads it as the A operand, zeroes V rows past the
+//              valid keys of a unit's last tile, and hands each row's running
+//              maximum and sum to the epilogue warps at the end of a unit;
+//   warps 6-9  epilogue: copy each unit's Q from shared to tensor memory
+//              (head_dim <= 128); once a unit's last P*V is done, write the
+//              normalised fp32 partial O and its log2-sum-exp2 and release
+//              that O buffer.
+// TMEM columns: S0 [0,64), S1 [64,128) (P_t aliases the first 32 columns of
+// S[t%2]: tcgen05.mma instructions issued by one thread execute in issue
+// order, and the Q*K^T that overwrites S[t%2] is issued after the P*V that
+// reads P_t), then NO O buffers of D columns (two where they fit, one at
+// head_dim 256), then Q[0], Q[1] of D/2 columns each (head_dim <= 128).
 // Every wait is bounded (1 s without progress); on expiry the CTA flags
 // BSP_DEVFLAG_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -53,25 +61,25 @@ template <int D>
 struct PrefixCfg {
     static constexpr int TK = kTileKeys;
     static constexpr int NC = D / 64;                        // 128-byte column regions per row
-    static constexpr int NQ = D == 256 ? 1 : 2;              // Q buffers
-    static constexpr int KST = D == 64 ? 8 : (D == 128 ? 4 : 2);   // K ring depth
-    static constexpr int VST = D == 64 ? 8 : (D == 128 ? 6 : 3);   // V ring depth
+    // Q is the A operand of Q*K^T from tensor memory where it fits next to S and O
+    // (head_dim <= 128); shared memory then only stages it.
+    static constexpr bool Q_IN_TMEM = D <= 128;
+    static constexpr int KST = D == 64 ? 8 : (D == 128 ? 5 : 2);   // K ring depth
+    static constexpr int VST = D == 64 ? 8 : (D == 128 ? 7 : 3);   // V ring depth
     static constexpr int Q_BYTES = kRowsPerBlock * D * 2;    // NC regions of 128 rows x 128 B
     static constexpr int KV_BYTES = TK * D * 2;              // one K (or V) tile
-    static constexpr int OFF_K = NQ * Q_BYTES;
+    static constexpr int OFF_K = Q_BYTES;                    // one shared-memory Q buffer
     static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
-    static constexpr int OFF_BAR = OFF_V + VST * KV_BYTES;
+    static constexpr int OFF_STATS = OFF_V + VST * KV_BYTES;  // float m[128], l[128]
+    static constexpr int OFF_BAR = OFF_STATS + 2 * kRowsPerBlock * 4;
     static constexpr int SMEM = OFF_BAR + 512 + 1024;        // barriers + alignment slack
-    // Q is the A operand of Q*K^T from tensor memory when it fits next to S, O and P
-    // (head_dim <= 128); P always is the A operand of P*V from tensor memory.
-    static constexpr bool Q_IN_TMEM = D <= 128;
     static constexpr int S_COL = 0;                          // S[0], S[1]: TK fp32 columns each
-    static constexpr int O_COL = 2 * TK;                     // O: D fp32 columns
-    static constexpr int QT_COL = O_COL + D;                 // Q[0], Q[1]: D/2 columns each (2 x 16-bit)
-    static constexpr int PT_COL = QT_COL + (Q_IN_TMEM ? D : 0);  // P[0], P[1]: TK/2 columns each
+    static constexpr int O_COL = 2 * TK;                     // O[0] (, O[1]): D fp32 columns each
+    static constexpr int NO = (O_COL + 2 * D + (Q_IN_TMEM ? D : 0) <= 512) ? 2 : 1;
+    static constexpr int QT_COL = O_COL + NO * D;            // Q[0], Q[1]: D/2 columns each (2 x 16-bit)
     static constexpr uint32_t TMEM_COLS = 512;
-    static_assert(PT_COL + TK <= 512, "tensor memory");
-    static constexpr int THREADS = 192;
+    static_assert(QT_COL + (Q_IN_TMEM ? D : 0) <= 512, "tensor memory");
+    static constexpr int THREADS = 320;
 };
 
 struct PrefixBarriers {
@@ -79,13 +87,16 @@ struct PrefixBarriers {
     uint64_t k_empty[8];  // KST <= 8
     uint64_t v_full[8];
     uint64_t v_empty[8];  // VST <= 8
-    uint64_t q_full[2];   // Q of a unit landed in shared memory
-    uint64_t q_empty[2];  // that shared-memory Q buffer may be reloaded
+    uint64_t q_full;      // Q of a unit landed in shared memory
+    uint64_t q_empty;     // the shared-memory Q buffer may be reloaded
     uint64_t qt_full[2];  // Q of unit k copied into tensor-memory buffer k % 2
     uint64_t s_full[2];
-    uint64_t s_free[2];
-    uint64_t p_full[2];  // tile t arrives on p_full[t % 2]
-    uint64_t o_done[2];  // P*V of tile t completes o_done[t % 2]
+    uint64_t p_full[2];   // tile t arrives on p_full[t % 2]
+    uint64_t o_done[2];   // P*V of tile t completes o_done[t % 2]
+    uint64_t o_final[2];  // the last P*V of unit k completes o_final[k % 2]
+    uint64_t o_free[2];   // the epilogue of unit k has read O[k % NO]
+    uint64_t st_full;     // row statistics of a unit written
+    uint64_t st_empty;    // ... and read by the epilogue warps
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -126,18 +137,21 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     }
 }
 
+__device__ __forceinline__ uint32_t (&cols32(uint32_t* p))[32] { return *reinterpret_cast<uint32_t(*)[32]>(p); }
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
 prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefixParams p) {
     using C = PrefixCfg<D>;
-    constexpr int TK = C::TK, NC = C::NC, NQ = C::NQ, KST = C::KST, VST = C::VST;
+    constexpr int TK = C::TK, NC = C::NC, KST = C::KST, VST = C::VST, NO = C::NO;
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    // shared-memory P tile of global tile gt
     auto k_tile = [&](int gt) -> uint8_t* { return smem + C::OFF_K + (gt % KST) * C::KV_BYTES; };
     auto v_tile = [&](int gt) -> uint8_t* { return smem + C::OFF_V + (gt % VST) * C::KV_BYTES; };
+    float* st_m = reinterpret_cast<float*>(smem + C::OFF_STATS);  // [128]
+    float* st_l = st_m + kRowsPerBlock;                            // [128]
     PrefixBarriers* bars = reinterpret_cast<PrefixBarriers*>(smem + C::OFF_BAR);
     volatile int* abort_flag = &bars->abort_flag;
 
@@ -146,6 +160,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int lane = tid & 31;
     const int u_begin = __ldg(p.cta_off + blockIdx.x);
     const int u_end = __ldg(p.cta_off + blockIdx.x + 1);
+    const int nunits = u_end - u_begin;
     const int ps = 1 << p.ps_log2;
 
     // ---- setup
@@ -158,19 +173,20 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_init(&bars->v_full[s], 1);
             mbar_init(&bars->v_empty[s], 1);
         }
-        for (int i = 0; i < NQ; ++i) {
-            mbar_init(&bars->q_full[i], 1);
-            // released by the softmax warps once they copied it to tensor memory, else by the
-            // MMA thread after the unit's last Q*K^T
-            mbar_init(&bars->q_empty[i], C::Q_IN_TMEM ? 4 : 1);
-        }
+        mbar_init(&bars->q_full, 1);
+        // released by the epilogue warps once they copied it to tensor memory, else by the
+        // MMA thread after the unit's last Q*K^T
+        mbar_init(&bars->q_empty, C::Q_IN_TMEM ? 4 : 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars->qt_full[i], 4);  // one arrival per softmax warp
+            mbar_init(&bars->qt_full[i], 4);  // one arrival per epilogue warp
             mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->s_free[i], 128);
+            mbar_init(&bars->p_full[i], 4);   // one arrival per softmax warp
+            mbar_init(&bars->o_done[i], 1);
+            mbar_init(&bars->o_final[i], 1);
+            mbar_init(&bars->o_free[i], 4);   // one arrival per epilogue warp
         }
-        for (int i = 0; i < 2; ++i) mbar_init(&bars->p_full[i], 4);  // one arrival per softmax warp
-        for (int i = 0; i < 2; ++i) mbar_init(&bars->o_done[i], 1);
+        mbar_init(&bars->st_full, 4);   // one arrival per softmax warp
+        mbar_init(&bars->st_empty, 4);  // one arrival per epilogue warp
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -183,17 +199,18 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     {
         const int filled = p.Wblk * p.G;
         const int nz = (kRowsPerBlock - filled) * 8;  // 16-byte chunks per region
-        for (int qb = 0; qb < NQ; ++qb)
-            for (int c = 0; c < NC; ++c)
-                for (int idx = tid; idx < nz; idx += C::THREADS)
-                    reinterpret_cast<uint4*>(smem + qb * C::Q_BYTES + c * kRowsPerBlock * 128 + filled * 128)[idx] =
-                        make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < NC; ++c)
+            for (int idx = tid; idx < nz; idx += C::THREADS)
+                reinterpret_cast<uint4*>(smem + c * kRowsPerBlock * 128 + filled * 128)[idx] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    // every CTA of this grid is resident: a dependent launch (the tail kernel) may start on the
+    // SMs this grid leaves; it waits for this grid's completion before reading the partials
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
         // ================= TMA producer =================
@@ -202,17 +219,16 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         bool ok = true;
         for (int u = u_begin; u < u_end && ok; ++u, ++k) {
             const UnitInfo ui = load_unit(p, u);
-            const int qb = k % NQ;
-            if (k >= NQ) {
-                ok = mbar_wait(&bars->q_empty[qb], ((k / NQ) - 1) & 1, abort_flag, kWaitTimeoutNs);
+            if (k >= 1) {
+                ok = mbar_wait(&bars->q_empty, (k - 1) & 1, abort_flag, kWaitTimeoutNs);
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
             }
             if (lane == 0) {
-                mbar_arrive_expect_tx(&bars->q_full[qb], NC * p.Wblk * p.G * 128);
+                mbar_arrive_expect_tx(&bars->q_full, NC * p.Wblk * p.G * 128);
                 for (int c = 0; c < NC; ++c)
-                    tma_load_3d(smem + qb * C::Q_BYTES + c * kRowsPerBlock * 128, &tm_q, &bars->q_full[qb], c * 64,
-                                ui.g * p.G, ui.b * p.W + ui.rb * p.Wblk);
+                    tma_load_3d(smem + c * kRowsPerBlock * 128, &tm_q, &bars->q_full, c * 64, ui.g * p.G,
+                                ui.b * p.W + ui.rb * p.Wblk);
             }
             const int key_begin = ui.kt0 * TK;
             const int key_end = min(ui.kt1 * TK, ui.P);
@@ -244,9 +260,9 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         ok = __all_sync(FULL, ok);
                         if (!ok) break;
                     }
-                    uint64_t* full = tensor ? &bars->v_full[gt % VST] : &bars->k_full[gt % KST];
-                    uint8_t* base = tensor ? v_tile(gt) : k_tile(gt);
-                    const void* map = tensor ? static_cast<const void*>(&tm_v) : static_cast<const void*>(&tm_k);
+                    uint64_t* full = tensor == 0 ? &bars->k_full[gt % KST] : &bars->v_full[gt % VST];
+                    uint8_t* base = tensor == 0 ? k_tile(gt) : v_tile(gt);
+                    const CUtensorMap* map = tensor == 0 ? &tm_k : &tm_v;
                     if (lane == 0) mbar_arrive_expect_tx(full, tile_bytes);
                     for (int b0 = 0; b0 < nbox; b0 += 32) {
                         const int bx = b0 + lane;
@@ -281,8 +297,8 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             for (int j = max(0, gt - VST); j <= gt; ++j)
                 while (!mbar_try_wait(&bars->v_full[j % VST], (j / VST) & 1) && globaltimer_ns() - t0 < kDrainNs) {
                 }
-            for (int j = max(0, k - NQ); j <= k; ++j)
-                while (!mbar_try_wait(&bars->q_full[j % NQ], (j / NQ) & 1) && globaltimer_ns() - t0 < kDrainNs) {
+            for (int j = max(0, k - 1); j <= k; ++j)
+                while (!mbar_try_wait(&bars->q_full, j & 1) && globaltimer_ns() - t0 < kDrainNs) {
                 }
         }
     } else if (warp == 1) {
@@ -291,40 +307,46 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             constexpr uint32_t ID_QK = idesc_f16(128, TK, BF16, false);
             constexpr uint32_t ID_PV = idesc_f16(128, D, BF16, true);
             int gt = 0, k = 0;
-            int pend = -1;           // tile whose P*V is not issued yet
-            bool pend_first = false;  // ... and it opens its unit (overwrite O)
+            int pend = -1, pend_unit = 0;  // tile whose P*V is not issued yet, and its unit
+            bool pend_first = false, pend_last = false;
             bool ok = true;
-            auto issue_pv = [&](int j, bool first) -> bool {
+            auto issue_pv = [&](int j, int unit, bool first, bool last) -> bool {
                 if (!mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, abort_flag, kWaitTimeoutNs)) return false;
                 if (!mbar_wait(&bars->v_full[j % VST], (j / VST) & 1, abort_flag, kWaitTimeoutNs)) return false;
+                if (first && unit >= NO) {
+                    // O[unit % NO] was last used by unit - NO: its epilogue must have read it
+                    const int f = unit - NO;
+                    if (!mbar_wait(&bars->o_free[f & 1], (f >> 1) & 1, abort_flag, kWaitTimeoutNs)) return false;
+                }
                 tc_fence_after();
-                const uint32_t p_tmem = tmem + C::PT_COL + (j & 1) * (TK / 2);
+                const uint32_t p_tmem = tmem + C::S_COL + (j & 1) * TK;
+                const uint32_t o_tmem = tmem + C::O_COL + (unit % NO) * D;
                 const uint32_t v_addr = smem_u32(v_tile(j));
 #pragma unroll
                 for (int kk = 0; kk < TK / 16; ++kk) {
                     const uint64_t bd = sdesc_sw128(v_addr + kk * 16 * 128, TK * 128, 1024);
-                    mma_f16_tmem_a(tmem + C::O_COL, p_tmem + kk * 8, bd, ID_PV, (!first || kk > 0) ? 1u : 0u);
+                    mma_f16_tmem_a(o_tmem, p_tmem + kk * 8, bd, ID_PV, (!first || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(&bars->o_done[j & 1]);
                 mma_commit(&bars->v_empty[j % VST]);
+                if (last) mma_commit(&bars->o_final[unit & 1]);
                 return true;
             };
             for (int u = u_begin; u < u_end && ok; ++u, ++k) {
                 const int4 a = __ldg(reinterpret_cast<const int4*>(p.units + static_cast<long long>(u) * kUnitFields));
                 const int kt1 = __ldg(p.units + static_cast<long long>(u) * kUnitFields + kUnitTile1);
                 const int ntiles = kt1 - a.w;
-                const int qb = k % NQ;
                 if constexpr (C::Q_IN_TMEM)
                     ok = mbar_wait(&bars->qt_full[k & 1], (k >> 1) & 1, abort_flag, kWaitTimeoutNs);
                 else
-                    ok = mbar_wait(&bars->q_full[qb], (k / NQ) & 1, abort_flag, kWaitTimeoutNs);
+                    ok = mbar_wait(&bars->q_full, k & 1, abort_flag, kWaitTimeoutNs);
                 if (!ok) break;
-                const uint32_t q_addr = smem_u32(smem + qb * C::Q_BYTES);
+                const uint32_t q_addr = smem_u32(smem);
                 const uint32_t q_tmem = tmem + C::QT_COL + (k & 1) * (D / 2);
                 for (int t = 0; t < ntiles; ++t, ++gt) {
                     ok = mbar_wait(&bars->k_full[gt % KST], (gt / KST) & 1, abort_flag, kWaitTimeoutNs);
-                    if (ok && gt >= 2) ok = mbar_wait(&bars->s_free[gt & 1], ((gt - 2) >> 1) & 1, abort_flag, kWaitTimeoutNs);
                     if (!ok) break;
+                    // S[gt % 2] holds P of tile gt - 2, whose P*V was issued before this Q*K^T
                     tc_fence_after();
                     const uint32_t k_addr = smem_u32(k_tile(gt));
 #pragma unroll
@@ -340,16 +362,18 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     }
                     mma_commit(&bars->s_full[gt & 1]);
                     mma_commit(&bars->k_empty[gt % KST]);  // K of this tile has been read
-                    if (!C::Q_IN_TMEM && t == ntiles - 1) mma_commit(&bars->q_empty[qb]);  // Q no longer read
+                    if (!C::Q_IN_TMEM && t == ntiles - 1) mma_commit(&bars->q_empty);  // Q no longer read
                     if (pend >= 0) {
-                        ok = issue_pv(pend, pend_first);
+                        ok = issue_pv(pend, pend_unit, pend_first, pend_last);
                         if (!ok) break;
                     }
                     pend = gt;
+                    pend_unit = k;
                     pend_first = t == 0;
+                    pend_last = t == ntiles - 1;
                 }
             }
-            if (ok && pend >= 0) ok = issue_pv(pend, pend_first);
+            if (ok && pend >= 0) ok = issue_pv(pend, pend_unit, pend_first, pend_last);
             if (!ok) {
                 *abort_flag = 1;
                 atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
@@ -360,7 +384,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             while (!mbar_try_wait(&bars->drain, 0) && globaltimer_ns() - t0 < kDrainNs) {
             }
         }
-    } else {
+    } else if (warp < 6) {
         // ================= softmax warps =================
         const int quad = warp & 3;  // TMEM lane quadrant this warp may access
         const int row = quad * 32 + lane;
@@ -368,51 +392,13 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const float sl2 = p.scale_log2;
         bool ok = true;
         int gt = 0;
-        // Copies Q of the k-th unit of this CTA from its shared-memory buffer (128-byte swizzle)
-        // into tensor-memory buffer k % 2, then releases the shared-memory buffer.
-        auto copy_q = [&](int k) -> bool {
-            if constexpr (C::Q_IN_TMEM) {
-                const int qb = k % NQ;
-                if (!__all_sync(FULL, mbar_wait(&bars->q_full[qb], (k / NQ) & 1, abort_flag, kWaitTimeoutNs)))
-                    return false;
-                const uint8_t* qrow = smem + qb * C::Q_BYTES + row * 128;
-#pragma unroll
-                for (int c0 = 0; c0 < D / 2; c0 += 32) {  // 32 columns = 64 elements = one region
-                    uint32_t qr[32];
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(qrow + (c0 / 32) * (kRowsPerBlock * 128) +
-                                                                        ((cc ^ (row & 7)) << 4));
-                        qr[4 * cc] = v.x;
-                        qr[4 * cc + 1] = v.y;
-                        qr[4 * cc + 2] = v.z;
-                        qr[4 * cc + 3] = v.w;
-                    }
-                    tmem_st32(lane_base + C::QT_COL + (k & 1) * (D / 2) + c0, qr);
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bars->qt_full[k & 1]);
-                    mbar_arrive(&bars->q_empty[qb]);
-                }
-            }
-            return true;
-        };
-        UnitInfo cur;
-        if (u_begin < u_end) {
-            cur = load_unit(p, u_begin);
-            ok = copy_q(0);
-        }
-        for (int u = u_begin; u < u_end && ok; ++u) {
-            UnitInfo nxt = cur;
-            if (u + 1 < u_end) nxt = load_unit(p, u + 1);  // prefetch
+        for (int k = 0; k < nunits && ok; ++k) {
+            const UnitInfo cur = load_unit(p, u_begin + k);
             const int key_begin = cur.kt0 * TK;
             const int key_end = min(cur.kt1 * TK, cur.P);
             const int ntiles = cur.kt1 - cur.kt0;
-            const int w0 = cur.rb * p.Wblk;
-            const int M = min(p.Wblk, p.W - w0) * p.G;
+            const int M = min(p.Wblk, p.W - cur.rb * p.Wblk) * p.G;
+            const uint32_t o_col = C::O_COL + (k % NO) * D;
             // a warp whose 32 rows are all padding skips the arithmetic but keeps the
             // barrier protocol (the p_full ordering below keeps its arrivals in the right phase)
             const bool warp_live = quad * 32 < M;
@@ -423,33 +409,28 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t sr[2][32];
                 if (warp_live) {
-                    tmem_ld32(lane_base + C::S_COL + (gt & 1) * TK, sr[0]);
-                    tmem_ld32(lane_base + C::S_COL + (gt & 1) * TK + 32, sr[1]);
+                    uint32_t sr[TK];
+                    tmem_ld32(lane_base + C::S_COL + (gt & 1) * TK, cols32(sr));
+                    tmem_ld32(lane_base + C::S_COL + (gt & 1) * TK + 32, cols32(sr + 32));
                     tmem_wait_ld();
-                }
-                tc_fence_before();
-                mbar_arrive(&bars->s_free[gt & 1]);
-                float alpha = 1.0f;
-                bool rescale = false;
-                uint32_t pk[TK / 2];
-                if (warp_live) {
-                    float sv[TK];
+                    if (valid < TK) {
+#pragma unroll
+                        for (int c = 0; c < TK; ++c)
+                            if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
+                    }
+                    // row maximum of the raw scores, then scaled (the scale is positive)
                     float mp[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) mp[j] = -INFINITY;
+                    for (int j = 0; j < 8; ++j) mp[j] = __uint_as_float(sr[j]);
 #pragma unroll
-                    for (int c = 0; c < TK; ++c) {
-                        const float v = (c < valid) ? __uint_as_float(sr[c >> 5][c & 31]) * sl2 : -INFINITY;
-                        sv[c] = v;
-                        mp[c & 7] = fmaxf(mp[c & 7], v);
-                    }
+                    for (int c = 8; c < TK; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(sr[c]));
                     const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                                           fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+                                           fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * sl2;
                     // lazy maximum: keep the old one unless the row maximum grew by more than 2^8
                     const bool need = t > 0 && mx > m + 8.0f;
-                    rescale = __any_sync(FULL, need);
+                    const bool rescale = __any_sync(FULL, need);
+                    float alpha = 1.0f;
                     if (t == 0) {
                         m = mx;
                     } else if (need) {
@@ -457,44 +438,44 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         m = mx;
                         l *= alpha;
                     }
-                    // probabilities and row sum, before waiting for the previous P*V
+                    // probabilities 2^(s * scale_log2 - m), their sum, and P packed in pairs in
+                    // place of the scores
+                    const float nm = -m;
                     float rsp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int c = 0; c < TK; c += 2) {
-                        const float p0 = exp2f(sv[c] - m);
-                        const float p1 = exp2f(sv[c + 1] - m);
+                        const float p0 = exp2f(fmaf(__uint_as_float(sr[c]), sl2, nm));
+                        const float p1 = exp2f(fmaf(__uint_as_float(sr[c + 1]), sl2, nm));
                         rsp[(c >> 1) & 3] += p0 + p1;
-                        pk[c >> 1] = pack2<BF16>(p0, p1);
+                        sr[c >> 1] = pack2<BF16>(p0, p1);
                     }
                     l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
-                }
-                if (rescale) {
-                    // O is rescaled only after P*V of the previous tile has finished; P*V of
-                    // this tile waits for p_full. (Q*K^T of this tile completing implies P*V two
-                    // tiles back has, so the phase of o_done[(t-1) % 2] waited for is exact.)
-                    ok = mbar_wait(&bars->o_done[(gt - 1) & 1], ((gt - 1) >> 1) & 1, abort_flag, kWaitTimeoutNs);
-                    ok = __all_sync(FULL, ok);
-                    if (!ok) break;
-                    tc_fence_after();
+                    if (rescale) {
+                        // O is rescaled only after P*V of the previous tile has finished; P*V of
+                        // this tile waits for p_full. (Q*K^T of this tile completing implies P*V
+                        // two tiles back has, so the phase of o_done[(t-1) % 2] waited for is exact.)
+                        ok = mbar_wait(&bars->o_done[(gt - 1) & 1], ((gt - 1) >> 1) & 1, abort_flag, kWaitTimeoutNs);
+                        ok = __all_sync(FULL, ok);
+                        if (ok) {
+                            tc_fence_after();
 #pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t orr[32];
-                        tmem_ld32(lane_base + C::O_COL + c0, orr);
-                        tmem_wait_ld();
+                            for (int c0 = 0; c0 < D; c0 += 32) {
+                                uint32_t orr[32];
+                                tmem_ld32(lane_base + o_col + c0, orr);
+                                tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                        tmem_st32(lane_base + C::O_COL + c0, orr);
+                                for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                                tmem_st32(lane_base + o_col + c0, orr);
+                            }
+                        }
                     }
+                    // P over the first TK/2 columns of this tile's S buffer: the A operand of P*V
+                    tmem_st32(lane_base + C::S_COL + (gt & 1) * TK, cols32(sr));
                     tmem_wait_st();
                 }
-                if (warp_live) {
-                    // P (16-bit pairs) to tensor-memory buffer t % 2, the A operand of P*V; it was
-                    // last read by P*V two tiles back, which Q*K^T of this tile completing implies is done
-                    tmem_st32(lane_base + C::PT_COL + (gt & 1) * (TK / 2), pk);
-                    tmem_wait_st();
-                }
+                if (!ok) break;
                 if (valid < TK) {
-                    // last tile: zero V rows past the valid keys (stale or garbage rows
+                    // a unit's last tile: zero V rows past the valid keys (stale or garbage rows
                     // times P = 0 must not produce NaN)
                     ok = mbar_wait(&bars->v_full[gt % VST], (gt / VST) & 1, abort_flag, kWaitTimeoutNs);
                     ok = __all_sync(FULL, ok);
@@ -504,8 +485,8 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     for (int c = 0; c < NC; ++c)
                         for (int idx = tid - 64; idx < nzc; idx += 128)
                             reinterpret_cast<uint4*>(sV + c * TK * 128 + valid * 128)[idx] = make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
                 tc_fence_before();
                 // a warp arrives for this tile only once every warp has arrived for the previous
                 // one, so no warp's arrival can land in an earlier tile's phase
@@ -517,29 +498,89 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->p_full[gt & 1]);
             }
-            if (!ok || ntiles == 0) break;
-            // the next unit's Q goes to tensor memory before this epilogue, so its first Q*K^T
-            // can be issued while the epilogue runs
-            if (u + 1 < u_end) {
-                ok = copy_q(u + 1 - u_begin);
+            if (!ok) break;
+            // hand the row statistics of this unit to the epilogue warps (they read the
+            // previous unit's early in this one)
+            if (k >= 1) {
+                ok = mbar_wait(&bars->st_empty, (k - 1) & 1, abort_flag, kWaitTimeoutNs);
+                ok = __all_sync(FULL, ok);
                 if (!ok) break;
             }
-            // ---- epilogue of the unit: normalised partial O and its log2-sum-exp2
-            // (P*V of the last tile completes o_done[last % 2]; P*V of the tile before it
-            // completed earlier, in issue order)
-            ok = mbar_wait(&bars->o_done[(gt - 1) & 1], ((gt - 1) >> 1) & 1, abort_flag, kWaitTimeoutNs);
+            st_m[row] = m;
+            st_l[row] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->st_full);
+        }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+        }
+    } else {
+        // ================= epilogue warps =================
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        bool ok = true;
+        // Copies Q of the k-th unit of this CTA from shared memory (128-byte swizzle) into
+        // tensor-memory buffer k % 2, then releases the shared-memory buffer. Buffer k % 2 was
+        // last read by unit k - 2, whose epilogue (which saw all its MMAs complete) ran before.
+        auto copy_q = [&](int k) -> bool {
+            if (!__all_sync(FULL, mbar_wait(&bars->q_full, k & 1, abort_flag, kWaitTimeoutNs))) return false;
+            const uint8_t* qrow = smem + row * 128;
+#pragma unroll
+            for (int c0 = 0; c0 < D / 2; c0 += 32) {  // 32 columns = 64 elements = one region
+                uint32_t qr[32];
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(qrow + (c0 / 32) * (kRowsPerBlock * 128) +
+                                                                    ((cc ^ (row & 7)) << 4));
+                    qr[4 * cc] = v.x;
+                    qr[4 * cc + 1] = v.y;
+                    qr[4 * cc + 2] = v.z;
+                    qr[4 * cc + 3] = v.w;
+                }
+                tmem_st32(lane_base + C::QT_COL + (k & 1) * (D / 2) + c0, qr);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bars->qt_full[k & 1]);
+                mbar_arrive(&bars->q_empty);
+            }
+            return true;
+        };
+        if (C::Q_IN_TMEM && nunits > 0) ok = copy_q(0);
+        for (int k = 0; k < nunits && ok; ++k) {
+            if (C::Q_IN_TMEM && k + 1 < nunits) {
+                ok = copy_q(k + 1);
+                if (!ok) break;
+            }
+            const UnitInfo cur = load_unit(p, u_begin + k);
+            const int w0 = cur.rb * p.Wblk;
+            const int M = min(p.Wblk, p.W - w0) * p.G;
+            const bool warp_live = quad * 32 < M;
+            const bool live = row < M;
+            ok = mbar_wait(&bars->st_full, k & 1, abort_flag, kWaitTimeoutNs);
+            ok = __all_sync(FULL, ok);
+            if (!ok) break;
+            const float m = st_m[row];
+            const float l = st_l[row];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->st_empty);
+            ok = mbar_wait(&bars->o_final[k & 1], (k >> 1) & 1, abort_flag, kWaitTimeoutNs);
             ok = __all_sync(FULL, ok);
             if (!ok) break;
             tc_fence_after();
-            const bool live = row < M;
             const int wl = row / p.G, jh = row % p.G;
             const long long prow = (static_cast<long long>(cur.part) * p.W + (w0 + wl)) * p.Hq + cur.g * p.G + jh;
             float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
             const float inv = 1.0f / l;
+            const uint32_t o_col = C::O_COL + (k % NO) * D;
 #pragma unroll 1
             for (int c0 = 0; c0 < D && warp_live; c0 += 32) {
                 uint32_t orr[32];
-                tmem_ld32(lane_base + C::O_COL + c0, orr);
+                tmem_ld32(lane_base + o_col + c0, orr);
                 tmem_wait_ld();
                 if (live) {
 #pragma unroll
@@ -550,7 +591,9 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 }
             }
             if (live) p.part_lse[prow] = m + log2f(l);
-            cur = nxt;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->o_free[k & 1]);
         }
         if (!ok && lane == 0) {
             *abort_flag = 1;
@@ -567,15 +610,31 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 }
 
 template <int D, bool BF16>
-static cudaError_t launch_prefix_t(int ctas, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                   const PrefixParams& p, cudaStream_t stream) {
+static cudaError_t prepare_prefix_t() {
     using C = PrefixCfg<D>;
     static_assert(sizeof(PrefixBarriers) <= 512, "barrier block");
     static_assert(C::SMEM <= 227 * 1024, "shared memory");
     cudaError_t e = cudaFuncSetAttribute(prefix_attn_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(prefix_attn_kernel<D, BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+}
+
+template <int D, bool BF16>
+static cudaError_t launch_prefix_t(int ctas, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const PrefixParams& p, cudaStream_t stream) {
+    using C = PrefixCfg<D>;
     prefix_attn_kernel<D, BF16><<<ctas, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
+}
+
+cudaError_t prepare_prefix(int head_dim, bool bf16) {
+    switch (head_dim) {
+        case 64: return bf16 ? prepare_prefix_t<64, true>() : prepare_prefix_t<64, false>();
+        case 128: return bf16 ? prepare_prefix_t<128, true>() : prepare_prefix_t<128, false>();
+        case 256: return bf16 ? prepare_prefix_t<256, true>() : prepare_prefix_t<256, false>();
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_prefix(int head_dim, bool bf16, int ctas, const CUtensorMap& tq, const CUtensorMap& tk,

@@ -104,6 +104,27 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
     const long long head_stride = static_cast<long long>(D) << p.ps_log2;  // next kv head, same page/slot
     const long long pstride = static_cast<long long>(p.W) * p.Hq;          // rows of one partial slot
     const int passes = (p.Hq + NW * HPW - 1) / (NW * HPW);
+
+    // Everything read so far, and the q, K and V rows warmed into L2 here, was written before
+    // the prompt kernel started. Launched as a dependent of the prompt kernel, this CTA may run
+    // while the prompt kernel still works, and waits for its completion (and the visibility of
+    // its partials) before the merge; launched plainly, the wait returns at once.
+    for (int pass = 0; pass < passes; ++pass) {
+        const int h = pass * NW * HPW + warp * HPW + hs;
+        if (h >= p.Hq) break;
+        const uint16_t* qbase = static_cast<const uint16_t*>(p.q) + (static_cast<long long>(r) * p.Hq + h) * D;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint4*>(qbase) + li));
+        const long long gofs = (h / p.G) * head_stride;
+        for (int t = 0; t < T; ++t) {
+            const long long off = s_off[t];
+            if (off < 0) continue;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(
+                reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k_pool) + off + gofs) + li));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(
+                reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.v_pool) + off + gofs) + li));
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int pass = 0; pass < passes; ++pass) {
         const int h = pass * NW * HPW + warp * HPW + hs;
         const bool active = h < p.Hq;  // lanes of a head slot agree
@@ -223,25 +244,59 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
     }
 }
 
-template <int D, bool BF16>
-static cudaError_t launch_tail_t(const TailParams& p, int max_tail_len, cudaStream_t stream) {
+template <int D, bool BF16, int MAXT>
+static cudaError_t launch_tail_k(const TailParams& p, bool after_prefix, cudaStream_t stream) {
     const long long rows = static_cast<long long>(p.B) * p.W;
-    if (rows == 0) return cudaSuccess;
-    const unsigned grid = static_cast<unsigned>(rows);
-    if (max_tail_len <= 2)
-        tail_merge_kernel<D, BF16, 2><<<grid, kTailThreads, 0, stream>>>(p);
-    else if (max_tail_len <= 4)
-        tail_merge_kernel<D, BF16, 4><<<grid, kTailThreads, 0, stream>>>(p);
-    else
-        tail_merge_kernel<D, BF16, 8><<<grid, kTailThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(rows));
+    cfg.blockDim = dim3(kTailThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_prefix ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, tail_merge_kernel<D, BF16, MAXT>, p);
 }
 
-cudaError_t launch_tail(int head_dim, bool bf16, int max_tail_len, const TailParams& p, cudaStream_t stream) {
+template <int D, bool BF16>
+static cudaError_t launch_tail_t(const TailParams& p, int max_tail_len, bool after_prefix, cudaStream_t stream) {
+    const long long rows = static_cast<long long>(p.B) * p.W;
+    if (rows == 0) return cudaSuccess;
+    if (max_tail_len <= 2) return launch_tail_k<D, BF16, 2>(p, after_prefix, stream);
+    if (max_tail_len <= 4) return launch_tail_k<D, BF16, 4>(p, after_prefix, stream);
+    return launch_tail_k<D, BF16, 8>(p, after_prefix, stream);
+}
+
+// the same L1/shared split as the prompt kernel, so SMs are not reconfigured between the
+// kernels of a step
+template <int D, bool BF16>
+static cudaError_t prepare_tail_t(int max_tail_len) {
+    const cudaFuncAttribute a = cudaFuncAttributePreferredSharedMemoryCarveout;
+    if (max_tail_len <= 2) return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, 2>, a, cudaSharedmemCarveoutMaxShared);
+    if (max_tail_len <= 4) return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, 4>, a, cudaSharedmemCarveoutMaxShared);
+    return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, 8>, a, cudaSharedmemCarveoutMaxShared);
+}
+
+cudaError_t prepare_tail(int head_dim, bool bf16, int max_tail_len) {
     switch (head_dim) {
-        case 64: return bf16 ? launch_tail_t<64, true>(p, max_tail_len, stream) : launch_tail_t<64, false>(p, max_tail_len, stream);
-        case 128: return bf16 ? launch_tail_t<128, true>(p, max_tail_len, stream) : launch_tail_t<128, false>(p, max_tail_len, stream);
-        case 256: return bf16 ? launch_tail_t<256, true>(p, max_tail_len, stream) : launch_tail_t<256, false>(p, max_tail_len, stream);
+        case 64: return bf16 ? prepare_tail_t<64, true>(max_tail_len) : prepare_tail_t<64, false>(max_tail_len);
+        case 128: return bf16 ? prepare_tail_t<128, true>(max_tail_len) : prepare_tail_t<128, false>(max_tail_len);
+        case 256: return bf16 ? prepare_tail_t<256, true>(max_tail_len) : prepare_tail_t<256, false>(max_tail_len);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_tail(int head_dim, bool bf16, int max_tail_len, const TailParams& p, bool after_prefix,
+                        cudaStream_t stream) {
+    switch (head_dim) {
+        case 64: return bf16 ? launch_tail_t<64, true>(p, max_tail_len, after_prefix, stream)
+                             : launch_tail_t<64, false>(p, max_tail_len, after_prefix, stream);
+        case 128: return bf16 ? launch_tail_t<128, true>(p, max_tail_len, after_prefix, stream)
+                              : launch_tail_t<128, false>(p, max_tail_len, after_prefix, stream);
+        case 256: return bf16 ? launch_tail_t<256, true>(p, max_tail_len, after_prefix, stream)
+                              : launch_tail_t<256, false>(p, max_tail_len, after_prefix, stream);
         default: return cudaErrorInvalidValue;
     }
 }

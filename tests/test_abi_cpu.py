@@ -160,6 +160,11 @@ def test_plan_image_wide_batch_needs_no_split(lib):
     tiles = units[:, 4] - units[:, 3]
     per_cta = np.array([tiles[cta_off[c]:cta_off[c + 1]].sum() for c in range(152)])
     assert per_cta.max() <= per_cta.mean() + tiles.max()    # greedy dealing balances the persistent CTAs
+    # no worse than dealing each unit, longest first, to the least-loaded CTA
+    lpt = np.zeros(152, np.int64)
+    for x in sorted(tiles.tolist(), reverse=True):
+        lpt[np.argmin(lpt)] += x
+    assert per_cta.max() <= lpt.max()
     for b in range(B):
         n = -(-P[b] // ps)
         np.testing.assert_array_equal(pl[req[b][4]:req[b][4] + n], pages[b, :n])
