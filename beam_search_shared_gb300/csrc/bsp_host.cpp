@@ -574,7 +574,7 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
     // first timing event
     const bool prefix = plan->num_units > 0;
     if (prefix && prepare_prefix(D, bf16) != cudaSuccess) return BSP_ERR_CUDA;
-    if (prepare_tail(D, bf16, plan->max_tail_len) != cudaSuccess) return BSP_ERR_CUDA;
+    if (prepare_tail(D, bf16, plan->max_tail_len, Hq) != cudaSuccess) return BSP_ERR_CUDA;
     CUtensorMap tq, tk, tv;
     PrefixParams pp{};
     if (prefix) {

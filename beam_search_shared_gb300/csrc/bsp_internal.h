@@ -71,7 +71,7 @@ cudaError_t launch_prefix(int head_dim, bool bf16, int ctas, const CUtensorMap& 
 // Kernel attributes (shared-memory size and split) are set by the prepare_* calls, once before
 // the launches, so that timing events recorded around a launch bracket the launch alone.
 cudaError_t prepare_prefix(int head_dim, bool bf16);
-cudaError_t prepare_tail(int head_dim, bool bf16, int max_tail_len);
+cudaError_t prepare_tail(int head_dim, bool bf16, int max_tail_len, int num_q_heads);
 // after_prefix: the prompt kernel was the last launch on `stream`; the tail kernel is then a
 // programmatic dependent launch of it (it starts on SMs the prompt kernel has left, resolves and
 // prefetches its tail rows, and waits for the prompt kernel's partials before merging).

@@ -200,7 +200,7 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
     tp.max_seq = max_seq;
     tp.scale_log2 = softmax_scale * log2e;
     tp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
-    if (prepare_tail(D, bf16, plan.max_tail_len) != cudaSuccess ||
+    if (prepare_tail(D, bf16, plan.max_tail_len, Hq) != cudaSuccess ||
         launch_tail(D, bf16, plan.max_tail_len, tp, plan.num_units > 0, s) != cudaSuccess)
         return BSP_ERR_CUDA;
     if (flags & BSP_FLAG_CHECK) {

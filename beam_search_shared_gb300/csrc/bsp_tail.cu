@@ -66,7 +66,10 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 constexpr int kTailThreads = 128;
 
 // MAXT: tail rows held in registers, the batch's longest tail rounded up to 2, 4 or 8.
-template <int D, bool BF16, int MAXT>
+// MAXP: head passes whose tail state is held in registers across the wait for the prompt kernel
+// (passes = Hq / (4 warps x heads per warp pass), rounded up to 1, 2 or 4; more passes are done
+// in groups of MAXP).
+template <int D, bool BF16, int MAXT, int MAXP>
 __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) {
     constexpr int LPR = D / 8;       // lanes per K/V row
     constexpr int HPW = 32 / LPR;    // heads per warp pass
@@ -105,146 +108,151 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
     const long long pstride = static_cast<long long>(p.W) * p.Hq;          // rows of one partial slot
     const int passes = (p.Hq + NW * HPW - 1) / (NW * HPW);
 
-    // Everything read so far, and the q, K and V rows warmed into L2 here, was written before
-    // the prompt kernel started. Launched as a dependent of the prompt kernel, this CTA may run
-    // while the prompt kernel still works, and waits for its completion (and the visibility of
-    // its partials) before the merge; launched plainly, the wait returns at once.
-    for (int pass = 0; pass < passes; ++pass) {
-        const int h = pass * NW * HPW + warp * HPW + hs;
-        if (h >= p.Hq) break;
-        const uint16_t* qbase = static_cast<const uint16_t*>(p.q) + (static_cast<long long>(r) * p.Hq + h) * D;
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint4*>(qbase) + li));
-        const long long gofs = (h / p.G) * head_stride;
-        for (int t = 0; t < T; ++t) {
-            const long long off = s_off[t];
-            if (off < 0) continue;
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(
-                reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k_pool) + off + gofs) + li));
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(
-                reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.v_pool) + off + gofs) + li));
-        }
-    }
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int pass = 0; pass < passes; ++pass) {
-        const int h = pass * NW * HPW + warp * HPW + hs;
-        const bool active = h < p.Hq;  // lanes of a head slot agree
-        const int hh = active ? h : 0;
-        const int g = hh / p.G;
-        const uint16_t* qbase = static_cast<const uint16_t*>(p.q) + (static_cast<long long>(r) * p.Hq + hh) * D;
-        const uint4 qraw = __ldg(reinterpret_cast<const uint4*>(qbase) + li);
-        uint4 kraw[MAXT], vraw[MAXT];
-        bool ok[MAXT];
+    for (int pg = 0; pg < passes; pg += MAXP) {
+        // ---- the tail keys of this group of head passes: softmax state (m, l) and the lane's
+        // 8 columns of sum_t 2^(s_t - m) V_t. Everything read here was written before the prompt
+        // kernel started, so a CTA launched as a dependent of the prompt kernel computes it while
+        // that kernel still runs.
+        float tm[MAXP], tl[MAXP], acc[MAXP][8];
 #pragma unroll
-        for (int t = 0; t < MAXT; ++t) {
-            const long long off = t < T ? s_off[t] : -1;
-            ok[t] = active && off >= 0;
-            kraw[t] = vraw[t] = make_uint4(0, 0, 0, 0);
-            if (ok[t]) {
-                const long long e = off + g * head_stride;
-                kraw[t] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k_pool) + e) + li);
-                vraw[t] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.v_pool) + e) + li);
-            }
-        }
-        // the first prompt partial state is loaded alongside (most requests have one split)
-        const long long prow = (static_cast<long long>(part_off) * p.W + w) * p.Hq + hh;
-        float lse0 = -INFINITY;
-        float4 o0a = make_float4(0.f, 0.f, 0.f, 0.f), o0b = o0a;
-        if (active && nsplit > 0) {
-            lse0 = __ldg(p.part_lse + prow);
-            const float4* po = reinterpret_cast<const float4*>(p.part_o + prow * D) + li * 2;
-            o0a = __ldg(po);
-            o0b = __ldg(po + 1);
-        }
-
-        float q[8];
-        unpack8<BF16>(qraw, q);
-        float s[MAXT];
-        float m = -INFINITY;
-#pragma unroll
-        for (int t = 0; t < MAXT; ++t) {
-            s[t] = -INFINITY;
-            if (t < T) {  // block-uniform: rows past the request's tail cost nothing
-                float kf[8];
-                unpack8<BF16>(kraw[t], kf);
-                float dot = 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) dot = fmaf(q[e], kf[e], dot);
-#pragma unroll
-                for (int off = LPR / 2; off >= 1; off >>= 1) dot += __shfl_xor_sync(FULL, dot, off);
-                if (ok[t]) s[t] = dot * p.scale_log2;
-                m = fmaxf(m, s[t]);
-            }
-        }
-        float l = 0.f;
-        float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        if (m != -INFINITY) {
+        for (int pi = 0; pi < MAXP; ++pi) {
+            const int h = (pg + pi) * NW * HPW + warp * HPW + hs;
+            const bool active = pg + pi < passes && h < p.Hq;  // lanes of a head slot agree
+            const int hh = active ? h : 0;
+            const int g = hh / p.G;
+            const uint4 qraw = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                                     (static_cast<long long>(r) * p.Hq + hh) * D) +
+                                     li);
+            uint4 kraw[MAXT], vraw[MAXT];
+            bool ok[MAXT];
 #pragma unroll
             for (int t = 0; t < MAXT; ++t) {
-                if (!ok[t]) continue;
-                const float e_s = exp2f(s[t] - m);
-                float vf[8];
-                unpack8<BF16>(vraw[t], vf);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = fmaf(e_s, vf[e], acc[e]);
-                l += e_s;
-            }
-        }
-        if (!active) continue;
-
-        // ---- merge with the prompt partial states by log-sum-exp (base 2)
-        float Lmax = (l > 0.f) ? m + log2f(l) : -INFINITY;
-        Lmax = fmaxf(Lmax, lse0);
-        for (int sp = 1; sp < nsplit; ++sp) Lmax = fmaxf(Lmax, __ldg(p.part_lse + prow + sp * pstride));
-        float out[8];
-        float lse2;
-        if (Lmax == -INFINITY) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) out[e] = 0.f;
-            lse2 = -INFINITY;
-        } else {
-            // tail weight exp2(m + log2 l - Lmax) times O_t = acc / l
-            const float ft = (l > 0.f) ? exp2f(m - Lmax) : 0.f;
-            float sum = l * ft;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) out[e] = acc[e] * ft;
-            for (int sp = 0; sp < nsplit; ++sp) {
-                float lse_s;
-                float4 a0, a1;
-                if (sp == 0) {
-                    lse_s = lse0;
-                    a0 = o0a;
-                    a1 = o0b;
-                } else {
-                    lse_s = __ldg(p.part_lse + prow + sp * pstride);
-                    const float4* po = reinterpret_cast<const float4*>(p.part_o + (prow + sp * pstride) * D) + li * 2;
-                    a0 = __ldg(po);
-                    a1 = __ldg(po + 1);
+                const long long off = t < T ? s_off[t] : -1;
+                ok[t] = active && off >= 0;
+                kraw[t] = vraw[t] = make_uint4(0, 0, 0, 0);
+                if (ok[t]) {
+                    const long long e = off + g * head_stride;
+                    kraw[t] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k_pool) + e) + li);
+                    vraw[t] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.v_pool) + e) + li);
                 }
-                const float wgt = exp2f(lse_s - Lmax);
-                out[0] = fmaf(wgt, a0.x, out[0]);
-                out[1] = fmaf(wgt, a0.y, out[1]);
-                out[2] = fmaf(wgt, a0.z, out[2]);
-                out[3] = fmaf(wgt, a0.w, out[3]);
-                out[4] = fmaf(wgt, a1.x, out[4]);
-                out[5] = fmaf(wgt, a1.y, out[5]);
-                out[6] = fmaf(wgt, a1.z, out[6]);
-                out[7] = fmaf(wgt, a1.w, out[7]);
-                sum += wgt;
             }
-            const float inv = 1.f / sum;
+            float q[8];
+            unpack8<BF16>(qraw, q);
+            float sc[MAXT];
+            float m = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) out[e] *= inv;
-            lse2 = Lmax + log2f(sum);
+            for (int t = 0; t < MAXT; ++t) {
+                sc[t] = -INFINITY;
+                if (t < T) {  // block-uniform: rows past the request's tail cost nothing
+                    float kf[8];
+                    unpack8<BF16>(kraw[t], kf);
+                    float dot = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) dot = fmaf(q[e], kf[e], dot);
+#pragma unroll
+                    for (int off = LPR / 2; off >= 1; off >>= 1) dot += __shfl_xor_sync(FULL, dot, off);
+                    if (ok[t]) sc[t] = dot * p.scale_log2;
+                    m = fmaxf(m, sc[t]);
+                }
+            }
+            float l = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[pi][e] = 0.f;
+            if (m != -INFINITY) {
+#pragma unroll
+                for (int t = 0; t < MAXT; ++t) {
+                    if (!ok[t]) continue;
+                    const float e_s = exp2f(sc[t] - m);
+                    float vf[8];
+                    unpack8<BF16>(vraw[t], vf);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[pi][e] = fmaf(e_s, vf[e], acc[pi][e]);
+                    l += e_s;
+                }
+            }
+            tm[pi] = m;
+            tl[pi] = l;
         }
-        uint16_t* obase = static_cast<uint16_t*>(p.o) + (static_cast<long long>(r) * p.Hq + h) * D;
-        reinterpret_cast<uint4*>(obase)[li] = pack8<BF16>(out);
-        if (li == 0) p.lse[static_cast<long long>(r) * p.Hq + h] = p.lse_base2 ? lse2 : lse2 * 0.69314718055994530942f;
+
+        // ---- wait for the prompt kernel's partial states (returns at once when launched plainly)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+
+        // ---- merge with the prompt partial states by log-sum-exp (base 2), one round of loads
+        float lse0[MAXP];
+        float4 o0a[MAXP], o0b[MAXP];
+#pragma unroll
+        for (int pi = 0; pi < MAXP; ++pi) {
+            const int h = (pg + pi) * NW * HPW + warp * HPW + hs;
+            const bool active = pg + pi < passes && h < p.Hq;
+            lse0[pi] = -INFINITY;
+            o0a[pi] = o0b[pi] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (active && nsplit > 0) {
+                const long long prow = (static_cast<long long>(part_off) * p.W + w) * p.Hq + h;
+                lse0[pi] = __ldg(p.part_lse + prow);
+                const float4* po = reinterpret_cast<const float4*>(p.part_o + prow * D) + li * 2;
+                o0a[pi] = __ldg(po);
+                o0b[pi] = __ldg(po + 1);
+            }
+        }
+#pragma unroll
+        for (int pi = 0; pi < MAXP; ++pi) {
+            const int h = (pg + pi) * NW * HPW + warp * HPW + hs;
+            if (!(pg + pi < passes && h < p.Hq)) continue;
+            const long long prow = (static_cast<long long>(part_off) * p.W + w) * p.Hq + h;
+            const float m = tm[pi], l = tl[pi];
+            float Lmax = (l > 0.f) ? m + log2f(l) : -INFINITY;
+            Lmax = fmaxf(Lmax, lse0[pi]);
+            for (int sp = 1; sp < nsplit; ++sp) Lmax = fmaxf(Lmax, __ldg(p.part_lse + prow + sp * pstride));
+            float out[8];
+            float lse2;
+            if (Lmax == -INFINITY) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) out[e] = 0.f;
+                lse2 = -INFINITY;
+            } else {
+                // tail weight exp2(m + log2 l - Lmax) times O_t = acc / l
+                const float ft = (l > 0.f) ? exp2f(m - Lmax) : 0.f;
+                float sum = l * ft;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) out[e] = acc[pi][e] * ft;
+                for (int sp = 0; sp < nsplit; ++sp) {
+                    float lse_s;
+                    float4 a0, a1;
+                    if (sp == 0) {
+                        lse_s = lse0[pi];
+                        a0 = o0a[pi];
+                        a1 = o0b[pi];
+                    } else {
+                        lse_s = __ldg(p.part_lse + prow + sp * pstride);
+                        const float4* po = reinterpret_cast<const float4*>(p.part_o + (prow + sp * pstride) * D) + li * 2;
+                        a0 = __ldg(po);
+                        a1 = __ldg(po + 1);
+                    }
+                    const float wgt = exp2f(lse_s - Lmax);
+                    out[0] = fmaf(wgt, a0.x, out[0]);
+                    out[1] = fmaf(wgt, a0.y, out[1]);
+                    out[2] = fmaf(wgt, a0.z, out[2]);
+                    out[3] = fmaf(wgt, a0.w, out[3]);
+                    out[4] = fmaf(wgt, a1.x, out[4]);
+                    out[5] = fmaf(wgt, a1.y, out[5]);
+                    out[6] = fmaf(wgt, a1.z, out[6]);
+                    out[7] = fmaf(wgt, a1.w, out[7]);
+                    sum += wgt;
+                }
+                const float inv = 1.f / sum;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) out[e] *= inv;
+                lse2 = Lmax + log2f(sum);
+            }
+            uint16_t* obase = static_cast<uint16_t*>(p.o) + (static_cast<long long>(r) * p.Hq + h) * D;
+            reinterpret_cast<uint4*>(obase)[li] = pack8<BF16>(out);
+            if (li == 0)
+                p.lse[static_cast<long long>(r) * p.Hq + h] = p.lse_base2 ? lse2 : lse2 * 0.69314718055994530942f;
+        }
     }
 }
 
-template <int D, bool BF16, int MAXT>
+template <int D, bool BF16, int MAXT, int MAXP>
 static cudaError_t launch_tail_k(const TailParams& p, bool after_prefix, cudaStream_t stream) {
     const long long rows = static_cast<long long>(p.B) * p.W;
     cudaLaunchConfig_t cfg = {};
@@ -257,33 +265,59 @@ static cudaError_t launch_tail_k(const TailParams& p, bool after_prefix, cudaStr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = after_prefix ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, tail_merge_kernel<D, BF16, MAXT>, p);
+    return cudaLaunchKernelEx(&cfg, tail_merge_kernel<D, BF16, MAXT, MAXP>, p);
+}
+
+// head passes of a 128-thread CTA: Hq / (4 warps x heads per warp pass)
+template <int D>
+static int tail_passes(int Hq) {
+    constexpr int hpw = 32 / (D / 8);
+    return (Hq + 4 * hpw - 1) / (4 * hpw);
+}
+
+template <int D, bool BF16, int MAXT>
+static cudaError_t launch_tail_p(const TailParams& p, bool after_prefix, cudaStream_t stream) {
+    const int passes = tail_passes<D>(p.Hq);
+    if (passes <= 1) return launch_tail_k<D, BF16, MAXT, 1>(p, after_prefix, stream);
+    if (passes <= 2) return launch_tail_k<D, BF16, MAXT, 2>(p, after_prefix, stream);
+    return launch_tail_k<D, BF16, MAXT, 4>(p, after_prefix, stream);
 }
 
 template <int D, bool BF16>
 static cudaError_t launch_tail_t(const TailParams& p, int max_tail_len, bool after_prefix, cudaStream_t stream) {
     const long long rows = static_cast<long long>(p.B) * p.W;
     if (rows == 0) return cudaSuccess;
-    if (max_tail_len <= 2) return launch_tail_k<D, BF16, 2>(p, after_prefix, stream);
-    if (max_tail_len <= 4) return launch_tail_k<D, BF16, 4>(p, after_prefix, stream);
-    return launch_tail_k<D, BF16, 8>(p, after_prefix, stream);
+    if (max_tail_len <= 2) return launch_tail_p<D, BF16, 2>(p, after_prefix, stream);
+    if (max_tail_len <= 4) return launch_tail_p<D, BF16, 4>(p, after_prefix, stream);
+    return launch_tail_p<D, BF16, 8>(p, after_prefix, stream);
 }
 
 // the same L1/shared split as the prompt kernel, so SMs are not reconfigured between the
 // kernels of a step
-template <int D, bool BF16>
-static cudaError_t prepare_tail_t(int max_tail_len) {
+template <int D, bool BF16, int MAXT>
+static cudaError_t prepare_tail_p(int Hq) {
     const cudaFuncAttribute a = cudaFuncAttributePreferredSharedMemoryCarveout;
-    if (max_tail_len <= 2) return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, 2>, a, cudaSharedmemCarveoutMaxShared);
-    if (max_tail_len <= 4) return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, 4>, a, cudaSharedmemCarveoutMaxShared);
-    return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, 8>, a, cudaSharedmemCarveoutMaxShared);
+    const int passes = tail_passes<D>(Hq);
+    if (passes <= 1) return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, MAXT, 1>, a, cudaSharedmemCarveoutMaxShared);
+    if (passes <= 2) return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, MAXT, 2>, a, cudaSharedmemCarveoutMaxShared);
+    return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, MAXT, 4>, a, cudaSharedmemCarveoutMaxShared);
 }
 
-cudaError_t prepare_tail(int head_dim, bool bf16, int max_tail_len) {
+template <int D, bool BF16>
+static cudaError_t prepare_tail_t(int max_tail_len, int Hq) {
+    if (max_tail_len <= 2) return prepare_tail_p<D, BF16, 2>(Hq);
+    if (max_tail_len <= 4) return prepare_tail_p<D, BF16, 4>(Hq);
+    return prepare_tail_p<D, BF16, 8>(Hq);
+}
+
+cudaError_t prepare_tail(int head_dim, bool bf16, int max_tail_len, int num_q_heads) {
     switch (head_dim) {
-        case 64: return bf16 ? prepare_tail_t<64, true>(max_tail_len) : prepare_tail_t<64, false>(max_tail_len);
-        case 128: return bf16 ? prepare_tail_t<128, true>(max_tail_len) : prepare_tail_t<128, false>(max_tail_len);
-        case 256: return bf16 ? prepare_tail_t<256, true>(max_tail_len) : prepare_tail_t<256, false>(max_tail_len);
+        case 64: return bf16 ? prepare_tail_t<64, true>(max_tail_len, num_q_heads)
+                             : prepare_tail_t<64, false>(max_tail_len, num_q_heads);
+        case 128: return bf16 ? prepare_tail_t<128, true>(max_tail_len, num_q_heads)
+                              : prepare_tail_t<128, false>(max_tail_len, num_q_heads);
+        case 256: return bf16 ? prepare_tail_t<256, true>(max_tail_len, num_q_heads)
+                              : prepare_tail_t<256, false>(max_tail_len, num_q_heads);
         default: return cudaErrorInvalidValue;
     }
 }
