@@ -4,46 +4,51 @@
 // request"; all beam_width x GQA-group query rows of a request share one K/V
 // stream, which makes Q*K^T and P*V dense contractions).
 //
-// Work unit = (request b, kv head g, query-row block, range of 64-key tiles).
-// Query rows of a block are (beam w, head j) pairs, row = w_local * G + j, at
-// most 128 (the MMA M). Only the valid prompt rows [0, P_b) are read
-// (TensorRT-Model-Connect PR #2202, "prefill and decode over the cached prefix,
-// not the whole KV allocation").
+// Work unit = (request b, kv head g, query-row block, key range of the plan's
+// 64-key tiles). Query rows of a block are (beam w, head j) pairs,
+// row = w_local * G + j, at most 128 (the MMA M). Only the valid prompt rows
+// [0, P_b) are read (TensorRT-Model-Connect PR #2202, "prefill and decode over
+// the cached prefix, not the whole KV allocation"). The kernel walks a unit's
+// key range in tiles of TK keys (128 at head_dim <= 128, 64 at 256); the last
+// tile of a unit may be partial.
 //
-// Persistent: one CTA per SM walks its own list of units (the host deals the
-// units longest first to the least-loaded CTA). Every ring is indexed by a
-// tile counter that runs across units, so the producer prefetches the next
-// unit's Q and K/V while the current one is still being reduced, and the
-// output of a finished unit is written by warps of its own while the next
-// unit's tiles go through the tensor core and the softmax.
+// Persistent: one CTA per SM walks its own list of units (the host deals them
+// so that the largest per-CTA load is small). Every ring is indexed by a tile
+// counter that runs across units, so the producer prefetches the next unit's
+// Q and K/V while the current one is still being reduced, and the output of a
+// finished unit is written by warps of its own while the next unit's tiles go
+// through the tensor core and the softmax.
 //
 // Warp roles (320 threads):
-//   warp 0     TMA producer: Q of each unit (3-D box [W_blk][G][64]) and the K
-//              and V of the unit's pages (beam 0's prompt pages) into a
-//              KST-deep K ring and a VST-deep V ring, one 2-D box of
-//              min(page, 64) rows x 64 columns per page, column half and
-//              tensor, each lane issuing its own boxes; a tile's column half c
-//              of K (or V) is a 128-byte-swizzled region of 64 rows; page ids
-//              come from a 32-entry window held one per lane. A K slot is
-//              released as soon as Q*K^T has read it, a V slot after P*V;
+//   warp 0     TMA producer: Q of each unit into one of NQ shared-memory
+//              buffers (3-D box [W_blk][G][64]) and the K and V of the unit's
+//              pages (beam 0's prompt pages) into a KST-deep K ring and a
+//              VST-deep V ring, one 2-D box of min(page, 64) rows x 64 columns
+//              per page slice, column half and tensor, each lane issuing its
+//              own boxes; a tile's column half c of K (or V) is a
+//              128-byte-swizzled region of TK rows; page ids come from a
+//              32-entry window held one per lane. A K slot is released as soon
+//              as Q*K^T has read it, a V slot after P*V, Q after the unit's
+//              last Q*K^T;
 //   warp 1     TMEM allocation; one thread issues tcgen05.mma:
-//              S[t%2] = Q K_t^T, then O[k%NO] (+)= P_{t-1} V_{t-1} (unit k);
-//   warps 2-5  softmax: thread <-> query row <-> TMEM lane; reads S from TMEM,
+//              S[t%2] = Q K_t^T (both operands in shared memory), then
+//              O[k%NO] (+)= P_{t-1} V_{t-1} (unit k);
+//   warps 2-5  softmax: thread <-> query row <-> TMEM lane; reads S from TMEM
+//              in 32-column chunks twice (row maximum, then probabilities),
 //              masks keys >= P_b, online softmax in base 2 with a lazy rescale
 //              of O (only when a row maximum grows by more than 2^8), writes P
 //              (16-bit pairs) over the first TK/2 columns of its own S buffer,
 //              where P*V reads it as the A operand, zeroes V rows past the
 //              valid keys of a unit's last tile, and hands each row's running
 //              maximum and sum to the epilogue warps at the end of a unit;
-//   warps 6-9  epilogue: copy each unit's Q from shared to tensor memory
-//              (head_dim <= 128); once a unit's last P*V is done, write the
-//              normalised fp32 partial O and its log2-sum-exp2 and release
-//              that O buffer.
-// TMEM columns: S0 [0,64), S1 [64,128) (P_t aliases the first 32 columns of
+//   warps 6-9  epilogue: once a unit's last P*V is done, write the normalised
+//              fp32 partial O and its log2-sum-exp2, then release that O
+//              buffer.
+// TMEM columns: S0 [0,TK), S1 [TK,2TK) (P_t aliases the first TK/2 columns of
 // S[t%2]: tcgen05.mma instructions issued by one thread execute in issue
 // order, and the Q*K^T that overwrites S[t%2] is issued after the P*V that
 // reads P_t), then NO O buffers of D columns (two where they fit, one at
-// head_dim 256), then Q[0], Q[1] of D/2 columns each (head_dim <= 128).
+// head_dim 256).
 // Every wait is bounded (1 s without progress); on expiry the CTA flags
 // BSP_DEVFLAG_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -59,26 +64,24 @@ namespace bsp {
 
 template <int D>
 struct PrefixCfg {
-    static constexpr int TK = kTileKeys;
+    static constexpr int TK = D <= 128 ? 128 : 64;            // keys per tile
     static constexpr int NC = D / 64;                        // 128-byte column regions per row
-    // Q is the A operand of Q*K^T from tensor memory where it fits next to S and O
-    // (head_dim <= 128); shared memory then only stages it.
-    static constexpr bool Q_IN_TMEM = D <= 128;
-    static constexpr int KST = D == 64 ? 8 : (D == 128 ? 5 : 2);   // K ring depth
-    static constexpr int VST = D == 64 ? 8 : (D == 128 ? 7 : 3);   // V ring depth
+    static constexpr int NQ = D <= 128 ? 2 : 1;              // Q buffers
+    static constexpr int KST = D == 64 ? 4 : 2;              // K ring depth
+    static constexpr int VST = D == 64 ? 7 : 3;              // V ring depth
     static constexpr int Q_BYTES = kRowsPerBlock * D * 2;    // NC regions of 128 rows x 128 B
     static constexpr int KV_BYTES = TK * D * 2;              // one K (or V) tile
-    static constexpr int OFF_K = Q_BYTES;                    // one shared-memory Q buffer
+    static constexpr int OFF_K = NQ * Q_BYTES;
     static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
     static constexpr int OFF_STATS = OFF_V + VST * KV_BYTES;  // float m[128], l[128]
     static constexpr int OFF_BAR = OFF_STATS + 2 * kRowsPerBlock * 4;
     static constexpr int SMEM = OFF_BAR + 512 + 1024;        // barriers + alignment slack
     static constexpr int S_COL = 0;                          // S[0], S[1]: TK fp32 columns each
     static constexpr int O_COL = 2 * TK;                     // O[0] (, O[1]): D fp32 columns each
-    static constexpr int NO = (O_COL + 2 * D + (Q_IN_TMEM ? D : 0) <= 512) ? 2 : 1;
-    static constexpr int QT_COL = O_COL + NO * D;            // Q[0], Q[1]: D/2 columns each (2 x 16-bit)
+    static constexpr int NO = (O_COL + 2 * D <= 512) ? 2 : 1;
     static constexpr uint32_t TMEM_COLS = 512;
-    static_assert(QT_COL + (Q_IN_TMEM ? D : 0) <= 512, "tensor memory");
+    static_assert(O_COL + NO * D <= 512, "tensor memory");
+    static_assert(TK % 64 == 0 && TK / 16 <= 8 && D / 16 <= 16, "tile shape");
     static constexpr int THREADS = 320;
 };
 
@@ -87,9 +90,8 @@ struct PrefixBarriers {
     uint64_t k_empty[8];  // KST <= 8
     uint64_t v_full[8];
     uint64_t v_empty[8];  // VST <= 8
-    uint64_t q_full;      // Q of a unit landed in shared memory
-    uint64_t q_empty;     // the shared-memory Q buffer may be reloaded
-    uint64_t qt_full[2];  // Q of unit k copied into tensor-memory buffer k % 2
+    uint64_t q_full[2];   // Q of unit k landed in shared-memory buffer k % NQ
+    uint64_t q_empty[2];  // ... and its last Q*K^T completed
     uint64_t s_full[2];
     uint64_t p_full[2];   // tile t arrives on p_full[t % 2]
     uint64_t o_done[2];   // P*V of tile t completes o_done[t % 2]
@@ -106,7 +108,8 @@ constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s without progress
 constexpr uint64_t kDrainNs = 200000000ull;
 
 struct UnitInfo {
-    int b, g, rb, kt0, kt1, part, P, page_off;
+    int b, g, rb, part, P, page_off;
+    int key_begin, key_end;  // keys [key_begin, key_end) of the request's prompt
 };
 
 __device__ __forceinline__ UnitInfo load_unit(const PrefixParams& p, int u) {
@@ -118,12 +121,17 @@ __device__ __forceinline__ UnitInfo load_unit(const PrefixParams& p, int u) {
     ui.b = a.x;
     ui.g = a.y;
     ui.rb = a.z;
-    ui.kt0 = a.w;
-    ui.kt1 = c.x;
     ui.part = c.y;
     ui.P = r.x;
     ui.page_off = r2.x;
+    ui.key_begin = a.w * kTileKeys;                // plan tiles are kTileKeys keys
+    ui.key_end = min(c.x * kTileKeys, ui.P);
     return ui;
+}
+
+template <int TK>
+__device__ __forceinline__ int unit_tiles(const UnitInfo& ui) {
+    return (ui.key_end - ui.key_begin + TK - 1) / TK;
 }
 
 template <bool BF16>
@@ -137,17 +145,16 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     }
 }
 
-__device__ __forceinline__ uint32_t (&cols32(uint32_t* p))[32] { return *reinterpret_cast<uint32_t(*)[32]>(p); }
-
 template <int D, bool BF16>
 __global__ void __launch_bounds__(320, 1)
 prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefixParams p) {
     using C = PrefixCfg<D>;
-    constexpr int TK = C::TK, NC = C::NC, KST = C::KST, VST = C::VST, NO = C::NO;
+    constexpr int TK = C::TK, NC = C::NC, NQ = C::NQ, KST = C::KST, VST = C::VST, NO = C::NO;
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    auto q_buf = [&](int k) -> uint8_t* { return smem + (k % NQ) * C::Q_BYTES; };
     auto k_tile = [&](int gt) -> uint8_t* { return smem + C::OFF_K + (gt % KST) * C::KV_BYTES; };
     auto v_tile = [&](int gt) -> uint8_t* { return smem + C::OFF_V + (gt % VST) * C::KV_BYTES; };
     float* st_m = reinterpret_cast<float*>(smem + C::OFF_STATS);  // [128]
@@ -173,12 +180,9 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_init(&bars->v_full[s], 1);
             mbar_init(&bars->v_empty[s], 1);
         }
-        mbar_init(&bars->q_full, 1);
-        // released by the epilogue warps once they copied it to tensor memory, else by the
-        // MMA thread after the unit's last Q*K^T
-        mbar_init(&bars->q_empty, C::Q_IN_TMEM ? 4 : 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars->qt_full[i], 4);  // one arrival per epilogue warp
+            mbar_init(&bars->q_full[i], 1);
+            mbar_init(&bars->q_empty[i], 1);  // the MMA thread, after the unit's last Q*K^T
             mbar_init(&bars->s_full[i], 1);
             mbar_init(&bars->p_full[i], 4);   // one arrival per softmax warp
             mbar_init(&bars->o_done[i], 1);
@@ -199,9 +203,11 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     {
         const int filled = p.Wblk * p.G;
         const int nz = (kRowsPerBlock - filled) * 8;  // 16-byte chunks per region
-        for (int c = 0; c < NC; ++c)
-            for (int idx = tid; idx < nz; idx += C::THREADS)
-                reinterpret_cast<uint4*>(smem + c * kRowsPerBlock * 128 + filled * 128)[idx] = make_uint4(0, 0, 0, 0);
+        for (int qb = 0; qb < NQ; ++qb)
+            for (int c = 0; c < NC; ++c)
+                for (int idx = tid; idx < nz; idx += C::THREADS)
+                    reinterpret_cast<uint4*>(q_buf(qb) + c * kRowsPerBlock * 128 + filled * 128)[idx] =
+                        make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -214,25 +220,24 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
     if (warp == 0) {
         // ================= TMA producer =================
-        const int BR = ps < TK ? ps : TK;  // rows per box (a page, or 64 rows of a larger page)
+        const int BR = ps < kTileKeys ? ps : kTileKeys;  // rows per box (a page, or 64 rows of a larger page)
         int gt = 0, k = 0;
         bool ok = true;
         for (int u = u_begin; u < u_end && ok; ++u, ++k) {
             const UnitInfo ui = load_unit(p, u);
-            if (k >= 1) {
-                ok = mbar_wait(&bars->q_empty, (k - 1) & 1, abort_flag, kWaitTimeoutNs);
+            const int qb = k % NQ;
+            if (k >= NQ) {
+                ok = mbar_wait(&bars->q_empty[qb], ((k / NQ) - 1) & 1, abort_flag, kWaitTimeoutNs);
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
             }
             if (lane == 0) {
-                mbar_arrive_expect_tx(&bars->q_full, NC * p.Wblk * p.G * 128);
+                mbar_arrive_expect_tx(&bars->q_full[qb], NC * p.Wblk * p.G * 128);
                 for (int c = 0; c < NC; ++c)
-                    tma_load_3d(smem + c * kRowsPerBlock * 128, &tm_q, &bars->q_full, c * 64, ui.g * p.G,
+                    tma_load_3d(q_buf(k) + c * kRowsPerBlock * 128, &tm_q, &bars->q_full[qb], c * 64, ui.g * p.G,
                                 ui.b * p.W + ui.rb * p.Wblk);
             }
-            const int key_begin = ui.kt0 * TK;
-            const int key_end = min(ui.kt1 * TK, ui.P);
-            const int ntiles = ui.kt1 - ui.kt0;
+            const int ntiles = unit_tiles<TK>(ui);
             const int* pg = p.pages + ui.page_off;
             const int npages = (ui.P + ps - 1) >> p.ps_log2;
             int win_base = -1, my_page = 0;
@@ -242,8 +247,8 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     ok = __all_sync(FULL, ok);
                     if (!ok) break;
                 }
-                const int key0 = key_begin + t * TK;
-                const int valid = min(TK, key_end - key0);
+                const int key0 = ui.key_begin + t * TK;
+                const int valid = min(TK, ui.key_end - key0);
                 const int nchunks = (valid + BR - 1) / BR;  // pages (or 64-row slices) with valid keys
                 const int tile_bytes = nchunks * BR * D * 2;
                 const int pidx0 = key0 >> p.ps_log2;
@@ -297,8 +302,8 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             for (int j = max(0, gt - VST); j <= gt; ++j)
                 while (!mbar_try_wait(&bars->v_full[j % VST], (j / VST) & 1) && globaltimer_ns() - t0 < kDrainNs) {
                 }
-            for (int j = max(0, k - 1); j <= k; ++j)
-                while (!mbar_try_wait(&bars->q_full, j & 1) && globaltimer_ns() - t0 < kDrainNs) {
+            for (int j = max(0, k - NQ); j <= k; ++j)
+                while (!mbar_try_wait(&bars->q_full[j % NQ], (j / NQ) & 1) && globaltimer_ns() - t0 < kDrainNs) {
                 }
         }
     } else if (warp == 1) {
@@ -333,16 +338,11 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 return true;
             };
             for (int u = u_begin; u < u_end && ok; ++u, ++k) {
-                const int4 a = __ldg(reinterpret_cast<const int4*>(p.units + static_cast<long long>(u) * kUnitFields));
-                const int kt1 = __ldg(p.units + static_cast<long long>(u) * kUnitFields + kUnitTile1);
-                const int ntiles = kt1 - a.w;
-                if constexpr (C::Q_IN_TMEM)
-                    ok = mbar_wait(&bars->qt_full[k & 1], (k >> 1) & 1, abort_flag, kWaitTimeoutNs);
-                else
-                    ok = mbar_wait(&bars->q_full, k & 1, abort_flag, kWaitTimeoutNs);
+                const int ntiles = unit_tiles<TK>(load_unit(p, u));
+                const int qb = k % NQ;
+                ok = mbar_wait(&bars->q_full[qb], (k / NQ) & 1, abort_flag, kWaitTimeoutNs);
                 if (!ok) break;
-                const uint32_t q_addr = smem_u32(smem);
-                const uint32_t q_tmem = tmem + C::QT_COL + (k & 1) * (D / 2);
+                const uint32_t q_addr = smem_u32(q_buf(k));
                 for (int t = 0; t < ntiles; ++t, ++gt) {
                     ok = mbar_wait(&bars->k_full[gt % KST], (gt / KST) & 1, abort_flag, kWaitTimeoutNs);
                     if (!ok) break;
@@ -351,18 +351,14 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     const uint32_t k_addr = smem_u32(k_tile(gt));
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t ad =
+                            sdesc_sw128(q_addr + (kk >> 2) * (kRowsPerBlock * 128) + (kk & 3) * 32, 16, 1024);
                         const uint64_t bd = sdesc_sw128(k_addr + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
-                        if constexpr (C::Q_IN_TMEM) {
-                            mma_f16_tmem_a(tmem + C::S_COL + (gt & 1) * TK, q_tmem + kk * 8, bd, ID_QK, kk > 0 ? 1u : 0u);
-                        } else {
-                            const uint64_t ad =
-                                sdesc_sw128(q_addr + (kk >> 2) * (kRowsPerBlock * 128) + (kk & 3) * 32, 16, 1024);
-                            mma_f16(tmem + C::S_COL + (gt & 1) * TK, ad, bd, ID_QK, kk > 0 ? 1u : 0u);
-                        }
+                        mma_f16(tmem + C::S_COL + (gt & 1) * TK, ad, bd, ID_QK, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(&bars->s_full[gt & 1]);
                     mma_commit(&bars->k_empty[gt % KST]);  // K of this tile has been read
-                    if (!C::Q_IN_TMEM && t == ntiles - 1) mma_commit(&bars->q_empty);  // Q no longer read
+                    if (t == ntiles - 1) mma_commit(&bars->q_empty[qb]);  // Q no longer read
                     if (pend >= 0) {
                         ok = issue_pv(pend, pend_unit, pend_first, pend_last);
                         if (!ok) break;
@@ -394,9 +390,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         int gt = 0;
         for (int k = 0; k < nunits && ok; ++k) {
             const UnitInfo cur = load_unit(p, u_begin + k);
-            const int key_begin = cur.kt0 * TK;
-            const int key_end = min(cur.kt1 * TK, cur.P);
-            const int ntiles = cur.kt1 - cur.kt0;
+            const int ntiles = unit_tiles<TK>(cur);
             const int M = min(p.Wblk, p.W - cur.rb * p.Wblk) * p.G;
             const uint32_t o_col = C::O_COL + (k % NO) * D;
             // a warp whose 32 rows are all padding skips the arithmetic but keeps the
@@ -404,27 +398,40 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const bool warp_live = quad * 32 < M;
             float m = -INFINITY, l = 0.f;
             for (int t = 0; t < ntiles; ++t, ++gt) {
-                const int valid = min(TK, key_end - (key_begin + t * TK));
+                const int valid = min(TK, cur.key_end - (cur.key_begin + t * TK));
                 ok = mbar_wait(&bars->s_full[gt & 1], (gt >> 1) & 1, abort_flag, kWaitTimeoutNs);
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
                 tc_fence_after();
                 if (warp_live) {
-                    uint32_t sr[TK];
-                    tmem_ld32(lane_base + C::S_COL + (gt & 1) * TK, cols32(sr));
-                    tmem_ld32(lane_base + C::S_COL + (gt & 1) * TK + 32, cols32(sr + 32));
-                    tmem_wait_ld();
-                    if (valid < TK) {
-#pragma unroll
-                        for (int c = 0; c < TK; ++c)
-                            if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
-                    }
-                    // row maximum of the raw scores, then scaled (the scale is positive)
+                    const uint32_t s_col = lane_base + C::S_COL + (gt & 1) * TK;
+                    // keys >= valid (a unit's partial last tile only) count as -inf: they take no part
+                    // in the maximum and their probability exp2(-inf) is 0
+                    const bool partial = valid < TK;
+                    const uint32_t ninf = __float_as_uint(-INFINITY);
+                    // pass 1: the row maximum of the raw scores, then scaled (the scale is positive)
                     float mp[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) mp[j] = __uint_as_float(sr[j]);
+                    for (int j = 0; j < 8; ++j) mp[j] = -INFINITY;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < TK; c0 += 64) {
+                        uint32_t sa[32], sb[32];
+                        tmem_ld32(s_col + c0, sa);
+                        tmem_ld32(s_col + c0 + 32, sb);
+                        tmem_wait_ld();
+                        if (partial) {
 #pragma unroll
-                    for (int c = 8; c < TK; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(sr[c]));
+                            for (int c = 0; c < 32; ++c) {
+                                if (c0 + c >= valid) sa[c] = ninf;
+                                if (c0 + 32 + c >= valid) sb[c] = ninf;
+                            }
+                        }
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(sa[c]));
+                            mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(sb[c]));
+                        }
+                    }
                     const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                                            fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * sl2;
                     // lazy maximum: keep the old one unless the row maximum grew by more than 2^8
@@ -438,18 +445,6 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         m = mx;
                         l *= alpha;
                     }
-                    // probabilities 2^(s * scale_log2 - m), their sum, and P packed in pairs in
-                    // place of the scores
-                    const float nm = -m;
-                    float rsp[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int c = 0; c < TK; c += 2) {
-                        const float p0 = exp2f(fmaf(__uint_as_float(sr[c]), sl2, nm));
-                        const float p1 = exp2f(fmaf(__uint_as_float(sr[c + 1]), sl2, nm));
-                        rsp[(c >> 1) & 3] += p0 + p1;
-                        sr[c >> 1] = pack2<BF16>(p0, p1);
-                    }
-                    l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
                     if (rescale) {
                         // O is rescaled only after P*V of the previous tile has finished; P*V of
                         // this tile waits for p_full. (Q*K^T of this tile completing implies P*V
@@ -469,9 +464,39 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                             }
                         }
                     }
-                    // P over the first TK/2 columns of this tile's S buffer: the A operand of P*V
-                    tmem_st32(lane_base + C::S_COL + (gt & 1) * TK, cols32(sr));
+                    // pass 2: probabilities 2^(s * scale_log2 - m) and their sum; P in 16-bit pairs
+                    // over the first TK/2 columns of this S buffer, 64 keys per store. P columns
+                    // [32i, 32i+32) overwrite score columns already read in this pass.
+                    const float nm = -m;
+                    float rsp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                    for (int c0 = 0; c0 < TK; c0 += 64) {
+                        uint32_t sa[32], sb[32], pk[32];
+                        tmem_ld32(s_col + c0, sa);
+                        tmem_ld32(s_col + c0 + 32, sb);
+                        tmem_wait_ld();
+                        if (partial) {
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) {
+                                if (c0 + c >= valid) sa[c] = ninf;
+                                if (c0 + 32 + c >= valid) sb[c] = ninf;
+                            }
+                        }
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            const float p0 = exp2f(fmaf(__uint_as_float(sa[c]), sl2, nm));
+                            const float p1 = exp2f(fmaf(__uint_as_float(sa[c + 1]), sl2, nm));
+                            const float p2 = exp2f(fmaf(__uint_as_float(sb[c]), sl2, nm));
+                            const float p3 = exp2f(fmaf(__uint_as_float(sb[c + 1]), sl2, nm));
+                            rsp[(c >> 1) & 1] += p0 + p1;
+                            rsp[2 + ((c >> 1) & 1)] += p2 + p3;
+                            pk[c >> 1] = pack2<BF16>(p0, p1);
+                            pk[16 + (c >> 1)] = pack2<BF16>(p2, p3);
+                        }
+                        tmem_st32(s_col + (c0 >> 1), pk);
+                    }
                     tmem_wait_st();
+                    l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
                 }
                 if (!ok) break;
                 if (valid < TK) {
@@ -521,41 +546,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         bool ok = true;
-        // Copies Q of the k-th unit of this CTA from shared memory (128-byte swizzle) into
-        // tensor-memory buffer k % 2, then releases the shared-memory buffer. Buffer k % 2 was
-        // last read by unit k - 2, whose epilogue (which saw all its MMAs complete) ran before.
-        auto copy_q = [&](int k) -> bool {
-            if (!__all_sync(FULL, mbar_wait(&bars->q_full, k & 1, abort_flag, kWaitTimeoutNs))) return false;
-            const uint8_t* qrow = smem + row * 128;
-#pragma unroll
-            for (int c0 = 0; c0 < D / 2; c0 += 32) {  // 32 columns = 64 elements = one region
-                uint32_t qr[32];
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(qrow + (c0 / 32) * (kRowsPerBlock * 128) +
-                                                                    ((cc ^ (row & 7)) << 4));
-                    qr[4 * cc] = v.x;
-                    qr[4 * cc + 1] = v.y;
-                    qr[4 * cc + 2] = v.z;
-                    qr[4 * cc + 3] = v.w;
-                }
-                tmem_st32(lane_base + C::QT_COL + (k & 1) * (D / 2) + c0, qr);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars->qt_full[k & 1]);
-                mbar_arrive(&bars->q_empty);
-            }
-            return true;
-        };
-        if (C::Q_IN_TMEM && nunits > 0) ok = copy_q(0);
         for (int k = 0; k < nunits && ok; ++k) {
-            if (C::Q_IN_TMEM && k + 1 < nunits) {
-                ok = copy_q(k + 1);
-                if (!ok) break;
-            }
             const UnitInfo cur = load_unit(p, u_begin + k);
             const int w0 = cur.rb * p.Wblk;
             const int M = min(p.Wblk, p.W - w0) * p.G;

@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include "bsp_internal.h"
+#include "bsp_ptx.cuh"
 #include "../../include/bsp.h"
 
 namespace bsp {
@@ -176,6 +177,8 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
 
         // ---- wait for the prompt kernel's partial states (returns at once when launched plainly)
         asm volatile("griddepcontrol.wait;" ::: "memory");
+        // the partial states are read coherently below (never through the read-only path, whose
+        // loads the compiler may move above the wait)
 
         // ---- merge with the prompt partial states by log-sum-exp (base 2), one round of loads
         float lse0[MAXP];
@@ -188,10 +191,10 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
             o0a[pi] = o0b[pi] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (active && nsplit > 0) {
                 const long long prow = (static_cast<long long>(part_off) * p.W + w) * p.Hq + h;
-                lse0[pi] = __ldg(p.part_lse + prow);
+                lse0[pi] = ld_dep(p.part_lse + prow);
                 const float4* po = reinterpret_cast<const float4*>(p.part_o + prow * D) + li * 2;
-                o0a[pi] = __ldg(po);
-                o0b[pi] = __ldg(po + 1);
+                o0a[pi] = ld_dep(po);
+                o0b[pi] = ld_dep(po + 1);
             }
         }
 #pragma unroll
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
             const float m = tm[pi], l = tl[pi];
             float Lmax = (l > 0.f) ? m + log2f(l) : -INFINITY;
             Lmax = fmaxf(Lmax, lse0[pi]);
-            for (int sp = 1; sp < nsplit; ++sp) Lmax = fmaxf(Lmax, __ldg(p.part_lse + prow + sp * pstride));
+            for (int sp = 1; sp < nsplit; ++sp) Lmax = fmaxf(Lmax, ld_dep(p.part_lse + prow + sp * pstride));
             float out[8];
             float lse2;
             if (Lmax == -INFINITY) {
@@ -223,10 +226,10 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
                         a0 = o0a[pi];
                         a1 = o0b[pi];
                     } else {
-                        lse_s = __ldg(p.part_lse + prow + sp * pstride);
+                        lse_s = ld_dep(p.part_lse + prow + sp * pstride);
                         const float4* po = reinterpret_cast<const float4*>(p.part_o + (prow + sp * pstride) * D) + li * 2;
-                        a0 = __ldg(po);
-                        a1 = __ldg(po + 1);
+                        a0 = ld_dep(po);
+                        a1 = ld_dep(po + 1);
                     }
                     const float wgt = exp2f(lse_s - Lmax);
                     out[0] = fmaf(wgt, a0.x, out[0]);
