@@ -24,6 +24,7 @@ FLAG_LSE_BASE2 = 1
 FLAG_CHECK = 2
 MAX_TAIL = 8
 MAX_GROUP = 8
+STATUS_BYTES = 256  # device status words ahead of the plan image in the workspace
 DEVFLAG_PAGE_INDEX = 1
 DEVFLAG_TIMEOUT = 2
 
@@ -52,7 +53,7 @@ class Plan(ctypes.Structure):
         ("ws_host", ctypes.c_void_p), ("image_bytes", ctypes.c_uint64), ("off_req", ctypes.c_uint64),
         ("off_units", ctypes.c_uint64), ("off_pages", ctypes.c_uint64), ("off_part_lse", ctypes.c_uint64),
         ("off_part_o", ctypes.c_uint64), ("device_bytes_used", ctypes.c_uint64),
-        ("reserved", ctypes.c_uint64 * 4)]
+        ("tail_requests", ctypes.c_int32), ("reserved0", ctypes.c_int32), ("reserved", ctypes.c_uint64 * 3)]
 
 
 _lib = None
@@ -159,6 +160,14 @@ def plan_build(geo: Geometry, batch, beam_width, prefix_len, tail_len, prefix_pa
         ctypes.byref(geo), int(batch), int(beam_width), _ptr(pl), _ptr(tl), _ptr(pp), pp.shape[1], int(max_tail),
         int(num_sms), _ptr(img), img.nbytes, ctypes.byref(plan)))
     return plan, img[:plan.image_bytes]
+
+
+def plan_requests(plan_: Plan, img: np.ndarray) -> np.ndarray:
+    """Per-request records of a host plan image (``plan_build``), int32 [batch, 8]: prompt length,
+    tail length, prompt partial states, first partial slot, first page entry, finished by the
+    prompt kernel (1) or by the tail kernel (0), two unused."""
+    lo = plan_.off_req - STATUS_BYTES
+    return img[lo:lo + plan_.batch * 32].view(np.int32).reshape(plan_.batch, 8)
 
 
 class Workspace:

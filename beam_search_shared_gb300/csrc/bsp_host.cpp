@@ -245,6 +245,11 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
         if (parts <= static_cast<int64_t>(batch) + kExtraParts) break;
         chunk *= 2;
     }
+    // a request is finished by the prompt kernel when its prompt is one partial state and its tail keys,
+    // for every row block (W_blk beams), fit one extra key tile
+    auto fused = [&](int b) -> bool {
+        return nsplit[b] == 1 && static_cast<int64_t>(tail_len[b]) * wblk <= prefix_tile_keys(geo->head_dim);
+    };
     struct Unit {
         int32_t f[kUnitFields];
     };
@@ -407,6 +412,7 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
         r[kReqSplits] = nsplit[b];
         r[kReqPartOff] = part_off[b];
         r[kReqPageOff] = page_off[b];
+        r[kReqFused] = fused(b) ? 1 : 0;
     }
     if (!units.empty()) std::memcpy(img + off_units, units.data(), units.size() * sizeof(Unit));
     std::memcpy(img + off_cta, cta_off.data(), cta_off.size() * 4);
@@ -432,6 +438,9 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
     out->num_sms = num_sms;
     out->max_tail_len = max_t;
     out->prefix_ctas = static_cast<int32_t>(ctas);
+    int32_t tail_requests = 0;
+    for (int b = 0; b < batch; ++b) tail_requests += !fused(b);
+    out->tail_requests = tail_requests;
     out->image_bytes = need;
     // offsets relative to the device workspace
     DeviceLayout L = device_layout(need, parts, beam_width, *geo);
@@ -589,6 +598,15 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
         if (!encode_map(&tq, geo.dtype, 3, q, qdims, qstr, qbox) || !encode_map(&tk, geo.dtype, 2, k_pool, kdims, kstr, kbox) ||
             !encode_map(&tv, geo.dtype, 2, v_pool, kdims, kstr, kbox))
             return BSP_ERR_CUDA;
+        pp.k_pool = k_pool;
+        pp.v_pool = v_pool;
+        pp.beam_pages = beam_pages;
+        pp.ci = cache_indirection;
+        pp.o = o;
+        pp.lse = lse;
+        pp.beam_pages_stride = beam_pages_stride;
+        pp.max_seq = max_seq;
+        pp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
         pp.units = reinterpret_cast<const int32_t*>(ws + plan->off_units);
         pp.cta_off = pp.units + static_cast<size_t>(plan->num_units) * kUnitFields;
         pp.req = reinterpret_cast<const int32_t*>(ws + plan->off_req);
@@ -635,7 +653,8 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
     if (prefix && launch_prefix(D, bf16, plan->prefix_ctas, tq, tk, tv, pp, s) != cudaSuccess) return BSP_ERR_CUDA;
     if (!record(1)) return BSP_ERR_CUDA;
     // without timing events between them, the tail kernel overlaps the end of the prompt kernel
-    if (launch_tail(D, bf16, plan->max_tail_len, tp, prefix && events == nullptr, s) != cudaSuccess)
+    if (plan->tail_requests > 0 &&
+        launch_tail(D, bf16, plan->max_tail_len, tp, prefix && events == nullptr, s) != cudaSuccess)
         return BSP_ERR_CUDA;
     if (!record(2)) return BSP_ERR_CUDA;
     if (flags & BSP_FLAG_CHECK) return bsp_read_device_status(plan, stream, 1, nullptr);

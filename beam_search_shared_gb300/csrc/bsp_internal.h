@@ -20,12 +20,25 @@ constexpr size_t kAlign = 256;
 // Plan image (int32 fields, offsets relative to the image start).
 constexpr int kImageHeaderBytes = 64;  // u64 generation, i32 batch, i32 num_units, ...
 // Per-request record.
-enum ReqField { kReqPrefix = 0, kReqTail = 1, kReqSplits = 2, kReqPartOff = 3, kReqPageOff = 4, kReqFields = 8 };
+// kReqFused: the prompt kernel finishes the request (one prompt partial state, and every row block's tail
+// keys fit one extra key tile of the prompt kernel); the tail kernel skips it.
+enum ReqField { kReqPrefix = 0, kReqTail = 1, kReqSplits = 2, kReqPartOff = 3, kReqPageOff = 4, kReqFused = 5,
+                kReqFields = 8 };
+// keys per tile of the prompt kernel, which bounds a row block's tail keys for the fused tail
+constexpr int prefix_tile_keys(int head_dim) { return head_dim <= 128 ? 128 : 64; }
 // Per-work-unit record: request, kv head, query-row block, key tiles [kt0, kt1), partial slot.
 enum UnitField { kUnitReq = 0, kUnitKvHead = 1, kUnitRowBlock = 2, kUnitTile0 = 3, kUnitTile1 = 4, kUnitPart = 5,
                  kUnitFields = 8 };
 
 struct PrefixParams {
+    // fused requests: tail keys gathered by the prompt kernel, final O / LSE written by it
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* beam_pages;
+    const int32_t* ci;
+    void* o;
+    float* lse;
+    int beam_pages_stride, max_seq, lse_base2;
     const int32_t* units;    // [num_units][kUnitFields], grouped by CTA
     const int32_t* cta_off;  // [gridDim.x + 1]: CTA c runs units cta_off[c] .. cta_off[c+1]-1
     const int32_t* req;

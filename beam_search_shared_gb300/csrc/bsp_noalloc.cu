@@ -157,6 +157,15 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
             !noalloc_encode(&tv, geo->dtype, 2, v_pool, kdims, kstr, kbox))
             return BSP_ERR_CUDA;
         PrefixParams pp{};
+        pp.k_pool = k_pool;
+        pp.v_pool = v_pool;
+        pp.beam_pages = beam_pages;
+        pp.ci = cache_indirection;
+        pp.o = o;
+        pp.lse = lse;
+        pp.beam_pages_stride = beam_pages_stride;
+        pp.max_seq = max_seq;
+        pp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
         pp.units = reinterpret_cast<const int32_t*>(ws + plan.off_units);
         pp.cta_off = pp.units + static_cast<size_t>(plan.num_units) * kUnitFields;
         pp.req = reinterpret_cast<const int32_t*>(ws + plan.off_req);
@@ -200,8 +209,8 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
     tp.max_seq = max_seq;
     tp.scale_log2 = softmax_scale * log2e;
     tp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
-    if (prepare_tail(D, bf16, plan.max_tail_len, Hq) != cudaSuccess ||
-        launch_tail(D, bf16, plan.max_tail_len, tp, plan.num_units > 0, s) != cudaSuccess)
+    if (plan.tail_requests > 0 && (prepare_tail(D, bf16, plan.max_tail_len, Hq) != cudaSuccess ||
+                                   launch_tail(D, bf16, plan.max_tail_len, tp, plan.num_units > 0, s) != cudaSuccess))
         return BSP_ERR_CUDA;
     if (flags & BSP_FLAG_CHECK) {
         int32_t dflags = 0;

@@ -43,7 +43,16 @@
 //              maximum and sum to the epilogue warps at the end of a unit;
 //   warps 6-9  epilogue: once a unit's last P*V is done, write the normalised
 //              fp32 partial O and its log2-sum-exp2, then release that O
-//              buffer.
+//              buffer. For a request the plan marks fused (its prompt is one
+//              key range and each row block's beams hold at most TK tail keys
+//              together) the unit ends with a tail tile: the epilogue warps
+//              resolve each tail key through cache_indirection and the beam's
+//              page table, copy its K and V rows into the ring slots the
+//              producer leaves free (16-byte cp.async into the swizzled layout
+//              a TMA box would have; absent keys are zero rows), and publish a
+//              key -> pool-row table; the softmax keeps only a row's own beam's
+//              keys of that tile. Such a unit writes the final O (q dtype) and
+//              LSE of its rows, and the tail kernel skips the request.
 // TMEM columns: S0 [0,TK), S1 [TK,2TK) (P_t aliases the first TK/2 columns of
 // S[t%2]: tcgen05.mma instructions issued by one thread execute in issue
 // order, and the Q*K^T that overwrites S[t%2] is issued after the P*V that
@@ -74,7 +83,8 @@ struct PrefixCfg {
     static constexpr int OFF_K = NQ * Q_BYTES;
     static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
     static constexpr int OFF_STATS = OFF_V + VST * KV_BYTES;  // float m[128], l[128]
-    static constexpr int OFF_BAR = OFF_STATS + 2 * kRowsPerBlock * 4;
+    static constexpr int OFF_TROW = OFF_STATS + 2 * kRowsPerBlock * 4;  // int pool row of tail key c [TK]
+    static constexpr int OFF_BAR = OFF_TROW + TK * 4;
     static constexpr int SMEM = OFF_BAR + 512 + 1024;        // barriers + alignment slack
     static constexpr int S_COL = 0;                          // S[0], S[1]: TK fp32 columns each
     static constexpr int O_COL = 2 * TK;                     // O[0] (, O[1]): D fp32 columns each
@@ -82,6 +92,8 @@ struct PrefixCfg {
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(O_COL + NO * D <= 512, "tensor memory");
     static_assert(TK % 64 == 0 && TK / 16 <= 8 && D / 16 <= 16, "tile shape");
+    static_assert(TK == prefix_tile_keys(D), "the host's fused-tail bound");
+    static constexpr int TAIL_CHUNKS = TK * (D / 8) / 128;  // 16-byte chunks per epilogue thread and tensor
     static constexpr int THREADS = 320;
 };
 
@@ -99,6 +111,9 @@ struct PrefixBarriers {
     uint64_t o_free[2];   // the epilogue of unit k has read O[k % NO]
     uint64_t st_full;     // row statistics of a unit written
     uint64_t st_empty;    // ... and read by the epilogue warps
+    uint64_t tail_go[2];    // tail tile n: its K and V ring slots are free (the producer)
+    uint64_t fill_done[2];  // ... each epilogue warp has stored its part of it
+    uint64_t tail_ready[2]; // ... and it is complete, with its key table (for the softmax)
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -110,6 +125,8 @@ constexpr uint64_t kDrainNs = 200000000ull;
 struct UnitInfo {
     int b, g, rb, part, P, page_off;
     int key_begin, key_end;  // keys [key_begin, key_end) of the request's prompt
+    int T;                   // tail positions of the request
+    bool fused;              // this kernel finishes the request: a tail tile when T > 0, final O / LSE
 };
 
 __device__ __forceinline__ UnitInfo load_unit(const PrefixParams& p, int u) {
@@ -126,12 +143,22 @@ __device__ __forceinline__ UnitInfo load_unit(const PrefixParams& p, int u) {
     ui.page_off = r2.x;
     ui.key_begin = a.w * kTileKeys;                // plan tiles are kTileKeys keys
     ui.key_end = min(c.x * kTileKeys, ui.P);
+    ui.T = r.y;
+    ui.fused = r2.y != 0;                            // kReqFused
     return ui;
 }
 
+// prompt tiles of a unit
+template <int TK>
+__device__ __forceinline__ int prompt_tiles(const UnitInfo& ui) {
+    return (ui.key_end - ui.key_begin + TK - 1) / TK;
+}
+// a fused unit with tail positions ends with one tile of its beams' tail keys, beam-major:
+// key column c = w_local * T + t
+__device__ __forceinline__ bool has_tail_tile(const UnitInfo& ui) { return ui.fused && ui.T > 0; }
 template <int TK>
 __device__ __forceinline__ int unit_tiles(const UnitInfo& ui) {
-    return (ui.key_end - ui.key_begin + TK - 1) / TK;
+    return prompt_tiles<TK>(ui) + (has_tail_tile(ui) ? 1 : 0);
 }
 
 template <bool BF16>
@@ -159,6 +186,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     auto v_tile = [&](int gt) -> uint8_t* { return smem + C::OFF_V + (gt % VST) * C::KV_BYTES; };
     float* st_m = reinterpret_cast<float*>(smem + C::OFF_STATS);  // [128]
     float* st_l = st_m + kRowsPerBlock;                            // [128]
+    int* s_trow = reinterpret_cast<int*>(smem + C::OFF_TROW);     // [TK] pool row of tail key, -1: none
     PrefixBarriers* bars = reinterpret_cast<PrefixBarriers*>(smem + C::OFF_BAR);
     volatile int* abort_flag = &bars->abort_flag;
 
@@ -191,6 +219,11 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         mbar_init(&bars->st_full, 4);   // one arrival per softmax warp
         mbar_init(&bars->st_empty, 4);  // one arrival per epilogue warp
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->tail_go[i], 1);
+            mbar_init(&bars->fill_done[i], 4);  // one arrival per epilogue warp
+            mbar_init(&bars->tail_ready[i], 1);
+        }
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -221,7 +254,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (warp == 0) {
         // ================= TMA producer =================
         const int BR = ps < kTileKeys ? ps : kTileKeys;  // rows per box (a page, or 64 rows of a larger page)
-        int gt = 0, k = 0;
+        int gt = 0, k = 0, ntail = 0;
         bool ok = true;
         for (int u = u_begin; u < u_end && ok; ++u, ++k) {
             const UnitInfo ui = load_unit(p, u);
@@ -238,6 +271,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                 ui.b * p.W + ui.rb * p.Wblk);
             }
             const int ntiles = unit_tiles<TK>(ui);
+            const int ptiles = prompt_tiles<TK>(ui);
             const int* pg = p.pages + ui.page_off;
             const int npages = (ui.P + ps - 1) >> p.ps_log2;
             int win_base = -1, my_page = 0;
@@ -246,6 +280,18 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     ok = mbar_wait(&bars->k_empty[gt % KST], ((gt / KST) - 1) & 1, abort_flag, kWaitTimeoutNs);
                     ok = __all_sync(FULL, ok);
                     if (!ok) break;
+                }
+                if (t == ptiles) {
+                    // the unit's tail tile: the epilogue warps gather it once both slots are free
+                    if (gt >= VST) {
+                        ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kWaitTimeoutNs);
+                        ok = __all_sync(FULL, ok);
+                        if (!ok) break;
+                    }
+                    if (lane == 0) mbar_arrive(&bars->tail_go[ntail & 1]);
+                    ++ntail;
+                    __syncwarp();
+                    continue;
                 }
                 const int key0 = ui.key_begin + t * TK;
                 const int valid = min(TK, ui.key_end - key0);
@@ -387,28 +433,69 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const float sl2 = p.scale_log2;
         bool ok = true;
-        int gt = 0;
+        int gt = 0, ntail = 0;
         for (int k = 0; k < nunits && ok; ++k) {
             const UnitInfo cur = load_unit(p, u_begin + k);
             const int ntiles = unit_tiles<TK>(cur);
+            const int ptiles = prompt_tiles<TK>(cur);
             const int M = min(p.Wblk, p.W - cur.rb * p.Wblk) * p.G;
+            // the row's own beam's keys in the tail tile: columns [lo, lo + T)
+            const int lo = (row / p.G) * cur.T, hi = lo + cur.T;
             const uint32_t o_col = C::O_COL + (k % NO) * D;
             // a warp whose 32 rows are all padding skips the arithmetic but keeps the
             // barrier protocol (the p_full ordering below keeps its arrivals in the right phase)
             const bool warp_live = quad * 32 < M;
             float m = -INFINITY, l = 0.f;
             for (int t = 0; t < ntiles; ++t, ++gt) {
-                const int valid = min(TK, cur.key_end - (cur.key_begin + t * TK));
+                const bool tail = t == ptiles;  // the tail tile (zero-filled past its keys)
+                const int valid = tail ? TK : min(TK, cur.key_end - (cur.key_begin + t * TK));
                 ok = mbar_wait(&bars->s_full[gt & 1], (gt >> 1) & 1, abort_flag, kWaitTimeoutNs);
+                if (ok && tail) {
+                    // the tail tile's key table (pool row per column, -1: none or unreadable)
+                    ok = mbar_wait(&bars->tail_ready[ntail & 1], (ntail >> 1) & 1, abort_flag, kWaitTimeoutNs);
+                    ++ntail;
+                }
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
                 tc_fence_after();
                 if (warp_live) {
                     const uint32_t s_col = lane_base + C::S_COL + (gt & 1) * TK;
-                    // keys >= valid (a unit's partial last tile only) count as -inf: they take no part
-                    // in the maximum and their probability exp2(-inf) is 0
-                    const bool partial = valid < TK;
+                    // masked keys count as -inf: they take no part in the maximum and their probability
+                    // exp2(-inf) is 0. A prompt tile masks keys >= P_b (a unit's partial last tile only),
+                    // the tail tile every key but the row's own beam's readable ones.
+                    const bool partial = valid < TK || tail;
                     const uint32_t ninf = __float_as_uint(-INFINITY);
+                    // kept columns of a partial tile, one bit per key: [0, valid) of a prompt tile; of the
+                    // tail tile the row's own beam's columns [lo, lo + T) (T <= 8, so they span at most two
+                    // 32-bit words) whose key is readable
+                    uint32_t km[TK / 32];
+                    if (partial) {
+                        uint64_t win = 0;
+                        const int wbase = lo & ~31;
+                        if (tail)
+                            for (int c = lo; c < hi && c < TK; ++c)
+                                if (s_trow[c] >= 0) win |= 1ull << (c - wbase);
+#pragma unroll
+                        for (int j = 0; j < TK / 32; ++j) {
+                            const int n = min(max(valid - 32 * j, 0), 32);
+                            const uint32_t pm = n == 32 ? ~0u : (1u << n) - 1u;
+                            const uint32_t tm = 32 * j == wbase        ? static_cast<uint32_t>(win)
+                                                : 32 * j == wbase + 32 ? static_cast<uint32_t>(win >> 32)
+                                                                       : 0u;
+                            km[j] = tail ? tm : pm;
+                        }
+                    }
+                    // the two mask words of columns [c0, c0 + 64) (c0 is 0 or 64)
+                    auto mask_pair = [&](int c0, uint32_t& ma, uint32_t& mb) {
+                        ma = km[0];
+                        mb = km[1];
+                        if constexpr (TK > 64) {
+                            if (c0 != 0) {
+                                ma = km[2];
+                                mb = km[3];
+                            }
+                        }
+                    };
                     // pass 1: the row maximum of the raw scores, then scaled (the scale is positive)
                     float mp[8];
 #pragma unroll
@@ -420,10 +507,12 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         tmem_ld32(s_col + c0 + 32, sb);
                         tmem_wait_ld();
                         if (partial) {
+                            uint32_t ma, mb;
+                            mask_pair(c0, ma, mb);
 #pragma unroll
                             for (int c = 0; c < 32; ++c) {
-                                if (c0 + c >= valid) sa[c] = ninf;
-                                if (c0 + 32 + c >= valid) sb[c] = ninf;
+                                sa[c] = (ma >> c) & 1u ? sa[c] : ninf;
+                                sb[c] = (mb >> c) & 1u ? sb[c] : ninf;
                             }
                         }
 #pragma unroll
@@ -476,10 +565,12 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         tmem_ld32(s_col + c0 + 32, sb);
                         tmem_wait_ld();
                         if (partial) {
+                            uint32_t ma, mb;
+                            mask_pair(c0, ma, mb);
 #pragma unroll
                             for (int c = 0; c < 32; ++c) {
-                                if (c0 + c >= valid) sa[c] = ninf;
-                                if (c0 + 32 + c >= valid) sb[c] = ninf;
+                                sa[c] = (ma >> c) & 1u ? sa[c] : ninf;
+                                sb[c] = (mb >> c) & 1u ? sb[c] : ninf;
                             }
                         }
 #pragma unroll
@@ -542,12 +633,90 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
     } else {
         // ================= epilogue warps =================
+        constexpr int CH = D / 8;               // 16-byte chunks of a K or V row
+        constexpr int RPW = 32 / CH;            // tail-tile rows a warp covers per gather step
+        constexpr int RS = kRowsPerBlock / CH;  // row step between one thread's gather steps
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        // tail-tile gather: thread (quad, lane) copies chunk kc = lane % CH of rows
+        // quad*RPW + lane/CH + i*RS (i < TAIL_CHUNKS); each lane resolves the pool row of one of the
+        // warp's rows (lrow), and the thread copying row quad*RPW + lane/CH + i*RS takes it from lane
+        // i*RPW + lane/CH
+        const int kc = lane % CH;
+        const int lrow = quad * RPW + lane % RPW + (lane / RPW) * RS;
+        const bool lrow_ok = lane / RPW < C::TAIL_CHUNKS;
+        // pool row of the tail key in column lrow of unit ui's tail tile (column c = w_local * T + t is
+        // position P_b + t of beam w0 + w_local, read through cache_indirection); -1 past the unit's
+        // keys or when the source beam or its page is out of range
+        auto tail_row = [&](const UnitInfo& ui) -> int {
+            const int w0 = ui.rb * p.Wblk;
+            const int nkeys = min(p.Wblk, p.W - w0) * ui.T;
+            if (!lrow_ok || lrow >= nkeys) return -1;
+            const int wl = lrow / ui.T, t = lrow - wl * ui.T;
+            const int pos = ui.P + t;
+            const int src = __ldg(p.ci + (static_cast<long long>(ui.b) * p.W + w0 + wl) * p.max_seq + pos);
+            int r = -1;
+            if (static_cast<unsigned>(src) < static_cast<unsigned>(p.W)) {
+                const int page = __ldg(p.beam_pages + (static_cast<long long>(ui.b) * p.W + src) * p.beam_pages_stride +
+                                       (pos >> p.ps_log2));
+                if (static_cast<unsigned>(page) < static_cast<unsigned>(p.num_pages))
+                    r = ((page * p.Hkv + ui.g) << p.ps_log2) + (pos & (ps - 1));
+            }
+            if (r < 0) atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
+            return r;
+        };
+        const uint16_t* k_pool = static_cast<const uint16_t*>(p.k_pool);
+        const uint16_t* v_pool = static_cast<const uint16_t*>(p.v_pool);
         bool ok = true;
+        int gt = 0, ntail = 0;
+        UnitInfo cur;
+        int trow = -1;  // this lane's resolved tail row (lrow) of the unit `cur`
+        if (nunits > 0) {
+            cur = load_unit(p, u_begin);
+            if (has_tail_tile(cur)) trow = tail_row(cur);
+        }
         for (int k = 0; k < nunits && ok; ++k) {
-            const UnitInfo cur = load_unit(p, u_begin + k);
+            if (has_tail_tile(cur)) {
+                // gather the unit's tail tile into the K and V ring slots the producer left for it.
+                // s_trow is free: the softmax finished the previous unit (its statistics were read).
+                const int gtt = gt + prompt_tiles<TK>(cur);
+                if (lrow_ok) s_trow[lrow] = trow;
+                ok = mbar_wait(&bars->tail_go[ntail & 1], (ntail >> 1) & 1, abort_flag, kWaitTimeoutNs);
+                ok = __all_sync(FULL, ok);
+                if (!ok) break;
+                uint8_t* kt = k_tile(gtt);
+                uint8_t* vt = v_tile(gtt);
+#pragma unroll 4
+                for (int i = 0; i < C::TAIL_CHUNKS; ++i) {
+                    const int r = __shfl_sync(FULL, trow, i * RPW + lane / CH);
+                    const int c = quad * RPW + lane / CH + i * RS;
+                    // the layout of a TMA box with 128-byte swizzle: chunk kc of row c in column half kc/8
+                    const uint32_t off = (kc >> 3) * (TK * 128) + c * 128 + (((kc & 7) ^ (c & 7)) << 4);
+                    const long long e = static_cast<long long>(r < 0 ? 0 : r) * D + kc * 8;
+                    const uint32_t nb = r < 0 ? 0u : 16u;  // absent keys are zero rows
+                    cp_async16(kt + off, k_pool + e, nb);
+                    cp_async16(vt + off, v_pool + e, nb);
+                }
+                cp_async_commit_wait_all();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->fill_done[ntail & 1]);
+                if (quad == 0) {
+                    if (lane == 0) {
+                        ok = mbar_wait(&bars->fill_done[ntail & 1], (ntail >> 1) & 1, abort_flag, kWaitTimeoutNs);
+                        if (ok) {
+                            mbar_arrive(&bars->k_full[gtt % KST]);
+                            mbar_arrive(&bars->v_full[gtt % VST]);
+                            mbar_arrive(&bars->tail_ready[ntail & 1]);
+                        }
+                    }
+                    ok = __all_sync(FULL, ok);
+                    if (!ok) break;
+                }
+                ++ntail;
+            }
+            gt += unit_tiles<TK>(cur);
             const int w0 = cur.rb * p.Wblk;
             const int M = min(p.Wblk, p.W - w0) * p.G;
             const bool warp_live = quad * 32 < M;
@@ -559,29 +728,62 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const float l = st_l[row];
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->st_empty);
+            // resolve the next unit's tail keys while this unit's last P*V runs
+            const UnitInfo done = cur;
+            if (k + 1 < nunits) {
+                cur = load_unit(p, u_begin + k + 1);
+                trow = has_tail_tile(cur) ? tail_row(cur) : -1;
+            }
             ok = mbar_wait(&bars->o_final[k & 1], (k >> 1) & 1, abort_flag, kWaitTimeoutNs);
             ok = __all_sync(FULL, ok);
             if (!ok) break;
             tc_fence_after();
             const int wl = row / p.G, jh = row % p.G;
-            const long long prow = (static_cast<long long>(cur.part) * p.W + (w0 + wl)) * p.Hq + cur.g * p.G + jh;
-            float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
             const float inv = 1.0f / l;
             const uint32_t o_col = C::O_COL + (k % NO) * D;
+            if (done.fused) {
+                // the request's whole key set went through this unit: the final O (q dtype) and LSE
+                const long long rh = (static_cast<long long>(done.b) * p.W + (w0 + wl)) * p.Hq + done.g * p.G + jh;
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + rh * D);
 #pragma unroll 1
-            for (int c0 = 0; c0 < D && warp_live; c0 += 32) {
-                uint32_t orr[32];
-                tmem_ld32(lane_base + o_col + c0, orr);
-                tmem_wait_ld();
-                if (live) {
+                for (int c0 = 0; c0 < D && warp_live; c0 += 32) {
+                    uint32_t orr[32];
+                    tmem_ld32(lane_base + o_col + c0, orr);
+                    tmem_wait_ld();
+                    if (live) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        dst[(c0 >> 2) + e] =
-                            make_float4(__uint_as_float(orr[4 * e]) * inv, __uint_as_float(orr[4 * e + 1]) * inv,
-                                        __uint_as_float(orr[4 * e + 2]) * inv, __uint_as_float(orr[4 * e + 3]) * inv);
+                        for (int e = 0; e < 4; ++e) {
+                            const float* f = reinterpret_cast<const float*>(orr) + 8 * e;
+                            dst[(c0 >> 3) + e] = make_uint4(pack2<BF16>(f[0] * inv, f[1] * inv),
+                                                            pack2<BF16>(f[2] * inv, f[3] * inv),
+                                                            pack2<BF16>(f[4] * inv, f[5] * inv),
+                                                            pack2<BF16>(f[6] * inv, f[7] * inv));
+                        }
+                    }
                 }
+                if (live) {
+                    const float lse2 = m + log2f(l);
+                    p.lse[rh] = p.lse_base2 ? lse2 : lse2 * 0.69314718055994530942f;
+                }
+            } else {
+                const long long prow =
+                    (static_cast<long long>(done.part) * p.W + (w0 + wl)) * p.Hq + done.g * p.G + jh;
+                float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
+#pragma unroll 1
+                for (int c0 = 0; c0 < D && warp_live; c0 += 32) {
+                    uint32_t orr[32];
+                    tmem_ld32(lane_base + o_col + c0, orr);
+                    tmem_wait_ld();
+                    if (live) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[(c0 >> 2) + e] =
+                                make_float4(__uint_as_float(orr[4 * e]) * inv, __uint_as_float(orr[4 * e + 1]) * inv,
+                                            __uint_as_float(orr[4 * e + 2]) * inv, __uint_as_float(orr[4 * e + 3]) * inv);
+                    }
+                }
+                if (live) p.part_lse[prow] = m + log2f(l);
             }
-            if (live) p.part_lse[prow] = m + log2f(l);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->o_free[k & 1]);

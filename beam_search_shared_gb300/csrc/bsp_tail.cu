@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
     const int lane = tid & 31;
     const int4 rq = __ldg(reinterpret_cast<const int4*>(p.req + b * kReqFields));
     const int P = rq.x, T = rq.y, nsplit = rq.z, part_off = rq.w;
+    if (__ldg(p.req + b * kReqFields + kReqFused)) return;  // the prompt kernel finished this request
 
     // ---- resolve the row's tail positions once (source beam, page, slot)
     if (tid < T) {

@@ -50,6 +50,14 @@ class DeviceStep:
                                  self.max_tail, stream=stream)
         return self.plan
 
+    def fused_requests(self) -> np.ndarray:
+        """Which requests the prompt kernel finishes, from a host-only plan of the same inputs."""
+        c = self.case
+        wl = c.workload
+        plan, img = bsp.plan_build(self.geo, wl.batch, wl.beam_width, c.prefix_len, c.tail_len, c.prefix_pages,
+                                   self.max_tail, self.plan.num_sms)
+        return bsp.plan_requests(plan, img)[:, 5] != 0
+
     def append(self, events=None, stream=None):
         bsp.append_kv(self.plan, self.k_new, self.v_new, self.out_cache_loc, self.k_pool, self.v_pool,
                       events=events, stream=stream)
@@ -62,16 +70,19 @@ class DeviceStep:
         """plan + append (full steps) + attention, then the device status (syncs)."""
         self.make_plan(stream)
         if self.case.full_step:
-            self.append(stream)
+            self.append(stream=stream)
         self.attend(flags, stream=stream)
         return bsp.read_device_status(self.plan, clear=True, stream=stream)
 
 
-def algorithmic_bytes(case: Case) -> dict:
+def algorithmic_bytes(case: Case, fused: Optional[np.ndarray] = None) -> dict:
     """Bytes each kernel must move at least once, from the drawn lengths.
 
-    prefix: valid K+V prompt rows once per (request, kv head) + Q + fp32 partial O/LSE write;
-    tail:   gathered K+V tail rows per (beam, kv head) + Q + partial read + O/LSE write;
+    fused[b]: request b is finished by the prompt kernel (default: none is).
+    prefix: valid K+V prompt rows once per (request, kv head) + Q; per request either the fp32
+            partial O/LSE write or, when fused, its beams' K+V tail rows + the final O/LSE write;
+    tail:   for the other requests, gathered K+V tail rows per (beam, kv head) + Q + partial
+            read + O/LSE write;
     append: read + write of the new K and V rows.
     """
     wl = case.workload
@@ -79,16 +90,22 @@ def algorithmic_bytes(case: Case) -> dict:
     D, Hq, Hkv, W = wl.head_dim, wl.num_q_heads, wl.num_kv_heads, wl.beam_width
     P = case.prefix_len.astype(np.int64)
     T = case.tail_len.astype(np.int64)
-    R = wl.batch * W
+    B = wl.batch
+    fz = np.zeros(B, bool) if fused is None else np.asarray(fused, bool)
     active = P > 0
-    prefix_kv = int(np.sum(P)) * Hkv * D * e * 2
-    q_bytes = R * Hq * D * e
-    part = int(np.sum(active)) * W * Hq * (D + 1) * 4
-    prefix = prefix_kv + int(np.sum(active)) * W * Hq * D * e + part
-    tail_kv = int(np.sum(T)) * W * Hkv * D * e * 2
-    tail = tail_kv + q_bytes + part + R * Hq * (D * e + 4)
+    row_kv = Hkv * D * e * 2              # K + V of one position, every kv head
+    row_q = Hq * D * e                    # one beam row's queries
+    row_part = Hq * (D + 1) * 4           # one beam row's fp32 partial O and LSE
+    row_out = Hq * (D * e + 4)            # one beam row's final O and LSE
+    prefix_kv = int(np.sum(P)) * row_kv
+    pa = active & ~fz
+    prefix = (prefix_kv + int(np.sum(active)) * W * row_q + int(np.sum(pa)) * W * row_part
+              + int(np.sum(T[fz])) * W * row_kv + int(np.sum(fz)) * W * row_out)
+    tl = ~fz
+    tail = (int(np.sum(T[tl])) * W * row_kv + int(np.sum(tl)) * W * (row_q + row_out)
+            + int(np.sum(pa)) * W * row_part)
     n = int(case.out_cache_loc.shape[0])
     append = n * Hkv * D * e * 2 * 2
-    flops = int(np.sum(P)) * W * Hq * D * 4
+    flops = (int(np.sum(P)) + int(np.sum(T[fz]))) * W * Hq * D * 4
     return {"prefix": prefix, "tail": tail, "append": append, "prefix_flops": flops,
             "prefix_kv": prefix_kv}

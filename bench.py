@@ -262,7 +262,8 @@ def main():
         st.make_plan()
         sets.append(st)
     torch.cuda.synchronize()
-    ab = [algorithmic_bytes(s.case) for s in sets]
+    ab = [algorithmic_bytes(s.case, s.fused_requests()) for s in sets]
+    tail_launch = [s.plan.tail_requests > 0 for s in sets]
     stream = torch.cuda.current_stream()
 
     def step(i, events=None):
@@ -342,7 +343,11 @@ def main():
     prefix_bytes = statistics.mean(a["prefix"] for a in ab)
     prefix_ms = statistics.mean(t_pre)
     achieved = prefix_bytes / (prefix_ms / 1e3) / 1e9
-    tail_gbs = statistics.mean(a["tail"] for a in ab) / (statistics.mean(t_tail) / 1e3) / 1e9
+    # the tail kernel is launched only for plans with requests the prompt kernel does not finish
+    t_tail_l = [t for i, t in enumerate(t_tail) if tail_launch[i % len(sets)]]
+    tail_ab = [a["tail"] for a, tl in zip(ab, tail_launch) if tl]
+    tail_us = 1e3 * statistics.mean(t_tail_l) if t_tail_l else None
+    tail_gbs = statistics.mean(tail_ab) / (tail_us / 1e6) / 1e9 if t_tail_l else None
     app_gbs = statistics.mean(a["append"] for a in ab) / (statistics.mean(t_app) / 1e3) / 1e9
     prefix_tflops = statistics.mean(a["prefix_flops"] for a in ab) / (prefix_ms / 1e3) / 1e12
     traffic = profiled_traffic(wl.name)
@@ -362,7 +367,7 @@ def main():
                    "l2": f"inputs larger than L2: {len(sets)} rotated input sets, each step moving "
                          f"{(prefix_bytes + statistics.mean(a['tail'] for a in ab)) / 1e6:.0f} MB",
                    "us_append": 1e3 * statistics.mean(t_app), "us_prefix": 1e3 * prefix_ms,
-                   "us_tail_merge": 1e3 * statistics.mean(t_tail),
+                   "us_tail_merge": tail_us,
                    "gbs_append": app_gbs, "gbs_tail_merge": tail_gbs, "prefix_tflops": prefix_tflops,
                    "prefix_units": sets[0].plan.num_units},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
@@ -370,7 +375,8 @@ def main():
                      "kernel": "prefix_attn_kernel", "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": prefix_bytes},
         "e2e": e2e,
-        "gpu_launches": K * (2 + (1 if sets[0].plan.num_units > 0 else 0)),
+        "gpu_launches": sum(1 + (s.plan.num_units > 0) + (s.plan.tail_requests > 0)
+                            for s in (sets[j % len(sets)] for j in range(K))),
         "timing": "value: CUDA-graph replay of exactly K steps without timing nodes; per-kernel times: a separate "
                   f"replay of {Kt} steps with an event pair around each kernel (upper bounds: an event node delays "
                   "the next launch by several microseconds)",

@@ -125,7 +125,12 @@ typedef struct bsp_plan_t {
     uint64_t off_part_lse;
     uint64_t off_part_o;
     uint64_t device_bytes_used;
-    uint64_t reserved[4];
+    int32_t tail_requests;       /* requests the tail kernel finishes (no prompt, a prompt split over
+                                    several partial states, or more tail keys per row block than one
+                                    tile holds); the prompt kernel finishes the others. No tail launch
+                                    when 0 */
+    int32_t reserved0;
+    uint64_t reserved[3];
 } bsp_plan_t;
 
 /* Human-readable name of a bsp_status value. Never NULL. */

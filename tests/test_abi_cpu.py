@@ -115,6 +115,15 @@ def decode_image(plan, img, with_cta=False):
     return req, units, pages
 
 
+def check_fused(plan, req, T, head_dim=128):
+    """A request is finished by the prompt kernel iff it has one prompt partial state and each row
+    block's tail keys fit one prompt-kernel tile (128 keys up to head_dim 128, 64 at 256)."""
+    tile = 128 if head_dim <= 128 else 64
+    want = (req[:, 2] == 1) & (np.asarray(T) * plan.beams_per_block <= tile)
+    np.testing.assert_array_equal(req[:, 5], want.astype(np.int32))
+    assert plan.tail_requests == int((~want).sum())
+
+
 def check_units_cover(plan, req, units, P, tile=64):
     """Every (request, kv head, row block) covers its prompt tiles exactly once."""
     B, Hkv, nrb = plan.batch, plan.geo.num_kv_heads, plan.row_blocks
@@ -155,6 +164,8 @@ def test_plan_image_wide_batch_needs_no_split(lib):
     np.testing.assert_array_equal(req[:, 1], T)
     np.testing.assert_array_equal(req[:, 2], 1)
     check_units_cover(plan, req, units, P)
+    check_fused(plan, req, T)
+    assert plan.tail_requests == 0                          # 30 beams x <= 4 tail keys fit one tile
     assert plan.prefix_ctas == 152 and len(cta_off) == 153
     assert cta_off[0] == 0 and cta_off[-1] == plan.num_units and np.all(np.diff(cta_off) >= 1)
     tiles = units[:, 4] - units[:, 3]
@@ -180,6 +191,12 @@ def test_plan_image_wide_beam_row_blocks(lib):
     assert plan.row_blocks == 2 and plan.beams_per_block == 48    # 192 rows -> 2 x 96
     check_units_cover(plan, req, units, P)
     assert req[2][2] == 0                                            # empty prompt: no split, no unit
+    check_fused(plan, req, T)
+    assert req[2][5] == 0 and plan.tail_requests >= 1
+    plan, img = bsp.plan_build(geo(npages=200), B, W, P, [3, 2, 1], pages, 8, 152)
+    req, _, _ = decode_image(plan, img)
+    check_fused(plan, req, [3, 2, 1])                                # 48 x 3 tail keys exceed a tile
+    assert req[0][5] == 0
 
 
 def test_plan_image_single_long_request_is_split(lib):
@@ -194,6 +211,8 @@ def test_plan_image_single_long_request_is_split(lib):
     check_units_cover(plan, req, units, P)
     lens = units[:, 4] - units[:, 3]
     assert lens.max() - lens.min() <= 1
+    check_fused(plan, req, [1])
+    assert plan.tail_requests == 1                                   # split prompt: merged by the tail kernel
 
 
 def test_plan_image_empty_batch_and_empty_prompts(lib):
@@ -201,6 +220,7 @@ def test_plan_image_empty_batch_and_empty_prompts(lib):
     assert plan.num_units == 0 and plan.batch == 0
     plan, img = bsp.plan_build(geo(), 2, 4, [0, 0], [1, 3], np.zeros((2, 1), np.int32), 8, 152)
     assert plan.num_units == 0 and plan.num_parts == 0 and plan.max_tail_len == 3
+    assert plan.tail_requests == 2
 
 
 def test_plan_struct_layout_matches_header(lib):

@@ -156,6 +156,20 @@ def test_tail_lengths_mixed_and_boundary_crossing():
     run_and_check(case)
 
 
+@pytest.mark.parametrize("name", ["qwen3_0p6b_b64_w30", "qwen3_4b_fp16_d64", "qwen3_4b_fp16_d128",
+                                  "qwen3_4b_fp16_d256"])
+def test_prompt_kernel_finishes_short_requests(name):
+    """Requests with one prompt partial state and few tail keys per row block are finished by the
+    prompt kernel (tail keys gathered as one extra key tile); the others, in the same batch, by
+    the tail kernel."""
+    wl = synth.WORKLOADS[name].scaled(6)
+    # 60 + 5 tail keys x 30 beams exceed a tile; 3000 keys are split over partial states
+    case = synth.make_case(wl, 84, full_step=True, device="cuda", prompt_lengths=[100, 128, 60, 3000, 31, 7],
+                           tail_lengths=[2, 0, 5, 2, 2, 1])
+    step = run_and_check(case)
+    assert step.plan.tail_requests == 2
+
+
 def test_empty_sequences():
     """P = 0 and T = 0 rows give O = 0 and LSE = -inf; other rows are unaffected."""
     wl = synth.WORKLOADS["qwen3_0p6b_b64_w30"].scaled(3).with_(beam_width=4)
