@@ -253,6 +253,15 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
     struct Unit {
         int32_t f[kUnitFields];
     };
+    // time of a unit on the prompt kernel, in eighths of a key tile: its TK-key tiles (the last one
+    // partial, costed in full), its tail tile, and half a tile for the unit's start and end
+    const int tk = prefix_tile_keys(geo->head_dim);
+    auto unit_cost = [&](int b, int32_t t0, int32_t t1) -> int64_t {
+        const int64_t keys = std::min<int64_t>(static_cast<int64_t>(t1) * kTileKeys, prefix_len[b]) -
+                             static_cast<int64_t>(t0) * kTileKeys;
+        const int64_t kt = ceil_div(keys, tk) + ((fused(b) && tail_len[b] > 0) ? 1 : 0);
+        return 8 * kt + 4;
+    };
     std::vector<Unit> units;
     units.reserve(static_cast<size_t>(parts * Hkv * nrb));
     std::vector<int32_t> part_off(batch), page_off(batch);
@@ -272,13 +281,14 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
                     u.f[kUnitTile0] = t0;
                     u.f[kUnitTile1] = t1;
                     u.f[kUnitPart] = static_cast<int32_t>(poff + s);
+                    u.f[kUnitCost] = static_cast<int32_t>(unit_cost(b, t0, t1));
                     units.push_back(u);
                 }
         }
         poff += nsplit[b];
         pgoff += ceil_div(prefix_len[b], ps);
     }
-    // Units go to the persistent CTAs so that the largest per-CTA tile count is small.
+    // Units go to the persistent CTAs so that the largest per-CTA cost (unit_cost) is small.
     // Longest units first (row blocks of one split stay adjacent: equal keys keep their
     // order); LPT (each unit to the least-loaded CTA) gives an upper bound L on the largest
     // load, then MULTIFIT (Coffman, Garey & Johnson 1978) looks for the smallest capacity
@@ -286,12 +296,11 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
     // few units per CTA, LPT alone can stack four short units on one CTA while others hold
     // three long ones. The list is written grouped by CTA; cta_off[c] .. cta_off[c+1] are
     // CTA c's units, longest first.
-    std::stable_sort(units.begin(), units.end(), [](const Unit& a, const Unit& c) {
-        return (a.f[kUnitTile1] - a.f[kUnitTile0]) > (c.f[kUnitTile1] - c.f[kUnitTile0]);
-    });
+    std::stable_sort(units.begin(), units.end(),
+                     [](const Unit& a, const Unit& c) { return a.f[kUnitCost] > c.f[kUnitCost]; });
     if (units.size() > static_cast<size_t>(std::numeric_limits<int32_t>::max())) return BSP_ERR_UNSUPPORTED;
     const int64_t nu = static_cast<int64_t>(units.size());
-    auto utiles = [&](int64_t i) -> int64_t { return units[i].f[kUnitTile1] - units[i].f[kUnitTile0]; };
+    auto utiles = [&](int64_t i) -> int64_t { return units[i].f[kUnitCost]; };
     std::vector<std::vector<int32_t>> lists;
     if (nu > 0) {
         const int64_t bins = std::min<int64_t>(nu, num_sms);

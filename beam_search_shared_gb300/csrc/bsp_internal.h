@@ -26,9 +26,10 @@ enum ReqField { kReqPrefix = 0, kReqTail = 1, kReqSplits = 2, kReqPartOff = 3, k
                 kReqFields = 8 };
 // keys per tile of the prompt kernel, which bounds a row block's tail keys for the fused tail
 constexpr int prefix_tile_keys(int head_dim) { return head_dim <= 128 ? 128 : 64; }
-// Per-work-unit record: request, kv head, query-row block, key tiles [kt0, kt1), partial slot.
+// Per-work-unit record: request, kv head, query-row block, key tiles [kt0, kt1), partial slot, and
+// the cost the host dealt it by (eighths of a prompt-kernel key tile; not read by the kernels).
 enum UnitField { kUnitReq = 0, kUnitKvHead = 1, kUnitRowBlock = 2, kUnitTile0 = 3, kUnitTile1 = 4, kUnitPart = 5,
-                 kUnitFields = 8 };
+                 kUnitCost = 6, kUnitFields = 8 };
 
 struct PrefixParams {
     // fused requests: tail keys gathered by the prompt kernel, final O / LSE written by it

@@ -502,13 +502,16 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     for (int j = 0; j < 8; ++j) mp[j] = -INFINITY;
 #pragma unroll 1
                     for (int c0 = 0; c0 < TK; c0 += 64) {
+                        uint32_t ma = ~0u, mb = ~0u;
+                        if (partial) {
+                            mask_pair(c0, ma, mb);
+                            if (!__any_sync(FULL, (ma | mb) != 0u)) continue;  // no row of the warp keeps one
+                        }
                         uint32_t sa[32], sb[32];
                         tmem_ld32(s_col + c0, sa);
                         tmem_ld32(s_col + c0 + 32, sb);
                         tmem_wait_ld();
-                        if (partial) {
-                            uint32_t ma, mb;
-                            mask_pair(c0, ma, mb);
+                        if (partial && __any_sync(FULL, (ma & mb) != ~0u)) {
 #pragma unroll
                             for (int c = 0; c < 32; ++c) {
                                 sa[c] = (ma >> c) & 1u ? sa[c] : ninf;
@@ -560,13 +563,21 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     float rsp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
                     for (int c0 = 0; c0 < TK; c0 += 64) {
-                        uint32_t sa[32], sb[32], pk[32];
+                        uint32_t ma = ~0u, mb = ~0u;
+                        if (partial) mask_pair(c0, ma, mb);
+                        uint32_t pk[32];
+                        if (partial && !__any_sync(FULL, (ma | mb) != 0u)) {
+                            // every key of these 64 columns is masked for the warp's rows: P = 0
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) pk[c] = 0u;
+                            tmem_st32(s_col + (c0 >> 1), pk);
+                            continue;
+                        }
+                        uint32_t sa[32], sb[32];
                         tmem_ld32(s_col + c0, sa);
                         tmem_ld32(s_col + c0 + 32, sb);
                         tmem_wait_ld();
-                        if (partial) {
-                            uint32_t ma, mb;
-                            mask_pair(c0, ma, mb);
+                        if (partial && __any_sync(FULL, (ma & mb) != ~0u)) {
 #pragma unroll
                             for (int c = 0; c < 32; ++c) {
                                 sa[c] = (ma >> c) & 1u ? sa[c] : ninf;
@@ -663,7 +674,16 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 if (static_cast<unsigned>(page) < static_cast<unsigned>(p.num_pages))
                     r = ((page * p.Hkv + ui.g) << p.ps_log2) + (pos & (ps - 1));
             }
-            if (r < 0) atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
+            if (r < 0) {
+                atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
+            } else {
+                // the gather runs a few tiles later: bring the row's K and V into L2 now
+#pragma unroll
+                for (int off = 0; off < D * 2; off += 128) {
+                    prefetch_l2(static_cast<const uint8_t*>(p.k_pool) + static_cast<long long>(r) * (D * 2) + off);
+                    prefetch_l2(static_cast<const uint8_t*>(p.v_pool) + static_cast<long long>(r) * (D * 2) + off);
+                }
+            }
             return r;
         };
         const uint16_t* k_pool = static_cast<const uint16_t*>(p.k_pool);

@@ -168,12 +168,16 @@ def test_plan_image_wide_batch_needs_no_split(lib):
     assert plan.tail_requests == 0                          # 30 beams x <= 4 tail keys fit one tile
     assert plan.prefix_ctas == 152 and len(cta_off) == 153
     assert cta_off[0] == 0 and cta_off[-1] == plan.num_units and np.all(np.diff(cta_off) >= 1)
-    tiles = units[:, 4] - units[:, 3]
-    per_cta = np.array([tiles[cta_off[c]:cta_off[c + 1]].sum() for c in range(152)])
-    assert per_cta.max() <= per_cta.mean() + tiles.max()    # greedy dealing balances the persistent CTAs
+    # dealing cost: eighths of a 128-key tile, for the unit's key tiles, its tail tile and half a tile
+    keys = np.minimum(units[:, 4] * 64, P[units[:, 0]]) - units[:, 3] * 64
+    want = 8 * (-(-keys // 128) + (T[units[:, 0]] > 0)) + 4
+    np.testing.assert_array_equal(units[:, 6], want)
+    cost = units[:, 6]
+    per_cta = np.array([cost[cta_off[c]:cta_off[c + 1]].sum() for c in range(152)])
+    assert per_cta.max() <= per_cta.mean() + cost.max()    # greedy dealing balances the persistent CTAs
     # no worse than dealing each unit, longest first, to the least-loaded CTA
     lpt = np.zeros(152, np.int64)
-    for x in sorted(tiles.tolist(), reverse=True):
+    for x in sorted(cost.tolist(), reverse=True):
         lpt[np.argmin(lpt)] += x
     assert per_cta.max() <= lpt.max()
     for b in range(B):
