@@ -598,7 +598,10 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
     if (prefix) {
         cuuint64_t qdims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(R)};
         cuuint64_t qstr[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2};
-        cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(plan->beams_per_block)};
+        // query rows per TMA box: the row block, or a quadrant's share of it (half-row softmax)
+        const int qbeams = prefix_quad_beams(D, plan->beams_per_block, G);
+        cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(G),
+                              static_cast<cuuint32_t>(qbeams > 0 ? qbeams : plan->beams_per_block)};
         const int ps = geo.page_size;
         // pools viewed as 2-D [pool row][head_dim]; one box = min(page, 64) rows x 64 columns
         cuuint64_t kdims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(geo.num_pages) * Hkv * ps};
@@ -629,6 +632,7 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
         pp.G = G;
         pp.ps_log2 = ilog2(ps);
         pp.Wblk = plan->beams_per_block;
+        pp.bq = qbeams;
         pp.num_pages = geo.num_pages;
         pp.num_units = plan->num_units;
         pp.scale_log2 = softmax_scale * log2e;

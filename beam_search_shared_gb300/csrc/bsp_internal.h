@@ -26,6 +26,14 @@ enum ReqField { kReqPrefix = 0, kReqTail = 1, kReqSplits = 2, kReqPartOff = 3, k
                 kReqFields = 8 };
 // keys per tile of the prompt kernel, which bounds a row block's tail keys for the fused tail
 constexpr int prefix_tile_keys(int head_dim) { return head_dim <= 128 ? 128 : 64; }
+// Beams per TMEM lane quadrant when the prompt kernel places a row block's query rows in lanes
+// 0-15 of each quadrant and gives each row two softmax threads (half of the keys each): the
+// block's beams spread over the four quadrants, at most 16 rows each, with 128-key tiles. 0 when
+// the block does not fit that way (the rows then fill the lanes densely, one thread per row).
+constexpr int prefix_quad_beams(int head_dim, int beams_per_block, int group) {
+    const int bq = (beams_per_block + 3) / 4;
+    return (prefix_tile_keys(head_dim) == 128 && bq * group <= 16) ? bq : 0;
+}
 // Per-work-unit record: request, kv head, query-row block, key tiles [kt0, kt1), partial slot, and
 // the cost the host dealt it by (eighths of a prompt-kernel key tile; not read by the kernels).
 enum UnitField { kUnitReq = 0, kUnitKvHead = 1, kUnitRowBlock = 2, kUnitTile0 = 3, kUnitTile1 = 4, kUnitPart = 5,
@@ -48,6 +56,7 @@ struct PrefixParams {
     float* part_lse;  // [part][W][Hq]      (log2-sum-exp2 of the scaled scores)
     int32_t* status;
     int W, Hq, Hkv, G, ps_log2, Wblk, num_pages;
+    int bq;            // > 0: half-row softmax, bq beams of the block per TMEM lane quadrant (prefix_quad_beams)
     int num_units;     // units in the list
     float scale_log2;  // softmax_scale * log2(e)
 };

@@ -148,7 +148,10 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
         CUtensorMap tq, tk, tv;
         cuuint64_t qdims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(R)};
         cuuint64_t qstr[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2};
-        cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(plan.beams_per_block)};
+        // query rows per TMA box: the row block, or a quadrant's share of it (half-row softmax)
+        const int qbeams = prefix_quad_beams(D, plan.beams_per_block, G);
+        cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(G),
+                              static_cast<cuuint32_t>(qbeams > 0 ? qbeams : plan.beams_per_block)};
         cuuint64_t kdims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(geo->num_pages) * Hkv * ps};
         cuuint64_t kstr[1] = {static_cast<cuuint64_t>(D) * 2};
         cuuint32_t kbox[2] = {64, static_cast<cuuint32_t>(ps < kTileKeys ? ps : kTileKeys)};
@@ -179,6 +182,7 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
         pp.G = G;
         pp.ps_log2 = noalloc_log2(ps);
         pp.Wblk = plan.beams_per_block;
+        pp.bq = qbeams;
         pp.num_pages = geo->num_pages;
         pp.num_units = plan.num_units;
         pp.scale_log2 = softmax_scale * log2e;

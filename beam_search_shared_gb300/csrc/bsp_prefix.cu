@@ -172,13 +172,31 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool SPLIT>
 __global__ void __launch_bounds__(320, 1)
 prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefixParams p) {
     using C = PrefixCfg<D>;
     constexpr int TK = C::TK, NC = C::NC, NQ = C::NQ, KST = C::KST, VST = C::VST, NO = C::NO;
     constexpr unsigned FULL = 0xffffffffu;
+    static_assert(!SPLIT || TK == 128, "half-row softmax: 128-key tiles");
+    // Score, probability and output columns a thread handles: all of its row's (dense), or half of
+    // them with two threads per row (SPLIT: query rows in TMEM lanes 0-15 of each quadrant, threads
+    // t and t + 16 of a warp on the same row through the 16x32bx2 access shape)
+    constexpr int HC = SPLIT ? TK / 2 : TK;
+    constexpr int HD = SPLIT ? D / 2 : D;
+    auto ld_s = [](uint32_t a, uint32_t(&r)[32]) {
+        if constexpr (SPLIT) tmem_ld16x2_32<TK / 2>(a, r); else tmem_ld32(a, r);
+    };
+    auto st_p = [](uint32_t a, const uint32_t(&r)[32]) {
+        if constexpr (SPLIT) tmem_st16x2_32<TK / 4>(a, r); else tmem_st32(a, r);
+    };
+    auto ld_o = [](uint32_t a, uint32_t(&r)[32]) {
+        if constexpr (SPLIT) tmem_ld16x2_32<D / 2>(a, r); else tmem_ld32(a, r);
+    };
+    auto st_o = [](uint32_t a, const uint32_t(&r)[32]) {
+        if constexpr (SPLIT) tmem_st16x2_32<D / 2>(a, r); else tmem_st32(a, r);
+    };
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     auto q_buf = [&](int k) -> uint8_t* { return smem + (k % NQ) * C::Q_BYTES; };
@@ -232,15 +250,15 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         prefetch_tmap(&tm_v);
     }
     if (warp == 1) tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
-    // zero the query rows no TMA box covers, so padded rows stay finite
+    // zero the query rows no TMA box covers, so padded rows stay finite: rows past W_blk * G, or
+    // (SPLIT) the rows of each 32-row quadrant past its bq * G
     {
-        const int filled = p.Wblk * p.G;
-        const int nz = (kRowsPerBlock - filled) * 8;  // 16-byte chunks per region
-        for (int qb = 0; qb < NQ; ++qb)
-            for (int c = 0; c < NC; ++c)
-                for (int idx = tid; idx < nz; idx += C::THREADS)
-                    reinterpret_cast<uint4*>(q_buf(qb) + c * kRowsPerBlock * 128 + filled * 128)[idx] =
-                        make_uint4(0, 0, 0, 0);
+        constexpr int NCHUNK = NQ * NC * kRowsPerBlock * 8;  // 16-byte chunks of the Q buffers
+        for (int idx = tid; idx < NCHUNK; idx += C::THREADS) {
+            const int r = (idx >> 3) % kRowsPerBlock;
+            const bool covered = SPLIT ? (r & 31) < p.bq * p.G : r < p.Wblk * p.G;
+            if (!covered) reinterpret_cast<uint4*>(smem)[idx] = make_uint4(0, 0, 0, 0);
+        }
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -265,10 +283,19 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 if (!ok) break;
             }
             if (lane == 0) {
-                mbar_arrive_expect_tx(&bars->q_full[qb], NC * p.Wblk * p.G * 128);
-                for (int c = 0; c < NC; ++c)
-                    tma_load_3d(q_buf(k) + c * kRowsPerBlock * 128, &tm_q, &bars->q_full[qb], c * 64, ui.g * p.G,
-                                ui.b * p.W + ui.rb * p.Wblk);
+                if constexpr (SPLIT) {
+                    // quadrant i's rows 32i .. 32i + bq*G - 1: beams i*bq .. of the block (box [bq][G][64])
+                    mbar_arrive_expect_tx(&bars->q_full[qb], NC * 4 * p.bq * p.G * 128);
+                    for (int c = 0; c < NC; ++c)
+                        for (int i = 0; i < 4; ++i)
+                            tma_load_3d(q_buf(k) + c * kRowsPerBlock * 128 + i * 32 * 128, &tm_q, &bars->q_full[qb],
+                                        c * 64, ui.g * p.G, ui.b * p.W + ui.rb * p.Wblk + i * p.bq);
+                } else {
+                    mbar_arrive_expect_tx(&bars->q_full[qb], NC * p.Wblk * p.G * 128);
+                    for (int c = 0; c < NC; ++c)
+                        tma_load_3d(q_buf(k) + c * kRowsPerBlock * 128, &tm_q, &bars->q_full[qb], c * 64,
+                                    ui.g * p.G, ui.b * p.W + ui.rb * p.Wblk);
+                }
             }
             const int ntiles = unit_tiles<TK>(ui);
             const int ptiles = prompt_tiles<TK>(ui);
@@ -429,7 +456,10 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     } else if (warp < 6) {
         // ================= softmax warps =================
         const int quad = warp & 3;  // TMEM lane quadrant this warp may access
-        const int row = quad * 32 + lane;
+        const int half = SPLIT ? lane >> 4 : 0;                 // which half of the row's columns
+        const int row = quad * 32 + (SPLIT ? (lane & 15) : lane);  // TMEM lane of the thread's query row
+        // beam (within the row block) of the row
+        const int beam = SPLIT ? quad * p.bq + (lane & 15) / p.G : row / p.G;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const float sl2 = p.scale_log2;
         bool ok = true;
@@ -438,13 +468,13 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const UnitInfo cur = load_unit(p, u_begin + k);
             const int ntiles = unit_tiles<TK>(cur);
             const int ptiles = prompt_tiles<TK>(cur);
-            const int M = min(p.Wblk, p.W - cur.rb * p.Wblk) * p.G;
+            const int nw = min(p.Wblk, p.W - cur.rb * p.Wblk);  // beams of the block
             // the row's own beam's keys in the tail tile: columns [lo, lo + T)
-            const int lo = (row / p.G) * cur.T, hi = lo + cur.T;
+            const int lo = beam * cur.T, hi = lo + cur.T;
             const uint32_t o_col = C::O_COL + (k % NO) * D;
             // a warp whose 32 rows are all padding skips the arithmetic but keeps the
             // barrier protocol (the p_full ordering below keeps its arrivals in the right phase)
-            const bool warp_live = quad * 32 < M;
+            const bool warp_live = SPLIT ? quad * p.bq < nw : quad * 32 < nw * p.G;
             float m = -INFINITY, l = 0.f;
             for (int t = 0; t < ntiles; ++t, ++gt) {
                 const bool tail = t == ptiles;  // the tail tile (zero-filled past its keys)
@@ -485,7 +515,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                             km[j] = tail ? tm : pm;
                         }
                     }
-                    // the two mask words of columns [c0, c0 + 64) (c0 is 0 or 64)
+                    // the two mask words of tile columns [c0, c0 + 64) (c0 is 0 or 64)
                     auto mask_pair = [&](int c0, uint32_t& ma, uint32_t& mb) {
                         ma = km[0];
                         mb = km[1];
@@ -501,15 +531,15 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
                     for (int j = 0; j < 8; ++j) mp[j] = -INFINITY;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < TK; c0 += 64) {
+                    for (int c0 = 0; c0 < HC; c0 += 64) {
                         uint32_t ma = ~0u, mb = ~0u;
                         if (partial) {
-                            mask_pair(c0, ma, mb);
+                            mask_pair(c0 + half * HC, ma, mb);
                             if (!__any_sync(FULL, (ma | mb) != 0u)) continue;  // no row of the warp keeps one
                         }
                         uint32_t sa[32], sb[32];
-                        tmem_ld32(s_col + c0, sa);
-                        tmem_ld32(s_col + c0 + 32, sb);
+                        ld_s(s_col + c0, sa);
+                        ld_s(s_col + c0 + 32, sb);
                         tmem_wait_ld();
                         if (partial && __any_sync(FULL, (ma & mb) != ~0u)) {
 #pragma unroll
@@ -524,8 +554,10 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                             mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(sb[c]));
                         }
                     }
-                    const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                                           fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * sl2;
+                    float mxr = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                      fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+                    if constexpr (SPLIT) mxr = fmaxf(mxr, __shfl_xor_sync(FULL, mxr, 16));  // the row's other half
+                    const float mx = mxr * sl2;
                     // lazy maximum: keep the old one unless the row maximum grew by more than 2^8
                     const bool need = t > 0 && mx > m + 8.0f;
                     const bool rescale = __any_sync(FULL, need);
@@ -546,13 +578,13 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         if (ok) {
                             tc_fence_after();
 #pragma unroll 1
-                            for (int c0 = 0; c0 < D; c0 += 32) {
+                            for (int c0 = 0; c0 < HD; c0 += 32) {
                                 uint32_t orr[32];
-                                tmem_ld32(lane_base + o_col + c0, orr);
+                                ld_o(lane_base + o_col + c0, orr);
                                 tmem_wait_ld();
 #pragma unroll
                                 for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                                tmem_st32(lane_base + o_col + c0, orr);
+                                st_o(lane_base + o_col + c0, orr);
                             }
                         }
                     }
@@ -562,20 +594,20 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     const float nm = -m;
                     float rsp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-                    for (int c0 = 0; c0 < TK; c0 += 64) {
+                    for (int c0 = 0; c0 < HC; c0 += 64) {
                         uint32_t ma = ~0u, mb = ~0u;
-                        if (partial) mask_pair(c0, ma, mb);
+                        if (partial) mask_pair(c0 + half * HC, ma, mb);
                         uint32_t pk[32];
                         if (partial && !__any_sync(FULL, (ma | mb) != 0u)) {
                             // every key of these 64 columns is masked for the warp's rows: P = 0
 #pragma unroll
                             for (int c = 0; c < 32; ++c) pk[c] = 0u;
-                            tmem_st32(s_col + (c0 >> 1), pk);
+                            st_p(s_col + (c0 >> 1), pk);
                             continue;
                         }
                         uint32_t sa[32], sb[32];
-                        tmem_ld32(s_col + c0, sa);
-                        tmem_ld32(s_col + c0 + 32, sb);
+                        ld_s(s_col + c0, sa);
+                        ld_s(s_col + c0 + 32, sb);
                         tmem_wait_ld();
                         if (partial && __any_sync(FULL, (ma & mb) != ~0u)) {
 #pragma unroll
@@ -595,7 +627,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                             pk[c >> 1] = pack2<BF16>(p0, p1);
                             pk[16 + (c >> 1)] = pack2<BF16>(p2, p3);
                         }
-                        tmem_st32(s_col + (c0 >> 1), pk);
+                        st_p(s_col + (c0 >> 1), pk);
                     }
                     tmem_wait_st();
                     l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
@@ -633,8 +665,11 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
             }
-            st_m[row] = m;
-            st_l[row] = l;
+            if constexpr (SPLIT) l += __shfl_xor_sync(FULL, l, 16);  // the row's other half
+            if (half == 0) {
+                st_m[row] = m;
+                st_l[row] = l;
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->st_full);
         }
@@ -648,7 +683,6 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         constexpr int RPW = 32 / CH;            // tail-tile rows a warp covers per gather step
         constexpr int RS = kRowsPerBlock / CH;  // row step between one thread's gather steps
         const int quad = warp & 3;
-        const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         // tail-tile gather: thread (quad, lane) copies chunk kc = lane % CH of rows
         // quad*RPW + lane/CH + i*RS (i < TAIL_CHUNKS); each lane resolves the pool row of one of the
@@ -738,14 +772,20 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
             gt += unit_tiles<TK>(cur);
             const int w0 = cur.rb * p.Wblk;
-            const int M = min(p.Wblk, p.W - w0) * p.G;
-            const bool warp_live = quad * 32 < M;
-            const bool live = row < M;
+            const int nw = min(p.Wblk, p.W - w0);
+            // the thread's query row: TMEM lane orow, beam wl of the block, head jh of the group; with
+            // SPLIT two threads per row, each writing half of its columns
+            const int r16 = lane & 15, ohalf = SPLIT ? lane >> 4 : 0;
+            const int orow = quad * 32 + (SPLIT ? r16 : lane);
+            const int wl = SPLIT ? quad * p.bq + r16 / p.G : orow / p.G;
+            const int jh = SPLIT ? r16 % p.G : orow % p.G;
+            const bool warp_live = SPLIT ? quad * p.bq < nw : quad * 32 < nw * p.G;
+            const bool live = SPLIT ? (r16 < p.bq * p.G && wl < nw) : orow < nw * p.G;
             ok = mbar_wait(&bars->st_full, k & 1, abort_flag, kWaitTimeoutNs);
             ok = __all_sync(FULL, ok);
             if (!ok) break;
-            const float m = st_m[row];
-            const float l = st_l[row];
+            const float m = st_m[orow];
+            const float l = st_l[orow];
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->st_empty);
             // resolve the next unit's tail keys while this unit's last P*V runs
@@ -758,30 +798,30 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             ok = __all_sync(FULL, ok);
             if (!ok) break;
             tc_fence_after();
-            const int wl = row / p.G, jh = row % p.G;
             const float inv = 1.0f / l;
             const uint32_t o_col = C::O_COL + (k % NO) * D;
+            const int cb = ohalf * HD;  // first output column of the thread
             if (done.fused) {
                 // the request's whole key set went through this unit: the final O (q dtype) and LSE
                 const long long rh = (static_cast<long long>(done.b) * p.W + (w0 + wl)) * p.Hq + done.g * p.G + jh;
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + rh * D);
 #pragma unroll 1
-                for (int c0 = 0; c0 < D && warp_live; c0 += 32) {
+                for (int c0 = 0; c0 < HD && warp_live; c0 += 32) {
                     uint32_t orr[32];
-                    tmem_ld32(lane_base + o_col + c0, orr);
+                    ld_o(lane_base + o_col + c0, orr);
                     tmem_wait_ld();
                     if (live) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float* f = reinterpret_cast<const float*>(orr) + 8 * e;
-                            dst[(c0 >> 3) + e] = make_uint4(pack2<BF16>(f[0] * inv, f[1] * inv),
+                            dst[((cb + c0) >> 3) + e] = make_uint4(pack2<BF16>(f[0] * inv, f[1] * inv),
                                                             pack2<BF16>(f[2] * inv, f[3] * inv),
                                                             pack2<BF16>(f[4] * inv, f[5] * inv),
                                                             pack2<BF16>(f[6] * inv, f[7] * inv));
                         }
                     }
                 }
-                if (live) {
+                if (live && ohalf == 0) {
                     const float lse2 = m + log2f(l);
                     p.lse[rh] = p.lse_base2 ? lse2 : lse2 * 0.69314718055994530942f;
                 }
@@ -790,19 +830,19 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     (static_cast<long long>(done.part) * p.W + (w0 + wl)) * p.Hq + done.g * p.G + jh;
                 float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
 #pragma unroll 1
-                for (int c0 = 0; c0 < D && warp_live; c0 += 32) {
+                for (int c0 = 0; c0 < HD && warp_live; c0 += 32) {
                     uint32_t orr[32];
-                    tmem_ld32(lane_base + o_col + c0, orr);
+                    ld_o(lane_base + o_col + c0, orr);
                     tmem_wait_ld();
                     if (live) {
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            dst[(c0 >> 2) + e] =
+                            dst[((cb + c0) >> 2) + e] =
                                 make_float4(__uint_as_float(orr[4 * e]) * inv, __uint_as_float(orr[4 * e + 1]) * inv,
                                             __uint_as_float(orr[4 * e + 2]) * inv, __uint_as_float(orr[4 * e + 3]) * inv);
                     }
                 }
-                if (live) p.part_lse[prow] = m + log2f(l);
+                if (live && ohalf == 0) p.part_lse[prow] = m + log2f(l);
             }
             tc_fence_before();
             __syncwarp();
@@ -822,22 +862,39 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
 }
 
-template <int D, bool BF16>
-static cudaError_t prepare_prefix_t() {
+template <int D, bool BF16, bool SPLIT>
+static cudaError_t prepare_prefix_k() {
     using C = PrefixCfg<D>;
     static_assert(sizeof(PrefixBarriers) <= 512, "barrier block");
     static_assert(C::SMEM <= 227 * 1024, "shared memory");
-    cudaError_t e = cudaFuncSetAttribute(prefix_attn_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(prefix_attn_kernel<D, BF16, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(prefix_attn_kernel<D, BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    return cudaFuncSetAttribute(prefix_attn_kernel<D, BF16, SPLIT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                 cudaSharedmemCarveoutMaxShared);
+}
+
+// the half-row variant exists for 128-key tiles (head_dim <= 128)
+template <int D, bool BF16>
+static cudaError_t prepare_prefix_t() {
+    cudaError_t e = prepare_prefix_k<D, BF16, false>();
+    if constexpr (PrefixCfg<D>::TK == 128)
+        if (e == cudaSuccess) e = prepare_prefix_k<D, BF16, true>();
+    return e;
 }
 
 template <int D, bool BF16>
 static cudaError_t launch_prefix_t(int ctas, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                    const PrefixParams& p, cudaStream_t stream) {
     using C = PrefixCfg<D>;
-    prefix_attn_kernel<D, BF16><<<ctas, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+    if constexpr (C::TK == 128) {
+        if (p.bq > 0) {
+            prefix_attn_kernel<D, BF16, true><<<ctas, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+            return cudaGetLastError();
+        }
+    }
+    if (p.bq > 0) return cudaErrorInvalidValue;
+    prefix_attn_kernel<D, BF16, false><<<ctas, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
