@@ -71,14 +71,17 @@
 
 namespace bsp {
 
-template <int D>
+// SPLIT: the half-row layout, whose MMAs have M = 64 (the accumulator's 64 rows sit in TMEM
+// lanes 0-15 of each quadrant), so a Q buffer holds 64 rows and the K ring gets a third slot
+template <int D, bool SPLIT>
 struct PrefixCfg {
     static constexpr int TK = D <= 128 ? 128 : 64;            // keys per tile
     static constexpr int NC = D / 64;                        // 128-byte column regions per row
     static constexpr int NQ = D <= 128 ? 2 : 1;              // Q buffers
-    static constexpr int KST = D == 64 ? 4 : 2;              // K ring depth
+    static constexpr int MR = SPLIT ? 64 : kRowsPerBlock;    // MMA M: query rows of a Q buffer
+    static constexpr int KST = D == 64 ? (SPLIT ? 6 : 4) : (SPLIT ? 3 : 2);  // K ring depth
     static constexpr int VST = D == 64 ? 7 : 3;              // V ring depth
-    static constexpr int Q_BYTES = kRowsPerBlock * D * 2;    // NC regions of 128 rows x 128 B
+    static constexpr int Q_BYTES = MR * D * 2;               // NC regions of MR rows x 128 B
     static constexpr int KV_BYTES = TK * D * 2;              // one K (or V) tile
     static constexpr int OFF_K = NQ * Q_BYTES;
     static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
@@ -176,8 +179,8 @@ template <int D, bool BF16, bool SPLIT>
 __global__ void __launch_bounds__(320, 1)
 prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefixParams p) {
-    using C = PrefixCfg<D>;
-    constexpr int TK = C::TK, NC = C::NC, NQ = C::NQ, KST = C::KST, VST = C::VST, NO = C::NO;
+    using C = PrefixCfg<D, SPLIT>;
+    constexpr int TK = C::TK, NC = C::NC, NQ = C::NQ, KST = C::KST, VST = C::VST, NO = C::NO, MR = C::MR;
     constexpr unsigned FULL = 0xffffffffu;
     static_assert(!SPLIT || TK == 128, "half-row softmax: 128-key tiles");
     // Score, probability and output columns a thread handles: all of its row's (dense), or half of
@@ -251,12 +254,12 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
     if (warp == 1) tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
     // zero the query rows no TMA box covers, so padded rows stay finite: rows past W_blk * G, or
-    // (SPLIT) the rows of each 32-row quadrant past its bq * G
+    // (SPLIT) the rows of each 16-row quadrant block past its bq * G
     {
-        constexpr int NCHUNK = NQ * NC * kRowsPerBlock * 8;  // 16-byte chunks of the Q buffers
+        constexpr int NCHUNK = NQ * NC * MR * 8;  // 16-byte chunks of the Q buffers
         for (int idx = tid; idx < NCHUNK; idx += C::THREADS) {
-            const int r = (idx >> 3) % kRowsPerBlock;
-            const bool covered = SPLIT ? (r & 31) < p.bq * p.G : r < p.Wblk * p.G;
+            const int r = (idx >> 3) % MR;
+            const bool covered = SPLIT ? (r & 15) < p.bq * p.G : r < p.Wblk * p.G;
             if (!covered) reinterpret_cast<uint4*>(smem)[idx] = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
@@ -284,16 +287,17 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
             if (lane == 0) {
                 if constexpr (SPLIT) {
-                    // quadrant i's rows 32i .. 32i + bq*G - 1: beams i*bq .. of the block (box [bq][G][64])
+                    // M rows 16i .. 16i + bq*G - 1 (TMEM lanes 32i ..): beams i*bq .. of the block (box
+                    // [bq][G][64])
                     mbar_arrive_expect_tx(&bars->q_full[qb], NC * 4 * p.bq * p.G * 128);
                     for (int c = 0; c < NC; ++c)
                         for (int i = 0; i < 4; ++i)
-                            tma_load_3d(q_buf(k) + c * kRowsPerBlock * 128 + i * 32 * 128, &tm_q, &bars->q_full[qb],
+                            tma_load_3d(q_buf(k) + c * MR * 128 + i * 16 * 128, &tm_q, &bars->q_full[qb],
                                         c * 64, ui.g * p.G, ui.b * p.W + ui.rb * p.Wblk + i * p.bq);
                 } else {
                     mbar_arrive_expect_tx(&bars->q_full[qb], NC * p.Wblk * p.G * 128);
                     for (int c = 0; c < NC; ++c)
-                        tma_load_3d(q_buf(k) + c * kRowsPerBlock * 128, &tm_q, &bars->q_full[qb], c * 64,
+                        tma_load_3d(q_buf(k) + c * MR * 128, &tm_q, &bars->q_full[qb], c * 64,
                                     ui.g * p.G, ui.b * p.W + ui.rb * p.Wblk);
                 }
             }
@@ -382,8 +386,8 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
-            constexpr uint32_t ID_QK = idesc_f16(128, TK, BF16, false);
-            constexpr uint32_t ID_PV = idesc_f16(128, D, BF16, true);
+            constexpr uint32_t ID_QK = idesc_f16(MR, TK, BF16, false);
+            constexpr uint32_t ID_PV = idesc_f16(MR, D, BF16, true);
             int gt = 0, k = 0;
             int pend = -1, pend_unit = 0;  // tile whose P*V is not issued yet, and its unit
             bool pend_first = false, pend_last = false;
@@ -425,7 +429,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint64_t ad =
-                            sdesc_sw128(q_addr + (kk >> 2) * (kRowsPerBlock * 128) + (kk & 3) * 32, 16, 1024);
+                            sdesc_sw128(q_addr + (kk >> 2) * (MR * 128) + (kk & 3) * 32, 16, 1024);
                         const uint64_t bd = sdesc_sw128(k_addr + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
                         mma_f16(tmem + C::S_COL + (gt & 1) * TK, ad, bd, ID_QK, kk > 0 ? 1u : 0u);
                     }
@@ -864,7 +868,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
 template <int D, bool BF16, bool SPLIT>
 static cudaError_t prepare_prefix_k() {
-    using C = PrefixCfg<D>;
+    using C = PrefixCfg<D, SPLIT>;
     static_assert(sizeof(PrefixBarriers) <= 512, "barrier block");
     static_assert(C::SMEM <= 227 * 1024, "shared memory");
     cudaError_t e =
@@ -878,7 +882,7 @@ static cudaError_t prepare_prefix_k() {
 template <int D, bool BF16>
 static cudaError_t prepare_prefix_t() {
     cudaError_t e = prepare_prefix_k<D, BF16, false>();
-    if constexpr (PrefixCfg<D>::TK == 128)
+    if constexpr (PrefixCfg<D, true>::TK == 128)
         if (e == cudaSuccess) e = prepare_prefix_k<D, BF16, true>();
     return e;
 }
@@ -886,14 +890,15 @@ static cudaError_t prepare_prefix_t() {
 template <int D, bool BF16>
 static cudaError_t launch_prefix_t(int ctas, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                    const PrefixParams& p, cudaStream_t stream) {
-    using C = PrefixCfg<D>;
-    if constexpr (C::TK == 128) {
+    if constexpr (PrefixCfg<D, true>::TK == 128) {
+        using CS = PrefixCfg<D, true>;
         if (p.bq > 0) {
-            prefix_attn_kernel<D, BF16, true><<<ctas, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+            prefix_attn_kernel<D, BF16, true><<<ctas, CS::THREADS, CS::SMEM, stream>>>(tq, tk, tv, p);
             return cudaGetLastError();
         }
     }
     if (p.bq > 0) return cudaErrorInvalidValue;
+    using C = PrefixCfg<D, false>;
     prefix_attn_kernel<D, BF16, false><<<ctas, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
