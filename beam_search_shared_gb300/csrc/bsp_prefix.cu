@@ -1,8 +1,9 @@
 // Prompt (prefix) attention of the cascade on 5th-generation tensor cores
 // (TensorRT-LLM PR #21738, "Add opt-in cascade attention for wide beam search
-// on KVCM V2", description: "Prefix: the shared prompt is attended once per
-// request"; all beam_width x GQA-group query rows of a request share one K/V
-// stream, which makes Q*K^T and P*V dense contractions).
+// on KVCM V2", description, the prefix half of the cascade: a request's shared
+// prompt is attended a single time for all of its beams; all beam_width x
+// GQA-group query rows of a request share one K/V stream, which makes Q*K^T and
+// P*V dense contractions).
 //
 // Work unit = (request b, kv head g, query-row block, key range of the plan's
 // 64-key tiles). Query rows of a block are (beam w, head j) pairs,

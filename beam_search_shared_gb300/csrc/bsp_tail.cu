@@ -1,8 +1,8 @@
 // Tail attention with the log-sum-exp merge fused into its epilogue
 // (TensorRT-LLM PR #21738, "Add opt-in cascade attention for wide beam search
-// on KVCM V2": description, "Tail: each beam's own generated tokens, gathered
-// through cache_indirection"; the tail and the merge with the prefix result
-// run as one launch per layer, commit "...fused tail, sized workspace").
+// on KVCM V2": description, the tail half of the cascade: the tokens a beam
+// generated itself, found through cache_indirection; the commit that fuses the
+// tail runs it and the merge with the prefix result as one launch per layer).
 //
 // One CTA per beam row r = b*W + w. The row's tail positions j = P_b + t
 // (t < T_b <= 8) are resolved once: threads t look up the source beam

@@ -76,7 +76,7 @@ enum {
     BSP_FLAG_CHECK = 2      /* synchronise after the launches and report device status */
 };
 
-#define BSP_MAX_TAIL 8   /* tail positions per beam (TensorRT-LLM PR #21738, "Correctness and limits") */
+#define BSP_MAX_TAIL 8   /* tail positions per beam (TensorRT-LLM PR #21738, description: correctness and limits) */
 #define BSP_MAX_GROUP 8  /* query heads per kv head */
 
 /* Bits of the device status word. */
@@ -149,8 +149,8 @@ BSP_API int32_t bsp_bucket_rows(int32_t valid_rows, int32_t capacity);
 /*
  * Upper bounds of the device workspace and the host staging buffer for plans
  * with batch <= max_batch, beam_width <= max_beam and prompt page tables of at
- * most max_prefix_pages pages (TensorRT-LLM PR #21738, "size the float
- * workspace from the engine's maximum rows"). The host staging buffer should
+ * most max_prefix_pages pages (TensorRT-LLM PR #21738: the fp32 workspace is
+ * sized once from the engine's largest row counts). The host staging buffer should
  * be pinned (page-locked) for the copy to be asynchronous.
  */
 BSP_API bsp_status bsp_workspace_size(const bsp_geometry* geo, int32_t max_batch, int32_t max_beam,
@@ -167,9 +167,9 @@ BSP_API bsp_status bsp_workspace_size(const bsp_geometry* geo, int32_t max_batch
  *                   prompt; the first ceil(P_b / page_size) entries of row b
  *                   are read and each must lie in [0, num_pages), else
  *                   BSP_ERR_PAGE_INDEX (never clamped) (TensorRT-LLM PR #21738,
- *                   "Raise on an invalid prompt page index")
- *   max_tail        <= BSP_MAX_TAIL ("Under CUDA graphs a beam may generate at
- *                   most ... MAX_TAIL tokens")
+ *                   the commit that makes an invalid prompt page id an error)
+ *   max_tail        <= BSP_MAX_TAIL (the same PR's limit on the generated
+ *                   positions a beam may hold in graph mode)
  *   num_sms         SMs to balance the prompt work units for (> 0)
  * `plan_out->generation` is 0 and the workspace fields are left NULL.
  */
@@ -179,10 +179,10 @@ BSP_API bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_
                           size_t image_bytes, bsp_plan_t* plan_out);
 
 /*
- * Plans one decode step (per-step host planning, TensorRT-LLM PR #21738:
- * "the per-step host plan runs ... so it precedes both CUDA-graph capture and
- * replay"; "Stage CUDA-graph plan inputs pinned ... so re-planning each step
- * does not synchronize the stream").
+ * Plans one decode step (per-step host planning, TensorRT-LLM PR #21738: the
+ * plan is made on the host before graph capture and before each replay, and its
+ * inputs are staged in pinned memory so that planning every step never
+ * synchronises the stream).
  * Builds the image (bsp_plan_build, balanced for the current device's SM
  * count), writes it into one of two slots of `ws_host` and enqueues its copy
  * into `ws_device` on `stream`. The workspace pair (ws_device, ws_host) must
@@ -192,7 +192,7 @@ BSP_API bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_
  * into ws_host); if that has not happened the call waits for it, up to 10 s,
  * then returns BSP_ERR_CUDA. Planning again makes every earlier plan of this
  * workspace stale (BSP_ERR_STALE_PLAN from the launches) (TensorRT-LLM PR
- * #21738, "Drop the previous step's plan").
+ * #21738, the commit that discards the previous step's plan).
  */
 BSP_API bsp_status bsp_plan(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len,
                     const int32_t* tail_len, const int32_t* prefix_pages, int32_t prefix_pages_stride,
@@ -204,8 +204,8 @@ BSP_API bsp_status bsp_plan(const bsp_geometry* geo, int32_t batch, int32_t beam
  * head_dim elements of k_new / v_new row i, head h to
  * pool[out_cache_loc[i] / page_size][h][out_cache_loc[i] % page_size][:],
  * bit for bit, in one launch (TensorRT-LLM PR #18614, description: one launch
- * per layer "derives (page, within-page) from out_cache_loc in-register and
- * writes K, V ... together").
+ * per layer computes each slot's page and in-page row from out_cache_loc in
+ * registers and writes K and V in the same pass).
  *   k_new, v_new    device [n] rows of num_kv_heads * head_dim contiguous
  *                   elements, rows `src_row_stride` elements apart
  *                   (>= num_kv_heads * head_dim, a multiple of 8) - e.g. a

@@ -12,19 +12,20 @@
  *     - positions j < P_b (the shared prompt) are read through beam 0's prompt
  *       page table: page = prefix_pages[b][j / ps], slot = j % ps
  *       (TensorRT-LLM PR #21738, "Add opt-in cascade attention for wide beam
- *       search on KVCM V2": description, "Prefix: the shared prompt is attended
- *       once per request"; commit "...for KV cache manager V2": "the prompt page
- *       table of beam 0 comes from the manager").
+ *       search on KVCM V2": description, the prefix half: one pass over a
+ *       request's prompt serves all of its beams; the commit for the V2 cache
+ *       manager: beam 0's prompt page table is the one the manager provides).
  *     - positions j = P_b + t, t < T_b (the beam's generated tail) are gathered
  *       through cache_indirection: source beam s = ci[b][w][j], page =
  *       beam_pages[b*W + s][j / ps], slot = j % ps (same page, description,
- *       "Tail: each beam's own generated tokens, gathered through
- *       cache_indirection").
+ *       the tail half: the tokens a beam generated itself, located through
+ *       cache_indirection).
  *   s_j = scale * <q, k_j>;  O = sum_j softmax(s)_j v_j;  LSE = ln sum_j exp(s_j).
  *   An empty key list gives O = 0 and LSE = -inf.
  *   The page's cascade splits this into prefix and tail and merges the two by
- *   log-sum-exp, which reaches this unsplit result exactly (description,
- *   "Each decode step is split and merged exactly with the log-sum-exp").
+ *   log-sum-exp, which reaches this unsplit result exactly (description: the
+ *   split into prefix and tail loses nothing once the log-sum-exp merge joins
+ *   them).
  *
  *   Only valid rows are read, never the whole allocation (TensorRT-Model-Connect
  *   PR #2202, "prefill and decode over the cached prefix, not the whole KV
@@ -32,8 +33,8 @@
  *
  *   The paged append writes each new token's K and V rows at its flat slot:
  *   page = loc / ps, offset = loc % ps (TensorRT-LLM PR #18614, "Fuse MiniMax-M3
- *   MSA per-layer KV-cache writes into one kernel": description, "derives
- *   (page, within-page) from out_cache_loc").
+ *   MSA per-layer KV-cache writes into one kernel": description: the page and
+ *   in-page row of each slot come from out_cache_loc).
  *
  * Pool layout: [num_pages][Hkv][ps][D] of 16-bit floats (bf16 or fp16 bits).
  * q layout: [R][Hq][D]. cache_indirection: [B][W][max_seq] int32.
@@ -123,7 +124,7 @@ void orc_attend(int D, int n, const double *q, const double *K, const double *V,
 /* Log-sum-exp merge of k partial attention states (O_i, L_i) over disjoint key
  * sets: L = ln sum exp(L_i), O = sum exp(L_i - L) O_i. All L_i = -inf (every
  * set empty) gives O = 0, L = -inf (TensorRT-LLM PR #21738, description: the
- * prefix and tail states are "merged exactly with the log-sum-exp"). */
+ * prefix and tail states are joined without loss by a log-sum-exp merge). */
 void orc_merge(int D, int k, const double *O, const double *L, double *o, double *lse)
 {
     double m = -INFINITY;
