@@ -251,3 +251,112 @@ def make_case(wl: Workload, seed: int, *, full_step: bool = True, device="cpu",
                 cache_indirection=ci.astype(np.int32), q=q, k_pool=k_pool, v_pool=v_pool,
                 k_new=k_new, v_new=v_new, out_cache_loc=np.asarray(loc, np.int32),
                 new_rows=np.asarray(new_rows, np.int32))
+
+
+# ---------------------------------------------------------------- prefill over the cached prefix
+@dataclasses.dataclass(frozen=True)
+class PrefillWorkload:
+    """Shape recipe of one synthetic prefill: per request, C cached rows and S prompt tokens."""
+    name: str
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    dtype: str
+    cached: Sequence[int]   # (lo, hi) inclusive uniform range of valid cached rows C
+    prompt: Sequence[int]   # (lo, hi) inclusive uniform range of prompt tokens S
+    causal: bool = True
+    alloc_rows: int = 0     # > 0: every request owns this many rows of pages (garbage past C + S)
+
+    def with_(self, **kw) -> "PrefillWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+# The phi4-multimodal shapes of the bucketed-prefix page: a 10368-row allocation per request, an image
+# prompt prefilled from an empty cache, or text after a cached prefix; the 4B-shaped heads of the decode
+# workloads (32 q heads, 8 kv heads, head_dim 128, fp16).
+PREFILL_WORKLOADS = {
+    "prefill_tiny_d64": PrefillWorkload("prefill_tiny_d64", 2, 4, 2, 64, 16, "bf16", (0, 40), (1, 20)),
+    "prefill_image_b4_s1024": PrefillWorkload("prefill_image_b4_s1024", 4, 32, 8, 128, 32, "fp16", (0, 0),
+                                              (1024, 1024), alloc_rows=10368),
+    "prefill_text_b8": PrefillWorkload("prefill_text_b8", 8, 32, 8, 128, 32, "fp16", (0, 3000), (16, 300),
+                                       alloc_rows=10368),
+}
+
+
+@dataclasses.dataclass
+class PrefillCase:
+    """One synthetic prefill. Index arrays are numpy int32; values are torch tensors."""
+    workload: PrefillWorkload
+    seed: int
+    num_pages: int
+    cached_len: np.ndarray    # [B]
+    prompt_len: np.ndarray    # [B]
+    pages: np.ndarray         # [B, maxp] the request's page table over its allocation
+    q: torch.Tensor           # [R, Hq, D], R = sum S
+    k_pool: torch.Tensor      # [num_pages, Hkv, ps, D] (before the prompt's K/V are written)
+    v_pool: torch.Tensor
+    k_new: torch.Tensor       # [R, Hkv, D] the prompt tokens' K/V
+    v_new: torch.Tensor
+    out_cache_loc: np.ndarray  # [R] slot of prompt token i of request b: position C_b + i
+
+    @property
+    def rows(self) -> int:
+        return int(self.prompt_len.sum())
+
+
+def make_prefill_case(wl: PrefillWorkload, seed: int, *, device="cpu", cached_lengths=None,
+                      prompt_lengths=None) -> PrefillCase:
+    B, Hq, Hkv, D, ps = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.page_size
+    tdt = TORCH_DTYPES[wl.dtype]
+    g = torch.Generator().manual_seed(seed)
+    if cached_lengths is not None:
+        C = np.asarray(cached_lengths, np.int64)
+    else:
+        C = torch.randint(wl.cached[0], wl.cached[1] + 1, (B,), generator=g).numpy().astype(np.int64)
+    if prompt_lengths is not None:
+        S = np.asarray(prompt_lengths, np.int64)
+    else:
+        S = torch.randint(wl.prompt[0], wl.prompt[1] + 1, (B,), generator=g).numpy().astype(np.int64)
+    assert C.shape == (B,) and S.shape == (B,)
+    rows_each = [max(int(wl.alloc_rows), int(C[b] + S[b])) for b in range(B)]
+    npg = [_ceil_div(r, ps) for r in rows_each]
+    num_pages = max(1, sum(npg)) + 2
+    perm = torch.randperm(num_pages, generator=g).numpy().astype(np.int64)
+    maxp = max([1] + npg)
+    pages = np.full((B, maxp), -1, np.int64)
+    cur = 0
+    row_valid = np.zeros((num_pages, ps), bool)
+    for b in range(B):
+        pages[b, :npg[b]] = perm[cur:cur + npg[b]]
+        cur += npg[b]
+        flat = np.arange(npg[b] * ps)
+        vr = flat < C[b]                       # cached rows; prompt rows are written by the append
+        for k_, pg in enumerate(pages[b, :npg[b]]):
+            row_valid[pg] = vr[k_ * ps:(k_ + 1) * ps]
+    dev = torch.device(device)
+    gd = torch.Generator(device=dev).manual_seed(seed + 7919)
+    k_pool = torch.empty((num_pages, Hkv, ps, D), dtype=tdt, device=dev)
+    v_pool = torch.empty_like(k_pool)
+    valid_t = torch.from_numpy(row_valid).to(dev)
+    chunk = max(1, (1 << 26) // max(1, Hkv * ps * D))
+    for pool in (k_pool, v_pool):
+        for p0 in range(0, num_pages, chunk):
+            p1 = min(num_pages, p0 + chunk)
+            shape = (p1 - p0, Hkv, ps, D)
+            garbage = torch.rand(shape, generator=gd, device=dev) * 2000.0 - 1000.0
+            normal = torch.randn(shape, generator=gd, device=dev)
+            pool[p0:p1] = torch.where(valid_t[p0:p1][:, None, :, None], normal, garbage).to(tdt)
+    R = int(S.sum())
+    q = torch.randn((R, Hq, D), generator=gd, device=dev).to(tdt)
+    k_new = torch.randn((R, Hkv, D), generator=gd, device=dev).to(tdt)
+    v_new = torch.randn((R, Hkv, D), generator=gd, device=dev).to(tdt)
+    loc = []
+    for b in range(B):
+        for i in range(int(S[b])):
+            pos = int(C[b]) + i
+            loc.append(int(pages[b, pos // ps]) * ps + pos % ps)
+    return PrefillCase(workload=wl, seed=seed, num_pages=num_pages, cached_len=C.astype(np.int32),
+                       prompt_len=S.astype(np.int32), pages=pages.astype(np.int32), q=q, k_pool=k_pool,
+                       v_pool=v_pool, k_new=k_new, v_new=v_new, out_cache_loc=np.asarray(loc, np.int32))

@@ -59,6 +59,9 @@ def _load():
     lib.orc_decode_attn.argtypes = [ctypes.c_int] * 8 + [p, p, p, ctypes.c_int, p, ctypes.c_int, p,
                                                        ctypes.c_int, p, p, p, ctypes.c_double, p,
                                                        ctypes.c_int, p, p]
+    lib.orc_prefill_attn.restype = ctypes.c_int
+    lib.orc_prefill_attn.argtypes = [ctypes.c_int] * 7 + [p, p, p, ctypes.c_int, ctypes.c_int, p, p, p,
+                                                       ctypes.c_double, p, p]
     lib.orc_append_kv.restype = ctypes.c_int
     lib.orc_append_kv.argtypes = [ctypes.c_int] * 5 + [p, p, p, ctypes.c_int64, p, p]
     _lib = lib
@@ -137,6 +140,29 @@ def decode_attn(*, dtype, B, W, Hq, Hkv, D, ps, num_pages, prefix_len, tail_len,
         None if rows_arr is None else _ptr(rows_arr), nrows, _ptr(O), _ptr(L))
     if rc != 0:
         raise ValueError(f"oracle decode_attn: {ERRORS.get(rc, rc)}")
+    return O, L
+
+
+def prefill_attn(*, dtype, B, Hq, Hkv, D, ps, num_pages, cached_len, prompt_len, pages, causal, q_bits,
+                 k_pool_bits, v_pool_bits, scale):
+    """fp64 prefill over the cached prefix: prompt token i of request b attends positions
+    0 .. C_b + i (causal) or 0 .. C_b + S_b - 1, read through pages[b]. q_bits [R,Hq,D] with
+    R = sum S_b (requests in order). Returns (O [R,Hq,D], LSE [R,Hq]) in float64."""
+    cached_len = _c(cached_len, np.int32)
+    prompt_len = _c(prompt_len, np.int32)
+    pages = _c(pages, np.int32).reshape(B, -1)
+    q_bits = _c(q_bits, np.uint16)
+    k_pool_bits = _c(k_pool_bits, np.uint16)
+    v_pool_bits = _c(v_pool_bits, np.uint16)
+    R = int(prompt_len.sum())
+    O = np.empty((R, Hq, D), np.float64)
+    L = np.empty((R, Hq), np.float64)
+    rc = _load().orc_prefill_attn(
+        DTYPES[dtype], B, Hq, Hkv, D, ps, num_pages, _ptr(cached_len), _ptr(prompt_len), _ptr(pages),
+        pages.shape[1], 1 if causal else 0, _ptr(q_bits), _ptr(k_pool_bits), _ptr(v_pool_bits), float(scale),
+        _ptr(O), _ptr(L))
+    if rc != 0:
+        raise ValueError(f"oracle prefill_attn: {ERRORS.get(rc, rc)}")
     return O, L
 
 

@@ -74,3 +74,33 @@ def decode_attn(*, dtype, B, W, Hq, Hkv, D, ps, prefix_len, tail_len, prefix_pag
             O.append(row_o)
             L.append(row_l)
     return O, L
+
+
+def prefill_attn(*, dtype, B, Hq, Hkv, D, ps, cached_len, prompt_len, pages, causal, q_bits, k_pool_bits,
+                 v_pool_bits, scale):
+    """Nested lists O[r][h][d], LSE[r][h] for every prompt row r (requests in order, tokens in order).
+
+    Prefill over the cached prefix (TensorRT-Model-Connect PR #2202, Implementation): prompt token i of
+    request b sees the request's cached rows and its prompt rows up to itself (all of them when not
+    causal), every position read through the request's page table."""
+    G = Hq // Hkv
+    O, L = [], []
+    r = 0
+    for b in range(B):
+        C, S = int(cached_len[b]), int(prompt_len[b])
+        for i in range(S):
+            n = C + i + 1 if causal else C + S
+            seq = [(int(pages[b][pos // ps]), pos % ps) for pos in range(n)]
+            row_o, row_l = [], []
+            for h in range(Hq):
+                g = h // G
+                q = [half_bits_to_float(x, dtype) for x in q_bits[r][h]]
+                keys = [[half_bits_to_float(x, dtype) for x in k_pool_bits[p][g][s]] for p, s in seq]
+                vals = [[half_bits_to_float(x, dtype) for x in v_pool_bits[p][g][s]] for p, s in seq]
+                o, lse = attend(q, keys, vals, scale)
+                row_o.append(o)
+                row_l.append(lse)
+            O.append(row_o)
+            L.append(row_l)
+            r += 1
+    return O, L

@@ -251,6 +251,104 @@ int orc_decode_attn(int dtype, int B, int W, int Hq, int Hkv, int D, int ps, int
     return err;
 }
 
+/* Prefill over the cached prefix (TensorRT-Model-Connect PR #2202, "prefill and
+ * decode over the cached prefix, not the whole KV allocation", Implementation:
+ * the prompt rows attend the bound cache rows followed by the prompt rows, a
+ * [Sq, cache_rows + Sq] mask with the prompt columns after the cache rows; only
+ * the valid cached prefix is bound). Request b holds C_b valid cached rows and
+ * S_b prompt tokens, whose K/V already sit at logical positions C_b .. C_b+S_b-1;
+ * every position p of request b is read through its page table:
+ * page = pages[b][p / ps], slot = p % ps. Query row r = off_b + i (prompt token
+ * i of request b; off_b = S_0 + ... + S_{b-1}) attends positions 0 .. C_b + i
+ * when `causal` (each prompt token sees the cache and the prompt up to itself),
+ * else 0 .. C_b + S_b - 1. q is [R][Hq][D] with R = sum S_b; O [R][Hq][D],
+ * LSE [R][Hq] (natural log). */
+int orc_prefill_attn(int dtype, int B, int Hq, int Hkv, int D, int ps, int num_pages,
+                     const int32_t *cached_len, const int32_t *prompt_len, const int32_t *pages, int maxp,
+                     int causal, const uint16_t *q, const uint16_t *kpool, const uint16_t *vpool,
+                     double scale, double *O, double *LSE)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || ps <= 0)
+        return ORC_ERR_ARG;
+    const int G = Hq / Hkv;
+    int R = 0, maxn = 0;
+    for (int b = 0; b < B; ++b) {
+        if (cached_len[b] < 0 || prompt_len[b] < 0)
+            return ORC_ERR_ARG;
+        R += prompt_len[b];
+        if (cached_len[b] + prompt_len[b] > maxn)
+            maxn = cached_len[b] + prompt_len[b];
+    }
+    int *req_of = malloc(sizeof(int) * ((size_t)R + 1));
+    int *tok_of = malloc(sizeof(int) * ((size_t)R + 1));
+    if (!req_of || !tok_of) {
+        free(req_of);
+        free(tok_of);
+        return ORC_ERR_NOMEM;
+    }
+    for (int b = 0, r = 0; b < B; ++b)
+        for (int i = 0; i < prompt_len[b]; ++i, ++r) {
+            req_of[r] = b;
+            tok_of[r] = i;
+        }
+    int err = ORC_OK;
+#pragma omp parallel
+    {
+        double *K = malloc(sizeof(double) * ((size_t)maxn * D + 1));
+        double *V = malloc(sizeof(double) * ((size_t)maxn * D + 1));
+        double *s = malloc(sizeof(double) * ((size_t)maxn + 1));
+        double *qd = malloc(sizeof(double) * (size_t)D);
+        if (!K || !V || !s || !qd) {
+#pragma omp atomic write
+            err = ORC_ERR_NOMEM;
+        }
+#pragma omp for collapse(2) schedule(dynamic, 1)
+        for (int r = 0; r < R; ++r) {
+            for (int g = 0; g < Hkv; ++g) {
+                if (err != ORC_OK)
+                    continue;
+                const int b = req_of[r], i = tok_of[r];
+                const int n = causal ? cached_len[b] + i + 1 : cached_len[b] + prompt_len[b];
+                int bad = 0;
+                for (int j = 0; j < n; ++j) {
+                    if (j / ps >= maxp) {
+                        bad = 1;
+                        break;
+                    }
+                    const int32_t page = pages[(size_t)b * maxp + j / ps];
+                    if (page < 0 || page >= num_pages) {
+                        bad = 1;
+                        break;
+                    }
+                    size_t base = (((size_t)page * Hkv + g) * ps + (size_t)(j % ps)) * D;
+                    for (int d = 0; d < D; ++d) {
+                        K[(size_t)j * D + d] = orc_half_to_double(kpool[base + d], dtype);
+                        V[(size_t)j * D + d] = orc_half_to_double(vpool[base + d], dtype);
+                    }
+                }
+                if (bad) {
+#pragma omp atomic write
+                    err = ORC_ERR_INDEX;
+                    continue;
+                }
+                for (int hh = 0; hh < G; ++hh) {
+                    int h = g * G + hh;
+                    for (int d = 0; d < D; ++d)
+                        qd[d] = orc_half_to_double(q[((size_t)r * Hq + h) * D + d], dtype);
+                    orc_attend(D, n, qd, K, V, scale, s, O + ((size_t)r * Hq + h) * D, LSE + (size_t)r * Hq + h);
+                }
+            }
+        }
+        free(K);
+        free(V);
+        free(s);
+        free(qd);
+    }
+    free(req_of);
+    free(tok_of);
+    return err;
+}
+
 /* Paged KV append: for each new token i and kv head h, copy the D-element K and
  * V rows to pool[loc_i / ps][h][loc_i % ps][:], as bits. All slots are checked
  * before anything is written, so a bad slot leaves both pools unchanged. */

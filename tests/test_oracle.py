@@ -341,3 +341,96 @@ def test_append_strided_source_bad_slot_and_empty():
     oracle.append_kv(Hkv=Hkv, D=D, ps=ps, num_pages=npg, out_cache_loc=np.zeros(0, np.int32),
                      k_new_bits=src_k[:0], v_new_bits=src_v[:0], k_pool_bits=kp, v_pool_bits=vp)
     np.testing.assert_array_equal(kp, before[0])
+
+
+# ------------------------------------------------------------------ prefill over the cached prefix
+def _prefill_oracle(case, causal, k_pool=None, v_pool=None):
+    wl = case.workload
+    kp = synth.bits(case.k_pool).copy() if k_pool is None else k_pool
+    vp = synth.bits(case.v_pool).copy() if v_pool is None else v_pool
+    if k_pool is None:
+        oracle.append_kv(Hkv=wl.num_kv_heads, D=wl.head_dim, ps=wl.page_size, num_pages=case.num_pages,
+                         out_cache_loc=case.out_cache_loc, k_new_bits=synth.bits(case.k_new),
+                         v_new_bits=synth.bits(case.v_new), k_pool_bits=kp, v_pool_bits=vp)
+    O, L = oracle.prefill_attn(dtype=wl.dtype, B=wl.batch, Hq=wl.num_q_heads, Hkv=wl.num_kv_heads, D=wl.head_dim,
+                               ps=wl.page_size, num_pages=case.num_pages, cached_len=case.cached_len,
+                               prompt_len=case.prompt_len, pages=case.pages, causal=causal,
+                               q_bits=synth.bits(case.q), k_pool_bits=kp, v_pool_bits=vp,
+                               scale=1 / math.sqrt(wl.head_dim))
+    return O, L, kp, vp
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("seed", [1, 2])
+def test_prefill_oracle_matches_brute_force(causal, seed):
+    wl = synth.PREFILL_WORKLOADS["prefill_tiny_d64"].with_(head_dim=8, page_size=4, cached=(0, 9), prompt=(1, 5))
+    case = synth.make_prefill_case(wl, seed)
+    O, L, kp, vp = _prefill_oracle(case, causal)
+    Ob, Lb = brute.prefill_attn(dtype=wl.dtype, B=wl.batch, Hq=wl.num_q_heads, Hkv=wl.num_kv_heads, D=wl.head_dim,
+                                ps=wl.page_size, cached_len=case.cached_len, prompt_len=case.prompt_len,
+                                pages=case.pages, causal=causal, q_bits=synth.bits(case.q).tolist(),
+                                k_pool_bits=kp.tolist(), v_pool_bits=vp.tolist(), scale=1 / math.sqrt(wl.head_dim))
+    np.testing.assert_allclose(O, np.asarray(Ob), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(L, np.asarray(Lb), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_rows_equal_decode_of_a_single_beam(causal):
+    """Prompt token i (causal) sees exactly the keys a one-beam decode step sees with a prompt of
+    C + i + 1 rows and no tail (C + S rows when not causal): the two oracle functions agree."""
+    wl = synth.PREFILL_WORKLOADS["prefill_tiny_d64"].with_(cached=(3, 30), prompt=(2, 9))
+    case = synth.make_prefill_case(wl, 7)
+    O, L, kp, vp = _prefill_oracle(case, causal)
+    qb = synth.bits(case.q)
+    r = 0
+    for b in range(wl.batch):
+        C, S = int(case.cached_len[b]), int(case.prompt_len[b])
+        for i in range(S):
+            n = C + i + 1 if causal else C + S
+            Od, Ld = oracle.decode_attn(
+                dtype=wl.dtype, B=1, W=1, Hq=wl.num_q_heads, Hkv=wl.num_kv_heads, D=wl.head_dim, ps=wl.page_size,
+                num_pages=case.num_pages, prefix_len=[n], tail_len=[0], prefix_pages=case.pages[b:b + 1],
+                beam_pages=case.pages[b:b + 1], cache_indirection=np.zeros((1, 1, max(1, n)), np.int32),
+                q_bits=qb[r:r + 1], k_pool_bits=kp, v_pool_bits=vp, scale=1 / math.sqrt(wl.head_dim))
+            np.testing.assert_array_equal(O[r], Od[0])
+            np.testing.assert_array_equal(L[r], Ld[0])
+            r += 1
+
+
+def test_prefill_first_token_of_empty_cache_sees_only_itself():
+    """Causal, no cached rows: token 0's only key is its own, so O = v_0 and LSE = scale * q.k_0."""
+    wl = synth.PREFILL_WORKLOADS["prefill_tiny_d64"]
+    case = synth.make_prefill_case(wl, 3, cached_lengths=[0, 0], prompt_lengths=[3, 1])
+    O, L, kp, vp = _prefill_oracle(case, True)
+    G = wl.num_q_heads // wl.num_kv_heads
+    r = 0
+    for b in range(wl.batch):
+        for h in range(wl.num_q_heads):
+            kb = synth.bits(case.k_new)[r, h // G]
+            vb = synth.bits(case.v_new)[r, h // G]
+            v0 = np.array([oracle.half_to_double(x, wl.dtype) for x in vb])
+            k0 = np.array([oracle.half_to_double(x, wl.dtype) for x in kb])
+            q0 = np.array([oracle.half_to_double(x, wl.dtype) for x in synth.bits(case.q)[r, h]])
+            np.testing.assert_array_equal(O[r, h], v0)
+            assert L[r, h] == pytest.approx(float(q0 @ k0) / math.sqrt(wl.head_dim), rel=1e-12, abs=1e-12)
+        r += int(case.prompt_len[b])
+
+
+def test_prefill_never_reads_rows_past_the_prompt():
+    """Rows of the allocation past C + S (and, causally, past each token) hold garbage the
+    result must not depend on: poisoning them with NaN changes nothing."""
+    wl = synth.PREFILL_WORKLOADS["prefill_tiny_d64"].with_(alloc_rows=96)
+    case = synth.make_prefill_case(wl, 5)
+    O, L, kp, vp = _prefill_oracle(case, True)
+    kp2, vp2 = kp.copy(), vp.copy()
+    nan = np.uint16(0x7FC0)
+    for b in range(wl.batch):
+        end = int(case.cached_len[b] + case.prompt_len[b])
+        for pos in range(end, (case.pages.shape[1]) * wl.page_size):
+            pg = int(case.pages[b, pos // wl.page_size])
+            if pg >= 0:
+                kp2[pg, :, pos % wl.page_size] = nan
+                vp2[pg, :, pos % wl.page_size] = nan
+    O2, L2, _, _ = _prefill_oracle(case, True, k_pool=kp2, v_pool=vp2)
+    np.testing.assert_array_equal(O, O2)
+    np.testing.assert_array_equal(L, L2)
