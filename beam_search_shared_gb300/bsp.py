@@ -53,12 +53,14 @@ class Plan(ctypes.Structure):
         ("ws_host", ctypes.c_void_p), ("image_bytes", ctypes.c_uint64), ("off_req", ctypes.c_uint64),
         ("off_units", ctypes.c_uint64), ("off_pages", ctypes.c_uint64), ("off_part_lse", ctypes.c_uint64),
         ("off_part_o", ctypes.c_uint64), ("device_bytes_used", ctypes.c_uint64),
-        ("tail_requests", ctypes.c_int32), ("reserved0", ctypes.c_int32), ("reserved", ctypes.c_uint64 * 3)]
+        ("tail_requests", ctypes.c_int32), ("total_rows", ctypes.c_int32), ("kind", ctypes.c_int32),
+        ("reserved1", ctypes.c_int32), ("reserved", ctypes.c_uint64 * 2)]
 
 
 _lib = None
 EXPORTS = ["bsp_status_string", "bsp_bucket_rows", "bsp_workspace_size", "bsp_plan_build", "bsp_plan",
-           "bsp_append_kv", "bsp_decode_attn", "bsp_read_device_status", "bsp_decode_attn_noalloc"]
+           "bsp_append_kv", "bsp_decode_attn", "bsp_read_device_status", "bsp_decode_attn_noalloc",
+           "bsp_plan_prefill_build", "bsp_plan_prefill", "bsp_prefill_attn"]
 NOALLOC_SCRATCH_MIB = 32
 
 
@@ -97,6 +99,12 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.bsp_append_kv.argtypes = [P(Plan), vp, vp, i64, vp, i32, vp, vp, vp, vp]
     lib.bsp_decode_attn.restype = i32
     lib.bsp_decode_attn.argtypes = [P(Plan), vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, i32, vp, vp, vp, vp]
+    lib.bsp_plan_prefill_build.restype = i32
+    lib.bsp_plan_prefill_build.argtypes = [P(Geometry), i32, vp, vp, vp, i32, i32, i32, vp, sz, P(Plan)]
+    lib.bsp_plan_prefill.restype = i32
+    lib.bsp_plan_prefill.argtypes = [P(Geometry), i32, vp, vp, vp, i32, i32, vp, sz, vp, sz, vp, P(Plan)]
+    lib.bsp_prefill_attn.restype = i32
+    lib.bsp_prefill_attn.argtypes = [P(Plan), vp, vp, vp, ctypes.c_float, i32, vp, vp, vp, vp]
     lib.bsp_read_device_status.restype = i32
     lib.bsp_read_device_status.argtypes = [P(Plan), vp, i32, P(i32)]
     lib.bsp_decode_attn_noalloc.restype = i32
@@ -168,6 +176,39 @@ def plan_requests(plan_: Plan, img: np.ndarray) -> np.ndarray:
     prompt kernel (1) or by the tail kernel (0), two unused."""
     lo = plan_.off_req - STATUS_BYTES
     return img[lo:lo + plan_.batch * 32].view(np.int32).reshape(plan_.batch, 8)
+
+
+def plan_prefill_build(geo: Geometry, batch, cached_len, prompt_len, pages, causal, num_sms,
+                       image_bytes: int = 1 << 24):
+    """Host-only prefill planning. Returns (Plan, image bytes as a numpy uint8 array)."""
+    cl, pl = _i32(cached_len), _i32(prompt_len)
+    pg = _i32(pages).reshape(int(batch), -1) if int(batch) else np.zeros((0, 1), np.int32)
+    img = np.zeros(int(image_bytes), np.uint8)
+    plan = Plan()
+    _check("bsp_plan_prefill_build", load().bsp_plan_prefill_build(
+        ctypes.byref(geo), int(batch), _ptr(cl), _ptr(pl), _ptr(pg), pg.shape[1], 1 if causal else 0,
+        int(num_sms), _ptr(img), img.nbytes, ctypes.byref(plan)))
+    return plan, img[:plan.image_bytes]
+
+
+def plan_prefill(geo: Geometry, batch, cached_len, prompt_len, pages, causal, ws: "Workspace",
+                 stream=None) -> Plan:
+    """bsp_plan_prefill: host arrays in, plan staged into ``ws`` on ``stream`` (no sync)."""
+    cl, pl = _i32(cached_len), _i32(prompt_len)
+    pg = _i32(pages).reshape(int(batch), -1) if int(batch) else np.zeros((0, 1), np.int32)
+    out = Plan()
+    _check("bsp_plan_prefill", load().bsp_plan_prefill(
+        ctypes.byref(geo), int(batch), _ptr(cl), _ptr(pl), _ptr(pg), pg.shape[1], 1 if causal else 0,
+        _dptr(ws.device), ws.device.numel(), _dptr(ws.host), ws.host.numel(), _stream(stream), ctypes.byref(out)))
+    return out
+
+
+def prefill_attn(plan_: Plan, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, softmax_scale: float,
+                 o: torch.Tensor, lse: torch.Tensor, flags: int = 0, events=None, stream=None):
+    """bsp_prefill_attn: writes o [total_rows,Hq,D] and lse [total_rows,Hq] (fp32)."""
+    _check("bsp_prefill_attn", load().bsp_prefill_attn(
+        ctypes.byref(plan_), _dptr(q), _dptr(k_pool), _dptr(v_pool), float(softmax_scale), int(flags), _dptr(o),
+        _dptr(lse), _events(events, 3), _stream(stream)))
 
 
 class Workspace:

@@ -182,19 +182,58 @@ bsp_status bsp_workspace_size(const bsp_geometry* geo, int32_t max_batch, int32_
     return BSP_OK;
 }
 
-bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len,
-                          const int32_t* tail_len, const int32_t* prefix_pages, int32_t prefix_pages_stride,
-                          int32_t max_tail, int32_t num_sms, void* image, size_t image_bytes, bsp_plan_t* out) {
+}  // extern "C"
+
+namespace {
+// A prefill plan: request b holds cached_len[b] valid cached rows and prompt_len[b] prompt tokens.
+struct PrefillSpec {
+    const int32_t* cached_len;
+    const int32_t* prompt_len;
+    bool causal;
+};
+
+// The plan image of a decode step (pf == nullptr: prefix_len / tail_len per request, beam_width rows
+// each) or of a prefill (pf: the prompt tokens are the rows, the keys are the cached rows and the
+// prompt, no tail, no key splits, every request finished by the prompt kernel).
+bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len_in,
+                           const int32_t* tail_len_in, const int32_t* prefix_pages, int32_t prefix_pages_stride,
+                           int32_t max_tail, int32_t num_sms, void* image, size_t image_bytes, bsp_plan_t* out,
+                           const PrefillSpec* pf) {
     bsp_status st = check_geometry(geo);
     if (st != BSP_OK) return st;
     if (!out || batch < 0 || beam_width < 1 || num_sms < 1 || prefix_pages_stride < 0) return BSP_ERR_INVALID_ARG;
     if (max_tail < 0) return BSP_ERR_INVALID_ARG;
     if (max_tail > BSP_MAX_TAIL) return BSP_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(batch) * beam_width > (int64_t(1) << 30)) return BSP_ERR_UNSUPPORTED;
-    if (batch > 0 && (!prefix_len || !tail_len)) return BSP_ERR_INVALID_ARG;
+    if (batch > 0 && !pf && (!prefix_len_in || !tail_len_in)) return BSP_ERR_INVALID_ARG;
+    if (batch > 0 && pf && (!pf->cached_len || !pf->prompt_len)) return BSP_ERR_INVALID_ARG;
     const int ps = geo->page_size;
     const int G = geo->num_q_heads / geo->num_kv_heads;
     const int Hkv = geo->num_kv_heads;
+    // per request: keys, tail, query rows, causal base, first row
+    std::vector<int32_t> pl(batch), tl(batch), rows(batch), causal(batch), row_off(batch);
+    int64_t total_rows = 0;
+    for (int b = 0; b < batch; ++b) {
+        if (pf) {
+            const int64_t c = pf->cached_len[b], sq = pf->prompt_len[b];
+            if (c < 0 || sq < 0) return BSP_ERR_INVALID_ARG;
+            if (c + sq > (1 << 30)) return BSP_ERR_UNSUPPORTED;
+            pl[b] = sq > 0 ? static_cast<int32_t>(c + sq) : 0;  // no rows: nothing to attend
+            tl[b] = 0;
+            rows[b] = static_cast<int32_t>(sq);
+            causal[b] = pf->causal ? static_cast<int32_t>(c) : -1;
+        } else {
+            pl[b] = prefix_len_in[b];
+            tl[b] = tail_len_in[b];
+            rows[b] = beam_width;
+            causal[b] = -1;
+        }
+        if (total_rows + rows[b] > (int64_t(1) << 30)) return BSP_ERR_UNSUPPORTED;
+        row_off[b] = static_cast<int32_t>(total_rows);
+        total_rows += rows[b];
+    }
+    const int32_t* prefix_len = pl.data();
+    const int32_t* tail_len = tl.data();
 
     int max_p = 0, max_total = 0, max_t = 0;
     int64_t total_pages = 0;
@@ -221,7 +260,15 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
 
     // ---- work units: (request, kv head, key split, query-row block)
     int nrb, wblk;
-    row_blocks(beam_width, G, &nrb, &wblk);
+    if (pf) {
+        // prompt tokens in blocks of one MMA's rows (dense layout: 128 rows = 128 / G tokens)
+        wblk = std::max(1, kRowsPerBlock / G);
+        nrb = 0;
+        for (int b = 0; b < batch; ++b) nrb = std::max<int>(nrb, static_cast<int>(ceil_div(rows[b], wblk)));
+    } else {
+        row_blocks(beam_width, G, &nrb, &wblk);
+    }
+    auto nrb_of = [&](int b) -> int { return pf ? static_cast<int>(ceil_div(rows[b], wblk)) : nrb; };
     std::vector<int64_t> tiles(batch);
     int64_t total_tiles = 0, active = 0;
     for (int b = 0; b < batch; ++b) {
@@ -229,10 +276,11 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
         total_tiles += tiles[b];
         active += tiles[b] > 0;
     }
-    const int64_t base_units = active * Hkv * nrb;
+    int64_t base_units = 0;
+    for (int b = 0; b < batch; ++b) base_units += tiles[b] > 0 ? static_cast<int64_t>(Hkv) * nrb_of(b) : 0;
     const int64_t target = 2 * static_cast<int64_t>(num_sms);
     int64_t chunk = std::numeric_limits<int32_t>::max();  // tiles per split
-    if (base_units > 0 && base_units < target)
+    if (!pf && base_units > 0 && base_units < target)  // a prefill's rows are never split by keys
         chunk = std::max<int64_t>(2, ceil_div(total_tiles * Hkv * nrb, target));
     std::vector<int32_t> nsplit(batch);
     int64_t parts = 0;
@@ -250,6 +298,12 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
     auto fused = [&](int b) -> bool {
         return nsplit[b] == 1 && static_cast<int64_t>(tail_len[b]) * wblk <= prefix_tile_keys(geo->head_dim);
     };
+    // the plan tiles a unit reads: a causal prefill block stops at its last token's keys
+    auto unit_end_tile = [&](int b, int rb, int32_t t1) -> int32_t {
+        if (causal[b] < 0) return t1;
+        const int64_t last_row = std::min<int64_t>(rows[b], static_cast<int64_t>(rb + 1) * wblk);
+        return static_cast<int32_t>(std::min<int64_t>(t1, ceil_div(causal[b] + last_row, kTileKeys)));
+    };
     struct Unit {
         int32_t f[kUnitFields];
     };
@@ -263,7 +317,7 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
         return 8 * kt + 4;
     };
     std::vector<Unit> units;
-    units.reserve(static_cast<size_t>(parts * Hkv * nrb));
+    units.reserve(static_cast<size_t>(base_units + parts * Hkv * nrb));
     std::vector<int32_t> part_off(batch), page_off(batch);
     int64_t poff = 0, pgoff = 0;
     for (int b = 0; b < batch; ++b) {
@@ -273,15 +327,16 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
             const int32_t t0 = static_cast<int32_t>(s * tiles[b] / nsplit[b]);
             const int32_t t1 = static_cast<int32_t>((s + 1) * tiles[b] / nsplit[b]);
             for (int g = 0; g < Hkv; ++g)
-                for (int rb = 0; rb < nrb; ++rb) {
+                for (int rb = 0; rb < nrb_of(b); ++rb) {
+                    const int32_t te = unit_end_tile(b, rb, t1);
                     Unit u{};
                     u.f[kUnitReq] = b;
                     u.f[kUnitKvHead] = g;
                     u.f[kUnitRowBlock] = rb;
                     u.f[kUnitTile0] = t0;
-                    u.f[kUnitTile1] = t1;
+                    u.f[kUnitTile1] = te;
                     u.f[kUnitPart] = static_cast<int32_t>(poff + s);
-                    u.f[kUnitCost] = static_cast<int32_t>(unit_cost(b, t0, t1));
+                    u.f[kUnitCost] = static_cast<int32_t>(unit_cost(b, t0, te));
                     units.push_back(u);
                 }
         }
@@ -422,6 +477,9 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
         r[kReqPartOff] = part_off[b];
         r[kReqPageOff] = page_off[b];
         r[kReqFused] = fused(b) ? 1 : 0;
+        r[kReqRows] = rows[b];
+        r[kReqCausal] = causal[b];
+        r[kReqRowOff] = row_off[b];
     }
     if (!units.empty()) std::memcpy(img + off_units, units.data(), units.size() * sizeof(Unit));
     std::memcpy(img + off_cta, cta_off.data(), cta_off.size() * 4);
@@ -448,8 +506,10 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
     out->max_tail_len = max_t;
     out->prefix_ctas = static_cast<int32_t>(ctas);
     int32_t tail_requests = 0;
-    for (int b = 0; b < batch; ++b) tail_requests += !fused(b);
+    for (int b = 0; b < batch; ++b) tail_requests += !pf && !fused(b);
     out->tail_requests = tail_requests;
+    out->total_rows = static_cast<int32_t>(total_rows);
+    out->kind = pf ? 1 : 0;
     out->image_bytes = need;
     // offsets relative to the device workspace
     DeviceLayout L = device_layout(need, parts, beam_width, *geo);
@@ -461,11 +521,34 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
     out->device_bytes_used = L.total;
     return BSP_OK;
 }
+}  // namespace
 
-bsp_status bsp_plan(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len,
-                    const int32_t* tail_len, const int32_t* prefix_pages, int32_t prefix_pages_stride, int32_t max_tail,
-                    void* ws_device, size_t ws_device_bytes, void* ws_host, size_t ws_host_bytes, void* stream,
-                    bsp_plan_t* out) {
+extern "C" {
+
+bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len,
+                          const int32_t* tail_len, const int32_t* prefix_pages, int32_t prefix_pages_stride,
+                          int32_t max_tail, int32_t num_sms, void* image, size_t image_bytes, bsp_plan_t* out) {
+    return plan_build_core(geo, batch, beam_width, prefix_len, tail_len, prefix_pages, prefix_pages_stride, max_tail,
+                           num_sms, image, image_bytes, out, nullptr);
+}
+
+bsp_status bsp_plan_prefill_build(const bsp_geometry* geo, int32_t batch, const int32_t* cached_len,
+                                  const int32_t* prompt_len, const int32_t* pages, int32_t pages_stride,
+                                  int32_t causal, int32_t num_sms, void* image, size_t image_bytes,
+                                  bsp_plan_t* out) {
+    const PrefillSpec pf{cached_len, prompt_len, causal != 0};
+    return plan_build_core(geo, batch, 1, nullptr, nullptr, pages, pages_stride, 0, num_sms, image, image_bytes, out,
+                           &pf);
+}
+
+}  // extern "C"
+
+namespace {
+// Builds a plan into a free slot of the pinned staging buffer (build(sms, slot, bytes, plan)) and
+// enqueues its copy into the device workspace with the generation echo.
+template <typename Build>
+bsp_status stage_plan(void* ws_device, size_t ws_device_bytes, void* ws_host, size_t ws_host_bytes, void* stream,
+                      bsp_plan_t* out, Build build) {
     if (!out || !ws_device || !ws_host) return BSP_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(ws_device) & (kAlign - 1)) || (reinterpret_cast<uintptr_t>(ws_host) & 63u))
         return BSP_ERR_INVALID_ARG;
@@ -498,8 +581,7 @@ bsp_status bsp_plan(const bsp_geometry* geo, int32_t batch, int32_t beam_width, 
         }
     }
     bsp_plan_t plan;
-    bsp_status st = bsp_plan_build(geo, batch, beam_width, prefix_len, tail_len, prefix_pages, prefix_pages_stride,
-                                   max_tail, sms, slot_ptr, slot_bytes, &plan);
+    bsp_status st = build(sms, slot_ptr, slot_bytes, &plan);
     if (st != BSP_OK) return st;
     if (plan.device_bytes_used > ws_device_bytes) return BSP_ERR_CAPACITY;
     std::memcpy(slot_ptr, &gen, sizeof gen);  // image header: generation
@@ -515,6 +597,31 @@ bsp_status bsp_plan(const bsp_geometry* geo, int32_t batch, int32_t beam_width, 
     *out = plan;
     return BSP_OK;
 }
+}  // namespace
+
+extern "C" {
+
+bsp_status bsp_plan(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len,
+                    const int32_t* tail_len, const int32_t* prefix_pages, int32_t prefix_pages_stride, int32_t max_tail,
+                    void* ws_device, size_t ws_device_bytes, void* ws_host, size_t ws_host_bytes, void* stream,
+                    bsp_plan_t* out) {
+    return stage_plan(ws_device, ws_device_bytes, ws_host, ws_host_bytes, stream, out,
+                      [&](int sms, void* img, size_t bytes, bsp_plan_t* p) {
+                          return bsp_plan_build(geo, batch, beam_width, prefix_len, tail_len, prefix_pages,
+                                                prefix_pages_stride, max_tail, sms, img, bytes, p);
+                      });
+}
+
+bsp_status bsp_plan_prefill(const bsp_geometry* geo, int32_t batch, const int32_t* cached_len,
+                            const int32_t* prompt_len, const int32_t* pages, int32_t pages_stride, int32_t causal,
+                            void* ws_device, size_t ws_device_bytes, void* ws_host, size_t ws_host_bytes, void* stream,
+                            bsp_plan_t* out) {
+    return stage_plan(ws_device, ws_device_bytes, ws_host, ws_host_bytes, stream, out,
+                      [&](int sms, void* img, size_t bytes, bsp_plan_t* p) {
+                          return bsp_plan_prefill_build(geo, batch, cached_len, prompt_len, pages, pages_stride,
+                                                        causal, sms, img, bytes, p);
+                      });
+}
 
 bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, const void* v_new, int64_t src_row_stride,
                          const int32_t* out_cache_loc, int32_t n, void* k_pool, void* v_pool,
@@ -524,7 +631,7 @@ bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, const void* 
     if (n < 0) return BSP_ERR_INVALID_ARG;
     if (n == 0) return BSP_OK;
     const bsp_geometry& geo = plan->geo;
-    if (static_cast<int64_t>(n) > static_cast<int64_t>(plan->batch) * plan->beam_width) return BSP_ERR_INVALID_ARG;
+    if (n > plan->total_rows) return BSP_ERR_INVALID_ARG;
     if (src_row_stride < static_cast<int64_t>(geo.num_kv_heads) * geo.head_dim || (src_row_stride & 7))
         return BSP_ERR_INVALID_ARG;
     if (!device_ptr_ok(k_new) || !device_ptr_ok(v_new) || !device_ptr_ok(out_cache_loc) || !device_ptr_ok(k_pool) ||
@@ -563,16 +670,22 @@ bsp_status bsp_read_device_status(const bsp_plan_t* plan, void* stream, int32_t 
     return BSP_OK;
 }
 
-bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
-                           const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
-                           int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse,
-                           void* const* events, void* stream) {
+}  // extern "C"
+
+namespace {
+// The attention launches of a decode step (prefill == false: prompt kernel, then the tail kernel for
+// the requests that need it) or of a prefill (the prompt kernel alone, dense row layout).
+bsp_status attn_impl(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
+                     const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
+                     int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse, void* const* events,
+                     void* stream, bool prefill) {
     bsp_status st = check_plan(plan);
     if (st != BSP_OK) return st;
+    if (plan->kind != (prefill ? 1 : 0)) return BSP_ERR_INVALID_ARG;
     if (flags & ~(BSP_FLAG_LSE_BASE2 | BSP_FLAG_CHECK)) return BSP_ERR_INVALID_ARG;
     if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BSP_ERR_INVALID_ARG;
     const bsp_geometry& geo = plan->geo;
-    const int64_t R = static_cast<int64_t>(plan->batch) * plan->beam_width;
+    const int64_t R = plan->total_rows;
     if (R == 0) return BSP_OK;
     if (!device_ptr_ok(q) || !device_ptr_ok(k_pool) || !device_ptr_ok(v_pool) || !device_ptr_ok(o) ||
         !device_ptr_ok(lse))
@@ -599,7 +712,7 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
         cuuint64_t qdims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(R)};
         cuuint64_t qstr[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2};
         // query rows per TMA box: the row block, or a quadrant's share of it (half-row softmax)
-        const int qbeams = prefix_quad_beams(D, plan->beams_per_block, G);
+        const int qbeams = prefill ? 0 : prefix_quad_beams(D, plan->beams_per_block, G);
         cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(G),
                               static_cast<cuuint32_t>(qbeams > 0 ? qbeams : plan->beams_per_block)};
         const int ps = geo.page_size;
@@ -672,6 +785,24 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
     if (!record(2)) return BSP_ERR_CUDA;
     if (flags & BSP_FLAG_CHECK) return bsp_read_device_status(plan, stream, 1, nullptr);
     return BSP_OK;
+}
+}  // namespace
+
+extern "C" {
+
+bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
+                           int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse,
+                           void* const* events, void* stream) {
+    return attn_impl(plan, q, k_pool, v_pool, beam_pages, beam_pages_stride, cache_indirection, max_seq,
+                     softmax_scale, flags, o, lse, events, stream, false);
+}
+
+bsp_status bsp_prefill_attn(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
+                            float softmax_scale, int32_t flags, void* o, float* lse, void* const* events,
+                            void* stream) {
+    return attn_impl(plan, q, k_pool, v_pool, nullptr, 0, nullptr, 0, softmax_scale, flags, o, lse, events, stream,
+                     true);
 }
 
 }  // extern "C"

@@ -22,8 +22,11 @@ constexpr int kImageHeaderBytes = 64;  // u64 generation, i32 batch, i32 num_uni
 // Per-request record.
 // kReqFused: the prompt kernel finishes the request (one prompt partial state, and every row block's tail
 // keys fit one extra key tile of the prompt kernel); the tail kernel skips it.
+// kReqRows: the request's query rows per (kv head, head in group) - beams for a decode step, prompt
+// tokens for a prefill; kReqRowOff: its first row of q / o (b * W, or the tokens of earlier requests);
+// kReqCausal: -1, or the cached rows C of a causal prefill (row t sees keys 0 .. C + t).
 enum ReqField { kReqPrefix = 0, kReqTail = 1, kReqSplits = 2, kReqPartOff = 3, kReqPageOff = 4, kReqFused = 5,
-                kReqFields = 8 };
+                kReqRows = 8, kReqCausal = 9, kReqRowOff = 10, kReqFields = 12 };
 // keys per tile of the prompt kernel, which bounds a row block's tail keys for the fused tail
 constexpr int prefix_tile_keys(int head_dim) { return head_dim <= 128 ? 128 : 64; }
 // Beams per TMEM lane quadrant when the prompt kernel places a row block's query rows in lanes

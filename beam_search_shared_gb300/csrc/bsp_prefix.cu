@@ -131,6 +131,9 @@ struct UnitInfo {
     int key_begin, key_end;  // keys [key_begin, key_end) of the request's prompt
     int T;                   // tail positions of the request
     bool fused;              // this kernel finishes the request: a tail tile when T > 0, final O / LSE
+    int rows;                // the request's query rows per head (beams, or prompt tokens of a prefill)
+    int causal;              // -1, or the cached rows C of a causal prefill: row t sees keys 0 .. C + t
+    int row_off;             // the request's first row of q and o
 };
 
 __device__ __forceinline__ UnitInfo load_unit(const PrefixParams& p, int u) {
@@ -138,6 +141,7 @@ __device__ __forceinline__ UnitInfo load_unit(const PrefixParams& p, int u) {
     const int4 c = __ldg(reinterpret_cast<const int4*>(p.units + static_cast<long long>(u) * kUnitFields + 4));
     const int4 r = __ldg(reinterpret_cast<const int4*>(p.req + a.x * kReqFields));
     const int4 r2 = __ldg(reinterpret_cast<const int4*>(p.req + a.x * kReqFields + 4));
+    const int4 r3 = __ldg(reinterpret_cast<const int4*>(p.req + a.x * kReqFields + 8));
     UnitInfo ui;
     ui.b = a.x;
     ui.g = a.y;
@@ -149,6 +153,9 @@ __device__ __forceinline__ UnitInfo load_unit(const PrefixParams& p, int u) {
     ui.key_end = min(c.x * kTileKeys, ui.P);
     ui.T = r.y;
     ui.fused = r2.y != 0;                            // kReqFused
+    ui.rows = r3.x;                                  // kReqRows
+    ui.causal = r3.y;                                // kReqCausal
+    ui.row_off = r3.z;                               // kReqRowOff
     return ui;
 }
 
@@ -294,12 +301,12 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     for (int c = 0; c < NC; ++c)
                         for (int i = 0; i < 4; ++i)
                             tma_load_3d(q_buf(k) + c * MR * 128 + i * 16 * 128, &tm_q, &bars->q_full[qb],
-                                        c * 64, ui.g * p.G, ui.b * p.W + ui.rb * p.Wblk + i * p.bq);
+                                        c * 64, ui.g * p.G, ui.row_off + ui.rb * p.Wblk + i * p.bq);
                 } else {
                     mbar_arrive_expect_tx(&bars->q_full[qb], NC * p.Wblk * p.G * 128);
                     for (int c = 0; c < NC; ++c)
                         tma_load_3d(q_buf(k) + c * MR * 128, &tm_q, &bars->q_full[qb], c * 64,
-                                    ui.g * p.G, ui.b * p.W + ui.rb * p.Wblk);
+                                    ui.g * p.G, ui.row_off + ui.rb * p.Wblk);
                 }
             }
             const int ntiles = unit_tiles<TK>(ui);
@@ -473,7 +480,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const UnitInfo cur = load_unit(p, u_begin + k);
             const int ntiles = unit_tiles<TK>(cur);
             const int ptiles = prompt_tiles<TK>(cur);
-            const int nw = min(p.Wblk, p.W - cur.rb * p.Wblk);  // beams of the block
+            const int nw = min(p.Wblk, cur.rows - cur.rb * p.Wblk);  // beams (prompt tokens) of the block
             // the row's own beam's keys in the tail tile: columns [lo, lo + T)
             const int lo = beam * cur.T, hi = lo + cur.T;
             const uint32_t o_col = C::O_COL + (k % NO) * D;
@@ -498,7 +505,11 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     // masked keys count as -inf: they take no part in the maximum and their probability
                     // exp2(-inf) is 0. A prompt tile masks keys >= P_b (a unit's partial last tile only),
                     // the tail tile every key but the row's own beam's readable ones.
-                    const bool partial = valid < TK || tail;
+                    // a causal prefill row t sees keys 0 .. C + t: its own count of valid keys in this tile
+                    int rvalid = valid;
+                    if (cur.causal >= 0)
+                        rvalid = min(valid, cur.causal + cur.rb * p.Wblk + beam + 1 - (cur.key_begin + t * TK));
+                    const bool partial = valid < TK || tail || (cur.causal >= 0 && __any_sync(FULL, rvalid < TK));
                     const uint32_t ninf = __float_as_uint(-INFINITY);
                     // kept columns of a partial tile, one bit per key: [0, valid) of a prompt tile; of the
                     // tail tile the row's own beam's columns [lo, lo + T) (T <= 8, so they span at most two
@@ -512,7 +523,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                 if (s_trow[c] >= 0) win |= 1ull << (c - wbase);
 #pragma unroll
                         for (int j = 0; j < TK / 32; ++j) {
-                            const int n = min(max(valid - 32 * j, 0), 32);
+                            const int n = min(max(rvalid - 32 * j, 0), 32);
                             const uint32_t pm = n == 32 ? ~0u : (1u << n) - 1u;
                             const uint32_t tm = 32 * j == wbase        ? static_cast<uint32_t>(win)
                                                 : 32 * j == wbase + 32 ? static_cast<uint32_t>(win >> 32)
@@ -777,7 +788,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
             gt += unit_tiles<TK>(cur);
             const int w0 = cur.rb * p.Wblk;
-            const int nw = min(p.Wblk, p.W - w0);
+            const int nw = min(p.Wblk, cur.rows - w0);
             // the thread's query row: TMEM lane orow, beam wl of the block, head jh of the group; with
             // SPLIT two threads per row, each writing half of its columns
             const int r16 = lane & 15, ohalf = SPLIT ? lane >> 4 : 0;
@@ -808,7 +819,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const int cb = ohalf * HD;  // first output column of the thread
             if (done.fused) {
                 // the request's whole key set went through this unit: the final O (q dtype) and LSE
-                const long long rh = (static_cast<long long>(done.b) * p.W + (w0 + wl)) * p.Hq + done.g * p.G + jh;
+                const long long rh = (static_cast<long long>(done.row_off) + (w0 + wl)) * p.Hq + done.g * p.G + jh;
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + rh * D);
 #pragma unroll 1
                 for (int c0 = 0; c0 < HD && warp_live; c0 += 32) {

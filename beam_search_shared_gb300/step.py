@@ -109,3 +109,65 @@ def algorithmic_bytes(case: Case, fused: Optional[np.ndarray] = None) -> dict:
     flops = (int(np.sum(P)) + int(np.sum(T[fz]))) * W * Hq * D * 4
     return {"prefix": prefix, "tail": tail, "append": append, "prefix_flops": flops,
             "prefix_kv": prefix_kv}
+
+
+class PrefillStep:
+    """Device buffers of one synthetic prefill (synth.PrefillCase), its plan, append and attention."""
+
+    def __init__(self, case, device="cuda"):
+        wl = case.workload
+        self.case = case
+        dev = torch.device(device)
+        self.geo = bsp.geometry(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.page_size, case.num_pages,
+                                wl.dtype)
+        self.q = case.q.to(dev)
+        self.k_pool = case.k_pool.to(dev)
+        self.v_pool = case.v_pool.to(dev)
+        R, row = case.rows, wl.num_kv_heads * wl.head_dim
+        self.k_new = case.k_new.to(dev).reshape(R, row)
+        self.v_new = case.v_new.to(dev).reshape(R, row)
+        self.out_cache_loc = torch.from_numpy(case.out_cache_loc).to(dev)
+        self.o = torch.empty((R, wl.num_q_heads, wl.head_dim), dtype=self.q.dtype, device=dev)
+        self.lse = torch.empty((R, wl.num_q_heads), dtype=torch.float32, device=dev)
+        self.scale = 1.0 / math.sqrt(wl.head_dim)
+        self.ws = bsp.Workspace(self.geo, max(1, wl.batch), max(1, int(case.prompt_len.max(initial=0))),
+                                case.pages.shape[1], device=dev)
+        self.plan = None
+
+    def make_plan(self, stream=None):
+        c = self.case
+        self.plan = bsp.plan_prefill(self.geo, c.workload.batch, c.cached_len, c.prompt_len, c.pages,
+                                     c.workload.causal, self.ws, stream=stream)
+        return self.plan
+
+    def append(self, stream=None):
+        bsp.append_kv(self.plan, self.k_new, self.v_new, self.out_cache_loc, self.k_pool, self.v_pool, stream=stream)
+
+    def attend(self, flags: int = 0, events=None, stream=None):
+        bsp.prefill_attn(self.plan, self.q, self.k_pool, self.v_pool, self.scale, self.o, self.lse, flags=flags,
+                         events=events, stream=stream)
+
+    def run(self, flags: int = 0, stream=None):
+        """plan + append of the prompt's K/V + attention, then the device status (syncs)."""
+        self.make_plan(stream)
+        self.append(stream)
+        self.attend(flags, stream=stream)
+        return bsp.read_device_status(self.plan, clear=True, stream=stream)
+
+
+def prefill_work(case) -> dict:
+    """Algorithmic bytes and flops of a prefill attention (the prompt kernel): each (request, kv head)
+    reads its keys' K and V once per block of rows that needs them, plus Q and O/LSE; the flops count
+    only the (row, key) pairs the mask keeps (Q*K^T and P*V, 2 flops per multiply-add)."""
+    wl = case.workload
+    e = 2
+    D, Hq, Hkv = wl.head_dim, wl.num_q_heads, wl.num_kv_heads
+    C = case.cached_len.astype(np.int64)
+    S = case.prompt_len.astype(np.int64)
+    if wl.causal:
+        pairs = int(np.sum(C * S + S * (S + 1) // 2))
+    else:
+        pairs = int(np.sum(S * (C + S)))
+    kv_bytes = int(np.sum(np.where(S > 0, C + S, 0))) * Hkv * D * e * 2   # each key once per kv head
+    io_bytes = int(S.sum()) * Hq * (D * e * 2 + 4)                         # Q in, O and LSE out
+    return {"bytes": kv_bytes + io_bytes, "flops": pairs * Hq * D * 4, "pairs": pairs}

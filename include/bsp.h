@@ -129,8 +129,11 @@ typedef struct bsp_plan_t {
                                     several partial states, or more tail keys per row block than one
                                     tile holds); the prompt kernel finishes the others. No tail launch
                                     when 0 */
-    int32_t reserved0;
-    uint64_t reserved[3];
+    int32_t total_rows;          /* query rows of the step: batch * beam_width (decode) or the prompt
+                                    tokens of all requests (prefill) */
+    int32_t kind;                /* 0: a decode-step plan (bsp_plan); 1: a prefill plan (bsp_plan_prefill) */
+    int32_t reserved1;
+    uint64_t reserved[2];
 } bsp_plan_t;
 
 /* Human-readable name of a bsp_status value. Never NULL. */
@@ -249,6 +252,49 @@ BSP_API bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const 
                            const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
                            int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse,
                            void* const* events, void* stream);
+
+/*
+ * Prefill over the cached prefix (TensorRT-Model-Connect PR #2202, "prefill and
+ * decode over the cached prefix, not the whole KV allocation", Implementation:
+ * the prompt rows attend the bound cache rows and then the prompt rows, with
+ * only the valid cached prefix bound). Request b holds cached_len[b] >= 0 valid
+ * cached rows and prompt_len[b] >= 0 prompt tokens, whose K/V the caller has
+ * already written (bsp_append_kv) at logical positions cached_len[b] ..
+ * cached_len[b] + prompt_len[b] - 1; every position p of request b is read
+ * through its page table: page = pages[b * pages_stride + p / page_size],
+ * slot = p % page_size (the first ceil((cached + prompt) / page_size) entries
+ * must lie in [0, num_pages), else BSP_ERR_PAGE_INDEX). With `causal` != 0,
+ * prompt token i sees positions 0 .. cached_len[b] + i, else all
+ * cached_len[b] + prompt_len[b] positions. Positions past those are never
+ * read. The query rows are the prompt tokens of all requests in order (request
+ * b's tokens start at the sum of the earlier prompt_len), `total_rows` in all.
+ * bsp_plan_prefill_build writes the host image only (as bsp_plan_build);
+ * bsp_plan_prefill stages it without a sync (as bsp_plan); the workspace must
+ * hold a plan of max_batch = batch and max_beam = the largest prompt_len
+ * (bsp_workspace_size).
+ */
+BSP_API bsp_status bsp_plan_prefill_build(const bsp_geometry* geo, int32_t batch, const int32_t* cached_len,
+                                  const int32_t* prompt_len, const int32_t* pages, int32_t pages_stride,
+                                  int32_t causal, int32_t num_sms, void* image, size_t image_bytes,
+                                  bsp_plan_t* plan_out);
+BSP_API bsp_status bsp_plan_prefill(const bsp_geometry* geo, int32_t batch, const int32_t* cached_len,
+                            const int32_t* prompt_len, const int32_t* pages, int32_t pages_stride,
+                            int32_t causal, void* ws_device, size_t ws_device_bytes, void* ws_host,
+                            size_t ws_host_bytes, void* stream, bsp_plan_t* plan_out);
+
+/*
+ * The prefill attention of a bsp_plan_prefill plan: for every prompt row r and
+ * query head h, O[r][h] = softmax(scale * q K^T) V and LSE[r][h] over the keys
+ * the plan gives that row, on the tensor cores (the prompt kernel, each
+ * (request, kv head, block of 128 / G prompt tokens) a work unit; a causal
+ * block reads keys only up to its last token). q, o [total_rows][Hq][head_dim]
+ * in the pools' dtype, lse [total_rows][Hq] fp32 (natural log, or base 2 with
+ * BSP_FLAG_LSE_BASE2). A decode plan is BSP_ERR_INVALID_ARG here (and a prefill
+ * plan in bsp_decode_attn). events: NULL or 3 cudaEvent_t, as bsp_decode_attn.
+ */
+BSP_API bsp_status bsp_prefill_attn(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
+                            float softmax_scale, int32_t flags, void* o, float* lse, void* const* events,
+                            void* stream);
 
 /*
  * Synchronises `stream`, then reads the workspace's device status word into

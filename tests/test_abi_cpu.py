@@ -105,7 +105,7 @@ def test_plan_build_validation(lib):
 def decode_image(plan, img, with_cta=False):
     i32 = img.view(np.int32)
     base = STATUS_OFFSET
-    req = i32[(plan.off_req - base) // 4:(plan.off_units - base) // 4].reshape(plan.batch, 8)
+    req = i32[(plan.off_req - base) // 4:(plan.off_units - base) // 4].reshape(plan.batch, 12)
     u0 = (plan.off_units - base) // 4
     units = i32[u0:u0 + plan.num_units * 8].reshape(plan.num_units, 8)
     cta_off = i32[u0 + plan.num_units * 8:(plan.off_pages - base) // 4]
@@ -163,6 +163,9 @@ def test_plan_image_wide_batch_needs_no_split(lib):
     np.testing.assert_array_equal(req[:, 0], P)
     np.testing.assert_array_equal(req[:, 1], T)
     np.testing.assert_array_equal(req[:, 2], 1)
+    # rows per request, no causal limit, first row b * W
+    np.testing.assert_array_equal(req[:, 8:11], np.stack([np.full(B, W), np.full(B, -1), np.arange(B) * W], 1))
+    assert plan.total_rows == B * W and plan.kind == 0
     check_units_cover(plan, req, units, P)
     check_fused(plan, req, T)
     assert plan.tail_requests == 0                          # 30 beams x <= 4 tail keys fit one tile
@@ -235,3 +238,40 @@ def test_plan_struct_layout_matches_header(lib):
     names = [f[0] for f in bsp.Plan._fields_]
     assert fields == names
     assert ctypes.sizeof(bsp.Plan) % 8 == 0
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_plan_units_and_records(lib, causal):
+    """A prefill plan: the prompt tokens are the rows (blocks of 128 / G tokens), keys are the cached
+    rows and the prompt, no tail and no key splits; a causal block reads keys only up to its last
+    token (rounded up to a 64-key plan tile)."""
+    C = np.array([0, 300, 5, 40])
+    S = np.array([1000, 7, 0, 200])
+    ps = 32
+    maxp = -(-(C + S).max() // ps)
+    rng = np.random.default_rng(4)
+    pages = rng.integers(0, 400, (4, maxp)).astype(np.int32)
+    g = geo(Hq=32, Hkv=8, npages=400)   # G = 4: blocks of 32 tokens
+    plan, img = bsp.plan_prefill_build(g, 4, C, S, pages, causal, 152)
+    req, units, pl = decode_image(plan, img)
+    assert plan.kind == 1 and plan.total_rows == S.sum() and plan.tail_requests == 0
+    assert plan.beams_per_block == 32 and plan.max_tail_len == 0
+    np.testing.assert_array_equal(req[:, 0], np.where(S > 0, C + S, 0))
+    np.testing.assert_array_equal(req[:, 1], 0)
+    np.testing.assert_array_equal(req[:, 8], S)
+    np.testing.assert_array_equal(req[:, 9], C if causal else -1)
+    np.testing.assert_array_equal(req[:, 10], np.concatenate([[0], np.cumsum(S)[:-1]]))
+    np.testing.assert_array_equal(req[:, 5], (S > 0).astype(np.int32))
+    np.testing.assert_array_equal(req[:, 2], (S > 0).astype(np.int32))
+    want = set()
+    for b in range(4):
+        for gg in range(8):
+            for rb in range(-(-S[b] // 32)):
+                last = min(S[b], (rb + 1) * 32)
+                end = -(-(C[b] + last) // 64) if causal else -(-(C[b] + S[b]) // 64)
+                want.add((b, gg, rb, 0, end))
+    got = set(tuple(int(x) for x in u[:5]) for u in units)
+    assert got == want
+    for b in range(4):
+        n = -(-(C[b] + S[b]) // ps) if S[b] else 0
+        np.testing.assert_array_equal(pl[req[b][4]:req[b][4] + n], pages[b, :n])
