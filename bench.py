@@ -221,6 +221,8 @@ def main():
     args = parse()
     rank, world, local = dist_init(args)
     from beam_search_shared_gb300 import synth
+    if args.workload in synth.PREFILL_WORKLOADS:
+        return run_prefill(args, rank, world, local)
     wl = synth.WORKLOADS[args.workload]
     R = wl.batch * wl.beam_width
 
@@ -460,6 +462,221 @@ def run_e2e(st, steps, world):
     st.make_plan()  # leave the set's own plan current
     torch.cuda.synchronize()
     return {"value": world * steps / dt, "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+# ---------------------------------------------------------------- prefill over the cached prefix
+PREFILL_METRIC = "prefill tokens/s"
+
+
+def run_prefill(args, rank, world, local):
+    """Prefill over the cached prefix: a step = bsp_append_kv of the prompt tokens' K/V + bsp_prefill_attn.
+    `value` is prompt tokens per second over all ranks; the roofline is the prompt kernel's tensor
+    throughput (flops of the kept (row, key) pairs only) against the measured dense 16-bit peak."""
+    from beam_search_shared_gb300 import bsp, synth
+    from beam_search_shared_gb300.step import PrefillStep, prefill_work
+    wl = synth.PREFILL_WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if rank == 0:
+            v, cores, sample = prefill_oracle_rate(wl, args.cpu_seconds)
+            print(json.dumps({"impl": "reference", "metric": PREFILL_METRIC, "value": v, "unit": "tokens/s",
+                              "n_gpus": args.gpus, "steps": args.steps, "warmup": max(3, args.warmup),
+                              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                              "data": "synthetic", "config": {"workload": wl.name},
+                              "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                               "sample": sample},
+                              "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                      "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    bsp.load(build_if_missing=True)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    sets = []
+    for i in range(args.sets):
+        st = PrefillStep(synth.make_prefill_case(wl, 2000 + 97 * rank + i, device=dev), device=dev)
+        st.make_plan()
+        sets.append(st)
+    torch.cuda.synchronize()
+    work = [prefill_work(s.case) for s in sets]
+    tokens = [s.case.rows for s in sets]
+    for i in range(max(3, args.warmup)):
+        s = sets[i % len(sets)]
+        s.append()
+        s.attend()
+    torch.cuda.synchronize()
+    for s in sets:
+        assert bsp.read_device_status(s.plan) == (0, 0)
+    K = args.steps
+    stream = torch.cuda.current_stream()
+    # the prompt kernel alone, back to back, one event pair around the graph
+    Kt = min(K, 50)
+    g_p = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_p):
+        for j in range(Kt):
+            sets[j % len(sets)].attend()
+    g_p.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g_p.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    attn_ms = e0.elapsed_time(e1) / Kt
+    # timed region: K steps (append + attention) from graphs without timing nodes
+    chunk = min(K, 500)
+    sizes = [chunk] * (K // chunk) + ([K % chunk] if K % chunk else [])
+    graphs, done = [], 0
+    for n in sizes:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for j in range(n):
+                s = sets[(done + j) % len(sets)]
+                s.append()
+                s.attend()
+        graphs.append(g)
+        done += n
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for g in graphs:
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    elapsed_ms = reduce_max(ev0.elapsed_time(ev1), world)
+    tok_per_step = statistics.mean(tokens[j % len(sets)] for j in range(K))
+    value = world * K * tok_per_step / (elapsed_ms / 1e3)
+    for s in sets:
+        assert bsp.read_device_status(s.plan) == (0, 0)
+    hbm_gbs, bf16_tflops, peak_kind = measured_peaks()
+    flops = statistics.mean(w["flops"] for w in work)
+    achieved = flops / (attn_ms / 1e3) / 1e12
+    e2e = run_prefill_e2e(sets[0], args.e2e_steps, world)
+    line = {
+        "metric": PREFILL_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.batch, "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads,
+                   "head_dim": wl.head_dim, "page_size": wl.page_size, "cached": f"U{{{wl.cached[0]}..{wl.cached[1]}}}",
+                   "prompt": f"U{{{wl.prompt[0]}..{wl.prompt[1]}}}", "causal": wl.causal,
+                   "alloc_rows": wl.alloc_rows, "parallelism": f"dp{world} (independent batches)",
+                   "l2": f"{len(sets)} rotated input sets, pools of "
+                         f"{sum(s.k_pool.numel() * 4 for s in sets) / 1e6:.0f} MB in all",
+                   "us_prefill_attn": 1e3 * attn_ms, "prefill_attn_gbs": statistics.mean(w["bytes"] for w in work)
+                   / (attn_ms / 1e3) / 1e9},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_tflops, "unit": "TFLOP/s",
+                     "frac": achieved / bf16_tflops, "traffic": None, "kernel": "prefix_attn_kernel",
+                     "peak_kind": peak_kind + " (16-bit dense; fp16 runs at the bf16 rate)",
+                     "algorithmic_flops_per_launch": flops},
+        "e2e": e2e,
+        "gpu_launches": K * 2,
+        "timing": f"value: CUDA-graph replay of exactly K steps (append + attention) without timing nodes; "
+                  f"us_prefill_attn: one event pair around {Kt} back-to-back attention launches",
+        "clocks": clk.result,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = prefill_oracle_rate(wl, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def prefill_oracle_rate(wl, seconds):
+    """The fp64 oracle's prefill rate on the host cores: one request of the workload's shape with fewer
+    prompt tokens (sized from a short probe to take about `seconds`), scaled by the kept (row, key) pairs
+    to the workload's own mix."""
+    import oracle
+    from beam_search_shared_gb300 import synth
+    from beam_search_shared_gb300.step import prefill_work
+    oracle.build()
+    full = synth.make_prefill_case(wl, 2000)
+    C0 = int(full.cached_len[0])
+
+    def timed(S):
+        sub = wl.with_(batch=1, alloc_rows=0)
+        case = synth.make_prefill_case(sub, 2001, cached_lengths=[C0], prompt_lengths=[S])
+        t0 = time.perf_counter()
+        oracle.prefill_attn(dtype=sub.dtype, B=1, Hq=sub.num_q_heads, Hkv=sub.num_kv_heads, D=sub.head_dim,
+                            ps=sub.page_size, num_pages=case.num_pages, cached_len=case.cached_len,
+                            prompt_len=case.prompt_len, pages=case.pages, causal=sub.causal,
+                            q_bits=synth.bits(case.q), k_pool_bits=synth.bits(case.k_pool),
+                            v_pool_bits=synth.bits(case.v_pool), scale=1 / math.sqrt(sub.head_dim))
+        return time.perf_counter() - t0, case
+
+    S_max = int(max(1, full.prompt_len.max()))
+    S = min(S_max, 16)
+    t, case = timed(S)
+    per_pair = t / max(1, prefill_work(case)["pairs"])
+    while S < S_max:
+        # the largest prompt whose pairs fit the budget at the probed rate
+        nxt = S
+        while nxt < S_max:
+            c_try = nxt * 2 if nxt * 2 <= S_max else S_max
+            pairs = C0 * c_try + c_try * (c_try + 1) // 2 if wl.causal else c_try * (C0 + c_try)
+            if pairs * per_pair > seconds:
+                break
+            nxt = c_try
+        if nxt == S:
+            break
+        S = nxt
+        t, case = timed(S)
+        per_pair = t / max(1, prefill_work(case)["pairs"])
+    pf, ps_ = prefill_work(full), prefill_work(case)
+    full_seconds = t * pf["pairs"] / max(1, ps_["pairs"])
+    cores = len(os.sched_getaffinity(0))
+    cores = min(cores, int(os.environ.get("OMP_NUM_THREADS", cores)))   # the oracle's OpenMP threads
+    sample = (f"1 request of {S} prompt tokens after {C0} cached rows ({t:.1f} s), scaled by kept (row, key) "
+              f"pairs to the {full.rows} prompt tokens of the workload; attention only; {cpu_model()}")
+    return full.rows / full_seconds, cores, sample
+
+
+def run_prefill_e2e(st, steps, world):
+    """Prefill steps from pinned host buffers through the public API: plan from host arrays, H2D of q,
+    the prompt K/V and its slots, append + attention, D2H of O and LSE; timed on the host."""
+    from beam_search_shared_gb300 import bsp
+    c = st.case
+    h_q = st.q.cpu().pin_memory()
+    h_kn, h_vn = st.k_new.cpu().pin_memory(), st.v_new.cpu().pin_memory()
+    h_loc = torch.from_numpy(c.out_cache_loc).pin_memory()
+    h_o = torch.empty(st.o.shape, dtype=st.o.dtype).pin_memory()
+    h_lse = torch.empty(st.lse.shape, dtype=torch.float32).pin_memory()
+    d_q, d_kn, d_vn = torch.empty_like(st.q), torch.empty_like(st.k_new), torch.empty_like(st.v_new)
+    d_loc = torch.empty_like(st.out_cache_loc)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_loc)) + int(st.plan.image_bytes)
+    d2h = h_o.numel() * h_o.element_size() + h_lse.numel() * 4
+
+    def one():
+        plan = bsp.plan_prefill(st.geo, c.workload.batch, c.cached_len, c.prompt_len, c.pages, c.workload.causal,
+                                st.ws)
+        d_q.copy_(h_q, non_blocking=True)
+        d_kn.copy_(h_kn, non_blocking=True)
+        d_vn.copy_(h_vn, non_blocking=True)
+        d_loc.copy_(h_loc, non_blocking=True)
+        bsp.append_kv(plan, d_kn, d_vn, d_loc, st.k_pool, st.v_pool)
+        bsp.prefill_attn(plan, d_q, st.k_pool, st.v_pool, st.scale, st.o, st.lse)
+        h_o.copy_(st.o, non_blocking=True)
+        h_lse.copy_(st.lse, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = reduce_max(time.perf_counter() - t0, world)
+    st.make_plan()  # leave the set's own plan current
+    torch.cuda.synchronize()
+    return {"value": world * steps * c.rows / dt, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps}
 
 
