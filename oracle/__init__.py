@@ -64,6 +64,15 @@ def _load():
                                                        ctypes.c_double, p, p]
     lib.orc_append_kv.restype = ctypes.c_int
     lib.orc_append_kv.argtypes = [ctypes.c_int] * 5 + [p, p, p, ctypes.c_int64, p, p]
+    lib.orc_round_half.restype = ctypes.c_uint16
+    lib.orc_round_half.argtypes = [ctypes.c_double, ctypes.c_int]
+    lib.orc_rope_cos_sin.restype = None
+    lib.orc_rope_cos_sin.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, p]
+    lib.orc_rope_rotate.restype = None
+    lib.orc_rope_rotate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, p, p]
+    lib.orc_rope_append_kv.restype = ctypes.c_int
+    lib.orc_rope_append_kv.argtypes = ([ctypes.c_int] * 6 + [ctypes.c_double] + [ctypes.c_int] * 4 +
+                                       [p, p, p, ctypes.c_int64, p, p, ctypes.c_int64, p, p])
     _lib = lib
     return lib
 
@@ -181,3 +190,54 @@ def append_kv(*, Hkv, D, ps, num_pages, out_cache_loc, k_new_bits, v_new_bits, k
                                int(row_stride), _ptr(k_pool_bits), _ptr(v_pool_bits))
     if rc != 0:
         raise ValueError(f"oracle append_kv: {ERRORS.get(rc, rc)}")
+
+
+def round_half(x: float, dtype: str) -> int:
+    """Nearest bf16 / binary16 bit pattern of a double, ties to even."""
+    return int(_load().orc_round_half(float(x), DTYPES[dtype]))
+
+
+def round_half_array(x, dtype: str) -> np.ndarray:
+    """round_half over an array (a loop over the C routine; small inputs)."""
+    x = np.asarray(x, np.float64)
+    f = _load().orc_round_half
+    d = DTYPES[dtype]
+    return np.array([f(float(v), d) for v in x.reshape(-1)], np.uint16).reshape(x.shape)
+
+
+def rope_cos_sin(max_pos: int, rot: int, base: float) -> np.ndarray:
+    """fp64 [max_pos][rot]: cos(p*theta_j) for j < rot/2, then sin(p*theta_j)."""
+    cs = np.empty((max_pos, rot), np.float64)
+    _load().orc_rope_cos_sin(int(max_pos), int(rot), float(base), _ptr(cs))
+    return cs
+
+
+def rope_rotate(x, *, rot: int, interleaved: bool, base: float, pos: int) -> np.ndarray:
+    """One head row (fp64 [D]) rotated by position ``pos``, unrounded."""
+    x = _c(x, np.float64)
+    y = np.empty_like(x)
+    _load().orc_rope_rotate(x.shape[0], int(rot), 1 if interleaved else 0, float(base), int(pos), _ptr(x), _ptr(y))
+    return y
+
+
+def rope_append_kv(*, dtype, Hq, Hkv, D, rot, interleaved, base, max_pos, ps, num_pages, positions,
+                   out_cache_loc, q_bits, k_new_bits, v_new_bits, k_pool_bits, v_pool_bits,
+                   q_row_stride=None, row_stride=None):
+    """RoPE on the paged append, in place on uint16 arrays: rotated K and plain V rows into the pools,
+    the query rows (``q_bits`` [n][..], may be None) rotated in place. Raises on a bad slot or
+    position (nothing written)."""
+    pos = _c(positions, np.int32)
+    loc = _c(out_cache_loc, np.int32)
+    n = loc.shape[0]
+    for a in (k_pool_bits, v_pool_bits) + (() if q_bits is None else (q_bits,)):
+        assert a.dtype == np.uint16 and a.flags.c_contiguous
+    kn = _c(k_new_bits, np.uint16).reshape(n, -1) if n else np.zeros((0, Hkv * D), np.uint16)
+    vn = _c(v_new_bits, np.uint16).reshape(n, -1) if n else np.zeros((0, Hkv * D), np.uint16)
+    rs = kn.shape[1] if row_stride is None else int(row_stride)
+    qrs = 0 if q_bits is None else (q_bits.size // max(n, 1) if q_row_stride is None else int(q_row_stride))
+    rc = _load().orc_rope_append_kv(
+        DTYPES[dtype], Hq, Hkv, D, int(rot), 1 if interleaved else 0, float(base), int(max_pos), ps, num_pages, n,
+        _ptr(pos), _ptr(loc), None if q_bits is None else _ptr(q_bits), qrs, _ptr(kn), _ptr(vn), rs,
+        _ptr(k_pool_bits), _ptr(v_pool_bits))
+    if rc != 0:
+        raise ValueError(f"oracle rope_append_kv: {ERRORS.get(rc, rc)}")

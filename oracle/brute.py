@@ -104,3 +104,77 @@ def prefill_attn(*, dtype, B, Hq, Hkv, D, ps, cached_len, prompt_len, pages, cau
             L.append(row_l)
             r += 1
     return O, L
+
+
+def nearest_half_bits(x: float, dtype: str) -> int:
+    """Nearest 16-bit pattern of a Python float by search over every finite pattern of the format
+    (ties to the pattern with the even fraction; past the largest finite value by half its spacing or
+    more: infinity). Slow and obvious; for small inputs."""
+    global _FINITE
+    if math.isnan(x):
+        return 0x7FC0 if dtype == "bf16" else 0x7E00
+    key = dtype
+    if key not in _FINITE:
+        vals = []
+        for b in range(0x8000):
+            v = half_bits_to_float(b, dtype)
+            if math.isfinite(v):
+                vals.append((v, b))
+        vals.sort()
+        _FINITE[key] = vals
+    vals = _FINITE[key]
+    sign = 0x8000 if math.copysign(1.0, x) < 0 else 0
+    a = abs(x)
+    top, top_bits = vals[-1]
+    step = top - vals[-2][0]
+    if a >= top + step / 2:
+        return sign | (top_bits + 1)          # the infinity pattern follows the largest finite one
+    lo, hi = 0, len(vals) - 1
+    while lo < hi:                             # first value >= a
+        mid = (lo + hi) // 2
+        if vals[mid][0] < a:
+            lo = mid + 1
+        else:
+            hi = mid
+    if vals[lo][0] == a or lo == 0:
+        return sign | vals[lo][1]
+    below, above = vals[lo - 1], vals[lo]
+    if a - below[0] < above[0] - a:
+        return sign | below[1]
+    if a - below[0] > above[0] - a:
+        return sign | above[1]
+    return sign | (below[1] if below[1] % 2 == 0 else above[1])
+
+
+_FINITE: dict = {}
+
+
+def rope_rotate(x, *, rot, interleaved, base, pos):
+    """RoPE of one head row as complex multiplication (RoFormer, the complex form of section 3.2):
+    pair j is the complex number x_a + i x_b, multiplied by e^{i pos theta_j}, theta_j = base^(-2j/rot)."""
+    half = rot // 2
+    y = list(x)
+    for j in range(half):
+        a, b = (2 * j, 2 * j + 1) if interleaved else (j, j + half)
+        theta = base ** (-2.0 * j / rot)
+        z = complex(x[a], x[b]) * complex(math.cos(pos * theta), math.sin(pos * theta))
+        y[a], y[b] = z.real, z.imag
+    return y
+
+
+def rope_append_kv(*, dtype, Hq, Hkv, D, rot, interleaved, base, ps, positions, out_cache_loc, q_bits,
+                   k_new_bits, v_new_bits, k_pool_bits, v_pool_bits):
+    """Nested-list restatement of the RoPE paged append (in place on the nested lists): rotated K and
+    plain V of token i, head h at pool[loc // ps][h][loc % ps]; q rows of token i rotated in place."""
+    for i, (p, loc) in enumerate(zip(positions, out_cache_loc)):
+        page, off = loc // ps, loc % ps
+        for h in range(Hkv):
+            k = [half_bits_to_float(v, dtype) for v in k_new_bits[i][h]]
+            k_pool_bits[page][h][off] = [nearest_half_bits(v, dtype)
+                                         for v in rope_rotate(k, rot=rot, interleaved=interleaved, base=base, pos=p)]
+            v_pool_bits[page][h][off] = list(v_new_bits[i][h])
+        if q_bits is not None:
+            for h in range(Hq):
+                qv = [half_bits_to_float(v, dtype) for v in q_bits[i][h]]
+                q_bits[i][h] = [nearest_half_bits(v, dtype)
+                                for v in rope_rotate(qv, rot=rot, interleaved=interleaved, base=base, pos=p)]

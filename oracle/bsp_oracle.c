@@ -370,3 +370,136 @@ int orc_append_kv(int Hkv, int D, int ps, int num_pages, int n, const int32_t *l
     }
     return ORC_OK;
 }
+
+/* Nearest bf16 or IEEE binary16 value of a double, ties to the even fraction
+ * (round to nearest even, the IEEE default), as a bit pattern. Values past the
+ * largest finite one by half a unit or more become infinity; NaN becomes the
+ * quiet NaN with a clear sign bit. Written from the formats' definitions:
+ * bf16 has 8 exponent bits (bias 127) and 7 fraction bits, binary16 has 5
+ * (bias 15) and 10; below the smallest normal the spacing stays that of the
+ * smallest binade (subnormals). */
+uint16_t orc_round_half(double x, int dtype)
+{
+    const int frac_bits = dtype == ORC_BF16 ? 7 : 10;
+    const int emin = dtype == ORC_BF16 ? -126 : -14;   /* exponent of the smallest normal */
+    const int emax = dtype == ORC_BF16 ? 127 : 15;     /* exponent of the largest binade */
+    const int bias = dtype == ORC_BF16 ? 127 : 15;
+    const uint16_t exp_ones = (uint16_t)(((1u << (15 - frac_bits)) - 1u) << frac_bits);
+    if (isnan(x))
+        return (uint16_t)(exp_ones | (1u << (frac_bits - 1)));
+    const uint16_t sign = signbit(x) ? (uint16_t)0x8000u : (uint16_t)0;
+    const double a = fabs(x);
+    if (isinf(a))
+        return (uint16_t)(sign | exp_ones);
+    if (a == 0.0)
+        return sign;
+    int e;
+    frexp(a, &e);                       /* a in [2^(e-1), 2^e) */
+    int be = e - 1;
+    if (be < emin)
+        be = emin;
+    const double spacing = ldexp(1.0, be - frac_bits);
+    const double r = nearbyint(a / spacing) * spacing;   /* default mode: ties to even */
+    if (r >= ldexp(1.0, emax + 1))
+        return (uint16_t)(sign | exp_ones);
+    if (r == 0.0)                       /* below half the smallest subnormal */
+        return sign;
+    int re;
+    frexp(r, &re);
+    const int rbe = re - 1;
+    if (rbe < emin)                     /* subnormal: exponent field 0 */
+        return (uint16_t)(sign | (uint16_t)(r / ldexp(1.0, emin - frac_bits)));
+    const uint32_t frac = (uint32_t)(r / ldexp(1.0, rbe - frac_bits)) - (1u << frac_bits);
+    return (uint16_t)(sign | (uint16_t)((uint32_t)(rbe + bias) << frac_bits) | (uint16_t)frac);
+}
+
+/* Rotary position embedding (RoPE; Su et al., "RoFormer: Enhanced Transformer
+ * with Rotary Position Embedding", the rotation matrix of its section 3.2). The
+ * pages apply it to K before the paged write (TensorRT-LLM PR #21738, the review
+ * of flash_attn4_kernels.py: the rope_write_kv_paged helper and its partial-RoPE
+ * partner lookup; the description: the model applies RoPE itself, Qwen3 for
+ * instance), but do not define it; this is the published definition.
+ *
+ * The first `rot` of the D dims of a head row form rot/2 pairs; pair j turns by
+ * the angle pos * theta_j with theta_j = base^(-2j/rot). Pair j is (j, j + rot/2)
+ * (the rotate-half layout of GPT-NeoX-style models such as Qwen3) or, with
+ * `interleaved`, (2j, 2j + 1) (the paper's own layout). A pair (x, y) becomes
+ * (x cos - y sin, y cos + x sin). Dims >= rot are left as they are. */
+void orc_rope_cos_sin(int max_pos, int rot, double base, double *cs)
+{
+    const int half = rot / 2;
+    for (int p = 0; p < max_pos; ++p)
+        for (int j = 0; j < half; ++j) {
+            const double angle = (double)p * pow(base, -2.0 * (double)j / (double)rot);
+            cs[(size_t)p * rot + j] = cos(angle);
+            cs[(size_t)p * rot + half + j] = sin(angle);
+        }
+}
+
+void orc_rope_rotate(int D, int rot, int interleaved, double base, int pos, const double *x, double *y)
+{
+    const int half = rot / 2;
+    for (int d = rot; d < D; ++d)
+        y[d] = x[d];
+    for (int j = 0; j < half; ++j) {
+        const double angle = (double)pos * pow(base, -2.0 * (double)j / (double)rot);
+        const double c = cos(angle), s = sin(angle);
+        const int i0 = interleaved ? 2 * j : j;
+        const int i1 = interleaved ? 2 * j + 1 : j + half;
+        y[i0] = x[i0] * c - x[i1] * s;
+        y[i1] = x[i1] * c + x[i0] * s;
+    }
+}
+
+/* RoPE on the paged append: for each new token i (position pos[i], slot loc[i])
+ * and kv head h, the rotated K row and the V row are written at
+ * pool[loc / ps][h][loc % ps][:]; when q is non-NULL, the token's Hq query rows
+ * (q + i*q_row_stride + h*D) are rotated in place by the same position. Rotated
+ * values are computed in fp64 from the exact inputs and rounded once to the
+ * dtype (orc_round_half). All slots and positions (0 <= pos < max_pos) are
+ * checked first: a bad one leaves pools and q unchanged. */
+int orc_rope_append_kv(int dtype, int Hq, int Hkv, int D, int rot, int interleaved, double base, int max_pos,
+                       int ps, int num_pages, int n, const int32_t *pos, const int32_t *loc,
+                       uint16_t *q, int64_t q_row_stride, const uint16_t *knew, const uint16_t *vnew,
+                       int64_t row_stride, uint16_t *kpool, uint16_t *vpool)
+{
+    if (rot < 2 || rot > D || (rot & 1) || !(base > 0.0))
+        return ORC_ERR_ARG;
+    for (int i = 0; i < n; ++i) {
+        if (loc[i] < 0 || (int64_t)loc[i] >= (int64_t)num_pages * ps)
+            return ORC_ERR_INDEX;
+        if (pos[i] < 0 || pos[i] >= max_pos)
+            return ORC_ERR_INDEX;
+    }
+    double *x = malloc(sizeof(double) * (size_t)D), *y = malloc(sizeof(double) * (size_t)D);
+    if (!x || !y) {
+        free(x);
+        free(y);
+        return ORC_ERR_NOMEM;
+    }
+    for (int i = 0; i < n; ++i) {
+        const int64_t page = loc[i] / ps, off = loc[i] % ps;
+        for (int h = 0; h < Hkv; ++h) {
+            const size_t dst = (((size_t)page * Hkv + h) * ps + (size_t)off) * D;
+            const size_t src = (size_t)i * (size_t)row_stride + (size_t)h * D;
+            for (int d = 0; d < D; ++d)
+                x[d] = orc_half_to_double(knew[src + d], dtype);
+            orc_rope_rotate(D, rot, interleaved, base, pos[i], x, y);
+            for (int d = 0; d < D; ++d)
+                kpool[dst + d] = orc_round_half(y[d], dtype);
+            memcpy(vpool + dst, vnew + src, sizeof(uint16_t) * (size_t)D);
+        }
+        if (q)
+            for (int h = 0; h < Hq; ++h) {
+                uint16_t *row = q + (size_t)i * (size_t)q_row_stride + (size_t)h * D;
+                for (int d = 0; d < D; ++d)
+                    x[d] = orc_half_to_double(row[d], dtype);
+                orc_rope_rotate(D, rot, interleaved, base, pos[i], x, y);
+                for (int d = 0; d < D; ++d)
+                    row[d] = orc_round_half(y[d], dtype);
+            }
+    }
+    free(x);
+    free(y);
+    return ORC_OK;
+}
