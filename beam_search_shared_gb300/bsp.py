@@ -27,6 +27,7 @@ MAX_GROUP = 8
 STATUS_BYTES = 256  # device status words ahead of the plan image in the workspace
 DEVFLAG_PAGE_INDEX = 1
 DEVFLAG_TIMEOUT = 2
+DEVFLAG_POSITION = 4
 
 
 class NativeLibraryError(RuntimeError):
@@ -57,10 +58,16 @@ class Plan(ctypes.Structure):
         ("reserved1", ctypes.c_int32), ("reserved", ctypes.c_uint64 * 2)]
 
 
+class RopeConfig(ctypes.Structure):
+    _fields_ = [("cos_sin", ctypes.c_void_p), ("max_position", ctypes.c_int32), ("rotary_dim", ctypes.c_int32),
+                ("interleaved", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 _lib = None
 EXPORTS = ["bsp_status_string", "bsp_bucket_rows", "bsp_workspace_size", "bsp_plan_build", "bsp_plan",
            "bsp_append_kv", "bsp_decode_attn", "bsp_read_device_status", "bsp_decode_attn_noalloc",
-           "bsp_plan_prefill_build", "bsp_plan_prefill", "bsp_prefill_attn"]
+           "bsp_plan_prefill_build", "bsp_plan_prefill", "bsp_prefill_attn", "bsp_rope_cos_sin",
+           "bsp_rope_append_kv"]
 NOALLOC_SCRATCH_MIB = 32
 
 
@@ -105,6 +112,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.bsp_plan_prefill.argtypes = [P(Geometry), i32, vp, vp, vp, i32, i32, vp, sz, vp, sz, vp, P(Plan)]
     lib.bsp_prefill_attn.restype = i32
     lib.bsp_prefill_attn.argtypes = [P(Plan), vp, vp, vp, ctypes.c_float, i32, vp, vp, vp, vp]
+    lib.bsp_rope_cos_sin.restype = i32
+    lib.bsp_rope_cos_sin.argtypes = [i32, i32, ctypes.c_double, vp, vp]
+    lib.bsp_rope_append_kv.restype = i32
+    lib.bsp_rope_append_kv.argtypes = [P(Plan), P(RopeConfig), vp, vp, i64, vp, vp, i64, vp, i32, vp, vp, vp, vp]
     lib.bsp_read_device_status.restype = i32
     lib.bsp_read_device_status.argtypes = [P(Plan), vp, i32, P(i32)]
     lib.bsp_decode_attn_noalloc.restype = i32
@@ -262,6 +273,48 @@ def append_kv(plan_: Plan, k_new: torch.Tensor, v_new: torch.Tensor, out_cache_l
     _check("bsp_append_kv", load().bsp_append_kv(
         ctypes.byref(plan_), _dptr(k_new), _dptr(v_new), int(src_row_stride), _dptr(out_cache_loc), n,
         _dptr(k_pool), _dptr(v_pool), _events(events, 2), _stream(stream)))
+
+
+class Rope:
+    """A RoPE table (device fp32 [max_position][rotary_dim], filled by bsp_rope_cos_sin) and its layout."""
+
+    def __init__(self, max_position: int, rotary_dim: int, base: float, interleaved: bool = False, device="cuda",
+                 stream=None):
+        self.cos_sin = torch.empty((int(max_position), int(rotary_dim)), dtype=torch.float32, device=device)
+        self.base = float(base)
+        _check("bsp_rope_cos_sin", load().bsp_rope_cos_sin(int(max_position), int(rotary_dim), self.base,
+                                                            _dptr(self.cos_sin), _stream(stream)))
+        self.config = RopeConfig(self.cos_sin.data_ptr(), int(max_position), int(rotary_dim), 1 if interleaved else 0, 0)
+
+    @property
+    def rotary_dim(self) -> int:
+        return int(self.config.rotary_dim)
+
+    @property
+    def interleaved(self) -> bool:
+        return bool(self.config.interleaved)
+
+    @property
+    def max_position(self) -> int:
+        return int(self.config.max_position)
+
+
+def rope_append_kv(plan_: Plan, rope: Rope, positions: torch.Tensor, q: Optional[torch.Tensor], k_new: torch.Tensor,
+                   v_new: torch.Tensor, out_cache_loc: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                   src_row_stride: Optional[int] = None, q_row_stride: Optional[int] = None, events=None,
+                   stream=None):
+    """bsp_rope_append_kv: rotated K and plain V rows into the pools, q [n, Hq*D] rotated in place (or None).
+    positions, out_cache_loc: int32 [n] on the device."""
+    n = int(out_cache_loc.numel())
+    row = plan_.geo.num_kv_heads * plan_.geo.head_dim
+    if src_row_stride is None:
+        src_row_stride = int(k_new.stride(0)) if k_new.dim() >= 1 and n else row
+    if q is not None and q_row_stride is None:
+        q_row_stride = int(q.stride(0)) if q.dim() >= 1 and n else plan_.geo.num_q_heads * plan_.geo.head_dim
+    _check("bsp_rope_append_kv", load().bsp_rope_append_kv(
+        ctypes.byref(plan_), ctypes.byref(rope.config), _dptr(positions), _dptr(q), int(q_row_stride or 0),
+        _dptr(k_new), _dptr(v_new), int(src_row_stride), _dptr(out_cache_loc), n, _dptr(k_pool), _dptr(v_pool),
+        _events(events, 2), _stream(stream)))
 
 
 def decode_attn(plan_: Plan, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,

@@ -17,6 +17,7 @@
 
 #include "../../include/bsp.h"
 #include "bsp_internal.h"
+#include "bsp_rope.h"
 
 namespace {
 
@@ -657,6 +658,63 @@ bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, const void* 
     return record_event(events, 1, s) ? BSP_OK : BSP_ERR_CUDA;
 }
 
+bsp_status bsp_rope_cos_sin(int32_t max_position, int32_t rotary_dim, double base, float* cos_sin, void* stream) {
+    if (max_position <= 0 || rotary_dim < 2 || rotary_dim > 1024 || (rotary_dim & 1)) return BSP_ERR_INVALID_ARG;
+    if (!(base > 1.0) || !std::isfinite(base)) return BSP_ERR_INVALID_ARG;
+    if (!device_ptr_ok(cos_sin)) return BSP_ERR_INVALID_ARG;
+    return launch_rope_cos_sin(max_position, rotary_dim, base, cos_sin, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? BSP_OK
+               : BSP_ERR_CUDA;
+}
+
+bsp_status bsp_rope_append_kv(const bsp_plan_t* plan, const bsp_rope_config* rope, const int32_t* positions, void* q,
+                              int64_t q_row_stride, const void* k_new, const void* v_new, int64_t src_row_stride,
+                              const int32_t* out_cache_loc, int32_t n, void* k_pool, void* v_pool,
+                              void* const* events, void* stream) {
+    bsp_status st = check_plan(plan);
+    if (st != BSP_OK) return st;
+    if (!rope || n < 0) return BSP_ERR_INVALID_ARG;
+    const bsp_geometry& geo = plan->geo;
+    const int D = geo.head_dim;
+    if (rope->rotary_dim < 16 || rope->rotary_dim > D || (rope->rotary_dim & 15) || rope->max_position <= 0 ||
+        (rope->interleaved != 0 && rope->interleaved != 1) || rope->reserved != 0)
+        return BSP_ERR_INVALID_ARG;
+    if (n == 0) return BSP_OK;
+    if (n > plan->total_rows) return BSP_ERR_INVALID_ARG;
+    if (src_row_stride < static_cast<int64_t>(geo.num_kv_heads) * D || (src_row_stride & 7)) return BSP_ERR_INVALID_ARG;
+    if (q && (q_row_stride < static_cast<int64_t>(geo.num_q_heads) * D || (q_row_stride & 7))) return BSP_ERR_INVALID_ARG;
+    if (!device_ptr_ok(k_new) || !device_ptr_ok(v_new) || !device_ptr_ok(out_cache_loc) || !device_ptr_ok(positions) ||
+        !device_ptr_ok(k_pool) || !device_ptr_ok(v_pool) || !device_ptr_ok(rope->cos_sin) || (q && !device_ptr_ok(q)))
+        return BSP_ERR_INVALID_ARG;
+    RopeAppendParams p{};
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.src_row_stride = src_row_stride;
+    p.q = q;
+    p.q_row_stride = q ? q_row_stride : 0;
+    p.loc = out_cache_loc;
+    p.pos = positions;
+    p.cos_sin = rope->cos_sin;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.status = static_cast<int32_t*>(plan->ws_device);
+    p.n = n;
+    p.Hq = geo.num_q_heads;
+    p.Hkv = geo.num_kv_heads;
+    p.ps_log2 = ilog2(geo.page_size);
+    p.num_pages = geo.num_pages;
+    p.rot = rope->rotary_dim;
+    p.interleaved = rope->interleaved;
+    p.max_pos = rope->max_position;
+    const bool bf16 = geo.dtype == BSP_DTYPE_BF16;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (prepare_rope_append(D, bf16) != cudaSuccess) return BSP_ERR_CUDA;
+    if (!record_event(events, 0, s)) return BSP_ERR_CUDA;
+    if (launch_rope_append(D, bf16, p, s) != cudaSuccess) return BSP_ERR_CUDA;
+    return record_event(events, 1, s) ? BSP_OK : BSP_ERR_CUDA;
+}
+
 bsp_status bsp_read_device_status(const bsp_plan_t* plan, void* stream, int32_t clear, int32_t* flags_out) {
     if (!plan || !plan->ws_device) return BSP_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -665,7 +723,7 @@ bsp_status bsp_read_device_status(const bsp_plan_t* plan, void* stream, int32_t 
     if (cudaMemcpy(&flags, plan->ws_device, sizeof flags, cudaMemcpyDeviceToHost) != cudaSuccess) return BSP_ERR_CUDA;
     if (clear && cudaMemset(plan->ws_device, 0, sizeof flags) != cudaSuccess) return BSP_ERR_CUDA;
     if (flags_out) *flags_out = flags;
-    if (flags & BSP_DEVFLAG_PAGE_INDEX) return BSP_ERR_PAGE_INDEX;
+    if (flags & (BSP_DEVFLAG_PAGE_INDEX | BSP_DEVFLAG_POSITION)) return BSP_ERR_PAGE_INDEX;
     if (flags & BSP_DEVFLAG_TIMEOUT) return BSP_ERR_DEVICE_TIMEOUT;
     return BSP_OK;
 }

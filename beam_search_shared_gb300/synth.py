@@ -253,6 +253,14 @@ def make_case(wl: Workload, seed: int, *, full_step: bool = True, device="cpu",
                 new_rows=np.asarray(new_rows, np.int32))
 
 
+def token_positions(case) -> np.ndarray:
+    """Logical position of each new token of a full decode step (the model's position ids): the
+    current token of every beam of request b sits at P_b + T_b - 1."""
+    W = case.workload.beam_width
+    b = case.new_rows // W
+    return (case.prefix_len[b] + case.tail_len[b] - 1).astype(np.int32)
+
+
 # ---------------------------------------------------------------- prefill over the cached prefix
 @dataclasses.dataclass(frozen=True)
 class PrefillWorkload:

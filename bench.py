@@ -377,6 +377,8 @@ def main():
 
     # ---- e2e: host buffers through the C ABI (plan from host arrays, H2D inputs, D2H outputs)
     e2e = run_e2e(sets[0], args.e2e_steps, world)
+    # ---- RoPE on the append, timed on its own after the step timing (it rewrites the new tokens' K rows)
+    rope_append = measure_rope_append(sets, Kt, hbm_gbs)
 
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
@@ -399,6 +401,7 @@ def main():
                      "kernel": "prefix_attn_kernel", "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": prefix_bytes},
         "e2e": e2e,
+        "rope_append": rope_append,
         "gpu_launches": sum(1 + (s.plan.num_units > 0) + (s.plan.tail_requests > 0)
                             for s in (sets[j % len(sets)] for j in range(K))),
         "timing": "value: CUDA-graph replay of exactly K steps without timing nodes; us_prefix (and the roofline): "
@@ -420,6 +423,55 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def measure_rope_append(sets, Kt, hbm_gbs):
+    """bsp_rope_append_kv over each set's new tokens (rotate-half over the whole head, base 1e6, a
+    40960-position table; the new tokens' q rows rotated in place): Kt launches back to back in one
+    graph, one event pair around its replay. Algorithmic bytes: K and V rows read and written to the
+    pools, q rows read and written, slots and positions, the table rows of the distinct positions."""
+    from beam_search_shared_gb300 import bsp, synth
+    wl = sets[0].case.workload
+    rope = bsp.Rope(40960, wl.head_dim, 1e6)
+    items, nbytes = [], []
+    for s in sets:
+        c = s.case
+        n = int(c.out_cache_loc.size)
+        pos_h = synth.token_positions(c)
+        pos = torch.from_numpy(pos_h).to(s.q.device)
+        qn = s.q[torch.from_numpy(c.new_rows).long().to(s.q.device)].reshape(n, -1).contiguous()
+        items.append((s, pos, qn))
+        e = 2
+        nbytes.append(n * (4 * wl.num_kv_heads * wl.head_dim * e + 2 * wl.num_q_heads * wl.head_dim * e + 8) +
+                      len(np.unique(pos_h)) * wl.head_dim * 4)
+
+    def launch(j):
+        s, pos, qn = items[j % len(items)]
+        bsp.rope_append_kv(s.plan, rope, pos, qn, s.k_new, s.v_new, s.out_cache_loc, s.k_pool, s.v_pool)
+
+    for j in range(3):
+        launch(j)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for j in range(Kt):
+            launch(j)
+    g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    for s, _, _ in items:
+        assert bsp.read_device_status(s.plan) == (0, 0)
+    us = 1e3 * e0.elapsed_time(e1) / Kt
+    b = statistics.mean(nbytes)
+    gbs = b / (us / 1e6) / 1e9
+    return {"kernel": "rope_append_kernel", "us": us, "gbs": gbs, "frac_of_hbm": gbs / hbm_gbs,
+            "algorithmic_bytes_per_launch": b, "rotary_dim": wl.head_dim, "layout": "rotate-half",
+            "timing": f"one event pair around {Kt} back-to-back launches (launch gaps included)"}
 
 
 def run_e2e(st, steps, world):

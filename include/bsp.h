@@ -61,7 +61,7 @@ typedef enum bsp_status {
     BSP_OK = 0,
     BSP_ERR_INVALID_ARG = 1,  /* null/misaligned/host pointer, bad length or stride */
     BSP_ERR_UNSUPPORTED = 2,  /* dtype, head_dim, group size, page size or tail outside the supported set */
-    BSP_ERR_PAGE_INDEX = 3,   /* a page id, slot or indirection value out of range */
+    BSP_ERR_PAGE_INDEX = 3,   /* a page id, slot, indirection value or RoPE position out of range */
     BSP_ERR_CAPACITY = 4,     /* workspace or staging buffer too small */
     BSP_ERR_STALE_PLAN = 5,   /* plan superseded by a newer bsp_plan on the same workspace */
     BSP_ERR_CUDA = 6,         /* a CUDA runtime/driver call failed */
@@ -82,6 +82,7 @@ enum {
 /* Bits of the device status word. */
 #define BSP_DEVFLAG_PAGE_INDEX 1
 #define BSP_DEVFLAG_TIMEOUT 2
+#define BSP_DEVFLAG_POSITION 4  /* a RoPE position outside [0, max_position) (bsp_rope_append_kv) */
 
 typedef struct bsp_geometry {
     int32_t num_q_heads;  /* Hq */
@@ -224,6 +225,70 @@ BSP_API bsp_status bsp_plan(const bsp_geometry* geo, int32_t batch, int32_t beam
 BSP_API bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, const void* v_new, int64_t src_row_stride,
                          const int32_t* out_cache_loc, int32_t n, void* k_pool, void* v_pool,
                          void* const* events, void* stream);
+
+/*
+ * Rotary position embedding (RoPE) on the paged append. The pages apply RoPE to
+ * K before it is written to the paged cache (TensorRT-LLM PR #21738: the model
+ * applies it itself, per the description; the review of flash_attn4_kernels.py
+ * names the rope_write_kv_paged helper and its partial-RoPE partner lookup) but
+ * do not define it; the definition is the published one (Su et al., RoFormer,
+ * section 3.2): the first rotary_dim dims of a head row form rotary_dim/2 pairs,
+ * pair j turns by the angle p * theta_j, theta_j = base^(-2j / rotary_dim),
+ * (x, y) -> (x cos - y sin, y cos + x sin); the other dims pass unchanged.
+ *
+ * The caller-owned table of cos/sin values, device fp32
+ *   cos_sin[p][j]                  = cos(p * theta_j),  j < rotary_dim / 2
+ *   cos_sin[p][rotary_dim / 2 + j] = sin(p * theta_j),
+ * p in [0, max_position), is filled once by bsp_rope_cos_sin.
+ */
+typedef struct bsp_rope_config {
+    const float* cos_sin;   /* device [max_position][rotary_dim], 16-byte aligned */
+    int32_t max_position;   /* rows of cos_sin */
+    int32_t rotary_dim;     /* rotated leading dims of a head row: a multiple of 16, 16 .. head_dim */
+    int32_t interleaved;    /* 0: pair j = dims (j, j + rotary_dim/2) (rotate-half, e.g. Qwen3);
+                               1: pair j = dims (2j, 2j + 1) */
+    int32_t reserved;       /* 0 */
+} bsp_rope_config;
+
+/*
+ * Fills the cos/sin table of a bsp_rope_config: angles and their cos/sin in
+ * fp64 on the device, each value rounded once to fp32. One launch on `stream`,
+ * no sync.
+ *   max_position   > 0 rows;  rotary_dim even, 2 .. 1024;  base > 1, finite
+ *   cos_sin        device fp32 [max_position][rotary_dim], 16-byte aligned
+ * Argument errors: BSP_ERR_INVALID_ARG before any launch.
+ */
+BSP_API bsp_status bsp_rope_cos_sin(int32_t max_position, int32_t rotary_dim, double base, float* cos_sin,
+                                    void* stream);
+
+/*
+ * Paged append with RoPE, one launch: for every new token i < n at position
+ * positions[i] and slot out_cache_loc[i], the kv head rows of k_new are rotated
+ * and written, the rows of v_new copied, to
+ * pool[slot / page_size][h][slot % page_size][:] (as bsp_append_kv); when q is
+ * non-NULL, the token's num_q_heads query rows are rotated in place. Rotation
+ * in fp32 from the fp32 table (one fused multiply-add per output after one
+ * product), rounded to nearest even into the pools' dtype; V rows and dims past
+ * rotary_dim are copied bit for bit.
+ *   plan            a decode or prefill plan (geometry, status word, n bound)
+ *   rope            table and layout (bsp_rope_config)
+ *   positions       device int32 [n]: the token's logical position (a decode
+ *                   step: P_b + T_b - 1 for every beam of request b; a
+ *                   prefill: C_b + t)
+ *   q               NULL, or device [n] rows of num_q_heads * head_dim elements
+ *                   q_row_stride elements apart (>= that, a multiple of 8)
+ *   k_new, v_new, src_row_stride, out_cache_loc, n, k_pool, v_pool, events:
+ *                   as bsp_append_kv
+ * A token whose slot is outside [0, num_pages * page_size) or whose position is
+ * outside [0, max_position) is skipped entirely (no pool row written, its q rows
+ * left as they were) and sets BSP_DEVFLAG_PAGE_INDEX or BSP_DEVFLAG_POSITION;
+ * bsp_read_device_status reports either as BSP_ERR_PAGE_INDEX. Host-checkable
+ * errors return before any launch with nothing written.
+ */
+BSP_API bsp_status bsp_rope_append_kv(const bsp_plan_t* plan, const bsp_rope_config* rope, const int32_t* positions,
+                                      void* q, int64_t q_row_stride, const void* k_new, const void* v_new,
+                                      int64_t src_row_stride, const int32_t* out_cache_loc, int32_t n,
+                                      void* k_pool, void* v_pool, void* const* events, void* stream);
 
 /*
  * Cascade decode attention (TensorRT-LLM PR #21738, description, "Solution"):

@@ -70,6 +70,11 @@ def _load():
     lib.orc_rope_cos_sin.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, p]
     lib.orc_rope_rotate.restype = None
     lib.orc_rope_rotate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, p, p]
+    lib.orc_round_half_array.restype = None
+    lib.orc_round_half_array.argtypes = [ctypes.c_int64, p, p, ctypes.c_int]
+    lib.orc_rope_rotate_rows.restype = None
+    lib.orc_rope_rotate_rows.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, p,
+                                         p, p]
     lib.orc_rope_append_kv.restype = ctypes.c_int
     lib.orc_rope_append_kv.argtypes = ([ctypes.c_int] * 6 + [ctypes.c_double] + [ctypes.c_int] * 4 +
                                        [p, p, p, ctypes.c_int64, p, p, ctypes.c_int64, p, p])
@@ -198,11 +203,11 @@ def round_half(x: float, dtype: str) -> int:
 
 
 def round_half_array(x, dtype: str) -> np.ndarray:
-    """round_half over an array (a loop over the C routine; small inputs)."""
-    x = np.asarray(x, np.float64)
-    f = _load().orc_round_half
-    d = DTYPES[dtype]
-    return np.array([f(float(v), d) for v in x.reshape(-1)], np.uint16).reshape(x.shape)
+    """round_half over an array."""
+    x = _c(x, np.float64)
+    out = np.empty(x.shape, np.uint16)
+    _load().orc_round_half_array(x.size, _ptr(x), _ptr(out), DTYPES[dtype])
+    return out
 
 
 def rope_cos_sin(max_pos: int, rot: int, base: float) -> np.ndarray:
@@ -217,6 +222,16 @@ def rope_rotate(x, *, rot: int, interleaved: bool, base: float, pos: int) -> np.
     x = _c(x, np.float64)
     y = np.empty_like(x)
     _load().orc_rope_rotate(x.shape[0], int(rot), 1 if interleaved else 0, float(base), int(pos), _ptr(x), _ptr(y))
+    return y
+
+
+def rope_rotate_rows(x, positions, *, rot: int, interleaved: bool, base: float) -> np.ndarray:
+    """rope_rotate over rows: x fp64 [rows][D], row i by positions[i]; unrounded."""
+    x = _c(x, np.float64)
+    rows, D = x.shape
+    pos = _c(positions, np.int32).reshape(rows)
+    y = np.empty_like(x)
+    _load().orc_rope_rotate_rows(rows, D, int(rot), 1 if interleaved else 0, float(base), _ptr(pos), _ptr(x), _ptr(y))
     return y
 
 

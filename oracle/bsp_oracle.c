@@ -503,3 +503,18 @@ int orc_rope_append_kv(int dtype, int Hq, int Hkv, int D, int rot, int interleav
     free(y);
     return ORC_OK;
 }
+
+/* orc_round_half over an array. */
+void orc_round_half_array(int64_t n, const double *x, uint16_t *out, int dtype)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_round_half(x[i], dtype);
+}
+
+/* orc_rope_rotate over `rows` head rows of D values, row i by position pos[i]. */
+void orc_rope_rotate_rows(int64_t rows, int D, int rot, int interleaved, double base, const int32_t *pos,
+                          const double *x, double *y)
+{
+    for (int64_t i = 0; i < rows; ++i)
+        orc_rope_rotate(D, rot, interleaved, base, pos[i], x + i * D, y + i * D);
+}

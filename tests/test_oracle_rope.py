@@ -206,3 +206,16 @@ def test_rope_append_position_zero_and_no_q():
     for i in range(n):
         pg, off = loc[i] // ps, loc[i] % ps
         np.testing.assert_array_equal(kp_o[pg, :, off], kn[i])
+
+
+def test_array_forms_equal_the_scalar_routines():
+    rng = np.random.default_rng(14)
+    x = rng.standard_normal(300) * np.exp2(rng.integers(-20, 20, 300))
+    for dtype in DT:
+        np.testing.assert_array_equal(oracle.round_half_array(x, dtype),
+                                      np.array([oracle.round_half(v, dtype) for v in x], np.uint16))
+    rows = rng.standard_normal((7, 32))
+    pos = rng.integers(0, 9000, 7)
+    y = oracle.rope_rotate_rows(rows, pos, rot=16, interleaved=True, base=5e5)
+    for i in range(7):
+        np.testing.assert_array_equal(y[i], oracle.rope_rotate(rows[i], rot=16, interleaved=True, base=5e5, pos=pos[i]))
