@@ -4,14 +4,17 @@
 // generated itself, found through cache_indirection; the commit that fuses the
 // tail runs it and the merge with the prefix result as one launch per layer).
 //
-// One CTA per beam row r = b*W + w. The row's tail positions j = P_b + t
+// One CTA per beam row r = b*W + w (per row and head pass when the step has
+// fewer rows than SMs). The row's tail positions j = P_b + t
 // (t < T_b <= 8) are resolved once: threads t look up the source beam
 // cache_indirection[b][w][j] and that beam's page id, and leave the row's
 // physical offset in shared memory. The warps then serve the query heads: a
 // head's row of head_dim 16-bit elements is read by D/8 lanes with 16-byte
 // loads (32/(D/8) heads per warp pass), every K and V chunk of the head's tail
 // rows is issued at once, and the softmax over those rows is merged with the
-// request's prompt partial states (one per key split) by log-sum-exp. O is
+// request's prompt partial states (one per key split) by log-sum-exp: the
+// head's lanes load the partial LSEs in parallel and reduce their maximum by
+// shuffles, then the partial O rows arrive a few splits per round. O is
 // written in the q dtype and LSE in fp32. So one chain of dependent lookups
 // serves all Hq heads of the row. All softmax arithmetic is in base 2 on
 // scores pre-scaled by softmax_scale * log2(e).
@@ -110,7 +113,8 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
     const long long pstride = static_cast<long long>(p.W) * p.Hq;          // rows of one partial slot
     const int passes = (p.Hq + NW * HPW - 1) / (NW * HPW);
 
-    for (int pg = 0; pg < passes; pg += MAXP) {
+    // with few rows the head passes are spread over gridDim.y CTAs per row
+    for (int pg = blockIdx.y * MAXP; pg < passes; pg += gridDim.y * MAXP) {
         // ---- the tail keys of this group of head passes: softmax state (m, l) and the lane's
         // 8 columns of sum_t 2^(s_t - m) V_t. Everything read here was written before the prompt
         // kernel started, so a CTA launched as a dependent of the prompt kernel computes it while
@@ -181,7 +185,12 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
         // the partial states are read coherently below (never through the read-only path, whose
         // loads the compiler may move above the wait)
 
-        // ---- merge with the prompt partial states by log-sum-exp (base 2), one round of loads
+        // ---- merge with the prompt partial states by log-sum-exp (base 2). Split 0 of every head
+        // of the group is loaded in one round; with more splits, the lanes of a head slot load the
+        // other partial LSEs in parallel (lane li: splits 1 + li, 1 + li + LPR, ...) and reduce
+        // their maximum by shuffles, then the other partial O rows arrive KB splits per round.
+        constexpr int KMAX = (kExtraParts + LPR - 1) / LPR;  // a request has at most 1 + kExtraParts splits
+        constexpr int KB = 4;
         float lse0[MAXP];
         float4 o0a[MAXP], o0b[MAXP];
 #pragma unroll
@@ -201,12 +210,23 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
 #pragma unroll
         for (int pi = 0; pi < MAXP; ++pi) {
             const int h = (pg + pi) * NW * HPW + warp * HPW + hs;
-            if (!(pg + pi < passes && h < p.Hq)) continue;
-            const long long prow = (static_cast<long long>(part_off) * p.W + w) * p.Hq + h;
+            const bool active = pg + pi < passes && h < p.Hq;  // every lane still takes part in the shuffles
+            const long long prow = (static_cast<long long>(part_off) * p.W + w) * p.Hq + (active ? h : 0);
             const float m = tm[pi], l = tl[pi];
             float Lmax = (l > 0.f) ? m + log2f(l) : -INFINITY;
             Lmax = fmaxf(Lmax, lse0[pi]);
-            for (int sp = 1; sp < nsplit; ++sp) Lmax = fmaxf(Lmax, ld_dep(p.part_lse + prow + sp * pstride));
+            if (nsplit > 1) {  // block-uniform
+                float lsev[KMAX];
+#pragma unroll
+                for (int k = 0; k < KMAX; ++k) {
+                    const int sp = 1 + k * LPR + li;
+                    lsev[k] = (active && sp < nsplit) ? ld_dep(p.part_lse + prow + sp * pstride) : -INFINITY;
+                }
+#pragma unroll
+                for (int k = 0; k < KMAX; ++k) Lmax = fmaxf(Lmax, lsev[k]);
+#pragma unroll
+                for (int off = LPR / 2; off >= 1; off >>= 1) Lmax = fmaxf(Lmax, __shfl_xor_sync(FULL, Lmax, off));
+            }
             float out[8];
             float lse2;
             if (Lmax == -INFINITY) {
@@ -214,40 +234,53 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
                 for (int e = 0; e < 8; ++e) out[e] = 0.f;
                 lse2 = -INFINITY;
             } else {
-                // tail weight exp2(m + log2 l - Lmax) times O_t = acc / l
+                // tail weight exp2(m + log2 l - Lmax) times O_t = acc / l, then split 0
                 const float ft = (l > 0.f) ? exp2f(m - Lmax) : 0.f;
-                float sum = l * ft;
+                const float w0 = exp2f(lse0[pi] - Lmax);  // 0 without a prompt
+                float sum = l * ft + w0;
+                out[0] = fmaf(w0, o0a[pi].x, acc[pi][0] * ft);
+                out[1] = fmaf(w0, o0a[pi].y, acc[pi][1] * ft);
+                out[2] = fmaf(w0, o0a[pi].z, acc[pi][2] * ft);
+                out[3] = fmaf(w0, o0a[pi].w, acc[pi][3] * ft);
+                out[4] = fmaf(w0, o0b[pi].x, acc[pi][4] * ft);
+                out[5] = fmaf(w0, o0b[pi].y, acc[pi][5] * ft);
+                out[6] = fmaf(w0, o0b[pi].z, acc[pi][6] * ft);
+                out[7] = fmaf(w0, o0b[pi].w, acc[pi][7] * ft);
+                for (int sp0 = 1; sp0 < nsplit; sp0 += KB) {
+                    float ls[KB];
+                    float4 a0[KB], a1[KB];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) out[e] = acc[pi][e] * ft;
-                for (int sp = 0; sp < nsplit; ++sp) {
-                    float lse_s;
-                    float4 a0, a1;
-                    if (sp == 0) {
-                        lse_s = lse0[pi];
-                        a0 = o0a[pi];
-                        a1 = o0b[pi];
-                    } else {
-                        lse_s = ld_dep(p.part_lse + prow + sp * pstride);
-                        const float4* po = reinterpret_cast<const float4*>(p.part_o + (prow + sp * pstride) * D) + li * 2;
-                        a0 = ld_dep(po);
-                        a1 = ld_dep(po + 1);
+                    for (int u = 0; u < KB; ++u) {
+                        const int sp = sp0 + u;
+                        ls[u] = -INFINITY;
+                        a0[u] = a1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (active && sp < nsplit) {
+                            ls[u] = ld_dep(p.part_lse + prow + sp * pstride);
+                            const float4* po = reinterpret_cast<const float4*>(p.part_o + (prow + sp * pstride) * D) + li * 2;
+                            a0[u] = ld_dep(po);
+                            a1[u] = ld_dep(po + 1);
+                        }
                     }
-                    const float wgt = exp2f(lse_s - Lmax);
-                    out[0] = fmaf(wgt, a0.x, out[0]);
-                    out[1] = fmaf(wgt, a0.y, out[1]);
-                    out[2] = fmaf(wgt, a0.z, out[2]);
-                    out[3] = fmaf(wgt, a0.w, out[3]);
-                    out[4] = fmaf(wgt, a1.x, out[4]);
-                    out[5] = fmaf(wgt, a1.y, out[5]);
-                    out[6] = fmaf(wgt, a1.z, out[6]);
-                    out[7] = fmaf(wgt, a1.w, out[7]);
-                    sum += wgt;
+#pragma unroll
+                    for (int u = 0; u < KB; ++u) {
+                        const float wgt = exp2f(ls[u] - Lmax);  // 0 for splits past nsplit
+                        out[0] = fmaf(wgt, a0[u].x, out[0]);
+                        out[1] = fmaf(wgt, a0[u].y, out[1]);
+                        out[2] = fmaf(wgt, a0[u].z, out[2]);
+                        out[3] = fmaf(wgt, a0[u].w, out[3]);
+                        out[4] = fmaf(wgt, a1[u].x, out[4]);
+                        out[5] = fmaf(wgt, a1[u].y, out[5]);
+                        out[6] = fmaf(wgt, a1[u].z, out[6]);
+                        out[7] = fmaf(wgt, a1[u].w, out[7]);
+                        sum += wgt;
+                    }
                 }
                 const float inv = 1.f / sum;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) out[e] *= inv;
                 lse2 = Lmax + log2f(sum);
             }
+            if (!active) continue;
             uint16_t* obase = static_cast<uint16_t*>(p.o) + (static_cast<long long>(r) * p.Hq + h) * D;
             reinterpret_cast<uint4*>(obase)[li] = pack8<BF16>(out);
             if (li == 0)
@@ -257,10 +290,10 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
 }
 
 template <int D, bool BF16, int MAXT, int MAXP>
-static cudaError_t launch_tail_k(const TailParams& p, bool after_prefix, cudaStream_t stream) {
+static cudaError_t launch_tail_k(const TailParams& p, bool after_prefix, int pass_ctas, cudaStream_t stream) {
     const long long rows = static_cast<long long>(p.B) * p.W;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(rows));
+    cfg.gridDim = dim3(static_cast<unsigned>(rows), static_cast<unsigned>(pass_ctas));
     cfg.blockDim = dim3(kTailThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -279,12 +312,28 @@ static int tail_passes(int Hq) {
     return (Hq + 4 * hpw - 1) / (4 * hpw);
 }
 
+// SMs of the current device (cached per device)
+static int device_sms() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 template <int D, bool BF16, int MAXT>
 static cudaError_t launch_tail_p(const TailParams& p, bool after_prefix, cudaStream_t stream) {
     const int passes = tail_passes<D>(p.Hq);
-    if (passes <= 1) return launch_tail_k<D, BF16, MAXT, 1>(p, after_prefix, stream);
-    if (passes <= 2) return launch_tail_k<D, BF16, MAXT, 2>(p, after_prefix, stream);
-    return launch_tail_k<D, BF16, MAXT, 4>(p, after_prefix, stream);
+    const long long rows = static_cast<long long>(p.B) * p.W;
+    // fewer rows than SMs: one CTA per (row, head pass), so a row's heads merge in parallel
+    if (passes > 1 && rows < device_sms()) return launch_tail_k<D, BF16, MAXT, 1>(p, after_prefix, passes, stream);
+    if (passes <= 1) return launch_tail_k<D, BF16, MAXT, 1>(p, after_prefix, 1, stream);
+    if (passes <= 2) return launch_tail_k<D, BF16, MAXT, 2>(p, after_prefix, 1, stream);
+    return launch_tail_k<D, BF16, MAXT, 4>(p, after_prefix, 1, stream);
 }
 
 template <int D, bool BF16>
@@ -302,7 +351,9 @@ template <int D, bool BF16, int MAXT>
 static cudaError_t prepare_tail_p(int Hq) {
     const cudaFuncAttribute a = cudaFuncAttributePreferredSharedMemoryCarveout;
     const int passes = tail_passes<D>(Hq);
-    if (passes <= 1) return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, MAXT, 1>, a, cudaSharedmemCarveoutMaxShared);
+    // the one-pass variant also serves steps with fewer rows than SMs
+    const cudaError_t e = cudaFuncSetAttribute(tail_merge_kernel<D, BF16, MAXT, 1>, a, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess || passes <= 1) return e;
     if (passes <= 2) return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, MAXT, 2>, a, cudaSharedmemCarveoutMaxShared);
     return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, MAXT, 4>, a, cudaSharedmemCarveoutMaxShared);
 }
