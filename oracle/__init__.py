@@ -75,6 +75,13 @@ def _load():
     lib.orc_rope_rotate_rows.restype = None
     lib.orc_rope_rotate_rows.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, p,
                                          p, p]
+    lib.orc_e4m3_to_double.restype = ctypes.c_double
+    lib.orc_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.orc_round_e4m3.restype = ctypes.c_uint8
+    lib.orc_round_e4m3.argtypes = [ctypes.c_double]
+    lib.orc_append_kv_fp8.restype = ctypes.c_int
+    lib.orc_append_kv_fp8.argtypes = [ctypes.c_int] * 6 + [p, p, p, ctypes.c_int64, ctypes.c_float, ctypes.c_float,
+                                                          p, p]
     lib.orc_rope_append_kv.restype = ctypes.c_int
     lib.orc_rope_append_kv.argtypes = ([ctypes.c_int] * 6 + [ctypes.c_double] + [ctypes.c_int] * 4 +
                                        [p, p, p, ctypes.c_int64, p, p, ctypes.c_int64, p, p])
@@ -256,3 +263,34 @@ def rope_append_kv(*, dtype, Hq, Hkv, D, rot, interleaved, base, max_pos, ps, nu
         _ptr(k_pool_bits), _ptr(v_pool_bits))
     if rc != 0:
         raise ValueError(f"oracle rope_append_kv: {ERRORS.get(rc, rc)}")
+
+
+def e4m3_to_double(bits: int) -> float:
+    return float(_load().orc_e4m3_to_double(int(bits) & 0xFF))
+
+
+def round_e4m3(x: float) -> int:
+    """Nearest E4M3 pattern, ties to even, saturating at +-448."""
+    return int(_load().orc_round_e4m3(float(x)))
+
+
+FP8_SRC = {"bf16": 0, "fp16": 1, "e4m3": 2}
+
+
+def append_kv_fp8(*, src_dtype, Hkv, D, ps, num_pages, out_cache_loc, k_new_bits, v_new_bits, k_pool_bits,
+                  v_pool_bits, k_mul=1.0, v_mul=1.0, row_stride=None):
+    """Paged append into uint8 E4M3 pools, in place: 16-bit sources quantised (fp32 product with the
+    multiplier, then round_e4m3), E4M3 sources copied. Raises on a bad slot (pools unchanged)."""
+    loc = _c(out_cache_loc, np.int32)
+    n = loc.shape[0]
+    et = np.uint8 if src_dtype == "e4m3" else np.uint16
+    kn = _c(k_new_bits, et).reshape(n, -1) if n else np.zeros((0, Hkv * D), et)
+    vn = _c(v_new_bits, et).reshape(n, -1) if n else np.zeros((0, Hkv * D), et)
+    for a in (k_pool_bits, v_pool_bits):
+        assert a.dtype == np.uint8 and a.flags.c_contiguous
+    rs = kn.shape[1] if row_stride is None else int(row_stride)
+    rc = _load().orc_append_kv_fp8(FP8_SRC[src_dtype], Hkv, D, ps, num_pages, n, _ptr(loc), _ptr(kn), _ptr(vn), rs,
+                                   float(np.float32(k_mul)), float(np.float32(v_mul)), _ptr(k_pool_bits),
+                                   _ptr(v_pool_bits))
+    if rc != 0:
+        raise ValueError(f"oracle append_kv_fp8: {ERRORS.get(rc, rc)}")

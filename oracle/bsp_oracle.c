@@ -518,3 +518,88 @@ void orc_rope_rotate_rows(int64_t rows, int D, int rot, int interleaved, double 
     for (int64_t i = 0; i < rows; ++i)
         orc_rope_rotate(D, rot, interleaved, base, pos[i], x + i * D, y + i * D);
 }
+
+/* FP8 E4M3 (the OCP 8-bit format, "e4m3fn"): 1 sign, 4 exponent (bias 7) and 3
+ * fraction bits, no infinities, exponent 15 with fraction 7 is NaN, so the
+ * largest finite value is 1.75 * 2^8 = 448; below 2^-6 the spacing stays 2^-9
+ * (subnormals). Exact value of a pattern. */
+double orc_e4m3_to_double(uint8_t bits)
+{
+    const int sign = bits >> 7, e = (bits >> 3) & 15, m = bits & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp((double)(m + 8), e - 10);   /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 value, ties to the even fraction, saturating: a finite value past
+ * 448 becomes +-448 (the satfinite conversion of CUDA's fp8 types), NaN the NaN
+ * pattern 0x7F. */
+uint8_t orc_round_e4m3(double x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs(x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    if (a == 0.0)
+        return sign;
+    int e;
+    frexp(a, &e);
+    int be = e - 1;
+    if (be < -6)
+        be = -6;
+    const double spacing = ldexp(1.0, be - 3);
+    const double r = nearbyint(a / spacing) * spacing;
+    if (r >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    if (r == 0.0)
+        return sign;
+    int re;
+    frexp(r, &re);
+    const int rbe = re - 1;
+    if (rbe < -6)
+        return (uint8_t)(sign | (uint8_t)(r / ldexp(1.0, -9)));
+    const unsigned frac = (unsigned)(r / ldexp(1.0, rbe - 3)) - 8u;
+    return (uint8_t)(sign | (uint8_t)((unsigned)(rbe + 7) << 3) | (uint8_t)frac);
+}
+
+/* Paged append into E4M3 pools ([num_pages][Hkv][ps][D] bytes). A 16-bit source
+ * element x (bf16 or fp16, src_dtype) is stored as round_e4m3(fp32(x) * mul),
+ * the product rounded once to fp32 (the conversion of a KV cache kept in fp8
+ * with a per-tensor quantisation multiplier, k_mul for K and v_mul for V); an
+ * E4M3 source (src_dtype 2) is copied bit for bit. Slots are checked first: a
+ * bad one leaves both pools unchanged. */
+int orc_append_kv_fp8(int src_dtype, int Hkv, int D, int ps, int num_pages, int n, const int32_t *loc,
+                      const void *knew, const void *vnew, int64_t row_stride, float k_mul, float v_mul,
+                      uint8_t *kpool, uint8_t *vpool)
+{
+    for (int i = 0; i < n; ++i)
+        if (loc[i] < 0 || (int64_t)loc[i] >= (int64_t)num_pages * ps)
+            return ORC_ERR_INDEX;
+    for (int i = 0; i < n; ++i) {
+        const int64_t page = loc[i] / ps, off = loc[i] % ps;
+        for (int h = 0; h < Hkv; ++h) {
+            const size_t dst = (((size_t)page * Hkv + h) * ps + (size_t)off) * D;
+            const size_t src = (size_t)i * (size_t)row_stride + (size_t)h * D;
+            if (src_dtype == 2) {
+                memcpy(kpool + dst, (const uint8_t *)knew + src, (size_t)D);
+                memcpy(vpool + dst, (const uint8_t *)vnew + src, (size_t)D);
+                continue;
+            }
+            for (int d = 0; d < D; ++d) {
+                const float kx = (float)orc_half_to_double(((const uint16_t *)knew)[src + d], src_dtype);
+                const float vx = (float)orc_half_to_double(((const uint16_t *)vnew)[src + d], src_dtype);
+                const float ky = kx * k_mul, vy = vx * v_mul;   /* one fp32 product each */
+                kpool[dst + d] = orc_round_e4m3((double)ky);
+                vpool[dst + d] = orc_round_e4m3((double)vy);
+            }
+        }
+    }
+    return ORC_OK;
+}

@@ -1,0 +1,120 @@
+"""Pins of the oracle's FP8 (E4M3) KV write: the format's decoding and round-to-nearest-even with
+saturation against the format definition and torch's own float -> float8_e4m3fn conversion, and the
+quantising paged append against a numpy/torch restatement.
+
+The pages ask for the fp8-source-into-fp8-cache pairing and the source/cache dtype conversion of the
+fused KV write (TensorRT-LLM PR #18614, the review follow-up on the fused per-layer KV-cache write and
+the review of msa_scatter.py); the quantisation multiplier and the saturation are the plain readings
+(a per-tensor scale, CUDA's satfinite conversion)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+def test_every_pattern_decodes_and_round_trips():
+    for b in range(256):
+        v = oracle.e4m3_to_double(b)
+        if b & 0x7F == 0x7F:
+            assert math.isnan(v)
+            continue
+        assert oracle.round_e4m3(v) == b, hex(b)
+    # the format's landmarks
+    assert oracle.e4m3_to_double(0x7E) == 448.0
+    assert oracle.e4m3_to_double(0x08) == 2.0 ** -6      # smallest normal
+    assert oracle.e4m3_to_double(0x01) == 2.0 ** -9      # smallest subnormal
+    assert oracle.e4m3_to_double(0x38) == 1.0
+    # decoding agrees with torch's float8_e4m3fn
+    bits = torch.arange(256, dtype=torch.uint8)
+    t = bits.view(torch.float8_e4m3fn).double().numpy()
+    o = np.array([oracle.e4m3_to_double(b) for b in range(256)])
+    np.testing.assert_array_equal(np.isnan(t), np.isnan(o))
+    np.testing.assert_array_equal(t[~np.isnan(t)], o[~np.isnan(o)])
+
+
+def test_midpoints_go_to_even_and_saturation():
+    for b in range(0, 0x7D):
+        lo, hi = oracle.e4m3_to_double(b), oracle.e4m3_to_double(b + 1)
+        mid = (lo + hi) / 2
+        even = b if b % 2 == 0 else b + 1
+        assert oracle.round_e4m3(mid) == even
+        assert oracle.round_e4m3(-mid) == even | 0x80
+        assert oracle.round_e4m3(math.nextafter(mid, 0.0)) == b
+        assert oracle.round_e4m3(math.nextafter(mid, math.inf)) == b + 1
+    for v in (448.0, 449.0, 463.9, 464.0, 1e6, math.inf):
+        assert oracle.round_e4m3(v) == 0x7E
+        assert oracle.round_e4m3(-v) == 0xFE
+    assert oracle.round_e4m3(math.nan) == 0x7F
+    assert oracle.round_e4m3(2.0 ** -10) == 0x00          # half the smallest subnormal: ties to even (zero)
+    assert oracle.round_e4m3(math.nextafter(2.0 ** -10, 1.0)) == 0x01
+
+
+def test_rounding_matches_torch_inside_the_range():
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal(5000) * np.exp2(rng.integers(-12, 9, 5000))).astype(np.float32)
+    x = x[np.abs(x) < 464]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.round_e4m3(float(v)) for v in x], np.uint8)
+    np.testing.assert_array_equal(got, want)
+
+
+def _restated(x_bits, dtype, mul):
+    """fp32 product with the multiplier, clamped to +-448 (satfinite), torch's RNE conversion."""
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    x = torch.from_numpy(x_bits.view(np.int16)).view(tdt).float()
+    y = x * torch.tensor(mul, dtype=torch.float32)
+    return y.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_fp8_append_matches_restatement(dtype):
+    rng = np.random.default_rng(22)
+    n, Hkv, D, ps, npg = 7, 2, 64, 4, 6
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    kn = (torch.randn(n, Hkv * D, generator=torch.Generator().manual_seed(1)) * 40).to(tdt)
+    vn = (torch.randn(n, Hkv * D, generator=torch.Generator().manual_seed(2)) * 3).to(tdt)
+    kb, vb = kn.view(torch.int16).numpy().view(np.uint16), vn.view(torch.int16).numpy().view(np.uint16)
+    loc = rng.choice(npg * ps, n, replace=False).astype(np.int32)
+    kp = rng.integers(0, 256, (npg, Hkv, ps, D)).astype(np.uint8)
+    vp = rng.integers(0, 256, (npg, Hkv, ps, D)).astype(np.uint8)
+    kp0, vp0 = kp.copy(), vp.copy()
+    k_mul, v_mul = 0.37, 11.0          # K saturates in places (|x| * 0.37 up to ~60; * 40 -> some > 448)
+    oracle.append_kv_fp8(src_dtype=dtype, Hkv=Hkv, D=D, ps=ps, num_pages=npg, out_cache_loc=loc, k_new_bits=kb,
+                         v_new_bits=vb, k_pool_bits=kp, v_pool_bits=vp, k_mul=k_mul * 40, v_mul=v_mul)
+    wk = _restated(kb, dtype, np.float32(k_mul * 40)).reshape(n, Hkv, D)
+    wv = _restated(vb, dtype, np.float32(v_mul)).reshape(n, Hkv, D)
+    assert (wk == 0x7E).any() or (wk == 0xFE).any()     # the saturating branch is exercised
+    for i in range(n):
+        pg, off = loc[i] // ps, loc[i] % ps
+        np.testing.assert_array_equal(kp[pg, :, off], wk[i])
+        np.testing.assert_array_equal(vp[pg, :, off], wv[i])
+    touched = np.zeros((npg, ps), bool)
+    touched[loc // ps, loc % ps] = True
+    np.testing.assert_array_equal(kp.transpose(0, 2, 1, 3)[~touched], kp0.transpose(0, 2, 1, 3)[~touched])
+
+
+def test_fp8_source_is_copied_and_bad_slot_writes_nothing():
+    rng = np.random.default_rng(23)
+    n, Hkv, D, ps, npg = 5, 2, 32, 4, 4
+    kb = rng.integers(0, 256, (n, Hkv * D)).astype(np.uint8)
+    vb = rng.integers(0, 256, (n, Hkv * D)).astype(np.uint8)
+    loc = rng.choice(npg * ps, n, replace=False).astype(np.int32)
+    kp = np.zeros((npg, Hkv, ps, D), np.uint8)
+    vp = np.zeros_like(kp)
+    oracle.append_kv_fp8(src_dtype="e4m3", Hkv=Hkv, D=D, ps=ps, num_pages=npg, out_cache_loc=loc, k_new_bits=kb,
+                         v_new_bits=vb, k_pool_bits=kp, v_pool_bits=vp, k_mul=3.0, v_mul=3.0)
+    for i in range(n):
+        pg, off = loc[i] // ps, loc[i] % ps
+        np.testing.assert_array_equal(kp[pg, :, off].reshape(-1), kb[i])
+        np.testing.assert_array_equal(vp[pg, :, off].reshape(-1), vb[i])
+    bad = loc.copy()
+    bad[2] = npg * ps
+    kp2, vp2 = kp.copy(), vp.copy()
+    with pytest.raises(ValueError):
+        oracle.append_kv_fp8(src_dtype="e4m3", Hkv=Hkv, D=D, ps=ps, num_pages=npg, out_cache_loc=bad, k_new_bits=kb,
+                             v_new_bits=vb, k_pool_bits=kp2, v_pool_bits=vp2)
+    np.testing.assert_array_equal(kp2, kp)
+    np.testing.assert_array_equal(vp2, vp)
