@@ -67,7 +67,7 @@ _lib = None
 EXPORTS = ["bsp_status_string", "bsp_bucket_rows", "bsp_workspace_size", "bsp_plan_build", "bsp_plan",
            "bsp_append_kv", "bsp_decode_attn", "bsp_read_device_status", "bsp_decode_attn_noalloc",
            "bsp_plan_prefill_build", "bsp_plan_prefill", "bsp_prefill_attn", "bsp_rope_cos_sin",
-           "bsp_rope_append_kv"]
+           "bsp_rope_append_kv", "bsp_append_kv_fp8"]
 NOALLOC_SCRATCH_MIB = 32
 
 
@@ -116,6 +116,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.bsp_rope_cos_sin.argtypes = [i32, i32, ctypes.c_double, vp, vp]
     lib.bsp_rope_append_kv.restype = i32
     lib.bsp_rope_append_kv.argtypes = [P(Plan), P(RopeConfig), vp, vp, i64, vp, vp, i64, vp, i32, vp, vp, vp, vp]
+    lib.bsp_append_kv_fp8.restype = i32
+    lib.bsp_append_kv_fp8.argtypes = [P(Plan), vp, vp, i64, i32, ctypes.c_float, ctypes.c_float, vp, i32, vp, vp, vp, vp]
     lib.bsp_read_device_status.restype = i32
     lib.bsp_read_device_status.argtypes = [P(Plan), vp, i32, P(i32)]
     lib.bsp_decode_attn_noalloc.restype = i32
@@ -273,6 +275,23 @@ def append_kv(plan_: Plan, k_new: torch.Tensor, v_new: torch.Tensor, out_cache_l
     _check("bsp_append_kv", load().bsp_append_kv(
         ctypes.byref(plan_), _dptr(k_new), _dptr(v_new), int(src_row_stride), _dptr(out_cache_loc), n,
         _dptr(k_pool), _dptr(v_pool), _events(events, 2), _stream(stream)))
+
+
+FP8_SRC_16BIT, FP8_SRC_E4M3 = 0, 1
+
+
+def append_kv_fp8(plan_: Plan, k_new: torch.Tensor, v_new: torch.Tensor, out_cache_loc: torch.Tensor,
+                  k_pool: torch.Tensor, v_pool: torch.Tensor, k_mul: float = 1.0, v_mul: float = 1.0,
+                  src_row_stride: Optional[int] = None, events=None, stream=None):
+    """bsp_append_kv_fp8: uint8 (E4M3) pools; k_new/v_new rows [n, Hkv*D] of the geometry's 16-bit dtype
+    (quantised with the multipliers) or of E4M3 bytes (torch.float8_e4m3fn or uint8, copied)."""
+    n = int(out_cache_loc.numel())
+    src = FP8_SRC_E4M3 if k_new.dtype in (torch.uint8, torch.float8_e4m3fn) else FP8_SRC_16BIT
+    if src_row_stride is None:
+        src_row_stride = int(k_new.stride(0)) if k_new.dim() >= 1 and n else plan_.geo.num_kv_heads * plan_.geo.head_dim
+    _check("bsp_append_kv_fp8", load().bsp_append_kv_fp8(
+        ctypes.byref(plan_), _dptr(k_new), _dptr(v_new), int(src_row_stride), src, float(k_mul), float(v_mul),
+        _dptr(out_cache_loc), n, _dptr(k_pool), _dptr(v_pool), _events(events, 2), _stream(stream)))
 
 
 class Rope:

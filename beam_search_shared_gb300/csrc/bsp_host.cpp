@@ -17,7 +17,7 @@
 
 #include "../../include/bsp.h"
 #include "bsp_internal.h"
-#include "bsp_rope.h"
+#include "bsp_write.h"
 
 namespace {
 
@@ -655,6 +655,49 @@ bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, const void* 
     if (prepare_append() != cudaSuccess) return BSP_ERR_CUDA;
     if (!record_event(events, 0, s)) return BSP_ERR_CUDA;
     if (launch_append(p, s) != cudaSuccess) return BSP_ERR_CUDA;
+    return record_event(events, 1, s) ? BSP_OK : BSP_ERR_CUDA;
+}
+
+bsp_status bsp_append_kv_fp8(const bsp_plan_t* plan, const void* k_new, const void* v_new, int64_t src_row_stride,
+                             int32_t src_dtype, float k_mul, float v_mul, const int32_t* out_cache_loc, int32_t n,
+                             void* k_pool, void* v_pool, void* const* events, void* stream) {
+    bsp_status st = check_plan(plan);
+    if (st != BSP_OK) return st;
+    if (n < 0) return BSP_ERR_INVALID_ARG;
+    if (src_dtype != BSP_FP8_SRC_16BIT && src_dtype != BSP_FP8_SRC_E4M3) return BSP_ERR_INVALID_ARG;
+    if (src_dtype == BSP_FP8_SRC_16BIT && (!std::isfinite(k_mul) || !std::isfinite(v_mul) || !(k_mul > 0.f) ||
+                                           !(v_mul > 0.f)))
+        return BSP_ERR_INVALID_ARG;
+    if (n == 0) return BSP_OK;
+    const bsp_geometry& geo = plan->geo;
+    if (n > plan->total_rows) return BSP_ERR_INVALID_ARG;
+    const int64_t align = src_dtype == BSP_FP8_SRC_E4M3 ? 16 : 8;  // elements in 16 bytes
+    if (src_row_stride < static_cast<int64_t>(geo.num_kv_heads) * geo.head_dim || (src_row_stride % align))
+        return BSP_ERR_INVALID_ARG;
+    if (!device_ptr_ok(k_new) || !device_ptr_ok(v_new) || !device_ptr_ok(out_cache_loc) || !device_ptr_ok(k_pool) ||
+        !device_ptr_ok(v_pool))
+        return BSP_ERR_INVALID_ARG;
+    AppendFp8Params p{};
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.src_row_stride = src_row_stride;
+    p.loc = out_cache_loc;
+    p.k_pool = static_cast<uint8_t*>(k_pool);
+    p.v_pool = static_cast<uint8_t*>(v_pool);
+    p.status = static_cast<int32_t*>(plan->ws_device);
+    p.k_mul = k_mul;
+    p.v_mul = v_mul;
+    p.n = n;
+    p.Hkv = geo.num_kv_heads;
+    p.D = geo.head_dim;
+    p.ps_log2 = ilog2(geo.page_size);
+    p.num_pages = geo.num_pages;
+    // the 16-bit source is the geometry's dtype
+    const int src = src_dtype == BSP_FP8_SRC_E4M3 ? 2 : (geo.dtype == BSP_DTYPE_BF16 ? 0 : 1);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (prepare_append_fp8(src) != cudaSuccess) return BSP_ERR_CUDA;
+    if (!record_event(events, 0, s)) return BSP_ERR_CUDA;
+    if (launch_append_fp8(src, p, s) != cudaSuccess) return BSP_ERR_CUDA;
     return record_event(events, 1, s) ? BSP_OK : BSP_ERR_CUDA;
 }
 

@@ -21,7 +21,7 @@
 #include <cuda_runtime.h>
 
 #include "bsp_internal.h"
-#include "bsp_rope.h"
+#include "bsp_write.h"
 #include "../../include/bsp.h"
 
 namespace bsp {

@@ -379,6 +379,7 @@ def main():
     e2e = run_e2e(sets[0], args.e2e_steps, world)
     # ---- RoPE on the append, timed on its own after the step timing (it rewrites the new tokens' K rows)
     rope_append = measure_rope_append(sets, Kt, hbm_gbs)
+    fp8_append = measure_fp8_append(sets, Kt, hbm_gbs)
 
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
@@ -402,6 +403,7 @@ def main():
                      "algorithmic_bytes_per_launch": prefix_bytes},
         "e2e": e2e,
         "rope_append": rope_append,
+        "fp8_append": fp8_append,
         "gpu_launches": sum(1 + (s.plan.num_units > 0) + (s.plan.tail_requests > 0)
                             for s in (sets[j % len(sets)] for j in range(K))),
         "timing": "value: CUDA-graph replay of exactly K steps without timing nodes; us_prefix (and the roofline): "
@@ -471,6 +473,51 @@ def measure_rope_append(sets, Kt, hbm_gbs):
     gbs = b / (us / 1e6) / 1e9
     return {"kernel": "rope_append_kernel", "us": us, "gbs": gbs, "frac_of_hbm": gbs / hbm_gbs,
             "algorithmic_bytes_per_launch": b, "rotary_dim": wl.head_dim, "layout": "rotate-half",
+            "timing": f"one event pair around {Kt} back-to-back launches (launch gaps included)"}
+
+
+def measure_fp8_append(sets, Kt, hbm_gbs):
+    """bsp_append_kv_fp8 of each set's new tokens into E4M3 pools of the same geometry (multipliers 1):
+    Kt launches back to back in one graph, one event pair. Algorithmic bytes: the 16-bit K and V rows
+    read, the 8-bit rows written, the slots."""
+    from beam_search_shared_gb300 import bsp
+    wl = sets[0].case.workload
+    items, nbytes = [], []
+    for s in sets:
+        c = s.case
+        shape = (c.num_pages, wl.num_kv_heads, wl.page_size, wl.head_dim)
+        k8 = torch.zeros(shape, dtype=torch.uint8, device=s.q.device)
+        v8 = torch.zeros(shape, dtype=torch.uint8, device=s.q.device)
+        items.append((s, k8, v8))
+        n = int(c.out_cache_loc.size)
+        nbytes.append(n * (2 * wl.num_kv_heads * wl.head_dim * (2 + 1) + 4))
+
+    def launch(j):
+        s, k8, v8 = items[j % len(items)]
+        bsp.append_kv_fp8(s.plan, s.k_new, s.v_new, s.out_cache_loc, k8, v8)
+
+    for j in range(3):
+        launch(j)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for j in range(Kt):
+            launch(j)
+    g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    for s, _, _ in items:
+        assert bsp.read_device_status(s.plan) == (0, 0)
+    us = 1e3 * e0.elapsed_time(e1) / Kt
+    b = statistics.mean(nbytes)
+    gbs = b / (us / 1e6) / 1e9
+    return {"kernel": "append_kv_fp8_kernel", "us": us, "gbs": gbs, "frac_of_hbm": gbs / hbm_gbs,
+            "algorithmic_bytes_per_launch": b, "source": wl.dtype, "cache": "e4m3",
             "timing": f"one event pair around {Kt} back-to-back launches (launch gaps included)"}
 
 

@@ -227,6 +227,32 @@ BSP_API bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, cons
                          void* const* events, void* stream);
 
 /*
+ * Paged append into FP8 E4M3 pools (a KV cache kept in 8 bits; TensorRT-LLM
+ * PR #18614, the review follow-up on the fused per-layer KV-cache write: the
+ * fp8-source-into-fp8-cache pairing, and the review of msa_scatter.py: the
+ * write converts the source dtype to the cache's). Same slots, layout and
+ * error behaviour as bsp_append_kv, with pools of one byte per element,
+ * uint8 [num_pages][num_kv_heads][page_size][head_dim]:
+ *   src_dtype = BSP_FP8_SRC_16BIT: k_new / v_new hold the geometry's dtype
+ *                   (bf16 or fp16); element x is stored as the E4M3 value
+ *                   nearest to fp32(x) * k_mul (v_mul for V), the product
+ *                   rounded once to fp32, ties to even, values past +-448
+ *                   saturated to +-448 (k_mul, v_mul finite and > 0: a cache's
+ *                   per-tensor quantisation multipliers, 1 for a plain cast)
+ *   src_dtype = BSP_FP8_SRC_E4M3: k_new / v_new hold E4M3 bytes, copied bit
+ *                   for bit (the multipliers are not used)
+ *   src_row_stride  elements of the source type between rows, >= num_kv_heads
+ *                   * head_dim, rows 16-byte aligned (a multiple of 8 for a
+ *                   16-bit source, of 16 for E4M3)
+ * The attention entry points read 16-bit pools only.
+ */
+enum { BSP_FP8_SRC_16BIT = 0, BSP_FP8_SRC_E4M3 = 1 };
+BSP_API bsp_status bsp_append_kv_fp8(const bsp_plan_t* plan, const void* k_new, const void* v_new,
+                                     int64_t src_row_stride, int32_t src_dtype, float k_mul, float v_mul,
+                                     const int32_t* out_cache_loc, int32_t n, void* k_pool, void* v_pool,
+                                     void* const* events, void* stream);
+
+/*
  * Rotary position embedding (RoPE) on the paged append. The pages apply RoPE to
  * K before it is written to the paged cache (TensorRT-LLM PR #21738: the model
  * applies it itself, per the description; the review of flash_attn4_kernels.py
