@@ -352,58 +352,102 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     // few units per CTA, LPT alone can stack four short units on one CTA while others hold
     // three long ones. The list is written grouped by CTA; cta_off[c] .. cta_off[c+1] are
     // CTA c's units, longest first.
-    std::stable_sort(units.begin(), units.end(),
-                     [](const Unit& a, const Unit& c) { return a.f[kUnitCost] > c.f[kUnitCost]; });
     if (units.size() > static_cast<size_t>(std::numeric_limits<int32_t>::max())) return BSP_ERR_UNSUPPORTED;
+    {
+        // stable: by cost, then by creation order
+        std::vector<std::pair<int64_t, int32_t>> key(units.size());
+        for (size_t i = 0; i < units.size(); ++i) key[i] = {-static_cast<int64_t>(units[i].f[kUnitCost]), static_cast<int32_t>(i)};
+        std::sort(key.begin(), key.end());
+        std::vector<Unit> sorted(units.size());
+        for (size_t i = 0; i < units.size(); ++i) sorted[i] = units[static_cast<size_t>(key[i].second)];
+        units.swap(sorted);
+    }
     const int64_t nu = static_cast<int64_t>(units.size());
     auto utiles = [&](int64_t i) -> int64_t { return units[i].f[kUnitCost]; };
     std::vector<std::vector<int32_t>> lists;
     if (nu > 0) {
         const int64_t bins = std::min<int64_t>(nu, num_sms);
-        lists.assign(static_cast<size_t>(bins), {});
-        using Load = std::pair<int64_t, int64_t>;  // (tiles so far, cta)
-        std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-        for (int64_t c = 0; c < bins; ++c) heap.push({0, c});
+        if (bins >= (int64_t{1} << 20)) return BSP_ERR_UNSUPPORTED;
+        // LPT: a binary min-heap of (load << 20 | cta) keys, ties to the lower CTA index
+        std::vector<uint64_t> heap(static_cast<size_t>(bins));
+        for (int64_t c = 0; c < bins; ++c) heap[static_cast<size_t>(c)] = static_cast<uint64_t>(c);  // a heap already
         int64_t total = 0, lpt_max = 0;
+        std::vector<int32_t> lpt_assign(static_cast<size_t>(nu));
         for (int64_t i = 0; i < nu; ++i) {
-            Load ld = heap.top();
-            heap.pop();
-            lists[static_cast<size_t>(ld.second)].push_back(static_cast<int32_t>(i));
-            heap.push({ld.first + utiles(i), ld.second});
-            lpt_max = std::max(lpt_max, ld.first + utiles(i));
+            const uint64_t top = heap[0];
+            const int64_t c = static_cast<int64_t>(top & 0xFFFFFu);
+            const int64_t ld = static_cast<int64_t>(top >> 20) + utiles(i);
+            lpt_assign[static_cast<size_t>(i)] = static_cast<int32_t>(c);
+            lpt_max = std::max(lpt_max, ld);
             total += utiles(i);
+            // replace the root with the grown load and sift it down
+            const uint64_t key = (static_cast<uint64_t>(ld) << 20) | static_cast<uint64_t>(c);
+            size_t pos = 0;
+            const size_t n = heap.size();
+            for (;;) {
+                size_t ch = 2 * pos + 1;
+                if (ch >= n) break;
+                if (ch + 1 < n && heap[ch + 1] < heap[ch]) ++ch;
+                if (heap[ch] >= key) break;
+                heap[pos] = heap[ch];
+                pos = ch;
+            }
+            heap[pos] = key;
         }
-        // first-fit-decreasing into bins of capacity cap; false if more than `bins` are needed
-        std::vector<std::vector<int32_t>> ffd;
+        // first-fit-decreasing into `bins` bins of capacity cap (false if a unit fits none): each unit
+        // goes to the lowest-numbered bin with room, found in a max-tree of the bins' free capacity,
+        // so a probe costs O(units x log bins); the same packing as opening bins one by one
+        int64_t tsize = 1;
+        while (tsize < bins) tsize <<= 1;
+        std::vector<int64_t> tree(static_cast<size_t>(2 * tsize));
+        std::vector<int32_t> assign(static_cast<size_t>(nu)), best_assign;
         auto pack = [&](int64_t cap) -> bool {
-            ffd.clear();
-            std::vector<int64_t> load;
+            for (int64_t j = 0; j < tsize; ++j) tree[static_cast<size_t>(tsize + j)] = j < bins ? cap : -1;
+            for (int64_t v = tsize - 1; v >= 1; --v)
+                tree[static_cast<size_t>(v)] = std::max(tree[static_cast<size_t>(2 * v)], tree[static_cast<size_t>(2 * v + 1)]);
             for (int64_t i = 0; i < nu; ++i) {
-                size_t j = 0;
-                while (j < load.size() && load[j] + utiles(i) > cap) ++j;
-                if (j == load.size()) {
-                    if (static_cast<int64_t>(load.size()) == bins) return false;
-                    load.push_back(0);
-                    ffd.emplace_back();
-                }
-                load[j] += utiles(i);
-                ffd[j].push_back(static_cast<int32_t>(i));
+                const int64_t x = utiles(i);
+                if (tree[1] < x) return false;
+                int64_t v = 1;
+                while (v < tsize) v = tree[static_cast<size_t>(2 * v)] >= x ? 2 * v : 2 * v + 1;
+                assign[static_cast<size_t>(i)] = static_cast<int32_t>(v - tsize);
+                tree[static_cast<size_t>(v)] -= x;
+                for (v >>= 1; v >= 1; v >>= 1)
+                    tree[static_cast<size_t>(v)] =
+                        std::max(tree[static_cast<size_t>(2 * v)], tree[static_cast<size_t>(2 * v + 1)]);
             }
             return true;
         };
+        // the smallest capacity below LPT's largest load at which FFD packs: galloping up from the
+        // lower bound (the answer is usually within a few units of it), then bisection
         int64_t lo = std::max<int64_t>(ceil_div(total, bins), utiles(0)), hi = lpt_max - 1;
-        std::vector<std::vector<int32_t>> best;
+        for (int64_t step = 1; lo <= hi; step *= 2) {
+            const int64_t probe = std::min(hi, lo + step - 1);
+            if (pack(probe)) {
+                best_assign = assign;
+                hi = probe - 1;
+                break;
+            }
+            lo = probe + 1;
+        }
         while (lo <= hi) {
             const int64_t mid = lo + (hi - lo) / 2;
             if (pack(mid)) {
-                best.swap(ffd);
+                best_assign = assign;
                 hi = mid - 1;
             } else {
                 lo = mid + 1;
             }
         }
-        if (!best.empty()) lists.swap(best);
-        lists.resize(static_cast<size_t>(bins));
+        // the CTAs' unit lists from MULTIFIT's packing, or LPT's when no smaller capacity packs
+        {
+            const std::vector<int32_t>& a = best_assign.empty() ? lpt_assign : best_assign;
+            std::vector<int32_t> cnt(static_cast<size_t>(bins), 0);
+            for (int64_t i = 0; i < nu; ++i) ++cnt[static_cast<size_t>(a[static_cast<size_t>(i)])];
+            lists.assign(static_cast<size_t>(bins), {});
+            for (int64_t c = 0; c < bins; ++c) lists[static_cast<size_t>(c)].reserve(static_cast<size_t>(cnt[static_cast<size_t>(c)]) + 2);
+            for (int64_t i = 0; i < nu; ++i) lists[static_cast<size_t>(a[static_cast<size_t>(i)])].push_back(static_cast<int32_t>(i));
+        }
         // local search on the most-loaded CTA: move one of its units to a CTA that stays below
         // its load, or swap one of its units for a shorter one of another CTA; stop when
         // neither lowers it
@@ -442,8 +486,16 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
         }
         lists.erase(std::remove_if(lists.begin(), lists.end(), [](const std::vector<int32_t>& l) { return l.empty(); }),
                     lists.end());
-        for (auto& l : lists)  // longest first within a CTA
-            std::stable_sort(l.begin(), l.end(), [&](int32_t x, int32_t y) { return utiles(x) > utiles(y); });
+        for (auto& l : lists)  // longest first within a CTA (stable insertion sort: a few units each)
+            for (size_t i = 1; i < l.size(); ++i) {
+                const int32_t x = l[i];
+                size_t j = i;
+                while (j > 0 && utiles(l[j - 1]) < utiles(x)) {
+                    l[j] = l[j - 1];
+                    --j;
+                }
+                l[j] = x;
+            }
     }
     const int64_t ctas = static_cast<int64_t>(lists.size());
     std::vector<int32_t> cta_off(static_cast<size_t>(ctas) + 1, 0);
