@@ -418,23 +418,17 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
             }
             return true;
         };
-        // the smallest capacity below LPT's largest load at which FFD packs: galloping up from the
-        // lower bound (the answer is usually within a few units of it), then bisection
+        // the smallest capacity below LPT's largest load at which FFD packs, by bisection; a packing
+        // that succeeds bounds the answer by its own largest load, which may be below the probe
         int64_t lo = std::max<int64_t>(ceil_div(total, bins), utiles(0)), hi = lpt_max - 1;
-        for (int64_t step = 1; lo <= hi; step *= 2) {
-            const int64_t probe = std::min(hi, lo + step - 1);
-            if (pack(probe)) {
-                best_assign = assign;
-                hi = probe - 1;
-                break;
-            }
-            lo = probe + 1;
-        }
         while (lo <= hi) {
             const int64_t mid = lo + (hi - lo) / 2;
             if (pack(mid)) {
                 best_assign = assign;
-                hi = mid - 1;
+                int64_t used = 0;  // the packing's largest load: cap minus the least free capacity
+                for (int64_t j = 0; j < bins; ++j)
+                    used = std::max(used, mid - tree[static_cast<size_t>(tsize + j)]);
+                hi = std::min(mid, used) - 1;
             } else {
                 lo = mid + 1;
             }
