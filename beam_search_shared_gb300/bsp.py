@@ -22,12 +22,14 @@ STATUS_NAMES = {0: "BSP_OK", 1: "BSP_ERR_INVALID_ARG", 2: "BSP_ERR_UNSUPPORTED",
 DTYPES = {"bf16": 0, "fp16": 1, torch.bfloat16: 0, torch.float16: 1}
 FLAG_LSE_BASE2 = 1
 FLAG_CHECK = 2
+FLAG_GRAPH = 4
 MAX_TAIL = 8
 MAX_GROUP = 8
 STATUS_BYTES = 256  # device status words ahead of the plan image in the workspace
 DEVFLAG_PAGE_INDEX = 1
 DEVFLAG_TIMEOUT = 2
 DEVFLAG_POSITION = 4
+DEVFLAG_GRAPH = 8
 
 
 class NativeLibraryError(RuntimeError):
@@ -55,7 +57,7 @@ class Plan(ctypes.Structure):
         ("off_units", ctypes.c_uint64), ("off_pages", ctypes.c_uint64), ("off_part_lse", ctypes.c_uint64),
         ("off_part_o", ctypes.c_uint64), ("device_bytes_used", ctypes.c_uint64),
         ("tail_requests", ctypes.c_int32), ("total_rows", ctypes.c_int32), ("kind", ctypes.c_int32),
-        ("reserved1", ctypes.c_int32), ("reserved", ctypes.c_uint64 * 2)]
+        ("reserved1", ctypes.c_int32), ("off_cta", ctypes.c_uint64), ("reserved", ctypes.c_uint64)]
 
 
 class RopeConfig(ctypes.Structure):
@@ -183,12 +185,16 @@ def plan_build(geo: Geometry, batch, beam_width, prefix_len, tail_len, prefix_pa
     return plan, img[:plan.image_bytes]
 
 
+REQ_FIELDS = 12  # int32 per request record of a plan image
+
+
 def plan_requests(plan_: Plan, img: np.ndarray) -> np.ndarray:
-    """Per-request records of a host plan image (``plan_build``), int32 [batch, 8]: prompt length,
+    """Per-request records of a host plan image (``plan_build``), int32 [batch, 12]: prompt length,
     tail length, prompt partial states, first partial slot, first page entry, finished by the
-    prompt kernel (1) or by the tail kernel (0), two unused."""
+    prompt kernel (1) or by the tail kernel (0), two unused, query rows per head, causal base (-1:
+    none), first query row, one unused."""
     lo = plan_.off_req - STATUS_BYTES
-    return img[lo:lo + plan_.batch * 32].view(np.int32).reshape(plan_.batch, 8)
+    return img[lo:lo + plan_.batch * REQ_FIELDS * 4].view(np.int32).reshape(plan_.batch, REQ_FIELDS)
 
 
 def plan_prefill_build(geo: Geometry, batch, cached_len, prompt_len, pages, causal, num_sms,

@@ -70,6 +70,9 @@ struct DeviceLayout {
     size_t image, part_lse, part_o, total;
 };
 
+// CTA-table entries the workspace reserves beyond the units (a plan's table has num_sms + 1 entries)
+constexpr int64_t kMaxCtas = 1024;
+
 DeviceLayout device_layout(size_t image_bytes, int64_t parts, int W, const bsp_geometry& geo) {
     DeviceLayout L;
     L.image = align_up(image_bytes, kAlign);
@@ -175,7 +178,8 @@ bsp_status bsp_workspace_size(const bsp_geometry* geo, int32_t max_batch, int32_
     const int64_t parts_cap = static_cast<int64_t>(max_batch) + kExtraParts;
     const int64_t units_max = parts_cap * geo->num_kv_heads * nrb;
     const size_t image = kImageHeaderBytes + static_cast<size_t>(max_batch) * kReqFields * 4 +
-                         static_cast<size_t>(units_max) * (kUnitFields + 1) * 4 + 4 +
+                         static_cast<size_t>(units_max) * kUnitFields * 4 +
+                         (static_cast<size_t>(std::max<int64_t>(units_max, kMaxCtas)) + 1) * 4 +
                          static_cast<size_t>(max_batch) * max_prefix_pages * 4;
     DeviceLayout L = device_layout(image, parts_cap, max_beam, *geo);
     *device_bytes = L.total;
@@ -203,6 +207,7 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     bsp_status st = check_geometry(geo);
     if (st != BSP_OK) return st;
     if (!out || batch < 0 || beam_width < 1 || num_sms < 1 || prefix_pages_stride < 0) return BSP_ERR_INVALID_ARG;
+    if (num_sms > kMaxCtas) return BSP_ERR_UNSUPPORTED;
     if (max_tail < 0) return BSP_ERR_INVALID_ARG;
     if (max_tail > BSP_MAX_TAIL) return BSP_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(batch) * beam_width > (int64_t(1) << 30)) return BSP_ERR_UNSUPPORTED;
@@ -492,7 +497,9 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
             }
     }
     const int64_t ctas = static_cast<int64_t>(lists.size());
-    std::vector<int32_t> cta_off(static_cast<size_t>(ctas) + 1, 0);
+    // a decode plan's CTA table has num_sms + 1 entries (CTAs past `ctas` have no units), so a launch
+    // of num_sms CTAs captured in a CUDA graph reads a valid table after any later plan
+    std::vector<int32_t> cta_off(static_cast<size_t>(pf ? ctas : std::max<int64_t>(ctas, num_sms)) + 1, 0);
     {
         std::vector<Unit> dealt;
         dealt.reserve(units.size());
@@ -500,20 +507,34 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
             for (int32_t i : lists[static_cast<size_t>(c)]) dealt.push_back(units[i]);
             cta_off[static_cast<size_t>(c) + 1] = static_cast<int32_t>(dealt.size());
         }
+        for (size_t c = static_cast<size_t>(ctas) + 1; c < cta_off.size(); ++c) cta_off[c] = static_cast<int32_t>(dealt.size());
         units.swap(dealt);
     }
 
-    // ---- image
+    // ---- image. A decode plan has a fixed layout for its batch, beam width, SM count and page-table
+    // stride: every section at an offset that does not depend on the lengths (the unit list sized
+    // for the most key splits the planner makes), so the device addresses baked into a captured
+    // CUDA graph stay valid for every later plan of the same shape. A prefill plan is packed.
+    const int64_t parts_cap = pf ? parts : static_cast<int64_t>(batch) + kExtraParts;
+    const size_t units_cap = pf ? units.size() : static_cast<size_t>(parts_cap) * Hkv * nrb;
+    const size_t pages_cap = pf ? static_cast<size_t>(total_pages) : static_cast<size_t>(batch) * prefix_pages_stride;
+    if (units.size() > units_cap || static_cast<size_t>(total_pages) > pages_cap) return BSP_ERR_CAPACITY;
     const size_t off_req = kImageHeaderBytes;
     const size_t off_units = off_req + static_cast<size_t>(batch) * kReqFields * 4;
-    const size_t off_cta = off_units + units.size() * kUnitFields * 4;
+    const size_t off_cta = off_units + units_cap * kUnitFields * 4;
     const size_t off_pages = off_cta + cta_off.size() * 4;
-    const size_t need = off_pages + static_cast<size_t>(total_pages) * 4;
+    const size_t need = off_pages + pages_cap * 4;
     if (!image || image_bytes < need) return BSP_ERR_CAPACITY;
     uint8_t* img = static_cast<uint8_t*>(image);
     std::memset(img, 0, kImageHeaderBytes);
+    // header: [2] batch, [3] units, [4] beam width, [5] SM count, [6] kind, [7] tail bound (what a
+    // replayed graph checks against its capture)
     reinterpret_cast<int32_t*>(img)[2] = batch;
     reinterpret_cast<int32_t*>(img)[3] = static_cast<int32_t>(units.size());
+    reinterpret_cast<int32_t*>(img)[4] = beam_width;
+    reinterpret_cast<int32_t*>(img)[5] = num_sms;
+    reinterpret_cast<int32_t*>(img)[6] = pf ? 1 : 0;
+    reinterpret_cast<int32_t*>(img)[7] = max_tail;
     int32_t* req = reinterpret_cast<int32_t*>(img + off_req);
     for (int b = 0; b < batch; ++b) {
         int32_t* r = req + static_cast<size_t>(b) * kReqFields;
@@ -559,9 +580,10 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     out->kind = pf ? 1 : 0;
     out->image_bytes = need;
     // offsets relative to the device workspace
-    DeviceLayout L = device_layout(need, parts, beam_width, *geo);
+    DeviceLayout L = device_layout(need, parts_cap, beam_width, *geo);
     out->off_req = kStatusBytes + off_req;
     out->off_units = kStatusBytes + off_units;
+    out->off_cta = kStatusBytes + off_cta;
     out->off_pages = kStatusBytes + off_pages;
     out->off_part_lse = kStatusBytes + L.image;
     out->off_part_o = kStatusBytes + L.image + L.part_lse;
@@ -813,6 +835,7 @@ bsp_status bsp_read_device_status(const bsp_plan_t* plan, void* stream, int32_t 
     if (clear && cudaMemset(plan->ws_device, 0, sizeof flags) != cudaSuccess) return BSP_ERR_CUDA;
     if (flags_out) *flags_out = flags;
     if (flags & (BSP_DEVFLAG_PAGE_INDEX | BSP_DEVFLAG_POSITION)) return BSP_ERR_PAGE_INDEX;
+    if (flags & BSP_DEVFLAG_GRAPH) return BSP_ERR_STALE_PLAN;
     if (flags & BSP_DEVFLAG_TIMEOUT) return BSP_ERR_DEVICE_TIMEOUT;
     return BSP_OK;
 }
@@ -829,7 +852,10 @@ bsp_status attn_impl(const bsp_plan_t* plan, const void* q, const void* k_pool, 
     bsp_status st = check_plan(plan);
     if (st != BSP_OK) return st;
     if (plan->kind != (prefill ? 1 : 0)) return BSP_ERR_INVALID_ARG;
-    if (flags & ~(BSP_FLAG_LSE_BASE2 | BSP_FLAG_CHECK)) return BSP_ERR_INVALID_ARG;
+    if (flags & ~(BSP_FLAG_LSE_BASE2 | BSP_FLAG_CHECK | BSP_FLAG_GRAPH)) return BSP_ERR_INVALID_ARG;
+    // graph mode: launch shapes that do not depend on the plan's lengths (decode plans only)
+    const bool graph = (flags & BSP_FLAG_GRAPH) != 0;
+    if (graph && (prefill || (flags & BSP_FLAG_CHECK))) return BSP_ERR_INVALID_ARG;
     if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BSP_ERR_INVALID_ARG;
     const bsp_geometry& geo = plan->geo;
     const int64_t R = plan->total_rows;
@@ -850,9 +876,9 @@ bsp_status attn_impl(const bsp_plan_t* plan, const void* q, const void* k_pool, 
 
     // everything that is not a launch (attributes, tensor maps, parameters) comes before the
     // first timing event
-    const bool prefix = plan->num_units > 0;
+    const bool prefix = graph || plan->num_units > 0;
     if (prefix && prepare_prefix(D, bf16) != cudaSuccess) return BSP_ERR_CUDA;
-    if (prepare_tail(D, bf16, plan->max_tail_len, Hq) != cudaSuccess) return BSP_ERR_CUDA;
+    if (prepare_tail(D, bf16, graph ? plan->max_tail : plan->max_tail_len, Hq) != cudaSuccess) return BSP_ERR_CUDA;
     CUtensorMap tq, tk, tv;
     PrefixParams pp{};
     if (prefix) {
@@ -880,7 +906,7 @@ bsp_status attn_impl(const bsp_plan_t* plan, const void* q, const void* k_pool, 
         pp.max_seq = max_seq;
         pp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
         pp.units = reinterpret_cast<const int32_t*>(ws + plan->off_units);
-        pp.cta_off = pp.units + static_cast<size_t>(plan->num_units) * kUnitFields;
+        pp.cta_off = reinterpret_cast<const int32_t*>(ws + plan->off_cta);
         pp.req = reinterpret_cast<const int32_t*>(ws + plan->off_req);
         pp.pages = reinterpret_cast<const int32_t*>(ws + plan->off_pages);
         pp.part_o = reinterpret_cast<float*>(ws + plan->off_part_o);
@@ -894,7 +920,11 @@ bsp_status attn_impl(const bsp_plan_t* plan, const void* q, const void* k_pool, 
         pp.Wblk = plan->beams_per_block;
         pp.bq = qbeams;
         pp.num_pages = geo.num_pages;
-        pp.num_units = plan->num_units;
+        pp.num_units = graph ? 1 : plan->num_units;  // (graph: launched whatever the captured plan holds)
+        if (graph) {
+            pp.graph_hdr = reinterpret_cast<const int32_t*>(ws + kStatusBytes);
+            pp.graph_batch = plan->batch;
+        }
         pp.scale_log2 = softmax_scale * log2e;
     }
     TailParams tp{};
@@ -920,14 +950,20 @@ bsp_status attn_impl(const bsp_plan_t* plan, const void* q, const void* k_pool, 
     tp.max_seq = max_seq;
     tp.scale_log2 = softmax_scale * log2e;
     tp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
+    if (graph) {
+        tp.graph_hdr = reinterpret_cast<const int32_t*>(ws + kStatusBytes);
+        tp.graph_max_tail = plan->max_tail;
+    }
 
     auto record = [&](int i) -> bool { return record_event(events, i, s); };
     if (!record(0)) return BSP_ERR_CUDA;
-    if (prefix && launch_prefix(D, bf16, plan->prefix_ctas, tq, tk, tv, pp, s) != cudaSuccess) return BSP_ERR_CUDA;
+    if (prefix && launch_prefix(D, bf16, graph ? plan->num_sms : plan->prefix_ctas, tq, tk, tv, pp, s) != cudaSuccess)
+        return BSP_ERR_CUDA;
     if (!record(1)) return BSP_ERR_CUDA;
     // without timing events between them, the tail kernel overlaps the end of the prompt kernel
-    if (plan->tail_requests > 0 &&
-        launch_tail(D, bf16, plan->max_tail_len, tp, prefix && events == nullptr, s) != cudaSuccess)
+    if ((graph || plan->tail_requests > 0) &&
+        launch_tail(D, bf16, graph ? plan->max_tail : plan->max_tail_len, tp, prefix && events == nullptr, s) !=
+            cudaSuccess)
         return BSP_ERR_CUDA;
     if (!record(2)) return BSP_ERR_CUDA;
     if (flags & BSP_FLAG_CHECK) return bsp_read_device_status(plan, stream, 1, nullptr);

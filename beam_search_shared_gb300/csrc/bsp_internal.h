@@ -61,6 +61,10 @@ struct PrefixParams {
     int W, Hq, Hkv, G, ps_log2, Wblk, num_pages;
     int bq;            // > 0: half-row softmax, bq beams of the block per TMEM lane quadrant (prefix_quad_beams)
     int num_units;     // units in the list
+    // graph mode (else null): the staged plan's header, checked at the start against the launch
+    // (batch, beam width, one CTA per SM of the plan, a decode plan)
+    const int32_t* graph_hdr;
+    int graph_batch;
     float scale_log2;  // softmax_scale * log2(e)
 };
 
@@ -79,6 +83,10 @@ struct TailParams {
     int B, W, Hq, Hkv, G, ps_log2, num_pages, beam_pages_stride, max_seq;
     float scale_log2;
     int lse_base2;
+    // graph mode (else null): the staged plan's header, checked against the launch (batch, beam width,
+    // a decode plan, a tail bound within the one the launch was made for)
+    const int32_t* graph_hdr;
+    int graph_max_tail;
 };
 
 struct AppendParams {

@@ -170,7 +170,7 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
         pp.max_seq = max_seq;
         pp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
         pp.units = reinterpret_cast<const int32_t*>(ws + plan.off_units);
-        pp.cta_off = pp.units + static_cast<size_t>(plan.num_units) * kUnitFields;
+        pp.cta_off = reinterpret_cast<const int32_t*>(ws + plan.off_cta);
         pp.req = reinterpret_cast<const int32_t*>(ws + plan.off_req);
         pp.pages = reinterpret_cast<const int32_t*>(ws + plan.off_pages);
         pp.part_o = reinterpret_cast<float*>(ws + plan.off_part_o);

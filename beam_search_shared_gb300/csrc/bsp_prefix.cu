@@ -219,6 +219,15 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     PrefixBarriers* bars = reinterpret_cast<PrefixBarriers*>(smem + C::OFF_BAR);
     volatile int* abort_flag = &bars->abort_flag;
 
+    if (p.graph_hdr != nullptr) {
+        // a launch replayed from a CUDA graph: the plan staged since must have the captured shape
+        const int4 h0 = __ldg(reinterpret_cast<const int4*>(p.graph_hdr));
+        const int4 h1 = __ldg(reinterpret_cast<const int4*>(p.graph_hdr) + 1);
+        if (h0.z != p.graph_batch || h1.x != p.W || h1.y != static_cast<int>(gridDim.x) || h1.z != 0) {
+            if (threadIdx.x == 0) atomicOr(p.status, BSP_DEVFLAG_GRAPH);
+            return;
+        }
+    }
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;

@@ -81,6 +81,15 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
     constexpr unsigned FULL = 0xffffffffu;
     __shared__ long long s_off[BSP_MAX_TAIL];  // element offset of tail row t for kv head 0, -1 if unreadable
 
+    if (p.graph_hdr != nullptr) {
+        // a launch replayed from a CUDA graph: the plan staged since must have the captured shape
+        const int4 h0 = __ldg(reinterpret_cast<const int4*>(p.graph_hdr));
+        const int4 h1 = __ldg(reinterpret_cast<const int4*>(p.graph_hdr) + 1);
+        if (h0.z != p.B || h1.x != p.W || h1.z != 0 || h1.w > p.graph_max_tail) {
+            if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.status, BSP_DEVFLAG_GRAPH);
+            return;
+        }
+    }
     const int r = blockIdx.x;
     const int b = r / p.W;
     const int w = r % p.W;

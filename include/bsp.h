@@ -73,7 +73,17 @@ enum { BSP_DTYPE_BF16 = 0, BSP_DTYPE_FP16 = 1 };
 /* bsp_decode_attn flags */
 enum {
     BSP_FLAG_LSE_BASE2 = 1, /* write LSE as log2-sum-exp2 instead of the natural log */
-    BSP_FLAG_CHECK = 2      /* synchronise after the launches and report device status */
+    BSP_FLAG_CHECK = 2,     /* synchronise after the launches and report device status */
+    BSP_FLAG_GRAPH = 4      /* bsp_decode_attn only, not with BSP_FLAG_CHECK: launch shapes that do not
+                               depend on the plan's lengths, so that the launches may be captured in a
+                               CUDA graph once and replayed after every later bsp_plan on the same
+                               workspace with the same batch, beam_width, max_tail, geometry, SM count,
+                               page-table stride and buffers (the CUDA-graph serving mode: TensorRT-LLM
+                               PR #21738, description: the per-step host plan runs before capture and
+                               before every replay; the tail bound caps the tail under graphs). The
+                               prompt kernel runs one CTA per SM of the plan and the tail kernel is
+                               always launched for max_tail tail rows; a replay whose staged plan has
+                               another shape writes nothing and sets BSP_DEVFLAG_GRAPH */
 };
 
 #define BSP_MAX_TAIL 8   /* tail positions per beam (TensorRT-LLM PR #21738, description: correctness and limits) */
@@ -83,6 +93,8 @@ enum {
 #define BSP_DEVFLAG_PAGE_INDEX 1
 #define BSP_DEVFLAG_TIMEOUT 2
 #define BSP_DEVFLAG_POSITION 4  /* a RoPE position outside [0, max_position) (bsp_rope_append_kv) */
+#define BSP_DEVFLAG_GRAPH 8     /* a replayed graph-mode launch found a plan of another shape (nothing
+                                   written); reported as BSP_ERR_STALE_PLAN */
 
 typedef struct bsp_geometry {
     int32_t num_q_heads;  /* Hq */
@@ -134,7 +146,8 @@ typedef struct bsp_plan_t {
                                     tokens of all requests (prefill) */
     int32_t kind;                /* 0: a decode-step plan (bsp_plan); 1: a prefill plan (bsp_plan_prefill) */
     int32_t reserved1;
-    uint64_t reserved[2];
+    uint64_t off_cta;            /* byte offset of the per-CTA unit table */
+    uint64_t reserved;
 } bsp_plan_t;
 
 /* Human-readable name of a bsp_status value. Never NULL. */

@@ -108,7 +108,7 @@ def decode_image(plan, img, with_cta=False):
     req = i32[(plan.off_req - base) // 4:(plan.off_units - base) // 4].reshape(plan.batch, 12)
     u0 = (plan.off_units - base) // 4
     units = i32[u0:u0 + plan.num_units * 8].reshape(plan.num_units, 8)
-    cta_off = i32[u0 + plan.num_units * 8:(plan.off_pages - base) // 4]
+    cta_off = i32[(plan.off_cta - base) // 4:(plan.off_pages - base) // 4]
     pages = i32[(plan.off_pages - base) // 4:]
     if with_cta:
         return req, units, pages, cta_off
@@ -275,3 +275,21 @@ def test_prefill_plan_units_and_records(lib, causal):
     for b in range(4):
         n = -(-(C[b] + S[b]) // ps) if S[b] else 0
         np.testing.assert_array_equal(pl[req[b][4]:req[b][4] + n], pages[b, :n])
+
+
+def test_plan_requests_reads_whole_records(lib):
+    """bsp.plan_requests returns the 12-field request records in order (the fused flag of a mixed
+    batch: request 1 has more tail keys per row block than one tile holds)."""
+    g = geo(Hq=32, Hkv=8, D=128, ps=16, npages=4000, dtype="fp16")
+    B, W = 3, 30
+    P = np.array([300, 500, 700], np.int32)
+    T = np.array([2, 8, 0], np.int32)
+    pages = np.arange(B * 64, dtype=np.int32).reshape(B, 64)
+    plan, img = bsp.plan_build(g, B, W, P, T, pages, 8, 8)    # 24 units fill 8 SMs: no key splits
+    req = bsp.plan_requests(plan, img)
+    assert req.shape == (B, 12)
+    np.testing.assert_array_equal(req[:, 2], 1)
+    np.testing.assert_array_equal(req[:, 0], P)
+    np.testing.assert_array_equal(req[:, 1], T)
+    np.testing.assert_array_equal(req[:, 5], [1, 0, 1])       # 30 x 8 = 240 tail keys > 128
+    np.testing.assert_array_equal(req[:, 10], np.arange(B) * W)
