@@ -69,7 +69,7 @@ _lib = None
 EXPORTS = ["bsp_status_string", "bsp_bucket_rows", "bsp_workspace_size", "bsp_plan_build", "bsp_plan",
            "bsp_append_kv", "bsp_decode_attn", "bsp_read_device_status", "bsp_decode_attn_noalloc",
            "bsp_plan_prefill_build", "bsp_plan_prefill", "bsp_prefill_attn", "bsp_rope_cos_sin",
-           "bsp_rope_append_kv", "bsp_append_kv_fp8"]
+           "bsp_rope_append_kv", "bsp_append_kv_fp8", "bsp_rope_append_kv_fp8"]
 NOALLOC_SCRATCH_MIB = 32
 
 
@@ -118,6 +118,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.bsp_rope_cos_sin.argtypes = [i32, i32, ctypes.c_double, vp, vp]
     lib.bsp_rope_append_kv.restype = i32
     lib.bsp_rope_append_kv.argtypes = [P(Plan), P(RopeConfig), vp, vp, i64, vp, vp, i64, vp, i32, vp, vp, vp, vp]
+    lib.bsp_rope_append_kv_fp8.restype = i32
+    lib.bsp_rope_append_kv_fp8.argtypes = [P(Plan), P(RopeConfig), vp, vp, i64, vp, vp, i64, ctypes.c_float,
+                                           ctypes.c_float, vp, i32, vp, vp, vp, vp]
     lib.bsp_append_kv_fp8.restype = i32
     lib.bsp_append_kv_fp8.argtypes = [P(Plan), vp, vp, i64, i32, ctypes.c_float, ctypes.c_float, vp, i32, vp, vp, vp, vp]
     lib.bsp_read_device_status.restype = i32
@@ -340,6 +343,24 @@ def rope_append_kv(plan_: Plan, rope: Rope, positions: torch.Tensor, q: Optional
         ctypes.byref(plan_), ctypes.byref(rope.config), _dptr(positions), _dptr(q), int(q_row_stride or 0),
         _dptr(k_new), _dptr(v_new), int(src_row_stride), _dptr(out_cache_loc), n, _dptr(k_pool), _dptr(v_pool),
         _events(events, 2), _stream(stream)))
+
+
+def rope_append_kv_fp8(plan_: Plan, rope: Rope, positions: torch.Tensor, q: Optional[torch.Tensor],
+                       k_new: torch.Tensor, v_new: torch.Tensor, out_cache_loc: torch.Tensor, k_pool: torch.Tensor,
+                       v_pool: torch.Tensor, k_mul: float = 1.0, v_mul: float = 1.0,
+                       src_row_stride: Optional[int] = None, q_row_stride: Optional[int] = None, events=None,
+                       stream=None):
+    """bsp_rope_append_kv_fp8: rotated K and V quantised into uint8 (E4M3) pools, q rotated in place."""
+    n = int(out_cache_loc.numel())
+    row = plan_.geo.num_kv_heads * plan_.geo.head_dim
+    if src_row_stride is None:
+        src_row_stride = int(k_new.stride(0)) if k_new.dim() >= 1 and n else row
+    if q is not None and q_row_stride is None:
+        q_row_stride = int(q.stride(0)) if q.dim() >= 1 and n else plan_.geo.num_q_heads * plan_.geo.head_dim
+    _check("bsp_rope_append_kv_fp8", load().bsp_rope_append_kv_fp8(
+        ctypes.byref(plan_), ctypes.byref(rope.config), _dptr(positions), _dptr(q), int(q_row_stride or 0),
+        _dptr(k_new), _dptr(v_new), int(src_row_stride), float(k_mul), float(v_mul), _dptr(out_cache_loc), n,
+        _dptr(k_pool), _dptr(v_pool), _events(events, 2), _stream(stream)))
 
 
 def decode_attn(plan_: Plan, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,

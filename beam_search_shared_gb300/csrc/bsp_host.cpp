@@ -779,13 +779,16 @@ bsp_status bsp_rope_cos_sin(int32_t max_position, int32_t rotary_dim, double bas
                : BSP_ERR_CUDA;
 }
 
-bsp_status bsp_rope_append_kv(const bsp_plan_t* plan, const bsp_rope_config* rope, const int32_t* positions, void* q,
-                              int64_t q_row_stride, const void* k_new, const void* v_new, int64_t src_row_stride,
-                              const int32_t* out_cache_loc, int32_t n, void* k_pool, void* v_pool,
-                              void* const* events, void* stream) {
+static bsp_status rope_append_impl(const bsp_plan_t* plan, const bsp_rope_config* rope, const int32_t* positions,
+                                   void* q, int64_t q_row_stride, const void* k_new, const void* v_new,
+                                   int64_t src_row_stride, bool fp8, float k_mul, float v_mul,
+                                   const int32_t* out_cache_loc, int32_t n, void* k_pool, void* v_pool,
+                                   void* const* events, void* stream) {
     bsp_status st = check_plan(plan);
     if (st != BSP_OK) return st;
     if (!rope || n < 0) return BSP_ERR_INVALID_ARG;
+    if (fp8 && (!std::isfinite(k_mul) || !std::isfinite(v_mul) || !(k_mul > 0.f) || !(v_mul > 0.f)))
+        return BSP_ERR_INVALID_ARG;
     const bsp_geometry& geo = plan->geo;
     const int D = geo.head_dim;
     if (rope->rotary_dim < 16 || rope->rotary_dim > D || (rope->rotary_dim & 15) || rope->max_position <= 0 ||
@@ -818,12 +821,30 @@ bsp_status bsp_rope_append_kv(const bsp_plan_t* plan, const bsp_rope_config* rop
     p.rot = rope->rotary_dim;
     p.interleaved = rope->interleaved;
     p.max_pos = rope->max_position;
+    p.k_mul = k_mul;
+    p.v_mul = v_mul;
     const bool bf16 = geo.dtype == BSP_DTYPE_BF16;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (prepare_rope_append(D, bf16) != cudaSuccess) return BSP_ERR_CUDA;
+    if (prepare_rope_append(D, bf16, fp8) != cudaSuccess) return BSP_ERR_CUDA;
     if (!record_event(events, 0, s)) return BSP_ERR_CUDA;
-    if (launch_rope_append(D, bf16, p, s) != cudaSuccess) return BSP_ERR_CUDA;
+    if (launch_rope_append(D, bf16, fp8, p, s) != cudaSuccess) return BSP_ERR_CUDA;
     return record_event(events, 1, s) ? BSP_OK : BSP_ERR_CUDA;
+}
+
+bsp_status bsp_rope_append_kv(const bsp_plan_t* plan, const bsp_rope_config* rope, const int32_t* positions, void* q,
+                              int64_t q_row_stride, const void* k_new, const void* v_new, int64_t src_row_stride,
+                              const int32_t* out_cache_loc, int32_t n, void* k_pool, void* v_pool,
+                              void* const* events, void* stream) {
+    return rope_append_impl(plan, rope, positions, q, q_row_stride, k_new, v_new, src_row_stride, false, 1.f, 1.f,
+                            out_cache_loc, n, k_pool, v_pool, events, stream);
+}
+
+bsp_status bsp_rope_append_kv_fp8(const bsp_plan_t* plan, const bsp_rope_config* rope, const int32_t* positions,
+                                  void* q, int64_t q_row_stride, const void* k_new, const void* v_new,
+                                  int64_t src_row_stride, float k_mul, float v_mul, const int32_t* out_cache_loc,
+                                  int32_t n, void* k_pool, void* v_pool, void* const* events, void* stream) {
+    return rope_append_impl(plan, rope, positions, q, q_row_stride, k_new, v_new, src_row_stride, true, k_mul, v_mul,
+                            out_cache_loc, n, k_pool, v_pool, events, stream);
 }
 
 bsp_status bsp_read_device_status(const bsp_plan_t* plan, void* stream, int32_t clear, int32_t* flags_out) {

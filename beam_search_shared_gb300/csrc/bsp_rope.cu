@@ -18,6 +18,7 @@
 // of the distinct positions.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "bsp_internal.h"
@@ -49,6 +50,21 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
     return w;
 }
 
+// 8 values times a multiplier, each product rounded to fp32, then to the nearest E4M3 (ties to even,
+// saturating at +-448); byte e of the result holds value e
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float mul) {
+    uint32_t w[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const float2 a = make_float2(__fmul_rn(f[4 * e], mul), __fmul_rn(f[4 * e + 1], mul));
+        const float2 b = make_float2(__fmul_rn(f[4 * e + 2], mul), __fmul_rn(f[4 * e + 3], mul));
+        const uint32_t lo = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+        const uint32_t hi = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3);
+        w[e] = (lo & 0xffffu) | (hi << 16);
+    }
+    return make_uint2(w[0], w[1]);
+}
+
 // x cos - y sin (sign = -1) or x cos + y sin (sign = +1): one product, one fused multiply-add
 __device__ __forceinline__ float rot1(float x, float y, float c, float s, float sign) {
     return __fmaf_rn(x, c, sign * __fmul_rn(y, s));
@@ -56,7 +72,9 @@ __device__ __forceinline__ float rot1(float x, float y, float c, float s, float 
 
 }  // namespace
 
-template <int D, bool BF16>
+// FP8: K and V go to E4M3 pools: the rotated K values (fp32, before any 16-bit rounding) and the V
+// values times their multipliers, quantised; q stays in its 16-bit dtype
+template <int D, bool BF16, bool FP8>
 __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendParams p) {
     constexpr int CPR = D / 8;     // 16-byte chunks per head row
     constexpr int RPW = 32 / CPR;  // head rows per warp
@@ -93,6 +111,16 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendParams p) {
     const bool rotated = !is_v && 8 * c < p.rot;
     const int half = p.rot >> 1;
     uint4 y = x;
+    float f[8];  // FP8: the chunk's values before quantisation
+    if constexpr (FP8) {
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 a = unpack2(xw[u], BF16);
+            f[2 * u] = a.x;
+            f[2 * u + 1] = a.y;
+        }
+    }
     if (!p.interleaved) {
         // partner chunk of the rotate-half layout: c +- rot/16 (every lane takes part in the shuffles)
         const int hc = p.rot >> 4;
@@ -120,8 +148,13 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendParams p) {
             for (int u = 0; u < 4; ++u) {
                 const float2 a = unpack2(xw[u], BF16);
                 const float2 b = unpack2(zw[u], BF16);
-                out[u] = pack2(rot1(a.x, b.x, cs[2 * u], sn[2 * u], sign), rot1(a.y, b.y, cs[2 * u + 1], sn[2 * u + 1], sign),
-                               BF16);
+                const float r0 = rot1(a.x, b.x, cs[2 * u], sn[2 * u], sign);
+                const float r1 = rot1(a.y, b.y, cs[2 * u + 1], sn[2 * u + 1], sign);
+                out[u] = pack2(r0, r1, BF16);
+                if constexpr (FP8) {
+                    f[2 * u] = r0;
+                    f[2 * u + 1] = r1;
+                }
             }
             y = make_uint4(out[0], out[1], out[2], out[3]);
         }
@@ -137,7 +170,13 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendParams p) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const float2 a = unpack2(xw[u], BF16);
-            out[u] = pack2(rot1(a.x, a.y, cs[u], sn[u], -1.f), rot1(a.y, a.x, cs[u], sn[u], 1.f), BF16);
+            const float r0 = rot1(a.x, a.y, cs[u], sn[u], -1.f);
+            const float r1 = rot1(a.y, a.x, cs[u], sn[u], 1.f);
+            out[u] = pack2(r0, r1, BF16);
+            if constexpr (FP8) {
+                f[2 * u] = r0;
+                f[2 * u + 1] = r1;
+            }
         }
         y = make_uint4(out[0], out[1], out[2], out[3]);
     }
@@ -150,8 +189,13 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendParams p) {
         const long long page = loc >> p.ps_log2;
         const long long off = loc & ((1 << p.ps_log2) - 1);
         const long long dst = (((page * p.Hkv + h) << p.ps_log2) + off) * D;
-        uint16_t* pool = static_cast<uint16_t*>(is_k ? p.k_pool : p.v_pool);
-        reinterpret_cast<uint4*>(pool + dst)[c] = y;
+        if constexpr (FP8) {
+            uint8_t* pool = static_cast<uint8_t*>(is_k ? p.k_pool : p.v_pool);
+            reinterpret_cast<uint2*>(pool + dst)[c] = quant8(f, is_k ? p.k_mul : p.v_mul);
+        } else {
+            uint16_t* pool = static_cast<uint16_t*>(is_k ? p.k_pool : p.v_pool);
+            reinterpret_cast<uint4*>(pool + dst)[c] = y;
+        }
     } else {
         reinterpret_cast<uint4*>(row)[c] = y;
     }
@@ -170,35 +214,45 @@ __global__ void rope_cos_sin_kernel(int max_pos, int rot, double base, float* cs
     cs[static_cast<long long>(pos) * rot + half + j] = __double2float_rn(s);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool FP8>
 static cudaError_t launch_rope_t(const RopeAppendParams& p, cudaStream_t stream) {
     constexpr int RPW = 32 / (D / 8);
     const long long rows = static_cast<long long>(p.n) * (2 * p.Hkv + (p.q ? p.Hq : 0));
     if (rows == 0) return cudaSuccess;
     const long long warps = (rows + RPW - 1) / RPW;
     const long long blocks = (warps + 7) / 8;
-    rope_append_kernel<D, BF16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+    rope_append_kernel<D, BF16, FP8><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_rope_append(int head_dim, bool bf16, const RopeAppendParams& p, cudaStream_t stream) {
+template <bool FP8>
+static cudaError_t launch_rope_d(int head_dim, bool bf16, const RopeAppendParams& p, cudaStream_t stream) {
     switch (head_dim) {
-        case 64: return bf16 ? launch_rope_t<64, true>(p, stream) : launch_rope_t<64, false>(p, stream);
-        case 128: return bf16 ? launch_rope_t<128, true>(p, stream) : launch_rope_t<128, false>(p, stream);
-        case 256: return bf16 ? launch_rope_t<256, true>(p, stream) : launch_rope_t<256, false>(p, stream);
+        case 64: return bf16 ? launch_rope_t<64, true, FP8>(p, stream) : launch_rope_t<64, false, FP8>(p, stream);
+        case 128: return bf16 ? launch_rope_t<128, true, FP8>(p, stream) : launch_rope_t<128, false, FP8>(p, stream);
+        case 256: return bf16 ? launch_rope_t<256, true, FP8>(p, stream) : launch_rope_t<256, false, FP8>(p, stream);
         default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_rope_append(int head_dim, bool bf16, bool fp8, const RopeAppendParams& p, cudaStream_t stream) {
+    return fp8 ? launch_rope_d<true>(head_dim, bf16, p, stream) : launch_rope_d<false>(head_dim, bf16, p, stream);
+}
+
+template <bool FP8>
+static const void* rope_fn(int head_dim, bool bf16) {
+    switch (head_dim) {
+        case 64: return bf16 ? (const void*)rope_append_kernel<64, true, FP8> : (const void*)rope_append_kernel<64, false, FP8>;
+        case 128: return bf16 ? (const void*)rope_append_kernel<128, true, FP8> : (const void*)rope_append_kernel<128, false, FP8>;
+        case 256: return bf16 ? (const void*)rope_append_kernel<256, true, FP8> : (const void*)rope_append_kernel<256, false, FP8>;
+        default: return nullptr;
     }
 }
 
 // the same L1/shared split as the prompt kernel, so SMs are not reconfigured between the kernels of a step
-cudaError_t prepare_rope_append(int head_dim, bool bf16) {
-    const void* f = nullptr;
-    switch (head_dim) {
-        case 64: f = bf16 ? (const void*)rope_append_kernel<64, true> : (const void*)rope_append_kernel<64, false>; break;
-        case 128: f = bf16 ? (const void*)rope_append_kernel<128, true> : (const void*)rope_append_kernel<128, false>; break;
-        case 256: f = bf16 ? (const void*)rope_append_kernel<256, true> : (const void*)rope_append_kernel<256, false>; break;
-        default: return cudaErrorInvalidValue;
-    }
+cudaError_t prepare_rope_append(int head_dim, bool bf16, bool fp8) {
+    const void* f = fp8 ? rope_fn<true>(head_dim, bf16) : rope_fn<false>(head_dim, bf16);
+    if (!f) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
 }
 

@@ -22,9 +22,11 @@ struct RopeAppendParams {
     int32_t* status;
     int n, Hq, Hkv, ps_log2, num_pages;
     int rot, interleaved, max_pos;
+    float k_mul, v_mul;      // fp8 pools: quantisation multipliers of K (after the rotation) and V
 };
-cudaError_t launch_rope_append(int head_dim, bool bf16, const RopeAppendParams& p, cudaStream_t stream);
-cudaError_t prepare_rope_append(int head_dim, bool bf16);
+// fp8: the pools are E4M3 bytes (K and V quantised), else the q dtype
+cudaError_t launch_rope_append(int head_dim, bool bf16, bool fp8, const RopeAppendParams& p, cudaStream_t stream);
+cudaError_t prepare_rope_append(int head_dim, bool bf16, bool fp8);
 cudaError_t launch_rope_cos_sin(int max_pos, int rot, double base, float* cos_sin, cudaStream_t stream);
 
 // Append into E4M3 pools (bsp_append.cu).

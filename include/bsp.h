@@ -330,6 +330,22 @@ BSP_API bsp_status bsp_rope_append_kv(const bsp_plan_t* plan, const bsp_rope_con
                                       void* k_pool, void* v_pool, void* const* events, void* stream);
 
 /*
+ * RoPE on the append into FP8 E4M3 pools (the fused write of the FP8 KV path:
+ * TensorRT-LLM PR #18614, the review follow-up on the fused per-layer KV-cache
+ * write, whose RoPE kernel emits E4M3 K/V). As bsp_rope_append_kv, except that
+ * k_pool / v_pool are uint8 E4M3 pools: each rotated K value (fp32, not rounded
+ * to 16 bits first) times k_mul and each V value times v_mul, the product
+ * rounded to fp32, is stored as the nearest E4M3 value (ties to even,
+ * saturating at +-448); q (if given) is rotated in place in its 16-bit dtype.
+ * k_mul, v_mul finite and > 0. Errors as bsp_rope_append_kv.
+ */
+BSP_API bsp_status bsp_rope_append_kv_fp8(const bsp_plan_t* plan, const bsp_rope_config* rope, const int32_t* positions,
+                                          void* q, int64_t q_row_stride, const void* k_new, const void* v_new,
+                                          int64_t src_row_stride, float k_mul, float v_mul,
+                                          const int32_t* out_cache_loc, int32_t n, void* k_pool, void* v_pool,
+                                          void* const* events, void* stream);
+
+/*
  * Cascade decode attention (TensorRT-LLM PR #21738, description, "Solution"):
  * for every row r = b*W + w and query head h,
  *   O[r][h] = softmax(scale * q K^T) V over the beam's logical sequence:

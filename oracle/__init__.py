@@ -82,6 +82,10 @@ def _load():
     lib.orc_append_kv_fp8.restype = ctypes.c_int
     lib.orc_append_kv_fp8.argtypes = [ctypes.c_int] * 6 + [p, p, p, ctypes.c_int64, ctypes.c_float, ctypes.c_float,
                                                           p, p]
+    lib.orc_rope_append_kv_fp8.restype = ctypes.c_int
+    lib.orc_rope_append_kv_fp8.argtypes = ([ctypes.c_int] * 6 + [ctypes.c_double] + [ctypes.c_int] * 4 +
+                                           [p, p, p, ctypes.c_int64, p, p, ctypes.c_int64, ctypes.c_float,
+                                            ctypes.c_float, p, p])
     lib.orc_rope_append_kv.restype = ctypes.c_int
     lib.orc_rope_append_kv.argtypes = ([ctypes.c_int] * 6 + [ctypes.c_double] + [ctypes.c_int] * 4 +
                                        [p, p, p, ctypes.c_int64, p, p, ctypes.c_int64, p, p])
@@ -294,3 +298,26 @@ def append_kv_fp8(*, src_dtype, Hkv, D, ps, num_pages, out_cache_loc, k_new_bits
                                    _ptr(v_pool_bits))
     if rc != 0:
         raise ValueError(f"oracle append_kv_fp8: {ERRORS.get(rc, rc)}")
+
+
+def rope_append_kv_fp8(*, dtype, Hq, Hkv, D, rot, interleaved, base, max_pos, ps, num_pages, positions,
+                       out_cache_loc, q_bits, k_new_bits, v_new_bits, k_pool_bits, v_pool_bits, k_mul=1.0, v_mul=1.0,
+                       q_row_stride=None, row_stride=None):
+    """RoPE on the append into uint8 E4M3 pools, in place (q rows, 16-bit, rotated in place when given)."""
+    pos = _c(positions, np.int32)
+    loc = _c(out_cache_loc, np.int32)
+    n = loc.shape[0]
+    for a in (k_pool_bits, v_pool_bits):
+        assert a.dtype == np.uint8 and a.flags.c_contiguous
+    if q_bits is not None:
+        assert q_bits.dtype == np.uint16 and q_bits.flags.c_contiguous
+    kn = _c(k_new_bits, np.uint16).reshape(n, -1) if n else np.zeros((0, Hkv * D), np.uint16)
+    vn = _c(v_new_bits, np.uint16).reshape(n, -1) if n else np.zeros((0, Hkv * D), np.uint16)
+    rs = kn.shape[1] if row_stride is None else int(row_stride)
+    qrs = 0 if q_bits is None else (q_bits.size // max(n, 1) if q_row_stride is None else int(q_row_stride))
+    rc = _load().orc_rope_append_kv_fp8(
+        DTYPES[dtype], Hq, Hkv, D, int(rot), 1 if interleaved else 0, float(base), int(max_pos), ps, num_pages, n,
+        _ptr(pos), _ptr(loc), None if q_bits is None else _ptr(q_bits), qrs, _ptr(kn), _ptr(vn), rs,
+        float(np.float32(k_mul)), float(np.float32(v_mul)), _ptr(k_pool_bits), _ptr(v_pool_bits))
+    if rc != 0:
+        raise ValueError(f"oracle rope_append_kv_fp8: {ERRORS.get(rc, rc)}")

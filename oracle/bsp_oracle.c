@@ -603,3 +603,57 @@ int orc_append_kv_fp8(int src_dtype, int Hkv, int D, int ps, int num_pages, int 
     }
     return ORC_OK;
 }
+
+/* RoPE on the append into E4M3 pools: the K row is rotated as in orc_rope_append_kv
+ * and its exact rotated value times k_mul rounded once to E4M3 (orc_round_e4m3);
+ * the V row is quantised as in orc_append_kv_fp8 (fp32 product with v_mul); the
+ * query rows, when q is non-NULL, are rotated in place in their 16-bit dtype.
+ * Slots and positions are checked first (nothing written on a bad one). */
+int orc_rope_append_kv_fp8(int dtype, int Hq, int Hkv, int D, int rot, int interleaved, double base, int max_pos,
+                           int ps, int num_pages, int n, const int32_t *pos, const int32_t *loc, uint16_t *q,
+                           int64_t q_row_stride, const uint16_t *knew, const uint16_t *vnew, int64_t row_stride,
+                           float k_mul, float v_mul, uint8_t *kpool, uint8_t *vpool)
+{
+    if (rot < 2 || rot > D || (rot & 1) || !(base > 0.0))
+        return ORC_ERR_ARG;
+    for (int i = 0; i < n; ++i) {
+        if (loc[i] < 0 || (int64_t)loc[i] >= (int64_t)num_pages * ps)
+            return ORC_ERR_INDEX;
+        if (pos[i] < 0 || pos[i] >= max_pos)
+            return ORC_ERR_INDEX;
+    }
+    double *x = malloc(sizeof(double) * (size_t)D), *y = malloc(sizeof(double) * (size_t)D);
+    if (!x || !y) {
+        free(x);
+        free(y);
+        return ORC_ERR_NOMEM;
+    }
+    for (int i = 0; i < n; ++i) {
+        const int64_t page = loc[i] / ps, off = loc[i] % ps;
+        for (int h = 0; h < Hkv; ++h) {
+            const size_t dst = (((size_t)page * Hkv + h) * ps + (size_t)off) * D;
+            const size_t src = (size_t)i * (size_t)row_stride + (size_t)h * D;
+            for (int d = 0; d < D; ++d)
+                x[d] = orc_half_to_double(knew[src + d], dtype);
+            orc_rope_rotate(D, rot, interleaved, base, pos[i], x, y);
+            for (int d = 0; d < D; ++d) {
+                kpool[dst + d] = orc_round_e4m3(y[d] * (double)k_mul);
+                const float vx = (float)orc_half_to_double(vnew[src + d], dtype);
+                const float vy = vx * v_mul;
+                vpool[dst + d] = orc_round_e4m3((double)vy);
+            }
+        }
+        if (q)
+            for (int h = 0; h < Hq; ++h) {
+                uint16_t *row = q + (size_t)i * (size_t)q_row_stride + (size_t)h * D;
+                for (int d = 0; d < D; ++d)
+                    x[d] = orc_half_to_double(row[d], dtype);
+                orc_rope_rotate(D, rot, interleaved, base, pos[i], x, y);
+                for (int d = 0; d < D; ++d)
+                    row[d] = orc_round_half(y[d], dtype);
+            }
+    }
+    free(x);
+    free(y);
+    return ORC_OK;
+}

@@ -213,3 +213,54 @@ def test_rope_append_argument_checks():
     before = pool.clone()
     bsp.rope_append_kv(plan, r, pos[:0], None, k[:0], k[:0], loc[:0], pool, pool)   # n == 0: no-op
     assert torch.equal(before, pool)
+
+
+E4M3 = np.array([oracle.e4m3_to_double(b) for b in range(256)])
+
+
+@pytest.mark.parametrize("dtype,Hkv,D,rot,inter,k_mul,v_mul", [
+    ("bf16", 8, 128, 128, False, 1.0, 1.0),
+    ("fp16", 2, 64, 32, False, 4.0, 0.5),       # partial rotation; large K products saturate
+    ("bf16", 4, 256, 128, True, 0.02, 3.0),
+])
+def test_rope_append_fp8_parity(dtype, Hkv, D, rot, inter, k_mul, v_mul):
+    """K rotated in fp32 and quantised: its E4M3 code lies between the codes of the exact rotation times
+    the multiplier, moved down and up by the fp32 error bound; V bit-exact; q as the 16-bit append."""
+    n, ps, num_pages, max_pos, base = 37, 16, 48, 20000, 1e6
+    Hq = 2 * Hkv
+    g = torch.Generator().manual_seed(D + rot)
+    plan, ws = make_plan(Hq, Hkv, D, ps, num_pages, dtype, n)
+    rope = bsp.Rope(max_pos, rot, base, interleaved=inter)
+    tdt = TDT[dtype]
+    k_new = (torch.randn((n, Hkv * D), generator=g) * 30).to(tdt).cuda()
+    v_new = torch.randn((n, Hkv * D), generator=g).to(tdt).cuda()
+    q = torch.randn((n, Hq * D), generator=g).to(tdt).cuda()
+    q0 = synth.bits(q).copy()
+    loc = torch.randperm(num_pages * ps, generator=g)[:n].to(torch.int32)
+    pos = torch.randint(0, max_pos, (n,), generator=g).to(torch.int32)
+    kp = torch.zeros((num_pages, Hkv, ps, D), dtype=torch.uint8, device="cuda")
+    vp = torch.zeros_like(kp)
+    bsp.rope_append_kv_fp8(plan, rope, pos.cuda(), q, k_new, v_new, loc.cuda(), kp, vp, k_mul=k_mul, v_mul=v_mul)
+    assert bsp.read_device_status(plan) == (0, 0)
+    locn, posn = loc.numpy(), pos.numpy()
+    page, off = locn // ps, locn % ps
+    kb, vb = synth.bits(k_new).reshape(n, -1), synth.bits(v_new).reshape(n, -1)
+    kp_o, vp_o = np.zeros(kp.shape, np.uint8), np.zeros(vp.shape, np.uint8)
+    q_o = q0.copy()
+    oracle.rope_append_kv_fp8(dtype=dtype, Hq=Hq, Hkv=Hkv, D=D, rot=rot, interleaved=inter, base=base,
+                              max_pos=max_pos, ps=ps, num_pages=num_pages, positions=posn, out_cache_loc=locn,
+                              q_bits=q_o, k_new_bits=kb, v_new_bits=vb, k_pool_bits=kp_o, v_pool_bits=vp_o,
+                              k_mul=k_mul, v_mul=v_mul)
+    np.testing.assert_array_equal(vp.cpu().numpy(), vp_o)
+    got = kp.cpu().numpy()[page, :, off].reshape(n * Hkv, D)
+    x = decode(kb.reshape(n * Hkv, D), dtype)
+    v = oracle.rope_rotate_rows(x, np.repeat(posn, Hkv), rot=rot, interleaved=inter, base=base)
+    m = float(np.float32(k_mul))
+    dk = 2.0 ** -21 * pair_bounds(x, rot, inter) * m * 1.001 + np.abs(v * m) * 2.0 ** -23
+    lo = np.vectorize(lambda t: E4M3[oracle.round_e4m3(float(t))])(v * m - dk)
+    hi = np.vectorize(lambda t: E4M3[oracle.round_e4m3(float(t))])(v * m + dk)
+    gv = E4M3[got]
+    assert ((gv >= lo) & (gv <= hi)).all()
+    assert (got == kp_o[page, :, off].reshape(n * Hkv, D)).mean() > 0.99
+    assert_rotated(synth.bits(q).reshape(n * Hq, D), q0.reshape(n * Hq, D), np.repeat(posn, Hq), dtype, rot, inter,
+                   base, "q")

@@ -118,3 +118,39 @@ def test_fp8_source_is_copied_and_bad_slot_writes_nothing():
                              v_new_bits=vb, k_pool_bits=kp2, v_pool_bits=vp2)
     np.testing.assert_array_equal(kp2, kp)
     np.testing.assert_array_equal(vp2, vp)
+
+
+@pytest.mark.parametrize("dtype,inter", [("bf16", False), ("fp16", True)])
+def test_rope_fp8_append_is_the_composition_of_its_pinned_parts(dtype, inter):
+    """K: the exact rotation (oracle.rope_rotate, pinned) times the multiplier, rounded by round_e4m3
+    (pinned); V: the quantising append (pinned); q: the 16-bit RoPE append (pinned)."""
+    rng = np.random.default_rng(31)
+    n, Hq, Hkv, D, ps, npg, rot = 5, 4, 2, 32, 4, 6, 16
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    kb = (torch.randn(n, Hkv * D) * 30).to(tdt).view(torch.int16).numpy().view(np.uint16)
+    vb = torch.randn(n, Hkv * D).to(tdt).view(torch.int16).numpy().view(np.uint16)
+    qb = torch.randn(n, Hq * D).to(tdt).view(torch.int16).numpy().view(np.uint16)
+    loc = rng.choice(npg * ps, n, replace=False).astype(np.int32)
+    pos = rng.integers(0, 3000, n).astype(np.int32)
+    kp = np.zeros((npg, Hkv, ps, D), np.uint8)
+    vp = np.zeros_like(kp)
+    q1 = qb.copy()
+    k_mul, v_mul = 2.5, 0.75
+    oracle.rope_append_kv_fp8(dtype=dtype, Hq=Hq, Hkv=Hkv, D=D, rot=rot, interleaved=inter, base=1e4, max_pos=3000,
+                              ps=ps, num_pages=npg, positions=pos, out_cache_loc=loc, q_bits=q1, k_new_bits=kb,
+                              v_new_bits=vb, k_pool_bits=kp, v_pool_bits=vp, k_mul=k_mul, v_mul=v_mul)
+    vp2 = np.zeros_like(vp)
+    oracle.append_kv_fp8(src_dtype=dtype, Hkv=Hkv, D=D, ps=ps, num_pages=npg, out_cache_loc=loc, k_new_bits=kb,
+                         v_new_bits=vb, k_pool_bits=np.zeros_like(kp), v_pool_bits=vp2, k_mul=1.0, v_mul=v_mul)
+    np.testing.assert_array_equal(vp, vp2)
+    q2 = qb.copy()
+    oracle.rope_append_kv(dtype=dtype, Hq=Hq, Hkv=Hkv, D=D, rot=rot, interleaved=inter, base=1e4, max_pos=3000, ps=ps,
+                          num_pages=npg, positions=pos, out_cache_loc=loc, q_bits=q2, k_new_bits=kb, v_new_bits=vb,
+                          k_pool_bits=np.zeros((npg, Hkv, ps, D), np.uint16), v_pool_bits=np.zeros((npg, Hkv, ps, D), np.uint16))
+    np.testing.assert_array_equal(q1, q2)
+    for i in range(n):
+        for h in range(Hkv):
+            x = np.array([oracle.half_to_double(int(b), dtype) for b in kb[i, h * D:(h + 1) * D]])
+            y = oracle.rope_rotate(x, rot=rot, interleaved=inter, base=1e4, pos=int(pos[i]))
+            want = [oracle.round_e4m3(float(v) * float(np.float32(k_mul))) for v in y]
+            np.testing.assert_array_equal(kp[loc[i] // ps, h, loc[i] % ps], np.array(want, np.uint8))
