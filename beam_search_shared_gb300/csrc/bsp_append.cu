@@ -77,7 +77,7 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
 }
 
 // Append into E4M3 pools (the KV write of a cache kept in fp8: TensorRT-LLM PR #18614, the review
-// follow-up on the fused per-layer KV-cache write: an fp8 source written into an fp8 cache, and the
+// follow-up commit on the fused KV write: an fp8 source written into an fp8 cache, and the
 // source/cache dtype conversion of the fused write). The same warp per (new token, kv head) as the
 // plain append. A 16-bit source element becomes the E4M3 value nearest to its fp32 product with the
 // tensor's multiplier (ties to even, saturating at +-448): a lane converts one 16-byte chunk of 8

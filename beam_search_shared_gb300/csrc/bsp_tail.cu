@@ -2,7 +2,7 @@
 // (TensorRT-LLM PR #21738, "Add opt-in cascade attention for wide beam search
 // on KVCM V2": description, the tail half of the cascade: the tokens a beam
 // generated itself, found through cache_indirection; the commit that fuses the
-// tail runs it and the merge with the prefix result as one launch per layer).
+// tail runs its attention and the join with the prompt part in a single launch per layer).
 //
 // One CTA per beam row r = b*W + w (per row and head pass when the step has
 // fewer rows than SMs). The row's tail positions j = P_b + t

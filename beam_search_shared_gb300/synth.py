@@ -282,7 +282,7 @@ class PrefillWorkload:
 
 
 # The phi4-multimodal shapes of the bucketed-prefix page: a 10368-row allocation per request, an image
-# prompt prefilled from an empty cache, or text after a cached prefix; the 4B-shaped heads of the decode
+# prompt prefilled with nothing cached, or text after a cached prefix; the 4B-shaped heads of the decode
 # workloads (32 q heads, 8 kv heads, head_dim 128, fp16).
 PREFILL_WORKLOADS = {
     "prefill_tiny_d64": PrefillWorkload("prefill_tiny_d64", 2, 4, 2, 64, 16, "bf16", (0, 40), (1, 20)),

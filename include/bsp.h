@@ -79,7 +79,7 @@ enum {
                                CUDA graph once and replayed after every later bsp_plan on the same
                                workspace with the same batch, beam_width, max_tail, geometry, SM count,
                                page-table stride and buffers (the CUDA-graph serving mode: TensorRT-LLM
-                               PR #21738, description: the per-step host plan runs before capture and
+                               PR #21738, description: the host plan of a step is made before capture and
                                before every replay; the tail bound caps the tail under graphs). The
                                prompt kernel runs one CTA per SM of the plan and the tail kernel is
                                always launched for max_tail tail rows; a replay whose staged plan has
@@ -155,8 +155,8 @@ BSP_API const char* bsp_status_string(int32_t status);
 
 /*
  * Rows to bind for a cached prefix of `valid_rows` rows in an allocation of
- * `capacity` rows: rounded up to a 256-row bucket, one (masked) row for an
- * empty cache, capped at the allocation (TensorRT-Model-Connect PR #2202,
+ * `capacity` rows: the next multiple of 256 rows, or a single row when nothing
+ * is cached, at most the allocation (TensorRT-Model-Connect PR #2202,
  * Implementation: kv_cache.{h,cpp}, kCacheRowBucket). The kernels themselves
  * read only the valid rows; this is the bound a caller binds when it needs a
  * shape that changes once per 256 tokens. Returns -1 if capacity < 1.
@@ -225,8 +225,8 @@ BSP_API bsp_status bsp_plan(const bsp_geometry* geo, int32_t batch, int32_t beam
  * registers and writes K and V in the same pass).
  *   k_new, v_new    device [n] rows of num_kv_heads * head_dim contiguous
  *                   elements, rows `src_row_stride` elements apart
- *                   (>= num_kv_heads * head_dim, a multiple of 8) - e.g. a
- *                   column slice of a fused QKV projection
+ *                   (>= num_kv_heads * head_dim, a multiple of 8), so that K
+ *                   and V may be column slices of one projection output
  *   out_cache_loc   device int32 [n] flat slots; a slot outside
  *                   [0, num_pages * page_size) is skipped and flagged
  *   n               0 is a no-op returning BSP_OK; must be <= batch * beam_width
@@ -241,8 +241,8 @@ BSP_API bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, cons
 
 /*
  * Paged append into FP8 E4M3 pools (a KV cache kept in 8 bits; TensorRT-LLM
- * PR #18614, the review follow-up on the fused per-layer KV-cache write: the
- * fp8-source-into-fp8-cache pairing, and the review of msa_scatter.py: the
+ * PR #18614, the review follow-up commit on the fused KV write: the
+ * case of an fp8 source written to an fp8 cache, and the review of msa_scatter.py: the
  * write converts the source dtype to the cache's). Same slots, layout and
  * error behaviour as bsp_append_kv, with pools of one byte per element,
  * uint8 [num_pages][num_kv_heads][page_size][head_dim]:
@@ -331,8 +331,8 @@ BSP_API bsp_status bsp_rope_append_kv(const bsp_plan_t* plan, const bsp_rope_con
 
 /*
  * RoPE on the append into FP8 E4M3 pools (the fused write of the FP8 KV path:
- * TensorRT-LLM PR #18614, the review follow-up on the fused per-layer KV-cache
- * write, whose RoPE kernel emits E4M3 K/V). As bsp_rope_append_kv, except that
+ * TensorRT-LLM PR #18614, the review follow-up commit on the fused KV
+ * write, where the RoPE kernel writes K and V as E4M3). As bsp_rope_append_kv, except that
  * k_pool / v_pool are uint8 E4M3 pools: each rotated K value (fp32, not rounded
  * to 16 bits first) times k_mul and each V value times v_mul, the product
  * rounded to fp32, is stored as the nearest E4M3 value (ties to even,
@@ -354,7 +354,7 @@ BSP_API bsp_status bsp_rope_append_kv_fp8(const bsp_plan_t* plan, const bsp_rope
  *             read through beam_pages[b*W + cache_indirection[b][w][j]];
  *   LSE[r][h] = log-sum-exp of the scaled scores (natural log, or base 2 with
  *             BSP_FLAG_LSE_BASE2); an empty sequence gives O = 0, LSE = -inf.
- * The prompt is attended once per (request, kv head) for all beams and query
+ * Each (request, kv head) reads its prompt keys a single time for all beams and query
  * heads (tensor cores), the tail per beam, and the two merge exactly by
  * log-sum-exp. Only the valid P_b prompt rows are read, never the allocation.
  *   beam_pages_stride  entries per beam_pages row, >= ceil(max(P_b+T_b)/page_size)

@@ -75,8 +75,8 @@ double orc_half_to_double(uint16_t bits, int dtype)
     return sign ? -v : v;
 }
 
-/* Bound cache rows for a valid prefix of `valid` rows: rounded up to a
- * 256-row bucket, one row for an empty cache, capped at the allocation
+/* Bound cache rows for a valid prefix of `valid` rows: the next multiple of
+ * 256 rows, or a single row when nothing is cached, at most the allocation
  * (TensorRT-Model-Connect PR #2202, Implementation: kv_cache.{h,cpp},
  * kCacheRowBucket; Notes For Future Readers). */
 int32_t orc_bucket_rows(int32_t valid, int32_t capacity)

@@ -72,7 +72,7 @@ def test_prefill_empty_requests_and_empty_cache():
 
 
 def test_prefill_image_prompt_from_empty_cache():
-    """An image prompt prefilled from an empty, fully masked cache (the page's case), 2 x 512 tokens."""
+    """Image tokens prefilled with nothing cached (the case the page measures), 2 x 512 tokens."""
     wl = synth.PREFILL_WORKLOADS["prefill_image_b4_s1024"].with_(batch=2, prompt=(512, 512))
     run_and_check(synth.make_prefill_case(wl, 13))
 

@@ -2,8 +2,8 @@
 saturation against the format definition and torch's own float -> float8_e4m3fn conversion, and the
 quantising paged append against a numpy/torch restatement.
 
-The pages ask for the fp8-source-into-fp8-cache pairing and the source/cache dtype conversion of the
-fused KV write (TensorRT-LLM PR #18614, the review follow-up on the fused per-layer KV-cache write and
+The pages ask that an fp8 source can be written to an fp8 cache and that the write converts between the
+fused KV write (TensorRT-LLM PR #18614, the review follow-up commit on the fused KV write and
 the review of msa_scatter.py); the quantisation multiplier and the saturation are the plain readings
 (a per-tensor scale, CUDA's satfinite conversion)."""
 import math
