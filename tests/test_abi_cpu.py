@@ -293,3 +293,30 @@ def test_plan_requests_reads_whole_records(lib):
     np.testing.assert_array_equal(req[:, 1], T)
     np.testing.assert_array_equal(req[:, 5], [1, 0, 1])       # 30 x 8 = 240 tail keys > 128
     np.testing.assert_array_equal(req[:, 10], np.arange(B) * W)
+
+
+def test_decode_plan_layout_is_fixed_by_its_shape(lib):
+    """Graph mode relies on it: decode plans of one shape (batch, beam width, SM count, page-table
+    stride) put every image section at the same offsets whatever the lengths, and the CTA table has
+    num_sms + 1 non-decreasing entries ending at the unit count."""
+    g = geo(Hq=32, Hkv=8, D=128, ps=16, npages=20000, dtype="fp16")
+    B, W, sms, stride = 6, 30, 152, 200
+    rng = np.random.default_rng(3)
+    pages = rng.integers(0, 20000, (B, stride)).astype(np.int32)
+    seen = set()
+    for trial in range(8):
+        P = rng.integers(0, stride * 16 + 1, B).astype(np.int32)
+        if trial == 1:
+            P[:] = 0
+        T = rng.integers(0, 9, B).astype(np.int32)
+        plan, img = bsp.plan_build(g, B, W, P, T, pages, 8, sms)
+        seen.add((plan.off_req, plan.off_units, plan.off_cta, plan.off_pages, plan.off_part_lse, plan.off_part_o,
+                  plan.image_bytes))
+        req, units, pg, cta = decode_image(plan, img, with_cta=True)
+        assert len(cta) == sms + 1 and cta[0] == 0 and cta[-1] == plan.num_units
+        assert (np.diff(cta) >= 0).all()
+    assert len(seen) == 1, seen
+    # a prefill plan is packed: its sections follow the unit count
+    pf1, _ = bsp.plan_prefill_build(g, 2, [0, 0], [10, 300], pages[:2], True, sms)
+    pf2, _ = bsp.plan_prefill_build(g, 2, [0, 0], [600, 900], pages[:2], True, sms)
+    assert pf1.off_cta != pf2.off_cta
