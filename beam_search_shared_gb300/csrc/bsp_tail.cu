@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
         // of the group is loaded in one round; with more splits, the lanes of a head slot load the
         // other partial LSEs in parallel (lane li: splits 1 + li, 1 + li + LPR, ...) and reduce
         // their maximum by shuffles, then the other partial O rows arrive KB splits per round.
-        constexpr int KMAX = (kExtraParts + LPR - 1) / LPR;  // a request has at most 1 + kExtraParts splits
+        constexpr int KMAX = (kExtraParts + LPR - 1) / LPR;  // unrolled loads: up to kExtraParts more splits
         constexpr int KB = 4;
         float lse0[MAXP];
         float4 o0a[MAXP], o0b[MAXP];
@@ -233,6 +233,10 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
                 }
 #pragma unroll
                 for (int k = 0; k < KMAX; ++k) Lmax = fmaxf(Lmax, lsev[k]);
+                // a request may hold more splits when others of the batch have none (the planner's bound
+                // is batch + kExtraParts in all): the rest, one load per lane at a time
+                for (int sp = 1 + KMAX * LPR + li; active && sp < nsplit; sp += LPR)
+                    Lmax = fmaxf(Lmax, ld_dep(p.part_lse + prow + sp * pstride));
 #pragma unroll
                 for (int off = LPR / 2; off >= 1; off >>= 1) Lmax = fmaxf(Lmax, __shfl_xor_sync(FULL, Lmax, off));
             }

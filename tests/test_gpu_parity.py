@@ -257,3 +257,19 @@ def test_full_size_sampled_parity(name):
     pg, off = loc // wl.page_size, loc % wl.page_size
     np.testing.assert_array_equal(synth.bits(step.k_pool[pg, :, off]), kp[pg, :, off])
     np.testing.assert_array_equal(synth.bits(step.v_pool[pg, :, off]), vp[pg, :, off])
+
+
+def test_one_request_with_more_key_splits_than_the_unrolled_merge():
+    """Nine requests without a prompt and one of 73 595 keys on one kv head: the planner gives the long
+    one 72 key splits (its bound is batch + 64 in all), more than the tail kernel's unrolled partial-LSE
+    loads cover; the merge must still take every split into its maximum."""
+    wl = synth.Workload("one_long_request_b10", 10, 1, 8, 1, 128, 32, "bf16", (0, 0), (1, 1))
+    P = [0] * 10
+    P[3] = 1150 * 64 - 5
+    case = synth.make_case(wl, 99, full_step=True, device="cuda", prompt_lengths=P, tail_lengths=[1] * 10)
+    step = DeviceStep(case)
+    step.make_plan()
+    plan, img = bsp.plan_build(step.geo, wl.batch, wl.beam_width, case.prefix_len, case.tail_len,
+                               case.prefix_pages, bsp.MAX_TAIL, step.plan.num_sms)
+    assert bsp.plan_requests(plan, img)[3, 2] > 65
+    run_and_check(case)
