@@ -320,3 +320,32 @@ def test_decode_plan_layout_is_fixed_by_its_shape(lib):
     pf1, _ = bsp.plan_prefill_build(g, 2, [0, 0], [10, 300], pages[:2], True, sms)
     pf2, _ = bsp.plan_prefill_build(g, 2, [0, 0], [600, 900], pages[:2], True, sms)
     assert pf1.off_cta != pf2.off_cta
+
+
+def test_write_side_entry_points_reject_bad_arguments_without_a_launch(lib):
+    """Host checks of the RoPE table, the RoPE append, the E4M3 append and the graph flag, before any
+    launch (no GPU needed: every call below fails on its arguments or on a plan that was never staged)."""
+    import ctypes
+    c = ctypes
+    name = lambda rc: bsp.STATUS_NAMES.get(rc, rc)
+    buf = np.zeros(1024, np.float32)
+    # bsp_rope_cos_sin: positions, rotary dim, base, and a host pointer
+    for args in ((0, 64, 1e4), (16, 63, 1e4), (16, 0, 1e4), (16, 64, 1.0), (16, 64, float("inf")), (16, 64, 1e4)):
+        rc = lib.bsp_rope_cos_sin(args[0], args[1], c.c_double(args[2]), buf.ctypes.data_as(c.c_void_p), None)
+        assert name(rc) == "BSP_ERR_INVALID_ARG", args
+    # an unstaged plan (built on the host only) is refused by every launch entry point
+    g = geo()
+    plan, _ = bsp.plan_build(g, 1, 4, [64], [1], np.zeros((1, 4), np.int32), 8, 152)
+    rope = bsp.RopeConfig(None, 16, 64, 0, 0)
+    rc = lib.bsp_rope_append_kv(c.byref(plan), c.byref(rope), None, None, 0, None, None, 1024, None, 1, None, None,
+                                None, None)
+    assert name(rc) != "BSP_OK"
+    rc = lib.bsp_append_kv_fp8(c.byref(plan), None, None, 1024, 0, c.c_float(1.0), c.c_float(1.0), None, 1, None, None,
+                               None, None)
+    assert name(rc) != "BSP_OK"
+    rc = lib.bsp_rope_append_kv_fp8(c.byref(plan), c.byref(rope), None, None, 0, None, None, 1024, c.c_float(1.0),
+                                    c.c_float(1.0), None, 1, None, None, None, None)
+    assert name(rc) != "BSP_OK"
+    rc = lib.bsp_decode_attn(c.byref(plan), None, None, None, None, 0, None, 0, c.c_float(0.1), bsp.FLAG_GRAPH, None,
+                             None, None, None)
+    assert name(rc) != "BSP_OK"
