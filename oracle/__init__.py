@@ -321,3 +321,25 @@ def rope_append_kv_fp8(*, dtype, Hq, Hkv, D, rot, interleaved, base, max_pos, ps
         float(np.float32(k_mul)), float(np.float32(v_mul)), _ptr(k_pool_bits), _ptr(v_pool_bits))
     if rc != 0:
         raise ValueError(f"oracle rope_append_kv_fp8: {ERRORS.get(rc, rc)}")
+
+
+def e4m3_to_half_bits(pool_bits: np.ndarray, dtype: str) -> np.ndarray:
+    """E4M3 bytes as bits of the 16-bit dtype with the same value: every E4M3 value (3 fraction bits,
+    2^-9 .. 448) is exact in bf16 and in binary16."""
+    table = np.array([round_half(e4m3_to_double(b), dtype) for b in range(256)], np.uint16)
+    return table[np.asarray(pool_bits, np.uint8)]
+
+
+def decode_attn_fp8(*, dtype, B, W, Hq, Hkv, D, ps, num_pages, prefix_len, tail_len, prefix_pages, beam_pages,
+                    cache_indirection, q_bits, k_pool_bits, v_pool_bits, scale, k_scale=1.0, v_scale=1.0, rows=None):
+    """Decode attention over uint8 E4M3 pools dequantised by per-tensor scales (key = E4M3 value x
+    k_scale, value = E4M3 value x v_scale): the unsplit attention over the same keys with the scores
+    scaled by scale x k_scale and O by v_scale (LSE unchanged), the pools carried exactly in the q dtype.
+    Returns (O, LSE) as decode_attn."""
+    kp = e4m3_to_half_bits(k_pool_bits, dtype)
+    vp = e4m3_to_half_bits(v_pool_bits, dtype)
+    O, L = decode_attn(dtype=dtype, B=B, W=W, Hq=Hq, Hkv=Hkv, D=D, ps=ps, num_pages=num_pages,
+                       prefix_len=prefix_len, tail_len=tail_len, prefix_pages=prefix_pages, beam_pages=beam_pages,
+                       cache_indirection=cache_indirection, q_bits=q_bits, k_pool_bits=kp, v_pool_bits=vp,
+                       scale=float(scale) * float(k_scale), rows=rows)
+    return O * float(v_scale), L

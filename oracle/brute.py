@@ -178,3 +178,41 @@ def rope_append_kv(*, dtype, Hq, Hkv, D, rot, interleaved, base, ps, positions, 
                 qv = [half_bits_to_float(v, dtype) for v in q_bits[i][h]]
                 q_bits[i][h] = [nearest_half_bits(v, dtype)
                                 for v in rope_rotate(qv, rot=rot, interleaved=interleaved, base=base, pos=p)]
+
+
+def e4m3_bits_to_float(bits: int) -> float:
+    """Decode one E4M3 byte from its fields: sign, 4 exponent bits (bias 7), 3 fraction bits; exponent 0
+    is subnormal (fraction x 2^-9), the all-ones pattern of exponent and fraction is NaN."""
+    bits &= 0xFF
+    sign = -1.0 if bits & 0x80 else 1.0
+    e, m = (bits >> 3) & 15, bits & 7
+    if e == 15 and m == 7:
+        return math.nan
+    if e == 0:
+        return sign * m * 2.0 ** -9
+    return sign * (1 + m / 8) * 2.0 ** (e - 7)
+
+
+def decode_attn_fp8(*, dtype, B, W, Hq, Hkv, D, ps, prefix_len, tail_len, prefix_pages, beam_pages,
+                    cache_indirection, q_bits, k_pool_bits, v_pool_bits, scale, k_scale, v_scale):
+    """Decode attention over E4M3 pools: every key is its E4M3 value times k_scale and every value row
+    its E4M3 values times v_scale (the dequantisation of a per-tensor-scaled fp8 cache); q in dtype."""
+    G = Hq // Hkv
+    O, L = [], []
+    for b in range(B):
+        for w in range(W):
+            r = b * W + w
+            seq = logical_sequence(b, w, W=W, ps=ps, prefix_len=prefix_len, tail_len=tail_len,
+                                   prefix_pages=prefix_pages, beam_pages=beam_pages, ci=cache_indirection)
+            row_o, row_l = [], []
+            for h in range(Hq):
+                g = h // G
+                q = [half_bits_to_float(x, dtype) for x in q_bits[r][h]]
+                keys = [[e4m3_bits_to_float(x) * k_scale for x in k_pool_bits[p][g][s]] for p, s in seq]
+                vals = [[e4m3_bits_to_float(x) * v_scale for x in v_pool_bits[p][g][s]] for p, s in seq]
+                o, lse = attend(q, keys, vals, scale)
+                row_o.append(o)
+                row_l.append(lse)
+            O.append(row_o)
+            L.append(row_l)
+    return O, L

@@ -154,3 +154,47 @@ def test_rope_fp8_append_is_the_composition_of_its_pinned_parts(dtype, inter):
             y = oracle.rope_rotate(x, rot=rot, interleaved=inter, base=1e4, pos=int(pos[i]))
             want = [oracle.round_e4m3(float(v) * float(np.float32(k_mul))) for v in y]
             np.testing.assert_array_equal(kp[loc[i] // ps, h, loc[i] % ps], np.array(want, np.uint8))
+
+
+def test_e4m3_values_are_exact_in_both_16bit_formats():
+    for dtype in ("bf16", "fp16"):
+        bits = oracle.e4m3_to_half_bits(np.arange(256, dtype=np.uint8), dtype)
+        for b in range(256):
+            v = oracle.e4m3_to_double(b)
+            h = oracle.half_to_double(int(bits[b]), dtype)
+            assert (math.isnan(v) and math.isnan(h)) or v == h, (dtype, b)
+    # the field decoder of the brute force agrees with the oracle's decoder
+    from oracle import brute
+    for b in range(256):
+        v, w = oracle.e4m3_to_double(b), brute.e4m3_bits_to_float(b)
+        assert (math.isnan(v) and math.isnan(w)) or v == w
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_decode_attention_over_e4m3_pools_matches_brute_force(dtype):
+    """The C oracle through exact 16-bit carriers against the nested-list restatement that scales each
+    decoded key and value itself; tiny paged cases with prompts, tails and the indirection."""
+    from oracle import brute
+    from beam_search_shared_gb300 import synth
+    rng = np.random.default_rng(41)
+    for seed, (k_scale, v_scale) in enumerate([(1.0, 1.0), (0.0625, 3.0), (0.3, 0.02)]):
+        wl = synth.WORKLOADS["tiny_b1_w4_d64"].with_(batch=2, prompt=(5, 40), tail=(0, 3), page_size=8,
+                                                       num_q_heads=4, num_kv_heads=2, head_dim=16, dtype=dtype)
+        case = synth.make_case(wl, 300 + seed, full_step=False, device="cpu")
+        k8 = rng.integers(0, 256, case.k_pool.shape).astype(np.uint8)
+        v8 = rng.integers(0, 256, case.v_pool.shape).astype(np.uint8)
+        k8[(k8 & 0x7F) == 0x7F] = 0x38     # no NaN patterns
+        v8[(v8 & 0x7F) == 0x7F] = 0x38
+        kw = dict(dtype=dtype, B=wl.batch, W=wl.beam_width, Hq=wl.num_q_heads, Hkv=wl.num_kv_heads, D=wl.head_dim,
+                  ps=wl.page_size, prefix_len=case.prefix_len, tail_len=case.tail_len, prefix_pages=case.prefix_pages,
+                  beam_pages=case.beam_pages, cache_indirection=case.cache_indirection, scale=0.25)
+        q = synth.bits(case.q)
+        O, L = oracle.decode_attn_fp8(num_pages=case.num_pages, q_bits=q, k_pool_bits=k8, v_pool_bits=v8,
+                                      k_scale=k_scale, v_scale=v_scale, **kw)
+        Ob, Lb = brute.decode_attn_fp8(q_bits=q.tolist(), k_pool_bits=k8.tolist(), v_pool_bits=v8.tolist(),
+                                       k_scale=k_scale, v_scale=v_scale, **kw)
+        np.testing.assert_allclose(O, np.array(Ob), rtol=1e-9, atol=1e-12)
+        Lb = np.array(Lb)
+        np.testing.assert_array_equal(np.isneginf(L), np.isneginf(Lb))
+        fin = ~np.isneginf(L)
+        np.testing.assert_allclose(L[fin], Lb[fin], rtol=1e-9, atol=1e-9)
