@@ -349,3 +349,43 @@ def test_write_side_entry_points_reject_bad_arguments_without_a_launch(lib):
     rc = lib.bsp_decode_attn(c.byref(plan), None, None, None, None, 0, None, 0, c.c_float(0.1), bsp.FLAG_GRAPH, None,
                              None, None, None)
     assert name(rc) != "BSP_OK"
+
+
+def test_planner_random_sweep(lib):
+    """Random shapes and lengths: every plan covers each (request, kv head, row block)'s prompt tiles once,
+    its CTA table is a monotone partition of the units over at most num_sms CTAs, the fused flags follow
+    the rule, each CTA's units are longest first, and no CTA's dealt cost exceeds the LPT bound of the
+    same units (the dealing only improves on LPT)."""
+    rng = np.random.default_rng(2024)
+    for trial in range(120):
+        D = int(rng.choice([64, 128, 256]))
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        G = int(rng.choice([1, 2, 4, 8]))
+        ps = int(rng.choice([8, 16, 32, 64]))
+        B = int(rng.integers(1, 40))
+        W = int(rng.integers(1, 100))
+        sms = int(rng.choice([8, 37, 148, 152]))
+        P = rng.integers(0, 3000, B)
+        P[rng.random(B) < 0.2] = 0
+        T = rng.integers(0, 9, B)
+        maxp = max(1, int(-(-P.max() // ps)))
+        pages = rng.integers(0, 100000, (B, maxp)).astype(np.int32)
+        g = bsp.geometry(G * Hkv, Hkv, D, ps, 100000, "bf16")
+        plan, img = bsp.plan_build(g, B, W, P, T, pages, 8, sms)
+        req, units, pl, cta = decode_image(plan, img, with_cta=True)
+        check_units_cover(plan, req, units, P)
+        check_fused(plan, req, T, head_dim=D)
+        assert len(cta) == sms + 1 and cta[0] == 0 and cta[-1] == plan.num_units and (np.diff(cta) >= 0).all()
+        assert plan.prefix_ctas <= sms
+        cost = units[:, 6].astype(np.int64)
+        loads = [int(cost[cta[c]:cta[c + 1]].sum()) for c in range(sms)]
+        for c in range(sms):
+            seg = cost[cta[c]:cta[c + 1]]
+            assert (np.diff(seg) <= 0).all()                   # longest first within a CTA
+        # LPT on the same costs (longest first, each to the least-loaded CTA) bounds the largest load
+        heap = [0] * min(len(cost), sms)
+        for x in sorted(cost, reverse=True):
+            i = int(np.argmin(heap))
+            heap[i] += int(x)
+        if len(cost):
+            assert max(loads) <= max(heap), (trial, max(loads), max(heap))
