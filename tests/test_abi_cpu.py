@@ -389,3 +389,40 @@ def test_planner_random_sweep(lib):
             heap[i] += int(x)
         if len(cost):
             assert max(loads) <= max(heap), (trial, max(loads), max(heap))
+
+
+def test_prefill_planner_random_sweep(lib):
+    """Random prefill batches: one unit per (request, kv head, block of 128 / G prompt tokens) reading
+    plan tiles [0, end) with end the block's last visible key (causal) or the prompt's end, the request
+    records' rows / row offsets / causal bases, and a CTA table partitioning the units."""
+    rng = np.random.default_rng(77)
+    for trial in range(60):
+        Hkv = int(rng.choice([1, 2, 8]))
+        G = int(rng.choice([1, 2, 4, 8]))
+        ps = int(rng.choice([16, 32, 64]))
+        B = int(rng.integers(1, 12))
+        causal = bool(rng.integers(0, 2))
+        C = rng.integers(0, 2000, B)
+        S = rng.integers(0, 700, B)
+        S[rng.random(B) < 0.2] = 0
+        maxp = max(1, int(-(-(C + S).max() // ps)))
+        pages = rng.integers(0, 50000, (B, maxp)).astype(np.int32)
+        g = bsp.geometry(G * Hkv, Hkv, 128, ps, 50000, "bf16")
+        sms = int(rng.choice([16, 152]))
+        plan, img = bsp.plan_prefill_build(g, B, C, S, pages, causal, sms)
+        req, units, pl, cta = decode_image(plan, img, with_cta=True)
+        wblk = max(1, 128 // G)
+        assert plan.kind == 1 and plan.total_rows == S.sum() and plan.beams_per_block == wblk
+        np.testing.assert_array_equal(req[:, 8], S)
+        np.testing.assert_array_equal(req[:, 9], C if causal else -1)
+        np.testing.assert_array_equal(req[:, 10], np.concatenate([[0], np.cumsum(S)[:-1]]))
+        want = set()
+        for b in range(B):
+            for gg in range(Hkv):
+                for rb in range(-(-int(S[b]) // wblk)):
+                    last = min(int(S[b]), (rb + 1) * wblk)
+                    end = -(-(int(C[b]) + last) // 64) if causal else -(-(int(C[b]) + int(S[b])) // 64)
+                    want.add((b, gg, rb, 0, end))
+        got = [tuple(int(x) for x in u[:5]) for u in units]
+        assert len(got) == len(set(got)) and set(got) == want, trial
+        assert cta[0] == 0 and cta[-1] == plan.num_units and (np.diff(cta) >= 0).all()
