@@ -22,3 +22,17 @@ def test_bucket_rows_printed_by_the_pages():
     for valid, capacity, bound in rows:
         assert oracle.bucket_rows(valid, capacity) == bound, (valid, capacity)
         assert bsp.bucket_rows(valid, capacity) == bound, (valid, capacity)
+
+
+def test_tail_bound_printed_by_the_pages(lib=None):
+    import re
+    limits = {}
+    with open(os.path.join(HERE, "golden", "limits.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, v = line.split()
+                limits[k] = int(v)
+    assert bsp.MAX_TAIL == limits["max_tail"]
+    header = open(os.path.join(HERE, "..", "include", "bsp.h")).read()
+    assert int(re.search(r"#define BSP_MAX_TAIL (\d+)", header).group(1)) == limits["max_tail"]
