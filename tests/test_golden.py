@@ -24,7 +24,7 @@ def test_bucket_rows_printed_by_the_pages():
         assert bsp.bucket_rows(valid, capacity) == bound, (valid, capacity)
 
 
-def test_tail_bound_printed_by_the_pages(lib=None):
+def test_tail_bound_printed_by_the_pages():
     import re
     limits = {}
     with open(os.path.join(HERE, "golden", "limits.txt")) as f:
