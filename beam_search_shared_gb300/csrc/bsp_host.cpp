@@ -203,7 +203,7 @@ struct PrefillSpec {
 bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len_in,
                            const int32_t* tail_len_in, const int32_t* prefix_pages, int32_t prefix_pages_stride,
                            int32_t max_tail, int32_t num_sms, void* image, size_t image_bytes, bsp_plan_t* out,
-                           const PrefillSpec* pf) {
+                           const PrefillSpec* pf, bool fixed_layout = true) {
     bsp_status st = check_geometry(geo);
     if (st != BSP_OK) return st;
     if (!out || batch < 0 || beam_width < 1 || num_sms < 1 || prefix_pages_stride < 0) return BSP_ERR_INVALID_ARG;
@@ -499,7 +499,8 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     const int64_t ctas = static_cast<int64_t>(lists.size());
     // a decode plan's CTA table has num_sms + 1 entries (CTAs past `ctas` have no units), so a launch
     // of num_sms CTAs captured in a CUDA graph reads a valid table after any later plan
-    std::vector<int32_t> cta_off(static_cast<size_t>(pf ? ctas : std::max<int64_t>(ctas, num_sms)) + 1, 0);
+    const bool fixed = !pf && fixed_layout;
+    std::vector<int32_t> cta_off(static_cast<size_t>(fixed ? std::max<int64_t>(ctas, num_sms) : ctas) + 1, 0);
     {
         std::vector<Unit> dealt;
         dealt.reserve(units.size());
@@ -515,9 +516,9 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     // stride: every section at an offset that does not depend on the lengths (the unit list sized
     // for the most key splits the planner makes), so the device addresses baked into a captured
     // CUDA graph stay valid for every later plan of the same shape. A prefill plan is packed.
-    const int64_t parts_cap = pf ? parts : static_cast<int64_t>(batch) + kExtraParts;
-    const size_t units_cap = pf ? units.size() : static_cast<size_t>(parts_cap) * Hkv * nrb;
-    const size_t pages_cap = pf ? static_cast<size_t>(total_pages) : static_cast<size_t>(batch) * prefix_pages_stride;
+    const int64_t parts_cap = fixed ? static_cast<int64_t>(batch) + kExtraParts : parts;
+    const size_t units_cap = fixed ? static_cast<size_t>(parts_cap) * Hkv * nrb : units.size();
+    const size_t pages_cap = fixed ? static_cast<size_t>(batch) * prefix_pages_stride : static_cast<size_t>(total_pages);
     if (units.size() > units_cap || static_cast<size_t>(total_pages) > pages_cap) return BSP_ERR_CAPACITY;
     const size_t off_req = kImageHeaderBytes;
     const size_t off_units = off_req + static_cast<size_t>(batch) * kReqFields * 4;
@@ -600,6 +601,21 @@ bsp_status bsp_plan_build(const bsp_geometry* geo, int32_t batch, int32_t beam_w
     return plan_build_core(geo, batch, beam_width, prefix_len, tail_len, prefix_pages, prefix_pages_stride, max_tail,
                            num_sms, image, image_bytes, out, nullptr);
 }
+
+}  // extern "C"
+
+namespace bsp {
+// A decode plan with the packed layout (sections and partial states sized by this plan's own units and
+// splits), for a caller that never replays it from a CUDA graph: the fixed-scratch entry point.
+bsp_status plan_build_packed(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len,
+                             const int32_t* tail_len, const int32_t* prefix_pages, int32_t prefix_pages_stride,
+                             int32_t max_tail, int32_t num_sms, void* image, size_t image_bytes, bsp_plan_t* out) {
+    return plan_build_core(geo, batch, beam_width, prefix_len, tail_len, prefix_pages, prefix_pages_stride, max_tail,
+                           num_sms, image, image_bytes, out, nullptr, false);
+}
+}  // namespace bsp
+
+extern "C" {
 
 bsp_status bsp_plan_prefill_build(const bsp_geometry* geo, int32_t batch, const int32_t* cached_len,
                                   const int32_t* prompt_len, const int32_t* pages, int32_t pages_stride,

@@ -99,6 +99,11 @@ int noalloc_log2(int x) {
 }
 
 }  // namespace
+
+// bsp_host.cpp: a decode plan with the packed layout (no fixed offsets for graph replays)
+bsp_status plan_build_packed(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len,
+                             const int32_t* tail_len, const int32_t* prefix_pages, int32_t prefix_pages_stride,
+                             int32_t max_tail, int32_t num_sms, void* image, size_t image_bytes, bsp_plan_t* out);
 }  // namespace bsp
 
 extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
@@ -118,8 +123,9 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
         return BSP_ERR_CUDA;
 
     bsp_plan_t plan;
-    st = bsp_plan_build(geo, batch, beam_width, prefix_len, tail_len, prefix_pages, prefix_pages_stride, max_tail, sms,
-                        g_noalloc_image, kNoallocImageBytes, &plan);
+    // the packed layout: this entry point is never replayed from a graph, and the scratch is fixed
+    st = bsp::plan_build_packed(geo, batch, beam_width, prefix_len, tail_len, prefix_pages, prefix_pages_stride, max_tail,
+                           sms, g_noalloc_image, kNoallocImageBytes, &plan);
     if (st != BSP_OK) return st;
     if (plan.device_bytes_used > kNoallocScratchBytes) return BSP_ERR_CAPACITY;
     const int64_t R = static_cast<int64_t>(batch) * beam_width;
