@@ -11,14 +11,30 @@
 // allocates nothing and calls no allocating routine.
 //
 // Rules that come with the shared array:
-//  * every GPU that loads libbsp.so holds kNoallocScratchBytes for the life of
-//    the process;
-//  * the first call on each device looks up the array's device address with
-//    that device current, so make that first call before any stream capture;
+//  * the array is part of this translation unit's device module. CUDA loads
+//    modules lazily by default (CUDA_MODULE_LOADING=LAZY): the driver places
+//    the array on a device when the module is first used there, which is the
+//    address lookup below. A caller that gives the rest of the GPU away at
+//    start-up therefore makes one set-up call per device first (batch 0, any
+//    valid geometry: it only looks the array up and returns), before it
+//    allocates its pools. With CUDA_MODULE_LOADING=EAGER the array is placed
+//    when the library's modules load. Either way the device then holds
+//    kNoallocScratchBytes until the process exits;
+//  * every call looks up the array's device address with the caller's device
+//    current (cheap once the module is loaded), so a device reset between
+//    calls leaves no stale address behind;
 //  * every call uses the same array and it keeps the last call's contents:
 //    the status word is cleared by each call, the rest is rewritten before it
 //    is read; calls whose GPU work overlaps (other streams, other host threads)
 //    race on the array, so serialise them;
+//  * a call on a stream that is being captured into a CUDA graph is refused
+//    (BSP_ERR_INVALID_ARG, nothing looked up or enqueued): each call copies its
+//    plan from one shared host array, so a captured copy would replay whatever
+//    a later call left there;
+//  * device-side index errors (a bad cache_indirection value, beam page or
+//    prompt page id) set the status word in the array, which only
+//    BSP_FLAG_CHECK reads back (it synchronises the stream); without that flag
+//    they are not reported;
 //  * steps whose plan and prompt partials exceed the array are rejected with
 //    BSP_ERR_CAPACITY before anything is enqueued.
 #include <cuda.h>
@@ -37,7 +53,6 @@ namespace {
 
 constexpr size_t kNoallocScratchBytes = size_t(BSP_NOALLOC_SCRATCH_MIB) << 20;
 constexpr size_t kNoallocImageBytes = size_t(1) << 20;
-constexpr int kMaxDevices = 64;
 
 // Device scratch shared by every call of bsp_decode_attn_noalloc on a device.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
@@ -46,21 +61,16 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes]
 alignas(64) static uint8_t g_noalloc_image[kNoallocImageBytes];
 
 std::mutex g_noalloc_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
 
-// Address of the device array on the current device, looked up once per device.
+// Address of the device array on the current device. Looked up on every call: the first lookup on a
+// device loads this file's module there (and with it the array); later ones only read the address.
 bsp_status scratch_for_current_device(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BSP_ERR_CUDA;
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-            cudaGetLastError();
-            return BSP_ERR_CUDA;
-        }
-        g_scratch_ptr[dev] = p;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return BSP_ERR_CUDA;
     }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return BSP_OK;
 }
 
@@ -114,6 +124,21 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
     using namespace bsp;
     if (flags & ~(BSP_FLAG_LSE_BASE2 | BSP_FLAG_CHECK)) return BSP_ERR_INVALID_ARG;
     if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BSP_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    {
+        // a captured call would record a copy from the shared host plan array: refused
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        const cudaError_t e = cudaStreamIsCapturing(s, &cs);
+        if (e == cudaErrorStreamCaptureImplicit) {
+            cudaGetLastError();
+            return BSP_ERR_INVALID_ARG;  // the legacy stream while another stream captures
+        }
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return BSP_ERR_CUDA;
+        }
+        if (cs != cudaStreamCaptureStatusNone) return BSP_ERR_INVALID_ARG;
+    }
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
     void* scratch = nullptr;
     bsp_status st = scratch_for_current_device(&scratch);
@@ -139,7 +164,6 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
         if (beam_pages_stride < (plan.max_total_len + geo->page_size - 1) / geo->page_size) return BSP_ERR_INVALID_ARG;
     }
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(scratch);
     // the status word must start at zero; the image and partials are rewritten before use
     if (cudaMemsetAsync(ws, 0, kStatusBytes, s) != cudaSuccess) return BSP_ERR_CUDA;

@@ -440,18 +440,32 @@ BSP_API bsp_status bsp_read_device_status(const bsp_plan_t* plan, void* stream, 
  * keeps its scratch (plan image, status word, prompt partial states) in one
  * fixed device array of BSP_NOALLOC_SCRATCH_MIB MiB compiled into the library.
  * It calls no cudaMalloc, cudaFree or other allocating routine.
- *  - Every GPU that loads libbsp.so holds that array until the process exits.
- *  - The first call on a device looks up the array's device address (with that
- *    device current); make that first call before any stream capture.
+ *  - Set-up: CUDA loads a library's device code lazily by default
+ *    (CUDA_MODULE_LOADING=LAZY), and the array is placed on a device when this
+ *    call first looks it up there. So call it once per device with batch = 0
+ *    (and a valid geometry; nothing else is read) before allocating the KV
+ *    pools: that call only looks the array up, with the device current, and
+ *    returns BSP_OK. (With CUDA_MODULE_LOADING=EAGER the array is placed when
+ *    the library is loaded.) From then on the device holds the array until the
+ *    process exits. Every call looks the address up again, so no address
+ *    outlives a device reset.
  *  - All calls share the array, which keeps the last call's contents; the call
  *    clears the status word itself. Calls whose GPU work overlaps (different
  *    streams or host threads) race on the array: serialise them.
+ *  - A call on a stream that is being captured into a CUDA graph returns
+ *    BSP_ERR_INVALID_ARG before anything is looked up or enqueued: each call
+ *    copies its plan from one shared host array, so a captured copy would
+ *    replay a later call's plan.
+ *  - Indices in device memory (cache_indirection, beam_pages) are checked by
+ *    the kernels as in bsp_decode_attn, and a bad one sets a bit in the array's
+ *    status word; only BSP_FLAG_CHECK (which synchronises the stream) reads it
+ *    back, as BSP_ERR_PAGE_INDEX. Without that flag such errors go unreported.
  *  - A step whose plan image and prompt partials need more than the array is
  *    rejected with BSP_ERR_CAPACITY before anything is enqueued.
  * Inputs, outputs, layouts, flags (BSP_FLAG_LSE_BASE2, BSP_FLAG_CHECK) and
- * errors are those of bsp_plan and bsp_decode_attn; the plan arrays are host
- * memory, every other pointer device memory. The plan image is copied from
- * host memory that is not page-locked.
+ * errors are otherwise those of bsp_plan and bsp_decode_attn; the plan arrays
+ * are host memory, every other pointer device memory. The plan image is copied
+ * from host memory that is not page-locked.
  */
 BSP_API bsp_status bsp_decode_attn_noalloc(const bsp_geometry* geo, int32_t batch, int32_t beam_width,
                                            const int32_t* prefix_len, const int32_t* tail_len,
