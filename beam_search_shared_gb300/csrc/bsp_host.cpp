@@ -266,7 +266,12 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
 
     // ---- work units: (request, kv head, key split, query-row block)
     int nrb, wblk;
-    if (pf) {
+    // all W*G query rows of a (request, kv head) in one unit as two MMA blocks (the wide kernel)
+    const bool wide = !pf && wide_quad_beams(geo->head_dim, beam_width, G) > 0;
+    if (wide) {
+        nrb = 1;
+        wblk = beam_width;
+    } else if (pf) {
         // prompt tokens in blocks of one MMA's rows (dense layout: 128 rows = 128 / G tokens)
         wblk = std::max(1, kRowsPerBlock / G);
         nrb = 0;
@@ -299,10 +304,15 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
         if (parts <= static_cast<int64_t>(batch) + kExtraParts) break;
         chunk *= 2;
     }
-    // a request is finished by the prompt kernel when its prompt is one partial state and its tail keys,
-    // for every row block (W_blk beams), fit one extra key tile
+    // a request is finished by the prompt kernel when its prompt is one partial state and its tail keys fit
+    // the kernel's tail tiles: one extra key tile per row block (W_blk beams), or for a wide unit (all W
+    // beams) up to kWideMaxTailTiles tiles of 128 keys
+    const int tk = prefix_tile_keys(geo->head_dim);
+    auto tail_tiles = [&](int b) -> int64_t {
+        return ceil_div(static_cast<int64_t>(tail_len[b]) * wblk, wide ? 128 : tk);
+    };
     auto fused = [&](int b) -> bool {
-        return nsplit[b] == 1 && static_cast<int64_t>(tail_len[b]) * wblk <= prefix_tile_keys(geo->head_dim);
+        return nsplit[b] == 1 && tail_tiles(b) <= (wide ? kWideMaxTailTiles : 1);
     };
     // the plan tiles a unit reads: a causal prefill block stops at its last token's keys
     auto unit_end_tile = [&](int b, int rb, int32_t t1) -> int32_t {
@@ -314,12 +324,11 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
         int32_t f[kUnitFields];
     };
     // time of a unit on the prompt kernel, in eighths of a key tile: its TK-key tiles (the last one
-    // partial, costed in full), its tail tile, and half a tile for the unit's start and end
-    const int tk = prefix_tile_keys(geo->head_dim);
+    // partial, costed in full), its tail tiles, and half a tile for the unit's start and end
     auto unit_cost = [&](int b, int32_t t0, int32_t t1) -> int64_t {
         const int64_t keys = std::min<int64_t>(static_cast<int64_t>(t1) * kTileKeys, prefix_len[b]) -
                              static_cast<int64_t>(t0) * kTileKeys;
-        const int64_t kt = ceil_div(keys, tk) + ((fused(b) && tail_len[b] > 0) ? 1 : 0);
+        const int64_t kt = ceil_div(keys, tk) + (fused(b) ? tail_tiles(b) : 0);
         return 8 * kt + 4;
     };
     std::vector<Unit> units;
@@ -579,6 +588,7 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     out->tail_requests = tail_requests;
     out->total_rows = static_cast<int32_t>(total_rows);
     out->kind = pf ? 1 : 0;
+    out->mma_blocks = wide ? 2 : 1;
     out->image_bytes = need;
     // offsets relative to the device workspace
     DeviceLayout L = device_layout(need, parts_cap, beam_width, *geo);
@@ -879,15 +889,12 @@ bsp_status bsp_read_device_status(const bsp_plan_t* plan, void* stream, int32_t 
 
 }  // extern "C"
 
-namespace {
-// The attention launches of a decode step (prefill == false: prompt kernel, then the tail kernel for
-// the requests that need it) or of a prefill (the prompt kernel alone, dense row layout).
-bsp_status attn_impl(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
-                     const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
-                     int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse, void* const* events,
-                     void* stream, bool prefill) {
-    bsp_status st = check_plan(plan);
-    if (st != BSP_OK) return st;
+namespace bsp {
+// Host-checkable arguments of the attention launches of `plan` (prefill == false: a decode plan, else a
+// prefill plan). Nothing is enqueued.
+bsp_status attn_check_args(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
+                           int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse, bool prefill) {
     if (plan->kind != (prefill ? 1 : 0)) return BSP_ERR_INVALID_ARG;
     if (flags & ~(BSP_FLAG_LSE_BASE2 | BSP_FLAG_CHECK | BSP_FLAG_GRAPH)) return BSP_ERR_INVALID_ARG;
     // graph mode: launch shapes that do not depend on the plan's lengths (decode plans only)
@@ -895,8 +902,7 @@ bsp_status attn_impl(const bsp_plan_t* plan, const void* q, const void* k_pool, 
     if (graph && (prefill || (flags & BSP_FLAG_CHECK))) return BSP_ERR_INVALID_ARG;
     if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BSP_ERR_INVALID_ARG;
     const bsp_geometry& geo = plan->geo;
-    const int64_t R = plan->total_rows;
-    if (R == 0) return BSP_OK;
+    if (plan->total_rows == 0) return BSP_OK;
     if (!device_ptr_ok(q) || !device_ptr_ok(k_pool) || !device_ptr_ok(v_pool) || !device_ptr_ok(o) ||
         !device_ptr_ok(lse))
         return BSP_ERR_INVALID_ARG;
@@ -905,24 +911,42 @@ bsp_status attn_impl(const bsp_plan_t* plan, const void* q, const void* k_pool, 
         if (max_seq < plan->max_total_len || max_seq < 1) return BSP_ERR_INVALID_ARG;
         if (beam_pages_stride < ceil_div(plan->max_total_len, geo.page_size)) return BSP_ERR_INVALID_ARG;
     }
+    return BSP_OK;
+}
+
+// The attention launches of a decode step (prefill == false: the prompt kernel, one or two MMA blocks
+// per unit as the plan says, then the tail kernel for the requests that need it) or of a prefill (the
+// prompt kernel alone, dense row layout), for a plan whose status word, image and partial states sit
+// at `ws`. The arguments have passed attn_check_args.
+bsp_status attn_launches(const bsp_plan_t* plan, uint8_t* ws, const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
+                         int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse,
+                         void* const* events, cudaStream_t s, bool prefill) {
+    const bool graph = (flags & BSP_FLAG_GRAPH) != 0;
+    const bsp_geometry& geo = plan->geo;
+    const int64_t R = plan->total_rows;
+    if (R == 0) return BSP_OK;
     const int D = geo.head_dim, Hq = geo.num_q_heads, Hkv = geo.num_kv_heads, G = Hq / Hkv;
     const bool bf16 = geo.dtype == BSP_DTYPE_BF16;
     const float log2e = 1.4426950408889634f;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    uint8_t* ws = static_cast<uint8_t*>(plan->ws_device);
+    const bool wide = plan->mma_blocks == 2;
 
     // everything that is not a launch (attributes, tensor maps, parameters) comes before the
     // first timing event
     const bool prefix = graph || plan->num_units > 0;
-    if (prefix && prepare_prefix(D, bf16) != cudaSuccess) return BSP_ERR_CUDA;
+    if (prefix && (wide ? prepare_wide(D, bf16) : prepare_prefix(D, bf16)) != cudaSuccess) return BSP_ERR_CUDA;
     if (prepare_tail(D, bf16, graph ? plan->max_tail : plan->max_tail_len, Hq) != cudaSuccess) return BSP_ERR_CUDA;
     CUtensorMap tq, tk, tv;
     PrefixParams pp{};
     if (prefix) {
         cuuint64_t qdims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(R)};
         cuuint64_t qstr[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2};
-        // query rows per TMA box: the row block, or a quadrant's share of it (half-row softmax)
-        const int qbeams = prefill ? 0 : prefix_quad_beams(D, plan->beams_per_block, G);
+        // query rows per TMA box: the row block, or a quadrant's share of it (half-row softmax; the wide
+        // layout's quadrants)
+        const int W = plan->beam_width;
+        const int qbeams = wide ? wide_quad_beams(D, W, G)
+                                : (prefill ? 0 : prefix_quad_beams(D, plan->beams_per_block, G));
+        if (wide && qbeams <= 0) return BSP_ERR_INVALID_ARG;
         cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(G),
                               static_cast<cuuint32_t>(qbeams > 0 ? qbeams : plan->beams_per_block)};
         const int ps = geo.page_size;
@@ -949,12 +973,12 @@ bsp_status attn_impl(const bsp_plan_t* plan, const void* q, const void* k_pool, 
         pp.part_o = reinterpret_cast<float*>(ws + plan->off_part_o);
         pp.part_lse = reinterpret_cast<float*>(ws + plan->off_part_lse);
         pp.status = reinterpret_cast<int32_t*>(ws);
-        pp.W = plan->beam_width;
+        pp.W = W;
         pp.Hq = Hq;
         pp.Hkv = Hkv;
         pp.G = G;
         pp.ps_log2 = ilog2(ps);
-        pp.Wblk = plan->beams_per_block;
+        pp.Wblk = wide ? (W + 1) / 2 : plan->beams_per_block;  // beams of one MMA block
         pp.bq = qbeams;
         pp.num_pages = geo.num_pages;
         pp.num_units = graph ? 1 : plan->num_units;  // (graph: launched whatever the captured plan holds)
@@ -994,8 +1018,12 @@ bsp_status attn_impl(const bsp_plan_t* plan, const void* q, const void* k_pool, 
 
     auto record = [&](int i) -> bool { return record_event(events, i, s); };
     if (!record(0)) return BSP_ERR_CUDA;
-    if (prefix && launch_prefix(D, bf16, graph ? plan->num_sms : plan->prefix_ctas, tq, tk, tv, pp, s) != cudaSuccess)
-        return BSP_ERR_CUDA;
+    if (prefix) {
+        const int ctas = graph ? plan->num_sms : plan->prefix_ctas;
+        const cudaError_t e = wide ? launch_wide(D, bf16, ctas, tq, tk, tv, pp, s)
+                                   : launch_prefix(D, bf16, ctas, tq, tk, tv, pp, s);
+        if (e != cudaSuccess) return BSP_ERR_CUDA;
+    }
     if (!record(1)) return BSP_ERR_CUDA;
     // without timing events between them, the tail kernel overlaps the end of the prompt kernel
     if ((graph || plan->tail_requests > 0) &&
@@ -1003,6 +1031,27 @@ bsp_status attn_impl(const bsp_plan_t* plan, const void* q, const void* k_pool, 
             cudaSuccess)
         return BSP_ERR_CUDA;
     if (!record(2)) return BSP_ERR_CUDA;
+    return BSP_OK;
+}
+}  // namespace bsp
+
+namespace {
+// The attention of a staged plan (decode or prefill): argument checks, the launches on the plan's
+// workspace, and with BSP_FLAG_CHECK the device status.
+bsp_status attn_impl(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
+                     const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
+                     int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse, void* const* events,
+                     void* stream, bool prefill) {
+    bsp_status st = check_plan(plan);
+    if (st != BSP_OK) return st;
+    st = attn_check_args(plan, q, k_pool, v_pool, beam_pages, beam_pages_stride, cache_indirection, max_seq,
+                         softmax_scale, flags, o, lse, prefill);
+    if (st != BSP_OK) return st;
+    if (plan->total_rows == 0) return BSP_OK;
+    st = attn_launches(plan, static_cast<uint8_t*>(plan->ws_device), q, k_pool, v_pool, beam_pages, beam_pages_stride,
+                       cache_indirection, max_seq, softmax_scale, flags, o, lse, events,
+                       static_cast<cudaStream_t>(stream), prefill);
+    if (st != BSP_OK) return st;
     if (flags & BSP_FLAG_CHECK) return bsp_read_device_status(plan, stream, 1, nullptr);
     return BSP_OK;
 }

@@ -6,6 +6,8 @@
 
 #include <cstdint>
 
+#include "../../include/bsp.h"
+
 namespace bsp {
 
 // Prompt-attention tiling.
@@ -37,6 +39,21 @@ constexpr int prefix_quad_beams(int head_dim, int beams_per_block, int group) {
     const int bq = (beams_per_block + 3) / 4;
     return (prefix_tile_keys(head_dim) == 128 && bq * group <= 16) ? bq : 0;
 }
+// The wide layout of a decode step (bsp_wide.cu): when a (request, kv head) has more query rows than
+// one MMA holds (W * G in (128, 256]) at head_dim <= 128, one unit holds all of them as two M = 128
+// blocks (beams [0, Wb) and [Wb, W), Wb = ceil(W / 2)) that share every K/V tile, so the prompt is read
+// once. Each block's beams spread over the four TMEM lane quadrants, bq = ceil(Wb / 4) beams (bq * G
+// rows) per quadrant. 0 when the beams do not fit that way.
+constexpr int wide_quad_beams(int head_dim, int beam_width, int group) {
+    const int wb = (beam_width + 1) / 2;
+    const int bq = (wb + 3) / 4;
+    return (head_dim <= 128 && beam_width * group > kRowsPerBlock && beam_width * group <= 2 * kRowsPerBlock &&
+            bq * group <= 32)
+               ? bq
+               : 0;
+}
+// tail tiles of 128 keys a wide unit may gather (the request is finished by the tail kernel beyond)
+constexpr int kWideMaxTailTiles = 4;
 // Per-work-unit record: request, kv head, query-row block, key tiles [kt0, kt1), partial slot, and
 // the cost the host dealt it by (eighths of a prompt-kernel key tile; not read by the kernels).
 enum UnitField { kUnitReq = 0, kUnitKvHead = 1, kUnitRowBlock = 2, kUnitTile0 = 3, kUnitTile1 = 4, kUnitPart = 5,
@@ -111,7 +128,27 @@ cudaError_t prepare_tail(int head_dim, bool bf16, int max_tail_len, int num_q_he
 // prefetches its tail rows, and waits for the prompt kernel's partials before merging).
 cudaError_t launch_tail(int head_dim, bool bf16, int max_tail_len, const TailParams& p, bool after_prefix,
                         cudaStream_t stream);
+// The wide-layout prompt kernel (p.Wblk = beams per block, p.bq = beams per quadrant).
+cudaError_t prepare_wide(int head_dim, bool bf16);
+cudaError_t launch_wide(int head_dim, bool bf16, int ctas, const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv, const PrefixParams& p, cudaStream_t stream);
 cudaError_t prepare_append();
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+
+// bsp_host.cpp: the attention of a plan whose status word, image and partial states sit at `ws`
+// (the caller's workspace, or the fixed scratch of the no-allocation entry point). attn_check_args
+// checks what the host can check and enqueues nothing; attn_launches enqueues the launches.
+bsp_status attn_check_args(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
+                           int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse, bool prefill);
+bsp_status attn_launches(const bsp_plan_t* plan, uint8_t* ws, const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
+                         int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse,
+                         void* const* events, cudaStream_t s, bool prefill);
+// A decode plan with the packed layout (sections and partial states sized by the plan's own units and
+// splits), for a caller that never replays it from a CUDA graph.
+bsp_status plan_build_packed(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len,
+                             const int32_t* tail_len, const int32_t* prefix_pages, int32_t prefix_pages_stride,
+                             int32_t max_tail, int32_t num_sms, void* image, size_t image_bytes, bsp_plan_t* out);
 
 }  // namespace bsp

@@ -74,46 +74,8 @@ bsp_status scratch_for_current_device(void** out) {
     return BSP_OK;
 }
 
-bool noalloc_device_ptr_ok(const void* p) {
-    if (!p || (reinterpret_cast<uintptr_t>(p) & 15u)) return false;
-    cudaPointerAttributes a;
-    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
-}
-
-bool noalloc_encode(CUtensorMap* m, int dtype, int rank, const void* base, const cuuint64_t* dims,
-                    const cuuint64_t* strides, const cuuint32_t* box) {
-    static PFN_cuTensorMapEncodeTiled_v12000 enc = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }();
-    if (!enc) return false;
-    cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, dtype == BSP_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-               static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int noalloc_log2(int x) {
-    int l = 0;
-    while ((1 << l) < x) ++l;
-    return l;
-}
-
 }  // namespace
 
-// bsp_host.cpp: a decode plan with the packed layout (no fixed offsets for graph replays)
-bsp_status plan_build_packed(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len,
-                             const int32_t* tail_len, const int32_t* prefix_pages, int32_t prefix_pages_stride,
-                             int32_t max_tail, int32_t num_sms, void* image, size_t image_bytes, bsp_plan_t* out);
 }  // namespace bsp
 
 extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
@@ -150,102 +112,22 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
     bsp_plan_t plan;
     // the packed layout: this entry point is never replayed from a graph, and the scratch is fixed
     st = bsp::plan_build_packed(geo, batch, beam_width, prefix_len, tail_len, prefix_pages, prefix_pages_stride, max_tail,
-                           sms, g_noalloc_image, kNoallocImageBytes, &plan);
+                                sms, g_noalloc_image, kNoallocImageBytes, &plan);
     if (st != BSP_OK) return st;
     if (plan.device_bytes_used > kNoallocScratchBytes) return BSP_ERR_CAPACITY;
-    const int64_t R = static_cast<int64_t>(batch) * beam_width;
-    if (R == 0) return BSP_OK;
-    if (!noalloc_device_ptr_ok(q) || !noalloc_device_ptr_ok(k_pool) || !noalloc_device_ptr_ok(v_pool) ||
-        !noalloc_device_ptr_ok(o) || !noalloc_device_ptr_ok(lse))
-        return BSP_ERR_INVALID_ARG;
-    if (plan.max_tail_len > 0) {
-        if (!noalloc_device_ptr_ok(beam_pages) || !noalloc_device_ptr_ok(cache_indirection)) return BSP_ERR_INVALID_ARG;
-        if (max_seq < plan.max_total_len || max_seq < 1) return BSP_ERR_INVALID_ARG;
-        if (beam_pages_stride < (plan.max_total_len + geo->page_size - 1) / geo->page_size) return BSP_ERR_INVALID_ARG;
-    }
+    if (plan.total_rows == 0) return BSP_OK;
+    st = attn_check_args(&plan, q, k_pool, v_pool, beam_pages, beam_pages_stride, cache_indirection, max_seq,
+                         softmax_scale, flags, o, lse, false);
+    if (st != BSP_OK) return st;
 
     uint8_t* ws = static_cast<uint8_t*>(scratch);
     // the status word must start at zero; the image and partials are rewritten before use
     if (cudaMemsetAsync(ws, 0, kStatusBytes, s) != cudaSuccess) return BSP_ERR_CUDA;
     if (cudaMemcpyAsync(ws + kStatusBytes, g_noalloc_image, plan.image_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return BSP_ERR_CUDA;
-
-    const int D = geo->head_dim, Hq = geo->num_q_heads, Hkv = geo->num_kv_heads, G = Hq / Hkv;
-    const bool bf16 = geo->dtype == BSP_DTYPE_BF16;
-    const float log2e = 1.4426950408889634f;
-    const int ps = geo->page_size;
-    if (plan.num_units > 0) {
-        CUtensorMap tq, tk, tv;
-        cuuint64_t qdims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(R)};
-        cuuint64_t qstr[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2};
-        // query rows per TMA box: the row block, or a quadrant's share of it (half-row softmax)
-        const int qbeams = prefix_quad_beams(D, plan.beams_per_block, G);
-        cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(G),
-                              static_cast<cuuint32_t>(qbeams > 0 ? qbeams : plan.beams_per_block)};
-        cuuint64_t kdims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(geo->num_pages) * Hkv * ps};
-        cuuint64_t kstr[1] = {static_cast<cuuint64_t>(D) * 2};
-        cuuint32_t kbox[2] = {64, static_cast<cuuint32_t>(ps < kTileKeys ? ps : kTileKeys)};
-        if (!noalloc_encode(&tq, geo->dtype, 3, q, qdims, qstr, qbox) ||
-            !noalloc_encode(&tk, geo->dtype, 2, k_pool, kdims, kstr, kbox) ||
-            !noalloc_encode(&tv, geo->dtype, 2, v_pool, kdims, kstr, kbox))
-            return BSP_ERR_CUDA;
-        PrefixParams pp{};
-        pp.k_pool = k_pool;
-        pp.v_pool = v_pool;
-        pp.beam_pages = beam_pages;
-        pp.ci = cache_indirection;
-        pp.o = o;
-        pp.lse = lse;
-        pp.beam_pages_stride = beam_pages_stride;
-        pp.max_seq = max_seq;
-        pp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
-        pp.units = reinterpret_cast<const int32_t*>(ws + plan.off_units);
-        pp.cta_off = reinterpret_cast<const int32_t*>(ws + plan.off_cta);
-        pp.req = reinterpret_cast<const int32_t*>(ws + plan.off_req);
-        pp.pages = reinterpret_cast<const int32_t*>(ws + plan.off_pages);
-        pp.part_o = reinterpret_cast<float*>(ws + plan.off_part_o);
-        pp.part_lse = reinterpret_cast<float*>(ws + plan.off_part_lse);
-        pp.status = reinterpret_cast<int32_t*>(ws);
-        pp.W = beam_width;
-        pp.Hq = Hq;
-        pp.Hkv = Hkv;
-        pp.G = G;
-        pp.ps_log2 = noalloc_log2(ps);
-        pp.Wblk = plan.beams_per_block;
-        pp.bq = qbeams;
-        pp.num_pages = geo->num_pages;
-        pp.num_units = plan.num_units;
-        pp.scale_log2 = softmax_scale * log2e;
-        if (prepare_prefix(D, bf16) != cudaSuccess ||
-            launch_prefix(D, bf16, plan.prefix_ctas, tq, tk, tv, pp, s) != cudaSuccess)
-            return BSP_ERR_CUDA;
-    }
-    TailParams tp{};
-    tp.q = q;
-    tp.k_pool = k_pool;
-    tp.v_pool = v_pool;
-    tp.beam_pages = beam_pages;
-    tp.ci = cache_indirection;
-    tp.req = reinterpret_cast<const int32_t*>(ws + plan.off_req);
-    tp.part_o = reinterpret_cast<const float*>(ws + plan.off_part_o);
-    tp.part_lse = reinterpret_cast<const float*>(ws + plan.off_part_lse);
-    tp.o = o;
-    tp.lse = lse;
-    tp.status = reinterpret_cast<int32_t*>(ws);
-    tp.B = batch;
-    tp.W = beam_width;
-    tp.Hq = Hq;
-    tp.Hkv = Hkv;
-    tp.G = G;
-    tp.ps_log2 = noalloc_log2(ps);
-    tp.num_pages = geo->num_pages;
-    tp.beam_pages_stride = beam_pages_stride;
-    tp.max_seq = max_seq;
-    tp.scale_log2 = softmax_scale * log2e;
-    tp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
-    if (plan.tail_requests > 0 && (prepare_tail(D, bf16, plan.max_tail_len, Hq) != cudaSuccess ||
-                                   launch_tail(D, bf16, plan.max_tail_len, tp, plan.num_units > 0, s) != cudaSuccess))
-        return BSP_ERR_CUDA;
+    st = attn_launches(&plan, ws, q, k_pool, v_pool, beam_pages, beam_pages_stride, cache_indirection, max_seq,
+                       softmax_scale, flags, o, lse, nullptr, s, false);
+    if (st != BSP_OK) return st;
     if (flags & BSP_FLAG_CHECK) {
         int32_t dflags = 0;
         if (cudaStreamSynchronize(s) != cudaSuccess) return BSP_ERR_CUDA;

@@ -1,0 +1,825 @@
+// Prompt (prefix) attention of the cascade for wide beams, on 5th-generation
+// tensor cores (TensorRT-LLM PR #21738, "Add opt-in cascade attention for wide
+// beam search on KVCM V2", description, Problem and Solution: a request's shared
+// prompt is attended a single time for all of its beams; the workload the
+// method was built for has batch 128, beam 96 and a ~3k-token prompt).
+//
+// When a (request b, kv head g) has more query rows W * G than one MMA holds
+// (128 < W * G <= 256), splitting them into row blocks that run as separate
+// units streams the prompt K/V once per block. Here one CTA holds all of them:
+// two M = 128 blocks, X = A (beams [0, Wb)) and X = B (beams [Wb, W)),
+// Wb = ceil(W / 2), which share every K/V tile in shared memory. Each block's
+// beams are spread over the four TMEM lane quadrants (bq = ceil(Wb / 4) beams,
+// bq * G rows, per quadrant; the rest of a quadrant is zero padding), so the
+// softmax work of a block is even over the four SM sub-partitions.
+//
+// Work unit = (request b, kv head g, key range of the plan's 64-key tiles).
+// Only the valid prompt rows [0, P_b) are read (TensorRT-Model-Connect PR #2202,
+// "prefill and decode over the cached prefix, not the whole KV allocation").
+// A unit the plan marks fused (one key range, at most kWideMaxTailTiles tiles of
+// tail keys) ends with ceil(W * T_b / 128) tail tiles: the tail keys of all W
+// beams, beam-major (key column w * T_b + t is position P_b + t of beam w, read
+// through cache_indirection and that beam's page table); every row keeps only
+// its own beam's columns. Such a unit writes the final O and LSE (the tail
+// attention and the log-sum-exp merge are the same online softmax), other units
+// write fp32 partial states for the tail kernel.
+//
+// Persistent: one CTA per SM walks the units the host dealt it; the K/V rings
+// are indexed by a tile counter that runs across units.
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer: each unit's Q of both blocks (3-D boxes
+//               [bq][G][64], one per quadrant and column half) after the unit's
+//               first K/V tile, and the prompt K/V tiles into a KST-deep K ring
+//               and a VST-deep V ring (one 2-D box of min(page, 64) rows x 64
+//               columns per page slice, column half and tensor). It is the one
+//               waiter on the slot-release barriers, taking every tile's release
+//               in order (a parity wait only names the right phase for a waiter
+//               that is never two phases behind); a tail tile's slots it hands
+//               to warps 10-11 by raising a shared counter;
+//   warp 1      TMEM allocation; one thread issues tcgen05.mma in the order
+//               Q K_t^T -> S_A, Q K_t^T -> S_B, P_A V_t -> O_A, Q K_{t+1}^T -> S_A,
+//               P_B V_t -> O_B, Q K_{t+1}^T -> S_B, ...: while the softmax warps of
+//               one block work on their scores, the tensor core serves the other;
+//   warps 2-5   softmax of block A, warps 6-9 softmax of block B: thread <->
+//               query row <-> TMEM lane; scores read from TMEM twice (row
+//               maximum, then probabilities), online softmax in base 2 with a
+//               lazy rescale of O (only when a row maximum grows by more than
+//               2^8), P written as 16-bit pairs over the first 64 columns of the
+//               block's S; at the end of a unit the same warps normalise O and
+//               write it (final O and LSE, or the fp32 partial state);
+//   warps 10-11 tail tiles: resolve a unit's tail keys one unit ahead (and
+//               bring their rows into L2), then copy K and V rows into the ring
+//               slots with 16-byte cp.async in the 128-byte-swizzled layout a
+//               TMA box would have (absent keys are zero rows), with a key ->
+//               pool-row table per V slot for the softmax's mask.
+// TMEM columns: S_A [0, 128), S_B [128, 256), O_A [256, 256 + D), O_B after it.
+// One S per block: Q K_{t+1}^T into S_X is issued after P_X V_t, and
+// tcgen05.mma instructions of one thread execute in issue order, so P_t (which
+// aliases S_X) is read before it is overwritten; the completion of Q K_{t+1}^T
+// also implies that of P_X V_t, which is what a rescale of O_X needs.
+// Every wait is bounded (1 s without progress); on expiry the CTA flags
+// BSP_DEVFLAG_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "bsp_internal.h"
+#include "bsp_prompt.cuh"
+#include "bsp_ptx.cuh"
+#include "../../include/bsp.h"
+
+namespace bsp {
+namespace {
+
+template <int D>
+struct WideCfg {
+    static constexpr int TK = 128;                          // keys per tile
+    static constexpr int NC = D / 64;                       // 128-byte column regions per row
+    static constexpr int Q_BYTES = kRowsPerBlock * D * 2;   // one block's Q: NC regions of 128 rows x 128 B
+    static constexpr int KV_BYTES = TK * D * 2;             // one K (or V) tile
+    static constexpr int KST = D == 64 ? 5 : 2;             // K ring depth
+    static constexpr int VST = D == 64 ? 6 : 3;             // V ring depth
+    static constexpr int OFF_K = 2 * Q_BYTES;
+    static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
+    static constexpr int OFF_TROW = OFF_V + VST * KV_BYTES;  // int [VST][TK]: pool row of tail key c, -1: none
+    static constexpr int OFF_BAR = OFF_TROW + VST * TK * 4;
+    static constexpr int SMEM = OFF_BAR + 512 + 1024;        // barriers + alignment slack
+    static constexpr int S_COL = 0;                          // S of block X: [X * TK, X * TK + TK)
+    static constexpr int O_COL = 2 * TK;                     // O of block X: [O_COL + X * D, + D)
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int THREADS = 384;
+    static constexpr int GATHER_TID0 = 320;                  // warps 10-11
+    static_assert(O_COL + 2 * D <= 512, "tensor memory");
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(KST <= 8 && VST <= 8, "barrier arrays");
+    static_assert(KST >= 2 && VST >= 2, "ring depth (one slot would stall the next tile's loads)");
+};
+
+struct WideBarriers {
+    uint64_t k_full[8];
+    uint64_t k_empty[8];   // both blocks' Q*K^T of the tile completed
+    uint64_t v_full[8];
+    uint64_t v_empty[8];   // both blocks' P*V of the tile completed
+    uint64_t q_full[2];    // block X's Q of a unit landed
+    uint64_t q_empty[2];   // ... and the unit's last Q*K^T of block X completed
+    uint64_t s_full[2];    // Q*K^T into S_X completed
+    uint64_t p_full[2];    // block X's softmax warps wrote P_X (one arrival per warp)
+    uint64_t o_final[2];   // the last P*V of a unit into O_X completed
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int tail_granted;      // tail tiles whose ring slots the producer has handed to the tail-tile warps
+};
+
+constexpr uint64_t kWideWaitNs = 1000000000ull;  // 1 s without progress
+constexpr uint64_t kWideDrainNs = 200000000ull;
+
+// tail tiles of a unit: the request's W * T tail keys, beam-major, in tiles of 128 keys
+__device__ __forceinline__ int wide_tail_tiles(const UnitInfo& ui) {
+    return (ui.fused && ui.T > 0) ? (ui.rows * ui.T + 127) / 128 : 0;
+}
+
+__device__ __forceinline__ void st_release_shared(int* p, int v) {
+    asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_shared(const int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+// Waits until the shared counter *c exceeds n. Gives up (false) when *abort becomes non-zero or
+// timeout_ns passes.
+__device__ __forceinline__ bool wait_counter(const int* c, int n, const volatile int* abort, uint64_t timeout_ns) {
+    if (ld_acquire_shared(c) > n) return true;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t spins = 0;
+    while (ld_acquire_shared(c) <= n) {
+        if ((++spins & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) return false;
+        }
+    }
+    return true;
+}
+
+// Named barrier 1 over the 64 tail-tile threads, returning the AND of their flags. Every one of them
+// takes part in every call (a flag that is false makes them all stop together).
+__device__ __forceinline__ bool gather_sync_and(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 64, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(ok))
+        : "memory");
+    return r != 0;
+}
+
+}  // namespace
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(384, 1)
+prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const PrefixParams p) {
+    using C = WideCfg<D>;
+    constexpr int TK = C::TK, NC = C::NC, KST = C::KST, VST = C::VST;
+    constexpr unsigned FULL = 0xffffffffu;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    auto q_buf = [&](int x) -> uint8_t* { return smem + x * C::Q_BYTES; };
+    auto k_tile = [&](int gt) -> uint8_t* { return smem + C::OFF_K + (gt % KST) * C::KV_BYTES; };
+    auto v_tile = [&](int gt) -> uint8_t* { return smem + C::OFF_V + (gt % VST) * C::KV_BYTES; };
+    auto trow_of = [&](int gt) -> int* { return reinterpret_cast<int*>(smem + C::OFF_TROW) + (gt % VST) * TK; };
+    WideBarriers* bars = reinterpret_cast<WideBarriers*>(smem + C::OFF_BAR);
+    volatile int* abort_flag = &bars->abort_flag;
+
+    if (p.graph_hdr != nullptr) {
+        // a launch replayed from a CUDA graph: the plan staged since must have the captured shape
+        const int4 h0 = __ldg(reinterpret_cast<const int4*>(p.graph_hdr));
+        const int4 h1 = __ldg(reinterpret_cast<const int4*>(p.graph_hdr) + 1);
+        if (h0.z != p.graph_batch || h1.x != p.W || h1.y != static_cast<int>(gridDim.x) || h1.z != 0) {
+            if (threadIdx.x == 0) atomicOr(p.status, BSP_DEVFLAG_GRAPH);
+            return;
+        }
+    }
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int u_begin = __ldg(p.cta_off + blockIdx.x);
+    const int u_end = __ldg(p.cta_off + blockIdx.x + 1);
+    const int nunits = u_end - u_begin;
+    const int ps = 1 << p.ps_log2;
+    const int qrows = p.bq * p.G;  // rows a quadrant's TMA box fills
+
+    // ---- setup
+    if (tid == 0) {
+        for (int s = 0; s < KST; ++s) {
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->k_empty[s], 1);
+        }
+        for (int s = 0; s < VST; ++s) {
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->v_empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->q_full[i], 1);
+            mbar_init(&bars->q_empty[i], 1);
+            mbar_init(&bars->s_full[i], 1);
+            mbar_init(&bars->p_full[i], 4);  // one arrival per softmax warp of the block
+            mbar_init(&bars->o_final[i], 1);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort_flag = 0;
+        bars->tail_granted = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    if (warp == 1) tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
+    // zero the query rows no TMA box covers (rows bq * G .. 31 of each quadrant of both blocks), so
+    // padded rows stay finite
+    {
+        constexpr int NCHUNK = 2 * NC * kRowsPerBlock * 8;  // 16-byte chunks of the two Q buffers
+        for (int idx = tid; idx < NCHUNK; idx += C::THREADS) {
+            const int r = (idx >> 3) & (kRowsPerBlock - 1);
+            if ((r & 31) >= qrows) reinterpret_cast<uint4*>(smem)[idx] = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    // every CTA of this grid is resident: a dependent launch (the tail kernel) may start on the
+    // SMs this grid leaves; it waits for this grid's completion before reading the partials
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        const int BR = ps < kTileKeys ? ps : kTileKeys;  // rows per box (a page, or 64 rows of a larger page)
+        int gt = 0, k = 0, ntail = 0;
+        bool ok = true;
+        for (int u = u_begin; u < u_end && ok; ++u, ++k) {
+            const UnitInfo ui = load_unit(p, u);
+            const int ptiles = prompt_tiles<TK>(ui);
+            const int ntiles = ptiles + wide_tail_tiles(ui);
+            const int* pg = p.pages + ui.page_off;
+            const int npages = (ui.P + ps - 1) >> p.ps_log2;
+            int win_base = -1, my_page = 0;
+            for (int t = 0; t < ntiles; ++t, ++gt) {
+                // this warp is the only waiter on the slot-release barriers and takes every tile's
+                // release in order, so each parity wait names the phase it means
+                if (gt >= KST) {
+                    ok = mbar_wait(&bars->k_empty[gt % KST], ((gt / KST) - 1) & 1, abort_flag, kWideWaitNs);
+                    ok = __all_sync(FULL, ok);
+                    if (!ok) break;
+                }
+                if (t >= ptiles) {
+                    // a tail tile: once its V slot is free too, hand both slots to the tail-tile warps
+                    // (a counter, not a barrier phase: they may lag several tail tiles behind)
+                    if (gt >= VST) {
+                        ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kWideWaitNs);
+                        ok = __all_sync(FULL, ok);
+                        if (!ok) break;
+                    }
+                    ++ntail;
+                    if (lane == 0) st_release_shared(&bars->tail_granted, ntail);
+                    __syncwarp();
+                    continue;
+                }
+                const int key0 = ui.key_begin + t * TK;
+                const int valid = min(TK, ui.key_end - key0);
+                const int nchunks = (valid + BR - 1) / BR;  // pages (or 64-row slices) with valid keys
+                const int tile_bytes = nchunks * BR * D * 2;
+                const int pidx0 = key0 >> p.ps_log2;
+                const int pidx_last = (key0 + (nchunks - 1) * BR) >> p.ps_log2;
+                if (win_base < 0 || pidx_last >= win_base + 32) {  // warp-uniform
+                    win_base = pidx0;
+                    my_page = (win_base + lane < npages) ? __ldg(pg + win_base + lane) : 0;
+                }
+                const int nbox = nchunks * NC;  // box b of a tensor: column half b % NC of chunk b / NC
+                for (int tensor = 0; tensor < 2; ++tensor) {
+                    if (tensor == 1 && gt >= VST) {
+                        ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kWideWaitNs);
+                        ok = __all_sync(FULL, ok);
+                        if (!ok) break;
+                    }
+                    uint64_t* full = tensor == 0 ? &bars->k_full[gt % KST] : &bars->v_full[gt % VST];
+                    uint8_t* base = tensor == 0 ? k_tile(gt) : v_tile(gt);
+                    const CUtensorMap* map = tensor == 0 ? &tm_k : &tm_v;
+                    if (lane == 0) mbar_arrive_expect_tx(full, tile_bytes);
+                    for (int b0 = 0; b0 < nbox; b0 += 32) {
+                        const int bx = b0 + lane;
+                        const int ch = min(bx / NC, nchunks - 1);
+                        const int key = key0 + ch * BR;
+                        int page = __shfl_sync(FULL, my_page, (key >> p.ps_log2) - win_base);
+                        if (bx < nbox) {
+                            if (static_cast<unsigned>(page) >= static_cast<unsigned>(p.num_pages)) {
+                                atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
+                                page = 0;
+                            }
+                            const int c = bx % NC;
+                            const int row = ((page * p.Hkv + ui.g) << p.ps_log2) + (key & (ps - 1));
+                            tma_load_2d(base + c * TK * 128 + ch * BR * 128, map, full, c * 64, row);
+                        }
+                    }
+                }
+                if (!ok) break;
+                if (t == 0) {
+                    // the unit's Q of both blocks, once the previous unit's last Q*K^T of the block is done
+                    // (issued after this unit's first K/V tile, which may already stream meanwhile)
+                    for (int x = 0; x < 2 && ok; ++x) {
+                        if (k >= 1) {
+                            ok = mbar_wait(&bars->q_empty[x], (k - 1) & 1, abort_flag, kWideWaitNs);
+                            ok = __all_sync(FULL, ok);
+                            if (!ok) break;
+                        }
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(&bars->q_full[x], NC * 4 * qrows * 128);
+                            for (int c = 0; c < NC; ++c)
+                                for (int i = 0; i < 4; ++i)
+                                    tma_load_3d(q_buf(x) + c * (kRowsPerBlock * 128) + i * 32 * 128, &tm_q,
+                                                &bars->q_full[x], c * 64, ui.g * p.G,
+                                                ui.row_off + x * p.Wblk + i * p.bq);
+                        }
+                    }
+                    if (!ok) break;
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok) {
+            if (lane == 0) {
+                *abort_flag = 1;
+                atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+            }
+            // drain: let this CTA's own copies land before the CTA exits
+            const uint64_t t0 = globaltimer_ns();
+            for (int j = max(0, gt - KST); j <= gt; ++j)
+                while (!mbar_try_wait(&bars->k_full[j % KST], (j / KST) & 1) && globaltimer_ns() - t0 < kWideDrainNs) {
+                }
+            for (int j = max(0, gt - VST); j <= gt; ++j)
+                while (!mbar_try_wait(&bars->v_full[j % VST], (j / VST) & 1) && globaltimer_ns() - t0 < kWideDrainNs) {
+                }
+            for (int x = 0; x < 2; ++x)
+                while (!mbar_try_wait(&bars->q_full[x], k & 1) && globaltimer_ns() - t0 < kWideDrainNs) {
+                }
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            constexpr uint32_t ID_QK = idesc_f16(kRowsPerBlock, TK, BF16, false);
+            constexpr uint32_t ID_PV = idesc_f16(kRowsPerBlock, D, BF16, true);
+            int gt = 0, k = 0;
+            int pend = -1;  // tile whose P*V is not issued yet
+            bool pend_first = false, pend_last = false;
+            bool ok = true;
+            auto issue_pv = [&](int x, int j, bool first, bool last) -> bool {
+                if (!mbar_wait(&bars->p_full[x], j & 1, abort_flag, kWideWaitNs)) return false;
+                if (x == 0 && !mbar_wait(&bars->v_full[j % VST], (j / VST) & 1, abort_flag, kWideWaitNs)) return false;
+                tc_fence_after();
+                const uint32_t p_tmem = tmem + C::S_COL + x * TK;
+                const uint32_t o_tmem = tmem + C::O_COL + x * D;
+                const uint32_t v_addr = smem_u32(v_tile(j));
+#pragma unroll
+                for (int kk = 0; kk < TK / 16; ++kk) {
+                    const uint64_t bd = sdesc_sw128(v_addr + kk * 16 * 128, TK * 128, 1024);
+                    mma_f16_tmem_a(o_tmem, p_tmem + kk * 8, bd, ID_PV, (!first || kk > 0) ? 1u : 0u);
+                }
+                if (x == 1) mma_commit(&bars->v_empty[j % VST]);  // both blocks' P*V read V of tile j
+                if (last) mma_commit(&bars->o_final[x]);
+                return true;
+            };
+            for (int u = u_begin; u < u_end && ok; ++u, ++k) {
+                const UnitInfo ui = load_unit(p, u);
+                const int ntiles = prompt_tiles<TK>(ui) + wide_tail_tiles(ui);
+                for (int t = 0; t < ntiles; ++t, ++gt) {
+                    const uint32_t k_addr = smem_u32(k_tile(gt));
+                    for (int x = 0; x < 2; ++x) {
+                        if (pend >= 0) {
+                            ok = issue_pv(x, pend, pend_first, pend_last);
+                            if (!ok) break;
+                        }
+                        if (x == 0) {
+                            ok = mbar_wait(&bars->k_full[gt % KST], (gt / KST) & 1, abort_flag, kWideWaitNs);
+                            if (!ok) break;
+                        }
+                        if (t == 0) {
+                            ok = mbar_wait(&bars->q_full[x], k & 1, abort_flag, kWideWaitNs);
+                            if (!ok) break;
+                        }
+                        // S_X holds P_X of the previous tile, whose P*V was issued just before
+                        tc_fence_after();
+                        const uint32_t q_addr = smem_u32(q_buf(x));
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t ad =
+                                sdesc_sw128(q_addr + (kk >> 2) * (kRowsPerBlock * 128) + (kk & 3) * 32, 16, 1024);
+                            const uint64_t bd = sdesc_sw128(k_addr + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
+                            mma_f16(tmem + C::S_COL + x * TK, ad, bd, ID_QK, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&bars->s_full[x]);
+                        if (x == 1) mma_commit(&bars->k_empty[gt % KST]);  // both blocks read K of this tile
+                        if (t == ntiles - 1) mma_commit(&bars->q_empty[x]);
+                    }
+                    if (!ok) break;
+                    pend = gt;
+                    pend_first = t == 0;
+                    pend_last = t == ntiles - 1;
+                }
+            }
+            if (ok && pend >= 0) {
+                ok = issue_pv(0, pend, pend_first, pend_last);
+                if (ok) ok = issue_pv(1, pend, pend_first, pend_last);
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+            }
+            // drain: every MMA issued by this thread completes before TMEM is freed
+            mma_commit(&bars->drain);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&bars->drain, 0) && globaltimer_ns() - t0 < kWideDrainNs) {
+            }
+        }
+    } else if (warp < 10) {
+        // ================= softmax warps (block x), then the unit's output =================
+        const int x = (warp - 2) >> 2;
+        const int quad = warp & 3;           // TMEM lane quadrant this warp may access
+        const int wq = lane / p.G;           // beam of the quadrant
+        const int jh = lane - wq * p.G;      // head of the group
+        const int wbl = quad * p.bq + wq;    // beam of the block
+        const int wb = x * p.Wblk + wbl;     // beam of the request
+        const bool row_ok = lane < qrows;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        const uint32_t s_col = lane_base + C::S_COL + x * TK;
+        const uint32_t o_col = lane_base + C::O_COL + x * D;
+        const float sl2 = p.scale_log2;
+        const uint32_t ninf = __float_as_uint(-INFINITY);
+        bool ok = true;
+        int gt = 0;
+        for (int k = 0; k < nunits && ok; ++k) {
+            const UnitInfo cur = load_unit(p, u_begin + k);
+            const int ptiles = prompt_tiles<TK>(cur);
+            const int ntiles = ptiles + wide_tail_tiles(cur);
+            const int nw = min(p.Wblk, cur.rows - x * p.Wblk);  // beams of this block
+            const bool live = row_ok && wbl < nw;
+            // a warp whose rows are all padding skips the arithmetic but keeps the barrier protocol
+            const bool warp_live = quad * p.bq < nw;
+            float m = -INFINITY, l = 0.f;
+            for (int t = 0; t < ntiles; ++t, ++gt) {
+                const bool tail = t >= ptiles;
+                const int valid = tail ? TK : min(TK, cur.key_end - (cur.key_begin + t * TK));
+                ok = mbar_wait(&bars->s_full[x], gt & 1, abort_flag, kWideWaitNs);
+                // a tail tile's key table is complete once its V slot is full
+                if (ok && tail) ok = mbar_wait(&bars->v_full[gt % VST], (gt / VST) & 1, abort_flag, kWideWaitNs);
+                ok = __all_sync(FULL, ok);
+                if (!ok) break;
+                tc_fence_after();
+                if (warp_live) {
+                    // masked keys count as -inf: no part in the maximum, probability exp2(-inf) = 0. A
+                    // partial prompt tile keeps [0, valid); a tail tile keeps the row's own beam's T
+                    // columns (w * T - first column of the tile, T <= 8: at most two 32-bit words) whose
+                    // key is readable
+                    const bool partial = valid < TK || tail;
+                    uint32_t km[TK / 32];
+                    if (partial) {
+                        if (tail) {
+                            uint64_t win = 0;
+                            int wbase = 0;
+                            if (live) {
+                                const int lo = wb * cur.T - (t - ptiles) * TK;
+                                const int c0 = max(lo, 0), c1 = min(lo + cur.T, TK);
+                                wbase = c0 & ~31;
+                                const int* trow = trow_of(gt);
+                                for (int c = c0; c < c1; ++c)
+                                    if (trow[c] >= 0) win |= 1ull << (c - wbase);
+                            }
+#pragma unroll
+                            for (int j = 0; j < TK / 32; ++j)
+                                km[j] = 32 * j == wbase        ? static_cast<uint32_t>(win)
+                                        : 32 * j == wbase + 32 ? static_cast<uint32_t>(win >> 32)
+                                                               : 0u;
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < TK / 32; ++j) {
+                                const int n = min(max(valid - 32 * j, 0), 32);
+                                km[j] = n == 32 ? ~0u : (1u << n) - 1u;
+                            }
+                        }
+                    }
+                    auto mask_pair = [&](int c0, uint32_t& ma, uint32_t& mb) {
+                        ma = c0 == 0 ? km[0] : km[2];
+                        mb = c0 == 0 ? km[1] : km[3];
+                    };
+                    // pass 1: the row maximum of the raw scores, then scaled (the scale is positive)
+                    float mp[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) mp[j] = -INFINITY;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < TK; c0 += 64) {
+                        uint32_t ma = ~0u, mb = ~0u;
+                        if (partial) {
+                            mask_pair(c0, ma, mb);
+                            if (!__any_sync(FULL, (ma | mb) != 0u)) continue;  // no row of the warp keeps one
+                        }
+                        uint32_t sa[32], sb[32];
+                        tmem_ld32(s_col + c0, sa);
+                        tmem_ld32(s_col + c0 + 32, sb);
+                        tmem_wait_ld();
+                        if (partial && __any_sync(FULL, (ma & mb) != ~0u)) {
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) {
+                                sa[c] = (ma >> c) & 1u ? sa[c] : ninf;
+                                sb[c] = (mb >> c) & 1u ? sb[c] : ninf;
+                            }
+                        }
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(sa[c]));
+                            mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(sb[c]));
+                        }
+                    }
+                    const float mxr = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                            fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+                    const float mx = mxr * sl2;
+                    // lazy maximum: keep the old one unless the row maximum grew by more than 2^8
+                    const bool need = t > 0 && mx > m + 8.0f;
+                    const bool rescale = __any_sync(FULL, need);
+                    float alpha = 1.0f;
+                    if (t == 0) {
+                        m = mx;
+                    } else if (need) {
+                        alpha = exp2f(m - mx);
+                        m = mx;
+                        l *= alpha;
+                    }
+                    if (rescale) {
+                        // P_X V of the previous tile has completed (it was issued before the Q*K^T whose
+                        // completion s_full reported), and this tile's P*V waits for p_full
+#pragma unroll 1
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t orr[32];
+                            tmem_ld32(o_col + c0, orr);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                            tmem_st32(o_col + c0, orr);
+                        }
+                    }
+                    // pass 2: probabilities 2^(s * scale_log2 - m) and their sum; P in 16-bit pairs over
+                    // the first 64 columns of S_X, 64 keys per store (P columns [32i, 32i + 32) overwrite
+                    // score columns already read in this pass)
+                    const float nm = -m;
+                    float rsp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                    for (int c0 = 0; c0 < TK; c0 += 64) {
+                        uint32_t ma = ~0u, mb = ~0u;
+                        if (partial) mask_pair(c0, ma, mb);
+                        uint32_t pk[32];
+                        if (partial && !__any_sync(FULL, (ma | mb) != 0u)) {
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) pk[c] = 0u;
+                            tmem_st32(s_col + (c0 >> 1), pk);
+                            continue;
+                        }
+                        uint32_t sa[32], sb[32];
+                        tmem_ld32(s_col + c0, sa);
+                        tmem_ld32(s_col + c0 + 32, sb);
+                        tmem_wait_ld();
+                        if (partial && __any_sync(FULL, (ma & mb) != ~0u)) {
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) {
+                                sa[c] = (ma >> c) & 1u ? sa[c] : ninf;
+                                sb[c] = (mb >> c) & 1u ? sb[c] : ninf;
+                            }
+                        }
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            const float p0 = exp2f(fmaf(__uint_as_float(sa[c]), sl2, nm));
+                            const float p1 = exp2f(fmaf(__uint_as_float(sa[c + 1]), sl2, nm));
+                            const float p2 = exp2f(fmaf(__uint_as_float(sb[c]), sl2, nm));
+                            const float p3 = exp2f(fmaf(__uint_as_float(sb[c + 1]), sl2, nm));
+                            rsp[(c >> 1) & 1] += p0 + p1;
+                            rsp[2 + ((c >> 1) & 1)] += p2 + p3;
+                            pk[c >> 1] = pack2<BF16>(p0, p1);
+                            pk[16 + (c >> 1)] = pack2<BF16>(p2, p3);
+                        }
+                        tmem_st32(s_col + (c0 >> 1), pk);
+                    }
+                    tmem_wait_st();
+                    l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
+                }
+                if (x == 0 && !tail && valid < TK) {
+                    // a unit's last prompt tile: zero V rows past the valid keys (stale or garbage rows
+                    // times P = 0 must not produce NaN); block A's warps, before block A's P*V, which the
+                    // tensor core issues before block B's
+                    ok = mbar_wait(&bars->v_full[gt % VST], (gt / VST) & 1, abort_flag, kWideWaitNs);
+                    ok = __all_sync(FULL, ok);
+                    if (!ok) break;
+                    uint8_t* sV = v_tile(gt);
+                    const int nzc = (TK - valid) * 8;  // 16-byte chunks per column half
+                    for (int c = 0; c < NC; ++c)
+                        for (int idx = tid - 64; idx < nzc; idx += 128)
+                            reinterpret_cast<uint4*>(sV + c * TK * 128 + valid * 128)[idx] = make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->p_full[x]);
+            }
+            if (!ok) break;
+            // ---- the unit's output: O_X once its last P*V has completed. The next unit's first P*V
+            // (which overwrites O_X) waits for this warp's next p_full arrival, after these reads.
+            ok = mbar_wait(&bars->o_final[x], k & 1, abort_flag, kWideWaitNs);
+            ok = __all_sync(FULL, ok);
+            if (!ok) break;
+            tc_fence_after();
+            if (warp_live) {
+                const float inv = 1.0f / l;
+                if (cur.fused) {
+                    // the request's whole key set went through this unit: the final O (q dtype) and LSE
+                    const long long rh = (static_cast<long long>(cur.row_off) + wb) * p.Hq + cur.g * p.G + jh;
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + rh * D);
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t orr[32];
+                        tmem_ld32(o_col + c0, orr);
+                        tmem_wait_ld();
+                        if (live) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float* f = reinterpret_cast<const float*>(orr) + 8 * e;
+                                dst[(c0 >> 3) + e] = make_uint4(pack2<BF16>(f[0] * inv, f[1] * inv),
+                                                                pack2<BF16>(f[2] * inv, f[3] * inv),
+                                                                pack2<BF16>(f[4] * inv, f[5] * inv),
+                                                                pack2<BF16>(f[6] * inv, f[7] * inv));
+                            }
+                        }
+                    }
+                    if (live) {
+                        const float lse2 = m + log2f(l);
+                        p.lse[rh] = p.lse_base2 ? lse2 : lse2 * 0.69314718055994530942f;
+                    }
+                } else {
+                    const long long prow = (static_cast<long long>(cur.part) * p.W + wb) * p.Hq + cur.g * p.G + jh;
+                    float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t orr[32];
+                        tmem_ld32(o_col + c0, orr);
+                        tmem_wait_ld();
+                        if (live) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                dst[(c0 >> 2) + e] =
+                                    make_float4(__uint_as_float(orr[4 * e]) * inv, __uint_as_float(orr[4 * e + 1]) * inv,
+                                                __uint_as_float(orr[4 * e + 2]) * inv,
+                                                __uint_as_float(orr[4 * e + 3]) * inv);
+                        }
+                    }
+                    if (live) p.part_lse[prow] = m + log2f(l);
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+        }
+    } else {
+        // ================= tail tiles =================
+        constexpr int CH = D / 8;     // 16-byte chunks of a K or V row
+        constexpr int RPS = 64 / CH;  // rows one pass of the 64 threads covers
+        const int gtid = tid - C::GATHER_TID0;
+        const int kc = gtid % CH;
+        const int rsub = gtid / CH;
+        const uint16_t* k_pool = static_cast<const uint16_t*>(p.k_pool);
+        const uint16_t* v_pool = static_cast<const uint16_t*>(p.v_pool);
+        // pool rows of this thread's two key columns (gtid, gtid + 64) of each tail tile of a unit,
+        // resolved a unit ahead; -1 past the request's tail keys or when unreadable
+        int res[kWideMaxTailTiles][2];
+        auto resolve = [&](const UnitInfo& ui) {
+            const int ntt = wide_tail_tiles(ui);
+#pragma unroll
+            for (int n = 0; n < kWideMaxTailTiles; ++n)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    res[n][h] = -1;
+                    const int cc = n * TK + gtid + 64 * h;
+                    if (n >= ntt || cc >= ui.rows * ui.T) continue;
+                    const int w = cc / ui.T, tt = cc - w * ui.T;
+                    const int pos = ui.P + tt;
+                    const int src = __ldg(p.ci + (static_cast<long long>(ui.b) * p.W + w) * p.max_seq + pos);
+                    int r = -1;
+                    if (static_cast<unsigned>(src) < static_cast<unsigned>(p.W)) {
+                        const int page = __ldg(p.beam_pages +
+                                               (static_cast<long long>(ui.b) * p.W + src) * p.beam_pages_stride +
+                                               (pos >> p.ps_log2));
+                        if (static_cast<unsigned>(page) < static_cast<unsigned>(p.num_pages))
+                            r = ((page * p.Hkv + ui.g) << p.ps_log2) + (pos & (ps - 1));
+                    }
+                    if (r < 0) {
+                        atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
+                    } else {
+                        // the gather runs at the end of the unit: bring the row's K and V into L2 now
+#pragma unroll
+                        for (int off = 0; off < D * 2; off += 128) {
+                            prefetch_l2(static_cast<const uint8_t*>(p.k_pool) + static_cast<long long>(r) * (D * 2) + off);
+                            prefetch_l2(static_cast<const uint8_t*>(p.v_pool) + static_cast<long long>(r) * (D * 2) + off);
+                        }
+                    }
+                    res[n][h] = r;
+                }
+        };
+        bool ok = true;
+        int gt = 0, ntail = 0;
+        UnitInfo cur;
+        if (nunits > 0) {
+            cur = load_unit(p, u_begin);
+            resolve(cur);
+        }
+        for (int k = 0; k < nunits && ok; ++k) {
+            const int ptiles = prompt_tiles<TK>(cur);
+            const int ntt = wide_tail_tiles(cur);
+#pragma unroll
+            for (int n = 0; n < kWideMaxTailTiles; ++n) {
+                if (n >= ntt) break;
+                const int gtt = gt + ptiles + n;
+                // the producer hands the tile's K and V slots over once both blocks' Q*K^T and P*V of
+                // their previous tiles are done
+                ok = wait_counter(&bars->tail_granted, ntail, abort_flag, kWideWaitNs);
+                ++ntail;
+                ok = __all_sync(FULL, ok);
+                int* trow = trow_of(gtt);
+                if (ok) {
+                    trow[gtid] = res[n][0];
+                    trow[gtid + 64] = res[n][1];
+                }
+                ok = gather_sync_and(ok);
+                if (ok) {
+                    uint8_t* kt = k_tile(gtt);
+                    uint8_t* vt = v_tile(gtt);
+#pragma unroll 4
+                    for (int i = 0; i < TK / RPS; ++i) {
+                        const int c = rsub + i * RPS;
+                        const int r = trow[c];
+                        // the layout of a TMA box with 128-byte swizzle: chunk kc of row c in column half kc / 8
+                        const uint32_t off = (kc >> 3) * (TK * 128) + c * 128 + (((kc & 7) ^ (c & 7)) << 4);
+                        const long long e = static_cast<long long>(r < 0 ? 0 : r) * D + kc * 8;
+                        const uint32_t nb = r < 0 ? 0u : 16u;  // absent keys are zero rows
+                        cp_async16(kt + off, k_pool + e, nb);
+                        cp_async16(vt + off, v_pool + e, nb);
+                    }
+                    cp_async_commit_wait_all();
+                    fence_proxy_async_smem();
+                }
+                ok = gather_sync_and(ok);
+                if (!ok) break;
+                if (gtid == 0) {
+                    mbar_arrive(&bars->k_full[gtt % KST]);
+                    mbar_arrive(&bars->v_full[gtt % VST]);
+                }
+            }
+            gt += ptiles + ntt;
+            if (ok && k + 1 < nunits) {
+                cur = load_unit(p, u_begin + k + 1);
+                resolve(cur);
+            }
+        }
+        if (!ok && gtid == 0) {
+            *abort_flag = 1;
+            atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D, bool BF16>
+static cudaError_t prepare_wide_k() {
+    using C = WideCfg<D>;
+    static_assert(sizeof(WideBarriers) <= 512, "barrier block");
+    cudaError_t e =
+        cudaFuncSetAttribute(prefix_wide_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(prefix_wide_kernel<D, BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+}
+
+cudaError_t prepare_wide(int head_dim, bool bf16) {
+    switch (head_dim) {
+        case 64: return bf16 ? prepare_wide_k<64, true>() : prepare_wide_k<64, false>();
+        case 128: return bf16 ? prepare_wide_k<128, true>() : prepare_wide_k<128, false>();
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_wide(int head_dim, bool bf16, int ctas, const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv, const PrefixParams& p, cudaStream_t stream) {
+    if (ctas == 0 || p.num_units == 0) return cudaSuccess;
+    if (p.bq <= 0 || p.bq * p.G > 32) return cudaErrorInvalidValue;
+    switch (head_dim) {
+        case 64:
+            if (bf16) prefix_wide_kernel<64, true><<<ctas, WideCfg<64>::THREADS, WideCfg<64>::SMEM, stream>>>(tq, tk, tv, p);
+            else prefix_wide_kernel<64, false><<<ctas, WideCfg<64>::THREADS, WideCfg<64>::SMEM, stream>>>(tq, tk, tv, p);
+            break;
+        case 128:
+            if (bf16) prefix_wide_kernel<128, true><<<ctas, WideCfg<128>::THREADS, WideCfg<128>::SMEM, stream>>>(tq, tk, tv, p);
+            else prefix_wide_kernel<128, false><<<ctas, WideCfg<128>::THREADS, WideCfg<128>::SMEM, stream>>>(tq, tk, tv, p);
+            break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace bsp

@@ -145,7 +145,9 @@ typedef struct bsp_plan_t {
     int32_t total_rows;          /* query rows of the step: batch * beam_width (decode) or the prompt
                                     tokens of all requests (prefill) */
     int32_t kind;                /* 0: a decode-step plan (bsp_plan); 1: a prefill plan (bsp_plan_prefill) */
-    int32_t reserved1;
+    int32_t mma_blocks;          /* query-row blocks of 128 rows one prompt-kernel unit holds: 2 when a
+                                    (request, kv head) has 129-256 query rows at head_dim <= 128 (all its
+                                    beams in one unit, the prompt read once), else 1 */
     uint64_t off_cta;            /* byte offset of the per-CTA unit table */
     uint64_t reserved;
 } bsp_plan_t;

@@ -115,11 +115,23 @@ def decode_image(plan, img, with_cta=False):
     return req, units, pages
 
 
+def wide_layout(D, W, G):
+    """All W*G query rows of a (request, kv head) in one unit as two 128-row MMA blocks: 128 < W*G <= 256
+    at head_dim <= 128, with each block's beams spread over four 32-lane quadrants."""
+    bq = -(-(-(-W // 2)) // 4)
+    return D <= 128 and 128 < W * G <= 256 and bq * G <= 32
+
+
 def check_fused(plan, req, T, head_dim=128):
-    """A request is finished by the prompt kernel iff it has one prompt partial state and each row
-    block's tail keys fit one prompt-kernel tile (128 keys up to head_dim 128, 64 at 256)."""
-    tile = 128 if head_dim <= 128 else 64
-    want = (req[:, 2] == 1) & (np.asarray(T) * plan.beams_per_block <= tile)
+    """A request is finished by the prompt kernel iff it has one prompt partial state and its tail keys
+    fit the kernel's tail tiles: each row block's in one prompt-kernel tile (128 keys up to head_dim 128,
+    64 at 256), or, for a two-block unit, all W beams' in at most 4 tiles of 128 keys."""
+    T = np.asarray(T)
+    if plan.mma_blocks == 2:
+        want = (req[:, 2] == 1) & (-(-T * plan.beam_width // 128) <= 4)
+    else:
+        tile = 128 if head_dim <= 128 else 64
+        want = (req[:, 2] == 1) & (T * plan.beams_per_block <= tile)
     np.testing.assert_array_equal(req[:, 5], want.astype(np.int32))
     assert plan.tail_requests == int((~want).sum())
 
@@ -188,22 +200,34 @@ def test_plan_image_wide_batch_needs_no_split(lib):
         np.testing.assert_array_equal(pl[req[b][4]:req[b][4] + n], pages[b, :n])
 
 
-def test_plan_image_wide_beam_row_blocks(lib):
+def test_plan_image_wide_beam_one_unit_per_kv_head(lib):
+    """192 query rows per (request, kv head) at head_dim 128: one unit holds both 96-row blocks, so the
+    prompt is read once; up to 4 tiles of 128 tail keys (96 beams x T <= 512) finish in the prompt kernel."""
     B, W = 3, 96
-    P = [3000, 2900, 0]
+    P = [3000, 2900, 0]                       # 16 units on 8 SMs: no key splits
     T = [1, 0, 3]
     pages = np.tile(np.arange(94, dtype=np.int32), (B, 1))
-    plan, img = bsp.plan_build(geo(npages=200), B, W, P, T, pages, 8, 152)
+    plan, img = bsp.plan_build(geo(npages=200), B, W, P, T, pages, 8, 8)
     req, units, _ = decode_image(plan, img)
-    assert plan.row_blocks == 2 and plan.beams_per_block == 48    # 192 rows -> 2 x 96
+    assert plan.mma_blocks == 2 and plan.row_blocks == 1 and plan.beams_per_block == 96
     check_units_cover(plan, req, units, P)
     assert req[2][2] == 0                                            # empty prompt: no split, no unit
     check_fused(plan, req, T)
-    assert req[2][5] == 0 and plan.tail_requests >= 1
-    plan, img = bsp.plan_build(geo(npages=200), B, W, P, [3, 2, 1], pages, 8, 152)
+    assert list(req[:, 5]) == [1, 1, 0] and plan.tail_requests == 1
+    # dealing cost: the prompt tiles and ceil(96 T / 128) tail tiles
+    keys = np.minimum(units[:, 4] * 64, np.asarray(P)[units[:, 0]]) - units[:, 3] * 64
+    want = 8 * (-(-keys // 128) + -(-np.asarray(T)[units[:, 0]] * 96 // 128)) + 4
+    np.testing.assert_array_equal(units[:, 6], want)
+    plan, img = bsp.plan_build(geo(npages=200), B, W, P, [5, 6, 1], pages, 8, 8)
     req, _, _ = decode_image(plan, img)
-    check_fused(plan, req, [3, 2, 1])                                # 48 x 3 tail keys exceed a tile
-    assert req[0][5] == 0
+    check_fused(plan, req, [5, 6, 1])                                # 96 x 6 tail keys exceed 4 tiles
+    assert list(req[:, 5]) == [1, 0, 0]
+    # head_dim 256 keeps two row blocks (two 256-column O accumulators would not fit tensor memory)
+    plan, img = bsp.plan_build(geo(D=256, npages=200), B, W, P, T, pages, 8, 8)
+    req, units, _ = decode_image(plan, img)
+    assert plan.mma_blocks == 1 and plan.row_blocks == 2 and plan.beams_per_block == 48
+    check_units_cover(plan, req, units, P)
+    check_fused(plan, req, T, head_dim=256)
 
 
 def test_plan_image_single_long_request_is_split(lib):
@@ -373,6 +397,9 @@ def test_planner_random_sweep(lib):
         g = bsp.geometry(G * Hkv, Hkv, D, ps, 100000, "bf16")
         plan, img = bsp.plan_build(g, B, W, P, T, pages, 8, sms)
         req, units, pl, cta = decode_image(plan, img, with_cta=True)
+        assert plan.mma_blocks == (2 if wide_layout(D, W, G) else 1)
+        if plan.mma_blocks == 2:
+            assert plan.row_blocks == 1 and plan.beams_per_block == W
         check_units_cover(plan, req, units, P)
         check_fused(plan, req, T, head_dim=D)
         assert len(cta) == sms + 1 and cta[0] == 0 and cta[-1] == plan.num_units and (np.diff(cta) >= 0).all()

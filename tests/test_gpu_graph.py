@@ -25,7 +25,8 @@ def oracle_attn(case, P, T):
         k_pool_bits=synth.bits(case.k_pool), v_pool_bits=synth.bits(case.v_pool), scale=1 / math.sqrt(wl.head_dim))
 
 
-@pytest.mark.parametrize("name,batch", [("qwen3_4b_fp16_d128", 4), ("qwen3_0p6b_b64_w30", 16), ("tiny_b1_w4_d64", 1)])
+@pytest.mark.parametrize("name,batch", [("qwen3_4b_fp16_d128", 4), ("qwen3_0p6b_b64_w30", 16), ("tiny_b1_w4_d64", 1),
+                                        ("wide_beam_b128_w96", 2)])
 def test_graph_replay_after_new_plans(name, batch):
     wl = synth.WORKLOADS[name].scaled(batch)
     case = synth.make_case(wl, 77 + batch, full_step=False, device="cuda")
