@@ -57,7 +57,7 @@ class Plan(ctypes.Structure):
         ("off_units", ctypes.c_uint64), ("off_pages", ctypes.c_uint64), ("off_part_lse", ctypes.c_uint64),
         ("off_part_o", ctypes.c_uint64), ("device_bytes_used", ctypes.c_uint64),
         ("tail_requests", ctypes.c_int32), ("total_rows", ctypes.c_int32), ("kind", ctypes.c_int32),
-        ("mma_blocks", ctypes.c_int32), ("off_cta", ctypes.c_uint64), ("reserved", ctypes.c_uint64)]
+        ("layout", ctypes.c_int32), ("off_cta", ctypes.c_uint64), ("reserved", ctypes.c_uint64)]
 
 
 class RopeConfig(ctypes.Structure):

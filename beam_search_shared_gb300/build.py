@@ -11,7 +11,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbsp.so")
-SOURCES = ["bsp_host.cpp", "bsp_append.cu", "bsp_rope.cu", "bsp_tail.cu", "bsp_prefix.cu", "bsp_wide.cu", "bsp_noalloc.cu"]
+SOURCES = ["bsp_host.cpp", "bsp_append.cu", "bsp_rope.cu", "bsp_tail.cu", "bsp_prefix.cu", "bsp_wide.cu", "bsp_alt.cu", "bsp_noalloc.cu"]
 HEADERS = ["bsp_internal.h", "bsp_ptx.cuh", "bsp_prompt.cuh", "bsp_write.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

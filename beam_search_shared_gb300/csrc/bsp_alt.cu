@@ -1,0 +1,872 @@
+// Prompt (prefix) attention of the cascade on 5th-generation tensor cores, with
+// two softmax warp sets that take alternate key tiles (TensorRT-LLM PR #21738,
+// "Add opt-in cascade attention for wide beam search on KVCM V2", description,
+// Problem and Solution: a request's shared prompt is attended a single time for
+// all of its beams, which makes Q*K^T and P*V dense contractions over the
+// beam_width x GQA-group query rows of a (request, kv head)).
+//
+// Work unit = (request b, kv head g, query-row block rb, key range of the
+// plan's 64-key tiles). A row block is up to 128 query rows (beams
+// [rb * Wb, rb * Wb + Wb) x the G heads of the group); its beams are spread over
+// the four TMEM lane quadrants (bq beams, bq * G <= 32 rows, per quadrant). When
+// a (request, kv head) has more rows than one block holds, the host deals its row
+// blocks to neighbouring CTAs at the same place of their unit lists, so the
+// blocks stream the same K/V tiles at about the same time and the second read
+// of a tile comes from L2. Only the valid prompt rows [0, P_b) are read
+// (TensorRT-Model-Connect PR #2202, "prefill and decode over the cached prefix,
+// not the whole KV allocation").
+//
+// The unit's key tiles (TK = 128 keys) go alternately to softmax set A (even
+// unit-local tiles) and set B (odd), each with its own score buffer S_X and
+// output accumulator O_X in TMEM and its own online-softmax state (m_X, l_X): two
+// independent streams over the unit's keys, so each set has two tiles of tensor
+// work to hide its softmax behind. At the end of the unit the two states merge
+// by log-sum-exp (set B hands its row statistics over in shared memory, set A
+// reads O_A and O_B and writes the result); the split is exact, like the split
+// of the prompt and the tail.
+//
+// A unit the plan marks fused (one key range, at most kAltMaxTailTiles tiles of
+// tail keys) ends with ceil(Wb * T_b / 128) tail tiles: the tail keys of the
+// block's beams, beam-major (key column w_local * T_b + t is position P_b + t of
+// beam rb * Wb + w_local, read through cache_indirection and that beam's page
+// table); each row keeps only its own beam's columns. Such a unit writes the
+// final O and LSE; other units write fp32 partial states for the tail kernel.
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer: each unit's Q (3-D boxes [bq][G][64], one per
+//               quadrant and column half) first, then the prompt K/V tiles into
+//               a KST-deep K ring and a VST-deep V ring (one 2-D box of
+//               min(page, 64) rows x 64 columns per page slice, column half and
+//               tensor). It is the one waiter on the slot-release barriers and
+//               takes every tile's release in order; a tail tile's slots it
+//               hands to warps 10-11 by raising a shared counter;
+//   warp 1      TMEM allocation; one thread issues tcgen05.mma: for tile t of set
+//               X = t % 2, first P_X V of set X's previous tile, then
+//               S_X = Q K_t^T (P_X aliases S_X, and tcgen05.mma instructions of
+//               one thread execute in issue order);
+//   warps 2-5   softmax set A, warps 6-9 softmax set B: thread <-> query row
+//               <-> TMEM lane; scores read from TMEM twice (row maximum, then
+//               probabilities), online softmax in base 2 with a lazy rescale of
+//               O_X (only when a row maximum grows by more than 2^8), P written
+//               as 16-bit pairs over the first 64 columns of S_X;
+//   warps 10-11 tail tiles: resolve a unit's tail keys one unit ahead (and bring
+//               their rows into L2), then copy K and V rows into the ring slots
+//               with 16-byte cp.async in the 128-byte-swizzled layout a TMA box
+//               would have (absent keys are zero rows), with a key -> pool-row
+//               table per V slot for the softmax's mask.
+// TMEM columns: S_A [0, 128), S_B [128, 256), O_A [256, 256 + D), O_B after it.
+// Every wait is bounded (1 s without progress); on expiry the CTA flags
+// BSP_DEVFLAG_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "bsp_internal.h"
+#include "bsp_prompt.cuh"
+#include "bsp_ptx.cuh"
+#include "../../include/bsp.h"
+
+namespace bsp {
+namespace {
+
+template <int D>
+struct AltCfg {
+    static constexpr int TK = 128;                          // keys per tile
+    static constexpr int NC = D / 64;                       // 128-byte column regions per row
+    static constexpr int Q_BYTES = kRowsPerBlock * D * 2;   // NC regions of 128 rows x 128 B
+    static constexpr int KV_BYTES = TK * D * 2;             // one K (or V) tile
+    static constexpr int KST = D == 64 ? 5 : 2;             // K ring depth
+    static constexpr int VST = D == 64 ? 7 : 3;             // V ring depth (a V slot is held longer)
+    static constexpr int OFF_K = Q_BYTES;
+    static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
+    static constexpr int OFF_TROW = OFF_V + VST * KV_BYTES;  // int [VST][TK]: pool row of tail key c, -1: none
+    static constexpr int OFF_STATS = OFF_TROW + VST * TK * 4;  // float m[128], l[128] of set B
+    static constexpr int OFF_BAR = OFF_STATS + 2 * kRowsPerBlock * 4;
+    static constexpr int SMEM = OFF_BAR + 512 + 1024;        // barriers + alignment slack
+    static constexpr int S_COL = 0;                          // S of set X: [X * TK, X * TK + TK)
+    static constexpr int O_COL = 2 * TK;                     // O of set X: [O_COL + X * D, + D)
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int THREADS = 384;
+    static constexpr int GATHER_TID0 = 320;                  // warps 10-11
+    static_assert(O_COL + 2 * D <= 512, "tensor memory");
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(KST <= 8 && VST <= 8, "barrier arrays");
+    static_assert(KST >= 2 && VST >= 2, "ring depth (one slot would stall the next tile's loads)");
+};
+
+struct AltBarriers {
+    uint64_t k_full[8];
+    uint64_t k_empty[8];   // the tile's Q*K^T completed
+    uint64_t v_full[8];
+    uint64_t v_empty[8];   // the tile's P*V completed
+    uint64_t q_full;       // a unit's Q landed
+    uint64_t q_empty;      // ... and the unit's last Q*K^T completed
+    uint64_t s_full[2];    // Q*K^T into S_X completed (one phase per tile of set X)
+    uint64_t p_full[2];    // set X's warps wrote P_X (one arrival per warp)
+    uint64_t o_final[2];   // set X's last P*V of a unit completed (one phase per unit)
+    uint64_t st_full;      // set B's row statistics of a unit written (one arrival per warp)
+    uint64_t o_merged;     // set A has read O_A and O_B of a unit (one arrival per warp)
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int tail_granted;      // tail tiles whose ring slots the producer has handed to the tail-tile warps
+};
+
+constexpr uint64_t kAltWaitNs = 1000000000ull;  // 1 s without progress
+constexpr uint64_t kAltDrainNs = 200000000ull;
+
+// beams of a unit's row block
+__device__ __forceinline__ int alt_block_beams(const UnitInfo& ui, int wblk) {
+    return min(wblk, ui.rows - ui.rb * wblk);
+}
+// tail tiles of a unit: the row block's W_b * T tail keys, beam-major, in tiles of 128 keys
+__device__ __forceinline__ int alt_tail_tiles(const UnitInfo& ui, int wblk) {
+    return (ui.fused && ui.T > 0) ? (alt_block_beams(ui, wblk) * ui.T + 127) / 128 : 0;
+}
+
+__device__ __forceinline__ void alt_st_release(int* p, int v) {
+    asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int alt_ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+// Waits until the shared counter *c exceeds n. Gives up (false) when *abort becomes non-zero or
+// timeout_ns passes.
+__device__ __forceinline__ bool alt_wait_counter(const int* c, int n, const volatile int* abort, uint64_t timeout_ns) {
+    if (alt_ld_acquire(c) > n) return true;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t spins = 0;
+    while (alt_ld_acquire(c) <= n) {
+        if ((++spins & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) return false;
+        }
+    }
+    return true;
+}
+// Named barrier 1 over the 64 tail-tile threads, returning the AND of their flags. Every one of them
+// takes part in every call (a flag that is false makes them all stop together).
+__device__ __forceinline__ bool alt_gather_sync_and(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 64, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(ok))
+        : "memory");
+    return r != 0;
+}
+
+}  // namespace
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(384, 1)
+prefix_alt_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const PrefixParams p) {
+    using C = AltCfg<D>;
+    constexpr int TK = C::TK, NC = C::NC, KST = C::KST, VST = C::VST;
+    constexpr unsigned FULL = 0xffffffffu;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* q_buf = smem;
+    auto k_tile = [&](int gt) -> uint8_t* { return smem + C::OFF_K + (gt % KST) * C::KV_BYTES; };
+    auto v_tile = [&](int gt) -> uint8_t* { return smem + C::OFF_V + (gt % VST) * C::KV_BYTES; };
+    auto trow_of = [&](int gt) -> int* { return reinterpret_cast<int*>(smem + C::OFF_TROW) + (gt % VST) * TK; };
+    float* st_m = reinterpret_cast<float*>(smem + C::OFF_STATS);  // [128] set B's row maximum (base 2)
+    float* st_l = st_m + kRowsPerBlock;                            // [128] set B's row sum
+    AltBarriers* bars = reinterpret_cast<AltBarriers*>(smem + C::OFF_BAR);
+    volatile int* abort_flag = &bars->abort_flag;
+
+    if (p.graph_hdr != nullptr) {
+        // a launch replayed from a CUDA graph: the plan staged since must have the captured shape
+        const int4 h0 = __ldg(reinterpret_cast<const int4*>(p.graph_hdr));
+        const int4 h1 = __ldg(reinterpret_cast<const int4*>(p.graph_hdr) + 1);
+        if (h0.z != p.graph_batch || h1.x != p.W || h1.y != static_cast<int>(gridDim.x) || h1.z != 0) {
+            if (threadIdx.x == 0) atomicOr(p.status, BSP_DEVFLAG_GRAPH);
+            return;
+        }
+    }
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int u_begin = __ldg(p.cta_off + blockIdx.x);
+    const int u_end = __ldg(p.cta_off + blockIdx.x + 1);
+    const int nunits = u_end - u_begin;
+    const int ps = 1 << p.ps_log2;
+    const int qrows = p.bq * p.G;  // rows a quadrant's TMA box fills
+
+    // ---- setup
+    if (tid == 0) {
+        for (int s = 0; s < KST; ++s) {
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->k_empty[s], 1);
+        }
+        for (int s = 0; s < VST; ++s) {
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->v_empty[s], 1);
+        }
+        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->s_full[i], 1);
+            mbar_init(&bars->p_full[i], 4);  // one arrival per softmax warp of the set
+            mbar_init(&bars->o_final[i], 1);
+        }
+        mbar_init(&bars->st_full, 4);   // set B's warps
+        mbar_init(&bars->o_merged, 4);  // set A's warps
+        mbar_init(&bars->drain, 1);
+        bars->abort_flag = 0;
+        bars->tail_granted = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    if (warp == 1) tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
+    // zero the query rows no TMA box covers (rows bq * G .. 31 of each quadrant), so padded rows stay
+    // finite
+    {
+        constexpr int NCHUNK = NC * kRowsPerBlock * 8;  // 16-byte chunks of the Q buffer
+        for (int idx = tid; idx < NCHUNK; idx += C::THREADS) {
+            const int r = (idx >> 3) & (kRowsPerBlock - 1);
+            if ((r & 31) >= qrows) reinterpret_cast<uint4*>(smem)[idx] = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    // every CTA of this grid is resident: a dependent launch (the tail kernel) may start on the
+    // SMs this grid leaves; it waits for this grid's completion before reading the partials
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        const int BR = ps < kTileKeys ? ps : kTileKeys;  // rows per box (a page, or 64 rows of a larger page)
+        int gt = 0, k = 0, ntail = 0;
+        bool ok = true;
+        for (int u = u_begin; u < u_end && ok; ++u, ++k) {
+            const UnitInfo ui = load_unit(p, u);
+            const int ptiles = prompt_tiles<TK>(ui);
+            const int ntiles = ptiles + alt_tail_tiles(ui, p.Wblk);
+            const int* pg = p.pages + ui.page_off;
+            const int npages = (ui.P + ps - 1) >> p.ps_log2;
+            int win_base = -1, my_page = 0;
+            // the unit's Q first, once the previous unit's last Q*K^T is done (a later load could wait
+            // for a ring slot whose P*V the tensor core issues only after this unit's first Q*K^T)
+            if (k >= 1) {
+                ok = mbar_wait(&bars->q_empty, (k - 1) & 1, abort_flag, kAltWaitNs);
+                ok = __all_sync(FULL, ok);
+                if (!ok) break;
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars->q_full, NC * 4 * qrows * 128);
+                for (int c = 0; c < NC; ++c)
+                    for (int i = 0; i < 4; ++i)
+                        tma_load_3d(q_buf + c * (kRowsPerBlock * 128) + i * 32 * 128, &tm_q, &bars->q_full, c * 64,
+                                    ui.g * p.G, ui.row_off + ui.rb * p.Wblk + i * p.bq);
+            }
+            for (int t = 0; t < ntiles; ++t, ++gt) {
+                // this warp is the only waiter on the slot-release barriers and takes every tile's
+                // release in order, so each parity wait names the phase it means
+                if (gt >= KST) {
+                    ok = mbar_wait(&bars->k_empty[gt % KST], ((gt / KST) - 1) & 1, abort_flag, kAltWaitNs);
+                    ok = __all_sync(FULL, ok);
+                    if (!ok) break;
+                }
+                if (t >= ptiles) {
+                    // a tail tile: once its V slot is free too, hand both slots to the tail-tile warps
+                    // (a counter, not a barrier phase: they may lag several tail tiles behind)
+                    if (gt >= VST) {
+                        ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kAltWaitNs);
+                        ok = __all_sync(FULL, ok);
+                        if (!ok) break;
+                    }
+                    ++ntail;
+                    if (lane == 0) alt_st_release(&bars->tail_granted, ntail);
+                    __syncwarp();
+                    continue;
+                }
+                const int key0 = ui.key_begin + t * TK;
+                const int valid = min(TK, ui.key_end - key0);
+                const int nchunks = (valid + BR - 1) / BR;  // pages (or 64-row slices) with valid keys
+                const int tile_bytes = nchunks * BR * D * 2;
+                const int pidx0 = key0 >> p.ps_log2;
+                const int pidx_last = (key0 + (nchunks - 1) * BR) >> p.ps_log2;
+                if (win_base < 0 || pidx_last >= win_base + 32) {  // warp-uniform
+                    win_base = pidx0;
+                    my_page = (win_base + lane < npages) ? __ldg(pg + win_base + lane) : 0;
+                }
+                const int nbox = nchunks * NC;  // box b of a tensor: column half b % NC of chunk b / NC
+                for (int tensor = 0; tensor < 2; ++tensor) {
+                    if (tensor == 1 && gt >= VST) {
+                        ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kAltWaitNs);
+                        ok = __all_sync(FULL, ok);
+                        if (!ok) break;
+                    }
+                    uint64_t* full = tensor == 0 ? &bars->k_full[gt % KST] : &bars->v_full[gt % VST];
+                    uint8_t* base = tensor == 0 ? k_tile(gt) : v_tile(gt);
+                    const CUtensorMap* map = tensor == 0 ? &tm_k : &tm_v;
+                    if (lane == 0) mbar_arrive_expect_tx(full, tile_bytes);
+                    for (int b0 = 0; b0 < nbox; b0 += 32) {
+                        const int bx = b0 + lane;
+                        const int ch = min(bx / NC, nchunks - 1);
+                        const int key = key0 + ch * BR;
+                        int page = __shfl_sync(FULL, my_page, (key >> p.ps_log2) - win_base);
+                        if (bx < nbox) {
+                            if (static_cast<unsigned>(page) >= static_cast<unsigned>(p.num_pages)) {
+                                atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
+                                page = 0;
+                            }
+                            const int c = bx % NC;
+                            const int row = ((page * p.Hkv + ui.g) << p.ps_log2) + (key & (ps - 1));
+                            tma_load_2d(base + c * TK * 128 + ch * BR * 128, map, full, c * 64, row);
+                        }
+                    }
+                }
+                if (!ok) break;
+                __syncwarp();
+            }
+        }
+        if (!ok) {
+            if (lane == 0) {
+                *abort_flag = 1;
+                atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+            }
+            // drain: let this CTA's own copies land before the CTA exits
+            const uint64_t t0 = globaltimer_ns();
+            for (int j = max(0, gt - KST); j <= gt; ++j)
+                while (!mbar_try_wait(&bars->k_full[j % KST], (j / KST) & 1) && globaltimer_ns() - t0 < kAltDrainNs) {
+                }
+            for (int j = max(0, gt - VST); j <= gt; ++j)
+                while (!mbar_try_wait(&bars->v_full[j % VST], (j / VST) & 1) && globaltimer_ns() - t0 < kAltDrainNs) {
+                }
+            while (!mbar_try_wait(&bars->q_full, k & 1) && globaltimer_ns() - t0 < kAltDrainNs) {
+            }
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            constexpr uint32_t ID_QK = idesc_f16(kRowsPerBlock, TK, BF16, false);
+            constexpr uint32_t ID_PV = idesc_f16(kRowsPerBlock, D, BF16, true);
+            int gt = 0, k = 0;
+            int cnt[2] = {0, 0};                           // Q*K^T issued per set
+            int pend[2] = {-1, -1}, pcnt[2] = {0, 0};      // tile of set X whose P*V is not issued yet
+            bool pfirst[2] = {false, false}, plast[2] = {false, false};
+            bool ok = true;
+            auto issue_pv = [&](int x) -> bool {
+                const int j = pend[x];
+                if (!mbar_wait(&bars->p_full[x], pcnt[x] & 1, abort_flag, kAltWaitNs)) return false;
+                if (!mbar_wait(&bars->v_full[j % VST], (j / VST) & 1, abort_flag, kAltWaitNs)) return false;
+                tc_fence_after();
+                const uint32_t p_tmem = tmem + C::S_COL + x * TK;
+                const uint32_t o_tmem = tmem + C::O_COL + x * D;
+                const uint32_t v_addr = smem_u32(v_tile(j));
+#pragma unroll
+                for (int kk = 0; kk < TK / 16; ++kk) {
+                    const uint64_t bd = sdesc_sw128(v_addr + kk * 16 * 128, TK * 128, 1024);
+                    mma_f16_tmem_a(o_tmem, p_tmem + kk * 8, bd, ID_PV, (!pfirst[x] || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&bars->v_empty[j % VST]);
+                if (plast[x]) mma_commit(&bars->o_final[x]);
+                pend[x] = -1;
+                return true;
+            };
+            const uint32_t q_addr = smem_u32(q_buf);
+            for (int u = u_begin; u < u_end && ok; ++u, ++k) {
+                const UnitInfo ui = load_unit(p, u);
+                const int ntiles = prompt_tiles<TK>(ui) + alt_tail_tiles(ui, p.Wblk);
+                for (int t = 0; t < ntiles; ++t, ++gt) {
+                    const int x = t & 1;
+                    // S_X holds P of set X's previous tile: its P*V goes first
+                    if (pend[x] >= 0) {
+                        ok = issue_pv(x);
+                        if (!ok) break;
+                    }
+                    if (t == 0) {
+                        ok = mbar_wait(&bars->q_full, k & 1, abort_flag, kAltWaitNs);
+                        if (!ok) break;
+                    }
+                    ok = mbar_wait(&bars->k_full[gt % KST], (gt / KST) & 1, abort_flag, kAltWaitNs);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t k_addr = smem_u32(k_tile(gt));
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t ad =
+                            sdesc_sw128(q_addr + (kk >> 2) * (kRowsPerBlock * 128) + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(k_addr + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
+                        mma_f16(tmem + C::S_COL + x * TK, ad, bd, ID_QK, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&bars->s_full[x]);
+                    mma_commit(&bars->k_empty[gt % KST]);
+                    if (t == ntiles - 1) mma_commit(&bars->q_empty);
+                    pend[x] = gt;
+                    pcnt[x] = cnt[x]++;
+                    pfirst[x] = t < 2;
+                    plast[x] = t >= ntiles - 2;
+                }
+                if (!ok) break;
+                if (ntiles == 1) {
+                    // set B has no tile in this unit: its previous unit's last P*V (and o_final) first,
+                    // then this unit's o_final, so that o_final[B] keeps one phase per unit, in order
+                    if (pend[1] >= 0) {
+                        ok = issue_pv(1);
+                        if (!ok) break;
+                    }
+                    mma_commit(&bars->o_final[1]);
+                }
+            }
+            for (int x = 0; x < 2 && ok; ++x)
+                if (pend[x] >= 0) ok = issue_pv(x);
+            if (!ok) {
+                *abort_flag = 1;
+                atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+            }
+            // drain: every MMA issued by this thread completes before TMEM is freed
+            mma_commit(&bars->drain);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&bars->drain, 0) && globaltimer_ns() - t0 < kAltDrainNs) {
+            }
+        }
+    } else if (warp < 10) {
+        // ================= softmax warps (set x), set A also merges and writes the unit's output ====
+        const int x = (warp - 2) >> 2;
+        const int quad = warp & 3;           // TMEM lane quadrant this warp may access
+        const int row = quad * 32 + lane;    // TMEM lane of the thread's query row
+        const int wq = lane / p.G;           // beam of the quadrant
+        const int jh = lane - wq * p.G;      // head of the group
+        const int wbl = quad * p.bq + wq;    // beam of the row block
+        const bool row_ok = lane < qrows;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        const uint32_t s_col = lane_base + C::S_COL + x * TK;
+        const uint32_t o_col = lane_base + C::O_COL + x * D;
+        const float sl2 = p.scale_log2;
+        const uint32_t ninf = __float_as_uint(-INFINITY);
+        bool ok = true;
+        int gt = 0, n = 0;  // global tile counter, tiles of this set so far
+        for (int k = 0; k < nunits && ok; ++k) {
+            const UnitInfo cur = load_unit(p, u_begin + k);
+            const int ptiles = prompt_tiles<TK>(cur);
+            const int ntiles = ptiles + alt_tail_tiles(cur, p.Wblk);
+            const int nw = alt_block_beams(cur, p.Wblk);  // beams of this row block
+            const int wb = cur.rb * p.Wblk + wbl;          // beam of the request
+            const bool live = row_ok && wbl < nw;
+            // a warp whose rows are all padding skips the arithmetic but keeps the barrier protocol
+            const bool warp_live = quad * p.bq < nw;
+            // set B may overwrite O_B (its first P*V of this unit) only once set A has read the previous
+            // unit's O_B: it waits for that before its first arrival of the unit
+            bool need_merged = x == 1 && k >= 1;
+            float m = -INFINITY, l = 0.f;
+            for (int t = 0; t < ntiles && ok; ++t, ++gt) {
+                if ((t & 1) != x) continue;
+                const bool tail = t >= ptiles;
+                const int valid = tail ? TK : min(TK, cur.key_end - (cur.key_begin + t * TK));
+                ok = mbar_wait(&bars->s_full[x], n & 1, abort_flag, kAltWaitNs);
+                // a tail tile's key table is complete once its V slot is full
+                if (ok && tail) ok = mbar_wait(&bars->v_full[gt % VST], (gt / VST) & 1, abort_flag, kAltWaitNs);
+                ok = __all_sync(FULL, ok);
+                if (!ok) break;
+                tc_fence_after();
+                if (warp_live) {
+                    // masked keys count as -inf: no part in the maximum, probability exp2(-inf) = 0. A
+                    // partial prompt tile keeps [0, valid); a tail tile keeps the row's own beam's T
+                    // columns (w * T - first column of the tile, T <= 8: at most two 32-bit words) whose
+                    // key is readable
+                    const bool partial = valid < TK || tail;
+                    uint32_t km[TK / 32];
+                    if (partial) {
+                        if (tail) {
+                            uint64_t win = 0;
+                            int wbase = 0;
+                            if (live) {
+                                const int lo = wbl * cur.T - (t - ptiles) * TK;
+                                const int c0 = max(lo, 0), c1 = min(lo + cur.T, TK);
+                                wbase = c0 & ~31;
+                                const int* trow = trow_of(gt);
+                                for (int c = c0; c < c1; ++c)
+                                    if (trow[c] >= 0) win |= 1ull << (c - wbase);
+                            }
+#pragma unroll
+                            for (int j = 0; j < TK / 32; ++j)
+                                km[j] = 32 * j == wbase        ? static_cast<uint32_t>(win)
+                                        : 32 * j == wbase + 32 ? static_cast<uint32_t>(win >> 32)
+                                                               : 0u;
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < TK / 32; ++j) {
+                                const int nk = min(max(valid - 32 * j, 0), 32);
+                                km[j] = nk == 32 ? ~0u : (1u << nk) - 1u;
+                            }
+                        }
+                    }
+                    auto mask_pair = [&](int c0, uint32_t& ma, uint32_t& mb) {
+                        ma = c0 == 0 ? km[0] : km[2];
+                        mb = c0 == 0 ? km[1] : km[3];
+                    };
+                    // pass 1: the row maximum of the raw scores, then scaled (the scale is positive)
+                    float mp[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) mp[j] = -INFINITY;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < TK; c0 += 64) {
+                        uint32_t ma = ~0u, mb = ~0u;
+                        if (partial) {
+                            mask_pair(c0, ma, mb);
+                            if (!__any_sync(FULL, (ma | mb) != 0u)) continue;  // no row of the warp keeps one
+                        }
+                        uint32_t sa[32], sb[32];
+                        __syncwarp();
+                        tmem_ld32(s_col + c0, sa);
+                        tmem_ld32(s_col + c0 + 32, sb);
+                        tmem_wait_ld();
+                        if (partial && __any_sync(FULL, (ma & mb) != ~0u)) {
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) {
+                                sa[c] = (ma >> c) & 1u ? sa[c] : ninf;
+                                sb[c] = (mb >> c) & 1u ? sb[c] : ninf;
+                            }
+                        }
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(sa[c]));
+                            mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(sb[c]));
+                        }
+                    }
+                    const float mxr = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                            fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+                    const float mx = mxr * sl2;
+                    // lazy maximum: keep the old one unless the row maximum grew by more than 2^8
+                    const bool first = t < 2;  // this set's first tile of the unit
+                    const bool need = !first && mx > m + 8.0f;
+                    const bool rescale = __any_sync(FULL, need);
+                    float alpha = 1.0f;
+                    if (first) {
+                        m = mx;
+                    } else if (need) {
+                        alpha = exp2f(m - mx);
+                        m = mx;
+                        l *= alpha;
+                    }
+                    if (rescale) {
+                        // P_X V of set X's previous tile has completed (it was issued before the Q*K^T
+                        // whose completion s_full reported), and this tile's P*V waits for p_full
+                        __syncwarp();
+#pragma unroll 1
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t orr[32];
+                            tmem_ld32(o_col + c0, orr);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                            tmem_st32(o_col + c0, orr);
+                        }
+                    }
+                    // pass 2: probabilities 2^(s * scale_log2 - m) and their sum; P in 16-bit pairs over
+                    // the first 64 columns of S_X, 64 keys per store (P columns [32i, 32i + 32) overwrite
+                    // score columns already read in this pass). A row that has kept no key yet (set B's
+                    // first tile can be a tail tile without the row's keys) has m = -inf: its P is 0.
+                    const float nm = m == -INFINITY ? 0.f : -m;
+                    float rsp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                    for (int c0 = 0; c0 < TK; c0 += 64) {
+                        uint32_t ma = ~0u, mb = ~0u;
+                        if (partial) mask_pair(c0, ma, mb);
+                        uint32_t pk[32];
+                        if (partial && !__any_sync(FULL, (ma | mb) != 0u)) {
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) pk[c] = 0u;
+                            tmem_st32(s_col + (c0 >> 1), pk);
+                            continue;
+                        }
+                        uint32_t sa[32], sb[32];
+                        __syncwarp();
+                        tmem_ld32(s_col + c0, sa);
+                        tmem_ld32(s_col + c0 + 32, sb);
+                        tmem_wait_ld();
+                        if (partial && __any_sync(FULL, (ma & mb) != ~0u)) {
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) {
+                                sa[c] = (ma >> c) & 1u ? sa[c] : ninf;
+                                sb[c] = (mb >> c) & 1u ? sb[c] : ninf;
+                            }
+                        }
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            const float p0 = exp2f(fmaf(__uint_as_float(sa[c]), sl2, nm));
+                            const float p1 = exp2f(fmaf(__uint_as_float(sa[c + 1]), sl2, nm));
+                            const float p2 = exp2f(fmaf(__uint_as_float(sb[c]), sl2, nm));
+                            const float p3 = exp2f(fmaf(__uint_as_float(sb[c + 1]), sl2, nm));
+                            rsp[(c >> 1) & 1] += p0 + p1;
+                            rsp[2 + ((c >> 1) & 1)] += p2 + p3;
+                            pk[c >> 1] = pack2<BF16>(p0, p1);
+                            pk[16 + (c >> 1)] = pack2<BF16>(p2, p3);
+                        }
+                        tmem_st32(s_col + (c0 >> 1), pk);
+                    }
+                    tmem_wait_st();
+                    l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
+                }
+                if (!tail && valid < TK) {
+                    // a unit's last prompt tile: zero V rows past the valid keys (stale or garbage rows
+                    // times P = 0 must not produce NaN); the set that owns the tile, before its P*V
+                    ok = mbar_wait(&bars->v_full[gt % VST], (gt / VST) & 1, abort_flag, kAltWaitNs);
+                    ok = __all_sync(FULL, ok);
+                    if (!ok) break;
+                    uint8_t* sV = v_tile(gt);
+                    const int nzc = (TK - valid) * 8;  // 16-byte chunks per column half
+                    for (int c = 0; c < NC; ++c)
+                        for (int idx = tid - 64 - 128 * x; idx < nzc; idx += 128)
+                            reinterpret_cast<uint4*>(sV + c * TK * 128 + valid * 128)[idx] = make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_smem();
+                }
+                if (need_merged) {
+                    ok = mbar_wait(&bars->o_merged, (k - 1) & 1, abort_flag, kAltWaitNs);
+                    ok = __all_sync(FULL, ok);
+                    if (!ok) break;
+                    need_merged = false;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->p_full[x]);
+                ++n;
+            }
+            if (!ok) break;
+            if (x == 1) {
+                // ---- set B: hand the row statistics of the unit to set A (none when it had no tile)
+                if (need_merged) {
+                    ok = mbar_wait(&bars->o_merged, (k - 1) & 1, abort_flag, kAltWaitNs);
+                    ok = __all_sync(FULL, ok);
+                    if (!ok) break;
+                }
+                st_m[row] = m;
+                st_l[row] = l;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->st_full);
+                continue;
+            }
+            // ---- set A: merge both states once both sets' last P*V of the unit have completed
+            ok = mbar_wait(&bars->o_final[0], k & 1, abort_flag, kAltWaitNs);
+            if (ok) ok = mbar_wait(&bars->o_final[1], k & 1, abort_flag, kAltWaitNs);
+            if (ok) ok = mbar_wait(&bars->st_full, k & 1, abort_flag, kAltWaitNs);
+            ok = __all_sync(FULL, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const bool has_b = ntiles >= 2;  // set B took a tile of this unit (the same for every row)
+            if (warp_live) {
+                const float mb_ = has_b ? st_m[row] : -INFINITY;
+                const float lb = has_b ? st_l[row] : 0.f;
+                const float M = fmaxf(m, mb_);
+                const float wa = exp2f(m - M);
+                const float wbw = lb > 0.f ? exp2f(mb_ - M) : 0.f;
+                const float L = l * wa + lb * wbw;
+                const float inv = 1.0f / L;
+                const float fa = wa * inv, fb = wbw * inv;
+                const long long rh = (static_cast<long long>(cur.row_off) + wb) * p.Hq + cur.g * p.G + jh;
+                const long long prow = (static_cast<long long>(cur.part) * p.W + wb) * p.Hq + cur.g * p.G + jh;
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t oa[32], ob[32];
+                    __syncwarp();
+                    tmem_ld32(lane_base + C::O_COL + c0, oa);
+                    if (has_b) tmem_ld32(lane_base + C::O_COL + D + c0, ob);
+                    tmem_wait_ld();
+                    float* f = reinterpret_cast<float*>(oa);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        f[e] = has_b ? fmaf(__uint_as_float(oa[e]), fa, __uint_as_float(ob[e]) * fb)
+                                     : __uint_as_float(oa[e]) * fa;
+                    if (live) {
+                        if (cur.fused) {
+                            // the request's whole key set went through this unit: the final O (q dtype)
+                            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + rh * D);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                dst[(c0 >> 3) + e] = make_uint4(pack2<BF16>(f[8 * e], f[8 * e + 1]),
+                                                                pack2<BF16>(f[8 * e + 2], f[8 * e + 3]),
+                                                                pack2<BF16>(f[8 * e + 4], f[8 * e + 5]),
+                                                                pack2<BF16>(f[8 * e + 6], f[8 * e + 7]));
+                        } else {
+                            float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                dst[(c0 >> 2) + e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2], f[4 * e + 3]);
+                        }
+                    }
+                }
+                if (live) {
+                    const float lse2 = M + log2f(L);
+                    if (cur.fused)
+                        p.lse[rh] = p.lse_base2 ? lse2 : lse2 * 0.69314718055994530942f;
+                    else
+                        p.part_lse[prow] = lse2;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->o_merged);
+        }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+        }
+    } else {
+        // ================= tail tiles =================
+        constexpr int CH = D / 8;     // 16-byte chunks of a K or V row
+        constexpr int RPS = 64 / CH;  // rows one pass of the 64 threads covers
+        const int gtid = tid - C::GATHER_TID0;
+        const int kc = gtid % CH;
+        const int rsub = gtid / CH;
+        const uint16_t* k_pool = static_cast<const uint16_t*>(p.k_pool);
+        const uint16_t* v_pool = static_cast<const uint16_t*>(p.v_pool);
+        // pool rows of this thread's two key columns (gtid, gtid + 64) of each tail tile of a unit,
+        // resolved a unit ahead; -1 past the block's tail keys or when unreadable
+        int res[kAltMaxTailTiles][2];
+        auto resolve = [&](const UnitInfo& ui) {
+            const int ntt = alt_tail_tiles(ui, p.Wblk);
+            const int nkeys = alt_block_beams(ui, p.Wblk) * ui.T;
+#pragma unroll
+            for (int nt = 0; nt < kAltMaxTailTiles; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    res[nt][h] = -1;
+                    const int cc = nt * TK + gtid + 64 * h;
+                    if (nt >= ntt || cc >= nkeys) continue;
+                    const int wl = cc / ui.T, tt = cc - wl * ui.T;
+                    const int w = ui.rb * p.Wblk + wl;
+                    const int pos = ui.P + tt;
+                    const int src = __ldg(p.ci + (static_cast<long long>(ui.b) * p.W + w) * p.max_seq + pos);
+                    int r = -1;
+                    if (static_cast<unsigned>(src) < static_cast<unsigned>(p.W)) {
+                        const int page = __ldg(p.beam_pages +
+                                               (static_cast<long long>(ui.b) * p.W + src) * p.beam_pages_stride +
+                                               (pos >> p.ps_log2));
+                        if (static_cast<unsigned>(page) < static_cast<unsigned>(p.num_pages))
+                            r = ((page * p.Hkv + ui.g) << p.ps_log2) + (pos & (ps - 1));
+                    }
+                    if (r < 0) {
+                        atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
+                    } else {
+                        // the gather runs at the end of the unit: bring the row's K and V into L2 now
+#pragma unroll
+                        for (int off = 0; off < D * 2; off += 128) {
+                            prefetch_l2(static_cast<const uint8_t*>(p.k_pool) + static_cast<long long>(r) * (D * 2) + off);
+                            prefetch_l2(static_cast<const uint8_t*>(p.v_pool) + static_cast<long long>(r) * (D * 2) + off);
+                        }
+                    }
+                    res[nt][h] = r;
+                }
+        };
+        bool ok = true;
+        int gt = 0, ntail = 0;
+        UnitInfo cur;
+        if (nunits > 0) {
+            cur = load_unit(p, u_begin);
+            resolve(cur);
+        }
+        for (int k = 0; k < nunits && ok; ++k) {
+            const int ptiles = prompt_tiles<TK>(cur);
+            const int ntt = alt_tail_tiles(cur, p.Wblk);
+#pragma unroll
+            for (int nt = 0; nt < kAltMaxTailTiles; ++nt) {
+                if (nt >= ntt) break;
+                const int gtt = gt + ptiles + nt;
+                // the producer hands the tile's K and V slots over once the previous tiles that used them
+                // are done
+                ok = alt_wait_counter(&bars->tail_granted, ntail, abort_flag, kAltWaitNs);
+                ++ntail;
+                ok = __all_sync(FULL, ok);
+                int* trow = trow_of(gtt);
+                if (ok) {
+                    trow[gtid] = res[nt][0];
+                    trow[gtid + 64] = res[nt][1];
+                }
+                ok = alt_gather_sync_and(ok);
+                if (ok) {
+                    uint8_t* kt = k_tile(gtt);
+                    uint8_t* vt = v_tile(gtt);
+#pragma unroll 4
+                    for (int i = 0; i < TK / RPS; ++i) {
+                        const int c = rsub + i * RPS;
+                        const int r = trow[c];
+                        // the layout of a TMA box with 128-byte swizzle: chunk kc of row c in column half kc / 8
+                        const uint32_t off = (kc >> 3) * (TK * 128) + c * 128 + (((kc & 7) ^ (c & 7)) << 4);
+                        const long long e = static_cast<long long>(r < 0 ? 0 : r) * D + kc * 8;
+                        const uint32_t nb = r < 0 ? 0u : 16u;  // absent keys are zero rows
+                        cp_async16(kt + off, k_pool + e, nb);
+                        cp_async16(vt + off, v_pool + e, nb);
+                    }
+                    cp_async_commit_wait_all();
+                    fence_proxy_async_smem();
+                }
+                ok = alt_gather_sync_and(ok);
+                if (!ok) break;
+                if (gtid == 0) {
+                    mbar_arrive(&bars->k_full[gtt % KST]);
+                    mbar_arrive(&bars->v_full[gtt % VST]);
+                }
+            }
+            gt += ptiles + ntt;
+            if (ok && k + 1 < nunits) {
+                cur = load_unit(p, u_begin + k + 1);
+                resolve(cur);
+            }
+        }
+        if (!ok && gtid == 0) {
+            *abort_flag = 1;
+            atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D, bool BF16>
+static cudaError_t prepare_alt_k() {
+    using C = AltCfg<D>;
+    static_assert(sizeof(AltBarriers) <= 512, "barrier block");
+    cudaError_t e =
+        cudaFuncSetAttribute(prefix_alt_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(prefix_alt_kernel<D, BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+}
+
+cudaError_t prepare_alt(int head_dim, bool bf16) {
+    switch (head_dim) {
+        case 64: return bf16 ? prepare_alt_k<64, true>() : prepare_alt_k<64, false>();
+        case 128: return bf16 ? prepare_alt_k<128, true>() : prepare_alt_k<128, false>();
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_alt(int head_dim, bool bf16, int ctas, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const PrefixParams& p, cudaStream_t stream) {
+    if (ctas == 0 || p.num_units == 0) return cudaSuccess;
+    if (p.bq <= 0 || p.bq * p.G > 32) return cudaErrorInvalidValue;
+    switch (head_dim) {
+        case 64:
+            if (bf16) prefix_alt_kernel<64, true><<<ctas, AltCfg<64>::THREADS, AltCfg<64>::SMEM, stream>>>(tq, tk, tv, p);
+            else prefix_alt_kernel<64, false><<<ctas, AltCfg<64>::THREADS, AltCfg<64>::SMEM, stream>>>(tq, tk, tv, p);
+            break;
+        case 128:
+            if (bf16) prefix_alt_kernel<128, true><<<ctas, AltCfg<128>::THREADS, AltCfg<128>::SMEM, stream>>>(tq, tk, tv, p);
+            else prefix_alt_kernel<128, false><<<ctas, AltCfg<128>::THREADS, AltCfg<128>::SMEM, stream>>>(tq, tk, tv, p);
+            break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace bsp

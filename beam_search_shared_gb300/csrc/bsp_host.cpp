@@ -266,12 +266,7 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
 
     // ---- work units: (request, kv head, key split, query-row block)
     int nrb, wblk;
-    // all W*G query rows of a (request, kv head) in one unit as two MMA blocks (the wide kernel)
-    const bool wide = !pf && wide_quad_beams(geo->head_dim, beam_width, G) > 0;
-    if (wide) {
-        nrb = 1;
-        wblk = beam_width;
-    } else if (pf) {
+    if (pf) {
         // prompt tokens in blocks of one MMA's rows (dense layout: 128 rows = 128 / G tokens)
         wblk = std::max(1, kRowsPerBlock / G);
         nrb = 0;
@@ -279,6 +274,24 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     } else {
         row_blocks(beam_width, G, &nrb, &wblk);
     }
+    // The prompt kernel of a decode step at head_dim <= 128 (prefill and head_dim 256: the one-set
+    // kernel, layout 0). A row block of at most 64 query rows, 16 per TMEM lane quadrant, keeps the one-set
+    // kernel's half-row layout (two threads per row). Otherwise a (request, kv head) with 129-256 rows
+    // goes to the wide kernel (layout 2: all its rows in one unit as two MMA blocks, the prompt read
+    // once), and any other to the alternating-tile kernel (layout 1), whose row blocks of one (request,
+    // kv head, key split) are dealt to `group` neighbouring CTAs at the same place of their lists.
+    int layout = 0;
+    if (!pf && geo->head_dim <= 128 && prefix_quad_beams(geo->head_dim, wblk, G) == 0) {
+        if (wide_quad_beams(geo->head_dim, beam_width, G) > 0) {
+            layout = 2;
+            nrb = 1;
+            wblk = beam_width;
+        } else if (alt_quad_beams(geo->head_dim, wblk, G) > 0) {
+            layout = 1;
+        }
+    }
+    const bool alt = layout == 1;
+    const int group = alt ? nrb : 1;
     auto nrb_of = [&](int b) -> int { return pf ? static_cast<int>(ceil_div(rows[b], wblk)) : nrb; };
     std::vector<int64_t> tiles(batch);
     int64_t total_tiles = 0, active = 0;
@@ -308,11 +321,15 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     // the kernel's tail tiles: one extra key tile per row block (W_blk beams), or for a wide unit (all W
     // beams) up to kWideMaxTailTiles tiles of 128 keys
     const int tk = prefix_tile_keys(geo->head_dim);
+    // a request is finished by the prompt kernel when its prompt is one partial state and the tail keys
+    // of a unit's beams (W_blk of them; all W for the wide kernel) fit the kernel's tail tiles: up to 4
+    // tiles of 128 keys (layouts 1 and 2), one prompt tile (layout 0)
     auto tail_tiles = [&](int b) -> int64_t {
-        return ceil_div(static_cast<int64_t>(tail_len[b]) * wblk, wide ? 128 : tk);
+        return ceil_div(static_cast<int64_t>(tail_len[b]) * wblk, layout ? 128 : tk);
     };
     auto fused = [&](int b) -> bool {
-        return nsplit[b] == 1 && tail_tiles(b) <= (wide ? kWideMaxTailTiles : 1);
+        return nsplit[b] == 1 &&
+               tail_tiles(b) <= (layout == 1 ? kAltMaxTailTiles : layout == 2 ? kWideMaxTailTiles : 1);
     };
     // the plan tiles a unit reads: a causal prefill block stops at its last token's keys
     auto unit_end_tile = [&](int b, int rb, int32_t t1) -> int32_t {
@@ -342,7 +359,7 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
             const int32_t t0 = static_cast<int32_t>(s * tiles[b] / nsplit[b]);
             const int32_t t1 = static_cast<int32_t>((s + 1) * tiles[b] / nsplit[b]);
             for (int g = 0; g < Hkv; ++g)
-                for (int rb = 0; rb < nrb_of(b); ++rb) {
+                for (int rb = 0; rb < (group > 1 ? 1 : nrb_of(b)); ++rb) {  // a group's other blocks follow
                     const int32_t te = unit_end_tile(b, rb, t1);
                     Unit u{};
                     u.f[kUnitReq] = b;
@@ -380,7 +397,7 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     auto utiles = [&](int64_t i) -> int64_t { return units[i].f[kUnitCost]; };
     std::vector<std::vector<int32_t>> lists;
     if (nu > 0) {
-        const int64_t bins = std::min<int64_t>(nu, num_sms);
+        const int64_t bins = std::min<int64_t>(nu, num_sms / group);
         if (bins >= (int64_t{1} << 20)) return BSP_ERR_UNSUPPORTED;
         // LPT: a binary min-heap of (load << 20 | cta) keys, ties to the lower CTA index
         std::vector<uint64_t> heap(static_cast<size_t>(bins));
@@ -504,6 +521,24 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
                 }
                 l[j] = x;
             }
+        if (group > 1) {
+            // each dealt list goes to `group` neighbouring CTAs, one per row block, in the same order
+            std::vector<Unit> all;
+            std::vector<std::vector<int32_t>> glists;
+            all.reserve(units.size() * static_cast<size_t>(group));
+            for (const auto& l : lists)
+                for (int rb = 0; rb < group; ++rb) {
+                    glists.emplace_back();
+                    for (int32_t i : l) {
+                        Unit u = units[static_cast<size_t>(i)];
+                        u.f[kUnitRowBlock] = rb;
+                        glists.back().push_back(static_cast<int32_t>(all.size()));
+                        all.push_back(u);
+                    }
+                }
+            units.swap(all);
+            lists.swap(glists);
+        }
     }
     const int64_t ctas = static_cast<int64_t>(lists.size());
     // a decode plan's CTA table has num_sms + 1 entries (CTAs past `ctas` have no units), so a launch
@@ -588,7 +623,7 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     out->tail_requests = tail_requests;
     out->total_rows = static_cast<int32_t>(total_rows);
     out->kind = pf ? 1 : 0;
-    out->mma_blocks = wide ? 2 : 1;
+    out->layout = layout;
     out->image_bytes = need;
     // offsets relative to the device workspace
     DeviceLayout L = device_layout(need, parts_cap, beam_width, *geo);
@@ -929,12 +964,13 @@ bsp_status attn_launches(const bsp_plan_t* plan, uint8_t* ws, const void* q, con
     const int D = geo.head_dim, Hq = geo.num_q_heads, Hkv = geo.num_kv_heads, G = Hq / Hkv;
     const bool bf16 = geo.dtype == BSP_DTYPE_BF16;
     const float log2e = 1.4426950408889634f;
-    const bool wide = plan->mma_blocks == 2;
+    const bool alt = plan->layout == 1, wide = plan->layout == 2;
 
     // everything that is not a launch (attributes, tensor maps, parameters) comes before the
     // first timing event
     const bool prefix = graph || plan->num_units > 0;
-    if (prefix && (wide ? prepare_wide(D, bf16) : prepare_prefix(D, bf16)) != cudaSuccess) return BSP_ERR_CUDA;
+    if (prefix && (alt ? prepare_alt(D, bf16) : wide ? prepare_wide(D, bf16) : prepare_prefix(D, bf16)) != cudaSuccess)
+        return BSP_ERR_CUDA;
     if (prepare_tail(D, bf16, graph ? plan->max_tail : plan->max_tail_len, Hq) != cudaSuccess) return BSP_ERR_CUDA;
     CUtensorMap tq, tk, tv;
     PrefixParams pp{};
@@ -944,9 +980,10 @@ bsp_status attn_launches(const bsp_plan_t* plan, uint8_t* ws, const void* q, con
         // query rows per TMA box: the row block, or a quadrant's share of it (half-row softmax; the wide
         // layout's quadrants)
         const int W = plan->beam_width;
-        const int qbeams = wide ? wide_quad_beams(D, W, G)
-                                : (prefill ? 0 : prefix_quad_beams(D, plan->beams_per_block, G));
-        if (wide && qbeams <= 0) return BSP_ERR_INVALID_ARG;
+        const int qbeams = alt    ? alt_quad_beams(D, plan->beams_per_block, G)
+                           : wide ? wide_quad_beams(D, W, G)
+                                  : (prefill ? 0 : prefix_quad_beams(D, plan->beams_per_block, G));
+        if ((alt || wide) && qbeams <= 0) return BSP_ERR_INVALID_ARG;
         cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(G),
                               static_cast<cuuint32_t>(qbeams > 0 ? qbeams : plan->beams_per_block)};
         const int ps = geo.page_size;
@@ -1020,7 +1057,8 @@ bsp_status attn_launches(const bsp_plan_t* plan, uint8_t* ws, const void* q, con
     if (!record(0)) return BSP_ERR_CUDA;
     if (prefix) {
         const int ctas = graph ? plan->num_sms : plan->prefix_ctas;
-        const cudaError_t e = wide ? launch_wide(D, bf16, ctas, tq, tk, tv, pp, s)
+        const cudaError_t e = alt    ? launch_alt(D, bf16, ctas, tq, tk, tv, pp, s)
+                              : wide ? launch_wide(D, bf16, ctas, tq, tk, tv, pp, s)
                                    : launch_prefix(D, bf16, ctas, tq, tk, tv, pp, s);
         if (e != cudaSuccess) return BSP_ERR_CUDA;
     }

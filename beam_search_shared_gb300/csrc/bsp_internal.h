@@ -54,6 +54,17 @@ constexpr int wide_quad_beams(int head_dim, int beam_width, int group) {
 }
 // tail tiles of 128 keys a wide unit may gather (the request is finished by the tail kernel beyond)
 constexpr int kWideMaxTailTiles = 4;
+// The alternating-tile layout of a decode step (bsp_alt.cu), at head_dim <= 128: a unit is one query-row
+// block (W_blk beams x G heads <= 128 rows) whose key tiles go alternately to two softmax warp sets;
+// the block's beams spread over the four TMEM lane quadrants, bq = ceil(W_blk / 4) beams (bq * G rows)
+// per quadrant. 0 when the beams do not fit that way.
+constexpr int alt_quad_beams(int head_dim, int beams_per_block, int group) {
+    const int bq = (beams_per_block + 3) / 4;
+    return (head_dim <= 128 && beams_per_block * group <= kRowsPerBlock && bq * group <= 32) ? bq : 0;
+}
+// tail tiles of 128 keys an alternating-tile unit may gather (the request is finished by the tail
+// kernel beyond)
+constexpr int kAltMaxTailTiles = 4;
 // Per-work-unit record: request, kv head, query-row block, key tiles [kt0, kt1), partial slot, and
 // the cost the host dealt it by (eighths of a prompt-kernel key tile; not read by the kernels).
 enum UnitField { kUnitReq = 0, kUnitKvHead = 1, kUnitRowBlock = 2, kUnitTile0 = 3, kUnitTile1 = 4, kUnitPart = 5,
@@ -128,6 +139,10 @@ cudaError_t prepare_tail(int head_dim, bool bf16, int max_tail_len, int num_q_he
 // prefetches its tail rows, and waits for the prompt kernel's partials before merging).
 cudaError_t launch_tail(int head_dim, bool bf16, int max_tail_len, const TailParams& p, bool after_prefix,
                         cudaStream_t stream);
+// The alternating-tile prompt kernel (p.Wblk = beams per row block, p.bq = beams per quadrant).
+cudaError_t prepare_alt(int head_dim, bool bf16);
+cudaError_t launch_alt(int head_dim, bool bf16, int ctas, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const PrefixParams& p, cudaStream_t stream);
 // The wide-layout prompt kernel (p.Wblk = beams per block, p.bq = beams per quadrant).
 cudaError_t prepare_wide(int head_dim, bool bf16);
 cudaError_t launch_wide(int head_dim, bool bf16, int ctas, const CUtensorMap& tq, const CUtensorMap& tk,

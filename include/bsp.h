@@ -145,9 +145,11 @@ typedef struct bsp_plan_t {
     int32_t total_rows;          /* query rows of the step: batch * beam_width (decode) or the prompt
                                     tokens of all requests (prefill) */
     int32_t kind;                /* 0: a decode-step plan (bsp_plan); 1: a prefill plan (bsp_plan_prefill) */
-    int32_t mma_blocks;          /* query-row blocks of 128 rows one prompt-kernel unit holds: 2 when a
-                                    (request, kv head) has 129-256 query rows at head_dim <= 128 (all its
-                                    beams in one unit, the prompt read once), else 1 */
+    int32_t layout;              /* prompt kernel of the plan: 0 one softmax warp set (prefill, head_dim
+                                    256, and row blocks of <= 64 query rows, two threads per row); 2 all
+                                    129-256 query rows of a (request, kv head) in one CTA as two MMA
+                                    blocks (the prompt read once); 1 two softmax warp sets taking a
+                                    unit's key tiles alternately (other decode steps at head_dim <= 128) */
     uint64_t off_cta;            /* byte offset of the per-CTA unit table */
     uint64_t reserved;
 } bsp_plan_t;

@@ -115,20 +115,34 @@ def decode_image(plan, img, with_cta=False):
     return req, units, pages
 
 
-def wide_layout(D, W, G):
-    """All W*G query rows of a (request, kv head) in one unit as two 128-row MMA blocks: 128 < W*G <= 256
-    at head_dim <= 128, with each block's beams spread over four 32-lane quadrants."""
-    bq = -(-(-(-W // 2)) // 4)
-    return D <= 128 and 128 < W * G <= 256 and bq * G <= 32
+def row_blocks(W, G):
+    """Query-row blocks of a (request, kv head): whole beams, at most 128 rows each, balanced."""
+    wmax = max(1, 128 // G)
+    nrb = -(-W // wmax)
+    return nrb, -(-W // nrb)
+
+
+def prompt_layout(D, W, G):
+    """The prompt kernel of a decode plan: 0 (one softmax set) at head_dim 256 or when a row block fits 16
+    rows per TMEM lane quadrant (half-row softmax); 2 (two MMA blocks per CTA) for 129-256 query rows per
+    (request, kv head) spread over the quadrants; 1 (alternating-tile sets) when a row block's beams
+    spread over the four 32-lane quadrants; else 0."""
+    _, wblk = row_blocks(W, G)
+    if D > 128 or -(-wblk // 4) * G <= 16:
+        return 0
+    if 128 < W * G <= 256 and -(-(-(-W // 2)) // 4) * G <= 32:
+        return 2
+    return 1 if -(-wblk // 4) * G <= 32 else 0
 
 
 def check_fused(plan, req, T, head_dim=128):
     """A request is finished by the prompt kernel iff it has one prompt partial state and its tail keys
-    fit the kernel's tail tiles: each row block's in one prompt-kernel tile (128 keys up to head_dim 128,
-    64 at 256), or, for a two-block unit, all W beams' in at most 4 tiles of 128 keys."""
+    fit the kernel's tail tiles: a unit's beams' (a row block's, or all W for the two-block kernel) in at
+    most 4 tiles of 128 keys (layouts 1 and 2), else in one prompt-kernel tile (128 keys up to head_dim
+    128, 64 at 256)."""
     T = np.asarray(T)
-    if plan.mma_blocks == 2:
-        want = (req[:, 2] == 1) & (-(-T * plan.beam_width // 128) <= 4)
+    if plan.layout in (1, 2):
+        want = (req[:, 2] == 1) & (-(-T * plan.beams_per_block // 128) <= 4)
     else:
         tile = 128 if head_dim <= 128 else 64
         want = (req[:, 2] == 1) & (T * plan.beams_per_block <= tile)
@@ -200,16 +214,34 @@ def test_plan_image_wide_batch_needs_no_split(lib):
         np.testing.assert_array_equal(pl[req[b][4]:req[b][4] + n], pages[b, :n])
 
 
+def check_groups(plan, units, cta):
+    """The row blocks of a (request, kv head, key split) sit on neighbouring CTAs at the same place of
+    their lists (CTA c * nrb + rb holds row block rb)."""
+    nrb = plan.row_blocks if plan.layout == 1 else 1
+    if nrb == 1:
+        return
+    ctas = len(cta) - 1
+    used = [c for c in range(ctas) if cta[c + 1] > cta[c]]
+    assert len(used) % nrb == 0 and used == list(range(len(used)))
+    for g0 in range(0, len(used), nrb):
+        lists = [units[cta[c]:cta[c + 1]] for c in range(g0, g0 + nrb)]
+        for rb, l in enumerate(lists):
+            assert len(l) == len(lists[0])
+            np.testing.assert_array_equal(l[:, 2], rb)
+            np.testing.assert_array_equal(np.delete(l, 2, axis=1), np.delete(lists[0], 2, axis=1))
+
+
 def test_plan_image_wide_beam_one_unit_per_kv_head(lib):
-    """192 query rows per (request, kv head) at head_dim 128: one unit holds both 96-row blocks, so the
-    prompt is read once; up to 4 tiles of 128 tail keys (96 beams x T <= 512) finish in the prompt kernel."""
+    """192 query rows per (request, kv head) at head_dim 128: one unit holds both 96-row blocks (the
+    two-block kernel), so the prompt is read once; up to 4 tiles of 128 tail keys (96 beams x T <= 512)
+    finish in the prompt kernel."""
     B, W = 3, 96
     P = [3000, 2900, 0]                       # 16 units on 8 SMs: no key splits
     T = [1, 0, 3]
     pages = np.tile(np.arange(94, dtype=np.int32), (B, 1))
     plan, img = bsp.plan_build(geo(npages=200), B, W, P, T, pages, 8, 8)
     req, units, _ = decode_image(plan, img)
-    assert plan.mma_blocks == 2 and plan.row_blocks == 1 and plan.beams_per_block == 96
+    assert plan.layout == 2 and plan.row_blocks == 1 and plan.beams_per_block == 96
     check_units_cover(plan, req, units, P)
     assert req[2][2] == 0                                            # empty prompt: no split, no unit
     check_fused(plan, req, T)
@@ -222,12 +254,40 @@ def test_plan_image_wide_beam_one_unit_per_kv_head(lib):
     req, _, _ = decode_image(plan, img)
     check_fused(plan, req, [5, 6, 1])                                # 96 x 6 tail keys exceed 4 tiles
     assert list(req[:, 5]) == [1, 0, 0]
-    # head_dim 256 keeps two row blocks (two 256-column O accumulators would not fit tensor memory)
-    plan, img = bsp.plan_build(geo(D=256, npages=200), B, W, P, T, pages, 8, 8)
+    # head_dim 256 keeps two row blocks on the one-set kernel
+    plan, img = bsp.plan_build(geo(D=256, npages=200), B, W, P, T, pages, 8, 152)
     req, units, _ = decode_image(plan, img)
-    assert plan.mma_blocks == 1 and plan.row_blocks == 2 and plan.beams_per_block == 48
+    assert plan.layout == 0 and plan.row_blocks == 2 and plan.beams_per_block == 48
     check_units_cover(plan, req, units, P)
     check_fused(plan, req, T, head_dim=256)
+
+
+def test_plan_image_row_block_groups_on_neighbouring_ctas(lib):
+    """384 query rows per (request, kv head) (96 beams x 4 heads): three 128-row blocks on the
+    alternating-tile kernel, dealt to three neighbouring CTAs in the same order; a block's tail keys
+    (32 beams x T) finish in the prompt kernel up to 4 tiles of 128 keys."""
+    B, W = 3, 96
+    P = [3000, 2900, 0]                       # 48 units on 24 SMs: no key splits
+    T = [1, 0, 3]
+    pages = np.tile(np.arange(94, dtype=np.int32), (B, 1))
+    g4 = geo(Hq=32, Hkv=8, npages=200)
+    plan, img = bsp.plan_build(g4, B, W, P, T, pages, 8, 24)
+    req, units, _, cta = decode_image(plan, img, with_cta=True)
+    assert plan.layout == 1 and plan.row_blocks == 3 and plan.beams_per_block == 32
+    check_units_cover(plan, req, units, P)
+    check_groups(plan, units, cta)
+    check_fused(plan, req, T)
+    assert list(req[:, 5]) == [1, 1, 0] and plan.tail_requests == 1
+    keys = np.minimum(units[:, 4] * 64, np.asarray(P)[units[:, 0]]) - units[:, 3] * 64
+    want = 8 * (-(-keys // 128) + -(-np.asarray(T)[units[:, 0]] * 32 // 128)) + 4
+    np.testing.assert_array_equal(units[:, 6], want)
+    # the tail kernel finishes a block's tail beyond 4 tiles (128 beams x 5 keys, one row per beam)
+    g1 = geo(Hq=8, Hkv=8, npages=200)
+    plan, img = bsp.plan_build(g1, B, 128, P, [5, 4, 1], pages, 8, 8)
+    req, _, _ = decode_image(plan, img)
+    assert plan.layout == 1 and plan.beams_per_block == 128
+    check_fused(plan, req, [5, 4, 1])
+    assert list(req[:, 5]) == [0, 1, 0]
 
 
 def test_plan_image_single_long_request_is_split(lib):
@@ -303,8 +363,8 @@ def test_prefill_plan_units_and_records(lib, causal):
 
 def test_plan_requests_reads_whole_records(lib):
     """bsp.plan_requests returns the 12-field request records in order (the fused flag of a mixed
-    batch: request 1 has more tail keys per row block than one tile holds)."""
-    g = geo(Hq=32, Hkv=8, D=128, ps=16, npages=4000, dtype="fp16")
+    batch at head_dim 256: request 1 has more tail keys per row block than one 64-key tile holds)."""
+    g = geo(Hq=32, Hkv=8, D=256, ps=16, npages=4000, dtype="fp16")
     B, W = 3, 30
     P = np.array([300, 500, 700], np.int32)
     T = np.array([2, 8, 0], np.int32)
@@ -315,7 +375,7 @@ def test_plan_requests_reads_whole_records(lib):
     np.testing.assert_array_equal(req[:, 2], 1)
     np.testing.assert_array_equal(req[:, 0], P)
     np.testing.assert_array_equal(req[:, 1], T)
-    np.testing.assert_array_equal(req[:, 5], [1, 0, 1])       # 30 x 8 = 240 tail keys > 128
+    np.testing.assert_array_equal(req[:, 5], [1, 0, 1])       # 30 x 2 = 60 <= 64 < 30 x 8 = 240
     np.testing.assert_array_equal(req[:, 10], np.arange(B) * W)
 
 
@@ -397,10 +457,9 @@ def test_planner_random_sweep(lib):
         g = bsp.geometry(G * Hkv, Hkv, D, ps, 100000, "bf16")
         plan, img = bsp.plan_build(g, B, W, P, T, pages, 8, sms)
         req, units, pl, cta = decode_image(plan, img, with_cta=True)
-        assert plan.mma_blocks == (2 if wide_layout(D, W, G) else 1)
-        if plan.mma_blocks == 2:
-            assert plan.row_blocks == 1 and plan.beams_per_block == W
+        assert plan.layout == prompt_layout(D, W, G)
         check_units_cover(plan, req, units, P)
+        check_groups(plan, units, cta)
         check_fused(plan, req, T, head_dim=D)
         assert len(cta) == sms + 1 and cta[0] == 0 and cta[-1] == plan.num_units and (np.diff(cta) >= 0).all()
         assert plan.prefix_ctas <= sms
@@ -409,9 +468,12 @@ def test_planner_random_sweep(lib):
         for c in range(sms):
             seg = cost[cta[c]:cta[c + 1]]
             assert (np.diff(seg) <= 0).all()                   # longest first within a CTA
-        # LPT on the same costs (longest first, each to the least-loaded CTA) bounds the largest load
-        heap = [0] * min(len(cost), sms)
-        for x in sorted(cost, reverse=True):
+        # LPT on the same costs (longest first, each to the least-loaded CTA) bounds the largest load; the
+        # row blocks of a group are dealt together, to the CTA groups
+        grp = plan.row_blocks if plan.layout == 1 else 1
+        gcost = units[units[:, 2] == 0][:, 6].astype(np.int64) if grp > 1 else cost
+        heap = [0] * min(len(gcost), sms // grp)
+        for x in sorted(gcost, reverse=True):
             i = int(np.argmin(heap))
             heap[i] += int(x)
         if len(cost):

@@ -160,14 +160,14 @@ def test_tail_lengths_mixed_and_boundary_crossing():
                                   "qwen3_4b_fp16_d256"])
 def test_prompt_kernel_finishes_short_requests(name):
     """Requests with one prompt partial state and few tail keys per row block are finished by the
-    prompt kernel (tail keys gathered as one extra key tile); the others, in the same batch, by
-    the tail kernel."""
+    prompt kernel (tail keys gathered as extra key tiles); the others, in the same batch, by the tail
+    kernel: the 3000-key prompt split over partial states always, the request with 5 x 30 tail keys
+    only where the kernel gathers one tail tile (the one-set kernel, layout 0)."""
     wl = synth.WORKLOADS[name].scaled(6)
-    # 60 + 5 tail keys x 30 beams exceed a tile; 3000 keys are split over partial states
     case = synth.make_case(wl, 84, full_step=True, device="cuda", prompt_lengths=[100, 128, 60, 3000, 31, 7],
                            tail_lengths=[2, 0, 5, 2, 2, 1])
     step = run_and_check(case)
-    assert step.plan.tail_requests == 2
+    assert step.plan.tail_requests == (2 if step.plan.layout == 0 else 1)
 
 
 def test_empty_sequences():
