@@ -2,8 +2,10 @@
 """Benchmark of one cascade beam decode step: paged KV append + shared-prefix decode attention.
 
 A step is one layer over the whole batch: bsp_append_kv then bsp_decode_attn (prompt kernel on tensor
-cores, tail + log-sum-exp merge kernel). Default workload: the Qwen3-0.6B-shaped layer (batch 64,
-beam 30, 16/8 heads, head_dim 128, bf16, page 32, prompt U{400..600}, tail U{0..4}).
+cores, which also finishes the requests whose tails it gathers; the tail + log-sum-exp merge kernel for
+the others). Default workload: the wide-beam shape (batch 128, beam 96, 16/8 heads, head_dim 128, bf16,
+page 32, prompt U{2800..3200}, tail U{0..3}); the line also carries the other decode workloads
+(config.configs: steps/s and per-kernel times of each) unless --no-configs.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 
@@ -29,7 +31,7 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "beam decode-attn steps/s"
-DEFAULT_WORKLOAD = "qwen3_0p6b_b64_w30"
+DEFAULT_WORKLOAD = "wide_beam_b128_w96"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "prefix_traffic.json")
 
 
@@ -44,6 +46,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--repeats", type=int, default=10, help="timed replays of the K steps (at least 10)")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads of the line")
     return ap.parse_args()
 
 
@@ -139,23 +143,27 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def prefix_source_hash():
+def kernel_source_hash(kernel_file: str):
+    """Hash of the sources a prompt kernel is built from (its own file and the shared device headers)."""
     h = hashlib.sha256()
-    for name in ("bsp_prefix.cu", "bsp_ptx.cuh", "bsp_internal.h"):
+    for name in (kernel_file, "bsp_ptx.cuh", "bsp_internal.h", "bsp_prompt.cuh"):
         with open(os.path.join(ROOT, "beam_search_shared_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per prompt-kernel launch from the committed ncu summary, if the kernel is unchanged."""
+def profiled_traffic(workload: str, kernel: str, kernel_file: str):
+    """DRAM bytes per prompt-kernel launch from the committed ncu record of this workload, if the kernel's
+    sources are unchanged since the capture."""
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
     with open(PROFILE_TRAFFIC) as f:
         d = json.load(f)
-    if d.get("kernel_source_sha") != prefix_source_hash() or d.get("workload") != workload:
-        return None
-    return d.get("dram_bytes_per_launch")
+    for r in d.get("records", []):
+        if (r.get("workload") == workload and r.get("kernel", "").startswith(kernel) and
+                r.get("kernel_source_sha") == kernel_source_hash(kernel_file)):
+            return r.get("dram_bytes_per_launch")
+    return None
 
 
 # ---------------------------------------------------------------- oracle timing (CPU)
@@ -217,6 +225,214 @@ def cpu_model():
 
 
 # ---------------------------------------------------------------- main
+# prompt kernel of each plan layout, and the sources it is built from (for the traffic record's key)
+LAYOUT_KERNEL = {0: ("prefix_attn_kernel", "bsp_prefix.cu"), 1: ("prefix_alt_kernel", "bsp_alt.cu"),
+                 2: ("prefix_wide_kernel", "bsp_wide.cu")}
+# the other decode workloads reported beside the headline, in the same line
+OTHER_CONFIGS = ["qwen3_0p6b_b64_w30", "qwen3_4b_fp16_d128", "qwen3_4b_fp16_d64", "qwen3_4b_fp16_d256"]
+
+
+def graph_of(fn, n):
+    """A CUDA graph of the calls fn(0) .. fn(n - 1)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for j in range(n):
+            fn(j)
+    return g
+
+
+def time_graph(g, reps, stream):
+    """Device time (ms) of each of `reps` replays of graph g, one event pair around each replay (after
+    one untimed replay)."""
+    g.replay()
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1))
+    return out
+
+
+class DecodeBench:
+    """Rotated input sets of one decode workload (each its own workspace and plan) and the timings of
+    a step (append + attention) and of its kernels."""
+
+    def __init__(self, wl, nsets, seed0, dev, **case_kw):
+        from beam_search_shared_gb300 import synth
+        from beam_search_shared_gb300.step import DeviceStep, algorithmic_bytes
+        self.wl = wl
+        self.sets = []
+        for i in range(nsets):
+            case = synth.make_case(wl, seed0 + i, full_step=True, device=dev, **case_kw)
+            st = DeviceStep(case, device=dev)
+            st.make_plan()
+            self.sets.append(st)
+        torch.cuda.synchronize()
+        self.ab = [algorithmic_bytes(s.case, s.fused_requests()) for s in self.sets]
+        self.tail_launch = [s.plan.tail_requests > 0 for s in self.sets]
+        self.layout = int(self.sets[0].plan.layout)
+        self.stream = torch.cuda.current_stream()
+
+    def set_of(self, j):
+        return self.sets[j % len(self.sets)]
+
+    def step(self, j):
+        s = self.set_of(j)
+        s.append()
+        s.attend()
+
+    def warm(self, n):
+        from beam_search_shared_gb300 import bsp
+        for j in range(n):
+            self.step(j)
+        torch.cuda.synchronize()
+        for s in self.sets:
+            assert bsp.read_device_status(s.plan) == (0, 0)
+
+    def launches(self, K):
+        return sum(1 + (s.plan.num_units > 0) + (s.plan.tail_requests > 0) for s in (self.set_of(j) for j in range(K)))
+
+    def kernel_times(self, Kt, reps):
+        """Per-kernel times (us): the append and the attention each as Kt launches back to back in one
+        graph (one event pair around each replay: launch gaps included, no event node between launches),
+        medians over `reps` replays; when a set needs the tail kernel, the attention time is the prompt
+        and tail kernels together, and their split comes from a replay with an event pair around each
+        kernel (an event node delays the next launch: upper bounds)."""
+        from beam_search_shared_gb300 import bsp
+        out = {}
+        g = graph_of(lambda j: self.set_of(j).append(), Kt)
+        out["us_append"] = 1e3 * statistics.median(time_graph(g, reps, self.stream)) / Kt
+        g = graph_of(lambda j: self.set_of(j).attend(), Kt)
+        out["us_attention"] = 1e3 * statistics.median(time_graph(g, reps, self.stream)) / Kt
+        del g
+        if any(self.tail_launch):
+            mk = lambda: torch.cuda.Event(enable_timing=True, external=True)
+            ev = [[mk() for _ in range(3)] for _ in range(Kt)]
+            for e in [e for tri in ev for e in tri]:
+                e.record()
+            torch.cuda.synchronize()
+            g = graph_of(lambda j: self.set_of(j).attend(events=ev[j]), Kt)
+            g.replay()
+            torch.cuda.synchronize()
+            g.replay()
+            torch.cuda.synchronize()
+            t_pre = [ev[i][0].elapsed_time(ev[i][1]) for i in range(Kt)]
+            t_tail = [ev[i][1].elapsed_time(ev[i][2]) for i in range(Kt) if self.tail_launch[i % len(self.sets)]]
+            out["us_prefix_event_pair"] = 1e3 * statistics.mean(t_pre)
+            out["us_tail_event_pair"] = 1e3 * statistics.mean(t_tail)
+            # the prompt kernel alone: the back-to-back attention time less the tail kernel's share
+            out["us_prefix"] = out["us_attention"] * statistics.mean(t_pre) / (statistics.mean(t_pre) +
+                                                                                statistics.mean(t_tail))
+            out["us_tail_merge"] = out["us_attention"] - out["us_prefix"]
+            del g
+        else:
+            out["us_prefix"] = out["us_attention"]
+            out["us_tail_merge"] = None
+        for s in self.sets:
+            assert bsp.read_device_status(s.plan) == (0, 0)
+        return out
+
+    def fractions(self, kt, hbm_gbs):
+        """Algorithmic bytes per kernel launch and the achieved fractions of HBM bandwidth."""
+        ab = self.ab
+        pre = statistics.mean(a["prefix"] for a in ab)
+        app = statistics.mean(a["append"] for a in ab)
+        tl = [a["tail"] for a, t in zip(ab, self.tail_launch) if t]
+        out = {"prefix_bytes": pre, "append_bytes": app,
+               "prefix_gbs": pre / (kt["us_prefix"] / 1e6) / 1e9,
+               "append_gbs": app / (kt["us_append"] / 1e6) / 1e9,
+               "prefix_tflops": statistics.mean(a["prefix_flops"] for a in ab) / (kt["us_prefix"] / 1e6) / 1e12}
+        out["prefix_frac"] = out["prefix_gbs"] / hbm_gbs
+        out["append_frac"] = out["append_gbs"] / hbm_gbs
+        if tl and kt["us_tail_merge"]:
+            out["tail_bytes"] = statistics.mean(tl)
+            out["tail_gbs"] = out["tail_bytes"] / (kt["us_tail_merge"] / 1e6) / 1e9
+            out["tail_frac"] = out["tail_gbs"] / hbm_gbs
+        return out
+
+    def step_graphs(self, K):
+        chunk = min(K, 2000)
+        sizes = [chunk] * (K // chunk) + ([K % chunk] if K % chunk else [])
+        graphs, done = [], 0
+        for n in sizes:
+            graphs.append(graph_of(lambda j, d=done: self.step(d + j), n))
+            done += n
+        for g in graphs:  # untimed warm replay
+            g.replay()
+        torch.cuda.synchronize()
+        return graphs
+
+    def time_steps(self, graphs, reps, world):
+        """ms of each of `reps` timed replays of all K steps (barrier + synchronize on both sides of each),
+        max over ranks."""
+        out = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier(world)
+            torch.cuda.synchronize()
+            e0.record(self.stream)
+            for g in graphs:
+                g.replay()
+            e1.record(self.stream)
+            torch.cuda.synchronize()
+            barrier(world)
+            out.append(reduce_max(e0.elapsed_time(e1), world))
+        return out
+
+    def release(self):
+        self.sets = []
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+
+def config_summary(wl, args, dev, hbm_gbs, reps=5, **case_kw):
+    """Steps/s and per-kernel times of one more decode workload (two rotated input sets)."""
+    b = DecodeBench(wl, 2, 3000, dev, **case_kw)
+    b.warm(max(3, args.warmup))
+    K = min(args.steps, 200)
+    kt = b.kernel_times(min(K, 20), reps)
+    fr = b.fractions(kt, hbm_gbs)
+    graphs = b.step_graphs(K)
+    ms = b.time_steps(graphs, reps, 1)
+    med = statistics.median(ms) / K
+    R = wl.batch * wl.beam_width
+    s0 = b.sets[0].plan
+    out = {"steps_per_s": 1e3 / med, "beam_steps_per_s": R * 1e3 / med, "us_per_step": 1e3 * med,
+           "us_per_step_spread": [1e3 * min(ms) / K, 1e3 * max(ms) / K], "layout": int(s0.layout),
+           "prompt_kernel": LAYOUT_KERNEL[int(s0.layout)][0], "tail_requests": int(s0.tail_requests),
+           "us_prefix": kt["us_prefix"], "us_tail_merge": kt["us_tail_merge"], "us_append": kt["us_append"],
+           "prefix_frac_of_hbm": fr["prefix_frac"], "append_frac_of_hbm": fr["append_frac"],
+           "tail_frac_of_hbm": fr.get("tail_frac"), "prefix_tflops": fr["prefix_tflops"]}
+    del graphs
+    b.release()
+    return out
+
+
+def bucketed_summary(args, dev, reps=5):
+    """The single-allocation decode (one request, one beam, 32/8 heads, fp16, 10368-row allocation, T = 1):
+    a step over the valid prefix against a step that attends every row of the allocation."""
+    from beam_search_shared_gb300 import synth
+    out = {}
+    for P in (10000, 2047):
+        wl = synth.WORKLOADS[f"bucketed_prefix_p{P}"]
+        us = {}
+        for name, kw in (("bound", {}), ("full_allocation", {"prompt_lengths": [10367]})):
+            b = DecodeBench(wl, 2, 4000, dev, **kw)
+            b.warm(max(3, args.warmup))
+            K = 200
+            graphs = b.step_graphs(K)
+            us[name] = 1e3 * statistics.median(b.time_steps(graphs, reps, 1)) / K
+            del graphs
+            b.release()
+        out[f"p{P}"] = {"us_per_step_bound": us["bound"], "us_per_step_full_allocation": us["full_allocation"],
+                        "full_over_bound": us["full_allocation"] / us["bound"]}
+    return out
+
+
 def main():
     args = parse()
     rank, world, local = dist_init(args)
@@ -251,135 +467,46 @@ def main():
         return
 
     from beam_search_shared_gb300 import bsp
-    from beam_search_shared_gb300.step import DeviceStep, algorithmic_bytes
     bsp.load(build_if_missing=True)
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
+    hbm_gbs, bf16_tflops, peak_kind = measured_peaks()
 
-    # ---- inputs: rotated sets, each its own workspace and plan
-    sets = []
-    for i in range(args.sets):
-        case = synth.make_case(wl, 1000 + 97 * rank + i, full_step=True, device=dev)
-        st = DeviceStep(case, device=dev)
-        st.make_plan()
-        sets.append(st)
-    torch.cuda.synchronize()
-    ab = [algorithmic_bytes(s.case, s.fused_requests()) for s in sets]
-    tail_launch = [s.plan.tail_requests > 0 for s in sets]
-    stream = torch.cuda.current_stream()
-
-    def step(i, events=None):
-        s = sets[i % len(sets)]
-        s.append()
-        s.attend(events=events)
-
-    for i in range(max(3, args.warmup)):
-        step(i)
-    torch.cuda.synchronize()
-    for s in sets:
-        assert bsp.read_device_status(s.plan) == (0, 0)
-
-    # ---- per-kernel times: a separate replay of Kt steps with a timing-event pair around each
-    # kernel. An event node delays the launch after it by several microseconds (and keeps the
-    # tail kernel from overlapping the prompt kernel), so these durations are upper bounds and
-    # the step time below is taken from graphs without them.
+    # ---- the headline workload: rotated input sets, each its own workspace and plan
+    hb = DecodeBench(wl, args.sets, 1000 + 97 * rank, dev)
+    hb.warm(max(3, args.warmup))
     K = args.steps
     Kt = min(K, 50)
-    mk = lambda: torch.cuda.Event(enable_timing=True, external=True)
-    ev_a = [[mk() for _ in range(2)] for _ in range(Kt)]
-    ev_d = [[mk() for _ in range(3)] for _ in range(Kt)]
-    for e in [e for pair in ev_a for e in pair] + [e for tri in ev_d for e in tri]:
-        e.record()  # create the events outside capture
-    torch.cuda.synchronize()
-    g_ev = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_ev):
-        for j in range(Kt):
-            s = sets[j % len(sets)]
-            s.append(events=ev_a[j])
-            s.attend(events=ev_d[j])
-    g_ev.replay()  # untimed warm replay
-    torch.cuda.synchronize()
-    g_ev.replay()
-    torch.cuda.synchronize()
-    t_app = [ev_a[i][0].elapsed_time(ev_a[i][1]) for i in range(Kt)]
-    t_pre = [ev_d[i][0].elapsed_time(ev_d[i][1]) for i in range(Kt)]
-    t_tail = [ev_d[i][1].elapsed_time(ev_d[i][2]) for i in range(Kt)]
-    for s in sets:
-        assert bsp.read_device_status(s.plan) == (0, 0)
+    kt = hb.kernel_times(Kt, 5)
+    fr = hb.fractions(kt, hbm_gbs)
 
-    # ---- the prompt kernel's average launch duration without event nodes between launches: a graph
-    # of Kt attention calls back to back (when no request needs the tail kernel, each call is the one
-    # prompt kernel), timed with one event pair around its replay. Re-attending the same inputs
-    # recomputes the same outputs.
-    prefix_loop_ms = None
-    if not any(tail_launch):
-        g_p = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_p):
-            for j in range(Kt):
-                sets[j % len(sets)].attend()
-        g_p.replay()
-        torch.cuda.synchronize()
-        ep0, ep1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ep0.record(stream)
-        g_p.replay()
-        ep1.record(stream)
-        torch.cuda.synchronize()
-        prefix_loop_ms = ep0.elapsed_time(ep1) / Kt
-        for s in sets:
-            assert bsp.read_device_status(s.plan) == (0, 0)
-
-    # ---- timed region: exactly K steps replayed from CUDA graphs without timing nodes
-    chunk = min(K, 2000)
-    sizes = [chunk] * (K // chunk) + ([K % chunk] if K % chunk else [])
-    graphs, done = [], 0
-    for n in sizes:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for j in range(n):
-                s = sets[(done + j) % len(sets)]
-                s.append()
-                s.attend()
-        graphs.append(g)
-        done += n
-    for g in graphs:  # untimed warm replay
-        g.replay()
-    torch.cuda.synchronize()
-    for s in sets:
-        assert bsp.read_device_status(s.plan) == (0, 0)
-    ev_step0 = torch.cuda.Event(enable_timing=True)
-    ev_step1 = torch.cuda.Event(enable_timing=True)
+    # ---- timed region: exactly K steps replayed from CUDA graphs without timing nodes, repeated; the
+    # value is the median repeat
+    graphs = hb.step_graphs(K)
+    reps = max(10, args.repeats)
     with ClockSampler(torch.cuda.current_device()) as clk:
-        barrier(world)
-        torch.cuda.synchronize()
-        ev_step0.record(stream)
-        for g in graphs:
-            g.replay()
-        ev_step1.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-    elapsed_ms = ev_step0.elapsed_time(ev_step1)
-    elapsed_ms = reduce_max(elapsed_ms, world)
-    ms_per_step = elapsed_ms / K
-    value = world * K / (elapsed_ms / 1e3)
+        rep_ms = hb.time_steps(graphs, reps, world)
+    del graphs
+    med_ms = statistics.median(rep_ms)
+    ms_per_step = med_ms / K
+    value = world * K / (med_ms / 1e3)
+    for s in hb.sets:
+        assert bsp.read_device_status(s.plan) == (0, 0)
 
-    hbm_gbs, bf16_tflops, peak_kind = measured_peaks()
-    prefix_bytes = statistics.mean(a["prefix"] for a in ab)
-    prefix_ms = prefix_loop_ms if prefix_loop_ms is not None else statistics.mean(t_pre)
-    achieved = prefix_bytes / (prefix_ms / 1e3) / 1e9
-    # the tail kernel is launched only for plans with requests the prompt kernel does not finish
-    t_tail_l = [t for i, t in enumerate(t_tail) if tail_launch[i % len(sets)]]
-    tail_ab = [a["tail"] for a, tl in zip(ab, tail_launch) if tl]
-    tail_us = 1e3 * statistics.mean(t_tail_l) if t_tail_l else None
-    tail_gbs = statistics.mean(tail_ab) / (tail_us / 1e6) / 1e9 if t_tail_l else None
-    app_gbs = statistics.mean(a["append"] for a in ab) / (statistics.mean(t_app) / 1e3) / 1e9
-    prefix_tflops = statistics.mean(a["prefix_flops"] for a in ab) / (prefix_ms / 1e3) / 1e12
-    traffic = profiled_traffic(wl.name)
+    layout = hb.layout
+    kname, ksrc = LAYOUT_KERNEL[layout]
+    traffic = profiled_traffic(wl.name, kname, ksrc)
+    achieved = fr["prefix_gbs"]
 
     # ---- e2e: host buffers through the C ABI (plan from host arrays, H2D inputs, D2H outputs)
-    e2e = run_e2e(sets[0], args.e2e_steps, world)
-    # ---- RoPE on the append, timed on its own after the step timing (it rewrites the new tokens' K rows)
-    rope_append = measure_rope_append(sets, Kt, hbm_gbs)
-    fp8_append = measure_fp8_append(sets, Kt, hbm_gbs)
+    e2e = run_e2e(hb.sets[0], args.e2e_steps, world)
+    # ---- RoPE and E4M3 appends, timed on their own after the step timing (they rewrite the new tokens' rows)
+    rope_append = measure_rope_append(hb.sets, Kt, hbm_gbs)
+    fp8_append = measure_fp8_append(hb.sets, Kt, hbm_gbs)
+    launches = hb.launches(K)
+    step_bytes = fr["prefix_bytes"] + statistics.mean(a["tail"] for a in hb.ab)
+    prefix_units = int(hb.sets[0].plan.num_units)
+    hb.release()
 
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
@@ -390,29 +517,35 @@ def main():
                    "page_size": wl.page_size, "prompt": f"U{{{wl.prompt[0]}..{wl.prompt[1]}}}",
                    "tail": f"U{{{wl.tail[0]}..{wl.tail[1]}}}", "parallelism": f"dp{world} (independent batches)",
                    "beam_steps_per_s": value * R,
-                   "l2": f"inputs larger than L2: {len(sets)} rotated input sets, each step moving "
-                         f"{(prefix_bytes + statistics.mean(a['tail'] for a in ab)) / 1e6:.0f} MB",
-                   "us_append": 1e3 * statistics.mean(t_app), "us_prefix": 1e3 * prefix_ms,
-                   "us_prefix_event_pair": 1e3 * statistics.mean(t_pre),
-                   "us_tail_merge": tail_us,
-                   "gbs_append": app_gbs, "gbs_tail_merge": tail_gbs, "prefix_tflops": prefix_tflops,
-                   "prefix_units": sets[0].plan.num_units},
+                   "l2": f"inputs larger than L2: {len(hb.ab)} rotated input sets, each step moving "
+                         f"{step_bytes / 1e6:.0f} MB",
+                   "repeats": reps, "ms_per_step_spread": [min(rep_ms) / K, max(rep_ms) / K],
+                   "prompt_kernel": kname, "layout": layout,
+                   "us_append": kt["us_append"], "us_prefix": kt["us_prefix"], "us_attention": kt["us_attention"],
+                   "us_prefix_event_pair": kt.get("us_prefix_event_pair"), "us_tail_merge": kt["us_tail_merge"],
+                   "gbs_append": fr["append_gbs"], "append_frac_of_hbm": fr["append_frac"],
+                   "gbs_tail_merge": fr.get("tail_gbs"), "tail_frac_of_hbm": fr.get("tail_frac"),
+                   "prefix_tflops": fr["prefix_tflops"], "prefix_units": prefix_units},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                      "frac": achieved / hbm_gbs, "traffic": traffic,
-                     "kernel": "prefix_attn_kernel", "peak_kind": peak_kind,
-                     "algorithmic_bytes_per_launch": prefix_bytes},
+                     "kernel": kname, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": fr["prefix_bytes"]},
         "e2e": e2e,
         "rope_append": rope_append,
         "fp8_append": fp8_append,
-        "gpu_launches": sum(1 + (s.plan.num_units > 0) + (s.plan.tail_requests > 0)
-                            for s in (sets[j % len(sets)] for j in range(K))),
-        "timing": "value: CUDA-graph replay of exactly K steps without timing nodes; us_prefix (and the roofline): "
-                  f"one event pair around a graph of {Kt} back-to-back prompt-kernel launches (launch gaps included), "
-                  "when no request needs the tail kernel; other per-kernel times: a separate replay of "
-                  f"{Kt} steps with an event pair around each kernel (upper bounds: an event node delays the next "
-                  "launch by several microseconds)",
+        "gpu_launches": launches * reps,
+        "timing": f"value: median of {reps} repeats of a CUDA-graph replay of exactly K steps without timing "
+                  f"nodes (spread in config.ms_per_step_spread); us_prefix (and the roofline), us_append: one event "
+                  f"pair around a graph of {Kt} back-to-back launches (launch gaps included), median of 5 replays; "
+                  "a tail-kernel share, when present, from a replay with an event pair around each kernel",
         "clocks": clk.result,
     }
+    if rank == 0 and world == 1 and not args.no_configs:
+        others = {}
+        for name in OTHER_CONFIGS:
+            others[name] = config_summary(synth.WORKLOADS[name], args, dev, hbm_gbs)
+        others["bucketed_prefix"] = bucketed_summary(args, dev)
+        line["configs"] = others
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         timer = OracleTimer(synth.make_case(wl, 1000, full_step=True, device="cpu"))
         n = timer.rows_for(args.cpu_seconds)
