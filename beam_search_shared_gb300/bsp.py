@@ -69,7 +69,7 @@ _lib = None
 EXPORTS = ["bsp_status_string", "bsp_bucket_rows", "bsp_workspace_size", "bsp_plan_build", "bsp_plan",
            "bsp_append_kv", "bsp_decode_attn", "bsp_read_device_status", "bsp_decode_attn_noalloc",
            "bsp_plan_prefill_build", "bsp_plan_prefill", "bsp_prefill_attn", "bsp_rope_cos_sin",
-           "bsp_rope_append_kv", "bsp_append_kv_fp8", "bsp_rope_append_kv_fp8"]
+           "bsp_rope_append_kv", "bsp_append_kv_fp8", "bsp_rope_append_kv_fp8", "bsp_plan_update_tails"]
 NOALLOC_SCRATCH_MIB = 32
 
 
@@ -104,6 +104,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.bsp_plan_build.argtypes = [P(Geometry), i32, i32, vp, vp, vp, i32, i32, i32, vp, sz, P(Plan)]
     lib.bsp_plan.restype = i32
     lib.bsp_plan.argtypes = [P(Geometry), i32, i32, vp, vp, vp, i32, i32, vp, sz, vp, sz, vp, P(Plan)]
+    lib.bsp_plan_update_tails.restype = i32
+    lib.bsp_plan_update_tails.argtypes = [P(Plan), vp, vp]
     lib.bsp_append_kv.restype = i32
     lib.bsp_append_kv.argtypes = [P(Plan), vp, vp, i64, vp, i32, vp, vp, vp, vp]
     lib.bsp_decode_attn.restype = i32
@@ -259,6 +261,15 @@ def plan(geo: Geometry, batch, beam_width, prefix_len, tail_len, prefix_pages, m
         ctypes.byref(geo), int(batch), int(beam_width), _ptr(pl), _ptr(tl), _ptr(pp), pp.shape[1], int(max_tail),
         _dptr(ws.device), ws.device.numel(), _dptr(ws.host), ws.host.numel(), _stream(stream), ctypes.byref(out)))
     return out
+
+
+def plan_update_tails(plan_: Plan, tail_len, stream=None) -> Plan:
+    """bsp_plan_update_tails: new tail lengths for a current decode plan, in place (no sync)."""
+    tl = _i32(tail_len)
+    if tl.shape[0] != plan_.batch:
+        raise ValueError(f"tail_len has {tl.shape[0]} entries for a batch of {plan_.batch}")
+    _check("bsp_plan_update_tails", load().bsp_plan_update_tails(ctypes.byref(plan_), _ptr(tl), _stream(stream)))
+    return plan_
 
 
 def _events(events, n):

@@ -32,6 +32,7 @@ struct StagingHeader {
     uint64_t generation;     // latest plan staged through this buffer
     uint64_t echoed[2];      // generation whose image copy from slot i has executed (written by the stream)
     uint64_t ws_device;      // device workspace this buffer is paired with
+    uint64_t slot_bytes;     // bytes of each of the two image slots that follow the header
 };
 static_assert(sizeof(StagingHeader) <= kStagingHeaderBytes, "staging header");
 
@@ -197,6 +198,17 @@ struct PrefillSpec {
     bool causal;
 };
 
+// Whether the prompt kernel of plan layout `layout` finishes a decode request: its prompt is one partial
+// state (nsplit == 1) and the tail keys of one unit's beams (wblk of them; all W for the wide kernel) fit
+// the kernel's tail tiles: up to 4 tiles of 128 keys (layouts 1 and 2), one prompt tile (layout 0).
+int64_t request_tail_tiles(int layout, int head_dim, int wblk, int32_t tail) {
+    return ceil_div(static_cast<int64_t>(tail) * wblk, layout ? 128 : prefix_tile_keys(head_dim));
+}
+bool request_fused(int layout, int head_dim, int wblk, int32_t nsplit, int32_t tail) {
+    return nsplit == 1 && request_tail_tiles(layout, head_dim, wblk, tail) <=
+                              (layout == 1 ? kAltMaxTailTiles : layout == 2 ? kWideMaxTailTiles : 1);
+}
+
 // The plan image of a decode step (pf == nullptr: prefix_len / tail_len per request, beam_width rows
 // each) or of a prefill (pf: the prompt tokens are the rows, the keys are the cached rows and the
 // prompt, no tail, no key splits, every request finished by the prompt kernel).
@@ -317,20 +329,9 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
         if (parts <= static_cast<int64_t>(batch) + kExtraParts) break;
         chunk *= 2;
     }
-    // a request is finished by the prompt kernel when its prompt is one partial state and its tail keys fit
-    // the kernel's tail tiles: one extra key tile per row block (W_blk beams), or for a wide unit (all W
-    // beams) up to kWideMaxTailTiles tiles of 128 keys
     const int tk = prefix_tile_keys(geo->head_dim);
-    // a request is finished by the prompt kernel when its prompt is one partial state and the tail keys
-    // of a unit's beams (W_blk of them; all W for the wide kernel) fit the kernel's tail tiles: up to 4
-    // tiles of 128 keys (layouts 1 and 2), one prompt tile (layout 0)
-    auto tail_tiles = [&](int b) -> int64_t {
-        return ceil_div(static_cast<int64_t>(tail_len[b]) * wblk, layout ? 128 : tk);
-    };
-    auto fused = [&](int b) -> bool {
-        return nsplit[b] == 1 &&
-               tail_tiles(b) <= (layout == 1 ? kAltMaxTailTiles : layout == 2 ? kWideMaxTailTiles : 1);
-    };
+    auto tail_tiles = [&](int b) -> int64_t { return request_tail_tiles(layout, geo->head_dim, wblk, tail_len[b]); };
+    auto fused = [&](int b) -> bool { return request_fused(layout, geo->head_dim, wblk, nsplit[b], tail_len[b]); };
     // the plan tiles a unit reads: a causal prefill block stops at its last token's keys
     auto unit_end_tile = [&](int b, int rb, int32_t t1) -> int32_t {
         if (causal[b] < 0) return t1;
@@ -674,6 +675,36 @@ bsp_status bsp_plan_prefill_build(const bsp_geometry* geo, int32_t batch, const 
 }  // extern "C"
 
 namespace {
+// The staging slot of generation `gen` (slot gen & 1), once the stream has executed the copy that last
+// read it (generation gen - 2, echoed back into the header); waits up to 10 s.
+bsp_status acquire_slot(StagingHeader* hdr, uint64_t gen, cudaStream_t s, uint8_t** slot_ptr) {
+    const int slot = static_cast<int>(gen & 1);
+    *slot_ptr = reinterpret_cast<uint8_t*>(hdr) + kStagingHeaderBytes + slot * hdr->slot_bytes;
+    if (gen >= 3) {
+        const auto t0 = std::chrono::steady_clock::now();
+        while (reinterpret_cast<volatile uint64_t*>(hdr->echoed)[slot] < gen - 2) {
+            cudaError_t q = cudaStreamQuery(s);
+            if (q != cudaSuccess && q != cudaErrorNotReady) return BSP_ERR_CUDA;
+            if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(10)) return BSP_ERR_CUDA;
+            std::this_thread::yield();
+        }
+    }
+    return BSP_OK;
+}
+
+// Stamps generation `gen` into the image in `slot_ptr`, enqueues the copy of its first `bytes` bytes into
+// the device workspace and the echo of the generation back into the header, and makes `gen` current.
+bsp_status enqueue_image(StagingHeader* hdr, uint64_t gen, uint8_t* slot_ptr, size_t bytes, void* ws_device,
+                         cudaStream_t s) {
+    std::memcpy(slot_ptr, &gen, sizeof gen);  // image header: generation
+    uint8_t* dimg = static_cast<uint8_t*>(ws_device) + kStatusBytes;
+    if (cudaMemcpyAsync(dimg, slot_ptr, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return BSP_ERR_CUDA;
+    if (cudaMemcpyAsync(&hdr->echoed[gen & 1], dimg, sizeof(uint64_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    hdr->generation = gen;
+    return BSP_OK;
+}
+
 // Builds a plan into a free slot of the pinned staging buffer (build(sms, slot, bytes, plan)) and
 // enqueues its copy into the device workspace with the generation echo.
 template <typename Build>
@@ -697,29 +728,16 @@ bsp_status stage_plan(void* ws_device, size_t ws_device_bytes, void* ws_host, si
         hdr->ws_device = reinterpret_cast<uint64_t>(ws_device);
     }
     const uint64_t gen = hdr->generation + 1;
-    const int slot = static_cast<int>(gen & 1);
-    const size_t slot_bytes = (ws_host_bytes - kStagingHeaderBytes) / 2 / kAlign * kAlign;
-    uint8_t* slot_ptr = static_cast<uint8_t*>(ws_host) + kStagingHeaderBytes + slot * slot_bytes;
-    if (gen >= 3) {
-        // the copy that last read this slot (generation gen-2) must have executed
-        const auto t0 = std::chrono::steady_clock::now();
-        while (reinterpret_cast<volatile uint64_t*>(hdr->echoed)[slot] < gen - 2) {
-            cudaError_t q = cudaStreamQuery(s);
-            if (q != cudaSuccess && q != cudaErrorNotReady) return BSP_ERR_CUDA;
-            if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(10)) return BSP_ERR_CUDA;
-            std::this_thread::yield();
-        }
-    }
+    hdr->slot_bytes = (ws_host_bytes - kStagingHeaderBytes) / 2 / kAlign * kAlign;
+    uint8_t* slot_ptr = nullptr;
+    bsp_status st = acquire_slot(hdr, gen, s, &slot_ptr);
+    if (st != BSP_OK) return st;
     bsp_plan_t plan;
-    bsp_status st = build(sms, slot_ptr, slot_bytes, &plan);
+    st = build(sms, slot_ptr, hdr->slot_bytes, &plan);
     if (st != BSP_OK) return st;
     if (plan.device_bytes_used > ws_device_bytes) return BSP_ERR_CAPACITY;
-    std::memcpy(slot_ptr, &gen, sizeof gen);  // image header: generation
-    uint8_t* dimg = static_cast<uint8_t*>(ws_device) + kStatusBytes;
-    if (cudaMemcpyAsync(dimg, slot_ptr, plan.image_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return BSP_ERR_CUDA;
-    if (cudaMemcpyAsync(&hdr->echoed[slot], dimg, sizeof(uint64_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return BSP_ERR_CUDA;
-    hdr->generation = gen;
+    st = enqueue_image(hdr, gen, slot_ptr, plan.image_bytes, ws_device, s);
+    if (st != BSP_OK) return st;
     plan.generation = gen;
     plan.ws_device = ws_device;
     plan.ws_device_bytes = ws_device_bytes;
@@ -751,6 +769,45 @@ bsp_status bsp_plan_prefill(const bsp_geometry* geo, int32_t batch, const int32_
                           return bsp_plan_prefill_build(geo, batch, cached_len, prompt_len, pages, pages_stride,
                                                         causal, sms, img, bytes, p);
                       });
+}
+
+bsp_status bsp_plan_update_tails(bsp_plan_t* plan, const int32_t* tail_len, void* stream) {
+    bsp_status st = check_plan(plan);
+    if (st != BSP_OK) return st;
+    if (plan->kind != 0) return BSP_ERR_INVALID_ARG;
+    const int B = plan->batch;
+    if (B > 0 && !tail_len) return BSP_ERR_INVALID_ARG;
+    for (int b = 0; b < B; ++b) {
+        if (tail_len[b] < 0) return BSP_ERR_INVALID_ARG;
+        if (tail_len[b] > plan->max_tail) return BSP_ERR_CAPACITY;
+    }
+    StagingHeader* hdr = static_cast<StagingHeader*>(plan->ws_host);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the current image (header and request records) is in the current generation's slot
+    const uint8_t* cur = reinterpret_cast<const uint8_t*>(hdr) + kStagingHeaderBytes + (hdr->generation & 1) * hdr->slot_bytes;
+    const uint64_t gen = hdr->generation + 1;
+    uint8_t* slot_ptr = nullptr;
+    st = acquire_slot(hdr, gen, s, &slot_ptr);
+    if (st != BSP_OK) return st;
+    const size_t bytes = plan->off_units - kStatusBytes;  // the image header and the request records
+    std::memcpy(slot_ptr, cur, bytes);
+    int32_t* req = reinterpret_cast<int32_t*>(slot_ptr + (plan->off_req - kStatusBytes));
+    int32_t max_t = 0, max_total = 0, tail_requests = 0;
+    for (int b = 0; b < B; ++b) {
+        int32_t* r = req + static_cast<size_t>(b) * kReqFields;
+        r[kReqTail] = tail_len[b];
+        r[kReqFused] = request_fused(plan->layout, plan->geo.head_dim, plan->beams_per_block, r[kReqSplits], tail_len[b]);
+        tail_requests += !r[kReqFused];
+        max_t = std::max(max_t, tail_len[b]);
+        max_total = std::max(max_total, r[kReqPrefix] + tail_len[b]);
+    }
+    st = enqueue_image(hdr, gen, slot_ptr, bytes, plan->ws_device, s);
+    if (st != BSP_OK) return st;
+    plan->generation = gen;
+    plan->max_tail_len = max_t;
+    plan->max_total_len = max_total;
+    plan->tail_requests = tail_requests;
+    return BSP_OK;
 }
 
 bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, const void* v_new, int64_t src_row_stride,

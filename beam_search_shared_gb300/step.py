@@ -50,6 +50,11 @@ class DeviceStep:
                                  self.max_tail, stream=stream)
         return self.plan
 
+    def update_tails(self, tail_len, stream=None):
+        """Per-step update of the current plan: new tail lengths, same prompts and pages."""
+        bsp.plan_update_tails(self.plan, tail_len, stream=stream)
+        return self.plan
+
     def fused_requests(self) -> np.ndarray:
         """Which requests the prompt kernel finishes, from a host-only plan of the same inputs."""
         c = self.case

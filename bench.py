@@ -399,6 +399,8 @@ def config_summary(wl, args, dev, hbm_gbs, reps=5, **case_kw):
     graphs = b.step_graphs(K)
     ms = b.time_steps(graphs, reps, 1)
     med = statistics.median(ms) / K
+    del graphs
+    e2e = run_e2e(b.sets[0], args.e2e_steps, 1)
     R = wl.batch * wl.beam_width
     s0 = b.sets[0].plan
     out = {"steps_per_s": 1e3 / med, "beam_steps_per_s": R * 1e3 / med, "us_per_step": 1e3 * med,
@@ -406,8 +408,9 @@ def config_summary(wl, args, dev, hbm_gbs, reps=5, **case_kw):
            "prompt_kernel": LAYOUT_KERNEL[int(s0.layout)][0], "tail_requests": int(s0.tail_requests),
            "us_prefix": kt["us_prefix"], "us_tail_merge": kt["us_tail_merge"], "us_append": kt["us_append"],
            "prefix_frac_of_hbm": fr["prefix_frac"], "append_frac_of_hbm": fr["append_frac"],
-           "tail_frac_of_hbm": fr.get("tail_frac"), "prefix_tflops": fr["prefix_tflops"]}
-    del graphs
+           "tail_frac_of_hbm": fr.get("tail_frac"), "prefix_tflops": fr["prefix_tflops"],
+           "e2e_steps_per_s": e2e["value"], "us_plan_host": e2e["us_plan_host"],
+           "us_plan_full_host": e2e["us_plan_full_host"]}
     b.release()
     return out
 
@@ -654,8 +657,22 @@ def measure_fp8_append(sets, Kt, hbm_gbs):
             "timing": f"one event pair around {Kt} back-to-back launches (launch gaps included)"}
 
 
+def host_us(fn, n=200):
+    """Median host time (us) of fn() over n calls, the stream drained between calls."""
+    ts = []
+    for _ in range(n):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        fn()
+        ts.append(time.perf_counter() - t0)
+    torch.cuda.synchronize()
+    return 1e6 * statistics.median(ts)
+
+
 def run_e2e(st, steps, world):
-    """Steps through the public API from pinned host buffers: plan + H2D inputs + append + attention + D2H."""
+    """Steps through the public API from pinned host buffers: per-step plan update (the batch's plan is
+    dealt once, before the loop) + H2D inputs + append + attention + D2H outputs. Also the host time of
+    a per-step plan update and of a full plan."""
     from beam_search_shared_gb300 import bsp
     c = st.case
     wl = c.workload
@@ -669,12 +686,18 @@ def run_e2e(st, steps, world):
     d_q, d_kn, d_vn = torch.empty_like(st.q), torch.empty_like(st.k_new), torch.empty_like(st.v_new)
     d_loc, d_bp, d_ci = torch.empty_like(st.out_cache_loc), torch.empty_like(st.beam_pages), torch.empty_like(
         st.cache_indirection)
+    tails = np.ascontiguousarray(c.tail_len, np.int32)
+    full_plan = lambda: st.ws.plan(st.geo, wl.batch, wl.beam_width, c.prefix_len, c.tail_len, c.prefix_pages,
+                                   st.max_tail)
+    us_plan_full = host_us(full_plan)
+    plan = full_plan()
+    us_plan_host = host_us(lambda: bsp.plan_update_tails(plan, tails))
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_loc, h_bp, h_ci))
-    h2d += int(st.plan.image_bytes)
+    h2d += 64 + 48 * wl.batch  # the update's image header and request records
     d2h = h_o.numel() * h_o.element_size() + h_lse.numel() * 4
 
     def one():
-        plan = st.ws.plan(st.geo, wl.batch, wl.beam_width, c.prefix_len, c.tail_len, c.prefix_pages, st.max_tail)
+        bsp.plan_update_tails(plan, tails)
         for d, h in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_loc, h_loc), (d_bp, h_bp), (d_ci, h_ci)):
             d.copy_(h, non_blocking=True)
         bsp.append_kv(plan, d_kn, d_vn, d_loc, st.k_pool, st.v_pool)
@@ -685,16 +708,20 @@ def run_e2e(st, steps, world):
     for _ in range(3):
         one()
     torch.cuda.synchronize()
+    assert bsp.read_device_status(plan) == (0, 0)
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(steps):
         one()
     torch.cuda.synchronize()
     dt = reduce_max(time.perf_counter() - t0, world)
+    assert bsp.read_device_status(plan) == (0, 0)
     st.make_plan()  # leave the set's own plan current
     torch.cuda.synchronize()
     return {"value": world * steps / dt, "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": steps}
+            "d2h_bytes_per_step": int(d2h), "steps": steps, "us_plan_host": us_plan_host,
+            "us_plan_full_host": us_plan_full,
+            "plan": "dealt once for the batch's prompts before the loop; bsp_plan_update_tails every step"}
 
 
 # ---------------------------------------------------------------- prefill over the cached prefix

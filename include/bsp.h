@@ -221,6 +221,32 @@ BSP_API bsp_status bsp_plan(const bsp_geometry* geo, int32_t batch, int32_t beam
                     size_t ws_host_bytes, void* stream, bsp_plan_t* plan_out);
 
 /*
+ * Per-step update of a staged decode plan: the same batch, beam width, prompt
+ * lengths and prompt pages, new tail lengths. Beam search keeps a request's
+ * prompt fixed while its tail grows by one position a step, so the work units,
+ * the CTA table and the prompt page list of the plan (the dealing, which costs
+ * the planner O(units log units) and more) stay as they are; only the request
+ * records change: T_b, and whether the prompt kernel or the tail kernel
+ * finishes request b (the same rule bsp_plan applies). O(batch) host work and
+ * one copy of the image header and request records (64 + 48 * batch bytes)
+ * through the next staging slot, with the slot protocol of bsp_plan (TensorRT-
+ * LLM PR #21738: per-step host planning with pinned staging and no stream
+ * synchronisation). The units stay balanced for the tails the plan was built
+ * with; re-plan with bsp_plan when the batch or a prompt changes.
+ *   plan       in/out: a current decode plan of its workspace (from bsp_plan or
+ *              an earlier update); on success its generation, max_tail_len,
+ *              max_total_len and tail_requests describe the new step and
+ *              every earlier plan of the workspace is stale
+ *   tail_len   host [batch]: T_b in [0, plan->max_tail] (BSP_ERR_CAPACITY
+ *              above it, BSP_ERR_INVALID_ARG below 0); nothing is changed on
+ *              error
+ *   stream     the stream of the step's launches (the copy is enqueued on it)
+ * A CUDA graph captured with BSP_FLAG_GRAPH from a plan of this workspace
+ * replays correctly after updates: the header it checks does not change.
+ */
+BSP_API bsp_status bsp_plan_update_tails(bsp_plan_t* plan, const int32_t* tail_len, void* stream);
+
+/*
  * Paged KV append: for every new token i < n and kv head h, copies the
  * head_dim elements of k_new / v_new row i, head h to
  * pool[out_cache_loc[i] / page_size][h][out_cache_loc[i] % page_size][:],
