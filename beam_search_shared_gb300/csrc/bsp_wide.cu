@@ -520,10 +520,8 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                             }
                         }
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(sa[c]));
-                            mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(sb[c]));
-                        }
+                        for (int c = 0; c < 32; ++c)
+                            mp[c & 7] = fmax3(mp[c & 7], __uint_as_float(sa[c]), __uint_as_float(sb[c]));
                     }
                     const float mxr = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
@@ -581,12 +579,12 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         }
 #pragma unroll
                         for (int c = 0; c < 32; c += 2) {
-                            const float p0 = exp2f(fmaf(__uint_as_float(sa[c]), sl2, nm));
-                            const float p1 = exp2f(fmaf(__uint_as_float(sa[c + 1]), sl2, nm));
-                            const float p2 = exp2f(fmaf(__uint_as_float(sb[c]), sl2, nm));
-                            const float p3 = exp2f(fmaf(__uint_as_float(sb[c + 1]), sl2, nm));
-                            rsp[(c >> 1) & 1] += p0 + p1;
-                            rsp[2 + ((c >> 1) & 1)] += p2 + p3;
+                            float e0, e1, e2, e3;
+                            fma2_bc(e0, e1, __uint_as_float(sa[c]), __uint_as_float(sa[c + 1]), sl2, nm);
+                            fma2_bc(e2, e3, __uint_as_float(sb[c]), __uint_as_float(sb[c + 1]), sl2, nm);
+                            const float p0 = exp2f(e0), p1 = exp2f(e1), p2 = exp2f(e2), p3 = exp2f(e3);
+                            add2_acc(rsp[0], rsp[1], p0, p1);
+                            add2_acc(rsp[2], rsp[3], p2, p3);
                             pk[c >> 1] = pack2<BF16>(p0, p1);
                             pk[16 + (c >> 1)] = pack2<BF16>(p2, p3);
                         }
