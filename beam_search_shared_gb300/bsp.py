@@ -44,7 +44,8 @@ class BspError(RuntimeError):
 
 class Geometry(ctypes.Structure):
     _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32)]
 
 
 class Plan(ctypes.Structure):
@@ -69,7 +70,8 @@ _lib = None
 EXPORTS = ["bsp_status_string", "bsp_bucket_rows", "bsp_workspace_size", "bsp_plan_build", "bsp_plan",
            "bsp_append_kv", "bsp_decode_attn", "bsp_read_device_status", "bsp_decode_attn_noalloc",
            "bsp_plan_prefill_build", "bsp_plan_prefill", "bsp_prefill_attn", "bsp_rope_cos_sin",
-           "bsp_rope_append_kv", "bsp_append_kv_fp8", "bsp_rope_append_kv_fp8", "bsp_plan_update_tails"]
+           "bsp_rope_append_kv", "bsp_append_kv_fp8", "bsp_rope_append_kv_fp8", "bsp_plan_update_tails",
+           "bsp_decode_attn_fp8"]
 NOALLOC_SCRATCH_MIB = 32
 
 
@@ -110,6 +112,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.bsp_append_kv.argtypes = [P(Plan), vp, vp, i64, vp, i32, vp, vp, vp, vp]
     lib.bsp_decode_attn.restype = i32
     lib.bsp_decode_attn.argtypes = [P(Plan), vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, i32, vp, vp, vp, vp]
+    f32 = ctypes.c_float
+    lib.bsp_decode_attn_fp8.restype = i32
+    lib.bsp_decode_attn_fp8.argtypes = [P(Plan), vp, vp, vp, vp, i32, vp, i32, f32, f32, f32, i32, vp, vp, vp, vp]
     lib.bsp_plan_prefill_build.restype = i32
     lib.bsp_plan_prefill_build.argtypes = [P(Geometry), i32, vp, vp, vp, i32, i32, i32, vp, sz, P(Plan)]
     lib.bsp_plan_prefill.restype = i32
@@ -143,9 +148,13 @@ def status_string(status: int) -> str:
     return load().bsp_status_string(int(status)).decode()
 
 
-def geometry(num_q_heads, num_kv_heads, head_dim, page_size, num_pages, dtype) -> Geometry:
+KV_DTYPE_SAME, KV_DTYPE_E4M3 = 0, 1
+
+
+def geometry(num_q_heads, num_kv_heads, head_dim, page_size, num_pages, dtype, kv_dtype: int = KV_DTYPE_SAME) -> Geometry:
+    """kv_dtype: KV_DTYPE_SAME (the pools hold `dtype`) or KV_DTYPE_E4M3 (one-byte E4M3 pools)."""
     return Geometry(int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size), int(num_pages),
-                    DTYPES[dtype])
+                    DTYPES[dtype], int(kv_dtype))
 
 
 def bucket_rows(valid_rows: int, capacity: int) -> int:
@@ -395,6 +404,21 @@ def read_device_status(plan_: Plan, clear: bool = True, stream=None):
     flags = ctypes.c_int32(0)
     st = load().bsp_read_device_status(ctypes.byref(plan_), _stream(stream), int(bool(clear)), ctypes.byref(flags))
     return int(st), int(flags.value)
+
+
+def decode_attn_fp8(plan_: Plan, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                    beam_pages: Optional[torch.Tensor], cache_indirection: Optional[torch.Tensor], softmax_scale: float,
+                    k_scale: float, v_scale: float, o: torch.Tensor, lse: torch.Tensor, flags: int = 0, events=None,
+                    stream=None):
+    """bsp_decode_attn_fp8: decode attention over uint8 E4M3 pools (key = code x k_scale, value = code x
+    v_scale); writes o [R,Hq,D] in the q dtype and lse [R,Hq] (fp32)."""
+    bps = int(beam_pages.shape[-1]) if beam_pages is not None else 0
+    max_seq = int(cache_indirection.shape[-1]) if cache_indirection is not None else 0
+    ev = _events(events, 3)
+    _check("bsp_decode_attn_fp8", load().bsp_decode_attn_fp8(
+        ctypes.byref(plan_), _dptr(q), _dptr(k_pool), _dptr(v_pool), _dptr(beam_pages), bps,
+        _dptr(cache_indirection), max_seq, float(softmax_scale), float(k_scale), float(v_scale), int(flags),
+        _dptr(o), _dptr(lse), ev, _stream(stream)))
 
 
 def decode_attn_noalloc(geo: Geometry, batch, beam_width, prefix_len, tail_len, prefix_pages, max_tail,

@@ -48,6 +48,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 bsp_status check_geometry(const bsp_geometry* geo) {
     if (!geo) return BSP_ERR_INVALID_ARG;
     if (geo->dtype != BSP_DTYPE_BF16 && geo->dtype != BSP_DTYPE_FP16) return BSP_ERR_UNSUPPORTED;
+    if (geo->kv_dtype != BSP_KV_DTYPE_SAME && geo->kv_dtype != BSP_KV_DTYPE_E4M3) return BSP_ERR_UNSUPPORTED;
     if (geo->head_dim != 64 && geo->head_dim != 128 && geo->head_dim != 256) return BSP_ERR_UNSUPPORTED;
     if (geo->num_q_heads <= 0 || geo->num_kv_heads <= 0 || geo->num_pages <= 0) return BSP_ERR_INVALID_ARG;
     if (geo->num_q_heads % geo->num_kv_heads != 0) return BSP_ERR_UNSUPPORTED;
@@ -120,15 +121,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+// A tiled tensor map of 16-bit elements with 128-byte swizzle (the MMA operand layout), or with
+// e4m3 = true of one-byte elements without swizzle (E4M3 tiles that the kernel widens itself).
 bool encode_map(CUtensorMap* m, int dtype, int rank, const void* base, const cuuint64_t* dims,
-                const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+                const cuuint64_t* strides_bytes, const cuuint32_t* box, bool e4m3 = false) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(m, dtype == BSP_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                     static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides_bytes, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUtensorMapDataType t = e4m3                     ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                  : dtype == BSP_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = enc(m, t, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides_bytes, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, e4m3 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -176,6 +181,8 @@ bsp_status bsp_workspace_size(const bsp_geometry* geo, int32_t max_batch, int32_
     const int G = geo->num_q_heads / geo->num_kv_heads;
     int nrb, wblk;
     row_blocks(max_beam, G, &nrb, &wblk);
+    // E4M3 pools: row blocks of at most 4 * floor(32 / G) beams (the planner's bound for those kernels)
+    if (geo->kv_dtype == BSP_KV_DTYPE_E4M3) nrb = std::max(nrb, static_cast<int>(ceil_div(max_beam, 4 * (32 / G))));
     const int64_t parts_cap = static_cast<int64_t>(max_batch) + kExtraParts;
     const int64_t units_max = parts_cap * geo->num_kv_heads * nrb;
     const size_t image = kImageHeaderBytes + static_cast<size_t>(max_batch) * kReqFields * 4 +
@@ -293,7 +300,24 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     // once), and any other to the alternating-tile kernel (layout 1), whose row blocks of one (request,
     // kv head, key split) are dealt to `group` neighbouring CTAs at the same place of their lists.
     int layout = 0;
-    if (!pf && geo->head_dim <= 128 && prefix_quad_beams(geo->head_dim, wblk, G) == 0) {
+    const bool e4m3 = geo->kv_dtype == BSP_KV_DTYPE_E4M3;
+    if (e4m3) {
+        // E4M3 pools: the wide and alternating-tile kernels widen the tiles (head_dim <= 128, decode); a
+        // row block holds at most 4 * floor(32 / G) beams, so that its rows fit the quadrant layout
+        if (pf || geo->head_dim > 128) return BSP_ERR_UNSUPPORTED;
+        if (wide_quad_beams(geo->head_dim, beam_width, G) > 0) {
+            layout = 2;
+            nrb = 1;
+            wblk = beam_width;
+        } else {
+            if (alt_quad_beams(geo->head_dim, wblk, G) == 0) {
+                const int wmax = 4 * (32 / G);
+                nrb = static_cast<int>(ceil_div(beam_width, wmax));
+                wblk = static_cast<int>(ceil_div(beam_width, nrb));
+            }
+            layout = 1;
+        }
+    } else if (!pf && geo->head_dim <= 128 && prefix_quad_beams(geo->head_dim, wblk, G) == 0) {
         if (wide_quad_beams(geo->head_dim, beam_width, G) > 0) {
             layout = 2;
             nrb = 1;
@@ -815,7 +839,7 @@ bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, const void* 
                          void* const* events, void* stream) {
     bsp_status st = check_plan(plan);
     if (st != BSP_OK) return st;
-    if (n < 0) return BSP_ERR_INVALID_ARG;
+    if (n < 0 || plan->geo.kv_dtype != BSP_KV_DTYPE_SAME) return BSP_ERR_INVALID_ARG;  // 16-bit pools only
     if (n == 0) return BSP_OK;
     const bsp_geometry& geo = plan->geo;
     if (n > plan->total_rows) return BSP_ERR_INVALID_ARG;
@@ -905,6 +929,7 @@ static bsp_status rope_append_impl(const bsp_plan_t* plan, const bsp_rope_config
     bsp_status st = check_plan(plan);
     if (st != BSP_OK) return st;
     if (!rope || n < 0) return BSP_ERR_INVALID_ARG;
+    if (!fp8 && plan->geo.kv_dtype != BSP_KV_DTYPE_SAME) return BSP_ERR_INVALID_ARG;  // 16-bit pools only
     if (fp8 && (!std::isfinite(k_mul) || !std::isfinite(v_mul) || !(k_mul > 0.f) || !(v_mul > 0.f)))
         return BSP_ERR_INVALID_ARG;
     const bsp_geometry& geo = plan->geo;
@@ -986,8 +1011,12 @@ namespace bsp {
 // prefill plan). Nothing is enqueued.
 bsp_status attn_check_args(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
                            const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
-                           int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse, bool prefill) {
+                           int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse, bool prefill,
+                           bool fp8, float k_scale, float v_scale) {
     if (plan->kind != (prefill ? 1 : 0)) return BSP_ERR_INVALID_ARG;
+    if ((plan->geo.kv_dtype == BSP_KV_DTYPE_E4M3) != fp8) return BSP_ERR_INVALID_ARG;
+    if (!(k_scale > 0.f) || !std::isfinite(k_scale) || !(v_scale > 0.f) || !std::isfinite(v_scale))
+        return BSP_ERR_INVALID_ARG;
     if (flags & ~(BSP_FLAG_LSE_BASE2 | BSP_FLAG_CHECK | BSP_FLAG_GRAPH)) return BSP_ERR_INVALID_ARG;
     // graph mode: launch shapes that do not depend on the plan's lengths (decode plans only)
     const bool graph = (flags & BSP_FLAG_GRAPH) != 0;
@@ -1013,7 +1042,7 @@ bsp_status attn_check_args(const bsp_plan_t* plan, const void* q, const void* k_
 bsp_status attn_launches(const bsp_plan_t* plan, uint8_t* ws, const void* q, const void* k_pool, const void* v_pool,
                          const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
                          int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse,
-                         void* const* events, cudaStream_t s, bool prefill) {
+                         void* const* events, cudaStream_t s, bool prefill, float k_scale, float v_scale) {
     const bool graph = (flags & BSP_FLAG_GRAPH) != 0;
     const bsp_geometry& geo = plan->geo;
     const int64_t R = plan->total_rows;
@@ -1022,13 +1051,16 @@ bsp_status attn_launches(const bsp_plan_t* plan, uint8_t* ws, const void* q, con
     const bool bf16 = geo.dtype == BSP_DTYPE_BF16;
     const float log2e = 1.4426950408889634f;
     const bool alt = plan->layout == 1, wide = plan->layout == 2;
+    const bool fp8 = geo.kv_dtype == BSP_KV_DTYPE_E4M3;  // the planner gave such a plan layout 1 or 2
+    if (fp8 && !alt && !wide) return BSP_ERR_INVALID_ARG;
 
     // everything that is not a launch (attributes, tensor maps, parameters) comes before the
     // first timing event
     const bool prefix = graph || plan->num_units > 0;
-    if (prefix && (alt ? prepare_alt(D, bf16) : wide ? prepare_wide(D, bf16) : prepare_prefix(D, bf16)) != cudaSuccess)
+    if (prefix && (alt ? prepare_alt(D, bf16, fp8) : wide ? prepare_wide(D, bf16, fp8) : prepare_prefix(D, bf16)) !=
+                      cudaSuccess)
         return BSP_ERR_CUDA;
-    if (prepare_tail(D, bf16, graph ? plan->max_tail : plan->max_tail_len, Hq) != cudaSuccess) return BSP_ERR_CUDA;
+    if (prepare_tail(D, bf16, graph ? plan->max_tail : plan->max_tail_len, Hq, fp8) != cudaSuccess) return BSP_ERR_CUDA;
     CUtensorMap tq, tk, tv;
     PrefixParams pp{};
     if (prefix) {
@@ -1044,12 +1076,14 @@ bsp_status attn_launches(const bsp_plan_t* plan, uint8_t* ws, const void* q, con
         cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(G),
                               static_cast<cuuint32_t>(qbeams > 0 ? qbeams : plan->beams_per_block)};
         const int ps = geo.page_size;
-        // pools viewed as 2-D [pool row][head_dim]; one box = min(page, 64) rows x 64 columns
+        // pools viewed as 2-D [pool row][head_dim]; one box = min(page, 64) rows x 64 columns (E4M3 pools:
+        // x head_dim one-byte columns)
         cuuint64_t kdims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(geo.num_pages) * Hkv * ps};
-        cuuint64_t kstr[1] = {static_cast<cuuint64_t>(D) * 2};
-        cuuint32_t kbox[2] = {64, static_cast<cuuint32_t>(std::min(ps, kTileKeys))};
-        if (!encode_map(&tq, geo.dtype, 3, q, qdims, qstr, qbox) || !encode_map(&tk, geo.dtype, 2, k_pool, kdims, kstr, kbox) ||
-            !encode_map(&tv, geo.dtype, 2, v_pool, kdims, kstr, kbox))
+        cuuint64_t kstr[1] = {static_cast<cuuint64_t>(D) * (fp8 ? 1 : 2)};
+        cuuint32_t kbox[2] = {static_cast<cuuint32_t>(fp8 ? D : 64), static_cast<cuuint32_t>(std::min(ps, kTileKeys))};
+        if (!encode_map(&tq, geo.dtype, 3, q, qdims, qstr, qbox) ||
+            !encode_map(&tk, geo.dtype, 2, k_pool, kdims, kstr, kbox, fp8) ||
+            !encode_map(&tv, geo.dtype, 2, v_pool, kdims, kstr, kbox, fp8))
             return BSP_ERR_CUDA;
         pp.k_pool = k_pool;
         pp.v_pool = v_pool;
@@ -1080,7 +1114,8 @@ bsp_status attn_launches(const bsp_plan_t* plan, uint8_t* ws, const void* q, con
             pp.graph_hdr = reinterpret_cast<const int32_t*>(ws + kStatusBytes);
             pp.graph_batch = plan->batch;
         }
-        pp.scale_log2 = softmax_scale * log2e;
+        pp.scale_log2 = softmax_scale * k_scale * log2e;
+        pp.v_scale = v_scale;
     }
     TailParams tp{};
     tp.q = q;
@@ -1103,8 +1138,9 @@ bsp_status attn_launches(const bsp_plan_t* plan, uint8_t* ws, const void* q, con
     tp.num_pages = geo.num_pages;
     tp.beam_pages_stride = beam_pages_stride;
     tp.max_seq = max_seq;
-    tp.scale_log2 = softmax_scale * log2e;
+    tp.scale_log2 = softmax_scale * k_scale * log2e;
     tp.lse_base2 = (flags & BSP_FLAG_LSE_BASE2) ? 1 : 0;
+    tp.v_scale = v_scale;
     if (graph) {
         tp.graph_hdr = reinterpret_cast<const int32_t*>(ws + kStatusBytes);
         tp.graph_max_tail = plan->max_tail;
@@ -1114,15 +1150,15 @@ bsp_status attn_launches(const bsp_plan_t* plan, uint8_t* ws, const void* q, con
     if (!record(0)) return BSP_ERR_CUDA;
     if (prefix) {
         const int ctas = graph ? plan->num_sms : plan->prefix_ctas;
-        const cudaError_t e = alt    ? launch_alt(D, bf16, ctas, tq, tk, tv, pp, s)
-                              : wide ? launch_wide(D, bf16, ctas, tq, tk, tv, pp, s)
+        const cudaError_t e = alt    ? launch_alt(D, bf16, ctas, tq, tk, tv, pp, s, fp8)
+                              : wide ? launch_wide(D, bf16, ctas, tq, tk, tv, pp, s, fp8)
                                    : launch_prefix(D, bf16, ctas, tq, tk, tv, pp, s);
         if (e != cudaSuccess) return BSP_ERR_CUDA;
     }
     if (!record(1)) return BSP_ERR_CUDA;
     // without timing events between them, the tail kernel overlaps the end of the prompt kernel
     if ((graph || plan->tail_requests > 0) &&
-        launch_tail(D, bf16, graph ? plan->max_tail : plan->max_tail_len, tp, prefix && events == nullptr, s) !=
+        launch_tail(D, bf16, graph ? plan->max_tail : plan->max_tail_len, tp, prefix && events == nullptr, s, fp8) !=
             cudaSuccess)
         return BSP_ERR_CUDA;
     if (!record(2)) return BSP_ERR_CUDA;
@@ -1136,16 +1172,16 @@ namespace {
 bsp_status attn_impl(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
                      const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
                      int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse, void* const* events,
-                     void* stream, bool prefill) {
+                     void* stream, bool prefill, bool fp8 = false, float k_scale = 1.f, float v_scale = 1.f) {
     bsp_status st = check_plan(plan);
     if (st != BSP_OK) return st;
     st = attn_check_args(plan, q, k_pool, v_pool, beam_pages, beam_pages_stride, cache_indirection, max_seq,
-                         softmax_scale, flags, o, lse, prefill);
+                         softmax_scale, flags, o, lse, prefill, fp8, k_scale, v_scale);
     if (st != BSP_OK) return st;
     if (plan->total_rows == 0) return BSP_OK;
     st = attn_launches(plan, static_cast<uint8_t*>(plan->ws_device), q, k_pool, v_pool, beam_pages, beam_pages_stride,
                        cache_indirection, max_seq, softmax_scale, flags, o, lse, events,
-                       static_cast<cudaStream_t>(stream), prefill);
+                       static_cast<cudaStream_t>(stream), prefill, k_scale, v_scale);
     if (st != BSP_OK) return st;
     if (flags & BSP_FLAG_CHECK) return bsp_read_device_status(plan, stream, 1, nullptr);
     return BSP_OK;
@@ -1160,6 +1196,15 @@ bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const void* k_
                            void* const* events, void* stream) {
     return attn_impl(plan, q, k_pool, v_pool, beam_pages, beam_pages_stride, cache_indirection, max_seq,
                      softmax_scale, flags, o, lse, events, stream, false);
+}
+
+bsp_status bsp_decode_attn_fp8(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* beam_pages, int32_t beam_pages_stride,
+                               const int32_t* cache_indirection, int32_t max_seq, float softmax_scale,
+                               float k_scale, float v_scale, int32_t flags, void* o, float* lse,
+                               void* const* events, void* stream) {
+    return attn_impl(plan, q, k_pool, v_pool, beam_pages, beam_pages_stride, cache_indirection, max_seq,
+                     softmax_scale, flags, o, lse, events, stream, false, true, k_scale, v_scale);
 }
 
 bsp_status bsp_prefill_attn(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,

@@ -89,6 +89,7 @@ struct PrefixParams {
     int W, Hq, Hkv, G, ps_log2, Wblk, num_pages;
     int bq;            // > 0: half-row softmax, bq beams of the block per TMEM lane quadrant (prefix_quad_beams)
     int num_units;     // units in the list
+    float v_scale;     // E4M3 pools: the values' per-tensor scale, applied to O (1 for 16-bit pools)
     // graph mode (else null): the staged plan's header, checked at the start against the launch
     // (batch, beam width, one CTA per SM of the plan, a decode plan)
     const int32_t* graph_hdr;
@@ -111,6 +112,7 @@ struct TailParams {
     int B, W, Hq, Hkv, G, ps_log2, num_pages, beam_pages_stride, max_seq;
     float scale_log2;
     int lse_base2;
+    float v_scale;     // E4M3 pools: the values' per-tensor scale, applied to the tail's O (1 otherwise)
     // graph mode (else null): the staged plan's header, checked against the launch (batch, beam width,
     // a decode plan, a tail bound within the one the launch was made for)
     const int32_t* graph_hdr;
@@ -133,33 +135,37 @@ cudaError_t launch_prefix(int head_dim, bool bf16, int ctas, const CUtensorMap& 
 // Kernel attributes (shared-memory size and split) are set by the prepare_* calls, once before
 // the launches, so that timing events recorded around a launch bracket the launch alone.
 cudaError_t prepare_prefix(int head_dim, bool bf16);
-cudaError_t prepare_tail(int head_dim, bool bf16, int max_tail_len, int num_q_heads);
+cudaError_t prepare_tail(int head_dim, bool bf16, int max_tail_len, int num_q_heads, bool fp8 = false);
 // after_prefix: the prompt kernel was the last launch on `stream`; the tail kernel is then a
 // programmatic dependent launch of it (it starts on SMs the prompt kernel has left, resolves and
 // prefetches its tail rows, and waits for the prompt kernel's partials before merging).
 cudaError_t launch_tail(int head_dim, bool bf16, int max_tail_len, const TailParams& p, bool after_prefix,
-                        cudaStream_t stream);
-// The alternating-tile prompt kernel (p.Wblk = beams per row block, p.bq = beams per quadrant).
-cudaError_t prepare_alt(int head_dim, bool bf16);
+                        cudaStream_t stream, bool fp8 = false);
+// The alternating-tile prompt kernel (p.Wblk = beams per row block, p.bq = beams per quadrant). fp8: E4M3
+// pools (tk, tv map one-byte elements without swizzle, boxes of min(page, 64) rows x head_dim bytes).
+cudaError_t prepare_alt(int head_dim, bool bf16, bool fp8 = false);
 cudaError_t launch_alt(int head_dim, bool bf16, int ctas, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const PrefixParams& p, cudaStream_t stream);
-// The wide-layout prompt kernel (p.Wblk = beams per block, p.bq = beams per quadrant).
-cudaError_t prepare_wide(int head_dim, bool bf16);
+                       const CUtensorMap& tv, const PrefixParams& p, cudaStream_t stream, bool fp8 = false);
+// The wide-layout prompt kernel (p.Wblk = beams per block, p.bq = beams per quadrant); fp8 as above.
+cudaError_t prepare_wide(int head_dim, bool bf16, bool fp8 = false);
 cudaError_t launch_wide(int head_dim, bool bf16, int ctas, const CUtensorMap& tq, const CUtensorMap& tk,
-                        const CUtensorMap& tv, const PrefixParams& p, cudaStream_t stream);
+                        const CUtensorMap& tv, const PrefixParams& p, cudaStream_t stream, bool fp8 = false);
 cudaError_t prepare_append();
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 
 // bsp_host.cpp: the attention of a plan whose status word, image and partial states sit at `ws`
 // (the caller's workspace, or the fixed scratch of the no-allocation entry point). attn_check_args
 // checks what the host can check and enqueues nothing; attn_launches enqueues the launches.
+// fp8: the caller is the E4M3 entry point (the plan's pools must then be E4M3, and 16-bit otherwise);
+// k_scale and v_scale are the E4M3 pools' per-tensor scales (1 for 16-bit pools).
 bsp_status attn_check_args(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
                            const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
-                           int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse, bool prefill);
+                           int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse, bool prefill,
+                           bool fp8 = false, float k_scale = 1.f, float v_scale = 1.f);
 bsp_status attn_launches(const bsp_plan_t* plan, uint8_t* ws, const void* q, const void* k_pool, const void* v_pool,
                          const int32_t* beam_pages, int32_t beam_pages_stride, const int32_t* cache_indirection,
                          int32_t max_seq, float softmax_scale, int32_t flags, void* o, float* lse,
-                         void* const* events, cudaStream_t s, bool prefill);
+                         void* const* events, cudaStream_t s, bool prefill, float k_scale = 1.f, float v_scale = 1.f);
 // A decode plan with the packed layout (sections and partial states sized by the plan's own units and
 // splits), for a caller that never replays it from a CUDA graph.
 bsp_status plan_build_packed(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len,

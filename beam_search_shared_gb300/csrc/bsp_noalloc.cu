@@ -86,6 +86,7 @@ extern "C" BSP_API bsp_status bsp_decode_attn_noalloc(
     using namespace bsp;
     if (flags & ~(BSP_FLAG_LSE_BASE2 | BSP_FLAG_CHECK)) return BSP_ERR_INVALID_ARG;
     if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BSP_ERR_INVALID_ARG;
+    if (geo && geo->kv_dtype != BSP_KV_DTYPE_SAME) return BSP_ERR_UNSUPPORTED;  // 16-bit pools only
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     {
         // a captured call would record a copy from the shared host plan array: refused

@@ -1,5 +1,5 @@
-// Device-side pieces shared by the prompt-attention kernels (bsp_prefix.cu, bsp_wide.cu): the work
-// unit as the plan image describes it, tile counts, and 16-bit packing.
+// Device-side pieces shared by the prompt-attention kernels (bsp_prefix.cu, bsp_wide.cu, bsp_alt.cu): the
+// work unit as the plan image describes it, tile counts, 16-bit packing, and the widening of E4M3 tiles.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -57,6 +57,101 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     } else {
         __half2 h = __floats2half2_rn(a, b);
         return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+// ---- E4M3 pools: the kernels load E4M3 tiles and widen them to the q dtype in shared memory
+
+// Two E4M3 codes (bits 0-7 and 8-15 of `two`) as a pair of 16-bit floats of the q dtype, the first in the
+// low half, exactly: every E4M3 value is a binary16 and a bfloat16 value. The hardware conversion gives
+// binary16; for bfloat16 the binary16 sign, exponent and fraction fields move into bfloat16 fields (the
+// exponent keeps its binary16 bias of 15 instead of 127: a factor 2^-112), and one multiplication by
+// 2^112 restores the value. E4M3-derived binary16 values are zero or normal (the smallest, 2^-9, has
+// exponent field 6), so the shifted bfloat16 value is zero or normal too and the product is exact.
+template <bool BF16>
+__device__ __forceinline__ uint32_t e4m3x2_to_16(uint32_t two) {
+    uint32_t h;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h) : "r"(two));
+    if constexpr (!BF16) return h;
+    // the fraction's low 7 bits are zero for these values, so nothing crosses from one half to the other
+    const uint32_t t = ((h & 0x7fff7fffu) >> 3) | (h & 0x80008000u);
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x77807780u));  // 2^112 in both halves
+    return r;
+}
+// 8 E4M3 codes (bytes in order) -> one 16-byte chunk of 8 16-bit values
+template <bool BF16>
+__device__ __forceinline__ uint4 e4m3x8_to_16(uint2 in) {
+    return make_uint4(e4m3x2_to_16<BF16>(in.x & 0xffffu), e4m3x2_to_16<BF16>(in.x >> 16),
+                      e4m3x2_to_16<BF16>(in.y & 0xffffu), e4m3x2_to_16<BF16>(in.y >> 16));
+}
+
+// Byte offset of 16-byte chunk kc (8 elements) of key row r in a 16-bit K or V tile of TK rows laid out
+// as a TMA box with 128-byte swizzle: column half kc / 8, then row r, then chunk (kc % 8) ^ (r % 8).
+template <int TK>
+__device__ __forceinline__ uint32_t sw128_chunk(int kc, int r) {
+    return static_cast<uint32_t>((kc >> 3) * (TK * 128) + r * 128 + (((kc & 7) ^ (r & 7)) << 4));
+}
+
+// Widens the E4M3 K or V tile that a TMA load left in the upper half of a ring slot (TK rows of D codes,
+// row r at slot + TK * D + r * D) into the slot's 16-bit layout (sw128_chunk); rows >= valid become zero
+// rows. Run by the 64 threads gtid = 0..63 of two warps, which synchronise on named barrier `bar` (64
+// threads) at head_dim 64. The 16-bit rows overwrite the E4M3 rows in place:
+//  - D = 128: a 16-bit row's first column half lies below the E4M3 rows and its second half on the E4M3
+//    row of the same key, so each key row belongs to one warp, which reads all of it before writing it;
+//  - D = 64: the 16-bit row r covers E4M3 rows 2r - TK and 2r - TK + 1, so all threads read the whole
+//    tile into registers before any of them writes.
+// The caller fences the writes for the tensor core and synchronises the 64 threads afterwards.
+template <int D, int TK, bool BF16>
+__device__ __forceinline__ void widen_e4m3_tile(uint8_t* slot, int valid, int gtid, int bar) {
+    static_assert(D == 64 || D == 128, "E4M3 tiles at head_dim 64 and 128");
+    const uint8_t* src = slot + TK * D;
+    if constexpr (D == 128) {
+        const int j = gtid & 7;    // codes 16j .. 16j + 15 of a row
+        const int r0 = gtid >> 3;  // rows r0 + 8i: warp 0 holds r0 < 4, warp 1 the rest
+#pragma unroll 1
+        for (int i0 = 0; i0 < TK / 8; i0 += 4) {
+            uint4 in[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = r0 + 8 * (i0 + u);
+                in[u] = r < valid ? *reinterpret_cast<const uint4*>(src + r * D + 16 * j) : make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = r0 + 8 * (i0 + u);
+                uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+                if (r < valid) {
+                    lo = e4m3x8_to_16<BF16>(make_uint2(in[u].x, in[u].y));
+                    hi = e4m3x8_to_16<BF16>(make_uint2(in[u].z, in[u].w));
+                }
+                *reinterpret_cast<uint4*>(slot + sw128_chunk<TK>(2 * j, r)) = lo;
+                *reinterpret_cast<uint4*>(slot + sw128_chunk<TK>(2 * j + 1, r)) = hi;
+            }
+            __syncwarp();
+        }
+    } else {
+        const int j = gtid & 3;    // codes 16j .. 16j + 15 of a row
+        const int r0 = gtid >> 2;  // rows r0 + 16i
+        uint4 in[TK / 16];
+#pragma unroll
+        for (int i = 0; i < TK / 16; ++i) {
+            const int r = r0 + 16 * i;
+            in[i] = r < valid ? *reinterpret_cast<const uint4*>(src + r * D + 16 * j) : make_uint4(0, 0, 0, 0);
+        }
+        asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
+#pragma unroll
+        for (int i = 0; i < TK / 16; ++i) {
+            const int r = r0 + 16 * i;
+            uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+            if (r < valid) {
+                lo = e4m3x8_to_16<BF16>(make_uint2(in[i].x, in[i].y));
+                hi = e4m3x8_to_16<BF16>(make_uint2(in[i].z, in[i].w));
+            }
+            *reinterpret_cast<uint4*>(slot + sw128_chunk<TK>(2 * j, r)) = lo;
+            *reinterpret_cast<uint4*>(slot + sw128_chunk<TK>(2 * j + 1, r)) = hi;
+        }
     }
 }
 

@@ -23,6 +23,7 @@
 #include <cuda_runtime.h>
 
 #include "bsp_internal.h"
+#include "bsp_prompt.cuh"
 #include "bsp_ptx.cuh"
 #include "../../include/bsp.h"
 
@@ -46,6 +47,18 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
             f[2 * i] = v.x;
             f[2 * i + 1] = v.y;
         }
+    }
+}
+
+// 8 E4M3 codes as fp32, exactly (through binary16)
+__device__ __forceinline__ void unpack8_e4m3(const uint2& u, float (&f)[8]) {
+    const uint4 h = e4m3x8_to_16<false>(u);
+    const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        f[2 * i] = v.x;
+        f[2 * i + 1] = v.y;
     }
 }
 
@@ -73,7 +86,9 @@ constexpr int kTailThreads = 128;
 // MAXP: head passes whose tail state is held in registers across the wait for the prompt kernel
 // (passes = Hq / (4 warps x heads per warp pass), rounded up to 1, 2 or 4; more passes are done
 // in groups of MAXP).
-template <int D, bool BF16, int MAXT, int MAXP>
+// FP8: E4M3 pools (a lane reads 8 one-byte codes of a row instead of 8 16-bit elements; the keys'
+// scale is folded into scale_log2, the values' scale into the tail's share of O).
+template <int D, bool BF16, int MAXT, int MAXP, bool FP8>
 __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) {
     constexpr int LPR = D / 8;       // lanes per K/V row
     constexpr int HPW = 32 / LPR;    // heads per warp pass
@@ -138,6 +153,7 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
             const uint4 qraw = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
                                                                      (static_cast<long long>(r) * p.Hq + hh) * D) +
                                      li);
+            // a lane's 8 elements of a K or V row: 16 bytes, or 8 E4M3 codes (the upper half unused)
             uint4 kraw[MAXT], vraw[MAXT];
             bool ok[MAXT];
 #pragma unroll
@@ -146,9 +162,16 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
                 ok[t] = active && off >= 0;
                 kraw[t] = vraw[t] = make_uint4(0, 0, 0, 0);
                 if (ok[t]) {
-                    const long long e = off + g * head_stride;
-                    kraw[t] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k_pool) + e) + li);
-                    vraw[t] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.v_pool) + e) + li);
+                    const long long e = off + g * head_stride;  // element offset
+                    if constexpr (FP8) {
+                        const uint2 kk = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(p.k_pool) + e) + li);
+                        const uint2 vv = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(p.v_pool) + e) + li);
+                        kraw[t] = make_uint4(kk.x, kk.y, 0, 0);
+                        vraw[t] = make_uint4(vv.x, vv.y, 0, 0);
+                    } else {
+                        kraw[t] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k_pool) + e) + li);
+                        vraw[t] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.v_pool) + e) + li);
+                    }
                 }
             }
             float q[8];
@@ -160,7 +183,8 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
                 sc[t] = -INFINITY;
                 if (t < T) {  // block-uniform: rows past the request's tail cost nothing
                     float kf[8];
-                    unpack8<BF16>(kraw[t], kf);
+                    if constexpr (FP8) unpack8_e4m3(make_uint2(kraw[t].x, kraw[t].y), kf);
+                    else unpack8<BF16>(kraw[t], kf);
                     float dot = 0.f;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) dot = fmaf(q[e], kf[e], dot);
@@ -179,7 +203,8 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
                     if (!ok[t]) continue;
                     const float e_s = exp2f(sc[t] - m);
                     float vf[8];
-                    unpack8<BF16>(vraw[t], vf);
+                    if constexpr (FP8) unpack8_e4m3(make_uint2(vraw[t].x, vraw[t].y), vf);
+                    else unpack8<BF16>(vraw[t], vf);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) acc[pi][e] = fmaf(e_s, vf[e], acc[pi][e]);
                     l += e_s;
@@ -249,16 +274,17 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
             } else {
                 // tail weight exp2(m + log2 l - Lmax) times O_t = acc / l, then split 0
                 const float ft = (l > 0.f) ? exp2f(m - Lmax) : 0.f;
+                const float fv = ft * p.v_scale;          // the tail's values in their E4M3 scale (1 otherwise)
                 const float w0 = exp2f(lse0[pi] - Lmax);  // 0 without a prompt
                 float sum = l * ft + w0;
-                out[0] = fmaf(w0, o0a[pi].x, acc[pi][0] * ft);
-                out[1] = fmaf(w0, o0a[pi].y, acc[pi][1] * ft);
-                out[2] = fmaf(w0, o0a[pi].z, acc[pi][2] * ft);
-                out[3] = fmaf(w0, o0a[pi].w, acc[pi][3] * ft);
-                out[4] = fmaf(w0, o0b[pi].x, acc[pi][4] * ft);
-                out[5] = fmaf(w0, o0b[pi].y, acc[pi][5] * ft);
-                out[6] = fmaf(w0, o0b[pi].z, acc[pi][6] * ft);
-                out[7] = fmaf(w0, o0b[pi].w, acc[pi][7] * ft);
+                out[0] = fmaf(w0, o0a[pi].x, acc[pi][0] * fv);
+                out[1] = fmaf(w0, o0a[pi].y, acc[pi][1] * fv);
+                out[2] = fmaf(w0, o0a[pi].z, acc[pi][2] * fv);
+                out[3] = fmaf(w0, o0a[pi].w, acc[pi][3] * fv);
+                out[4] = fmaf(w0, o0b[pi].x, acc[pi][4] * fv);
+                out[5] = fmaf(w0, o0b[pi].y, acc[pi][5] * fv);
+                out[6] = fmaf(w0, o0b[pi].z, acc[pi][6] * fv);
+                out[7] = fmaf(w0, o0b[pi].w, acc[pi][7] * fv);
                 for (int sp0 = 1; sp0 < nsplit; sp0 += KB) {
                     float ls[KB];
                     float4 a0[KB], a1[KB];
@@ -302,7 +328,7 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
     }
 }
 
-template <int D, bool BF16, int MAXT, int MAXP>
+template <int D, bool BF16, int MAXT, int MAXP, bool FP8>
 static cudaError_t launch_tail_k(const TailParams& p, bool after_prefix, int pass_ctas, cudaStream_t stream) {
     const long long rows = static_cast<long long>(p.B) * p.W;
     cudaLaunchConfig_t cfg = {};
@@ -315,7 +341,7 @@ static cudaError_t launch_tail_k(const TailParams& p, bool after_prefix, int pas
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = after_prefix ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, tail_merge_kernel<D, BF16, MAXT, MAXP>, p);
+    return cudaLaunchKernelEx(&cfg, tail_merge_kernel<D, BF16, MAXT, MAXP, FP8>, p);
 }
 
 // head passes of a 128-thread CTA: Hq / (4 warps x heads per warp pass)
@@ -338,67 +364,80 @@ static int device_sms() {
     return cache[dev];
 }
 
-template <int D, bool BF16, int MAXT>
+template <int D, bool BF16, int MAXT, bool FP8>
 static cudaError_t launch_tail_p(const TailParams& p, bool after_prefix, cudaStream_t stream) {
     const int passes = tail_passes<D>(p.Hq);
     const long long rows = static_cast<long long>(p.B) * p.W;
     // fewer rows than SMs: one CTA per (row, head pass), so a row's heads merge in parallel
-    if (passes > 1 && rows < device_sms()) return launch_tail_k<D, BF16, MAXT, 1>(p, after_prefix, passes, stream);
-    if (passes <= 1) return launch_tail_k<D, BF16, MAXT, 1>(p, after_prefix, 1, stream);
-    if (passes <= 2) return launch_tail_k<D, BF16, MAXT, 2>(p, after_prefix, 1, stream);
-    return launch_tail_k<D, BF16, MAXT, 4>(p, after_prefix, 1, stream);
+    if (passes > 1 && rows < device_sms()) return launch_tail_k<D, BF16, MAXT, 1, FP8>(p, after_prefix, passes, stream);
+    if (passes <= 1) return launch_tail_k<D, BF16, MAXT, 1, FP8>(p, after_prefix, 1, stream);
+    if (passes <= 2) return launch_tail_k<D, BF16, MAXT, 2, FP8>(p, after_prefix, 1, stream);
+    return launch_tail_k<D, BF16, MAXT, 4, FP8>(p, after_prefix, 1, stream);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool FP8>
 static cudaError_t launch_tail_t(const TailParams& p, int max_tail_len, bool after_prefix, cudaStream_t stream) {
     const long long rows = static_cast<long long>(p.B) * p.W;
     if (rows == 0) return cudaSuccess;
-    if (max_tail_len <= 2) return launch_tail_p<D, BF16, 2>(p, after_prefix, stream);
-    if (max_tail_len <= 4) return launch_tail_p<D, BF16, 4>(p, after_prefix, stream);
-    return launch_tail_p<D, BF16, 8>(p, after_prefix, stream);
+    if (max_tail_len <= 2) return launch_tail_p<D, BF16, 2, FP8>(p, after_prefix, stream);
+    if (max_tail_len <= 4) return launch_tail_p<D, BF16, 4, FP8>(p, after_prefix, stream);
+    return launch_tail_p<D, BF16, 8, FP8>(p, after_prefix, stream);
 }
 
 // the same L1/shared split as the prompt kernel, so SMs are not reconfigured between the
 // kernels of a step
-template <int D, bool BF16, int MAXT>
+template <int D, bool BF16, int MAXT, bool FP8>
 static cudaError_t prepare_tail_p(int Hq) {
     const cudaFuncAttribute a = cudaFuncAttributePreferredSharedMemoryCarveout;
     const int passes = tail_passes<D>(Hq);
     // the one-pass variant also serves steps with fewer rows than SMs
-    const cudaError_t e = cudaFuncSetAttribute(tail_merge_kernel<D, BF16, MAXT, 1>, a, cudaSharedmemCarveoutMaxShared);
+    const cudaError_t e =
+        cudaFuncSetAttribute(tail_merge_kernel<D, BF16, MAXT, 1, FP8>, a, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess || passes <= 1) return e;
-    if (passes <= 2) return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, MAXT, 2>, a, cudaSharedmemCarveoutMaxShared);
-    return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, MAXT, 4>, a, cudaSharedmemCarveoutMaxShared);
+    if (passes <= 2) return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, MAXT, 2, FP8>, a, cudaSharedmemCarveoutMaxShared);
+    return cudaFuncSetAttribute(tail_merge_kernel<D, BF16, MAXT, 4, FP8>, a, cudaSharedmemCarveoutMaxShared);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool FP8>
 static cudaError_t prepare_tail_t(int max_tail_len, int Hq) {
-    if (max_tail_len <= 2) return prepare_tail_p<D, BF16, 2>(Hq);
-    if (max_tail_len <= 4) return prepare_tail_p<D, BF16, 4>(Hq);
-    return prepare_tail_p<D, BF16, 8>(Hq);
+    if (max_tail_len <= 2) return prepare_tail_p<D, BF16, 2, FP8>(Hq);
+    if (max_tail_len <= 4) return prepare_tail_p<D, BF16, 4, FP8>(Hq);
+    return prepare_tail_p<D, BF16, 8, FP8>(Hq);
 }
 
-cudaError_t prepare_tail(int head_dim, bool bf16, int max_tail_len, int num_q_heads) {
+template <int D, bool FP8>
+static cudaError_t prepare_tail_d(bool bf16, int max_tail_len, int Hq) {
+    return bf16 ? prepare_tail_t<D, true, FP8>(max_tail_len, Hq) : prepare_tail_t<D, false, FP8>(max_tail_len, Hq);
+}
+
+template <int D, bool FP8>
+static cudaError_t launch_tail_d(bool bf16, int max_tail_len, const TailParams& p, bool after_prefix,
+                                 cudaStream_t stream) {
+    return bf16 ? launch_tail_t<D, true, FP8>(p, max_tail_len, after_prefix, stream)
+                : launch_tail_t<D, false, FP8>(p, max_tail_len, after_prefix, stream);
+}
+
+// E4M3 pools at head_dim 64 and 128 only
+cudaError_t prepare_tail(int head_dim, bool bf16, int max_tail_len, int num_q_heads, bool fp8) {
     switch (head_dim) {
-        case 64: return bf16 ? prepare_tail_t<64, true>(max_tail_len, num_q_heads)
-                             : prepare_tail_t<64, false>(max_tail_len, num_q_heads);
-        case 128: return bf16 ? prepare_tail_t<128, true>(max_tail_len, num_q_heads)
-                              : prepare_tail_t<128, false>(max_tail_len, num_q_heads);
-        case 256: return bf16 ? prepare_tail_t<256, true>(max_tail_len, num_q_heads)
-                              : prepare_tail_t<256, false>(max_tail_len, num_q_heads);
+        case 64: return fp8 ? prepare_tail_d<64, true>(bf16, max_tail_len, num_q_heads)
+                            : prepare_tail_d<64, false>(bf16, max_tail_len, num_q_heads);
+        case 128: return fp8 ? prepare_tail_d<128, true>(bf16, max_tail_len, num_q_heads)
+                             : prepare_tail_d<128, false>(bf16, max_tail_len, num_q_heads);
+        case 256: return fp8 ? cudaErrorInvalidValue : prepare_tail_d<256, false>(bf16, max_tail_len, num_q_heads);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_tail(int head_dim, bool bf16, int max_tail_len, const TailParams& p, bool after_prefix,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool fp8) {
     switch (head_dim) {
-        case 64: return bf16 ? launch_tail_t<64, true>(p, max_tail_len, after_prefix, stream)
-                             : launch_tail_t<64, false>(p, max_tail_len, after_prefix, stream);
-        case 128: return bf16 ? launch_tail_t<128, true>(p, max_tail_len, after_prefix, stream)
-                              : launch_tail_t<128, false>(p, max_tail_len, after_prefix, stream);
-        case 256: return bf16 ? launch_tail_t<256, true>(p, max_tail_len, after_prefix, stream)
-                              : launch_tail_t<256, false>(p, max_tail_len, after_prefix, stream);
+        case 64: return fp8 ? launch_tail_d<64, true>(bf16, max_tail_len, p, after_prefix, stream)
+                            : launch_tail_d<64, false>(bf16, max_tail_len, p, after_prefix, stream);
+        case 128: return fp8 ? launch_tail_d<128, true>(bf16, max_tail_len, p, after_prefix, stream)
+                             : launch_tail_d<128, false>(bf16, max_tail_len, p, after_prefix, stream);
+        case 256: return fp8 ? cudaErrorInvalidValue
+                             : launch_tail_d<256, false>(bf16, max_tail_len, p, after_prefix, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -108,6 +108,8 @@ struct WideBarriers {
     uint64_t p_full[2];    // block X's softmax warps wrote P_X (one arrival per warp)
     uint64_t o_final[2];   // the last P*V of a unit into O_X completed
     uint64_t drain;
+    uint64_t k8_full[8];   // E4M3 pools: the E4M3 K tile landed in the upper half of the K slot
+    uint64_t v8_full[8];   // ... the E4M3 V tile in the V slot
     uint32_t tmem_base;
     int abort_flag;
     int tail_granted;      // tail tiles whose ring slots the producer has handed to the tail-tile warps
@@ -161,7 +163,7 @@ __device__ __forceinline__ bool gather_sync_and(bool ok) {
 
 }  // namespace
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool FP8>
 __global__ void __launch_bounds__(384, 1)
 prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefixParams p) {
@@ -213,6 +215,10 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_init(&bars->o_final[i], 1);
         }
         mbar_init(&bars->drain, 1);
+        if constexpr (FP8) {
+            for (int s = 0; s < KST; ++s) mbar_init(&bars->k8_full[s], 1);
+            for (int s = 0; s < VST; ++s) mbar_init(&bars->v8_full[s], 1);
+        }
         bars->abort_flag = 0;
         bars->tail_granted = 0;
         fence_mbar_init();
@@ -268,34 +274,46 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         if (!ok) break;
                     }
                     ++ntail;
-                    if (lane == 0) st_release_shared(&bars->tail_granted, ntail);
+                    if (lane == 0) {
+                        st_release_shared(&bars->tail_granted, ntail);
+                        if constexpr (FP8) {
+                            // no E4M3 tile here: complete the slots' E4M3 phases, which the widening warps
+                            // skip for a tail tile, so that the phases keep counting the slot's tiles
+                            mbar_arrive(&bars->k8_full[gt % KST]);
+                            mbar_arrive(&bars->v8_full[gt % VST]);
+                        }
+                    }
                     __syncwarp();
                     continue;
                 }
                 const int key0 = ui.key_begin + t * TK;
                 const int valid = min(TK, ui.key_end - key0);
                 const int nchunks = (valid + BR - 1) / BR;  // pages (or 64-row slices) with valid keys
-                const int tile_bytes = nchunks * BR * D * 2;
+                const int tile_bytes = nchunks * BR * D * (FP8 ? 1 : 2);
                 const int pidx0 = key0 >> p.ps_log2;
                 const int pidx_last = (key0 + (nchunks - 1) * BR) >> p.ps_log2;
                 if (win_base < 0 || pidx_last >= win_base + 32) {  // warp-uniform
                     win_base = pidx0;
                     my_page = (win_base + lane < npages) ? __ldg(pg + win_base + lane) : 0;
                 }
-                const int nbox = nchunks * NC;  // box b of a tensor: column half b % NC of chunk b / NC
+                // box b of a tensor: column half b % NC of chunk b / NC (E4M3: one box of head_dim bytes
+                // per chunk, into the upper half of the slot, where the widening warps pick it up)
+                constexpr int NB = FP8 ? 1 : NC;
+                const int nbox = nchunks * NB;
                 for (int tensor = 0; tensor < 2; ++tensor) {
                     if (tensor == 1 && gt >= VST) {
                         ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kWideWaitNs);
                         ok = __all_sync(FULL, ok);
                         if (!ok) break;
                     }
-                    uint64_t* full = tensor == 0 ? &bars->k_full[gt % KST] : &bars->v_full[gt % VST];
+                    uint64_t* full = FP8 ? (tensor == 0 ? &bars->k8_full[gt % KST] : &bars->v8_full[gt % VST])
+                                         : (tensor == 0 ? &bars->k_full[gt % KST] : &bars->v_full[gt % VST]);
                     uint8_t* base = tensor == 0 ? k_tile(gt) : v_tile(gt);
                     const CUtensorMap* map = tensor == 0 ? &tm_k : &tm_v;
                     if (lane == 0) mbar_arrive_expect_tx(full, tile_bytes);
                     for (int b0 = 0; b0 < nbox; b0 += 32) {
                         const int bx = b0 + lane;
-                        const int ch = min(bx / NC, nchunks - 1);
+                        const int ch = min(bx / NB, nchunks - 1);
                         const int key = key0 + ch * BR;
                         int page = __shfl_sync(FULL, my_page, (key >> p.ps_log2) - win_base);
                         if (bx < nbox) {
@@ -303,9 +321,13 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                 atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
                                 page = 0;
                             }
-                            const int c = bx % NC;
                             const int row = ((page * p.Hkv + ui.g) << p.ps_log2) + (key & (ps - 1));
-                            tma_load_2d(base + c * TK * 128 + ch * BR * 128, map, full, c * 64, row);
+                            if constexpr (FP8) {
+                                tma_load_2d(base + TK * D + ch * BR * D, map, full, 0, row);
+                            } else {
+                                const int c = bx % NC;
+                                tma_load_2d(base + c * TK * 128 + ch * BR * 128, map, full, c * 64, row);
+                            }
                         }
                     }
                 }
@@ -339,12 +361,15 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
             }
             // drain: let this CTA's own copies land before the CTA exits
+            // (the TMA loads complete the E4M3 barriers over E4M3 pools)
             const uint64_t t0 = globaltimer_ns();
+            uint64_t* kf = FP8 ? bars->k8_full : bars->k_full;
+            uint64_t* vf = FP8 ? bars->v8_full : bars->v_full;
             for (int j = max(0, gt - KST); j <= gt; ++j)
-                while (!mbar_try_wait(&bars->k_full[j % KST], (j / KST) & 1) && globaltimer_ns() - t0 < kWideDrainNs) {
+                while (!mbar_try_wait(&kf[j % KST], (j / KST) & 1) && globaltimer_ns() - t0 < kWideDrainNs) {
                 }
             for (int j = max(0, gt - VST); j <= gt; ++j)
-                while (!mbar_try_wait(&bars->v_full[j % VST], (j / VST) & 1) && globaltimer_ns() - t0 < kWideDrainNs) {
+                while (!mbar_try_wait(&vf[j % VST], (j / VST) & 1) && globaltimer_ns() - t0 < kWideDrainNs) {
                 }
             for (int x = 0; x < 2; ++x)
                 while (!mbar_try_wait(&bars->q_full[x], k & 1) && globaltimer_ns() - t0 < kWideDrainNs) {
@@ -501,6 +526,7 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     float mp[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) mp[j] = -INFINITY;
+                    float mred = -INFINITY;
 #pragma unroll 1
                     for (int c0 = 0; c0 < TK; c0 += 64) {
                         uint32_t ma = ~0u, mb = ~0u;
@@ -509,10 +535,19 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                             if (!__any_sync(FULL, (ma | mb) != 0u)) continue;  // no row of the warp keeps one
                         }
                         uint32_t sa[32], sb[32];
+                        if (!partial) {
+                            // the loads reduce each 32-column half to its maximum
+                            float ra, rb;
+                            tmem_ld32_max(s_col + c0, sa, ra);
+                            tmem_ld32_max(s_col + c0 + 32, sb, rb);
+                            tmem_wait_ld();
+                            mred = fmax3(mred, ra, rb);
+                            continue;
+                        }
                         tmem_ld32(s_col + c0, sa);
                         tmem_ld32(s_col + c0 + 32, sb);
                         tmem_wait_ld();
-                        if (partial && __any_sync(FULL, (ma & mb) != ~0u)) {
+                        if (__any_sync(FULL, (ma & mb) != ~0u)) {
 #pragma unroll
                             for (int c = 0; c < 32; ++c) {
                                 sa[c] = (ma >> c) & 1u ? sa[c] : ninf;
@@ -523,8 +558,8 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         for (int c = 0; c < 32; ++c)
                             mp[c & 7] = fmax3(mp[c & 7], __uint_as_float(sa[c]), __uint_as_float(sb[c]));
                     }
-                    const float mxr = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                                            fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+                    const float mxr = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]),
+                                            fmax3(mp[6], mp[7], mred));
                     const float mx = mxr * sl2;
                     // lazy maximum: keep the old one unless the row maximum grew by more than 2^8
                     const bool need = t > 0 && mx > m + 8.0f;
@@ -593,7 +628,7 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     tmem_wait_st();
                     l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
                 }
-                if (x == 0 && !tail && valid < TK) {
+                if (!FP8 && x == 0 && !tail && valid < TK) {
                     // a unit's last prompt tile: zero V rows past the valid keys (stale or garbage rows
                     // times P = 0 must not produce NaN); block A's warps, before block A's P*V, which the
                     // tensor core issues before block B's
@@ -619,7 +654,7 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (!ok) break;
             tc_fence_after();
             if (warp_live) {
-                const float inv = 1.0f / l;
+                const float inv = p.v_scale / l;  // the values' E4M3 scale (1 over 16-bit pools)
                 if (cur.fused) {
                     // the request's whole key set went through this unit: the final O (q dtype) and LSE
                     const long long rh = (static_cast<long long>(cur.row_off) + wb) * p.Hq + cur.g * p.G + jh;
@@ -670,14 +705,15 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
         }
     } else {
-        // ================= tail tiles =================
-        constexpr int CH = D / 8;     // 16-byte chunks of a K or V row
+        // ================= tail tiles (over E4M3 pools also the widening of every prompt tile) =================
+        constexpr int CH = D / 8;     // 16-byte chunks of a 16-bit K or V row
         constexpr int RPS = 64 / CH;  // rows one pass of the 64 threads covers
+        constexpr int EB = FP8 ? 1 : 2;  // bytes per pool element
         const int gtid = tid - C::GATHER_TID0;
         const int kc = gtid % CH;
         const int rsub = gtid / CH;
-        const uint16_t* k_pool = static_cast<const uint16_t*>(p.k_pool);
-        const uint16_t* v_pool = static_cast<const uint16_t*>(p.v_pool);
+        const uint8_t* k_pool = static_cast<const uint8_t*>(p.k_pool);
+        const uint8_t* v_pool = static_cast<const uint8_t*>(p.v_pool);
         // pool rows of this thread's two key columns (gtid, gtid + 64) of each tail tile of a unit,
         // resolved a unit ahead; -1 past the request's tail keys or when unreadable
         int res[kWideMaxTailTiles][2];
@@ -706,9 +742,9 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     } else {
                         // the gather runs at the end of the unit: bring the row's K and V into L2 now
 #pragma unroll
-                        for (int off = 0; off < D * 2; off += 128) {
-                            prefetch_l2(static_cast<const uint8_t*>(p.k_pool) + static_cast<long long>(r) * (D * 2) + off);
-                            prefetch_l2(static_cast<const uint8_t*>(p.v_pool) + static_cast<long long>(r) * (D * 2) + off);
+                        for (int off = 0; off < D * EB; off += 128) {
+                            prefetch_l2(k_pool + static_cast<long long>(r) * (D * EB) + off);
+                            prefetch_l2(v_pool + static_cast<long long>(r) * (D * EB) + off);
                         }
                     }
                     res[n][h] = r;
@@ -724,6 +760,29 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         for (int k = 0; k < nunits && ok; ++k) {
             const int ptiles = prompt_tiles<TK>(cur);
             const int ntt = wide_tail_tiles(cur);
+            if constexpr (FP8) {
+                // each prompt tile: K, then V, once its E4M3 tile has landed, widened in place and handed
+                // to the tensor core (these warps take every phase of the E4M3 barriers in order, and a
+                // slot's next E4M3 load waits for the tensor core to release this tile)
+                for (int t = 0; t < ptiles && ok; ++t) {
+                    const int g2 = gt + t;
+                    const int valid = min(TK, cur.key_end - (cur.key_begin + t * TK));
+                    for (int tensor = 0; tensor < 2; ++tensor) {
+                        uint64_t* full8 = tensor == 0 ? &bars->k8_full[g2 % KST] : &bars->v8_full[g2 % VST];
+                        const uint32_t ph = tensor == 0 ? (g2 / KST) & 1 : (g2 / VST) & 1;
+                        ok = mbar_wait(full8, ph, abort_flag, kWideWaitNs);
+                        ok = __all_sync(FULL, ok);
+                        ok = gather_sync_and(ok);
+                        if (!ok) break;
+                        widen_e4m3_tile<D, TK, BF16>(tensor == 0 ? k_tile(g2) : v_tile(g2), valid, gtid, 1);
+                        fence_proxy_async_smem();
+                        ok = gather_sync_and(ok);
+                        if (!ok) break;
+                        if (gtid == 0) mbar_arrive(tensor == 0 ? &bars->k_full[g2 % KST] : &bars->v_full[g2 % VST]);
+                    }
+                }
+                if (!ok) break;
+            }
 #pragma unroll
             for (int n = 0; n < kWideMaxTailTiles; ++n) {
                 if (n >= ntt) break;
@@ -747,13 +806,23 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         const int c = rsub + i * RPS;
                         const int r = trow[c];
                         // the layout of a TMA box with 128-byte swizzle: chunk kc of row c in column half kc / 8
-                        const uint32_t off = (kc >> 3) * (TK * 128) + c * 128 + (((kc & 7) ^ (c & 7)) << 4);
-                        const long long e = static_cast<long long>(r < 0 ? 0 : r) * D + kc * 8;
-                        const uint32_t nb = r < 0 ? 0u : 16u;  // absent keys are zero rows
-                        cp_async16(kt + off, k_pool + e, nb);
-                        cp_async16(vt + off, v_pool + e, nb);
+                        const uint32_t off = sw128_chunk<TK>(kc, c);
+                        const long long e = static_cast<long long>(r < 0 ? 0 : r) * D + kc * 8;  // element offset
+                        if constexpr (FP8) {
+                            uint4 kw = make_uint4(0, 0, 0, 0), vw = kw;  // absent keys are zero rows
+                            if (r >= 0) {
+                                kw = e4m3x8_to_16<BF16>(__ldg(reinterpret_cast<const uint2*>(k_pool + e)));
+                                vw = e4m3x8_to_16<BF16>(__ldg(reinterpret_cast<const uint2*>(v_pool + e)));
+                            }
+                            *reinterpret_cast<uint4*>(kt + off) = kw;
+                            *reinterpret_cast<uint4*>(vt + off) = vw;
+                        } else {
+                            const uint32_t nb = r < 0 ? 0u : 16u;  // absent keys are zero rows
+                            cp_async16(kt + off, k_pool + 2 * e, nb);
+                            cp_async16(vt + off, v_pool + 2 * e, nb);
+                        }
                     }
-                    cp_async_commit_wait_all();
+                    if constexpr (!FP8) cp_async_commit_wait_all();
                     fence_proxy_async_smem();
                 }
                 ok = gather_sync_and(ok);
@@ -783,38 +852,55 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool FP8>
 static cudaError_t prepare_wide_k() {
     using C = WideCfg<D>;
     static_assert(sizeof(WideBarriers) <= 512, "barrier block");
     cudaError_t e =
-        cudaFuncSetAttribute(prefix_wide_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaFuncSetAttribute(prefix_wide_kernel<D, BF16, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(prefix_wide_kernel<D, BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    return cudaFuncSetAttribute(prefix_wide_kernel<D, BF16, FP8>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                 cudaSharedmemCarveoutMaxShared);
 }
 
-cudaError_t prepare_wide(int head_dim, bool bf16) {
+template <int D, bool FP8>
+static cudaError_t prepare_wide_d(bool bf16) {
+    return bf16 ? prepare_wide_k<D, true, FP8>() : prepare_wide_k<D, false, FP8>();
+}
+
+cudaError_t prepare_wide(int head_dim, bool bf16, bool fp8) {
     switch (head_dim) {
-        case 64: return bf16 ? prepare_wide_k<64, true>() : prepare_wide_k<64, false>();
-        case 128: return bf16 ? prepare_wide_k<128, true>() : prepare_wide_k<128, false>();
+        case 64: return fp8 ? prepare_wide_d<64, true>(bf16) : prepare_wide_d<64, false>(bf16);
+        case 128: return fp8 ? prepare_wide_d<128, true>(bf16) : prepare_wide_d<128, false>(bf16);
         default: return cudaErrorInvalidValue;
     }
 }
 
+template <int D, bool BF16, bool FP8>
+static void launch_wide_k(int ctas, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const PrefixParams& p, cudaStream_t stream) {
+    prefix_wide_kernel<D, BF16, FP8><<<ctas, WideCfg<D>::THREADS, WideCfg<D>::SMEM, stream>>>(tq, tk, tv, p);
+}
+
+template <int D>
+static void launch_wide_d(bool bf16, bool fp8, int ctas, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const PrefixParams& p, cudaStream_t stream) {
+    if (bf16) {
+        if (fp8) launch_wide_k<D, true, true>(ctas, tq, tk, tv, p, stream);
+        else launch_wide_k<D, true, false>(ctas, tq, tk, tv, p, stream);
+    } else {
+        if (fp8) launch_wide_k<D, false, true>(ctas, tq, tk, tv, p, stream);
+        else launch_wide_k<D, false, false>(ctas, tq, tk, tv, p, stream);
+    }
+}
+
 cudaError_t launch_wide(int head_dim, bool bf16, int ctas, const CUtensorMap& tq, const CUtensorMap& tk,
-                        const CUtensorMap& tv, const PrefixParams& p, cudaStream_t stream) {
+                        const CUtensorMap& tv, const PrefixParams& p, cudaStream_t stream, bool fp8) {
     if (ctas == 0 || p.num_units == 0) return cudaSuccess;
     if (p.bq <= 0 || p.bq * p.G > 32) return cudaErrorInvalidValue;
     switch (head_dim) {
-        case 64:
-            if (bf16) prefix_wide_kernel<64, true><<<ctas, WideCfg<64>::THREADS, WideCfg<64>::SMEM, stream>>>(tq, tk, tv, p);
-            else prefix_wide_kernel<64, false><<<ctas, WideCfg<64>::THREADS, WideCfg<64>::SMEM, stream>>>(tq, tk, tv, p);
-            break;
-        case 128:
-            if (bf16) prefix_wide_kernel<128, true><<<ctas, WideCfg<128>::THREADS, WideCfg<128>::SMEM, stream>>>(tq, tk, tv, p);
-            else prefix_wide_kernel<128, false><<<ctas, WideCfg<128>::THREADS, WideCfg<128>::SMEM, stream>>>(tq, tk, tv, p);
-            break;
+        case 64: launch_wide_d<64>(bf16, fp8, ctas, tq, tk, tv, p, stream); break;
+        case 128: launch_wide_d<128>(bf16, fp8, ctas, tq, tk, tv, p, stream); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

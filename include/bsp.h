@@ -69,6 +69,10 @@ typedef enum bsp_status {
 } bsp_status;
 
 enum { BSP_DTYPE_BF16 = 0, BSP_DTYPE_FP16 = 1 };
+/* What the K/V pools hold (bsp_geometry.kv_dtype): elements of `dtype`, or one-byte FP8 E4M3 values
+   ("e4m3fn": 4 exponent bits with bias 7, 3 fraction bits, no infinities, max 448) in the same
+   [page][kv head][slot][head_dim] layout */
+enum { BSP_KV_DTYPE_SAME = 0, BSP_KV_DTYPE_E4M3 = 1 };
 
 /* bsp_decode_attn flags */
 enum {
@@ -102,7 +106,11 @@ typedef struct bsp_geometry {
     int32_t head_dim;     /* 64, 128 or 256 */
     int32_t page_size;    /* tokens per page: 8, 16, 32, 64 or 128 */
     int32_t num_pages;    /* pages in each pool */
-    int32_t dtype;        /* BSP_DTYPE_*; q, pools, o and new K/V share it */
+    int32_t dtype;        /* BSP_DTYPE_*; q, o and new K/V share it, and the pools unless kv_dtype says */
+    int32_t kv_dtype;     /* BSP_KV_DTYPE_*: 0 (the pools hold `dtype`), or E4M3 pools, which decode
+                             plans at head_dim 64 and 128 support (bsp_decode_attn_fp8; the writes:
+                             bsp_append_kv_fp8, bsp_rope_append_kv_fp8); any other use returns
+                             BSP_ERR_UNSUPPORTED */
 } bsp_geometry;
 
 /*
@@ -287,7 +295,8 @@ BSP_API bsp_status bsp_append_kv(const bsp_plan_t* plan, const void* k_new, cons
  *   src_row_stride  elements of the source type between rows, >= num_kv_heads
  *                   * head_dim, rows 16-byte aligned (a multiple of 8 for a
  *                   16-bit source, of 16 for E4M3)
- * The attention entry points read 16-bit pools only.
+ * The plan may have either kv_dtype (the pools passed here are E4M3 either way);
+ * bsp_decode_attn_fp8 reads such pools.
  */
 enum { BSP_FP8_SRC_16BIT = 0, BSP_FP8_SRC_E4M3 = 1 };
 BSP_API bsp_status bsp_append_kv_fp8(const bsp_plan_t* plan, const void* k_new, const void* v_new,
@@ -404,6 +413,32 @@ BSP_API bsp_status bsp_decode_attn(const bsp_plan_t* plan, const void* q, const 
                            void* const* events, void* stream);
 
 /*
+ * bsp_decode_attn over FP8 E4M3 pools (TensorRT-LLM PR #18614, the review
+ * follow-up commit on the fused KV write: a KV cache kept in 8 bits, written by
+ * bsp_append_kv_fp8). The plan's geometry has kv_dtype = BSP_KV_DTYPE_E4M3 (and
+ * head_dim 64 or 128); k_pool and v_pool hold one byte per element. Key and
+ * value element x of the pools stand for e4m3(x) * k_scale and
+ * e4m3(x) * v_scale (per-tensor scales, finite and > 0; 1 and 1 read the codes
+ * as they are). The result is the decode attention of bsp_decode_attn over
+ * those keys and values:
+ *   O   = softmax(softmax_scale * k_scale * q . e4m3(K)) e4m3(V) * v_scale
+ *   LSE = log-sum-exp of softmax_scale * k_scale * q . e4m3(K)
+ * The kernels read the E4M3 tiles (half the bytes of the 16-bit pools) and
+ * widen them exactly to the q dtype in shared memory (every E4M3 value is a
+ * bf16 and a binary16 value), so the tensor-core products are those of the
+ * 16-bit path. A NaN code (0x7f, 0xff) in a key or value row that is read
+ * makes that row's output NaN. Other arguments, flags, events and errors as
+ * bsp_decode_attn; a plan whose pools are not E4M3 is BSP_ERR_INVALID_ARG here,
+ * and an E4M3 plan is BSP_ERR_INVALID_ARG for bsp_decode_attn, bsp_append_kv
+ * and bsp_rope_append_kv.
+ */
+BSP_API bsp_status bsp_decode_attn_fp8(const bsp_plan_t* plan, const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* beam_pages, int32_t beam_pages_stride,
+                               const int32_t* cache_indirection, int32_t max_seq, float softmax_scale,
+                               float k_scale, float v_scale, int32_t flags, void* o, float* lse,
+                               void* const* events, void* stream);
+
+/*
  * Prefill over the cached prefix (TensorRT-Model-Connect PR #2202, "prefill and
  * decode over the cached prefix, not the whole KV allocation", Implementation:
  * the prompt rows attend the bound cache rows and then the prompt rows, with
@@ -495,7 +530,8 @@ BSP_API bsp_status bsp_read_device_status(const bsp_plan_t* plan, void* stream, 
  * Inputs, outputs, layouts, flags (BSP_FLAG_LSE_BASE2, BSP_FLAG_CHECK) and
  * errors are otherwise those of bsp_plan and bsp_decode_attn; the plan arrays
  * are host memory, every other pointer device memory. The plan image is copied
- * from host memory that is not page-locked.
+ * from host memory that is not page-locked. 16-bit pools only: a geometry with
+ * E4M3 pools is BSP_ERR_UNSUPPORTED here.
  */
 BSP_API bsp_status bsp_decode_attn_noalloc(const bsp_geometry* geo, int32_t batch, int32_t beam_width,
                                            const int32_t* prefix_len, const int32_t* tail_len,

@@ -324,6 +324,50 @@ def test_plan_struct_layout_matches_header(lib):
     assert ctypes.sizeof(bsp.Plan) % 8 == 0
 
 
+def test_geometry_struct_layout_matches_header(lib):
+    text = open(os.path.join(ROOT, "include", "bsp.h")).read()
+    body = text[text.index("typedef struct bsp_geometry"):text.index("} bsp_geometry;")]
+    fields = re.findall(r"^\s+int32_t\s+(\w+);", body, flags=re.M)
+    assert fields == [f[0] for f in bsp.Geometry._fields_]
+
+
+def test_e4m3_pool_plans(lib):
+    """Plans over E4M3 pools use the kernels that widen E4M3 tiles: the wide kernel for 129-256 query rows
+    per (request, kv head), else alternating-tile row blocks of at most 4 * floor(32 / G) beams; head_dim
+    256, prefill and an unknown pool type are unsupported."""
+    def plan8(Hq, Hkv, W, D=128, B=3, T=2):
+        g = bsp.geometry(Hq, Hkv, D, 32, 5000, "bf16", kv_dtype=bsp.KV_DTYPE_E4M3)
+        P = [700, 90, 1]
+        pages = np.arange(B * 32, dtype=np.int32).reshape(B, 32)
+        return bsp.plan_build(g, B, W, P[:B], [T] * B, pages[:B], 8, 152)
+    for Hq, Hkv, W, layout, rb, wblk in [(16, 8, 30, 1, 1, 30), (16, 8, 96, 2, 1, 96), (24, 8, 42, 1, 2, 21),
+                                         (24, 8, 50, 2, 1, 50), (64, 8, 12, 1, 1, 12), (64, 8, 20, 2, 1, 20),
+                                         (8, 8, 128, 1, 1, 128), (64, 8, 40, 1, 3, 14)]:
+        plan, img = plan8(Hq, Hkv, W)
+        G = Hq // Hkv
+        # the workspace sized for this shape holds the plan
+        dev_bytes, host_bytes = bsp.workspace_size(
+            bsp.geometry(Hq, Hkv, 128, 32, 5000, "bf16", kv_dtype=bsp.KV_DTYPE_E4M3), 3, W, 32)
+        assert plan.device_bytes_used <= dev_bytes and 256 + 2 * plan.image_bytes <= host_bytes
+        assert (plan.layout, plan.row_blocks, plan.beams_per_block) == (layout, rb, wblk), (Hq, Hkv, W)
+        if layout == 1:
+            assert -(-wblk // 4) * G <= 32 and wblk * G <= 128
+        req, units, _ = decode_image(plan, img)
+        check_fused(plan, req, np.array([2, 2, 2]))
+        # the 16-bit plan of the same shape may pick another kernel, with the same request records' lengths
+        p16, img16 = bsp.plan_build(geo(Hq=Hq, Hkv=Hkv), 3, W, [700, 90, 1], [2, 2, 2],
+                                    np.arange(96, dtype=np.int32).reshape(3, 32), 8, 152)
+        np.testing.assert_array_equal(decode_image(p16, img16)[0][:, :2], req[:, :2])
+    with pytest.raises(bsp.BspError) as e:
+        plan8(16, 8, 30, D=256)
+    assert bsp.STATUS_NAMES[e.value.status] == "BSP_ERR_UNSUPPORTED"
+    g = bsp.geometry(16, 8, 128, 32, 5000, "bf16", kv_dtype=2)
+    assert _err(bsp.plan_build, g, 1, 4, [10], [1], np.zeros((1, 1), np.int32), 8, 152) == "BSP_ERR_UNSUPPORTED"
+    g = bsp.geometry(16, 8, 128, 32, 5000, "bf16", kv_dtype=bsp.KV_DTYPE_E4M3)
+    assert _err(bsp.plan_prefill_build, g, 1, [0], [20], np.zeros((1, 1), np.int32), True, 152) == \
+        "BSP_ERR_UNSUPPORTED"
+
+
 @pytest.mark.parametrize("causal", [True, False])
 def test_prefill_plan_units_and_records(lib, causal):
     """A prefill plan: the prompt tokens are the rows (blocks of 128 / G tokens), keys are the cached
