@@ -112,22 +112,23 @@ class Case:
 
 
 def e4m3_codes(shape, generator: torch.Generator, exp_mean: float = 7.0, exp_sd: float = 1.5,
-               zero_frac: float = 0.02) -> torch.Tensor:
+               zero_frac: float = 0.02, device="cpu") -> torch.Tensor:
     """Random E4M3 codes (uint8) for synthetic 8-bit pools, drawn as bit patterns: a random sign and
     3-bit fraction, the 4-bit exponent field drawn around exp_mean (bias 7: magnitudes near 1) and
     clipped to [0, 15] (0: the subnormal codes), a fraction zero_frac of +-0 codes, and the two NaN
     codes (exponent 15, fraction 7) replaced by the largest finite ones. Drawn in chunks of 2^24 codes
-    (the same codes for the same generator state)."""
-    out = torch.empty(int(np.prod(shape)), dtype=torch.uint8)
+    (the same codes for the same generator state) on `device`, the generator's device."""
+    out = torch.empty(int(np.prod(shape)), dtype=torch.uint8, device=device)
     chunk = 1 << 24
     for lo in range(0, out.numel(), chunk):
         n = min(chunk, out.numel() - lo)
-        sign = torch.randint(0, 2, (n,), generator=generator, dtype=torch.int32)
-        frac = torch.randint(0, 8, (n,), generator=generator, dtype=torch.int32)
-        expo = torch.round(torch.randn((n,), generator=generator) * exp_sd + exp_mean).clamp(0, 15).to(torch.int32)
+        sign = torch.randint(0, 2, (n,), generator=generator, dtype=torch.int32, device=device)
+        frac = torch.randint(0, 8, (n,), generator=generator, dtype=torch.int32, device=device)
+        expo = torch.round(torch.randn((n,), generator=generator, device=device) * exp_sd + exp_mean)
+        expo = expo.clamp(0, 15).to(torch.int32)
         frac = torch.where((expo == 15) & (frac == 7), torch.full_like(frac, 6), frac)
         code = (sign << 7) | (expo << 3) | frac
-        zero = torch.rand((n,), generator=generator) < zero_frac
+        zero = torch.rand((n,), generator=generator, device=device) < zero_frac
         out[lo:lo + n] = torch.where(zero, sign << 7, code).to(torch.uint8)
     return out.reshape(tuple(shape))
 

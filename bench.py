@@ -506,6 +506,7 @@ def main():
     # ---- RoPE and E4M3 appends, timed on their own after the step timing (they rewrite the new tokens' rows)
     rope_append = measure_rope_append(hb.sets, Kt, hbm_gbs)
     fp8_append = measure_fp8_append(hb.sets, Kt, hbm_gbs)
+    fp8_attention = measure_fp8_attention(hb.sets[0], Kt, hbm_gbs)
     launches = hb.launches(K)
     step_bytes = fr["prefix_bytes"] + statistics.mean(a["tail"] for a in hb.ab)
     prefix_units = int(hb.sets[0].plan.num_units)
@@ -536,6 +537,7 @@ def main():
         "e2e": e2e,
         "rope_append": rope_append,
         "fp8_append": fp8_append,
+        "fp8_attention": fp8_attention,
         "gpu_launches": launches * reps,
         "timing": f"value: median of {reps} repeats of a CUDA-graph replay of exactly K steps without timing "
                   f"nodes (spread in config.ms_per_step_spread); us_prefix (and the roofline), us_append: one event "
@@ -610,6 +612,52 @@ def measure_rope_append(sets, Kt, hbm_gbs):
     return {"kernel": "rope_append_kernel", "us": us, "gbs": gbs, "frac_of_hbm": gbs / hbm_gbs,
             "algorithmic_bytes_per_launch": b, "rotary_dim": wl.head_dim, "layout": "rotate-half",
             "timing": f"one event pair around {Kt} back-to-back launches (launch gaps included)"}
+
+
+def measure_fp8_attention(st, Kt, hbm_gbs):
+    """bsp_decode_attn_fp8 over E4M3 pools of the same shape as the set's 16-bit pools (random E4M3 codes,
+    k_scale = v_scale = 0.5): Kt launches back to back in one graph, one event pair around each of 5
+    replays (median). The pools (one byte per element) are larger than L2. Algorithmic bytes: the 16-bit
+    step's with the K/V rows at one byte per element."""
+    from beam_search_shared_gb300 import bsp, synth
+    from beam_search_shared_gb300.step import algorithmic_bytes
+    c = st.case
+    wl = c.workload
+    g = torch.Generator(device=st.q.device).manual_seed(4242)
+    k8 = synth.e4m3_codes(tuple(c.k_pool.shape), g, device=st.q.device)
+    v8 = synth.e4m3_codes(tuple(c.v_pool.shape), g, device=st.q.device)
+    geo = bsp.geometry(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.page_size, c.num_pages, wl.dtype,
+                       kv_dtype=bsp.KV_DTYPE_E4M3)
+    ws = bsp.Workspace(geo, wl.batch, wl.beam_width, c.prefix_pages.shape[1], device=st.q.device)
+    plan = ws.plan(geo, wl.batch, wl.beam_width, c.prefix_len, c.tail_len, c.prefix_pages, st.max_tail)
+
+    def launch(j):
+        bsp.decode_attn_fp8(plan, st.q, k8, v8, st.beam_pages, st.cache_indirection, st.scale, 0.5, 0.5, st.o,
+                            st.lse)
+
+    for j in range(3):
+        launch(j)
+    torch.cuda.synchronize()
+    assert bsp.read_device_status(plan) == (0, 0)
+    fused = bsp.plan_requests(*bsp.plan_build(geo, wl.batch, wl.beam_width, c.prefix_len, c.tail_len,
+                                              c.prefix_pages, st.max_tail, plan.num_sms))[:, 5] != 0
+    ab16 = algorithmic_bytes(c, fused)
+    # the 16-bit step's prompt-kernel bytes less half of every K/V row it reads
+    T = c.tail_len.astype(np.int64)
+    kv16 = ab16["prefix_kv"] + int(np.sum(T[fused])) * wl.beam_width * wl.num_kv_heads * wl.head_dim * 4
+    b = ab16["prefix"] - kv16 // 2
+    g_ = graph_of(launch, Kt)
+    us = 1e3 * statistics.median(time_graph(g_, 5, torch.cuda.current_stream())) / Kt
+    del g_
+    assert bsp.read_device_status(plan) == (0, 0)
+    gbs = b / (us / 1e6) / 1e9
+    kname = LAYOUT_KERNEL[int(plan.layout)][0]
+    out = {"kernel": f"{kname} (E4M3 pools)", "us": us, "gbs": gbs, "frac_of_hbm": gbs / hbm_gbs,
+           "algorithmic_bytes_per_launch": b, "tail_requests": int(plan.tail_requests),
+           "timing": f"one event pair around {Kt} back-to-back launches (launch gaps included), median of 5 replays"}
+    del k8, v8, ws
+    torch.cuda.empty_cache()
+    return out
 
 
 def measure_fp8_append(sets, Kt, hbm_gbs):
