@@ -127,28 +127,6 @@ __device__ __forceinline__ int alt_tail_tiles(const UnitInfo& ui, int wblk) {
     return (ui.fused && ui.T > 0) ? (alt_block_beams(ui, wblk) * ui.T + 127) / 128 : 0;
 }
 
-__device__ __forceinline__ void alt_st_release(int* p, int v) {
-    asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ int alt_ld_acquire(const int* p) {
-    int v;
-    asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-    return v;
-}
-// Waits until the shared counter *c exceeds n. Gives up (false) when *abort becomes non-zero or
-// timeout_ns passes.
-__device__ __forceinline__ bool alt_wait_counter(const int* c, int n, const volatile int* abort, uint64_t timeout_ns) {
-    if (alt_ld_acquire(c) > n) return true;
-    const uint64_t t0 = globaltimer_ns();
-    uint32_t spins = 0;
-    while (alt_ld_acquire(c) <= n) {
-        if ((++spins & 63u) == 0) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > timeout_ns) return false;
-        }
-    }
-    return true;
-}
 // Named barrier 1 over the 64 tail-tile threads, returning the AND of their flags. Every one of them
 // takes part in every call (a flag that is false makes them all stop together).
 __device__ __forceinline__ bool alt_gather_sync_and(bool ok) {
@@ -296,7 +274,7 @@ prefix_alt_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     }
                     ++ntail;
                     if (lane == 0) {
-                        alt_st_release(&bars->tail_granted, ntail);
+                        counter_release(&bars->tail_granted, ntail);
                         if constexpr (FP8) {
                             // no E4M3 tile here: complete the slots' E4M3 phases, which the widening warps
                             // skip for a tail tile, so that the phases keep counting the slot's tiles
@@ -837,7 +815,7 @@ prefix_alt_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const int gtt = gt + ptiles + nt;
                 // the producer hands the tile's K and V slots over once the previous tiles that used them
                 // are done
-                ok = alt_wait_counter(&bars->tail_granted, ntail, abort_flag, kAltWaitNs);
+                ok = counter_wait(&bars->tail_granted, ntail, abort_flag, kAltWaitNs);
                 ++ntail;
                 ok = __all_sync(FULL, ok);
                 int* trow = trow_of(gtt);

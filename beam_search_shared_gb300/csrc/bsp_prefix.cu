@@ -116,12 +116,12 @@ struct PrefixBarriers {
     uint64_t o_free[2];   // the epilogue of unit k has read O[k % NO]
     uint64_t st_full;     // row statistics of a unit written
     uint64_t st_empty;    // ... and read by the epilogue warps
-    uint64_t tail_go[2];    // tail tile n: its K and V ring slots are free (the producer)
-    uint64_t fill_done[2];  // ... each epilogue warp has stored its part of it
+    uint64_t fill_done[2];  // tail tile n: each epilogue warp has stored its part of it
     uint64_t tail_ready[2]; // ... and it is complete, with its key table (for the softmax)
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
+    int tail_granted;  // tail tiles whose ring slots the producer has handed to the epilogue warps
 };
 
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s without progress
@@ -210,12 +210,12 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_init(&bars->st_full, 4);   // one arrival per softmax warp
         mbar_init(&bars->st_empty, 4);  // one arrival per epilogue warp
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars->tail_go[i], 1);
             mbar_init(&bars->fill_done[i], 4);  // one arrival per epilogue warp
             mbar_init(&bars->tail_ready[i], 1);
         }
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
+        bars->tail_granted = 0;
         fence_mbar_init();
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
@@ -288,8 +288,10 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         ok = __all_sync(FULL, ok);
                         if (!ok) break;
                     }
-                    if (lane == 0) mbar_arrive(&bars->tail_go[ntail & 1]);
+                    // hand them over by a counter: the producer may run several tail tiles ahead of the
+                    // epilogue warps (short units, deep rings), which a parity wait could not follow
                     ++ntail;
+                    if (lane == 0) counter_release(&bars->tail_granted, ntail);
                     __syncwarp();
                     continue;
                 }
@@ -713,7 +715,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 // s_trow is free: the softmax finished the previous unit (its statistics were read).
                 const int gtt = gt + prompt_tiles<TK>(cur);
                 if (lrow_ok) s_trow[lrow] = trow;
-                ok = mbar_wait(&bars->tail_go[ntail & 1], (ntail >> 1) & 1, abort_flag, kWaitTimeoutNs);
+                ok = counter_wait(&bars->tail_granted, ntail, abort_flag, kWaitTimeoutNs);
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
                 uint8_t* kt = k_tile(gtt);

@@ -88,6 +88,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     return true;
 }
 
+// A monotonic counter in shared memory that hands work from one warp to others. Unlike a parity wait
+// on an mbarrier, which names the right phase only for a waiter that is never two phases behind,
+// "wait until the counter exceeds n" is right however far the producing warp has run ahead.
+__device__ __forceinline__ void counter_release(int* p, int v) {
+    asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int counter_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+// Waits until the shared counter *c exceeds n. Gives up (false) when *abort becomes non-zero or
+// timeout_ns passes.
+__device__ __forceinline__ bool counter_wait(const int* c, int n, const volatile int* abort, uint64_t timeout_ns) {
+    if (counter_acquire(c) > n) return true;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t spins = 0;
+    while (counter_acquire(c) <= n) {
+        if ((++spins & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) return false;
+        }
+    }
+    return true;
+}
+
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -171,3 +171,21 @@ def test_alt_shapes(kw, batch):
     wl = FOURB.scaled(batch).with_(prompt=(40, 1500), **kw)
     step = run(wl, 25 + batch, 1)
     check(step, sample_rows(wl, batch))
+
+
+# ------------------------------------------------------------------ layout 0: one softmax set
+@pytest.mark.parametrize("kw,batch", [
+    (dict(head_dim=64, page_size=16), 96),   # half-row layout at head_dim 64: K ring 6 deep, V ring 7
+    (dict(head_dim=64, page_size=8), 64),
+    (dict(), 96),                            # head_dim 128, half-row
+])
+def test_one_set_kernel_many_short_units_with_tail_tiles(kw, batch):
+    """Prompts of one key tile and fused tails in every unit: the producer runs several tail tiles ahead
+    of the epilogue warps that gather them (deep rings, short units), and the hand-over must follow."""
+    wl = synth.WORKLOADS["qwen3_0p6b_b64_w30"].scaled(batch).with_(**kw)
+    rng = np.random.default_rng(batch)
+    P = rng.integers(1, 129, batch).astype(np.int32)
+    T = rng.integers(1, 5, batch).astype(np.int32)
+    step = run(wl, 31 + batch, 0, prompt_lengths=P, tail_lengths=T)
+    assert step.plan.tail_requests == 0 and step.plan.num_units == batch * wl.num_kv_heads
+    check(step)
