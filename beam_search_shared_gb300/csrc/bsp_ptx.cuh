@@ -100,13 +100,17 @@ __device__ __forceinline__ int counter_acquire(const int* p) {
     return v;
 }
 // Waits until the shared counter *c exceeds n. Gives up (false) when *abort becomes non-zero or
-// timeout_ns passes.
+// timeout_ns passes. The waiting warp sleeps between polls (32 ns, doubling up to 256 ns): unlike an
+// mbarrier try_wait, a polling load keeps the warp issuing, and the warps that wait here share their
+// schedulers with softmax warps.
 __device__ __forceinline__ bool counter_wait(const int* c, int n, const volatile int* abort, uint64_t timeout_ns) {
     if (counter_acquire(c) > n) return true;
     const uint64_t t0 = globaltimer_ns();
-    uint32_t spins = 0;
+    uint32_t spins = 0, sleep_ns = 32;
     while (counter_acquire(c) <= n) {
-        if ((++spins & 63u) == 0) {
+        __nanosleep(sleep_ns);
+        sleep_ns = sleep_ns < 256 ? 2 * sleep_ns : 256;
+        if ((++spins & 15u) == 0) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > timeout_ns) return false;
         }

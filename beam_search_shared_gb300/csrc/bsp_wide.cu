@@ -99,9 +99,10 @@ struct WideCfg {
 
 struct WideBarriers {
     uint64_t k_full[8];
-    uint64_t k_empty[8];   // both blocks' Q*K^T of the tile completed
+    uint64_t k_empty[8];   // both blocks' Q*K^T of the tile completed (arrived by block B's warp 6)
     uint64_t v_full[8];
-    uint64_t v_empty[8];   // both blocks' P*V of the tile completed
+    uint64_t v_empty[8];   // both blocks' P*V of the tile completed (arrived by block B's warp 6 with the next
+                           // tile's S_B)
     uint64_t q_full[2];    // block X's Q of a unit landed
     uint64_t q_empty[2];   // ... and the unit's last Q*K^T of block X completed
     uint64_t s_full[2];    // Q*K^T into S_X completed
@@ -361,9 +362,10 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             int pend = -1;  // tile whose P*V is not issued yet
             bool pend_first = false, pend_last = false;
             bool ok = true;
+            // (V of tile j is waited for before block A's P: a wait that has already completed still costs
+            // a shared-memory round trip, which would otherwise sit between P and the MMAs)
             auto issue_pv = [&](int x, int j, bool first, bool last) -> bool {
                 if (!mbar_wait(&bars->p_full[x], j & 1, abort_flag, kWideWaitNs)) return false;
-                if (x == 0 && !mbar_wait(&bars->v_full[j % VST], (j / VST) & 1, abort_flag, kWideWaitNs)) return false;
                 tc_fence_after();
                 const uint32_t p_tmem = tmem + C::S_COL + x * TK;
                 const uint32_t o_tmem = tmem + C::O_COL + x * D;
@@ -373,7 +375,6 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     const uint64_t bd = sdesc_sw128(v_addr + kk * 16 * 128, TK * 128, 1024);
                     mma_f16_tmem_a(o_tmem, p_tmem + kk * 8, bd, ID_PV, (!first || kk > 0) ? 1u : 0u);
                 }
-                if (x == 1) mma_commit(&bars->v_empty[j % VST]);  // both blocks' P*V read V of tile j
                 if (last) mma_commit(&bars->o_final[x]);
                 return true;
             };
@@ -382,17 +383,17 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const int ntiles = prompt_tiles<TK>(ui) + wide_tail_tiles(ui);
                 for (int t = 0; t < ntiles; ++t, ++gt) {
                     const uint32_t k_addr = smem_u32(k_tile(gt));
+                    // the loads this tile's MMAs need, first: they do not depend on the softmax, and once
+                    // a block's P is ready its P*V and the next Q*K^T go out back to back
+                    ok = mbar_wait(&bars->k_full[gt % KST], (gt / KST) & 1, abort_flag, kWideWaitNs);
+                    if (ok && t == 0) ok = mbar_wait(&bars->q_full[0], k & 1, abort_flag, kWideWaitNs);
+                    if (ok && t == 0) ok = mbar_wait(&bars->q_full[1], k & 1, abort_flag, kWideWaitNs);
+                    if (ok && pend >= 0)
+                        ok = mbar_wait(&bars->v_full[pend % VST], (pend / VST) & 1, abort_flag, kWideWaitNs);
+                    if (!ok) break;
                     for (int x = 0; x < 2; ++x) {
                         if (pend >= 0) {
                             ok = issue_pv(x, pend, pend_first, pend_last);
-                            if (!ok) break;
-                        }
-                        if (x == 0) {
-                            ok = mbar_wait(&bars->k_full[gt % KST], (gt / KST) & 1, abort_flag, kWideWaitNs);
-                            if (!ok) break;
-                        }
-                        if (t == 0) {
-                            ok = mbar_wait(&bars->q_full[x], k & 1, abort_flag, kWideWaitNs);
                             if (!ok) break;
                         }
                         // S_X holds P_X of the previous tile, whose P*V was issued just before
@@ -405,8 +406,9 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                             const uint64_t bd = sdesc_sw128(k_addr + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
                             mma_f16(tmem + C::S_COL + x * TK, ad, bd, ID_QK, kk > 0 ? 1u : 0u);
                         }
+                        // (the K and V slots are released by block B's softmax warp 6 once it sees S_B
+                        // complete)
                         mma_commit(&bars->s_full[x]);
-                        if (x == 1) mma_commit(&bars->k_empty[gt % KST]);  // both blocks read K of this tile
                         if (t == ntiles - 1) mma_commit(&bars->q_empty[x]);
                     }
                     if (!ok) break;
@@ -416,7 +418,8 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 }
             }
             if (ok && pend >= 0) {
-                ok = issue_pv(0, pend, pend_first, pend_last);
+                ok = mbar_wait(&bars->v_full[pend % VST], (pend / VST) & 1, abort_flag, kWideWaitNs);
+                if (ok) ok = issue_pv(0, pend, pend_first, pend_last);
                 if (ok) ok = issue_pv(1, pend, pend_first, pend_last);
             }
             if (!ok) {
@@ -458,6 +461,15 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const bool tail = t >= ptiles;
                 const int valid = tail ? TK : min(TK, cur.key_end - (cur.key_begin + t * TK));
                 ok = mbar_wait(&bars->s_full[x], gt & 1, abort_flag, kWideWaitNs);
+                // S_B complete: every MMA the issuing thread issued before Q*K_gt^T -> S_B has completed:
+                // both blocks' Q*K^T of this tile and both blocks' P*V of the previous one. One thread of
+                // block B hands the K slot of this tile and the V slot of the previous tile back to the
+                // producer (no further commits in the MMA thread: a commit right after another holds the
+                // issuing thread until the first one's MMAs finish)
+                if (ok && warp == 6 && lane == 0) {
+                    mbar_arrive(&bars->k_empty[gt % KST]);
+                    if (gt >= 1) mbar_arrive(&bars->v_empty[(gt - 1) % VST]);
+                }
                 // a tail tile's key table is complete once its V slot is full
                 if (ok && tail) ok = mbar_wait(&bars->v_full[gt % VST], (gt / VST) & 1, abort_flag, kWideWaitNs);
                 ok = __all_sync(FULL, ok);
