@@ -104,14 +104,13 @@ struct PrefixCfg {
 
 struct PrefixBarriers {
     uint64_t k_full[8];
-    uint64_t k_empty[8];  // KST <= 8
+    uint64_t k_empty[8];  // KST <= 8; arrived by softmax warp 2 when it sees the tile's S complete
     uint64_t v_full[8];
-    uint64_t v_empty[8];  // VST <= 8
+    uint64_t v_empty[8];  // VST <= 8; the tile's P*V completed (also what a rescale of O waits for)
     uint64_t q_full[2];   // Q of unit k landed in shared-memory buffer k % NQ
     uint64_t q_empty[2];  // ... and its last Q*K^T completed
     uint64_t s_full[2];
     uint64_t p_full[2];   // tile t arrives on p_full[t % 2]
-    uint64_t o_done[2];   // P*V of tile t completes o_done[t % 2]
     uint64_t o_final[2];  // the last P*V of unit k completes o_final[k % 2]
     uint64_t o_free[2];   // the epilogue of unit k has read O[k % NO]
     uint64_t st_full;     // row statistics of a unit written
@@ -203,7 +202,6 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_init(&bars->q_empty[i], 1);  // the MMA thread, after the unit's last Q*K^T
             mbar_init(&bars->s_full[i], 1);
             mbar_init(&bars->p_full[i], 4);   // one arrival per softmax warp
-            mbar_init(&bars->o_done[i], 1);
             mbar_init(&bars->o_final[i], 1);
             mbar_init(&bars->o_free[i], 4);   // one arrival per epilogue warp
         }
@@ -363,9 +361,11 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             int pend = -1, pend_unit = 0;  // tile whose P*V is not issued yet, and its unit
             bool pend_first = false, pend_last = false;
             bool ok = true;
+            // (V first: its load does not depend on the softmax, and a wait that has already completed
+            // still costs a shared-memory round trip, which would otherwise sit between P and the MMAs)
             auto issue_pv = [&](int j, int unit, bool first, bool last) -> bool {
-                if (!mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, abort_flag, kWaitTimeoutNs)) return false;
                 if (!mbar_wait(&bars->v_full[j % VST], (j / VST) & 1, abort_flag, kWaitTimeoutNs)) return false;
+                if (!mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, abort_flag, kWaitTimeoutNs)) return false;
                 if (first && unit >= NO) {
                     // O[unit % NO] was last used by unit - NO: its epilogue must have read it
                     const int f = unit - NO;
@@ -380,7 +380,9 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     const uint64_t bd = sdesc_sw128(v_addr + kk * 16 * 128, TK * 128, 1024);
                     mma_f16_tmem_a(o_tmem, p_tmem + kk * 8, bd, ID_PV, (!first || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(&bars->o_done[j & 1]);
+                // one commit per batch of MMAs: a commit right after another holds this thread until the
+                // first one's MMAs finish. v_empty also tells the softmax that this P*V is done (its
+                // rescale of O), and the K slot is handed back by a softmax warp (s_full)
                 mma_commit(&bars->v_empty[j % VST]);
                 if (last) mma_commit(&bars->o_final[unit & 1]);
                 return true;
@@ -405,7 +407,6 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         mma_f16(tmem + C::S_COL + (gt & 1) * TK, ad, bd, ID_QK, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(&bars->s_full[gt & 1]);
-                    mma_commit(&bars->k_empty[gt % KST]);  // K of this tile has been read
                     if (t == ntiles - 1) mma_commit(&bars->q_empty[qb]);  // Q no longer read
                     if (pend >= 0) {
                         ok = issue_pv(pend, pend_unit, pend_first, pend_last);
@@ -455,6 +456,8 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const bool tail = t == ptiles;  // the tail tile (zero-filled past its keys)
                 const int valid = tail ? TK : min(TK, cur.key_end - (cur.key_begin + t * TK));
                 ok = mbar_wait(&bars->s_full[gt & 1], (gt >> 1) & 1, abort_flag, kWaitTimeoutNs);
+                // S complete: this tile's Q*K^T has read its K slot; one thread hands it back
+                if (ok && warp == 2 && lane == 0) mbar_arrive(&bars->k_empty[gt % KST]);
                 if (ok && tail) {
                     // the tail tile's key table (pool row per column, -1: none or unreadable)
                     ok = mbar_wait(&bars->tail_ready[ntail & 1], (ntail >> 1) & 1, abort_flag, kWaitTimeoutNs);
@@ -549,10 +552,11 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         l *= alpha;
                     }
                     if (rescale) {
-                        // O is rescaled only after P*V of the previous tile has finished; P*V of
-                        // this tile waits for p_full. (Q*K^T of this tile completing implies P*V
-                        // two tiles back has, so the phase of o_done[(t-1) % 2] waited for is exact.)
-                        ok = mbar_wait(&bars->o_done[(gt - 1) & 1], ((gt - 1) >> 1) & 1, abort_flag, kWaitTimeoutNs);
+                        // O is rescaled only after P*V of the previous tile has finished (the release of
+                        // its V slot); P*V of this tile waits for p_full. (The slot's next phase needs
+                        // the P*V of tile gt - 1 + VST > gt, whose P this warp has not written yet, so
+                        // the phase waited for is exact.)
+                        ok = mbar_wait(&bars->v_empty[(gt - 1) % VST], ((gt - 1) / VST) & 1, abort_flag, kWaitTimeoutNs);
                         ok = __all_sync(FULL, ok);
                         if (ok) {
                             tc_fence_after();
