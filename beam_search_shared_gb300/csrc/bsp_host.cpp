@@ -207,13 +207,14 @@ struct PrefillSpec {
 
 // Whether the prompt kernel of plan layout `layout` finishes a decode request: its prompt is one partial
 // state (nsplit == 1) and the tail keys of one unit's beams (wblk of them; all W for the wide kernel) fit
-// the kernel's tail tiles: up to 4 tiles of 128 keys (layouts 1 and 2), one prompt tile (layout 0).
+// the kernel's tail tiles: up to 4 tiles of 128 keys (layouts 1 and 2), up to 4 prompt tiles (layout 0:
+// 128 keys, 64 at head_dim 256).
 int64_t request_tail_tiles(int layout, int head_dim, int wblk, int32_t tail) {
     return ceil_div(static_cast<int64_t>(tail) * wblk, layout ? 128 : prefix_tile_keys(head_dim));
 }
 bool request_fused(int layout, int head_dim, int wblk, int32_t nsplit, int32_t tail) {
     return nsplit == 1 && request_tail_tiles(layout, head_dim, wblk, tail) <=
-                              (layout == 1 ? kAltMaxTailTiles : layout == 2 ? kWideMaxTailTiles : 1);
+                              (layout == 1 ? kAltMaxTailTiles : layout == 2 ? kWideMaxTailTiles : kPrefixMaxTailTiles);
 }
 
 // The plan image of a decode step (pf == nullptr: prefix_len / tail_len per request, beam_width rows

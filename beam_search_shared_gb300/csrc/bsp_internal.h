@@ -22,8 +22,8 @@ constexpr size_t kAlign = 256;
 // Plan image (int32 fields, offsets relative to the image start).
 constexpr int kImageHeaderBytes = 64;  // u64 generation, i32 batch, i32 num_units, ...
 // Per-request record.
-// kReqFused: the prompt kernel finishes the request (one prompt partial state, and every row block's tail
-// keys fit one extra key tile of the prompt kernel); the tail kernel skips it.
+// kReqFused: the prompt kernel finishes the request (one prompt partial state, and every unit's tail keys
+// fit the prompt kernel's tail tiles); the tail kernel skips it.
 // kReqRows: the request's query rows per (kv head, head in group) - beams for a decode step, prompt
 // tokens for a prefill; kReqRowOff: its first row of q / o (b * W, or the tokens of earlier requests);
 // kReqCausal: -1, or the cached rows C of a causal prefill (row t sees keys 0 .. C + t).
@@ -31,6 +31,9 @@ enum ReqField { kReqPrefix = 0, kReqTail = 1, kReqSplits = 2, kReqPartOff = 3, k
                 kReqRows = 8, kReqCausal = 9, kReqRowOff = 10, kReqFields = 12 };
 // keys per tile of the prompt kernel, which bounds a row block's tail keys for the fused tail
 constexpr int prefix_tile_keys(int head_dim) { return head_dim <= 128 ? 128 : 64; }
+// tail tiles of prefix_tile_keys(head_dim) keys the one-set prompt kernel may gather for a unit (the
+// request is finished by the tail kernel beyond)
+constexpr int kPrefixMaxTailTiles = 4;
 // Beams per TMEM lane quadrant when the prompt kernel places a row block's query rows in lanes
 // 0-15 of each quadrant and gives each row two softmax threads (half of the keys each): the
 // block's beams spread over the four quadrants, at most 16 rows each, with 128-key tiles. 0 when

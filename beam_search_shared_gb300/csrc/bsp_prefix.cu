@@ -45,15 +45,17 @@
 //   warps 6-9  epilogue: once a unit's last P*V is done, write the normalised
 //              fp32 partial O and its log2-sum-exp2, then release that O
 //              buffer. For a request the plan marks fused (its prompt is one
-//              key range and each row block's beams hold at most TK tail keys
-//              together) the unit ends with a tail tile: the epilogue warps
-//              resolve each tail key through cache_indirection and the beam's
-//              page table, copy its K and V rows into the ring slots the
-//              producer leaves free (16-byte cp.async into the swizzled layout
-//              a TMA box would have; absent keys are zero rows), and publish a
-//              key -> pool-row table; the softmax keeps only a row's own beam's
-//              keys of that tile. Such a unit writes the final O (q dtype) and
-//              LSE of its rows, and the tail kernel skips the request.
+//              key range and each row block's beams hold at most 4 * TK tail
+//              keys together) the unit ends with up to four tail tiles (the
+//              block's tail keys, beam-major): the epilogue warps resolve each
+//              tail key through cache_indirection and the beam's page table,
+//              copy its K and V rows into the ring slots the producer hands
+//              over (by a counter; 16-byte cp.async into the swizzled layout a
+//              TMA box would have; absent keys are zero rows), and publish
+//              which keys are readable (one byte per key column and tile); the
+//              softmax keeps only a row's own beam's keys of a tail tile. Such
+//              a unit writes the final O (q dtype) and LSE of its rows, and the
+//              tail kernel skips the request.
 // TMEM columns: S0 [0,TK), S1 [TK,2TK) (P_t aliases the first TK/2 columns of
 // S[t%2]: tcgen05.mma instructions issued by one thread execute in issue
 // order, and the Q*K^T that overwrites S[t%2] is issued after the P*V that
@@ -116,7 +118,8 @@ struct PrefixBarriers {
     uint64_t st_full;     // row statistics of a unit written
     uint64_t st_empty;    // ... and read by the epilogue warps
     uint64_t fill_done[2];  // tail tile n: each epilogue warp has stored its part of it
-    uint64_t tail_ready[2]; // ... and it is complete, with its key table (for the softmax)
+    uint64_t tail_ready[8]; // tail tile n complete, with its key-validity words: barrier n % 8 (the epilogue
+                            // warps run at most KST < 8 tail tiles ahead of the softmax)
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -126,12 +129,16 @@ struct PrefixBarriers {
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s without progress
 constexpr uint64_t kDrainNs = 200000000ull;
 
-// a fused unit with tail positions ends with one tile of its beams' tail keys, beam-major:
-// key column c = w_local * T + t
-__device__ __forceinline__ bool has_tail_tile(const UnitInfo& ui) { return ui.fused && ui.T > 0; }
+// a fused unit with tail positions ends with ceil(W_blk * T / TK) (at most kPrefixMaxTailTiles) tiles of
+// its beams' tail keys, beam-major: key column c = w_local * T + t of the unit's tail key list
 template <int TK>
-__device__ __forceinline__ int unit_tiles(const UnitInfo& ui) {
-    return prompt_tiles<TK>(ui) + (has_tail_tile(ui) ? 1 : 0);
+__device__ __forceinline__ int tail_tiles(const UnitInfo& ui, int wblk) {
+    if (!(ui.fused && ui.T > 0)) return 0;
+    return (min(wblk, ui.rows - ui.rb * wblk) * ui.T + TK - 1) / TK;
+}
+template <int TK>
+__device__ __forceinline__ int unit_tiles(const UnitInfo& ui, int wblk) {
+    return prompt_tiles<TK>(ui) + tail_tiles<TK>(ui, wblk);
 }
 
 template <int D, bool BF16, bool SPLIT>
@@ -142,6 +149,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     constexpr int TK = C::TK, NC = C::NC, NQ = C::NQ, KST = C::KST, VST = C::VST, NO = C::NO, MR = C::MR;
     constexpr unsigned FULL = 0xffffffffu;
     static_assert(!SPLIT || TK == 128, "half-row softmax: 128-key tiles");
+    static_assert(KST < 8, "tail_ready: the epilogue warps run at most KST tail tiles ahead of the softmax");
     // Score, probability and output columns a thread handles: all of its row's (dense), or half of
     // them with two threads per row (SPLIT: query rows in TMEM lanes 0-15 of each quadrant, threads
     // t and t + 16 of a warp on the same row through the 16x32bx2 access shape)
@@ -166,7 +174,9 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     auto v_tile = [&](int gt) -> uint8_t* { return smem + C::OFF_V + (gt % VST) * C::KV_BYTES; };
     float* st_m = reinterpret_cast<float*>(smem + C::OFF_STATS);  // [128]
     float* st_l = st_m + kRowsPerBlock;                            // [128]
-    int* s_trow = reinterpret_cast<int*>(smem + C::OFF_TROW);     // [TK] pool row of tail key, -1: none
+    // [kPrefixMaxTailTiles][TK]: per tail tile of the current unit and key column, 1 if the key is readable
+    uint8_t* s_tok = smem + C::OFF_TROW;
+    static_assert(kPrefixMaxTailTiles * TK <= TK * 4, "tail-key flags fit the table area");
     PrefixBarriers* bars = reinterpret_cast<PrefixBarriers*>(smem + C::OFF_BAR);
     volatile int* abort_flag = &bars->abort_flag;
 
@@ -209,8 +219,8 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_init(&bars->st_empty, 4);  // one arrival per epilogue warp
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->fill_done[i], 4);  // one arrival per epilogue warp
-            mbar_init(&bars->tail_ready[i], 1);
         }
+        for (int i = 0; i < 8; ++i) mbar_init(&bars->tail_ready[i], 1);
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         bars->tail_granted = 0;
@@ -268,7 +278,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                     ui.g * p.G, ui.row_off + ui.rb * p.Wblk);
                 }
             }
-            const int ntiles = unit_tiles<TK>(ui);
+            const int ntiles = unit_tiles<TK>(ui, p.Wblk);
             const int ptiles = prompt_tiles<TK>(ui);
             const int* pg = p.pages + ui.page_off;
             const int npages = (ui.P + ps - 1) >> p.ps_log2;
@@ -279,8 +289,8 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     ok = __all_sync(FULL, ok);
                     if (!ok) break;
                 }
-                if (t == ptiles) {
-                    // the unit's tail tile: the epilogue warps gather it once both slots are free
+                if (t >= ptiles) {
+                    // a tail tile: the epilogue warps gather it once both slots are free
                     if (gt >= VST) {
                         ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kWaitTimeoutNs);
                         ok = __all_sync(FULL, ok);
@@ -388,7 +398,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 return true;
             };
             for (int u = u_begin; u < u_end && ok; ++u, ++k) {
-                const int ntiles = unit_tiles<TK>(load_unit(p, u));
+                const int ntiles = unit_tiles<TK>(load_unit(p, u), p.Wblk);
                 const int qb = k % NQ;
                 ok = mbar_wait(&bars->q_full[qb], (k / NQ) & 1, abort_flag, kWaitTimeoutNs);
                 if (!ok) break;
@@ -442,10 +452,10 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         int gt = 0, ntail = 0;
         for (int k = 0; k < nunits && ok; ++k) {
             const UnitInfo cur = load_unit(p, u_begin + k);
-            const int ntiles = unit_tiles<TK>(cur);
+            const int ntiles = unit_tiles<TK>(cur, p.Wblk);
             const int ptiles = prompt_tiles<TK>(cur);
             const int nw = min(p.Wblk, cur.rows - cur.rb * p.Wblk);  // beams (prompt tokens) of the block
-            // the row's own beam's keys in the tail tile: columns [lo, lo + T)
+            // the row's own beam's keys in the unit's tail key list: columns [lo, lo + T)
             const int lo = beam * cur.T, hi = lo + cur.T;
             const uint32_t o_col = C::O_COL + (k % NO) * D;
             // a warp whose 32 rows are all padding skips the arithmetic but keeps the
@@ -453,14 +463,18 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const bool warp_live = SPLIT ? quad * p.bq < nw : quad * 32 < nw * p.G;
             float m = -INFINITY, l = 0.f;
             for (int t = 0; t < ntiles; ++t, ++gt) {
-                const bool tail = t == ptiles;  // the tail tile (zero-filled past its keys)
+                const bool tail = t >= ptiles;  // a tail tile (zero-filled past its keys)
+                const int tn = t - ptiles;      // its index among the unit's tail tiles
                 const int valid = tail ? TK : min(TK, cur.key_end - (cur.key_begin + t * TK));
                 ok = mbar_wait(&bars->s_full[gt & 1], (gt >> 1) & 1, abort_flag, kWaitTimeoutNs);
                 // S complete: this tile's Q*K^T has read its K slot; one thread hands it back
                 if (ok && warp == 2 && lane == 0) mbar_arrive(&bars->k_empty[gt % KST]);
                 if (ok && tail) {
-                    // the tail tile's key table (pool row per column, -1: none or unreadable)
-                    ok = mbar_wait(&bars->tail_ready[ntail & 1], (ntail >> 1) & 1, abort_flag, kWaitTimeoutNs);
+                    // the tail tile's key-validity words. The epilogue warps gather tail tile n only once the
+                    // producer has the slot of the tile KST positions earlier back, which needs this
+                    // warp's S wait for that tile: they run at most KST < 8 tail tiles ahead, so a parity
+                    // wait on barrier n % 8 names the right phase.
+                    ok = mbar_wait(&bars->tail_ready[ntail & 7], (ntail >> 3) & 1, abort_flag, kWaitTimeoutNs);
                     ++ntail;
                 }
                 ok = __all_sync(FULL, ok);
@@ -483,10 +497,12 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     uint32_t km[TK / 32];
                     if (partial) {
                         uint64_t win = 0;
-                        const int wbase = lo & ~31;
+                        // the row's columns in this tail tile, [c0, c1)
+                        const int c0 = max(lo - tn * TK, 0), c1 = min(hi - tn * TK, TK);
+                        const int wbase = c0 & ~31;
                         if (tail)
-                            for (int c = lo; c < hi && c < TK; ++c)
-                                if (s_trow[c] >= 0) win |= 1ull << (c - wbase);
+                            for (int c = c0; c < c1; ++c)
+                                if (s_tok[tn * TK + c]) win |= 1ull << (c - wbase);
 #pragma unroll
                         for (int j = 0; j < TK / 32; ++j) {
                             const int n = min(max(rvalid - 32 * j, 0), 32);
@@ -674,14 +690,15 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int kc = lane % CH;
         const int lrow = quad * RPW + lane % RPW + (lane / RPW) * RS;
         const bool lrow_ok = lane / RPW < C::TAIL_CHUNKS;
-        // pool row of the tail key in column lrow of unit ui's tail tile (column c = w_local * T + t is
-        // position P_b + t of beam w0 + w_local, read through cache_indirection); -1 past the unit's
+        // pool row of the tail key in column n * TK + lrow of unit ui's tail key list (column c = w_local * T +
+        // t is position P_b + t of beam w0 + w_local, read through cache_indirection); -1 past the unit's
         // keys or when the source beam or its page is out of range
-        auto tail_row = [&](const UnitInfo& ui) -> int {
+        auto tail_row = [&](const UnitInfo& ui, int n) -> int {
             const int w0 = ui.rb * p.Wblk;
             const int nkeys = min(p.Wblk, p.W - w0) * ui.T;
-            if (!lrow_ok || lrow >= nkeys) return -1;
-            const int wl = lrow / ui.T, t = lrow - wl * ui.T;
+            const int cc = n * TK + lrow;
+            if (!lrow_ok || cc >= nkeys) return -1;
+            const int wl = cc / ui.T, t = cc - wl * ui.T;
             const int pos = ui.P + t;
             const int src = __ldg(p.ci + (static_cast<long long>(ui.b) * p.W + w0 + wl) * p.max_seq + pos);
             int r = -1;
@@ -708,25 +725,48 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         bool ok = true;
         int gt = 0, ntail = 0;
         UnitInfo cur;
-        int trow = -1;  // this lane's resolved tail row (lrow) of the unit `cur`
+        int trow[kPrefixMaxTailTiles];  // this lane's resolved tail rows (column n * TK + lrow) of the unit `cur`
+        // (loops over the tail tiles are not unrolled, and pick trow[n] by selects: one copy of their
+        // code, and trow stays in registers)
+        auto pick = [&](int n) -> int { return n == 0 ? trow[0] : n == 1 ? trow[1] : n == 2 ? trow[2] : trow[3]; };
+        static_assert(kPrefixMaxTailTiles == 4, "pick");
+        auto resolve = [&](const UnitInfo& ui) {
+            const int ntt = tail_tiles<TK>(ui, p.Wblk);
+#pragma unroll
+            for (int n = 0; n < kPrefixMaxTailTiles; ++n) trow[n] = -1;
+#pragma unroll 1
+            for (int n = 0; n < ntt; ++n) {
+                const int r = tail_row(ui, n);
+                trow[0] = n == 0 ? r : trow[0];
+                trow[1] = n == 1 ? r : trow[1];
+                trow[2] = n == 2 ? r : trow[2];
+                trow[3] = n == 3 ? r : trow[3];
+            }
+        };
         if (nunits > 0) {
             cur = load_unit(p, u_begin);
-            if (has_tail_tile(cur)) trow = tail_row(cur);
+            resolve(cur);
         }
         for (int k = 0; k < nunits && ok; ++k) {
-            if (has_tail_tile(cur)) {
-                // gather the unit's tail tile into the K and V ring slots the producer left for it.
-                // s_trow is free: the softmax finished the previous unit (its statistics were read).
-                const int gtt = gt + prompt_tiles<TK>(cur);
-                if (lrow_ok) s_trow[lrow] = trow;
+            // gather the unit's tail tiles into the K and V ring slots the producer hands over. The validity
+            // words of the unit's tail tiles are free: the softmax finished the previous unit (its
+            // statistics were read).
+            const int ntt = tail_tiles<TK>(cur, p.Wblk);
+#pragma unroll 1
+            for (int n = 0; n < ntt; ++n) {
+                const int gtt = gt + prompt_tiles<TK>(cur) + n;
                 ok = counter_wait(&bars->tail_granted, ntail, abort_flag, kWaitTimeoutNs);
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
+                const int myrow = pick(n);
+                if (lrow_ok) s_tok[n * TK + lrow] = myrow >= 0 ? 1 : 0;
                 uint8_t* kt = k_tile(gtt);
                 uint8_t* vt = v_tile(gtt);
-#pragma unroll 4
+                // (not unrolled: this code runs next to the softmax's, and a smaller instruction footprint
+                // keeps the softmax loop in the instruction cache)
+#pragma unroll 1
                 for (int i = 0; i < C::TAIL_CHUNKS; ++i) {
-                    const int r = __shfl_sync(FULL, trow, i * RPW + lane / CH);
+                    const int r = __shfl_sync(FULL, myrow, i * RPW + lane / CH);
                     const int c = quad * RPW + lane / CH + i * RS;
                     // the layout of a TMA box with 128-byte swizzle: chunk kc of row c in column half kc/8
                     const uint32_t off = (kc >> 3) * (TK * 128) + c * 128 + (((kc & 7) ^ (c & 7)) << 4);
@@ -741,11 +781,13 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 if (lane == 0) mbar_arrive(&bars->fill_done[ntail & 1]);
                 if (quad == 0) {
                     if (lane == 0) {
+                        // (each warp arrives for tail tile n + 2 only after arriving for n + 1, so this
+                        // warp's own arrival keeps the phase waited for exact)
                         ok = mbar_wait(&bars->fill_done[ntail & 1], (ntail >> 1) & 1, abort_flag, kWaitTimeoutNs);
                         if (ok) {
                             mbar_arrive(&bars->k_full[gtt % KST]);
                             mbar_arrive(&bars->v_full[gtt % VST]);
-                            mbar_arrive(&bars->tail_ready[ntail & 1]);
+                            mbar_arrive(&bars->tail_ready[ntail & 7]);
                         }
                     }
                     ok = __all_sync(FULL, ok);
@@ -753,7 +795,8 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 }
                 ++ntail;
             }
-            gt += unit_tiles<TK>(cur);
+            if (!ok) break;
+            gt += unit_tiles<TK>(cur, p.Wblk);
             const int w0 = cur.rb * p.Wblk;
             const int nw = min(p.Wblk, cur.rows - w0);
             // the thread's query row: TMEM lane orow, beam wl of the block, head jh of the group; with
@@ -775,7 +818,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const UnitInfo done = cur;
             if (k + 1 < nunits) {
                 cur = load_unit(p, u_begin + k + 1);
-                trow = has_tail_tile(cur) ? tail_row(cur) : -1;
+                resolve(cur);
             }
             ok = mbar_wait(&bars->o_final[k & 1], (k >> 1) & 1, abort_flag, kWaitTimeoutNs);
             ok = __all_sync(FULL, ok);

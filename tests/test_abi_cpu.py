@@ -138,14 +138,11 @@ def prompt_layout(D, W, G):
 def check_fused(plan, req, T, head_dim=128):
     """A request is finished by the prompt kernel iff it has one prompt partial state and its tail keys
     fit the kernel's tail tiles: a unit's beams' (a row block's, or all W for the two-block kernel) in at
-    most 4 tiles of 128 keys (layouts 1 and 2), else in one prompt-kernel tile (128 keys up to head_dim
-    128, 64 at 256)."""
+    most 4 tiles of 128 keys (layouts 1 and 2), else in at most 4 prompt-kernel tiles (128 keys up to
+    head_dim 128, 64 at 256)."""
     T = np.asarray(T)
-    if plan.layout in (1, 2):
-        want = (req[:, 2] == 1) & (-(-T * plan.beams_per_block // 128) <= 4)
-    else:
-        tile = 128 if head_dim <= 128 else 64
-        want = (req[:, 2] == 1) & (T * plan.beams_per_block <= tile)
+    tile = 128 if plan.layout in (1, 2) or head_dim <= 128 else 64
+    want = (req[:, 2] == 1) & (-(-T * plan.beams_per_block // tile) <= 4)
     np.testing.assert_array_equal(req[:, 5], want.astype(np.int32))
     assert plan.tail_requests == int((~want).sum())
 
@@ -407,9 +404,9 @@ def test_prefill_plan_units_and_records(lib, causal):
 
 def test_plan_requests_reads_whole_records(lib):
     """bsp.plan_requests returns the 12-field request records in order (the fused flag of a mixed
-    batch at head_dim 256: request 1 has more tail keys per row block than one 64-key tile holds)."""
-    g = geo(Hq=32, Hkv=8, D=256, ps=16, npages=4000, dtype="fp16")
-    B, W = 3, 30
+    batch at head_dim 256: request 1 has more tail keys per row block than four 64-key tiles hold)."""
+    g = geo(Hq=8, Hkv=8, D=256, ps=16, npages=4000, dtype="fp16")
+    B, W = 3, 64
     P = np.array([300, 500, 700], np.int32)
     T = np.array([2, 8, 0], np.int32)
     pages = np.arange(B * 64, dtype=np.int32).reshape(B, 64)
@@ -419,7 +416,7 @@ def test_plan_requests_reads_whole_records(lib):
     np.testing.assert_array_equal(req[:, 2], 1)
     np.testing.assert_array_equal(req[:, 0], P)
     np.testing.assert_array_equal(req[:, 1], T)
-    np.testing.assert_array_equal(req[:, 5], [1, 0, 1])       # 30 x 2 = 60 <= 64 < 30 x 8 = 240
+    np.testing.assert_array_equal(req[:, 5], [1, 0, 1])       # 64 x 2 = 128 <= 4 x 64 < 64 x 8 = 512
     np.testing.assert_array_equal(req[:, 10], np.arange(B) * W)
 
 

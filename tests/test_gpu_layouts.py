@@ -189,3 +189,24 @@ def test_one_set_kernel_many_short_units_with_tail_tiles(kw, batch):
     step = run(wl, 31 + batch, 0, prompt_lengths=P, tail_lengths=T)
     assert step.plan.tail_requests == 0 and step.plan.num_units == batch * wl.num_kv_heads
     check(step)
+
+
+@pytest.mark.parametrize("name,kw,batch", [
+    ("qwen3_4b_fp16_d256", dict(), 8),                          # 64-key tiles: 30 x 8 tail keys in 4 tiles
+    ("qwen3_0p6b_b64_w30", dict(), 16),                         # half-row: 30 x 8 in 2 tiles of 128
+    ("qwen3_0p6b_b64_w30", dict(head_dim=64, page_size=16), 16),
+    ("qwen3_4b_fp16_d256", dict(beam_width=21), 6),             # a partial last tail tile, odd beams
+])
+def test_one_set_kernel_several_tail_tiles(name, kw, batch):
+    """Fused units ending with up to four tail tiles (tails of up to 8 tokens), short and long prompts in
+    one batch; the request whose prompt is split over partial states goes to the tail kernel."""
+    wl = synth.WORKLOADS[name].scaled(batch).with_(**kw)
+    rng = np.random.default_rng(batch + len(kw))
+    P = rng.integers(1, 700, batch).astype(np.int32)
+    T = rng.integers(0, bsp.MAX_TAIL + 1, batch).astype(np.int32)
+    T[0], T[1] = bsp.MAX_TAIL, 5
+    step = run(wl, 61 + batch, 0, prompt_lengths=P, tail_lengths=T)
+    wblk = step.plan.beams_per_block
+    tile = 64 if wl.head_dim == 256 else 128
+    assert max(-(-int(t) * wblk // tile) for t in T) >= 2     # some unit has several tail tiles
+    check(step)

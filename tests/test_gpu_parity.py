@@ -160,14 +160,14 @@ def test_tail_lengths_mixed_and_boundary_crossing():
                                   "qwen3_4b_fp16_d256"])
 def test_prompt_kernel_finishes_short_requests(name):
     """Requests with one prompt partial state and few tail keys per row block are finished by the
-    prompt kernel (tail keys gathered as extra key tiles); the others, in the same batch, by the tail
-    kernel: the 3000-key prompt split over partial states always, the request with 5 x 30 tail keys
-    only where the kernel gathers one tail tile (the one-set kernel, layout 0)."""
+    prompt kernel (tail keys gathered as up to four extra key tiles: 5 x 30 tail keys take two 128-key
+    tiles, or three 64-key tiles at head_dim 256); the other, in the same batch, by the tail kernel: the
+    3000-key prompt split over partial states."""
     wl = synth.WORKLOADS[name].scaled(6)
     case = synth.make_case(wl, 84, full_step=True, device="cuda", prompt_lengths=[100, 128, 60, 3000, 31, 7],
                            tail_lengths=[2, 0, 5, 2, 2, 1])
     step = run_and_check(case)
-    assert step.plan.tail_requests == (2 if step.plan.layout == 0 else 1)
+    assert step.plan.tail_requests == 1
 
 
 def test_empty_sequences():
