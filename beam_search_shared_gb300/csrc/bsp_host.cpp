@@ -286,11 +286,17 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
 
     // ---- work units: (request, kv head, key split, query-row block)
     int nrb, wblk;
+    // prompt tokens per unit of a prefill: one MMA block of rows, or at head_dim <= 128 two of them (the
+    // two-block kernel, layout 2: both blocks' rows against the same K/V tiles)
+    int urows = 0;
     if (pf) {
-        // prompt tokens in blocks of one MMA's rows (dense layout: 128 rows = 128 / G tokens)
-        wblk = std::max(1, kRowsPerBlock / G);
+        // prompt tokens in blocks of one MMA's rows: 128 / G tokens (dense layout), or at head_dim <= 128
+        // 4 * floor(32 / G) tokens, 32 / G per TMEM lane quadrant, two blocks per unit
+        const bool two = geo->head_dim <= 128;
+        wblk = two ? 4 * (32 / G) : std::max(1, kRowsPerBlock / G);
+        urows = two ? 2 * wblk : wblk;
         nrb = 0;
-        for (int b = 0; b < batch; ++b) nrb = std::max<int>(nrb, static_cast<int>(ceil_div(rows[b], wblk)));
+        for (int b = 0; b < batch; ++b) nrb = std::max<int>(nrb, static_cast<int>(ceil_div(rows[b], urows)));
     } else {
         row_blocks(beam_width, G, &nrb, &wblk);
     }
@@ -318,7 +324,9 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
             }
             layout = 1;
         }
-    } else if (!pf && geo->head_dim <= 128 && prefix_quad_beams(geo->head_dim, wblk, G) == 0) {
+    } else if (pf) {
+        if (geo->head_dim <= 128) layout = 2;
+    } else if (geo->head_dim <= 128 && prefix_quad_beams(geo->head_dim, wblk, G) == 0) {
         if (wide_quad_beams(geo->head_dim, beam_width, G) > 0) {
             layout = 2;
             nrb = 1;
@@ -329,7 +337,8 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     }
     const bool alt = layout == 1;
     const int group = alt ? nrb : 1;
-    auto nrb_of = [&](int b) -> int { return pf ? static_cast<int>(ceil_div(rows[b], wblk)) : nrb; };
+    if (!pf) urows = wblk;
+    auto nrb_of = [&](int b) -> int { return pf ? static_cast<int>(ceil_div(rows[b], urows)) : nrb; };
     std::vector<int64_t> tiles(batch);
     int64_t total_tiles = 0, active = 0;
     for (int b = 0; b < batch; ++b) {
@@ -360,19 +369,21 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     // the plan tiles a unit reads: a causal prefill block stops at its last token's keys
     auto unit_end_tile = [&](int b, int rb, int32_t t1) -> int32_t {
         if (causal[b] < 0) return t1;
-        const int64_t last_row = std::min<int64_t>(rows[b], static_cast<int64_t>(rb + 1) * wblk);
+        const int64_t last_row = std::min<int64_t>(rows[b], static_cast<int64_t>(rb + 1) * urows);
         return static_cast<int32_t>(std::min<int64_t>(t1, ceil_div(causal[b] + last_row, kTileKeys)));
     };
     struct Unit {
         int32_t f[kUnitFields];
     };
     // time of a unit on the prompt kernel, in eighths of a key tile: its TK-key tiles (the last one
-    // partial, costed in full), its tail tiles, and half a tile for the unit's start and end
+    // partial, costed in full), its tail tiles, and the unit's start and end: half a tile, a whole one
+    // on the two-block kernel (its units write 256 output rows; measured there as about one tile)
+    const int64_t unit_ends = layout == 2 ? 8 : 4;
     auto unit_cost = [&](int b, int32_t t0, int32_t t1) -> int64_t {
         const int64_t keys = std::min<int64_t>(static_cast<int64_t>(t1) * kTileKeys, prefix_len[b]) -
                              static_cast<int64_t>(t0) * kTileKeys;
         const int64_t kt = ceil_div(keys, tk) + (fused(b) ? tail_tiles(b) : 0);
-        return 8 * kt + 4;
+        return 8 * kt + unit_ends;
     };
     std::vector<Unit> units;
     units.reserve(static_cast<size_t>(base_units + parts * Hkv * nrb));
@@ -1070,8 +1081,9 @@ bsp_status attn_launches(const bsp_plan_t* plan, uint8_t* ws, const void* q, con
         // query rows per TMA box: the row block, or a quadrant's share of it (half-row softmax; the wide
         // layout's quadrants)
         const int W = plan->beam_width;
+        // (a prefill on the two-block kernel: units of two blocks of beams_per_block prompt tokens)
         const int qbeams = alt    ? alt_quad_beams(D, plan->beams_per_block, G)
-                           : wide ? wide_quad_beams(D, W, G)
+                           : wide ? wide_quad_beams(D, prefill ? 2 * plan->beams_per_block : W, G)
                                   : (prefill ? 0 : prefix_quad_beams(D, plan->beams_per_block, G));
         if ((alt || wide) && qbeams <= 0) return BSP_ERR_INVALID_ARG;
         cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(G),
@@ -1107,7 +1119,7 @@ bsp_status attn_launches(const bsp_plan_t* plan, uint8_t* ws, const void* q, con
         pp.Hkv = Hkv;
         pp.G = G;
         pp.ps_log2 = ilog2(ps);
-        pp.Wblk = wide ? (W + 1) / 2 : plan->beams_per_block;  // beams of one MMA block
+        pp.Wblk = wide && !prefill ? (W + 1) / 2 : plan->beams_per_block;  // beams (prompt tokens) of one MMA block
         pp.bq = qbeams;
         pp.num_pages = geo.num_pages;
         pp.num_units = graph ? 1 : plan->num_units;  // (graph: launched whatever the captured plan holds)

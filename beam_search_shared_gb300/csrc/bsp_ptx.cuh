@@ -319,6 +319,13 @@ __device__ __forceinline__ void add2_acc(float& s0, float& s1, float a0, float a
         : "+f"(s0), "+f"(s1)
         : "f"(a0), "f"(a1));
 }
+// 32-byte global store of two 16-byte chunks in one 256-bit access (one whole 32-byte sector per thread);
+// ptr is 32-byte aligned
+__device__ __forceinline__ void st_global_v8(void* ptr, uint4 lo, uint4 hi) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ptr), "r"(lo.x), "r"(lo.y), "r"(lo.z),
+                 "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
+                 : "memory");
+}
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

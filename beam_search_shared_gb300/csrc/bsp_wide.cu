@@ -24,6 +24,12 @@
 // attention and the log-sum-exp merge are the same online softmax), other units
 // write fp32 partial states for the tail kernel.
 //
+// A prefill at head_dim <= 128 runs here too: a unit is (request b, kv head g,
+// pair of row blocks rb), block X holding prompt tokens [(2 rb + X) Wb,
+// (2 rb + X + 1) Wb), Wb = 4 floor(32 / G), and in a causal prefill each row
+// masks the keys past its own position (token t sees the C_b cached rows and
+// tokens 0 .. t). The pair reads each K/V tile once for up to 256 rows.
+//
 // Persistent: one CTA per SM walks the units the host dealt it; the K/V rings
 // are indexed by a tile counter that runs across units.
 //
@@ -325,7 +331,7 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                 for (int i = 0; i < 4; ++i)
                                     tma_load_3d(q_buf(x) + c * (kRowsPerBlock * 128) + i * 32 * 128, &tm_q,
                                                 &bars->q_full[x], c * 64, ui.g * p.G,
-                                                ui.row_off + x * p.Wblk + i * p.bq);
+                                                ui.row_off + (2 * ui.rb + x) * p.Wblk + i * p.bq);
                         }
                     }
                     if (!ok) break;
@@ -439,7 +445,6 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int wq = lane / p.G;           // beam of the quadrant
         const int jh = lane - wq * p.G;      // head of the group
         const int wbl = quad * p.bq + wq;    // beam of the block
-        const int wb = x * p.Wblk + wbl;     // beam of the request
         const bool row_ok = lane < qrows;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const uint32_t s_col = lane_base + C::S_COL + x * TK;
@@ -452,7 +457,10 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const UnitInfo cur = load_unit(p, u_begin + k);
             const int ptiles = prompt_tiles<TK>(cur);
             const int ntiles = ptiles + wide_tail_tiles(cur);
-            const int nw = min(p.Wblk, cur.rows - x * p.Wblk);  // beams of this block
+            // the block's first beam (prompt token of a prefill: units of two blocks each)
+            const int w0 = (2 * cur.rb + x) * p.Wblk;
+            const int wb = w0 + wbl;                    // beam of the request
+            const int nw = min(p.Wblk, cur.rows - w0);  // beams of this block (<= 0: none)
             const bool live = row_ok && wbl < nw;
             // a warp whose rows are all padding skips the arithmetic but keeps the barrier protocol
             const bool warp_live = quad * p.bq < nw;
@@ -480,7 +488,10 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     // partial prompt tile keeps [0, valid); a tail tile keeps the row's own beam's T
                     // columns (w * T - first column of the tile, T <= 8: at most two 32-bit words) whose
                     // key is readable
-                    const bool partial = valid < TK || tail;
+                    // a causal prefill row t sees keys 0 .. C + t: its own count of valid keys in this tile
+                    int rvalid = valid;
+                    if (cur.causal >= 0) rvalid = min(valid, cur.causal + wb + 1 - (cur.key_begin + t * TK));
+                    const bool partial = valid < TK || tail || (cur.causal >= 0 && __any_sync(FULL, rvalid < TK));
                     uint32_t km[TK / 32];
                     if (partial) {
                         if (tail) {
@@ -502,7 +513,7 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         } else {
 #pragma unroll
                             for (int j = 0; j < TK / 32; ++j) {
-                                const int n = min(max(valid - 32 * j, 0), 32);
+                                const int n = min(max(rvalid - 32 * j, 0), 32);
                                 km[j] = n == 32 ? ~0u : (1u << n) - 1u;
                             }
                         }
@@ -648,19 +659,27 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     // the request's whole key set went through this unit: the final O (q dtype) and LSE
                     const long long rh = (static_cast<long long>(cur.row_off) + wb) * p.Hq + cur.g * p.G + jh;
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + rh * D);
+                    // rows start at multiples of 128 bytes: 32-byte stores when o is 32-byte aligned
+                    const bool st32 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
 #pragma unroll 1
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t orr[32];
                         tmem_ld32(o_col + c0, orr);
                         tmem_wait_ld();
                         if (live) {
+                            uint4 w[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const float* f = reinterpret_cast<const float*>(orr) + 8 * e;
-                                dst[(c0 >> 3) + e] = make_uint4(pack2<BF16>(f[0] * inv, f[1] * inv),
-                                                                pack2<BF16>(f[2] * inv, f[3] * inv),
-                                                                pack2<BF16>(f[4] * inv, f[5] * inv),
-                                                                pack2<BF16>(f[6] * inv, f[7] * inv));
+                                w[e] = make_uint4(pack2<BF16>(f[0] * inv, f[1] * inv), pack2<BF16>(f[2] * inv, f[3] * inv),
+                                                  pack2<BF16>(f[4] * inv, f[5] * inv), pack2<BF16>(f[6] * inv, f[7] * inv));
+                            }
+                            if (st32) {
+                                st_global_v8(dst + (c0 >> 3), w[0], w[1]);
+                                st_global_v8(dst + (c0 >> 3) + 2, w[2], w[3]);
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) dst[(c0 >> 3) + e] = w[e];
                             }
                         }
                     }
@@ -677,12 +696,19 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         tmem_ld32(o_col + c0, orr);
                         tmem_wait_ld();
                         if (live) {
+                            // (the workspace's partial rows are 32-byte aligned)
 #pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                dst[(c0 >> 2) + e] =
-                                    make_float4(__uint_as_float(orr[4 * e]) * inv, __uint_as_float(orr[4 * e + 1]) * inv,
-                                                __uint_as_float(orr[4 * e + 2]) * inv,
-                                                __uint_as_float(orr[4 * e + 3]) * inv);
+                            for (int e = 0; e < 8; e += 2) {
+                                const uint4 lo = make_uint4(__float_as_uint(__uint_as_float(orr[4 * e]) * inv),
+                                                            __float_as_uint(__uint_as_float(orr[4 * e + 1]) * inv),
+                                                            __float_as_uint(__uint_as_float(orr[4 * e + 2]) * inv),
+                                                            __float_as_uint(__uint_as_float(orr[4 * e + 3]) * inv));
+                                const uint4 hi = make_uint4(__float_as_uint(__uint_as_float(orr[4 * e + 4]) * inv),
+                                                            __float_as_uint(__uint_as_float(orr[4 * e + 5]) * inv),
+                                                            __float_as_uint(__uint_as_float(orr[4 * e + 6]) * inv),
+                                                            __float_as_uint(__uint_as_float(orr[4 * e + 7]) * inv));
+                                st_global_v8(dst + (c0 >> 2) + e, lo, hi);
+                            }
                         }
                     }
                     if (live) p.part_lse[prow] = m + log2f(l);

@@ -877,7 +877,8 @@ def run_prefill(args, rank, world, local):
                    "us_prefill_attn": 1e3 * attn_ms, "prefill_attn_gbs": statistics.mean(w["bytes"] for w in work)
                    / (attn_ms / 1e3) / 1e9},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_tflops, "unit": "TFLOP/s",
-                     "frac": achieved / bf16_tflops, "traffic": None, "kernel": "prefix_attn_kernel",
+                     "frac": achieved / bf16_tflops, "traffic": None,
+                     "kernel": LAYOUT_KERNEL[int(sets[0].plan.layout)][0],
                      "peak_kind": peak_kind + " (16-bit dense; fp16 runs at the bf16 rate)",
                      "algorithmic_flops_per_launch": flops},
         "e2e": e2e,

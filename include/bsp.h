@@ -153,11 +153,14 @@ typedef struct bsp_plan_t {
     int32_t total_rows;          /* query rows of the step: batch * beam_width (decode) or the prompt
                                     tokens of all requests (prefill) */
     int32_t kind;                /* 0: a decode-step plan (bsp_plan); 1: a prefill plan (bsp_plan_prefill) */
-    int32_t layout;              /* prompt kernel of the plan: 0 one softmax warp set (prefill, head_dim
-                                    256, and row blocks of <= 64 query rows, two threads per row); 2 all
-                                    129-256 query rows of a (request, kv head) in one CTA as two MMA
-                                    blocks (the prompt read once); 1 two softmax warp sets taking a
-                                    unit's key tiles alternately (other decode steps at head_dim <= 128) */
+    int32_t layout;              /* prompt kernel of the plan: 0 one softmax warp set (head_dim 256, and
+                                    decode row blocks of <= 64 query rows, two threads per row); 2 two
+                                    MMA blocks in one CTA sharing every K/V tile: all 129-256 query rows
+                                    of a (request, kv head) of a decode step (the prompt read once), or
+                                    a prefill's prompt tokens at head_dim <= 128 in units of two blocks
+                                    of beams_per_block = 4 * floor(32 / G) tokens; 1 two softmax warp
+                                    sets taking a unit's key tiles alternately (other decode steps at
+                                    head_dim <= 128) */
     uint64_t off_cta;            /* byte offset of the per-CTA unit table */
     uint64_t reserved;
 } bsp_plan_t;

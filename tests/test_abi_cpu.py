@@ -243,9 +243,9 @@ def test_plan_image_wide_beam_one_unit_per_kv_head(lib):
     assert req[2][2] == 0                                            # empty prompt: no split, no unit
     check_fused(plan, req, T)
     assert list(req[:, 5]) == [1, 1, 0] and plan.tail_requests == 1
-    # dealing cost: the prompt tiles and ceil(96 T / 128) tail tiles
+    # dealing cost: the prompt tiles, ceil(96 T / 128) tail tiles and one tile for the unit's ends
     keys = np.minimum(units[:, 4] * 64, np.asarray(P)[units[:, 0]]) - units[:, 3] * 64
-    want = 8 * (-(-keys // 128) + -(-np.asarray(T)[units[:, 0]] * 96 // 128)) + 4
+    want = 8 * (-(-keys // 128) + -(-np.asarray(T)[units[:, 0]] * 96 // 128)) + 8
     np.testing.assert_array_equal(units[:, 6], want)
     plan, img = bsp.plan_build(geo(npages=200), B, W, P, [5, 6, 1], pages, 8, 8)
     req, _, _ = decode_image(plan, img)
@@ -366,21 +366,27 @@ def test_e4m3_pool_plans(lib):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-def test_prefill_plan_units_and_records(lib, causal):
-    """A prefill plan: the prompt tokens are the rows (blocks of 128 / G tokens), keys are the cached
-    rows and the prompt, no tail and no key splits; a causal block reads keys only up to its last
-    token (rounded up to a 64-key plan tile)."""
+@pytest.mark.parametrize("Hq,D", [(32, 128), (24, 64), (32, 256), (24, 256)])
+def test_prefill_plan_units_and_records(lib, causal, Hq, D):
+    """A prefill plan: the prompt tokens are the rows, keys are the cached rows and the prompt, no tail
+    and no key splits; a causal unit reads keys only up to its last token (rounded up to a 64-key plan
+    tile). At head_dim <= 128 a unit is a pair of row blocks of 4 * floor(32 / G) tokens on the two-block
+    kernel (layout 2), at head_dim 256 one block of floor(128 / G) tokens on the one-set kernel."""
     C = np.array([0, 300, 5, 40])
     S = np.array([1000, 7, 0, 200])
     ps = 32
     maxp = -(-(C + S).max() // ps)
     rng = np.random.default_rng(4)
     pages = rng.integers(0, 400, (4, maxp)).astype(np.int32)
-    g = geo(Hq=32, Hkv=8, npages=400)   # G = 4: blocks of 32 tokens
+    G = Hq // 8
+    g = geo(Hq=Hq, Hkv=8, D=D, npages=400)
     plan, img = bsp.plan_prefill_build(g, 4, C, S, pages, causal, 152)
     req, units, pl = decode_image(plan, img)
+    wblk = 4 * (32 // G) if D <= 128 else 128 // G
+    urows = 2 * wblk if D <= 128 else wblk
     assert plan.kind == 1 and plan.total_rows == S.sum() and plan.tail_requests == 0
-    assert plan.beams_per_block == 32 and plan.max_tail_len == 0
+    assert plan.beams_per_block == wblk and plan.max_tail_len == 0
+    assert plan.layout == (2 if D <= 128 else 0)
     np.testing.assert_array_equal(req[:, 0], np.where(S > 0, C + S, 0))
     np.testing.assert_array_equal(req[:, 1], 0)
     np.testing.assert_array_equal(req[:, 8], S)
@@ -391,8 +397,8 @@ def test_prefill_plan_units_and_records(lib, causal):
     want = set()
     for b in range(4):
         for gg in range(8):
-            for rb in range(-(-S[b] // 32)):
-                last = min(S[b], (rb + 1) * 32)
+            for rb in range(-(-S[b] // urows)):
+                last = min(S[b], (rb + 1) * urows)
                 end = -(-(C[b] + last) // 64) if causal else -(-(C[b] + S[b]) // 64)
                 want.add((b, gg, rb, 0, end))
     got = set(tuple(int(x) for x in u[:5]) for u in units)
@@ -522,9 +528,10 @@ def test_planner_random_sweep(lib):
 
 
 def test_prefill_planner_random_sweep(lib):
-    """Random prefill batches: one unit per (request, kv head, block of 128 / G prompt tokens) reading
-    plan tiles [0, end) with end the block's last visible key (causal) or the prompt's end, the request
-    records' rows / row offsets / causal bases, and a CTA table partitioning the units."""
+    """Random prefill batches: one unit per (request, kv head, run of prompt tokens: two blocks of
+    4 * floor(32 / G) at head_dim <= 128, one block of floor(128 / G) at head_dim 256) reading plan tiles
+    [0, end) with end the unit's last visible key (causal) or the prompt's end, the request records'
+    rows / row offsets / causal bases, and a CTA table partitioning the units."""
     rng = np.random.default_rng(77)
     for trial in range(60):
         Hkv = int(rng.choice([1, 2, 8]))
@@ -537,20 +544,23 @@ def test_prefill_planner_random_sweep(lib):
         S[rng.random(B) < 0.2] = 0
         maxp = max(1, int(-(-(C + S).max() // ps)))
         pages = rng.integers(0, 50000, (B, maxp)).astype(np.int32)
-        g = bsp.geometry(G * Hkv, Hkv, 128, ps, 50000, "bf16")
+        D = int(rng.choice([64, 128, 256]))
+        g = bsp.geometry(G * Hkv, Hkv, D, ps, 50000, "bf16")
         sms = int(rng.choice([16, 152]))
         plan, img = bsp.plan_prefill_build(g, B, C, S, pages, causal, sms)
         req, units, pl, cta = decode_image(plan, img, with_cta=True)
-        wblk = max(1, 128 // G)
+        wblk = 4 * (32 // G) if D <= 128 else 128 // G
+        urows = 2 * wblk if D <= 128 else wblk
         assert plan.kind == 1 and plan.total_rows == S.sum() and plan.beams_per_block == wblk
+        assert plan.layout == (2 if D <= 128 else 0)
         np.testing.assert_array_equal(req[:, 8], S)
         np.testing.assert_array_equal(req[:, 9], C if causal else -1)
         np.testing.assert_array_equal(req[:, 10], np.concatenate([[0], np.cumsum(S)[:-1]]))
         want = set()
         for b in range(B):
             for gg in range(Hkv):
-                for rb in range(-(-int(S[b]) // wblk)):
-                    last = min(int(S[b]), (rb + 1) * wblk)
+                for rb in range(-(-int(S[b]) // urows)):
+                    last = min(int(S[b]), (rb + 1) * urows)
                     end = -(-(int(C[b]) + last) // 64) if causal else -(-(int(C[b]) + int(S[b])) // 64)
                     want.add((b, gg, rb, 0, end))
         got = [tuple(int(x) for x in u[:5]) for u in units]

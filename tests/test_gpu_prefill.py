@@ -56,6 +56,11 @@ CASES = [
     ("prefill_text_b8", dict(batch=2, num_q_heads=8, num_kv_heads=8, page_size=8, prompt=(100, 180),
                              cached=(0, 90))),   # MHA: blocks of 128 tokens
     ("prefill_text_b8", dict(batch=2, num_q_heads=24, num_kv_heads=4, prompt=(5, 60), cached=(3, 60))),  # G 6
+    ("prefill_text_b8", dict(batch=3, num_q_heads=24, num_kv_heads=8, prompt=(30, 200), cached=(0, 400))),  # G 3
+    ("prefill_text_b8", dict(batch=2, num_q_heads=40, num_kv_heads=8, prompt=(50, 130), cached=(0, 100),
+                             causal=False)),     # G 5: blocks of 24 tokens, 30 rows per TMEM lane quadrant
+    ("prefill_text_b8", dict(batch=2, num_q_heads=8, num_kv_heads=8, head_dim=64, dtype="bf16", prompt=(250, 300),
+                             cached=(0, 64))),   # MHA at head_dim 64: units of 256 tokens
 ]
 
 
@@ -69,6 +74,21 @@ def test_prefill_empty_requests_and_empty_cache():
     wl = synth.PREFILL_WORKLOADS["prefill_text_b8"].with_(batch=4)
     case = synth.make_prefill_case(wl, 12, cached_lengths=[0, 50, 300, 0], prompt_lengths=[33, 0, 1, 64])
     run_and_check(case)
+
+
+@pytest.mark.parametrize("Hq,D", [(32, 128), (24, 64), (8, 128)])
+def test_prefill_two_block_unit_edges(Hq, D):
+    """Units of two row blocks (head_dim <= 128): prompts ending at a block's end, one token past it, at
+    the unit's end and one past it (the next unit's second block empty), cached rows ending inside a key
+    tile; the causal mask of each row follows its own position."""
+    wl = synth.PREFILL_WORKLOADS["prefill_text_b8"].with_(batch=6, num_q_heads=Hq, num_kv_heads=8, head_dim=D,
+                                                          dtype="bf16" if D == 64 else "fp16")
+    G = Hq // 8
+    wblk = 4 * (32 // G)
+    S = [wblk, wblk + 1, 2 * wblk, 2 * wblk + 1, 1, 3 * wblk + 5]
+    case = synth.make_prefill_case(wl, 15, cached_lengths=[0, 10, 130, 64, 0, 500], prompt_lengths=S)
+    step = run_and_check(case)
+    assert step.plan.layout == 2 and step.plan.beams_per_block == wblk
 
 
 def test_prefill_image_prompt_from_empty_cache():
