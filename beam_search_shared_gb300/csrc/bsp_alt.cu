@@ -696,19 +696,32 @@ prefix_alt_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                      : __uint_as_float(oa[e]) * fa;
                     if (live) {
                         if (cur.fused) {
-                            // the request's whole key set went through this unit: the final O (q dtype)
+                            // the request's whole key set went through this unit: the final O (q dtype);
+                            // rows start at multiples of 128 bytes: 32-byte stores when o is 32-byte aligned
                             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + rh * D);
+                            uint4 w[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                dst[(c0 >> 3) + e] = make_uint4(pack2<BF16>(f[8 * e], f[8 * e + 1]),
-                                                                pack2<BF16>(f[8 * e + 2], f[8 * e + 3]),
-                                                                pack2<BF16>(f[8 * e + 4], f[8 * e + 5]),
-                                                                pack2<BF16>(f[8 * e + 6], f[8 * e + 7]));
+                                w[e] = make_uint4(pack2<BF16>(f[8 * e], f[8 * e + 1]), pack2<BF16>(f[8 * e + 2], f[8 * e + 3]),
+                                                  pack2<BF16>(f[8 * e + 4], f[8 * e + 5]),
+                                                  pack2<BF16>(f[8 * e + 6], f[8 * e + 7]));
+                            if ((reinterpret_cast<uintptr_t>(p.o) & 31u) == 0) {
+                                st_global_v8(dst + (c0 >> 3), w[0], w[1]);
+                                st_global_v8(dst + (c0 >> 3) + 2, w[2], w[3]);
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) dst[(c0 >> 3) + e] = w[e];
+                            }
                         } else {
+                            // (the workspace's partial rows are 32-byte aligned)
                             float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                dst[(c0 >> 2) + e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2], f[4 * e + 3]);
+                            for (int e = 0; e < 8; e += 2)
+                                st_global_v8(dst + (c0 >> 2) + e,
+                                             make_uint4(__float_as_uint(f[4 * e]), __float_as_uint(f[4 * e + 1]),
+                                                        __float_as_uint(f[4 * e + 2]), __float_as_uint(f[4 * e + 3])),
+                                             make_uint4(__float_as_uint(f[4 * e + 4]), __float_as_uint(f[4 * e + 5]),
+                                                        __float_as_uint(f[4 * e + 6]), __float_as_uint(f[4 * e + 7])));
                         }
                     }
                 }

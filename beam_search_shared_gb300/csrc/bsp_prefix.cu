@@ -837,13 +837,21 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     ld_o(lane_base + o_col + c0, orr);
                     tmem_wait_ld();
                     if (live) {
+                        uint4 w[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float* f = reinterpret_cast<const float*>(orr) + 8 * e;
-                            dst[((cb + c0) >> 3) + e] = make_uint4(pack2<BF16>(f[0] * inv, f[1] * inv),
-                                                            pack2<BF16>(f[2] * inv, f[3] * inv),
-                                                            pack2<BF16>(f[4] * inv, f[5] * inv),
-                                                            pack2<BF16>(f[6] * inv, f[7] * inv));
+                            w[e] = make_uint4(pack2<BF16>(f[0] * inv, f[1] * inv), pack2<BF16>(f[2] * inv, f[3] * inv),
+                                              pack2<BF16>(f[4] * inv, f[5] * inv), pack2<BF16>(f[6] * inv, f[7] * inv));
+                        }
+                        // rows and column halves start at multiples of 64 bytes: 32-byte stores when o is
+                        // 32-byte aligned
+                        if ((reinterpret_cast<uintptr_t>(p.o) & 31u) == 0) {
+                            st_global_v8(dst + ((cb + c0) >> 3), w[0], w[1]);
+                            st_global_v8(dst + ((cb + c0) >> 3) + 2, w[2], w[3]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) dst[((cb + c0) >> 3) + e] = w[e];
                         }
                     }
                 }
@@ -861,11 +869,18 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     ld_o(lane_base + o_col + c0, orr);
                     tmem_wait_ld();
                     if (live) {
+                        // (the workspace's partial rows are 32-byte aligned)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            dst[((cb + c0) >> 2) + e] =
-                                make_float4(__uint_as_float(orr[4 * e]) * inv, __uint_as_float(orr[4 * e + 1]) * inv,
-                                            __uint_as_float(orr[4 * e + 2]) * inv, __uint_as_float(orr[4 * e + 3]) * inv);
+                        for (int e = 0; e < 8; e += 2)
+                            st_global_v8(dst + ((cb + c0) >> 2) + e,
+                                         make_uint4(__float_as_uint(__uint_as_float(orr[4 * e]) * inv),
+                                                    __float_as_uint(__uint_as_float(orr[4 * e + 1]) * inv),
+                                                    __float_as_uint(__uint_as_float(orr[4 * e + 2]) * inv),
+                                                    __float_as_uint(__uint_as_float(orr[4 * e + 3]) * inv)),
+                                         make_uint4(__float_as_uint(__uint_as_float(orr[4 * e + 4]) * inv),
+                                                    __float_as_uint(__uint_as_float(orr[4 * e + 5]) * inv),
+                                                    __float_as_uint(__uint_as_float(orr[4 * e + 6]) * inv),
+                                                    __float_as_uint(__uint_as_float(orr[4 * e + 7]) * inv)));
                     }
                 }
                 if (live && ohalf == 0) p.part_lse[prow] = m + log2f(l);

@@ -162,7 +162,7 @@ class PrefillStep:
 
 def prefill_work(case) -> dict:
     """Algorithmic bytes and flops of a prefill attention (the prompt kernel): each (request, kv head)
-    reads its keys' K and V once per block of rows that needs them, plus Q and O/LSE; the flops count
+    reads its keys' K and V once, plus Q and O/LSE; the flops count
     only the (row, key) pairs the mask keeps (Q*K^T and P*V, 2 flops per multiply-add)."""
     wl = case.workload
     e = 2
