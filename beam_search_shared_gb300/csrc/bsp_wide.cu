@@ -58,7 +58,12 @@
 //               bring their rows into L2), then copy K and V rows into the ring
 //               slots with 16-byte cp.async in the 128-byte-swizzled layout a
 //               TMA box would have (absent keys are zero rows), with a key ->
-//               pool-row table per V slot for the softmax's mask.
+//               pool-row table per V slot for the softmax's mask;
+//   warps 12-15 (E4M3 pools only, 512 threads): the producer loads each E4M3
+//               tile into the upper half of its 16-bit ring slot; warps 12-13
+//               widen every K tile, warps 14-15 every V tile, in place, to the
+//               q dtype, and complete the slot's full barrier (two streams, so
+//               a late V tile does not hold the next K tile back).
 // TMEM columns: S_A [0, 128), S_B [128, 256), O_A [256, 256 + D), O_B after it.
 // One S per block: Q K_{t+1}^T into S_X is issued after P_X V_t, and
 // tcgen05.mma instructions of one thread execute in issue order, so P_t (which
@@ -97,6 +102,10 @@ struct WideCfg {
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int THREADS = 384;
     static constexpr int GATHER_TID0 = 320;                  // warps 10-11
+    // over E4M3 pools four more warps (12-15, one per SM sub-partition) widen the prompt tiles: warps
+    // 12-13 every K tile, warps 14-15 every V tile, two streams that do not wait on each other
+    static constexpr int THREADS_E4M3 = 512;
+    static constexpr int CONV_TID0 = 384;
     static_assert(O_COL + 2 * D <= 512, "tensor memory");
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(KST <= 8 && VST <= 8, "barrier arrays");
@@ -130,6 +139,20 @@ __device__ __forceinline__ int wide_tail_tiles(const UnitInfo& ui) {
     return (ui.fused && ui.T > 0) ? (ui.rows * ui.T + 127) / 128 : 0;
 }
 
+// Named barrier `id` over `n` threads, returning the AND of their flags. Every one of them takes part in
+// every call (a flag that is false makes them all stop together).
+__device__ __forceinline__ bool named_sync_and(int id, int n, bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(ok)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
 // Named barrier 1 over the 64 tail-tile threads, returning the AND of their flags. Every one of them
 // takes part in every call (a flag that is false makes them all stop together).
 __device__ __forceinline__ bool gather_sync_and(bool ok) {
@@ -148,7 +171,7 @@ __device__ __forceinline__ bool gather_sync_and(bool ok) {
 }  // namespace
 
 template <int D, bool BF16, bool FP8>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(FP8 ? 512 : 384, 1)
 prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefixParams p) {
     using C = WideCfg<D>;
@@ -215,7 +238,7 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // padded rows stay finite
     {
         constexpr int NCHUNK = 2 * NC * kRowsPerBlock * 8;  // 16-byte chunks of the two Q buffers
-        for (int idx = tid; idx < NCHUNK; idx += C::THREADS) {
+        for (int idx = tid; idx < NCHUNK; idx += (FP8 ? C::THREADS_E4M3 : C::THREADS)) {
             const int r = (idx >> 3) & (kRowsPerBlock - 1);
             if ((r & 31) >= qrows) reinterpret_cast<uint4*>(smem)[idx] = make_uint4(0, 0, 0, 0);
         }
@@ -261,8 +284,9 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     if (lane == 0) {
                         counter_release(&bars->tail_granted, ntail);
                         if constexpr (FP8) {
-                            // no E4M3 tile here: complete the slots' E4M3 phases, which the widening warps
-                            // skip for a tail tile, so that the phases keep counting the slot's tiles
+                            // no E4M3 tile here: complete the slots' E4M3 phases (the widening warps wait
+                            // for every phase in order and have nothing to widen for a tail tile), so that
+                            // the phases keep counting the slot's tiles
                             mbar_arrive(&bars->k8_full[gt % KST]);
                             mbar_arrive(&bars->v8_full[gt % VST]);
                         }
@@ -719,8 +743,8 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             *abort_flag = 1;
             atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
         }
-    } else {
-        // ================= tail tiles (over E4M3 pools also the widening of every prompt tile) =================
+    } else if (warp < 12) {
+        // ================= tail tiles =================
         constexpr int CH = D / 8;     // 16-byte chunks of a 16-bit K or V row
         constexpr int RPS = 64 / CH;  // rows one pass of the 64 threads covers
         constexpr int EB = FP8 ? 1 : 2;  // bytes per pool element
@@ -775,29 +799,6 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         for (int k = 0; k < nunits && ok; ++k) {
             const int ptiles = prompt_tiles<TK>(cur);
             const int ntt = wide_tail_tiles(cur);
-            if constexpr (FP8) {
-                // each prompt tile: K, then V, once its E4M3 tile has landed, widened in place and handed
-                // to the tensor core (these warps take every phase of the E4M3 barriers in order, and a
-                // slot's next E4M3 load waits for the tensor core to release this tile)
-                for (int t = 0; t < ptiles && ok; ++t) {
-                    const int g2 = gt + t;
-                    const int valid = min(TK, cur.key_end - (cur.key_begin + t * TK));
-                    for (int tensor = 0; tensor < 2; ++tensor) {
-                        uint64_t* full8 = tensor == 0 ? &bars->k8_full[g2 % KST] : &bars->v8_full[g2 % VST];
-                        const uint32_t ph = tensor == 0 ? (g2 / KST) & 1 : (g2 / VST) & 1;
-                        ok = mbar_wait(full8, ph, abort_flag, kWideWaitNs);
-                        ok = __all_sync(FULL, ok);
-                        ok = gather_sync_and(ok);
-                        if (!ok) break;
-                        widen_e4m3_tile<D, TK, BF16>(tensor == 0 ? k_tile(g2) : v_tile(g2), valid, gtid, 1);
-                        fence_proxy_async_smem();
-                        ok = gather_sync_and(ok);
-                        if (!ok) break;
-                        if (gtid == 0) mbar_arrive(tensor == 0 ? &bars->k_full[g2 % KST] : &bars->v_full[g2 % VST]);
-                    }
-                }
-                if (!ok) break;
-            }
 #pragma unroll
             for (int n = 0; n < kWideMaxTailTiles; ++n) {
                 if (n >= ntt) break;
@@ -857,6 +858,41 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             *abort_flag = 1;
             atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
         }
+    } else {
+        // ================= E4M3 pools: widening of the prompt tiles (warps 12-15) =================
+        if constexpr (FP8) {
+            const int ctid = tid - C::CONV_TID0;
+            const int tensor = ctid >> 6;  // 0: K tiles (warps 12-13), 1: V tiles (warps 14-15)
+            const int stid = ctid & 63;
+            const int bar = 2 + tensor;    // named barrier of the stream's 64 threads
+            bool ok = true;
+            int gt = 0;
+            for (int k = 0; k < nunits && ok; ++k) {
+                const UnitInfo cur = load_unit(p, u_begin + k);
+                const int ptiles = prompt_tiles<TK>(cur);
+                const int ntiles = ptiles + wide_tail_tiles(cur);
+                for (int t = 0; t < ntiles && ok; ++t, ++gt) {
+                    // every tile's E4M3 phase in order, a tail tile's too (the producer completes it when it
+                    // hands the slots over; nothing to widen): so each parity wait names the phase it means
+                    uint64_t* full8 = tensor == 0 ? &bars->k8_full[gt % KST] : &bars->v8_full[gt % VST];
+                    const uint32_t ph = tensor == 0 ? (gt / KST) & 1 : (gt / VST) & 1;
+                    ok = mbar_wait(full8, ph, abort_flag, kWideWaitNs);
+                    ok = __all_sync(FULL, ok);
+                    ok = named_sync_and(bar, 64, ok);
+                    if (!ok || t >= ptiles) continue;
+                    const int valid = min(TK, cur.key_end - (cur.key_begin + t * TK));
+                    widen_e4m3_tile<D, TK, BF16>(tensor == 0 ? k_tile(gt) : v_tile(gt), valid, stid, bar);
+                    fence_proxy_async_smem();
+                    ok = named_sync_and(bar, 64, ok);
+                    if (ok && stid == 0)
+                        mbar_arrive(tensor == 0 ? &bars->k_full[gt % KST] : &bars->v_full[gt % VST]);
+                }
+            }
+            if (!ok && stid == 0) {
+                *abort_flag = 1;
+                atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -894,7 +930,8 @@ cudaError_t prepare_wide(int head_dim, bool bf16, bool fp8) {
 template <int D, bool BF16, bool FP8>
 static void launch_wide_k(int ctas, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const PrefixParams& p, cudaStream_t stream) {
-    prefix_wide_kernel<D, BF16, FP8><<<ctas, WideCfg<D>::THREADS, WideCfg<D>::SMEM, stream>>>(tq, tk, tv, p);
+    constexpr int threads = FP8 ? WideCfg<D>::THREADS_E4M3 : WideCfg<D>::THREADS;
+    prefix_wide_kernel<D, BF16, FP8><<<ctas, threads, WideCfg<D>::SMEM, stream>>>(tq, tk, tv, p);
 }
 
 template <int D>
