@@ -95,32 +95,35 @@ __device__ __forceinline__ uint32_t sw128_chunk(int kc, int r) {
 
 // Widens the E4M3 K or V tile that a TMA load left in the upper half of a ring slot (TK rows of D codes,
 // row r at slot + TK * D + r * D) into the slot's 16-bit layout (sw128_chunk); rows >= valid become zero
-// rows. Run by the 64 threads gtid = 0..63 of two warps, which synchronise on named barrier `bar` (64
-// threads) at head_dim 64. The 16-bit rows overwrite the E4M3 rows in place:
+// rows. Run by the NT threads gtid = 0 .. NT - 1 (NT = 64 or 128) of NT / 32 warps, which synchronise on
+// named barrier `bar` (NT threads) at head_dim 64. The 16-bit rows overwrite the E4M3 rows in place:
 //  - D = 128: a 16-bit row's first column half lies below the E4M3 rows and its second half on the E4M3
-//    row of the same key, so each key row belongs to one warp, which reads all of it before writing it;
+//    row of the same key, so each key row belongs to one warp (rows r with r mod (NT / 8) in the warp's
+//    four values), which reads all of it before writing it;
 //  - D = 64: the 16-bit row r covers E4M3 rows 2r - TK and 2r - TK + 1, so all threads read the whole
 //    tile into registers before any of them writes.
-// The caller fences the writes for the tensor core and synchronises the 64 threads afterwards.
-template <int D, int TK, bool BF16>
+// The caller fences the writes for the tensor core and synchronises the NT threads afterwards.
+template <int D, int TK, bool BF16, int NT = 64>
 __device__ __forceinline__ void widen_e4m3_tile(uint8_t* slot, int valid, int gtid, int bar) {
     static_assert(D == 64 || D == 128, "E4M3 tiles at head_dim 64 and 128");
+    static_assert(NT == 64 || NT == 128, "64 or 128 threads");
     const uint8_t* src = slot + TK * D;
     if constexpr (D == 128) {
-        const int j = gtid & 7;    // codes 16j .. 16j + 15 of a row
-        const int r0 = gtid >> 3;  // rows r0 + 8i: warp 0 holds r0 < 4, warp 1 the rest
+        constexpr int RS = NT / 8;  // rows one pass of the threads covers
+        const int j = gtid & 7;     // codes 16j .. 16j + 15 of a row
+        const int r0 = gtid >> 3;   // rows r0 + RS i: warp w holds r0 in [4w, 4w + 4)
 #pragma unroll 1
-        for (int i0 = 0; i0 < TK / 8; i0 += 4) {
+        for (int i0 = 0; i0 < TK / RS; i0 += 4) {
             uint4 in[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int r = r0 + 8 * (i0 + u);
+                const int r = r0 + RS * (i0 + u);
                 in[u] = r < valid ? *reinterpret_cast<const uint4*>(src + r * D + 16 * j) : make_uint4(0, 0, 0, 0);
             }
             __syncwarp();
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int r = r0 + 8 * (i0 + u);
+                const int r = r0 + RS * (i0 + u);
                 uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
                 if (r < valid) {
                     lo = e4m3x8_to_16<BF16>(make_uint2(in[u].x, in[u].y));
@@ -132,18 +135,19 @@ __device__ __forceinline__ void widen_e4m3_tile(uint8_t* slot, int valid, int gt
             __syncwarp();
         }
     } else {
-        const int j = gtid & 3;    // codes 16j .. 16j + 15 of a row
-        const int r0 = gtid >> 2;  // rows r0 + 16i
-        uint4 in[TK / 16];
+        constexpr int RS = NT / 4;  // rows one pass of the threads covers
+        const int j = gtid & 3;     // codes 16j .. 16j + 15 of a row
+        const int r0 = gtid >> 2;   // rows r0 + RS i
+        uint4 in[TK / RS];
 #pragma unroll
-        for (int i = 0; i < TK / 16; ++i) {
-            const int r = r0 + 16 * i;
+        for (int i = 0; i < TK / RS; ++i) {
+            const int r = r0 + RS * i;
             in[i] = r < valid ? *reinterpret_cast<const uint4*>(src + r * D + 16 * j) : make_uint4(0, 0, 0, 0);
         }
-        asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
+        asm volatile("bar.sync %0, %1;" ::"r"(bar), "n"(NT) : "memory");
 #pragma unroll
-        for (int i = 0; i < TK / 16; ++i) {
-            const int r = r0 + 16 * i;
+        for (int i = 0; i < TK / RS; ++i) {
+            const int r = r0 + RS * i;
             uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
             if (r < valid) {
                 lo = e4m3x8_to_16<BF16>(make_uint2(in[i].x, in[i].y));

@@ -326,6 +326,17 @@ __device__ __forceinline__ void st_global_v8(void* ptr, uint4 lo, uint4 hi) {
                  "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
                  : "memory");
 }
+// Per-thread register limit of the executing warpgroup (all four of its warps execute the same
+// instruction): down to N, the registers returning to the CTA's pool, or up to N, waiting until the pool
+// holds them (the pool is what the CTA was launched with)
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

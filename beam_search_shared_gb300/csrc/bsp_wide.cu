@@ -102,10 +102,18 @@ struct WideCfg {
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int THREADS = 384;
     static constexpr int GATHER_TID0 = 320;                  // warps 10-11
-    // over E4M3 pools four more warps (12-15, one per SM sub-partition) widen the prompt tiles: warps
-    // 12-13 every K tile, warps 14-15 every V tile, two streams that do not wait on each other
-    static constexpr int THREADS_E4M3 = 512;
+    // over E4M3 pools eight more warps (12-19, two warpgroups) widen the prompt tiles: warps 12-15 every K
+    // tile, warps 16-19 every V tile, two streams that do not wait on each other. Registers per thread:
+    // 96 at launch (__launch_bounds__(640, 1)), then the widening warps down to REGS_CONV and the softmax
+    // warps (0-7) up to REGS_SOFTMAX (setmaxnreg draws on the launch's registers; warps 8-11 keep 96)
+    static constexpr int THREADS_E4M3 = 640;
     static constexpr int CONV_TID0 = 384;
+    static constexpr int CONV_THREADS = 128;  // per stream
+    static constexpr int REGS_LAUNCH_E4M3 = 96;
+    static constexpr int REGS_CONV = 64;
+    static constexpr int REGS_SOFTMAX = 128;
+    static_assert(256 * REGS_SOFTMAX + 128 * REGS_LAUNCH_E4M3 + 256 * REGS_CONV <= THREADS_E4M3 * REGS_LAUNCH_E4M3,
+                  "register split");
     static_assert(O_COL + 2 * D <= 512, "tensor memory");
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(KST <= 8 && VST <= 8, "barrier arrays");
@@ -171,7 +179,7 @@ __device__ __forceinline__ bool gather_sync_and(bool ok) {
 }  // namespace
 
 template <int D, bool BF16, bool FP8>
-__global__ void __launch_bounds__(FP8 ? 512 : 384, 1)
+__global__ void __launch_bounds__(FP8 ? 640 : 384, 1)
 prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefixParams p) {
     using C = WideCfg<D>;
@@ -233,7 +241,7 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
     }
-    if (warp == 1) tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
+    if (warp == 9) tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
     // zero the query rows no TMA box covers (rows bq * G .. 31 of each quadrant of both blocks), so
     // padded rows stay finite
     {
@@ -252,219 +260,378 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // SMs this grid leaves; it waits for this grid's completion before reading the partials
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    if (warp == 0) {
-        // ================= TMA producer =================
-        const int BR = ps < kTileKeys ? ps : kTileKeys;  // rows per box (a page, or 64 rows of a larger page)
-        int gt = 0, k = 0, ntail = 0;
-        bool ok = true;
-        for (int u = u_begin; u < u_end && ok; ++u, ++k) {
-            const UnitInfo ui = load_unit(p, u);
-            const int ptiles = prompt_tiles<TK>(ui);
-            const int ntiles = ptiles + wide_tail_tiles(ui);
-            const int* pg = p.pages + ui.page_off;
-            const int npages = (ui.P + ps - 1) >> p.ps_log2;
-            int win_base = -1, my_page = 0;
-            for (int t = 0; t < ntiles; ++t, ++gt) {
-                // this warp is the only waiter on the slot-release barriers and takes every tile's
-                // release in order, so each parity wait names the phase it means
-                if (gt >= KST) {
-                    ok = mbar_wait(&bars->k_empty[gt % KST], ((gt / KST) - 1) & 1, abort_flag, kWideWaitNs);
-                    ok = __all_sync(FULL, ok);
-                    if (!ok) break;
-                }
-                if (t >= ptiles) {
-                    // a tail tile: once its V slot is free too, hand both slots to the tail-tile warps
-                    // (a counter, not a barrier phase: they may lag several tail tiles behind)
-                    if (gt >= VST) {
-                        ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kWideWaitNs);
+    if (warp >= 8) {
+        // over E4M3 pools the widening warps (12-19, two warpgroups) give registers to the softmax
+        // warpgroups
+        if constexpr (FP8) {
+            if (warp >= 12) setmaxnreg_dec<C::REGS_CONV>();
+        }
+        if (warp == 8) {
+            // ================= TMA producer =================
+            const int BR = ps < kTileKeys ? ps : kTileKeys;  // rows per box (a page, or 64 rows of a larger page)
+            int gt = 0, k = 0, ntail = 0;
+            bool ok = true;
+            for (int u = u_begin; u < u_end && ok; ++u, ++k) {
+                const UnitInfo ui = load_unit(p, u);
+                const int ptiles = prompt_tiles<TK>(ui);
+                const int ntiles = ptiles + wide_tail_tiles(ui);
+                const int* pg = p.pages + ui.page_off;
+                const int npages = (ui.P + ps - 1) >> p.ps_log2;
+                int win_base = -1, my_page = 0;
+                for (int t = 0; t < ntiles; ++t, ++gt) {
+                    // this warp is the only waiter on the slot-release barriers and takes every tile's
+                    // release in order, so each parity wait names the phase it means
+                    if (gt >= KST) {
+                        ok = mbar_wait(&bars->k_empty[gt % KST], ((gt / KST) - 1) & 1, abort_flag, kWideWaitNs);
                         ok = __all_sync(FULL, ok);
                         if (!ok) break;
                     }
-                    ++ntail;
-                    if (lane == 0) {
-                        counter_release(&bars->tail_granted, ntail);
-                        if constexpr (FP8) {
-                            // no E4M3 tile here: complete the slots' E4M3 phases (the widening warps wait
-                            // for every phase in order and have nothing to widen for a tail tile), so that
-                            // the phases keep counting the slot's tiles
-                            mbar_arrive(&bars->k8_full[gt % KST]);
-                            mbar_arrive(&bars->v8_full[gt % VST]);
-                        }
-                    }
-                    __syncwarp();
-                    continue;
-                }
-                const int key0 = ui.key_begin + t * TK;
-                const int valid = min(TK, ui.key_end - key0);
-                const int nchunks = (valid + BR - 1) / BR;  // pages (or 64-row slices) with valid keys
-                const int tile_bytes = nchunks * BR * D * (FP8 ? 1 : 2);
-                const int pidx0 = key0 >> p.ps_log2;
-                const int pidx_last = (key0 + (nchunks - 1) * BR) >> p.ps_log2;
-                if (win_base < 0 || pidx_last >= win_base + 32) {  // warp-uniform
-                    win_base = pidx0;
-                    my_page = (win_base + lane < npages) ? __ldg(pg + win_base + lane) : 0;
-                }
-                // box b of a tensor: column half b % NC of chunk b / NC (E4M3: one box of head_dim bytes
-                // per chunk, into the upper half of the slot, where the widening warps pick it up)
-                constexpr int NB = FP8 ? 1 : NC;
-                const int nbox = nchunks * NB;
-                for (int tensor = 0; tensor < 2; ++tensor) {
-                    if (tensor == 1 && gt >= VST) {
-                        ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kWideWaitNs);
-                        ok = __all_sync(FULL, ok);
-                        if (!ok) break;
-                    }
-                    uint64_t* full = FP8 ? (tensor == 0 ? &bars->k8_full[gt % KST] : &bars->v8_full[gt % VST])
-                                         : (tensor == 0 ? &bars->k_full[gt % KST] : &bars->v_full[gt % VST]);
-                    uint8_t* base = tensor == 0 ? k_tile(gt) : v_tile(gt);
-                    const CUtensorMap* map = tensor == 0 ? &tm_k : &tm_v;
-                    if (lane == 0) mbar_arrive_expect_tx(full, tile_bytes);
-                    for (int b0 = 0; b0 < nbox; b0 += 32) {
-                        const int bx = b0 + lane;
-                        const int ch = min(bx / NB, nchunks - 1);
-                        const int key = key0 + ch * BR;
-                        int page = __shfl_sync(FULL, my_page, (key >> p.ps_log2) - win_base);
-                        if (bx < nbox) {
-                            if (static_cast<unsigned>(page) >= static_cast<unsigned>(p.num_pages)) {
-                                atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
-                                page = 0;
-                            }
-                            const int row = ((page * p.Hkv + ui.g) << p.ps_log2) + (key & (ps - 1));
-                            if constexpr (FP8) {
-                                tma_load_2d(base + TK * D + ch * BR * D, map, full, 0, row);
-                            } else {
-                                const int c = bx % NC;
-                                tma_load_2d(base + c * TK * 128 + ch * BR * 128, map, full, c * 64, row);
-                            }
-                        }
-                    }
-                }
-                if (!ok) break;
-                if (t == 0) {
-                    // the unit's Q of both blocks, once the previous unit's last Q*K^T of the block is done
-                    // (issued after this unit's first K/V tile, which may already stream meanwhile)
-                    for (int x = 0; x < 2 && ok; ++x) {
-                        if (k >= 1) {
-                            ok = mbar_wait(&bars->q_empty[x], (k - 1) & 1, abort_flag, kWideWaitNs);
+                    if (t >= ptiles) {
+                        // a tail tile: once its V slot is free too, hand both slots to the tail-tile warps
+                        // (a counter, not a barrier phase: they may lag several tail tiles behind)
+                        if (gt >= VST) {
+                            ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kWideWaitNs);
                             ok = __all_sync(FULL, ok);
                             if (!ok) break;
                         }
+                        ++ntail;
                         if (lane == 0) {
-                            mbar_arrive_expect_tx(&bars->q_full[x], NC * 4 * qrows * 128);
-                            for (int c = 0; c < NC; ++c)
-                                for (int i = 0; i < 4; ++i)
-                                    tma_load_3d(q_buf(x) + c * (kRowsPerBlock * 128) + i * 32 * 128, &tm_q,
-                                                &bars->q_full[x], c * 64, ui.g * p.G,
-                                                ui.row_off + (2 * ui.rb + x) * p.Wblk + i * p.bq);
+                            counter_release(&bars->tail_granted, ntail);
+                            if constexpr (FP8) {
+                                // no E4M3 tile here: complete the slots' E4M3 phases (the widening warps wait
+                                // for every phase in order and have nothing to widen for a tail tile), so that
+                                // the phases keep counting the slot's tiles
+                                mbar_arrive(&bars->k8_full[gt % KST]);
+                                mbar_arrive(&bars->v8_full[gt % VST]);
+                            }
                         }
+                        __syncwarp();
+                        continue;
                     }
-                    if (!ok) break;
-                }
-                __syncwarp();
-            }
-        }
-        if (!ok) {
-            if (lane == 0) {
-                *abort_flag = 1;
-                atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
-            }
-            // drain: let this CTA's own copies land before the CTA exits
-            // (the TMA loads complete the E4M3 barriers over E4M3 pools)
-            const uint64_t t0 = globaltimer_ns();
-            uint64_t* kf = FP8 ? bars->k8_full : bars->k_full;
-            uint64_t* vf = FP8 ? bars->v8_full : bars->v_full;
-            for (int j = max(0, gt - KST); j <= gt; ++j)
-                while (!mbar_try_wait(&kf[j % KST], (j / KST) & 1) && globaltimer_ns() - t0 < kWideDrainNs) {
-                }
-            for (int j = max(0, gt - VST); j <= gt; ++j)
-                while (!mbar_try_wait(&vf[j % VST], (j / VST) & 1) && globaltimer_ns() - t0 < kWideDrainNs) {
-                }
-            for (int x = 0; x < 2; ++x)
-                while (!mbar_try_wait(&bars->q_full[x], k & 1) && globaltimer_ns() - t0 < kWideDrainNs) {
-                }
-        }
-    } else if (warp == 1) {
-        // ================= MMA issuer =================
-        if (lane == 0) {
-            constexpr uint32_t ID_QK = idesc_f16(kRowsPerBlock, TK, BF16, false);
-            constexpr uint32_t ID_PV = idesc_f16(kRowsPerBlock, D, BF16, true);
-            int gt = 0, k = 0;
-            int pend = -1;  // tile whose P*V is not issued yet
-            bool pend_first = false, pend_last = false;
-            bool ok = true;
-            // (V of tile j is waited for before block A's P: a wait that has already completed still costs
-            // a shared-memory round trip, which would otherwise sit between P and the MMAs)
-            auto issue_pv = [&](int x, int j, bool first, bool last) -> bool {
-                if (!mbar_wait(&bars->p_full[x], j & 1, abort_flag, kWideWaitNs)) return false;
-                tc_fence_after();
-                const uint32_t p_tmem = tmem + C::S_COL + x * TK;
-                const uint32_t o_tmem = tmem + C::O_COL + x * D;
-                const uint32_t v_addr = smem_u32(v_tile(j));
-#pragma unroll
-                for (int kk = 0; kk < TK / 16; ++kk) {
-                    const uint64_t bd = sdesc_sw128(v_addr + kk * 16 * 128, TK * 128, 1024);
-                    mma_f16_tmem_a(o_tmem, p_tmem + kk * 8, bd, ID_PV, (!first || kk > 0) ? 1u : 0u);
-                }
-                if (last) mma_commit(&bars->o_final[x]);
-                return true;
-            };
-            for (int u = u_begin; u < u_end && ok; ++u, ++k) {
-                const UnitInfo ui = load_unit(p, u);
-                const int ntiles = prompt_tiles<TK>(ui) + wide_tail_tiles(ui);
-                for (int t = 0; t < ntiles; ++t, ++gt) {
-                    const uint32_t k_addr = smem_u32(k_tile(gt));
-                    // the loads this tile's MMAs need, first: they do not depend on the softmax, and once
-                    // a block's P is ready its P*V and the next Q*K^T go out back to back
-                    ok = mbar_wait(&bars->k_full[gt % KST], (gt / KST) & 1, abort_flag, kWideWaitNs);
-                    if (ok && t == 0) ok = mbar_wait(&bars->q_full[0], k & 1, abort_flag, kWideWaitNs);
-                    if (ok && t == 0) ok = mbar_wait(&bars->q_full[1], k & 1, abort_flag, kWideWaitNs);
-                    if (ok && pend >= 0)
-                        ok = mbar_wait(&bars->v_full[pend % VST], (pend / VST) & 1, abort_flag, kWideWaitNs);
-                    if (!ok) break;
-                    for (int x = 0; x < 2; ++x) {
-                        if (pend >= 0) {
-                            ok = issue_pv(x, pend, pend_first, pend_last);
+                    const int key0 = ui.key_begin + t * TK;
+                    const int valid = min(TK, ui.key_end - key0);
+                    const int nchunks = (valid + BR - 1) / BR;  // pages (or 64-row slices) with valid keys
+                    const int tile_bytes = nchunks * BR * D * (FP8 ? 1 : 2);
+                    const int pidx0 = key0 >> p.ps_log2;
+                    const int pidx_last = (key0 + (nchunks - 1) * BR) >> p.ps_log2;
+                    if (win_base < 0 || pidx_last >= win_base + 32) {  // warp-uniform
+                        win_base = pidx0;
+                        my_page = (win_base + lane < npages) ? __ldg(pg + win_base + lane) : 0;
+                    }
+                    // box b of a tensor: column half b % NC of chunk b / NC (E4M3: one box of head_dim bytes
+                    // per chunk, into the upper half of the slot, where the widening warps pick it up)
+                    constexpr int NB = FP8 ? 1 : NC;
+                    const int nbox = nchunks * NB;
+                    for (int tensor = 0; tensor < 2; ++tensor) {
+                        if (tensor == 1 && gt >= VST) {
+                            ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kWideWaitNs);
+                            ok = __all_sync(FULL, ok);
                             if (!ok) break;
                         }
-                        // S_X holds P_X of the previous tile, whose P*V was issued just before
-                        tc_fence_after();
-                        const uint32_t q_addr = smem_u32(q_buf(x));
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint64_t ad =
-                                sdesc_sw128(q_addr + (kk >> 2) * (kRowsPerBlock * 128) + (kk & 3) * 32, 16, 1024);
-                            const uint64_t bd = sdesc_sw128(k_addr + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
-                            mma_f16(tmem + C::S_COL + x * TK, ad, bd, ID_QK, kk > 0 ? 1u : 0u);
+                        uint64_t* full = FP8 ? (tensor == 0 ? &bars->k8_full[gt % KST] : &bars->v8_full[gt % VST])
+                                             : (tensor == 0 ? &bars->k_full[gt % KST] : &bars->v_full[gt % VST]);
+                        uint8_t* base = tensor == 0 ? k_tile(gt) : v_tile(gt);
+                        const CUtensorMap* map = tensor == 0 ? &tm_k : &tm_v;
+                        if (lane == 0) mbar_arrive_expect_tx(full, tile_bytes);
+                        for (int b0 = 0; b0 < nbox; b0 += 32) {
+                            const int bx = b0 + lane;
+                            const int ch = min(bx / NB, nchunks - 1);
+                            const int key = key0 + ch * BR;
+                            int page = __shfl_sync(FULL, my_page, (key >> p.ps_log2) - win_base);
+                            if (bx < nbox) {
+                                if (static_cast<unsigned>(page) >= static_cast<unsigned>(p.num_pages)) {
+                                    atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
+                                    page = 0;
+                                }
+                                const int row = ((page * p.Hkv + ui.g) << p.ps_log2) + (key & (ps - 1));
+                                if constexpr (FP8) {
+                                    tma_load_2d(base + TK * D + ch * BR * D, map, full, 0, row);
+                                } else {
+                                    const int c = bx % NC;
+                                    tma_load_2d(base + c * TK * 128 + ch * BR * 128, map, full, c * 64, row);
+                                }
+                            }
                         }
-                        // (the K and V slots are released by block B's softmax warp 6 once it sees S_B
-                        // complete)
-                        mma_commit(&bars->s_full[x]);
-                        if (t == ntiles - 1) mma_commit(&bars->q_empty[x]);
                     }
                     if (!ok) break;
-                    pend = gt;
-                    pend_first = t == 0;
-                    pend_last = t == ntiles - 1;
+                    if (t == 0) {
+                        // the unit's Q of both blocks, once the previous unit's last Q*K^T of the block is done
+                        // (issued after this unit's first K/V tile, which may already stream meanwhile)
+                        for (int x = 0; x < 2 && ok; ++x) {
+                            if (k >= 1) {
+                                ok = mbar_wait(&bars->q_empty[x], (k - 1) & 1, abort_flag, kWideWaitNs);
+                                ok = __all_sync(FULL, ok);
+                                if (!ok) break;
+                            }
+                            if (lane == 0) {
+                                mbar_arrive_expect_tx(&bars->q_full[x], NC * 4 * qrows * 128);
+                                for (int c = 0; c < NC; ++c)
+                                    for (int i = 0; i < 4; ++i)
+                                        tma_load_3d(q_buf(x) + c * (kRowsPerBlock * 128) + i * 32 * 128, &tm_q,
+                                                    &bars->q_full[x], c * 64, ui.g * p.G,
+                                                    ui.row_off + (2 * ui.rb + x) * p.Wblk + i * p.bq);
+                            }
+                        }
+                        if (!ok) break;
+                    }
+                    __syncwarp();
                 }
             }
-            if (ok && pend >= 0) {
-                ok = mbar_wait(&bars->v_full[pend % VST], (pend / VST) & 1, abort_flag, kWideWaitNs);
-                if (ok) ok = issue_pv(0, pend, pend_first, pend_last);
-                if (ok) ok = issue_pv(1, pend, pend_first, pend_last);
-            }
             if (!ok) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+                }
+                // drain: let this CTA's own copies land before the CTA exits
+                // (the TMA loads complete the E4M3 barriers over E4M3 pools)
+                const uint64_t t0 = globaltimer_ns();
+                uint64_t* kf = FP8 ? bars->k8_full : bars->k_full;
+                uint64_t* vf = FP8 ? bars->v8_full : bars->v_full;
+                for (int j = max(0, gt - KST); j <= gt; ++j)
+                    while (!mbar_try_wait(&kf[j % KST], (j / KST) & 1) && globaltimer_ns() - t0 < kWideDrainNs) {
+                    }
+                for (int j = max(0, gt - VST); j <= gt; ++j)
+                    while (!mbar_try_wait(&vf[j % VST], (j / VST) & 1) && globaltimer_ns() - t0 < kWideDrainNs) {
+                    }
+                for (int x = 0; x < 2; ++x)
+                    while (!mbar_try_wait(&bars->q_full[x], k & 1) && globaltimer_ns() - t0 < kWideDrainNs) {
+                    }
+            }
+        } else if (warp == 9) {
+            // ================= MMA issuer =================
+            if (lane == 0) {
+                constexpr uint32_t ID_QK = idesc_f16(kRowsPerBlock, TK, BF16, false);
+                constexpr uint32_t ID_PV = idesc_f16(kRowsPerBlock, D, BF16, true);
+                int gt = 0, k = 0;
+                int pend = -1;  // tile whose P*V is not issued yet
+                bool pend_first = false, pend_last = false;
+                bool ok = true;
+                // (V of tile j is waited for before block A's P: a wait that has already completed still costs
+                // a shared-memory round trip, which would otherwise sit between P and the MMAs)
+                auto issue_pv = [&](int x, int j, bool first, bool last) -> bool {
+                    if (!mbar_wait(&bars->p_full[x], j & 1, abort_flag, kWideWaitNs)) return false;
+                    tc_fence_after();
+                    const uint32_t p_tmem = tmem + C::S_COL + x * TK;
+                    const uint32_t o_tmem = tmem + C::O_COL + x * D;
+                    const uint32_t v_addr = smem_u32(v_tile(j));
+#pragma unroll
+                    for (int kk = 0; kk < TK / 16; ++kk) {
+                        const uint64_t bd = sdesc_sw128(v_addr + kk * 16 * 128, TK * 128, 1024);
+                        mma_f16_tmem_a(o_tmem, p_tmem + kk * 8, bd, ID_PV, (!first || kk > 0) ? 1u : 0u);
+                    }
+                    if (last) mma_commit(&bars->o_final[x]);
+                    return true;
+                };
+                for (int u = u_begin; u < u_end && ok; ++u, ++k) {
+                    const UnitInfo ui = load_unit(p, u);
+                    const int ntiles = prompt_tiles<TK>(ui) + wide_tail_tiles(ui);
+                    for (int t = 0; t < ntiles; ++t, ++gt) {
+                        const uint32_t k_addr = smem_u32(k_tile(gt));
+                        // the loads this tile's MMAs need, first: they do not depend on the softmax, and once
+                        // a block's P is ready its P*V and the next Q*K^T go out back to back
+                        ok = mbar_wait(&bars->k_full[gt % KST], (gt / KST) & 1, abort_flag, kWideWaitNs);
+                        if (ok && t == 0) ok = mbar_wait(&bars->q_full[0], k & 1, abort_flag, kWideWaitNs);
+                        if (ok && t == 0) ok = mbar_wait(&bars->q_full[1], k & 1, abort_flag, kWideWaitNs);
+                        if (ok && pend >= 0)
+                            ok = mbar_wait(&bars->v_full[pend % VST], (pend / VST) & 1, abort_flag, kWideWaitNs);
+                        if (!ok) break;
+                        for (int x = 0; x < 2; ++x) {
+                            if (pend >= 0) {
+                                ok = issue_pv(x, pend, pend_first, pend_last);
+                                if (!ok) break;
+                            }
+                            // S_X holds P_X of the previous tile, whose P*V was issued just before
+                            tc_fence_after();
+                            const uint32_t q_addr = smem_u32(q_buf(x));
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint64_t ad =
+                                    sdesc_sw128(q_addr + (kk >> 2) * (kRowsPerBlock * 128) + (kk & 3) * 32, 16, 1024);
+                                const uint64_t bd = sdesc_sw128(k_addr + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
+                                mma_f16(tmem + C::S_COL + x * TK, ad, bd, ID_QK, kk > 0 ? 1u : 0u);
+                            }
+                            // (the K and V slots are released by block B's softmax warp 6 once it sees S_B
+                            // complete)
+                            mma_commit(&bars->s_full[x]);
+                            if (t == ntiles - 1) mma_commit(&bars->q_empty[x]);
+                        }
+                        if (!ok) break;
+                        pend = gt;
+                        pend_first = t == 0;
+                        pend_last = t == ntiles - 1;
+                    }
+                }
+                if (ok && pend >= 0) {
+                    ok = mbar_wait(&bars->v_full[pend % VST], (pend / VST) & 1, abort_flag, kWideWaitNs);
+                    if (ok) ok = issue_pv(0, pend, pend_first, pend_last);
+                    if (ok) ok = issue_pv(1, pend, pend_first, pend_last);
+                }
+                if (!ok) {
+                    *abort_flag = 1;
+                    atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+                }
+                // drain: every MMA issued by this thread completes before TMEM is freed
+                mma_commit(&bars->drain);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(&bars->drain, 0) && globaltimer_ns() - t0 < kWideDrainNs) {
+                }
+            }
+        } else if (warp < 12) {
+            // ================= tail tiles =================
+            constexpr int CH = D / 8;     // 16-byte chunks of a 16-bit K or V row
+            constexpr int RPS = 64 / CH;  // rows one pass of the 64 threads covers
+            constexpr int EB = FP8 ? 1 : 2;  // bytes per pool element
+            const int gtid = tid - C::GATHER_TID0;
+            const int kc = gtid % CH;
+            const int rsub = gtid / CH;
+            const uint8_t* k_pool = static_cast<const uint8_t*>(p.k_pool);
+            const uint8_t* v_pool = static_cast<const uint8_t*>(p.v_pool);
+            // pool rows of this thread's two key columns (gtid, gtid + 64) of each tail tile of a unit,
+            // resolved a unit ahead; -1 past the request's tail keys or when unreadable
+            int res[kWideMaxTailTiles][2];
+            auto resolve = [&](const UnitInfo& ui) {
+                const int ntt = wide_tail_tiles(ui);
+#pragma unroll
+                for (int n = 0; n < kWideMaxTailTiles; ++n)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        res[n][h] = -1;
+                        const int cc = n * TK + gtid + 64 * h;
+                        if (n >= ntt || cc >= ui.rows * ui.T) continue;
+                        const int w = cc / ui.T, tt = cc - w * ui.T;
+                        const int pos = ui.P + tt;
+                        const int src = __ldg(p.ci + (static_cast<long long>(ui.b) * p.W + w) * p.max_seq + pos);
+                        int r = -1;
+                        if (static_cast<unsigned>(src) < static_cast<unsigned>(p.W)) {
+                            const int page = __ldg(p.beam_pages +
+                                                   (static_cast<long long>(ui.b) * p.W + src) * p.beam_pages_stride +
+                                                   (pos >> p.ps_log2));
+                            if (static_cast<unsigned>(page) < static_cast<unsigned>(p.num_pages))
+                                r = ((page * p.Hkv + ui.g) << p.ps_log2) + (pos & (ps - 1));
+                        }
+                        if (r < 0) {
+                            atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
+                        } else {
+                            // the gather runs at the end of the unit: bring the row's K and V into L2 now
+#pragma unroll
+                            for (int off = 0; off < D * EB; off += 128) {
+                                prefetch_l2(k_pool + static_cast<long long>(r) * (D * EB) + off);
+                                prefetch_l2(v_pool + static_cast<long long>(r) * (D * EB) + off);
+                            }
+                        }
+                        res[n][h] = r;
+                    }
+            };
+            bool ok = true;
+            int gt = 0, ntail = 0;
+            UnitInfo cur;
+            if (nunits > 0) {
+                cur = load_unit(p, u_begin);
+                resolve(cur);
+            }
+            for (int k = 0; k < nunits && ok; ++k) {
+                const int ptiles = prompt_tiles<TK>(cur);
+                const int ntt = wide_tail_tiles(cur);
+#pragma unroll
+                for (int n = 0; n < kWideMaxTailTiles; ++n) {
+                    if (n >= ntt) break;
+                    const int gtt = gt + ptiles + n;
+                    // the producer hands the tile's K and V slots over once both blocks' Q*K^T and P*V of
+                    // their previous tiles are done
+                    ok = counter_wait(&bars->tail_granted, ntail, abort_flag, kWideWaitNs);
+                    ++ntail;
+                    ok = __all_sync(FULL, ok);
+                    int* trow = trow_of(gtt);
+                    if (ok) {
+                        trow[gtid] = res[n][0];
+                        trow[gtid + 64] = res[n][1];
+                    }
+                    ok = gather_sync_and(ok);
+                    if (ok) {
+                        uint8_t* kt = k_tile(gtt);
+                        uint8_t* vt = v_tile(gtt);
+#pragma unroll 4
+                        for (int i = 0; i < TK / RPS; ++i) {
+                            const int c = rsub + i * RPS;
+                            const int r = trow[c];
+                            // the layout of a TMA box with 128-byte swizzle: chunk kc of row c in column half kc / 8
+                            const uint32_t off = sw128_chunk<TK>(kc, c);
+                            const long long e = static_cast<long long>(r < 0 ? 0 : r) * D + kc * 8;  // element offset
+                            if constexpr (FP8) {
+                                uint4 kw = make_uint4(0, 0, 0, 0), vw = kw;  // absent keys are zero rows
+                                if (r >= 0) {
+                                    kw = e4m3x8_to_16<BF16>(__ldg(reinterpret_cast<const uint2*>(k_pool + e)));
+                                    vw = e4m3x8_to_16<BF16>(__ldg(reinterpret_cast<const uint2*>(v_pool + e)));
+                                }
+                                *reinterpret_cast<uint4*>(kt + off) = kw;
+                                *reinterpret_cast<uint4*>(vt + off) = vw;
+                            } else {
+                                const uint32_t nb = r < 0 ? 0u : 16u;  // absent keys are zero rows
+                                cp_async16(kt + off, k_pool + 2 * e, nb);
+                                cp_async16(vt + off, v_pool + 2 * e, nb);
+                            }
+                        }
+                        if constexpr (!FP8) cp_async_commit_wait_all();
+                        fence_proxy_async_smem();
+                    }
+                    ok = gather_sync_and(ok);
+                    if (!ok) break;
+                    if (gtid == 0) {
+                        mbar_arrive(&bars->k_full[gtt % KST]);
+                        mbar_arrive(&bars->v_full[gtt % VST]);
+                    }
+                }
+                gt += ptiles + ntt;
+                if (ok && k + 1 < nunits) {
+                    cur = load_unit(p, u_begin + k + 1);
+                    resolve(cur);
+                }
+            }
+            if (!ok && gtid == 0) {
                 *abort_flag = 1;
                 atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
             }
-            // drain: every MMA issued by this thread completes before TMEM is freed
-            mma_commit(&bars->drain);
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(&bars->drain, 0) && globaltimer_ns() - t0 < kWideDrainNs) {
+        } else {
+            // ================= E4M3 pools: widening of the prompt tiles (warps 12-15) =================
+            if constexpr (FP8) {
+                const int ctid = tid - C::CONV_TID0;
+                const int tensor = ctid / C::CONV_THREADS;  // 0: K tiles (warps 12-15), 1: V tiles (warps 16-19)
+                const int stid = ctid % C::CONV_THREADS;
+                const int bar = 2 + tensor;                 // named barrier of the stream's threads
+                bool ok = true;
+                int gt = 0;
+                for (int k = 0; k < nunits && ok; ++k) {
+                    const UnitInfo cur = load_unit(p, u_begin + k);
+                    const int ptiles = prompt_tiles<TK>(cur);
+                    const int ntiles = ptiles + wide_tail_tiles(cur);
+                    for (int t = 0; t < ntiles && ok; ++t, ++gt) {
+                        // every tile's E4M3 phase in order, a tail tile's too (the producer completes it when it
+                        // hands the slots over; nothing to widen): so each parity wait names the phase it means
+                        uint64_t* full8 = tensor == 0 ? &bars->k8_full[gt % KST] : &bars->v8_full[gt % VST];
+                        const uint32_t ph = tensor == 0 ? (gt / KST) & 1 : (gt / VST) & 1;
+                        ok = mbar_wait(full8, ph, abort_flag, kWideWaitNs);
+                        ok = __all_sync(FULL, ok);
+                        ok = named_sync_and(bar, C::CONV_THREADS, ok);
+                        if (!ok || t >= ptiles) continue;
+                        const int valid = min(TK, cur.key_end - (cur.key_begin + t * TK));
+                        widen_e4m3_tile<D, TK, BF16, C::CONV_THREADS>(tensor == 0 ? k_tile(gt) : v_tile(gt), valid,
+                                                                      stid, bar);
+                        fence_proxy_async_smem();
+                        ok = named_sync_and(bar, C::CONV_THREADS, ok);
+                        if (ok && stid == 0)
+                            mbar_arrive(tensor == 0 ? &bars->k_full[gt % KST] : &bars->v_full[gt % VST]);
+                    }
+                }
+                if (!ok && stid == 0) {
+                    *abort_flag = 1;
+                    atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+                }
             }
         }
-    } else if (warp < 10) {
+    } else {
+        if constexpr (FP8) setmaxnreg_inc<C::REGS_SOFTMAX>();
         // ================= softmax warps (block x), then the unit's output =================
-        const int x = (warp - 2) >> 2;
+        const int x = warp >> 2;
         const int quad = warp & 3;           // TMEM lane quadrant this warp may access
         const int wq = lane / p.G;           // beam of the quadrant
         const int jh = lane - wq * p.G;      // head of the group
@@ -662,7 +829,7 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     uint8_t* sV = v_tile(gt);
                     const int nzc = (TK - valid) * 8;  // 16-byte chunks per column half
                     for (int c = 0; c < NC; ++c)
-                        for (int idx = tid - 64; idx < nzc; idx += 128)
+                        for (int idx = tid; idx < nzc; idx += 128)
                             reinterpret_cast<uint4*>(sV + c * TK * 128 + valid * 128)[idx] = make_uint4(0, 0, 0, 0);
                     fence_proxy_async_smem();
                 }
@@ -743,160 +910,10 @@ prefix_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             *abort_flag = 1;
             atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
         }
-    } else if (warp < 12) {
-        // ================= tail tiles =================
-        constexpr int CH = D / 8;     // 16-byte chunks of a 16-bit K or V row
-        constexpr int RPS = 64 / CH;  // rows one pass of the 64 threads covers
-        constexpr int EB = FP8 ? 1 : 2;  // bytes per pool element
-        const int gtid = tid - C::GATHER_TID0;
-        const int kc = gtid % CH;
-        const int rsub = gtid / CH;
-        const uint8_t* k_pool = static_cast<const uint8_t*>(p.k_pool);
-        const uint8_t* v_pool = static_cast<const uint8_t*>(p.v_pool);
-        // pool rows of this thread's two key columns (gtid, gtid + 64) of each tail tile of a unit,
-        // resolved a unit ahead; -1 past the request's tail keys or when unreadable
-        int res[kWideMaxTailTiles][2];
-        auto resolve = [&](const UnitInfo& ui) {
-            const int ntt = wide_tail_tiles(ui);
-#pragma unroll
-            for (int n = 0; n < kWideMaxTailTiles; ++n)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    res[n][h] = -1;
-                    const int cc = n * TK + gtid + 64 * h;
-                    if (n >= ntt || cc >= ui.rows * ui.T) continue;
-                    const int w = cc / ui.T, tt = cc - w * ui.T;
-                    const int pos = ui.P + tt;
-                    const int src = __ldg(p.ci + (static_cast<long long>(ui.b) * p.W + w) * p.max_seq + pos);
-                    int r = -1;
-                    if (static_cast<unsigned>(src) < static_cast<unsigned>(p.W)) {
-                        const int page = __ldg(p.beam_pages +
-                                               (static_cast<long long>(ui.b) * p.W + src) * p.beam_pages_stride +
-                                               (pos >> p.ps_log2));
-                        if (static_cast<unsigned>(page) < static_cast<unsigned>(p.num_pages))
-                            r = ((page * p.Hkv + ui.g) << p.ps_log2) + (pos & (ps - 1));
-                    }
-                    if (r < 0) {
-                        atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
-                    } else {
-                        // the gather runs at the end of the unit: bring the row's K and V into L2 now
-#pragma unroll
-                        for (int off = 0; off < D * EB; off += 128) {
-                            prefetch_l2(k_pool + static_cast<long long>(r) * (D * EB) + off);
-                            prefetch_l2(v_pool + static_cast<long long>(r) * (D * EB) + off);
-                        }
-                    }
-                    res[n][h] = r;
-                }
-        };
-        bool ok = true;
-        int gt = 0, ntail = 0;
-        UnitInfo cur;
-        if (nunits > 0) {
-            cur = load_unit(p, u_begin);
-            resolve(cur);
-        }
-        for (int k = 0; k < nunits && ok; ++k) {
-            const int ptiles = prompt_tiles<TK>(cur);
-            const int ntt = wide_tail_tiles(cur);
-#pragma unroll
-            for (int n = 0; n < kWideMaxTailTiles; ++n) {
-                if (n >= ntt) break;
-                const int gtt = gt + ptiles + n;
-                // the producer hands the tile's K and V slots over once both blocks' Q*K^T and P*V of
-                // their previous tiles are done
-                ok = counter_wait(&bars->tail_granted, ntail, abort_flag, kWideWaitNs);
-                ++ntail;
-                ok = __all_sync(FULL, ok);
-                int* trow = trow_of(gtt);
-                if (ok) {
-                    trow[gtid] = res[n][0];
-                    trow[gtid + 64] = res[n][1];
-                }
-                ok = gather_sync_and(ok);
-                if (ok) {
-                    uint8_t* kt = k_tile(gtt);
-                    uint8_t* vt = v_tile(gtt);
-#pragma unroll 4
-                    for (int i = 0; i < TK / RPS; ++i) {
-                        const int c = rsub + i * RPS;
-                        const int r = trow[c];
-                        // the layout of a TMA box with 128-byte swizzle: chunk kc of row c in column half kc / 8
-                        const uint32_t off = sw128_chunk<TK>(kc, c);
-                        const long long e = static_cast<long long>(r < 0 ? 0 : r) * D + kc * 8;  // element offset
-                        if constexpr (FP8) {
-                            uint4 kw = make_uint4(0, 0, 0, 0), vw = kw;  // absent keys are zero rows
-                            if (r >= 0) {
-                                kw = e4m3x8_to_16<BF16>(__ldg(reinterpret_cast<const uint2*>(k_pool + e)));
-                                vw = e4m3x8_to_16<BF16>(__ldg(reinterpret_cast<const uint2*>(v_pool + e)));
-                            }
-                            *reinterpret_cast<uint4*>(kt + off) = kw;
-                            *reinterpret_cast<uint4*>(vt + off) = vw;
-                        } else {
-                            const uint32_t nb = r < 0 ? 0u : 16u;  // absent keys are zero rows
-                            cp_async16(kt + off, k_pool + 2 * e, nb);
-                            cp_async16(vt + off, v_pool + 2 * e, nb);
-                        }
-                    }
-                    if constexpr (!FP8) cp_async_commit_wait_all();
-                    fence_proxy_async_smem();
-                }
-                ok = gather_sync_and(ok);
-                if (!ok) break;
-                if (gtid == 0) {
-                    mbar_arrive(&bars->k_full[gtt % KST]);
-                    mbar_arrive(&bars->v_full[gtt % VST]);
-                }
-            }
-            gt += ptiles + ntt;
-            if (ok && k + 1 < nunits) {
-                cur = load_unit(p, u_begin + k + 1);
-                resolve(cur);
-            }
-        }
-        if (!ok && gtid == 0) {
-            *abort_flag = 1;
-            atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
-        }
-    } else {
-        // ================= E4M3 pools: widening of the prompt tiles (warps 12-15) =================
-        if constexpr (FP8) {
-            const int ctid = tid - C::CONV_TID0;
-            const int tensor = ctid >> 6;  // 0: K tiles (warps 12-13), 1: V tiles (warps 14-15)
-            const int stid = ctid & 63;
-            const int bar = 2 + tensor;    // named barrier of the stream's 64 threads
-            bool ok = true;
-            int gt = 0;
-            for (int k = 0; k < nunits && ok; ++k) {
-                const UnitInfo cur = load_unit(p, u_begin + k);
-                const int ptiles = prompt_tiles<TK>(cur);
-                const int ntiles = ptiles + wide_tail_tiles(cur);
-                for (int t = 0; t < ntiles && ok; ++t, ++gt) {
-                    // every tile's E4M3 phase in order, a tail tile's too (the producer completes it when it
-                    // hands the slots over; nothing to widen): so each parity wait names the phase it means
-                    uint64_t* full8 = tensor == 0 ? &bars->k8_full[gt % KST] : &bars->v8_full[gt % VST];
-                    const uint32_t ph = tensor == 0 ? (gt / KST) & 1 : (gt / VST) & 1;
-                    ok = mbar_wait(full8, ph, abort_flag, kWideWaitNs);
-                    ok = __all_sync(FULL, ok);
-                    ok = named_sync_and(bar, 64, ok);
-                    if (!ok || t >= ptiles) continue;
-                    const int valid = min(TK, cur.key_end - (cur.key_begin + t * TK));
-                    widen_e4m3_tile<D, TK, BF16>(tensor == 0 ? k_tile(gt) : v_tile(gt), valid, stid, bar);
-                    fence_proxy_async_smem();
-                    ok = named_sync_and(bar, 64, ok);
-                    if (ok && stid == 0)
-                        mbar_arrive(tensor == 0 ? &bars->k_full[gt % KST] : &bars->v_full[gt % VST]);
-                }
-            }
-            if (!ok && stid == 0) {
-                *abort_flag = 1;
-                atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
-            }
-        }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 9) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
@@ -907,6 +924,17 @@ template <int D, bool BF16, bool FP8>
 static cudaError_t prepare_wide_k() {
     using C = WideCfg<D>;
     static_assert(sizeof(WideBarriers) <= 512, "barrier block");
+    if constexpr (FP8) {
+        // the register split (setmaxnreg) draws on the launch's registers: a build that runs the kernel at
+        // another per-thread count would leave the softmax warps waiting for registers, so it is refused
+        static const cudaError_t regs = [] {
+            cudaFuncAttributes fa{};
+            const cudaError_t r = cudaFuncGetAttributes(&fa, prefix_wide_kernel<D, BF16, FP8>);
+            if (r != cudaSuccess) return r;
+            return fa.numRegs == C::REGS_LAUNCH_E4M3 ? cudaSuccess : cudaErrorInvalidConfiguration;
+        }();
+        if (regs != cudaSuccess) return regs;
+    }
     cudaError_t e =
         cudaFuncSetAttribute(prefix_wide_kernel<D, BF16, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
