@@ -89,12 +89,18 @@ def test_fp8_attention_matches_oracle(name, batch, k_scale, v_scale, layout):
     (dict(num_q_heads=64, num_kv_heads=8, beam_width=20), 2),   # G = 8, 160 rows: the wide kernel
     (dict(page_size=16, beam_width=7), 4),
     (dict(page_size=128), 3),
+    (dict(head_dim=64, num_q_heads=32, num_kv_heads=8, beam_width=40), 3),   # head_dim 64, 160 rows: wide
+    (dict(head_dim=64, num_q_heads=16, num_kv_heads=8, beam_width=96, dtype="fp16"), 2),  # D 64, fp16, 192 rows
+    (dict(head_dim=64, beam_width=30), 3),                                    # head_dim 64, 60 rows: alternating
 ])
 def test_fp8_attention_shapes(kw, batch):
     wl = synth.WORKLOADS["qwen3_0p6b_b64_w30"].scaled(batch).with_(**kw)
     case = synth.make_case(wl, 700 + batch, full_step=False, device="cpu")
     st = Fp8Step(case, 800 + batch, 0.5, 1.5)
     assert st.plan.layout in (1, 2)
+    G = wl.num_q_heads // wl.num_kv_heads
+    if wl.head_dim == 64:  # the intended kernel: two blocks above 128 rows per (request, kv head)
+        assert st.plan.layout == (2 if wl.beam_width * G > 128 else 1)
     st.attend(flags=bsp.FLAG_CHECK)
     O, L = st.oracle()
     assert_close(st.o, st.lse, O, L)
