@@ -203,6 +203,7 @@ struct PrefillSpec {
     const int32_t* cached_len;
     const int32_t* prompt_len;
     bool causal;
+    bool splits;  // key splits of the cached rows allowed (partial states the tail kernel merges)
 };
 
 // Whether the prompt kernel of plan layout `layout` finishes a decode request: its prompt is one partial
@@ -219,7 +220,9 @@ bool request_fused(int layout, int head_dim, int wblk, int32_t nsplit, int32_t t
 
 // The plan image of a decode step (pf == nullptr: prefix_len / tail_len per request, beam_width rows
 // each) or of a prefill (pf: the prompt tokens are the rows, the keys are the cached rows and the
-// prompt, no tail, no key splits, every request finished by the prompt kernel).
+// prompt, no tail; a request whose units are much longer than the mean CTA load has its cached rows
+// split into key ranges whose partial states the tail kernel merges, the others are finished by the
+// prompt kernel).
 bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_width, const int32_t* prefix_len_in,
                            const int32_t* tail_len_in, const int32_t* prefix_pages, int32_t prefix_pages_stride,
                            int32_t max_tail, int32_t num_sms, void* image, size_t image_bytes, bsp_plan_t* out,
@@ -364,21 +367,79 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
         chunk *= 2;
     }
     const int tk = prefix_tile_keys(geo->head_dim);
-    auto tail_tiles = [&](int b) -> int64_t { return request_tail_tiles(layout, geo->head_dim, wblk, tail_len[b]); };
-    auto fused = [&](int b) -> bool { return request_fused(layout, geo->head_dim, wblk, nsplit[b], tail_len[b]); };
+    const int64_t unit_ends = layout == 2 ? 8 : 4;
     // the plan tiles a unit reads: a causal prefill block stops at its last token's keys
     auto unit_end_tile = [&](int b, int rb, int32_t t1) -> int32_t {
         if (causal[b] < 0) return t1;
         const int64_t last_row = std::min<int64_t>(rows[b], static_cast<int64_t>(rb + 1) * urows);
         return static_cast<int32_t>(std::min<int64_t>(t1, ceil_div(causal[b] + last_row, kTileKeys)));
     };
+    // key range [t0, t1) of split s of request b, in plan tiles
+    std::vector<std::vector<int32_t>> pf_cut(pf ? batch : 0);
+    if (pf) {
+        // A prefill's units are (request, kv head, row block): a long cached prefix makes a request's
+        // units the longest of the launch, and the largest CTA load cannot drop below the longest unit.
+        // The cached rows of a request whose longest unit is above twice the mean CTA load are cut into
+        // about longest / mean key ranges of equal length, each cut inside the cached rows so that every
+        // row of every block has keys in every range (the last range holds the rest and the prompt),
+        // while the extra partial states last. Below twice the mean the fp32 partial states and the
+        // merge cost more than the balance gains. Costs as the dealing below counts them: eighths of a
+        // kernel tile.
+        auto full_cost = [&](int b, int rb) -> int64_t {
+            const int64_t keys = std::min<int64_t>(static_cast<int64_t>(unit_end_tile(b, rb, static_cast<int32_t>(tiles[b]))) *
+                                                       kTileKeys, prefix_len[b]);
+            return 8 * ceil_div(keys, tk) + unit_ends;
+        };
+        int64_t total = 0;
+        std::vector<int> order;
+        for (int b = 0; b < batch; ++b) {
+            if (tiles[b] == 0) continue;
+            order.push_back(b);
+            for (int rb = 0; rb < nrb_of(b); ++rb) total += static_cast<int64_t>(Hkv) * full_cost(b, rb);
+        }
+        const int64_t mean = std::max<int64_t>(1, ceil_div(total, num_sms));
+        std::stable_sort(order.begin(), order.end(), [&](int a, int c) {
+            return full_cost(a, nrb_of(a) - 1) > full_cost(c, nrb_of(c) - 1);
+        });
+        int64_t extra = 0;
+        for (int b = 0; b < batch; ++b) pf_cut[b] = {0, static_cast<int32_t>(tiles[b])};
+        for (int b : order) {
+            const int64_t longest = full_cost(b, nrb_of(b) - 1);
+            int64_t n = pf->splits && longest > 2 * mean ? ceil_div(longest, mean) : 1;
+            n = std::min<int64_t>(n, 1 + kExtraParts - extra);
+            const int32_t span = unit_end_tile(b, nrb_of(b) - 1, static_cast<int32_t>(tiles[b]));
+            const int32_t cmax = pf->cached_len[b] / kTileKeys;  // cuts at or below the cached rows
+            for (; n > 1; --n) {
+                std::vector<int32_t> cut{0};
+                bool okc = true;
+                for (int64_t i = 1; i < n && okc; ++i) {
+                    const int32_t c = std::min<int32_t>(static_cast<int32_t>(i * span / n), cmax);
+                    okc = c > cut.back();
+                    cut.push_back(c);
+                }
+                if (!okc) continue;
+                cut.push_back(static_cast<int32_t>(tiles[b]));
+                pf_cut[b] = cut;
+                break;
+            }
+            nsplit[b] = static_cast<int32_t>(pf_cut[b].size()) - 1;
+            extra += nsplit[b] - 1;
+        }
+        parts = 0;
+        for (int b = 0; b < batch; ++b) parts += nsplit[b];
+    }
+    auto split_range = [&](int b, int s) -> std::pair<int32_t, int32_t> {
+        if (pf) return {pf_cut[b][static_cast<size_t>(s)], pf_cut[b][static_cast<size_t>(s) + 1]};
+        return {static_cast<int32_t>(s * tiles[b] / nsplit[b]), static_cast<int32_t>((s + 1) * tiles[b] / nsplit[b])};
+    };
+    auto tail_tiles = [&](int b) -> int64_t { return request_tail_tiles(layout, geo->head_dim, wblk, tail_len[b]); };
+    auto fused = [&](int b) -> bool { return request_fused(layout, geo->head_dim, wblk, nsplit[b], tail_len[b]); };
     struct Unit {
         int32_t f[kUnitFields];
     };
     // time of a unit on the prompt kernel, in eighths of a key tile: its TK-key tiles (the last one
     // partial, costed in full), its tail tiles, and the unit's start and end: half a tile, a whole one
     // on the two-block kernel (its units write 256 output rows; measured there as about one tile)
-    const int64_t unit_ends = layout == 2 ? 8 : 4;
     auto unit_cost = [&](int b, int32_t t0, int32_t t1) -> int64_t {
         const int64_t keys = std::min<int64_t>(static_cast<int64_t>(t1) * kTileKeys, prefix_len[b]) -
                              static_cast<int64_t>(t0) * kTileKeys;
@@ -393,8 +454,7 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
         part_off[b] = static_cast<int32_t>(poff);
         page_off[b] = static_cast<int32_t>(pgoff);
         for (int s = 0; s < nsplit[b]; ++s) {
-            const int32_t t0 = static_cast<int32_t>(s * tiles[b] / nsplit[b]);
-            const int32_t t1 = static_cast<int32_t>((s + 1) * tiles[b] / nsplit[b]);
+            const auto [t0, t1] = split_range(b, s);
             for (int g = 0; g < Hkv; ++g)
                 for (int rb = 0; rb < (group > 1 ? 1 : nrb_of(b)); ++rb) {  // a group's other blocks follow
                     const int32_t te = unit_end_tile(b, rb, t1);
@@ -598,6 +658,11 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     // for the most key splits the planner makes), so the device addresses baked into a captured
     // CUDA graph stay valid for every later plan of the same shape. A prefill plan is packed.
     const int64_t parts_cap = fixed ? static_cast<int64_t>(batch) + kExtraParts : parts;
+    // rows of a request's partial-state slot: the beams of a decode step, the longest prompt of a prefill
+    // with key splits (a prefill without them writes no partial state)
+    int32_t part_w = beam_width;
+    if (pf && std::any_of(nsplit.begin(), nsplit.end(), [](int32_t n) { return n > 1; }))
+        for (int b = 0; b < batch; ++b) part_w = std::max(part_w, rows[b]);
     const size_t units_cap = fixed ? static_cast<size_t>(parts_cap) * Hkv * nrb : units.size();
     const size_t pages_cap = fixed ? static_cast<size_t>(batch) * prefix_pages_stride : static_cast<size_t>(total_pages);
     if (units.size() > units_cap || static_cast<size_t>(total_pages) > pages_cap) return BSP_ERR_CAPACITY;
@@ -613,7 +678,7 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     // replayed graph checks against its capture)
     reinterpret_cast<int32_t*>(img)[2] = batch;
     reinterpret_cast<int32_t*>(img)[3] = static_cast<int32_t>(units.size());
-    reinterpret_cast<int32_t*>(img)[4] = beam_width;
+    reinterpret_cast<int32_t*>(img)[4] = part_w;
     reinterpret_cast<int32_t*>(img)[5] = num_sms;
     reinterpret_cast<int32_t*>(img)[6] = pf ? 1 : 0;
     reinterpret_cast<int32_t*>(img)[7] = max_tail;
@@ -642,7 +707,7 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     std::memset(out, 0, sizeof(*out));
     out->geo = *geo;
     out->batch = batch;
-    out->beam_width = beam_width;
+    out->beam_width = part_w;
     out->max_tail = max_tail;
     out->prefix_pages_stride = prefix_pages_stride;
     out->num_units = static_cast<int32_t>(units.size());
@@ -656,14 +721,15 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     out->max_tail_len = max_t;
     out->prefix_ctas = static_cast<int32_t>(ctas);
     int32_t tail_requests = 0;
-    for (int b = 0; b < batch; ++b) tail_requests += !pf && !fused(b);
+    // (a prefill request is the tail kernel's when its keys were split)
+    for (int b = 0; b < batch; ++b) tail_requests += pf ? nsplit[b] > 1 : !fused(b);
     out->tail_requests = tail_requests;
     out->total_rows = static_cast<int32_t>(total_rows);
     out->kind = pf ? 1 : 0;
     out->layout = layout;
     out->image_bytes = need;
     // offsets relative to the device workspace
-    DeviceLayout L = device_layout(need, parts_cap, beam_width, *geo);
+    DeviceLayout L = device_layout(need, parts_cap, part_w, *geo);
     out->off_req = kStatusBytes + off_req;
     out->off_units = kStatusBytes + off_units;
     out->off_cta = kStatusBytes + off_cta;
@@ -703,7 +769,7 @@ bsp_status bsp_plan_prefill_build(const bsp_geometry* geo, int32_t batch, const 
                                   const int32_t* prompt_len, const int32_t* pages, int32_t pages_stride,
                                   int32_t causal, int32_t num_sms, void* image, size_t image_bytes,
                                   bsp_plan_t* out) {
-    const PrefillSpec pf{cached_len, prompt_len, causal != 0};
+    const PrefillSpec pf{cached_len, prompt_len, causal != 0, true};
     return plan_build_core(geo, batch, 1, nullptr, nullptr, pages, pages_stride, 0, num_sms, image, image_bytes, out,
                            &pf);
 }
@@ -802,8 +868,15 @@ bsp_status bsp_plan_prefill(const bsp_geometry* geo, int32_t batch, const int32_
                             bsp_plan_t* out) {
     return stage_plan(ws_device, ws_device_bytes, ws_host, ws_host_bytes, stream, out,
                       [&](int sms, void* img, size_t bytes, bsp_plan_t* p) {
-                          return bsp_plan_prefill_build(geo, batch, cached_len, prompt_len, pages, pages_stride,
-                                                        causal, sms, img, bytes, p);
+                          bsp_status r = bsp_plan_prefill_build(geo, batch, cached_len, prompt_len, pages,
+                                                                pages_stride, causal, sms, img, bytes, p);
+                          if (r == BSP_OK && p->device_bytes_used > ws_device_bytes) {
+                              // no room for the partial states of key splits: the plan without them
+                              const PrefillSpec pf{cached_len, prompt_len, causal != 0, false};
+                              r = plan_build_core(geo, batch, 1, nullptr, nullptr, pages, pages_stride, 0, sms, img,
+                                                  bytes, p, &pf);
+                          }
+                          return r;
                       });
 }
 

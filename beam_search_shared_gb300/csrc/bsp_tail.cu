@@ -18,6 +18,10 @@
 // written in the q dtype and LSE in fp32. So one chain of dependent lookups
 // serves all Hq heads of the row. All softmax arithmetic is in base 2 on
 // scores pre-scaled by softmax_scale * log2(e).
+//
+// A prefill request whose cached keys the plan split is merged here too: its
+// prompt tokens are the rows (w < the request's rows, W the longest prompt of
+// the batch; q, O and LSE at the request's first row + w), with no tail keys.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -114,6 +118,10 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
     const int4 rq = __ldg(reinterpret_cast<const int4*>(p.req + b * kReqFields));
     const int P = rq.x, T = rq.y, nsplit = rq.z, part_off = rq.w;
     if (__ldg(p.req + b * kReqFields + kReqFused)) return;  // the prompt kernel finished this request
+    // the request's rows (beams; prompt tokens of a prefill, W = the longest prompt) and its first row
+    const int4 rq3 = __ldg(reinterpret_cast<const int4*>(p.req + b * kReqFields + 8));
+    if (w >= rq3.x) return;                                  // kReqRows
+    const long long orow = static_cast<long long>(rq3.z) + w;  // kReqRowOff: the row of q, o and lse
 
     // ---- resolve the row's tail positions once (source beam, page, slot)
     if (tid < T) {
@@ -151,7 +159,7 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
             const int hh = active ? h : 0;
             const int g = hh / p.G;
             const uint4 qraw = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                                     (static_cast<long long>(r) * p.Hq + hh) * D) +
+                                                                     (orow * p.Hq + hh) * D) +
                                      li);
             // a lane's 8 elements of a K or V row: 16 bytes, or 8 E4M3 codes (the upper half unused)
             uint4 kraw[MAXT], vraw[MAXT];
@@ -320,10 +328,9 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
                 lse2 = Lmax + log2f(sum);
             }
             if (!active) continue;
-            uint16_t* obase = static_cast<uint16_t*>(p.o) + (static_cast<long long>(r) * p.Hq + h) * D;
+            uint16_t* obase = static_cast<uint16_t*>(p.o) + (orow * p.Hq + h) * D;
             reinterpret_cast<uint4*>(obase)[li] = pack8<BF16>(out);
-            if (li == 0)
-                p.lse[static_cast<long long>(r) * p.Hq + h] = p.lse_base2 ? lse2 : lse2 * 0.69314718055994530942f;
+            if (li == 0) p.lse[orow * p.Hq + h] = p.lse_base2 ? lse2 : lse2 * 0.69314718055994530942f;
         }
     }
 }

@@ -28,7 +28,9 @@
 // pair of row blocks rb), block X holding prompt tokens [(2 rb + X) Wb,
 // (2 rb + X + 1) Wb), Wb = 4 floor(32 / G), and in a causal prefill each row
 // masks the keys past its own position (token t sees the C_b cached rows and
-// tokens 0 .. t). The pair reads each K/V tile once for up to 256 rows.
+// tokens 0 .. t). The pair reads each K/V tile once for up to 256 rows. A
+// request whose cached rows the plan cut into key ranges writes one fp32
+// partial state per range, as a decode request with key splits does.
 //
 // Persistent: one CTA per SM walks the units the host dealt it; the K/V rings
 // are indexed by a tile counter that runs across units.

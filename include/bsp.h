@@ -122,7 +122,7 @@ typedef struct bsp_geometry {
 typedef struct bsp_plan_t {
     bsp_geometry geo;
     int32_t batch;               /* B */
-    int32_t beam_width;          /* W */
+    int32_t beam_width;          /* W (a prefill plan: the rows of a partial slot, the largest prompt) */
     int32_t max_tail;            /* bound on every tail_len, <= BSP_MAX_TAIL */
     int32_t prefix_pages_stride; /* row stride of the prefix_pages table given to the plan */
     int32_t num_units;           /* prompt-attention work units (CTAs) */
@@ -456,10 +456,17 @@ BSP_API bsp_status bsp_decode_attn_fp8(const bsp_plan_t* plan, const void* q, co
  * cached_len[b] + prompt_len[b] positions. Positions past those are never
  * read. The query rows are the prompt tokens of all requests in order (request
  * b's tokens start at the sum of the earlier prompt_len), `total_rows` in all.
- * bsp_plan_prefill_build writes the host image only (as bsp_plan_build);
- * bsp_plan_prefill stages it without a sync (as bsp_plan); the workspace must
- * hold a plan of max_batch = batch and max_beam = the largest prompt_len
- * (bsp_workspace_size).
+ * A request whose longest work unit is above the launch's mean load per SM has
+ * its cached rows cut into key ranges (every cut inside the cached rows, so
+ * that each prompt row has keys in each range); the prompt kernel writes one
+ * partial state per range and the tail kernel merges them (the plan's
+ * tail_requests counts such requests, its beam_width is then the rows of a
+ * partial slot: the largest prompt_len). bsp_plan_prefill_build writes the host
+ * image only (as bsp_plan_build); bsp_plan_prefill stages it without a sync (as
+ * bsp_plan); the workspace must hold a plan of max_batch = batch and max_beam =
+ * 1 (bsp_workspace_size), and with max_beam = the largest prompt_len it also
+ * holds the partial states of key splits: bsp_plan_prefill plans without them
+ * when they do not fit.
  */
 BSP_API bsp_status bsp_plan_prefill_build(const bsp_geometry* geo, int32_t batch, const int32_t* cached_len,
                                   const int32_t* prompt_len, const int32_t* pages, int32_t pages_stride,
@@ -473,9 +480,12 @@ BSP_API bsp_status bsp_plan_prefill(const bsp_geometry* geo, int32_t batch, cons
 /*
  * The prefill attention of a bsp_plan_prefill plan: for every prompt row r and
  * query head h, O[r][h] = softmax(scale * q K^T) V and LSE[r][h] over the keys
- * the plan gives that row, on the tensor cores (the prompt kernel, each
- * (request, kv head, block of 128 / G prompt tokens) a work unit; a causal
- * block reads keys only up to its last token). q, o [total_rows][Hq][head_dim]
+ * the plan gives that row, on the tensor cores (the prompt kernel: at head_dim
+ * <= 128 each (request, kv head, two blocks of 4 * floor(32 / G) prompt tokens,
+ * key range) a work unit of the two-block kernel, at 256 each (request, kv
+ * head, block of floor(128 / G) tokens, key range) one of the one-set kernel; a
+ * causal unit reads keys only up to its last token; then the tail kernel for
+ * the requests whose keys were split). q, o [total_rows][Hq][head_dim]
  * in the pools' dtype, lse [total_rows][Hq] fp32 (natural log, or base 2 with
  * BSP_FLAG_LSE_BASE2). A decode plan is BSP_ERR_INVALID_ARG here (and a prefill
  * plan in bsp_decode_attn). events: NULL or 3 cudaEvent_t, as bsp_decode_attn.

@@ -527,6 +527,43 @@ def test_planner_random_sweep(lib):
             assert max(loads) <= max(heap), (trial, max(loads), max(heap))
 
 
+def check_prefill_units(plan, req, units, B, Hkv, C, S, causal, urows, trial=None):
+    """A prefill plan's units: for every (request, kv head, run of urows tokens) their key ranges tile
+    [0, end) in 64-key plan tiles (end: the run's last visible key, or the prompt's end); a request's
+    ranges are the same for all its units but the last one's end, every cut lies inside the cached
+    rows (so each row has keys in each range), range s writes partial slot part_off + s, and a request
+    with more than one range is the tail kernel's (not fused)."""
+    by = {}
+    for u in units:
+        b, g, rb, t0, t1, part = (int(x) for x in u[:6])
+        by.setdefault((b, g, rb), []).append((t0, t1, part))
+    want_keys = set()
+    tail = 0
+    for b in range(B):
+        nsplit, part_off, fused = int(req[b][2]), int(req[b][3]), int(req[b][5])
+        if S[b] == 0:
+            assert nsplit == 0
+            continue
+        assert nsplit >= 1 and fused == (nsplit == 1), (trial, b)
+        tail += nsplit > 1
+        cuts = None
+        for g in range(Hkv):
+            for rb in range(-(-int(S[b]) // urows)):
+                want_keys.add((b, g, rb))
+                last = min(int(S[b]), (rb + 1) * urows)
+                end = -(-(int(C[b]) + last) // 64) if causal else -(-(int(C[b]) + int(S[b])) // 64)
+                r = sorted(by.get((b, g, rb), []))
+                assert len(r) == nsplit and r[0][0] == 0 and r[-1][1] == end, (trial, b, g, rb, r, end)
+                assert all(r[i][1] == r[i + 1][0] for i in range(nsplit - 1)), (trial, r)
+                assert [x[2] for x in r] == list(range(part_off, part_off + nsplit)), (trial, r)
+                c = [x[0] for x in r[1:]]
+                assert cuts is None or c == cuts
+                cuts = c
+                assert all(x * 64 <= C[b] for x in c), (trial, b, c, C[b])
+    assert set(by) == want_keys, trial
+    assert plan.tail_requests == tail and plan.num_parts <= B + 64
+
+
 def test_prefill_planner_random_sweep(lib):
     """Random prefill batches: one unit per (request, kv head, run of prompt tokens: two blocks of
     4 * floor(32 / G) at head_dim <= 128, one block of floor(128 / G) at head_dim 256) reading plan tiles
@@ -556,13 +593,5 @@ def test_prefill_planner_random_sweep(lib):
         np.testing.assert_array_equal(req[:, 8], S)
         np.testing.assert_array_equal(req[:, 9], C if causal else -1)
         np.testing.assert_array_equal(req[:, 10], np.concatenate([[0], np.cumsum(S)[:-1]]))
-        want = set()
-        for b in range(B):
-            for gg in range(Hkv):
-                for rb in range(-(-int(S[b]) // urows)):
-                    last = min(int(S[b]), (rb + 1) * urows)
-                    end = -(-(int(C[b]) + last) // 64) if causal else -(-(int(C[b]) + int(S[b])) // 64)
-                    want.add((b, gg, rb, 0, end))
-        got = [tuple(int(x) for x in u[:5]) for u in units]
-        assert len(got) == len(set(got)) and set(got) == want, trial
+        check_prefill_units(plan, req, units, B, Hkv, C, S, causal, urows, trial)
         assert cta[0] == 0 and cta[-1] == plan.num_units and (np.diff(cta) >= 0).all()

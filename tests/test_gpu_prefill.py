@@ -91,6 +91,38 @@ def test_prefill_two_block_unit_edges(Hq, D):
     assert step.plan.layout == 2 and step.plan.beams_per_block == wblk
 
 
+@pytest.mark.parametrize("kw", [
+    dict(),                                   # head_dim 128: the two-block kernel writes the partial states
+    dict(causal=False),
+    dict(head_dim=64, dtype="bf16"),
+    dict(head_dim=256, num_q_heads=16),       # the one-set kernel
+])
+def test_prefill_key_splits_of_long_caches(kw):
+    """Requests with long cached prefixes and short prompts: the planner cuts their cached keys into
+    ranges (partial states merged by the tail kernel), the others stay whole."""
+    wl = synth.PREFILL_WORKLOADS["prefill_text_b8"].with_(batch=4, **kw)
+    case = synth.make_prefill_case(wl, 16, cached_lengths=[3000, 2500, 40, 1900], prompt_lengths=[20, 57, 300, 1])
+    step = run_and_check(case)
+    assert step.plan.tail_requests > 0
+    assert step.plan.beam_width == 300            # partial-state rows: the longest prompt
+
+
+def test_prefill_without_room_for_partials_is_planned_whole():
+    """A workspace sized for one row per partial slot cannot hold the split requests' partial states: the
+    plan keeps every request whole (no tail kernel) and stays correct."""
+    wl = synth.PREFILL_WORKLOADS["prefill_text_b8"].with_(batch=4)
+    case = synth.make_prefill_case(wl, 17, cached_lengths=[3000, 2500, 40, 1900], prompt_lengths=[20, 57, 300, 1])
+    step = PrefillStep(case)
+    step.ws = bsp.Workspace(step.geo, wl.batch, 1, case.pages.shape[1])
+    st, flags = step.run()
+    assert st == 0 and flags == 0
+    assert step.plan.tail_requests == 0
+    O, L, _, _ = oracle_prefill(case)
+    o = step.o.float().double().cpu().numpy()
+    assert (np.abs(o - O) <= ATOL + RTOL * np.abs(O)).all()
+    assert np.abs(step.lse.double().cpu().numpy() - L).max() <= LSE_TOL
+
+
 def test_prefill_image_prompt_from_empty_cache():
     """Image tokens prefilled with nothing cached (the case the page measures), 2 x 512 tokens."""
     wl = synth.PREFILL_WORKLOADS["prefill_image_b4_s1024"].with_(batch=2, prompt=(512, 512))
