@@ -564,6 +564,28 @@ def check_prefill_units(plan, req, units, B, Hkv, C, S, causal, urows, trial=Non
     assert plan.tail_requests == tail and plan.num_parts <= B + 64
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_key_splits_of_a_long_cache(lib, causal):
+    """One request with a long cached prefix among short ones: its cached keys are cut into ranges (cuts
+    inside the cached rows), the others stay whole; without long caches nothing is split."""
+    C = np.array([20000, 500, 300, 800, 100, 600, 700, 200])
+    S = np.array([100, 200, 150, 250, 90, 300, 120, 60])
+    ps = 32
+    maxp = -(-(C + S).max() // ps)
+    pages = np.arange(8 * maxp, dtype=np.int32).reshape(8, maxp) % 4000
+    g = geo(Hq=32, Hkv=8, npages=4000)
+    plan, img = bsp.plan_prefill_build(g, 8, C, S, pages, causal, 152)
+    req, units, _ = decode_image(plan, img)
+    assert plan.tail_requests == 1 and req[0][2] > 1 and (req[1:, 2] == 1).all()
+    assert plan.beam_width == S.max() and plan.num_parts == 8 + req[0][2] - 1
+    check_prefill_units(plan, req, units, 8, 8, C, S, causal, 64)
+    # the same batch with short caches: whole requests, no partial slots
+    plan2, img2 = bsp.plan_prefill_build(g, 8, np.minimum(C, 800), S, pages, causal, 152)
+    req2, units2, _ = decode_image(plan2, img2)
+    assert plan2.tail_requests == 0 and (req2[:, 2] == 1).all() and plan2.beam_width == 1
+    check_prefill_units(plan2, req2, units2, 8, 8, np.minimum(C, 800), S, causal, 64)
+
+
 def test_prefill_planner_random_sweep(lib):
     """Random prefill batches: one unit per (request, kv head, run of prompt tokens: two blocks of
     4 * floor(32 / G) at head_dim <= 128, one block of floor(128 / G) at head_dim 256) reading plan tiles
