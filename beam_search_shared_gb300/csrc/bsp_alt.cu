@@ -32,19 +32,20 @@
 // table); each row keeps only its own beam's columns. Such a unit writes the
 // final O and LSE; other units write fp32 partial states for the tail kernel.
 //
-// Warp roles (384 threads):
-//   warp 0      TMA producer: each unit's Q (3-D boxes [bq][G][64], one per
+// Warp roles (384 threads; the register split and warps 12-15 or 12-19 over
+// E4M3 pools are described next to the kernel's configuration):
+//   warp 8      TMA producer: each unit's Q (3-D boxes [bq][G][64], one per
 //               quadrant and column half) first, then the prompt K/V tiles into
 //               a KST-deep K ring and a VST-deep V ring (one 2-D box of
 //               min(page, 64) rows x 64 columns per page slice, column half and
 //               tensor). It is the one waiter on the slot-release barriers and
 //               takes every tile's release in order; a tail tile's slots it
 //               hands to warps 10-11 by raising a shared counter;
-//   warp 1      TMEM allocation; one thread issues tcgen05.mma: for tile t of set
+//   warp 9      TMEM allocation; one thread issues tcgen05.mma: for tile t of set
 //               X = t % 2, first P_X V of set X's previous tile, then
 //               S_X = Q K_t^T (P_X aliases S_X, and tcgen05.mma instructions of
 //               one thread execute in issue order);
-//   warps 2-5   softmax set A, warps 6-9 softmax set B: thread <-> query row
+//   warps 0-3   softmax set A, warps 4-7 softmax set B: thread <-> query row
 //               <-> TMEM lane; scores read from TMEM twice (row maximum, then
 //               probabilities), online softmax in base 2 with a lazy rescale of
 //               O_X (only when a row maximum grows by more than 2^8), P written
@@ -53,7 +54,12 @@
 //               their rows into L2), then copy K and V rows into the ring slots
 //               with 16-byte cp.async in the 128-byte-swizzled layout a TMA box
 //               would have (absent keys are zero rows), with a key -> pool-row
-//               table per V slot for the softmax's mask.
+//               table per V slot for the softmax's mask; over E4M3 pools at
+//               head_dim 64 they also widen every prompt tile;
+//   warps 12-15 (E4M3 pools at head_dim 128 only, 512 threads): the producer
+//               loads each E4M3 tile into the upper half of its 16-bit ring
+//               slot; warps 12-13 widen every K tile, warps 14-15 every V tile,
+//               in place, to the q dtype, and complete the slot's full barrier.
 // TMEM columns: S_A [0, 128), S_B [128, 256), O_A [256, 256 + D), O_B after it.
 // Every wait is bounded (1 s without progress); on expiry the CTA flags
 // BSP_DEVFLAG_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
@@ -89,6 +95,21 @@ struct AltCfg {
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int THREADS = 384;
     static constexpr int GATHER_TID0 = 320;                  // warps 10-11
+    // over E4M3 pools at head_dim 128 four more warps (12-15, one warpgroup) widen the prompt tiles (at 64
+    // the tail-tile warps do, as the tiles are half the size): warps 12-13 every K
+    // tile, warps 14-15 every V tile, two streams that do not wait on each other. Registers per thread:
+    // 128 at launch (__launch_bounds__(512, 1)), then warps 8-11 down to REGS_OTHER, the widening warps
+    // down to REGS_CONV and the softmax warps (0-7) up to REGS_SOFTMAX (setmaxnreg draws on the launch's
+    // registers)
+    static constexpr int THREADS_E4M3 = 512;
+    static constexpr int CONV_TID0 = 384;
+    static constexpr int CONV_THREADS = 64;  // per stream
+    static constexpr int REGS_LAUNCH_E4M3 = 128;
+    static constexpr int REGS_OTHER = 104;
+    static constexpr int REGS_CONV = 72;
+    static constexpr int REGS_SOFTMAX = 168;
+    static_assert(256 * REGS_SOFTMAX + 128 * REGS_OTHER + 128 * REGS_CONV <= THREADS_E4M3 * REGS_LAUNCH_E4M3,
+                  "register split");
     static_assert(O_COL + 2 * D <= 512, "tensor memory");
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(KST <= 8 && VST <= 8, "barrier arrays");
@@ -129,6 +150,19 @@ __device__ __forceinline__ int alt_tail_tiles(const UnitInfo& ui, int wblk) {
 
 // Named barrier 1 over the 64 tail-tile threads, returning the AND of their flags. Every one of them
 // takes part in every call (a flag that is false makes them all stop together).
+// Named barrier `id` over `n` threads, returning the AND of their flags (every one of them takes part).
+__device__ __forceinline__ bool alt_named_sync_and(int id, int n, bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(ok)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
 __device__ __forceinline__ bool alt_gather_sync_and(bool ok) {
     uint32_t r;
     asm volatile(
@@ -145,10 +179,11 @@ __device__ __forceinline__ bool alt_gather_sync_and(bool ok) {
 }  // namespace
 
 template <int D, bool BF16, bool FP8>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(FP8 && D == 128 ? 512 : 384, 1)
 prefix_alt_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const PrefixParams p) {
     using C = AltCfg<D>;
+    constexpr bool CONVW = FP8 && D == 128;  // E4M3 prompt tiles widened by warps 12-15
     constexpr int TK = C::TK, NC = C::NC, KST = C::KST, VST = C::VST;
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ uint8_t smem_raw[];
@@ -211,12 +246,12 @@ prefix_alt_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
     }
-    if (warp == 1) tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
+    if (warp == 9) tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
     // zero the query rows no TMA box covers (rows bq * G .. 31 of each quadrant), so padded rows stay
     // finite
     {
         constexpr int NCHUNK = NC * kRowsPerBlock * 8;  // 16-byte chunks of the Q buffer
-        for (int idx = tid; idx < NCHUNK; idx += C::THREADS) {
+        for (int idx = tid; idx < NCHUNK; idx += (CONVW ? C::THREADS_E4M3 : C::THREADS)) {
             const int r = (idx >> 3) & (kRowsPerBlock - 1);
             if ((r & 31) >= qrows) reinterpret_cast<uint4*>(smem)[idx] = make_uint4(0, 0, 0, 0);
         }
@@ -230,217 +265,404 @@ prefix_alt_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // SMs this grid leaves; it waits for this grid's completion before reading the partials
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    if (warp == 0) {
-        // ================= TMA producer =================
-        const int BR = ps < kTileKeys ? ps : kTileKeys;  // rows per box (a page, or 64 rows of a larger page)
-        int gt = 0, k = 0, ntail = 0;
-        bool ok = true;
-        for (int u = u_begin; u < u_end && ok; ++u, ++k) {
-            const UnitInfo ui = load_unit(p, u);
-            const int ptiles = prompt_tiles<TK>(ui);
-            const int ntiles = ptiles + alt_tail_tiles(ui, p.Wblk);
-            const int* pg = p.pages + ui.page_off;
-            const int npages = (ui.P + ps - 1) >> p.ps_log2;
-            int win_base = -1, my_page = 0;
-            // the unit's Q first, once the previous unit's last Q*K^T is done (a later load could wait
-            // for a ring slot whose P*V the tensor core issues only after this unit's first Q*K^T)
-            if (k >= 1) {
-                ok = mbar_wait(&bars->q_empty, (k - 1) & 1, abort_flag, kAltWaitNs);
-                ok = __all_sync(FULL, ok);
-                if (!ok) break;
-            }
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bars->q_full, NC * 4 * qrows * 128);
-                for (int c = 0; c < NC; ++c)
-                    for (int i = 0; i < 4; ++i)
-                        tma_load_3d(q_buf + c * (kRowsPerBlock * 128) + i * 32 * 128, &tm_q, &bars->q_full, c * 64,
-                                    ui.g * p.G, ui.row_off + ui.rb * p.Wblk + i * p.bq);
-            }
-            for (int t = 0; t < ntiles; ++t, ++gt) {
-                // this warp is the only waiter on the slot-release barriers and takes every tile's
-                // release in order, so each parity wait names the phase it means
-                if (gt >= KST) {
-                    ok = mbar_wait(&bars->k_empty[gt % KST], ((gt / KST) - 1) & 1, abort_flag, kAltWaitNs);
+    if (warp >= 8) {
+        // over E4M3 pools the producer, MMA and tail-tile warps (8-11) and the widening warps (12-15)
+        // give registers to the softmax warpgroups
+        if constexpr (CONVW) {
+            if (warp >= 12) setmaxnreg_dec<C::REGS_CONV>();
+            else setmaxnreg_dec<C::REGS_OTHER>();
+        }
+        if (warp == 8) {
+            // ================= TMA producer =================
+            const int BR = ps < kTileKeys ? ps : kTileKeys;  // rows per box (a page, or 64 rows of a larger page)
+            int gt = 0, k = 0, ntail = 0;
+            bool ok = true;
+            for (int u = u_begin; u < u_end && ok; ++u, ++k) {
+                const UnitInfo ui = load_unit(p, u);
+                const int ptiles = prompt_tiles<TK>(ui);
+                const int ntiles = ptiles + alt_tail_tiles(ui, p.Wblk);
+                const int* pg = p.pages + ui.page_off;
+                const int npages = (ui.P + ps - 1) >> p.ps_log2;
+                int win_base = -1, my_page = 0;
+                // the unit's Q first, once the previous unit's last Q*K^T is done (a later load could wait
+                // for a ring slot whose P*V the tensor core issues only after this unit's first Q*K^T)
+                if (k >= 1) {
+                    ok = mbar_wait(&bars->q_empty, (k - 1) & 1, abort_flag, kAltWaitNs);
                     ok = __all_sync(FULL, ok);
                     if (!ok) break;
                 }
-                if (t >= ptiles) {
-                    // a tail tile: once its V slot is free too, hand both slots to the tail-tile warps
-                    // (a counter, not a barrier phase: they may lag several tail tiles behind)
-                    if (gt >= VST) {
-                        ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kAltWaitNs);
-                        ok = __all_sync(FULL, ok);
-                        if (!ok) break;
-                    }
-                    ++ntail;
-                    if (lane == 0) {
-                        counter_release(&bars->tail_granted, ntail);
-                        if constexpr (FP8) {
-                            // no E4M3 tile here: complete the slots' E4M3 phases, which the widening warps
-                            // skip for a tail tile, so that the phases keep counting the slot's tiles
-                            mbar_arrive(&bars->k8_full[gt % KST]);
-                            mbar_arrive(&bars->v8_full[gt % VST]);
-                        }
-                    }
-                    __syncwarp();
-                    continue;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars->q_full, NC * 4 * qrows * 128);
+                    for (int c = 0; c < NC; ++c)
+                        for (int i = 0; i < 4; ++i)
+                            tma_load_3d(q_buf + c * (kRowsPerBlock * 128) + i * 32 * 128, &tm_q, &bars->q_full, c * 64,
+                                        ui.g * p.G, ui.row_off + ui.rb * p.Wblk + i * p.bq);
                 }
-                const int key0 = ui.key_begin + t * TK;
-                const int valid = min(TK, ui.key_end - key0);
-                const int nchunks = (valid + BR - 1) / BR;  // pages (or 64-row slices) with valid keys
-                const int tile_bytes = nchunks * BR * D * (FP8 ? 1 : 2);
-                const int pidx0 = key0 >> p.ps_log2;
-                const int pidx_last = (key0 + (nchunks - 1) * BR) >> p.ps_log2;
-                if (win_base < 0 || pidx_last >= win_base + 32) {  // warp-uniform
-                    win_base = pidx0;
-                    my_page = (win_base + lane < npages) ? __ldg(pg + win_base + lane) : 0;
-                }
-                // box b of a tensor: column half b % NC of chunk b / NC (E4M3: one box of head_dim bytes
-                // per chunk, into the upper half of the slot, where the widening warps pick it up)
-                constexpr int NB = FP8 ? 1 : NC;
-                const int nbox = nchunks * NB;
-                for (int tensor = 0; tensor < 2; ++tensor) {
-                    if (tensor == 1 && gt >= VST) {
-                        ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kAltWaitNs);
-                        ok = __all_sync(FULL, ok);
-                        if (!ok) break;
-                    }
-                    uint64_t* full = FP8 ? (tensor == 0 ? &bars->k8_full[gt % KST] : &bars->v8_full[gt % VST])
-                                         : (tensor == 0 ? &bars->k_full[gt % KST] : &bars->v_full[gt % VST]);
-                    uint8_t* base = tensor == 0 ? k_tile(gt) : v_tile(gt);
-                    const CUtensorMap* map = tensor == 0 ? &tm_k : &tm_v;
-                    if (lane == 0) mbar_arrive_expect_tx(full, tile_bytes);
-                    for (int b0 = 0; b0 < nbox; b0 += 32) {
-                        const int bx = b0 + lane;
-                        const int ch = min(bx / NB, nchunks - 1);
-                        const int key = key0 + ch * BR;
-                        int page = __shfl_sync(FULL, my_page, (key >> p.ps_log2) - win_base);
-                        if (bx < nbox) {
-                            if (static_cast<unsigned>(page) >= static_cast<unsigned>(p.num_pages)) {
-                                atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
-                                page = 0;
-                            }
-                            const int row = ((page * p.Hkv + ui.g) << p.ps_log2) + (key & (ps - 1));
-                            if constexpr (FP8) {
-                                tma_load_2d(base + TK * D + ch * BR * D, map, full, 0, row);
-                            } else {
-                                const int c = bx % NC;
-                                tma_load_2d(base + c * TK * 128 + ch * BR * 128, map, full, c * 64, row);
-                            }
-                        }
-                    }
-                }
-                if (!ok) break;
-                __syncwarp();
-            }
-        }
-        if (!ok) {
-            if (lane == 0) {
-                *abort_flag = 1;
-                atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
-            }
-            // drain: let this CTA's own copies land before the CTA exits
-            // (the TMA loads complete the E4M3 barriers over E4M3 pools)
-            const uint64_t t0 = globaltimer_ns();
-            uint64_t* kf = FP8 ? bars->k8_full : bars->k_full;
-            uint64_t* vf = FP8 ? bars->v8_full : bars->v_full;
-            for (int j = max(0, gt - KST); j <= gt; ++j)
-                while (!mbar_try_wait(&kf[j % KST], (j / KST) & 1) && globaltimer_ns() - t0 < kAltDrainNs) {
-                }
-            for (int j = max(0, gt - VST); j <= gt; ++j)
-                while (!mbar_try_wait(&vf[j % VST], (j / VST) & 1) && globaltimer_ns() - t0 < kAltDrainNs) {
-                }
-            while (!mbar_try_wait(&bars->q_full, k & 1) && globaltimer_ns() - t0 < kAltDrainNs) {
-            }
-        }
-    } else if (warp == 1) {
-        // ================= MMA issuer =================
-        if (lane == 0) {
-            constexpr uint32_t ID_QK = idesc_f16(kRowsPerBlock, TK, BF16, false);
-            constexpr uint32_t ID_PV = idesc_f16(kRowsPerBlock, D, BF16, true);
-            int gt = 0, k = 0;
-            int cnt[2] = {0, 0};                           // Q*K^T issued per set
-            int pend[2] = {-1, -1}, pcnt[2] = {0, 0};      // tile of set X whose P*V is not issued yet
-            bool pfirst[2] = {false, false}, plast[2] = {false, false};
-            bool ok = true;
-            auto issue_pv = [&](int x) -> bool {
-                const int j = pend[x];
-                if (!mbar_wait(&bars->p_full[x], pcnt[x] & 1, abort_flag, kAltWaitNs)) return false;
-                if (!mbar_wait(&bars->v_full[j % VST], (j / VST) & 1, abort_flag, kAltWaitNs)) return false;
-                tc_fence_after();
-                const uint32_t p_tmem = tmem + C::S_COL + x * TK;
-                const uint32_t o_tmem = tmem + C::O_COL + x * D;
-                const uint32_t v_addr = smem_u32(v_tile(j));
-#pragma unroll
-                for (int kk = 0; kk < TK / 16; ++kk) {
-                    const uint64_t bd = sdesc_sw128(v_addr + kk * 16 * 128, TK * 128, 1024);
-                    mma_f16_tmem_a(o_tmem, p_tmem + kk * 8, bd, ID_PV, (!pfirst[x] || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(&bars->v_empty[j % VST]);
-                if (plast[x]) mma_commit(&bars->o_final[x]);
-                pend[x] = -1;
-                return true;
-            };
-            const uint32_t q_addr = smem_u32(q_buf);
-            for (int u = u_begin; u < u_end && ok; ++u, ++k) {
-                const UnitInfo ui = load_unit(p, u);
-                const int ntiles = prompt_tiles<TK>(ui) + alt_tail_tiles(ui, p.Wblk);
                 for (int t = 0; t < ntiles; ++t, ++gt) {
-                    const int x = t & 1;
-                    // S_X holds P of set X's previous tile: its P*V goes first
-                    if (pend[x] >= 0) {
-                        ok = issue_pv(x);
+                    // this warp is the only waiter on the slot-release barriers and takes every tile's
+                    // release in order, so each parity wait names the phase it means
+                    if (gt >= KST) {
+                        ok = mbar_wait(&bars->k_empty[gt % KST], ((gt / KST) - 1) & 1, abort_flag, kAltWaitNs);
+                        ok = __all_sync(FULL, ok);
                         if (!ok) break;
                     }
-                    if (t == 0) {
-                        ok = mbar_wait(&bars->q_full, k & 1, abort_flag, kAltWaitNs);
-                        if (!ok) break;
+                    if (t >= ptiles) {
+                        // a tail tile: once its V slot is free too, hand both slots to the tail-tile warps
+                        // (a counter, not a barrier phase: they may lag several tail tiles behind)
+                        if (gt >= VST) {
+                            ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kAltWaitNs);
+                            ok = __all_sync(FULL, ok);
+                            if (!ok) break;
+                        }
+                        ++ntail;
+                        if (lane == 0) {
+                            counter_release(&bars->tail_granted, ntail);
+                            if constexpr (FP8) {
+                                // no E4M3 tile here: complete the slots' E4M3 phases (the widening warps wait
+                                // for them or, at head_dim 64, skip a tail tile's), so that the phases keep
+                                // counting the slot's tiles
+                                mbar_arrive(&bars->k8_full[gt % KST]);
+                                mbar_arrive(&bars->v8_full[gt % VST]);
+                            }
+                        }
+                        __syncwarp();
+                        continue;
                     }
-                    ok = mbar_wait(&bars->k_full[gt % KST], (gt / KST) & 1, abort_flag, kAltWaitNs);
+                    const int key0 = ui.key_begin + t * TK;
+                    const int valid = min(TK, ui.key_end - key0);
+                    const int nchunks = (valid + BR - 1) / BR;  // pages (or 64-row slices) with valid keys
+                    const int tile_bytes = nchunks * BR * D * (FP8 ? 1 : 2);
+                    const int pidx0 = key0 >> p.ps_log2;
+                    const int pidx_last = (key0 + (nchunks - 1) * BR) >> p.ps_log2;
+                    if (win_base < 0 || pidx_last >= win_base + 32) {  // warp-uniform
+                        win_base = pidx0;
+                        my_page = (win_base + lane < npages) ? __ldg(pg + win_base + lane) : 0;
+                    }
+                    // box b of a tensor: column half b % NC of chunk b / NC (E4M3: one box of head_dim bytes
+                    // per chunk, into the upper half of the slot, where the widening warps pick it up)
+                    constexpr int NB = FP8 ? 1 : NC;
+                    const int nbox = nchunks * NB;
+                    for (int tensor = 0; tensor < 2; ++tensor) {
+                        if (tensor == 1 && gt >= VST) {
+                            ok = mbar_wait(&bars->v_empty[gt % VST], ((gt / VST) - 1) & 1, abort_flag, kAltWaitNs);
+                            ok = __all_sync(FULL, ok);
+                            if (!ok) break;
+                        }
+                        uint64_t* full = FP8 ? (tensor == 0 ? &bars->k8_full[gt % KST] : &bars->v8_full[gt % VST])
+                                             : (tensor == 0 ? &bars->k_full[gt % KST] : &bars->v_full[gt % VST]);
+                        uint8_t* base = tensor == 0 ? k_tile(gt) : v_tile(gt);
+                        const CUtensorMap* map = tensor == 0 ? &tm_k : &tm_v;
+                        if (lane == 0) mbar_arrive_expect_tx(full, tile_bytes);
+                        for (int b0 = 0; b0 < nbox; b0 += 32) {
+                            const int bx = b0 + lane;
+                            const int ch = min(bx / NB, nchunks - 1);
+                            const int key = key0 + ch * BR;
+                            int page = __shfl_sync(FULL, my_page, (key >> p.ps_log2) - win_base);
+                            if (bx < nbox) {
+                                if (static_cast<unsigned>(page) >= static_cast<unsigned>(p.num_pages)) {
+                                    atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
+                                    page = 0;
+                                }
+                                const int row = ((page * p.Hkv + ui.g) << p.ps_log2) + (key & (ps - 1));
+                                if constexpr (FP8) {
+                                    tma_load_2d(base + TK * D + ch * BR * D, map, full, 0, row);
+                                } else {
+                                    const int c = bx % NC;
+                                    tma_load_2d(base + c * TK * 128 + ch * BR * 128, map, full, c * 64, row);
+                                }
+                            }
+                        }
+                    }
                     if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t k_addr = smem_u32(k_tile(gt));
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t ad =
-                            sdesc_sw128(q_addr + (kk >> 2) * (kRowsPerBlock * 128) + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(k_addr + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
-                        mma_f16(tmem + C::S_COL + x * TK, ad, bd, ID_QK, kk > 0 ? 1u : 0u);
-                    }
-                    mma_commit(&bars->s_full[x]);
-                    mma_commit(&bars->k_empty[gt % KST]);
-                    if (t == ntiles - 1) mma_commit(&bars->q_empty);
-                    pend[x] = gt;
-                    pcnt[x] = cnt[x]++;
-                    pfirst[x] = t < 2;
-                    plast[x] = t >= ntiles - 2;
-                }
-                if (!ok) break;
-                if (ntiles == 1) {
-                    // set B has no tile in this unit: its previous unit's last P*V (and o_final) first,
-                    // then this unit's o_final, so that o_final[B] keeps one phase per unit, in order
-                    if (pend[1] >= 0) {
-                        ok = issue_pv(1);
-                        if (!ok) break;
-                    }
-                    mma_commit(&bars->o_final[1]);
+                    __syncwarp();
                 }
             }
-            for (int x = 0; x < 2 && ok; ++x)
-                if (pend[x] >= 0) ok = issue_pv(x);
             if (!ok) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+                }
+                // drain: let this CTA's own copies land before the CTA exits
+                // (the TMA loads complete the E4M3 barriers over E4M3 pools)
+                const uint64_t t0 = globaltimer_ns();
+                uint64_t* kf = FP8 ? bars->k8_full : bars->k_full;
+                uint64_t* vf = FP8 ? bars->v8_full : bars->v_full;
+                for (int j = max(0, gt - KST); j <= gt; ++j)
+                    while (!mbar_try_wait(&kf[j % KST], (j / KST) & 1) && globaltimer_ns() - t0 < kAltDrainNs) {
+                    }
+                for (int j = max(0, gt - VST); j <= gt; ++j)
+                    while (!mbar_try_wait(&vf[j % VST], (j / VST) & 1) && globaltimer_ns() - t0 < kAltDrainNs) {
+                    }
+                while (!mbar_try_wait(&bars->q_full, k & 1) && globaltimer_ns() - t0 < kAltDrainNs) {
+                }
+            }
+        } else if (warp == 9) {
+            // ================= MMA issuer =================
+            if (lane == 0) {
+                constexpr uint32_t ID_QK = idesc_f16(kRowsPerBlock, TK, BF16, false);
+                constexpr uint32_t ID_PV = idesc_f16(kRowsPerBlock, D, BF16, true);
+                int gt = 0, k = 0;
+                int cnt[2] = {0, 0};                           // Q*K^T issued per set
+                int pend[2] = {-1, -1}, pcnt[2] = {0, 0};      // tile of set X whose P*V is not issued yet
+                bool pfirst[2] = {false, false}, plast[2] = {false, false};
+                bool ok = true;
+                auto issue_pv = [&](int x) -> bool {
+                    const int j = pend[x];
+                    if (!mbar_wait(&bars->p_full[x], pcnt[x] & 1, abort_flag, kAltWaitNs)) return false;
+                    if (!mbar_wait(&bars->v_full[j % VST], (j / VST) & 1, abort_flag, kAltWaitNs)) return false;
+                    tc_fence_after();
+                    const uint32_t p_tmem = tmem + C::S_COL + x * TK;
+                    const uint32_t o_tmem = tmem + C::O_COL + x * D;
+                    const uint32_t v_addr = smem_u32(v_tile(j));
+#pragma unroll
+                    for (int kk = 0; kk < TK / 16; ++kk) {
+                        const uint64_t bd = sdesc_sw128(v_addr + kk * 16 * 128, TK * 128, 1024);
+                        mma_f16_tmem_a(o_tmem, p_tmem + kk * 8, bd, ID_PV, (!pfirst[x] || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&bars->v_empty[j % VST]);
+                    if (plast[x]) mma_commit(&bars->o_final[x]);
+                    pend[x] = -1;
+                    return true;
+                };
+                const uint32_t q_addr = smem_u32(q_buf);
+                for (int u = u_begin; u < u_end && ok; ++u, ++k) {
+                    const UnitInfo ui = load_unit(p, u);
+                    const int ntiles = prompt_tiles<TK>(ui) + alt_tail_tiles(ui, p.Wblk);
+                    for (int t = 0; t < ntiles; ++t, ++gt) {
+                        const int x = t & 1;
+                        // S_X holds P of set X's previous tile: its P*V goes first
+                        if (pend[x] >= 0) {
+                            ok = issue_pv(x);
+                            if (!ok) break;
+                        }
+                        if (t == 0) {
+                            ok = mbar_wait(&bars->q_full, k & 1, abort_flag, kAltWaitNs);
+                            if (!ok) break;
+                        }
+                        ok = mbar_wait(&bars->k_full[gt % KST], (gt / KST) & 1, abort_flag, kAltWaitNs);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t k_addr = smem_u32(k_tile(gt));
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t ad =
+                                sdesc_sw128(q_addr + (kk >> 2) * (kRowsPerBlock * 128) + (kk & 3) * 32, 16, 1024);
+                            const uint64_t bd = sdesc_sw128(k_addr + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
+                            mma_f16(tmem + C::S_COL + x * TK, ad, bd, ID_QK, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&bars->s_full[x]);
+                        mma_commit(&bars->k_empty[gt % KST]);
+                        if (t == ntiles - 1) mma_commit(&bars->q_empty);
+                        pend[x] = gt;
+                        pcnt[x] = cnt[x]++;
+                        pfirst[x] = t < 2;
+                        plast[x] = t >= ntiles - 2;
+                    }
+                    if (!ok) break;
+                    if (ntiles == 1) {
+                        // set B has no tile in this unit: its previous unit's last P*V (and o_final) first,
+                        // then this unit's o_final, so that o_final[B] keeps one phase per unit, in order
+                        if (pend[1] >= 0) {
+                            ok = issue_pv(1);
+                            if (!ok) break;
+                        }
+                        mma_commit(&bars->o_final[1]);
+                    }
+                }
+                for (int x = 0; x < 2 && ok; ++x)
+                    if (pend[x] >= 0) ok = issue_pv(x);
+                if (!ok) {
+                    *abort_flag = 1;
+                    atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+                }
+                // drain: every MMA issued by this thread completes before TMEM is freed
+                mma_commit(&bars->drain);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(&bars->drain, 0) && globaltimer_ns() - t0 < kAltDrainNs) {
+                }
+            }
+        } else if (warp < 12) {
+            // ================= tail tiles (over E4M3 pools also the widening of every prompt tile) =================
+            constexpr int CH = D / 8;     // 16-byte chunks of a 16-bit K or V row
+            constexpr int RPS = 64 / CH;  // rows one pass of the 64 threads covers
+            constexpr int EB = FP8 ? 1 : 2;  // bytes per pool element
+            const int gtid = tid - C::GATHER_TID0;
+            const int kc = gtid % CH;
+            const int rsub = gtid / CH;
+            const uint8_t* k_pool = static_cast<const uint8_t*>(p.k_pool);
+            const uint8_t* v_pool = static_cast<const uint8_t*>(p.v_pool);
+            // pool rows of this thread's two key columns (gtid, gtid + 64) of each tail tile of a unit,
+            // resolved a unit ahead; -1 past the block's tail keys or when unreadable
+            int res[kAltMaxTailTiles][2];
+            auto resolve = [&](const UnitInfo& ui) {
+                const int ntt = alt_tail_tiles(ui, p.Wblk);
+                const int nkeys = alt_block_beams(ui, p.Wblk) * ui.T;
+#pragma unroll
+                for (int nt = 0; nt < kAltMaxTailTiles; ++nt)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        res[nt][h] = -1;
+                        const int cc = nt * TK + gtid + 64 * h;
+                        if (nt >= ntt || cc >= nkeys) continue;
+                        const int wl = cc / ui.T, tt = cc - wl * ui.T;
+                        const int w = ui.rb * p.Wblk + wl;
+                        const int pos = ui.P + tt;
+                        const int src = __ldg(p.ci + (static_cast<long long>(ui.b) * p.W + w) * p.max_seq + pos);
+                        int r = -1;
+                        if (static_cast<unsigned>(src) < static_cast<unsigned>(p.W)) {
+                            const int page = __ldg(p.beam_pages +
+                                                   (static_cast<long long>(ui.b) * p.W + src) * p.beam_pages_stride +
+                                                   (pos >> p.ps_log2));
+                            if (static_cast<unsigned>(page) < static_cast<unsigned>(p.num_pages))
+                                r = ((page * p.Hkv + ui.g) << p.ps_log2) + (pos & (ps - 1));
+                        }
+                        if (r < 0) {
+                            atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
+                        } else {
+                            // the gather runs at the end of the unit: bring the row's K and V into L2 now
+#pragma unroll
+                            for (int off = 0; off < D * EB; off += 128) {
+                                prefetch_l2(k_pool + static_cast<long long>(r) * (D * EB) + off);
+                                prefetch_l2(v_pool + static_cast<long long>(r) * (D * EB) + off);
+                            }
+                        }
+                        res[nt][h] = r;
+                    }
+            };
+            bool ok = true;
+            int gt = 0, ntail = 0;
+            UnitInfo cur;
+            if (nunits > 0) {
+                cur = load_unit(p, u_begin);
+                resolve(cur);
+            }
+            for (int k = 0; k < nunits && ok; ++k) {
+                const int ptiles = prompt_tiles<TK>(cur);
+                const int ntt = alt_tail_tiles(cur, p.Wblk);
+                if constexpr (FP8 && !CONVW) {
+                    // (head_dim 64: the tail-tile warps widen every prompt tile too)
+                    // each prompt tile: K, then V, once its E4M3 tile has landed, widened in place and handed
+                    // to the tensor core (these warps take every phase of the E4M3 barriers in order, and a
+                    // slot's next E4M3 load waits for the tensor core to release this tile)
+                    for (int t = 0; t < ptiles && ok; ++t) {
+                        const int g2 = gt + t;
+                        const int valid = min(TK, cur.key_end - (cur.key_begin + t * TK));
+                        for (int tensor = 0; tensor < 2; ++tensor) {
+                            uint64_t* full8 = tensor == 0 ? &bars->k8_full[g2 % KST] : &bars->v8_full[g2 % VST];
+                            const uint32_t ph = tensor == 0 ? (g2 / KST) & 1 : (g2 / VST) & 1;
+                            ok = mbar_wait(full8, ph, abort_flag, kAltWaitNs);
+                            ok = __all_sync(FULL, ok);
+                            ok = alt_gather_sync_and(ok);
+                            if (!ok) break;
+                            widen_e4m3_tile<D, TK, BF16>(tensor == 0 ? k_tile(g2) : v_tile(g2), valid, gtid, 1);
+                            fence_proxy_async_smem();
+                            ok = alt_gather_sync_and(ok);
+                            if (!ok) break;
+                            if (gtid == 0) mbar_arrive(tensor == 0 ? &bars->k_full[g2 % KST] : &bars->v_full[g2 % VST]);
+                        }
+                    }
+                    if (!ok) break;
+                }
+#pragma unroll
+                for (int nt = 0; nt < kAltMaxTailTiles; ++nt) {
+                    if (nt >= ntt) break;
+                    const int gtt = gt + ptiles + nt;
+                    // the producer hands the tile's K and V slots over once the previous tiles that used them
+                    // are done
+                    ok = counter_wait(&bars->tail_granted, ntail, abort_flag, kAltWaitNs);
+                    ++ntail;
+                    ok = __all_sync(FULL, ok);
+                    int* trow = trow_of(gtt);
+                    if (ok) {
+                        trow[gtid] = res[nt][0];
+                        trow[gtid + 64] = res[nt][1];
+                    }
+                    ok = alt_gather_sync_and(ok);
+                    if (ok) {
+                        uint8_t* kt = k_tile(gtt);
+                        uint8_t* vt = v_tile(gtt);
+#pragma unroll 4
+                        for (int i = 0; i < TK / RPS; ++i) {
+                            const int c = rsub + i * RPS;
+                            const int r = trow[c];
+                            // the layout of a TMA box with 128-byte swizzle: chunk kc of row c in column half kc / 8
+                            const uint32_t off = sw128_chunk<TK>(kc, c);
+                            const long long e = static_cast<long long>(r < 0 ? 0 : r) * D + kc * 8;  // element offset
+                            if constexpr (FP8) {
+                                uint4 kw = make_uint4(0, 0, 0, 0), vw = kw;  // absent keys are zero rows
+                                if (r >= 0) {
+                                    kw = e4m3x8_to_16<BF16>(__ldg(reinterpret_cast<const uint2*>(k_pool + e)));
+                                    vw = e4m3x8_to_16<BF16>(__ldg(reinterpret_cast<const uint2*>(v_pool + e)));
+                                }
+                                *reinterpret_cast<uint4*>(kt + off) = kw;
+                                *reinterpret_cast<uint4*>(vt + off) = vw;
+                            } else {
+                                const uint32_t nb = r < 0 ? 0u : 16u;  // absent keys are zero rows
+                                cp_async16(kt + off, k_pool + 2 * e, nb);
+                                cp_async16(vt + off, v_pool + 2 * e, nb);
+                            }
+                        }
+                        if constexpr (!FP8) cp_async_commit_wait_all();
+                        fence_proxy_async_smem();
+                    }
+                    ok = alt_gather_sync_and(ok);
+                    if (!ok) break;
+                    if (gtid == 0) {
+                        mbar_arrive(&bars->k_full[gtt % KST]);
+                        mbar_arrive(&bars->v_full[gtt % VST]);
+                    }
+                }
+                gt += ptiles + ntt;
+                if (ok && k + 1 < nunits) {
+                    cur = load_unit(p, u_begin + k + 1);
+                    resolve(cur);
+                }
+            }
+            if (!ok && gtid == 0) {
                 *abort_flag = 1;
                 atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
             }
-            // drain: every MMA issued by this thread completes before TMEM is freed
-            mma_commit(&bars->drain);
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(&bars->drain, 0) && globaltimer_ns() - t0 < kAltDrainNs) {
+        } else {
+            // ================= E4M3 pools: widening of the prompt tiles (warps 12-15) =================
+            if constexpr (CONVW) {
+                const int ctid = tid - C::CONV_TID0;
+                const int tensor = ctid / C::CONV_THREADS;  // 0: K tiles (warps 12-13), 1: V tiles (warps 14-15)
+                const int stid = ctid % C::CONV_THREADS;
+                const int bar = 2 + tensor;                 // named barrier of the stream's threads
+                bool ok = true;
+                int gt = 0;
+                for (int k = 0; k < nunits && ok; ++k) {
+                    const UnitInfo cur = load_unit(p, u_begin + k);
+                    const int ptiles = prompt_tiles<TK>(cur);
+                    const int ntiles = ptiles + alt_tail_tiles(cur, p.Wblk);
+                    for (int t = 0; t < ntiles && ok; ++t, ++gt) {
+                        // every tile's E4M3 phase in order, a tail tile's too (the producer completes it when it
+                        // hands the slots over; nothing to widen): so each parity wait names the phase it means
+                        uint64_t* full8 = tensor == 0 ? &bars->k8_full[gt % KST] : &bars->v8_full[gt % VST];
+                        const uint32_t ph = tensor == 0 ? (gt / KST) & 1 : (gt / VST) & 1;
+                        ok = mbar_wait(full8, ph, abort_flag, kAltWaitNs);
+                        ok = __all_sync(FULL, ok);
+                        ok = alt_named_sync_and(bar, C::CONV_THREADS, ok);
+                        if (!ok || t >= ptiles) continue;
+                        const int valid = min(TK, cur.key_end - (cur.key_begin + t * TK));
+                        widen_e4m3_tile<D, TK, BF16, C::CONV_THREADS>(tensor == 0 ? k_tile(gt) : v_tile(gt), valid,
+                                                                      stid, bar);
+                        fence_proxy_async_smem();
+                        ok = alt_named_sync_and(bar, C::CONV_THREADS, ok);
+                        if (ok && stid == 0)
+                            mbar_arrive(tensor == 0 ? &bars->k_full[gt % KST] : &bars->v_full[gt % VST]);
+                    }
+                }
+                if (!ok && stid == 0) {
+                    *abort_flag = 1;
+                    atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
+                }
             }
         }
-    } else if (warp < 10) {
+    } else {
+        if constexpr (CONVW) setmaxnreg_inc<C::REGS_SOFTMAX>();
         // ================= softmax warps (set x), set A also merges and writes the unit's output ====
-        const int x = (warp - 2) >> 2;
+        const int x = warp >> 2;
         const int quad = warp & 3;           // TMEM lane quadrant this warp may access
         const int row = quad * 32 + lane;    // TMEM lane of the thread's query row
         const int wq = lane / p.G;           // beam of the quadrant
@@ -634,7 +856,7 @@ prefix_alt_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     uint8_t* sV = v_tile(gt);
                     const int nzc = (TK - valid) * 8;  // 16-byte chunks per column half
                     for (int c = 0; c < NC; ++c)
-                        for (int idx = tid - 64 - 128 * x; idx < nzc; idx += 128)
+                        for (int idx = tid - 128 * x; idx < nzc; idx += 128)
                             reinterpret_cast<uint4*>(sV + c * TK * 128 + valid * 128)[idx] = make_uint4(0, 0, 0, 0);
                     fence_proxy_async_smem();
                 }
@@ -741,150 +963,10 @@ prefix_alt_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             *abort_flag = 1;
             atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
         }
-    } else {
-        // ================= tail tiles (over E4M3 pools also the widening of every prompt tile) =================
-        constexpr int CH = D / 8;     // 16-byte chunks of a 16-bit K or V row
-        constexpr int RPS = 64 / CH;  // rows one pass of the 64 threads covers
-        constexpr int EB = FP8 ? 1 : 2;  // bytes per pool element
-        const int gtid = tid - C::GATHER_TID0;
-        const int kc = gtid % CH;
-        const int rsub = gtid / CH;
-        const uint8_t* k_pool = static_cast<const uint8_t*>(p.k_pool);
-        const uint8_t* v_pool = static_cast<const uint8_t*>(p.v_pool);
-        // pool rows of this thread's two key columns (gtid, gtid + 64) of each tail tile of a unit,
-        // resolved a unit ahead; -1 past the block's tail keys or when unreadable
-        int res[kAltMaxTailTiles][2];
-        auto resolve = [&](const UnitInfo& ui) {
-            const int ntt = alt_tail_tiles(ui, p.Wblk);
-            const int nkeys = alt_block_beams(ui, p.Wblk) * ui.T;
-#pragma unroll
-            for (int nt = 0; nt < kAltMaxTailTiles; ++nt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    res[nt][h] = -1;
-                    const int cc = nt * TK + gtid + 64 * h;
-                    if (nt >= ntt || cc >= nkeys) continue;
-                    const int wl = cc / ui.T, tt = cc - wl * ui.T;
-                    const int w = ui.rb * p.Wblk + wl;
-                    const int pos = ui.P + tt;
-                    const int src = __ldg(p.ci + (static_cast<long long>(ui.b) * p.W + w) * p.max_seq + pos);
-                    int r = -1;
-                    if (static_cast<unsigned>(src) < static_cast<unsigned>(p.W)) {
-                        const int page = __ldg(p.beam_pages +
-                                               (static_cast<long long>(ui.b) * p.W + src) * p.beam_pages_stride +
-                                               (pos >> p.ps_log2));
-                        if (static_cast<unsigned>(page) < static_cast<unsigned>(p.num_pages))
-                            r = ((page * p.Hkv + ui.g) << p.ps_log2) + (pos & (ps - 1));
-                    }
-                    if (r < 0) {
-                        atomicOr(p.status, BSP_DEVFLAG_PAGE_INDEX);
-                    } else {
-                        // the gather runs at the end of the unit: bring the row's K and V into L2 now
-#pragma unroll
-                        for (int off = 0; off < D * EB; off += 128) {
-                            prefetch_l2(k_pool + static_cast<long long>(r) * (D * EB) + off);
-                            prefetch_l2(v_pool + static_cast<long long>(r) * (D * EB) + off);
-                        }
-                    }
-                    res[nt][h] = r;
-                }
-        };
-        bool ok = true;
-        int gt = 0, ntail = 0;
-        UnitInfo cur;
-        if (nunits > 0) {
-            cur = load_unit(p, u_begin);
-            resolve(cur);
-        }
-        for (int k = 0; k < nunits && ok; ++k) {
-            const int ptiles = prompt_tiles<TK>(cur);
-            const int ntt = alt_tail_tiles(cur, p.Wblk);
-            if constexpr (FP8) {
-                // each prompt tile: K, then V, once its E4M3 tile has landed, widened in place and handed
-                // to the tensor core (these warps take every phase of the E4M3 barriers in order, and a
-                // slot's next E4M3 load waits for the tensor core to release this tile)
-                for (int t = 0; t < ptiles && ok; ++t) {
-                    const int g2 = gt + t;
-                    const int valid = min(TK, cur.key_end - (cur.key_begin + t * TK));
-                    for (int tensor = 0; tensor < 2; ++tensor) {
-                        uint64_t* full8 = tensor == 0 ? &bars->k8_full[g2 % KST] : &bars->v8_full[g2 % VST];
-                        const uint32_t ph = tensor == 0 ? (g2 / KST) & 1 : (g2 / VST) & 1;
-                        ok = mbar_wait(full8, ph, abort_flag, kAltWaitNs);
-                        ok = __all_sync(FULL, ok);
-                        ok = alt_gather_sync_and(ok);
-                        if (!ok) break;
-                        widen_e4m3_tile<D, TK, BF16>(tensor == 0 ? k_tile(g2) : v_tile(g2), valid, gtid, 1);
-                        fence_proxy_async_smem();
-                        ok = alt_gather_sync_and(ok);
-                        if (!ok) break;
-                        if (gtid == 0) mbar_arrive(tensor == 0 ? &bars->k_full[g2 % KST] : &bars->v_full[g2 % VST]);
-                    }
-                }
-                if (!ok) break;
-            }
-#pragma unroll
-            for (int nt = 0; nt < kAltMaxTailTiles; ++nt) {
-                if (nt >= ntt) break;
-                const int gtt = gt + ptiles + nt;
-                // the producer hands the tile's K and V slots over once the previous tiles that used them
-                // are done
-                ok = counter_wait(&bars->tail_granted, ntail, abort_flag, kAltWaitNs);
-                ++ntail;
-                ok = __all_sync(FULL, ok);
-                int* trow = trow_of(gtt);
-                if (ok) {
-                    trow[gtid] = res[nt][0];
-                    trow[gtid + 64] = res[nt][1];
-                }
-                ok = alt_gather_sync_and(ok);
-                if (ok) {
-                    uint8_t* kt = k_tile(gtt);
-                    uint8_t* vt = v_tile(gtt);
-#pragma unroll 4
-                    for (int i = 0; i < TK / RPS; ++i) {
-                        const int c = rsub + i * RPS;
-                        const int r = trow[c];
-                        // the layout of a TMA box with 128-byte swizzle: chunk kc of row c in column half kc / 8
-                        const uint32_t off = sw128_chunk<TK>(kc, c);
-                        const long long e = static_cast<long long>(r < 0 ? 0 : r) * D + kc * 8;  // element offset
-                        if constexpr (FP8) {
-                            uint4 kw = make_uint4(0, 0, 0, 0), vw = kw;  // absent keys are zero rows
-                            if (r >= 0) {
-                                kw = e4m3x8_to_16<BF16>(__ldg(reinterpret_cast<const uint2*>(k_pool + e)));
-                                vw = e4m3x8_to_16<BF16>(__ldg(reinterpret_cast<const uint2*>(v_pool + e)));
-                            }
-                            *reinterpret_cast<uint4*>(kt + off) = kw;
-                            *reinterpret_cast<uint4*>(vt + off) = vw;
-                        } else {
-                            const uint32_t nb = r < 0 ? 0u : 16u;  // absent keys are zero rows
-                            cp_async16(kt + off, k_pool + 2 * e, nb);
-                            cp_async16(vt + off, v_pool + 2 * e, nb);
-                        }
-                    }
-                    if constexpr (!FP8) cp_async_commit_wait_all();
-                    fence_proxy_async_smem();
-                }
-                ok = alt_gather_sync_and(ok);
-                if (!ok) break;
-                if (gtid == 0) {
-                    mbar_arrive(&bars->k_full[gtt % KST]);
-                    mbar_arrive(&bars->v_full[gtt % VST]);
-                }
-            }
-            gt += ptiles + ntt;
-            if (ok && k + 1 < nunits) {
-                cur = load_unit(p, u_begin + k + 1);
-                resolve(cur);
-            }
-        }
-        if (!ok && gtid == 0) {
-            *abort_flag = 1;
-            atomicOr(p.status, BSP_DEVFLAG_TIMEOUT);
-        }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 9) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
@@ -895,6 +977,17 @@ template <int D, bool BF16, bool FP8>
 static cudaError_t prepare_alt_k() {
     using C = AltCfg<D>;
     static_assert(sizeof(AltBarriers) <= 512, "barrier block");
+    if constexpr (FP8 && D == 128) {
+        // the register split (setmaxnreg) draws on the launch's registers: a build that runs the kernel at
+        // another per-thread count would leave the softmax warps waiting for registers, so it is refused
+        static const cudaError_t regs = [] {
+            cudaFuncAttributes fa{};
+            const cudaError_t r = cudaFuncGetAttributes(&fa, prefix_alt_kernel<D, BF16, FP8>);
+            if (r != cudaSuccess) return r;
+            return fa.numRegs == C::REGS_LAUNCH_E4M3 ? cudaSuccess : cudaErrorInvalidConfiguration;
+        }();
+        if (regs != cudaSuccess) return regs;
+    }
     cudaError_t e =
         cudaFuncSetAttribute(prefix_alt_kernel<D, BF16, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
@@ -918,7 +1011,8 @@ cudaError_t prepare_alt(int head_dim, bool bf16, bool fp8) {
 template <int D, bool BF16, bool FP8>
 static void launch_alt_k(int ctas, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const PrefixParams& p, cudaStream_t stream) {
-    prefix_alt_kernel<D, BF16, FP8><<<ctas, AltCfg<D>::THREADS, AltCfg<D>::SMEM, stream>>>(tq, tk, tv, p);
+    constexpr int threads = FP8 && D == 128 ? AltCfg<D>::THREADS_E4M3 : AltCfg<D>::THREADS;
+    prefix_alt_kernel<D, BF16, FP8><<<ctas, threads, AltCfg<D>::SMEM, stream>>>(tq, tk, tv, p);
 }
 
 template <int D>

@@ -35,8 +35,9 @@
 // Persistent: one CTA per SM walks the units the host dealt it; the K/V rings
 // are indexed by a tile counter that runs across units.
 //
-// Warp roles (384 threads):
-//   warp 0      TMA producer: each unit's Q of both blocks (3-D boxes
+// Warp roles (384 threads; the register split and warps 12-15 or 12-19 over
+// E4M3 pools are described next to the kernel's configuration):
+//   warp 8      TMA producer: each unit's Q of both blocks (3-D boxes
 //               [bq][G][64], one per quadrant and column half) after the unit's
 //               first K/V tile, and the prompt K/V tiles into a KST-deep K ring
 //               and a VST-deep V ring (one 2-D box of min(page, 64) rows x 64
@@ -45,11 +46,11 @@
 //               in order (a parity wait only names the right phase for a waiter
 //               that is never two phases behind); a tail tile's slots it hands
 //               to warps 10-11 by raising a shared counter;
-//   warp 1      TMEM allocation; one thread issues tcgen05.mma in the order
+//   warp 9      TMEM allocation; one thread issues tcgen05.mma in the order
 //               Q K_t^T -> S_A, Q K_t^T -> S_B, P_A V_t -> O_A, Q K_{t+1}^T -> S_A,
 //               P_B V_t -> O_B, Q K_{t+1}^T -> S_B, ...: while the softmax warps of
 //               one block work on their scores, the tensor core serves the other;
-//   warps 2-5   softmax of block A, warps 6-9 softmax of block B: thread <->
+//   warps 0-3   softmax of block A, warps 4-7 softmax of block B: thread <->
 //               query row <-> TMEM lane; scores read from TMEM twice (row
 //               maximum, then probabilities), online softmax in base 2 with a
 //               lazy rescale of O (only when a row maximum grows by more than
@@ -61,9 +62,9 @@
 //               slots with 16-byte cp.async in the 128-byte-swizzled layout a
 //               TMA box would have (absent keys are zero rows), with a key ->
 //               pool-row table per V slot for the softmax's mask;
-//   warps 12-15 (E4M3 pools only, 512 threads): the producer loads each E4M3
-//               tile into the upper half of its 16-bit ring slot; warps 12-13
-//               widen every K tile, warps 14-15 every V tile, in place, to the
+//   warps 12-19 (E4M3 pools only, 640 threads): the producer loads each E4M3
+//               tile into the upper half of its 16-bit ring slot; warps 12-15
+//               widen every K tile, warps 16-19 every V tile, in place, to the
 //               q dtype, and complete the slot's full barrier (two streams, so
 //               a late V tile does not hold the next K tile back).
 // TMEM columns: S_A [0, 128), S_B [128, 256), O_A [256, 256 + D), O_B after it.
