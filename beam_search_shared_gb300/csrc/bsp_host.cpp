@@ -353,7 +353,7 @@ bsp_status plan_build_core(const bsp_geometry* geo, int32_t batch, int32_t beam_
     for (int b = 0; b < batch; ++b) base_units += tiles[b] > 0 ? static_cast<int64_t>(Hkv) * nrb_of(b) : 0;
     const int64_t target = 2 * static_cast<int64_t>(num_sms);
     int64_t chunk = std::numeric_limits<int32_t>::max();  // tiles per split
-    if (!pf && base_units > 0 && base_units < target)  // a prefill's rows are never split by keys
+    if (!pf && base_units > 0 && base_units < target)  // (a prefill's key ranges are chosen below)
         chunk = std::max<int64_t>(2, ceil_div(total_tiles * Hkv * nrb, target));
     std::vector<int32_t> nsplit(batch);
     int64_t parts = 0;
