@@ -617,3 +617,7 @@ def test_prefill_planner_random_sweep(lib):
         np.testing.assert_array_equal(req[:, 10], np.concatenate([[0], np.cumsum(S)[:-1]]))
         check_prefill_units(plan, req, units, B, Hkv, C, S, causal, urows, trial)
         assert cta[0] == 0 and cta[-1] == plan.num_units and (np.diff(cta) >= 0).all()
+        # a workspace sized for the batch with the longest prompt as beam width holds the plan, key
+        # splits' partial states included
+        dev_bytes, host_bytes = bsp.workspace_size(g, B, max(1, int(S.max())), maxp)
+        assert plan.device_bytes_used <= dev_bytes and 256 + 2 * plan.image_bytes <= host_bytes, trial
